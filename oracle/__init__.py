@@ -1,0 +1,218 @@
+"""fp64 CPU oracle for absorbed MLA decode over a paged latent cache.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the benchmark's
+``cpu_baseline`` / ``--impl reference`` legs are the only callers.  The product package never
+imports this module, and this module imports nothing from the product package.
+
+The arithmetic lives in ``mla_oracle.c`` (plain C, fp64, optional OpenMP over heads); this file
+only compiles it with gcc and marshals numpy arrays through ctypes.  Each function cites the
+web-page passage it follows; see the C source for the definitions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BF16 = 0
+FP8_MIXED = 1
+D_C = 512
+D_R = 64
+D_K = D_C + D_R
+PAGE = 64
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mla_oracle.c`` into ``liboracle.so`` next to it (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_double
+            lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f64.restype = f64
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_decode.restype = f64
+            lib.oracle_e4m3_encode.argtypes = [f32]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_encode_array.argtypes = [P, P, i64, ctypes.c_int]
+            lib.oracle_e4m3_encode_array.restype = None
+            lib.oracle_attend.argtypes = [P, P, i64, P, i64, i64, ctypes.c_int, ctypes.c_int, f64, P, P, P]
+            lib.oracle_attend.restype = None
+            lib.oracle_record_bytes.argtypes = [ctypes.c_int]
+            lib.oracle_record_bytes.restype = i64
+            lib.oracle_cache_append.argtypes = [ctypes.c_int, P, i64, P, P, P, i64]
+            lib.oracle_cache_append.restype = i64
+            lib.oracle_read_record.argtypes = [ctypes.c_int, P, i64, P, P]
+            lib.oracle_read_record.restype = None
+            lib.oracle_mla_decode.argtypes = [ctypes.c_int, P, i64, P, P, P, i32, P, P, i32, i32, i32,
+                                              f32, P, i64, P, P, ctypes.c_int]
+            lib.oracle_mla_decode.restype = ctypes.c_int
+            lib.oracle_combine.argtypes = [P, P, i32, i64, P, P]
+            lib.oracle_combine.restype = None
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def e4m3_decode(code: int) -> float:
+    """OCP OFP8 E4M3 value of one code (exact)."""
+    return float(_load().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    """OCP OFP8 E4M3 round-to-nearest-even, saturating at +-448, of one fp32 value."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def e4m3_encode_array(x: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(x), _ptr(out), x.size, nthreads)
+    return out
+
+
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, return_scores: bool = False):
+    """Scaled dot-product attention of one query (fp64): returns (out[dv], lse[, scores[n]]).
+
+    s_t = scale * q.K_t ; lse = ln sum exp(s_t) ; out = sum exp(s_t - lse) V_t
+    ("What attention stores, and what DeepSeek changed", section "The four numbers attention
+    works with").
+    """
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    K = np.ascontiguousarray(K, dtype=np.float64)
+    V = np.ascontiguousarray(V, dtype=np.float64)
+    n, dk = K.shape
+    nv, dv = V.shape
+    assert nv == n and q.shape == (dk,)
+    out = np.empty(dv, dtype=np.float64)
+    lse = np.empty(1, dtype=np.float64)
+    s = np.empty(max(n, 1), dtype=np.float64)
+    _load().oracle_attend(_ptr(q), _ptr(K), dk, _ptr(V), dv, n, dk, dv, float(scale),
+                          _ptr(out), _ptr(lse), _ptr(s))
+    if return_scores:
+        return out, float(lse[0]), s[:n]
+    return out, float(lse[0])
+
+
+def record_bytes(fmt: int) -> int:
+    return int(_load().oracle_record_bytes(int(fmt)))
+
+
+def new_pool(fmt: int, num_pages: int) -> np.ndarray:
+    """A zero-filled host pool of ``num_pages`` 64-token pages (uint8)."""
+    return np.zeros(num_pages * PAGE * record_bytes(fmt), dtype=np.uint8)
+
+
+def cache_append(fmt: int, pool: np.ndarray, c_kv: np.ndarray, k_rope: np.ndarray,
+                 slot: np.ndarray) -> int:
+    """Write T tokens (bf16 bits c_kv[T,512], k_rope[T,64]) into ``pool`` at ``slot``.
+
+    Returns the number of rows whose slot lies outside the pool (not written).
+    """
+    c_kv = np.ascontiguousarray(c_kv, dtype=np.uint16)
+    k_rope = np.ascontiguousarray(k_rope, dtype=np.uint16)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    T = slot.shape[0]
+    assert c_kv.shape == (T, D_C) and k_rope.shape == (T, D_R)
+    num_pages = pool.size // (PAGE * record_bytes(fmt))
+    return int(_load().oracle_cache_append(fmt, _ptr(pool), num_pages, _ptr(c_kv), _ptr(k_rope),
+                                           _ptr(slot), T))
+
+
+def read_record(fmt: int, pool: np.ndarray, slot: int):
+    """(c[512], k_rope[64]) of one cached token as exact doubles."""
+    c = np.empty(D_C, dtype=np.float64)
+    kr = np.empty(D_R, dtype=np.float64)
+    _load().oracle_read_record(fmt, _ptr(pool), int(slot), _ptr(c), _ptr(kr))
+    return c, kr
+
+
+def mla_decode(fmt: int, pool: np.ndarray, q_lat: np.ndarray, q_rope: np.ndarray,
+               block_table: np.ndarray, seq_lens: np.ndarray, scale: float,
+               topk_idx: np.ndarray | None = None, pairs=None, nthreads: int = 0):
+    """Absorbed MLA decode in fp64 for the (b, h) pairs given (all pairs by default).
+
+    q_lat: bf16 bits [B,H,512]; q_rope: bf16 bits [B,H,64]; block_table int32 [B,max_pages];
+    seq_lens int32 [B]; topk_idx int32 [B,topk] or None.
+    Returns (out float64[n_pairs,512], lse float64[n_pairs], pairs int32[n_pairs,2]).
+    """
+    q_lat = np.ascontiguousarray(q_lat, dtype=np.uint16)
+    q_rope = np.ascontiguousarray(q_rope, dtype=np.uint16)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, H, _ = q_lat.shape
+    if pairs is None:
+        pairs = np.stack(np.meshgrid(np.arange(B), np.arange(H), indexing="ij"), -1).reshape(-1, 2)
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    order = np.argsort(pairs[:, 0], kind="stable")
+    sp = np.ascontiguousarray(pairs[order])
+    n = sp.shape[0]
+    out = np.empty((n, D_C), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    topk = 0
+    if topk_idx is not None:
+        topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+        topk = topk_idx.shape[1]
+    num_pages = pool.size // (PAGE * record_bytes(fmt))
+    rc = _load().oracle_mla_decode(fmt, _ptr(pool), num_pages, _ptr(q_lat), _ptr(q_rope),
+                                   _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                   _ptr(topk_idx), topk, B, H, float(np.float32(scale)),
+                                   _ptr(sp), n, _ptr(out), _ptr(lse), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_mla_decode: a visible position maps outside the pool")
+    res_out = np.empty_like(out)
+    res_lse = np.empty_like(lse)
+    res_out[order] = out
+    res_lse[order] = lse
+    return res_out, res_lse, pairs
+
+
+def combine(o_part: np.ndarray, lse_part: np.ndarray):
+    """Merge split-KV partials: o_part float32[S,D], lse_part float32[S] -> (out[D], lse)."""
+    o_part = np.ascontiguousarray(o_part, dtype=np.float32)
+    lse_part = np.ascontiguousarray(lse_part, dtype=np.float32)
+    S, D = o_part.shape
+    out = np.empty(D, dtype=np.float64)
+    lse = np.empty(1, dtype=np.float64)
+    _load().oracle_combine(_ptr(o_part), _ptr(lse_part), S, D, _ptr(out), _ptr(lse))
+    return out, float(lse[0])

@@ -1,0 +1,345 @@
+/*
+ * mla_oracle.c -- plain fp64 CPU oracle for absorbed MLA decode over a paged latent cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or call this file:
+ * only the tests, the package smoke check and the benchmark's CPU-baseline leg use it.  It
+ * shares no code, header, table or constant generator with the CUDA library.
+ *
+ * Sources (web pages; section / figure named in each function):
+ *   [KV]  "DeepSeek's KV Cache: From 3.9 MB to 890 B per Token" (ai-systems-engineering.com)
+ *   [MLA] "What attention stores, and what DeepSeek changed" (yashdatta.dev)
+ *   [SKV] "Shared KV Memory: From Transformers to DeepSeek" (nilsonchapagain.com.np)
+ *   [OCP] OCP 8-bit Floating Point Specification (OFP8), format E4M3 -- the FP8 code the
+ *         [KV] page's "Calculating V3.2's KV cache" section stores C^KV in.
+ *
+ * Every floating-point step is done in double precision.  Inputs are bf16 bit patterns
+ * (uint16) and fp32 scales, widened exactly; the FP8 encoder works on fp32 as the cache
+ * format prescribes.  Nothing is blocked, fused or reordered beyond the plain definitions.
+ *
+ * Parity status: every function is pinned by a test under tests/ (worked example, expanded
+ * brute force, closed forms, codec properties, special cases); none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_DC 512      /* latent width d_c of C^KV  ([KV] Fig. 3, "Shared KV path")      */
+#define ORACLE_DR 64       /* rotary key width d_R of K^R ([KV] Fig. 3, "Shared rotary key") */
+#define ORACLE_DK (ORACLE_DC + ORACLE_DR)
+#define ORACLE_PAGE 64     /* tokens per cache page (paged-pool layout of this library)     */
+#define ORACLE_FP8_GROUP 128 /* one fp32 scale per 128 latent dims ([KV] "Calculating V3.2") */
+
+enum { ORACLE_BF16 = 0, ORACLE_FP8_MIXED = 1 };
+
+/* ---------------------------------------------------------------------------------------- */
+/* Scalar codecs                                                                             */
+/* ---------------------------------------------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+double oracle_bf16_to_f64(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* [OCP] E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
+ * S.1111.111 is NaN.  Normal: 2^(E-7) * (1 + M/8) for E in 1..15; subnormal (E = 0):
+ * 2^-6 * M/8.  Decoding is exact in double. */
+double oracle_e4m3_decode(uint8_t code) {
+    int s = (code >> 7) & 1;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* [OCP] E4M3 encoding of an fp32 value, round-to-nearest-even, saturating to the largest
+ * finite magnitude (448) instead of producing NaN ("satfinite").  Written from the
+ * definition: the non-negative finite codes 0x00..0x7E are strictly increasing in value,
+ * so the result is the code nearest to |x|, and on an exact tie the code whose lowest
+ * mantissa bit is 0 (the "even" one).  NaN input maps to the NaN code 0x7F. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    /* binary search for the largest code lo with value(lo) <= a */
+    int lo = 0, hi = 0x7E;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (oracle_e4m3_decode((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+    }
+    if (lo == 0x7E) return sign | 0x7E;
+    double vlo = oracle_e4m3_decode((uint8_t)lo);
+    double vhi = oracle_e4m3_decode((uint8_t)(lo + 1));
+    int code;
+    if (a - vlo < vhi - a) code = lo;
+    else if (a - vlo > vhi - a) code = lo + 1;
+    else code = (lo & 1) ? lo + 1 : lo;   /* tie: even mantissa */
+    return sign | (uint8_t)code;
+}
+
+/* Bulk wrappers for the exhaustive codec sweep in the tests. */
+void oracle_e4m3_encode_array(const float* x, uint8_t* codes, int64_t n, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < n; ++i) codes[i] = oracle_e4m3_encode(x[i]);
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Attention core                                                                            */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Scaled dot-product attention of one query over n keys/values ([MLA] "The four numbers
+ * attention works with"; [SKV] section 1 "Attention reads a set of vectors"):
+ *   s_t   = scale * (q . K_t)
+ *   lse   = ln sum_t exp(s_t)          (computed as m + ln sum exp(s_t - m), m = max s_t)
+ *   out   = sum_t exp(s_t - lse) * V_t
+ * K rows have dk entries at stride ldk, V rows dv entries at stride ldv (V may alias K).
+ * n == 0: out = 0 and lse = -inf (nothing visible).  The scores are returned when s != NULL. */
+void oracle_attend(const double* q, const double* K, int64_t ldk, const double* V, int64_t ldv,
+                   int64_t n, int dk, int dv, double scale, double* out, double* lse, double* s_out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int j = 0; j < dv; ++j) out[j] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        free(s);
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int k = 0; k < dk; ++k) dot += q[k] * K[t * ldk + k];
+        s[t] = scale * dot;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int64_t t = 0; t < n; ++t) l += exp(s[t] - m);
+    double L = m + log(l);
+    for (int64_t t = 0; t < n; ++t) {
+        double p = exp(s[t] - L);
+        for (int j = 0; j < dv; ++j) out[j] += p * V[t * ldv + j];
+    }
+    *lse = L;
+    if (s_out) memcpy(s_out, s, sizeof(double) * (size_t)n);
+    free(s);
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Cache record format                                                                       */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Bytes of one token's record in one layer.
+ *   BF16: (C^KV 512 + K^R 64) x 2 B = 1,152 B        ([KV] "Calculating V2's KV cache")
+ *   FP8 mixed: 512 B e4m3 + 4 x 4 B fp32 scales + 64 x 2 B bf16 rope = 656 B
+ *              ([KV] "Calculating V3.2's KV cache"; field order as in FlashMLA's FP8 format,
+ *               listed in the page's "Cache formats used for storage", no padding). */
+int64_t oracle_record_bytes(int fmt) {
+    if (fmt == ORACLE_BF16) return (ORACLE_DC + ORACLE_DR) * 2;
+    if (fmt == ORACLE_FP8_MIXED) return ORACLE_DC + (ORACLE_DC / ORACLE_FP8_GROUP) * 4 + ORACLE_DR * 2;
+    return -1;
+}
+
+/* Write T new tokens into their slots (slot = page * 64 + row; slot < 0 skips the row).
+ * BF16: the 576 bf16 values are stored as they are.
+ * FP8 mixed, per 128-dim group g of the latent (the scale rule is absmax / 448, so that the
+ * largest magnitude maps onto the largest finite E4M3 value):
+ *     amax = max |x| (fp32),  s_g = fl32(amax / 448),  code = E4M3_RNE_satfinite(fl32(x / s_g)),
+ *     amax == 0 gives s_g = 0 and all-zero codes;  the 64 rope values stay bf16.
+ * Returns the number of rows whose slot is outside the pool (those rows are not written). */
+int64_t oracle_cache_append(int fmt, uint8_t* pool, int64_t num_pages, const uint16_t* c_kv,
+                            const uint16_t* k_rope, const int32_t* slot, int64_t T) {
+    int64_t rb = oracle_record_bytes(fmt);
+    int64_t bad = 0;
+    for (int64_t i = 0; i < T; ++i) {
+        int64_t sl = slot[i];
+        if (sl < 0) continue;
+        if (sl >= num_pages * ORACLE_PAGE) { ++bad; continue; }
+        uint8_t* rec = pool + sl * rb;
+        const uint16_t* c = c_kv + i * ORACLE_DC;
+        const uint16_t* r = k_rope + i * ORACLE_DR;
+        if (fmt == ORACLE_BF16) {
+            memcpy(rec, c, ORACLE_DC * 2);
+            memcpy(rec + ORACLE_DC * 2, r, ORACLE_DR * 2);
+        } else {
+            for (int g = 0; g < ORACLE_DC / ORACLE_FP8_GROUP; ++g) {
+                float amax = 0.0f;
+                for (int k = 0; k < ORACLE_FP8_GROUP; ++k) {
+                    float v = fabsf((float)oracle_bf16_to_f64(c[g * ORACLE_FP8_GROUP + k]));
+                    if (v > amax) amax = v;
+                }
+                float sg = amax / 448.0f;
+                for (int k = 0; k < ORACLE_FP8_GROUP; ++k) {
+                    float v = (float)oracle_bf16_to_f64(c[g * ORACLE_FP8_GROUP + k]);
+                    rec[g * ORACLE_FP8_GROUP + k] = (amax == 0.0f) ? 0 : oracle_e4m3_encode(v / sg);
+                }
+                memcpy(rec + ORACLE_DC + 4 * g, &sg, 4);
+            }
+            memcpy(rec + ORACLE_DC + 16, r, ORACLE_DR * 2);
+        }
+    }
+    return bad;
+}
+
+/* Read one record back as exact doubles: c[512], kr[64].
+ * FP8 mixed: c[k] = e4m3_value(code[k]) * s_{k / 128}, exact in double (at most 4 + 24
+ * significant bits); the scale "brings values stored at low precision back to their
+ * original size" ([KV] "KV cache per token at a glance"). */
+void oracle_read_record(int fmt, const uint8_t* pool, int64_t slot, double* c, double* kr) {
+    int64_t rb = oracle_record_bytes(fmt);
+    const uint8_t* rec = pool + slot * rb;
+    if (fmt == ORACLE_BF16) {
+        for (int k = 0; k < ORACLE_DC; ++k) {
+            uint16_t b;
+            memcpy(&b, rec + 2 * k, 2);
+            c[k] = oracle_bf16_to_f64(b);
+        }
+        for (int r = 0; r < ORACLE_DR; ++r) {
+            uint16_t b;
+            memcpy(&b, rec + 2 * ORACLE_DC + 2 * r, 2);
+            kr[r] = oracle_bf16_to_f64(b);
+        }
+    } else {
+        float sc[ORACLE_DC / ORACLE_FP8_GROUP];
+        memcpy(sc, rec + ORACLE_DC, sizeof sc);
+        for (int k = 0; k < ORACLE_DC; ++k)
+            c[k] = oracle_e4m3_decode(rec[k]) * (double)sc[k / ORACLE_FP8_GROUP];
+        for (int r = 0; r < ORACLE_DR; ++r) {
+            uint16_t b;
+            memcpy(&b, rec + ORACLE_DC + 16 + 2 * r, 2);
+            kr[r] = oracle_bf16_to_f64(b);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Absorbed MLA decode                                                                       */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Absorbed MLA decode for a list of (request b, head h) pairs.
+ *
+ * Per request b the visible set is every cached position t = 0 .. seq_lens[b]-1, the newest
+ * token included ([KV] "The score that picks positions": "itself included"; [SKV] causal
+ * mask M_tj = 0 for j <= t).  With topk_idx != NULL it is instead the listed entries
+ * topk_idx[b][j] with 0 <= idx < seq_lens[b], each taken once as listed ([KV] Fig. 10:
+ * the selection mask M keeps probability only at picked positions, and the softmax
+ * renormalises over them).
+ *
+ * Position t lives at page block_table[b][t / 64], row t % 64.  For each visible t the
+ * record gives c_t (512) and k^R_t (64), and for head h
+ *     s_t = scale * ( q_lat[b,h,:] . c_t + q_rope[b,h,:] . k^R_t )
+ * which is the absorbed content score (Q^C_h (W^UK_h)^T) (C^KV)^T plus the rotary score
+ * Q^R_h (K^R)^T, divided by sqrt(d_k + d_r) ([KV] Fig. 4 (1) and Fig. 5 (2)).  The output is
+ * the absorbed value path U_h = sum_t P_t c_t ([KV] Fig. 6 (2)), i.e. attention with
+ * K_t = [c_t | k^R_t] and V_t = c_t, plus lse = ln sum_t exp(s_t).
+ *
+ * out: double[n_pairs][512], lse: double[n_pairs].
+ * Returns 0, or -1 if a visible position's page lies outside the pool or a page index is
+ * negative (nothing is computed for that pair then; its lse is NaN). */
+int oracle_mla_decode(int fmt, const uint8_t* pool, int64_t num_pages,
+                      const uint16_t* q_lat, const uint16_t* q_rope,
+                      const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                      const int32_t* topk_idx, int32_t topk, int32_t B, int32_t H, float scale,
+                      const int32_t* pairs, int64_t n_pairs, double* out, double* lse,
+                      int nthreads) {
+    int rc = 0;
+    (void)B;
+    /* Group pairs by request so each request's K rows are gathered once. */
+    for (int64_t i0 = 0; i0 < n_pairs;) {
+        int32_t b = pairs[2 * i0];
+        int64_t i1 = i0;
+        while (i1 < n_pairs && pairs[2 * i1] == b) ++i1;
+
+        int64_t N = seq_lens[b];
+        int64_t n = 0;
+        int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)((topk_idx ? topk : N) + 1));
+        if (topk_idx) {
+            for (int32_t j = 0; j < topk; ++j) {
+                int64_t t = topk_idx[(int64_t)b * topk + j];
+                if (t >= 0 && t < N) pos[n++] = t;
+            }
+        } else {
+            for (int64_t t = 0; t < N; ++t) pos[n++] = t;
+        }
+        double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORACLE_DK);
+        int bad = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t t = pos[j];
+            int64_t pg = t / ORACLE_PAGE;
+            if (pg >= max_pages) { bad = 1; break; }
+            int64_t page = block_table[(int64_t)b * max_pages + pg];
+            if (page < 0 || page >= num_pages) { bad = 1; break; }
+            oracle_read_record(fmt, pool, page * ORACLE_PAGE + t % ORACLE_PAGE,
+                               K + j * ORACLE_DK, K + j * ORACLE_DK + ORACLE_DC);
+        }
+        if (bad) {
+            rc = -1;
+            for (int64_t i = i0; i < i1; ++i) lse[i] = NAN;
+        } else {
+#ifdef _OPENMP
+            if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+#endif
+            for (int64_t i = i0; i < i1; ++i) {
+                int32_t h = pairs[2 * i + 1];
+                double q[ORACLE_DK];
+                for (int k = 0; k < ORACLE_DC; ++k)
+                    q[k] = oracle_bf16_to_f64(q_lat[((int64_t)b * H + h) * ORACLE_DC + k]);
+                for (int r = 0; r < ORACLE_DR; ++r)
+                    q[ORACLE_DC + r] = oracle_bf16_to_f64(q_rope[((int64_t)b * H + h) * ORACLE_DR + r]);
+                oracle_attend(q, K, ORACLE_DK, K, ORACLE_DK, n, ORACLE_DK, ORACLE_DC,
+                              (double)scale, out + i * ORACLE_DC, lse + i, NULL);
+            }
+        }
+        free(K);
+        free(pos);
+        i0 = i1;
+    }
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Split-KV merge                                                                            */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Merge S partial results of the same query over disjoint position sets.  Partial i holds the
+ * normalised output o_i over its positions and lse_i = ln sum exp(s_t) over them.  Then, with
+ * lse = ln sum_i exp(lse_i), the whole-set output is sum_i exp(lse_i - lse) o_i: the softmax
+ * over the union renormalises each part by its share of the mass (the same renormalisation
+ * [KV] Fig. 10 applies to a subset).  Partials with lse_i = -inf (no positions) contribute
+ * nothing; if all are empty, out = 0 and lse = -inf. */
+void oracle_combine(const float* o_part, const float* lse_part, int32_t S, int64_t D,
+                    double* out, double* lse) {
+    double m = -INFINITY;
+    for (int32_t i = 0; i < S; ++i)
+        if ((double)lse_part[i] > m) m = lse_part[i];
+    for (int64_t j = 0; j < D; ++j) out[j] = 0.0;
+    if (m == -INFINITY) { *lse = -INFINITY; return; }
+    double l = 0.0;
+    for (int32_t i = 0; i < S; ++i) l += exp((double)lse_part[i] - m);
+    double L = m + log(l);
+    for (int32_t i = 0; i < S; ++i) {
+        double w = exp((double)lse_part[i] - L);
+        if (w == 0.0) continue;
+        for (int64_t j = 0; j < D; ++j) out[j] += w * (double)o_part[(int64_t)i * D + j];
+    }
+    *lse = L;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
