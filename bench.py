@@ -1,0 +1,410 @@
+#!/usr/bin/env python3
+"""Benchmark of absorbed MLA decode over a paged latent cache on GB300.
+
+A step is one pass of the hot path over one batch: mla_cache_append of the newest token of
+every request (bf16 record) followed by mla_decode of the whole batch (page gather, scores,
+online softmax, weighted latent sum, split-KV merge).  Default workload: the batched paged
+decode (B=32, H=128, seq_lens uniform in [1024, 8192], 64-token pages shuffled in a shared pool,
+bf16 cache, scale 1/sqrt(192)).
+
+Timing: W warm-up steps, then exactly K steps bracketed by a barrier and a device synchronise,
+timed with CUDA events on the launching stream, max over ranks.  Each step is a CUDA graph of
+the two library calls (the calls take about as long as the kernels, so eager launches would
+time the host).  The inputs rotate over several identical pool replicas whose total exceeds L2,
+so every step reads its cache from HBM.
+
+One JSON line on stdout (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode KV GB/s, TFLOP/s and % of GB300 roofline; decode tokens/s at B×ctx"
+UNIT = "KV GB/s"
+L2_BYTES = 126 * 2 ** 20
+
+# DRAM bytes per decode launch from an ncu capture, keyed by the sha256 of the decode kernel
+# sources it was taken on; any change to those sources makes the entry stale (traffic = null).
+NCU_TRAFFIC = {}
+DECODE_SOURCES = ["mla_latent_kv_decode_gb300/csrc/decode_simt.cu",
+                  "mla_latent_kv_decode_gb300/csrc/combine.cu"]
+
+
+def _sources_hash() -> str:
+    h = hashlib.sha256()
+    for p in DECODE_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+# Reference arm / CPU baseline: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------------------------
+
+def _oracle_requests(w, budget_s: float, nthreads: int):
+    import oracle
+    from mla_latent_kv_decode_gb300 import synth
+    ql, qr = w.queries()
+    done, tokens, spent = 0, 0, 0.0
+    b = 0
+    while b < w.B and (spent < budget_s or done == 0):
+        n = int(w.seq_lens[b])
+        pages = (n + 63) // 64
+        pool = oracle.new_pool(w.fmt, pages)
+        c, r = synth.kv_rows(w.seed, b, 0, n)
+        oracle.cache_append(w.fmt, pool, c, r, np.arange(n, dtype=np.int32))
+        bt = np.arange(pages, dtype=np.int32)[None]
+        pairs = [(0, h) for h in range(w.H)]
+        t0 = time.perf_counter()
+        oracle.mla_decode(w.fmt, pool, ql[b:b + 1], qr[b:b + 1], bt, w.seq_lens[b:b + 1], w.scale,
+                          pairs=pairs, nthreads=nthreads)
+        spent += time.perf_counter() - t0
+        tokens += n
+        done += 1
+        b += 1
+    return tokens, spent, done
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    import oracle
+    nth = os.cpu_count() or 1
+    oracle.build()
+    tokens, spent, done = _oracle_requests(w, budget_s, nth)
+    rb = 1152 if w.fmt == 0 else 656
+    return {"value": round(tokens * rb / spent / 1e9, 6), "unit": UNIT, "cores": nth,
+            "kind": "oracle",
+            "sample": f"{done} of {w.B} requests of the {w.name} workload, all {w.H} heads, "
+                      f"{tokens} attended positions, {spent:.1f} s of fp64 oracle time "
+                      f"({nth} OpenMP threads)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from mla_latent_kv_decode_gb300 import synth
+    import oracle
+    oracle.build()
+    w = synth.make_workload(args.workload)
+    nth = os.cpu_count() or 1
+    rb = 1152 if w.fmt == 0 else 656
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_requests(w, budget / 4, nth)
+    tok, sec, req = 0, 0.0, 0
+    for _ in range(args.steps):
+        t, s, d = _oracle_requests(w, budget, nth)
+        tok, sec, req = tok + t, sec + s, req + d
+    value = tok * rb / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "kv_format": "bf16" if w.fmt == 0 else "fp8_mixed",
+                       "description": w.description},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": nth, "kind": "oracle",
+                             "sample": f"each step: whole requests of the {w.name} workload "
+                                       f"(all heads) for ~{budget:.1f} s; {req} requests, {tok} "
+                                       f"positions in total"},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import mla_latent_kv_decode_gb300 as mla
+    from mla_latent_kv_decode_gb300 import harness, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    mla.load()
+    w = synth.make_workload(args.workload)
+    one_pool = mla.pool_bytes(w.fmt, w.num_pages)
+    replicas = max(1, min(8, -(-3 * L2_BYTES // max(one_pool, 1)) + 1)) if args.replicas == 0 else args.replicas
+    skip = 1 if w.appended == 0 else w.appended
+    dw = harness.DeviceWorkload(w, replicas=replicas, prefill_skip_last=skip)
+    dw.alloc_outputs()
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # eager warm-up (also sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for r in range(replicas):
+            dw.step(r)
+    stream.synchronize()
+    rc = mla.check_status()
+    if rc != 0:
+        raise mla.MlaError(rc, "warm-up")
+
+    # one graph per replica: append + decode
+    graphs = []
+    for r in range(replicas):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            dw.step(r)
+        graphs.append(g)
+    dec_graphs = []
+    reps = 20
+    for r in range(replicas):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                dw.decode((r + i) % replicas)
+        dec_graphs.append(g)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % replicas].replay()
+    barrier()
+
+    # ---- timed region: exactly K steps ----
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % replicas].replay()
+        ev1.record(stream)
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- decode-kernel timing (roofline): graphs of `reps` back-to-back decode calls ----
+    n_dec = max(10, min(200, args.steps // reps + 1))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n_dec):
+            dec_graphs[i % replicas].replay()
+        e1.record(stream)
+    barrier()
+    dec_ms = e0.elapsed_time(e1) / (n_dec * reps)
+    clocks = sampler.stop()
+    rc = mla.check_status()
+    if rc != 0:
+        raise mla.MlaError(rc, "timed region")
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, dw, torch, mla, stream, barrier, dist)
+
+    kv_bytes = dw.kv_bytes()
+    alg_bytes = dw.algorithmic_bytes()
+    flops = dw.flops()
+    step_s = ms / 1e3 / args.steps
+    value = world * kv_bytes / step_s / 1e9
+    peaks = _peaks()
+    dec_s = dec_ms / 1e3
+    achieved = alg_bytes / dec_s / 1e9
+    traffic = NCU_TRAFFIC.get(_sources_hash())
+    launches_per_step = 1 + int(mla.load().mla_decode_launches(w.fmt, w.B, w.H, w.max_seq_len, 0))
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "kv_format": "bf16" if w.fmt == 0 else "fp8_mixed",
+                   "seq_lens": "uniform in [1024, 8192]" if w.name == "paged_batch" else w.description,
+                   "attended_tokens": w.attended(), "page_tokens": 64, "scale": w.scale,
+                   "step": "cache_append of each request's newest token + mla_decode of the batch",
+                   "l2": f"inputs larger than L2: {replicas} rotating pool replicas of "
+                         f"{one_pool / 2**20:.0f} MiB", "parallelism": f"replicas x{world}"},
+        "decode_tokens_per_s": round(world * w.B / step_s, 1),
+        "tflops": round(world * flops / step_s / 1e12, 3),
+        "step_frac_of_hbm_roofline": round((alg_bytes / (peaks['hbm_gbs'] * 1e9)) / step_s, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "peak_source": peaks["source"],
+                     "kernel": "mla_decode call", "ms_per_launch": round(dec_ms, 6),
+                     "bytes_per_launch": alg_bytes},
+        "tensor_util": {"achieved_tflops": round(flops / dec_s / 1e12, 2),
+                        "peak": peaks["bf16_tflops_sustained"],
+                        "frac": round(flops / dec_s / 1e12 / peaks["bf16_tflops_sustained"], 4)},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, dw, torch, mla, stream, barrier, dist):
+    """Same metric through the public API with pinned host buffers: every step copies its inputs
+    (queries, block table, seq_lens, new rows and slots) host->device, runs append + decode, and
+    reads out + lse back."""
+    w = dw.w
+    host = {}
+    dev = {"q_lat": dw.q_lat, "q_rope": dw.q_rope, "block_table": dw.block_table,
+           "seq_lens": dw.seq_lens, "new_c": dw.new_c, "new_r": dw.new_r, "new_slot": dw.new_slot}
+    for k, v in dev.items():
+        host[k] = v.cpu().pin_memory()
+    out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    lse_h = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    steps = max(3, min(args.steps, 200))
+
+    def one(i):
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        dw.step(i % dw.replicas)
+        out_h.copy_(dw.out, non_blocking=True)
+        lse_h.copy_(dw.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            one(i)
+        e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = 1 if dist is None else dist.get_world_size()
+    value = world * dw.kv_bytes() / (ms / 1e3 / steps) / 1e9
+    return {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="paged_batch",
+                    choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse"])
+    ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0 = enough to exceed L2 3x)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

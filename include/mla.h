@@ -1,0 +1,153 @@
+/*
+ * mla.h -- libmla: absorbed Multi-head Latent Attention decode over a paged latent cache,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  Each cached token of one layer is a latent record [c_KV (512) | k_rope (64)]
+ * ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token", Fig. 3: "What stays in the cache is
+ * C^KV (512 dimensions) and K^R (64 dimensions)").  For a new token, every head h brings a query
+ * already absorbed into the latent space, q_lat[h] = Q^C_h (W^UK_h)^T (512), and a rotary query
+ * q_rope[h] (64) (same page, Fig. 5 (2) "Absorb").  Decode scores every visible position t,
+ *     s_t = scale * (q_lat[h] . c_t + q_rope[h] . k_rope_t)              (Fig. 4 (1); scale is
+ *                                                                        1/sqrt(d_k + d_r))
+ * and returns the absorbed value path U_h = sum_t softmax(s)_t c_t (Fig. 6 (2)) together with
+ * lse_h = ln sum_t exp(s_t).  Optionally only listed positions are visible (the DSA selection
+ * mask of Fig. 10, "MLA that reads only the picked positions").
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; libmla allocates nothing.
+ *    Calls are asynchronous on the caller's stream; host-side validation failures return a
+ *    non-zero status and launch nothing.
+ *  - bf16 arrays hold IEEE bfloat16 values; every array is dense, row-major, C-contiguous.
+ *  - Errors the kernels detect (a page index outside the pool, a wait that ran out) are recorded
+ *    in a per-device error word and reported, then cleared, by mla_check_status().  The outputs
+ *    of a call that recorded an error are undefined.
+ *  - Outputs must not alias inputs.  A token must be written by mla_cache_append before an
+ *    mla_decode reads it; ordering on one stream is enough.
+ *  - Device buffers must be 16-byte aligned; the cache pool must be 128-byte aligned.
+ *
+ * Geometry fixed by the format: D_C = 512 latent dims, D_R = 64 rope dims, H = 128 heads,
+ * 64 tokens per page.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID = 1,      /* bad argument (null pointer, size, alignment, format)        */
+    MLA_ERR_BOUNDS = 2,       /* a kernel met a page/slot index outside the pool             */
+    MLA_ERR_TIMEOUT = 3,      /* a bounded wait inside a kernel ran out; the kernel returned */
+    MLA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed                           */
+    MLA_ERR_UNSUPPORTED = 5   /* the device is not sm_103 / sm_100-family, or a size limit   */
+} mla_status;
+
+typedef enum {
+    /* 1,152 B per token: 512 bf16 latent then 64 bf16 rope ("DeepSeek's KV Cache",
+     * "Calculating V2's KV cache": (C^KV 512 + K^R 64) x 2 B). */
+    MLA_KV_BF16 = 0,
+    /* 656 B per token: 512 E4M3 latent codes, 4 fp32 scales (one per 128 latent dims),
+     * 64 bf16 rope, in that order and without padding ("DeepSeek's KV Cache",
+     * "Calculating V3.2's KV cache": 512 + 16 + 128 = 656 B). */
+    MLA_KV_FP8_MIXED = 1
+} mla_kv_format;
+
+#define MLA_D_C 512
+#define MLA_D_R 64
+#define MLA_HEADS 128
+#define MLA_PAGE_TOKENS 64
+
+/* Bytes of one token's record: 1152 (MLA_KV_BF16) or 656 (MLA_KV_FP8_MIXED); 0 for an unknown
+ * format.  Host only. */
+size_t mla_record_bytes(int32_t fmt);
+
+/* Write T new tokens into the paged pool ("DeepSeek's KV Cache", Fig. 3: C^KV and K^R are what
+ * is cached; "Calculating V3.2's KV cache" for the FP8 mixed record).
+ *   pool       : device, num_pages * 64 * mla_record_bytes(fmt) bytes; slot s lives at byte
+ *                s * mla_record_bytes(fmt) (page = s / 64, row = s % 64).
+ *   c_kv       : device bf16 [T, 512]  latent of each new token.
+ *   k_rope     : device bf16 [T, 64]   rotary key of each new token (already rotated).
+ *   slot       : device int32 [T]      destination slot; a negative slot skips the row; a slot
+ *                >= num_pages * 64 is not written and records MLA_ERR_BOUNDS.
+ * BF16: the 576 values are stored as given.  FP8 mixed, per 128-dim group g: amax = max |x|,
+ * s_g = amax / 448 (fp32, correctly rounded), code = E4M3(x / s_g) rounded to nearest even and
+ * saturated to +-448; amax = 0 gives s_g = 0 and zero codes; rope is stored as bf16.
+ * Only the listed slots change.  Returns MLA_ERR_INVALID for null pointers, T < 0, an unknown
+ * format or a misaligned pool. */
+mla_status mla_cache_append(int32_t fmt, void* pool, int64_t num_pages, const void* c_kv,
+                            const void* k_rope, const int32_t* slot, int64_t T,
+                            cudaStream_t stream);
+
+/* Workspace bytes mla_decode needs for these sizes (0 when no split-KV partials are needed).
+ * max_seq_len is an upper bound of seq_lens; topk is 0 for dense decode. Host only. */
+size_t mla_decode_workspace_bytes(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len,
+                                  int32_t topk);
+
+/* Number of kernels one mla_decode call with these sizes launches (1, or 2 when split-KV
+ * partials are merged by a separate kernel).  Host only. */
+int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len, int32_t topk);
+
+/* Absorbed MLA decode of one layer for B requests (the per-head computation in the file
+ * comment; "DeepSeek's KV Cache", Fig. 4 (1), Fig. 5 (2), Fig. 6 (2), Fig. 10).
+ *   fmt, pool, num_pages : the cache written by mla_cache_append.
+ *   q_lat      : device bf16 [B, H, 512]  absorbed content queries.
+ *   q_rope     : device bf16 [B, H, 64]   rotary queries.
+ *   block_table: device int32 [B, max_pages]; position t of request b is row t % 64 of page
+ *                block_table[b][t / 64].
+ *   seq_lens   : device int32 [B]; request b sees positions 0 .. seq_lens[b]-1 (the newest
+ *                token included).  Every seq_lens[b] must be <= max_seq_len <= max_pages * 64.
+ *   max_seq_len: host-side upper bound of seq_lens, used to size the split-KV grid.
+ *   topk_idx   : NULL for dense decode, or device int32 [B, topk]: request b sees only the
+ *                listed positions p with 0 <= p < seq_lens[b] (others, e.g. -1 padding, are
+ *                skipped).  Listed positions are expected distinct; a repeated one is counted
+ *                as often as it is listed.
+ *   B >= 0, H == 128, scale > 0 finite (normally 1/sqrt(192)).
+ *   out        : device bf16 [B, H, 512] = sum_t softmax(s)_t c_t (zeros if nothing is visible).
+ *   lse        : device fp32 [B, H] = ln sum_t exp(s_t) (-inf if nothing is visible).
+ *   workspace  : device scratch of at least mla_decode_workspace_bytes(...) bytes (may be NULL
+ *                when that is 0); 256-byte aligned; its contents are clobbered.
+ * A page index outside [0, num_pages) met while reading records MLA_ERR_BOUNDS. */
+mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
+                      const void* q_rope, const int32_t* block_table, int32_t max_pages,
+                      const int32_t* seq_lens, int32_t max_seq_len, const int32_t* topk_idx,
+                      int32_t topk, int32_t B, int32_t H, float scale, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Split-KV merge: S partial results of the same queries over disjoint position sets.
+ *   o_part  : device fp32 [S, B, H, 512] normalised partial outputs.
+ *   lse_part: device fp32 [S, B, H] partial log-sum-exps (-inf for an empty part).
+ *   out     : device bf16 [B, H, 512] = sum_i exp(lse_i - lse) o_i;  lse: device fp32 [B, H]
+ *             = ln sum_i exp(lse_i).  All parts empty: out = 0, lse = -inf.
+ * This is the renormalisation of a softmax restricted to parts of the visible set ("DeepSeek's
+ * KV Cache", Fig. 10; "Shared KV Memory", "What is lost by restricting the support?"). */
+mla_status mla_combine(const float* o_part, const float* lse_part, int32_t S, int32_t B,
+                       int32_t H, void* out, float* lse, cudaStream_t stream);
+
+/* Synchronise `stream`, then return and clear the first error a kernel recorded on the current
+ * device (MLA_OK if none); a pending CUDA error is returned as MLA_ERR_CUDA. */
+mla_status mla_check_status(cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* mla_status_string(mla_status status);
+
+/* Iteration cap of every bounded wait inside libmla kernels on the current device (0 restores
+ * the default).  When a wait runs out the kernel records MLA_ERR_TIMEOUT, drains its own
+ * copies in flight, frees its tensor memory and returns.  Meant for tests of that path. */
+mla_status mla_set_wait_limit(uint32_t iterations);
+
+/* E4M3 encoding of n fp32 values with the device conversion mla_cache_append uses (round to
+ * nearest even, saturating to +-448): codes[i] = E4M3(x[i]).  Device pointers; for checking
+ * the conversion against an independent encoder (OCP OFP8 specification, format E4M3). */
+mla_status mla_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

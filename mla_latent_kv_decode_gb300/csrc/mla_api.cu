@@ -1,0 +1,217 @@
+// mla_api.cu -- the C ABI of libmla: argument validation, per-device state, launches.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+__device__ DevCtl g_ctl = {0, 0, kDefaultWaitLimit, 0};
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DevCtl* g_ctl_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+int g_cc[kMaxDevices] = {};
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+bool init_device(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ctl_ptr[dev]) return true;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ctl) != cudaSuccess) return false;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return false;
+    g_sms[dev] = prop.multiProcessorCount;
+    g_cc[dev] = prop.major * 10 + prop.minor;
+    g_ctl_ptr[dev] = static_cast<DevCtl*>(p);
+    return true;
+}
+}  // namespace
+
+DevCtl* device_ctl() {
+    int dev = current_device();
+    if (dev < 0 || !init_device(dev)) return nullptr;
+    return g_ctl_ptr[dev];
+}
+
+int num_sms() {
+    int dev = current_device();
+    if (dev < 0 || !init_device(dev)) return 0;
+    return g_sms[dev];
+}
+
+int device_cc() {
+    int dev = current_device();
+    if (dev < 0 || !init_device(dev)) return 0;
+    return g_cc[dev];
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+namespace {
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool fmt_ok(int32_t fmt) { return fmt == MLA_KV_BF16 || fmt == MLA_KV_FP8_MIXED; }
+mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+// The kernels are built for sm_103a only; any other device would fail at launch.
+bool device_supported() { return device_cc() == 103; }
+}  // namespace
+
+extern "C" {
+
+size_t mla_record_bytes(int32_t fmt) {
+    if (fmt == MLA_KV_BF16) return kBf16RecordBytes;
+    if (fmt == MLA_KV_FP8_MIXED) return kFp8RecordBytes;
+    return 0;
+}
+
+mla_status mla_cache_append(int32_t fmt, void* pool, int64_t num_pages, const void* c_kv,
+                            const void* k_rope, const int32_t* slot, int64_t T,
+                            cudaStream_t stream) {
+    if (!fmt_ok(fmt) || T < 0 || num_pages < 0) return MLA_ERR_INVALID;
+    if (T == 0) return MLA_OK;
+    if (!pool || !c_kv || !k_rope || !slot) return MLA_ERR_INVALID;
+    if (!aligned(pool, 128) || !aligned(c_kv, 16) || !aligned(k_rope, 16) || !aligned(slot, 4))
+        return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_cache_append(fmt, static_cast<uint8_t*>(pool), num_pages,
+                                         static_cast<const __nv_bfloat16*>(c_kv),
+                                         static_cast<const __nv_bfloat16*>(k_rope), slot, T, ctl,
+                                         stream));
+}
+
+size_t mla_decode_workspace_bytes(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len,
+                                  int32_t topk) {
+    if (!fmt_ok(fmt) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;
+    int sms = num_sms();
+    if (sms <= 0) sms = 152;
+    return plan_decode(fmt, B, max_seq_len, topk, sms).workspace;
+}
+
+int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len,
+                            int32_t topk) {
+    if (!fmt_ok(fmt) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;
+    int sms = num_sms();
+    if (sms <= 0) sms = 152;
+    return plan_decode(fmt, B, max_seq_len, topk, sms).launches;
+}
+
+mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
+                      const void* q_rope, const int32_t* block_table, int32_t max_pages,
+                      const int32_t* seq_lens, int32_t max_seq_len, const int32_t* topk_idx,
+                      int32_t topk, int32_t B, int32_t H, float scale, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!fmt_ok(fmt) || B < 0 || H != kHeads || num_pages < 0 || max_pages < 0 ||
+        max_seq_len < 0 || topk < 0)
+        return MLA_ERR_INVALID;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * kPage) return MLA_ERR_INVALID;
+    if (B == 0) return MLA_OK;
+    if (!pool || !q_lat || !q_rope || !block_table || !seq_lens || !out || !lse)
+        return MLA_ERR_INVALID;
+    if (topk_idx == nullptr && topk != 0) return MLA_ERR_INVALID;
+    if (topk_idx != nullptr && topk == 0) return MLA_ERR_INVALID;
+    if (!aligned(pool, 128) || !aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(out, 16) ||
+        !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+        (topk_idx && !aligned(topk_idx, 4)))
+        return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    DecodePlan plan = plan_decode(fmt, B, max_seq_len, topk, num_sms());
+    DecodeArgs a;
+    a.fmt = fmt;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.num_pages = num_pages;
+    a.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+    a.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.topk_idx = topk_idx;
+    a.topk = topk;
+    a.B = B;
+    a.scale = scale;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.o_part = nullptr;
+    a.lse_part = nullptr;
+    a.ctl = ctl;
+    if (plan.workspace > 0) {
+        if (!workspace || workspace_bytes < plan.workspace || !aligned(workspace, 256))
+            return MLA_ERR_INVALID;
+        a.o_part = static_cast<float*>(workspace);
+        a.lse_part = a.o_part + (size_t)plan.splits * B * kHeads * kDc;
+    }
+    return from_cuda(launch_decode(a, plan, stream));
+}
+
+mla_status mla_combine(const float* o_part, const float* lse_part, int32_t S, int32_t B, int32_t H,
+                       void* out, float* lse, cudaStream_t stream) {
+    if (S <= 0 || B < 0 || H <= 0) return MLA_ERR_INVALID;
+    if (B == 0) return MLA_OK;
+    if (!o_part || !lse_part || !out || !lse) return MLA_ERR_INVALID;
+    if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(out, 16) || !aligned(lse, 4))
+        return MLA_ERR_INVALID;
+    if (!device_ctl()) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_combine(o_part, lse_part, S, B, H, static_cast<__nv_bfloat16*>(out),
+                                    lse, stream));
+}
+
+mla_status mla_check_status(cudaStream_t stream) {
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    DevCtl h;
+    if (cudaMemcpy(&h, ctl, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    if (h.status != 0) {
+        int32_t zero[2] = {0, 0};
+        if (cudaMemcpy(ctl, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
+    return static_cast<mla_status>(h.status);
+}
+
+const char* mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID: return "invalid argument";
+        case MLA_ERR_BOUNDS: return "index outside the cache pool";
+        case MLA_ERR_TIMEOUT: return "bounded wait ran out inside a kernel";
+        case MLA_ERR_CUDA: return "CUDA error";
+        case MLA_ERR_UNSUPPORTED: return "unsupported device or size";
+    }
+    return "unknown status";
+}
+
+mla_status mla_set_wait_limit(uint32_t iterations) {
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    uint32_t v = iterations ? iterations : kDefaultWaitLimit;
+    return from_cuda(cudaMemcpy(&ctl->wait_limit, &v, sizeof v, cudaMemcpyHostToDevice));
+}
+
+mla_status mla_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t stream) {
+    if (n < 0) return MLA_ERR_INVALID;
+    if (n == 0) return MLA_OK;
+    if (!x || !codes || !aligned(x, 4)) return MLA_ERR_INVALID;
+    if (!device_ctl()) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_e4m3_encode(x, codes, n, stream));
+}
+
+}  // extern "C"

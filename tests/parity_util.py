@@ -1,0 +1,100 @@
+"""Shared helpers of the parity tests: oracle-side set-up from the same seeded inputs, and the
+comparison bar.
+
+Tolerances (written here once, used by every decode parity test):
+  out : max |gpu - oracle| <= 1e-2 over all elements (bf16 outputs, unit-variance inputs)
+  lse : max |gpu - oracle| <= 1e-3
+  and, per (request, head), ||gpu - oracle||_2 <= 1e-2 * ||oracle||_2 so that a near-zero
+  output cannot pass the absolute bar at long context.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from mla_latent_kv_decode_gb300 import synth
+
+OUT_ABS = 1e-2
+LSE_ABS = 1e-3
+OUT_REL = 1e-2
+
+
+def oracle_pool(w: synth.Workload, upto=None):
+    """Host pool holding every request's rows at the workload's slots (small workloads only).
+    ``upto[b]`` limits request b to positions < upto[b] (default: seq_lens)."""
+    pool = oracle.new_pool(w.fmt, w.num_pages)
+    for b in range(w.B):
+        n = int(w.seq_lens[b] if upto is None else upto[b])
+        if n <= 0:
+            continue
+        c, r = synth.kv_rows(w.seed, b, 0, n)
+        bad = oracle.cache_append(w.fmt, pool, c, r, w.slots(b, 0, n))
+        assert bad == 0
+    return pool
+
+
+def request_pool(w: synth.Workload, b: int, positions=None):
+    """A one-request host pool with contiguous pages holding request b's rows (all positions
+    below seq_lens[b], or only ``positions``; the rest of the pool stays zero)."""
+    n = int(w.seq_lens[b])
+    pages = (n + 63) // 64
+    pool = oracle.new_pool(w.fmt, max(pages, 1))
+    if positions is None:
+        c, r = synth.kv_rows(w.seed, b, 0, n)
+        slot = np.arange(n, dtype=np.int32)
+    else:
+        positions = np.asarray(positions, dtype=np.int64)
+        c, r = synth.kv_rows_at(w.seed, b, positions)
+        slot = positions.astype(np.int32)
+    assert oracle.cache_append(w.fmt, pool, c, r, slot) == 0
+    bt = np.arange(max(pages, 1), dtype=np.int32)[None]
+    return pool, bt
+
+
+def oracle_decode_pairs(w: synth.Workload, pairs, nthreads=0):
+    """Oracle (out, lse) for sampled (b, h) pairs, each request rebuilt on its own pool."""
+    ql, qr = w.queries()
+    outs = np.empty((len(pairs), synth.D_C))
+    lses = np.empty(len(pairs))
+    by_b = {}
+    for i, (b, h) in enumerate(pairs):
+        by_b.setdefault(int(b), []).append((i, int(h)))
+    for b, items in by_b.items():
+        if w.topk_idx is not None:
+            idx = w.topk_idx[b]
+            vis = idx[(idx >= 0) & (idx < w.seq_lens[b])]
+            pool, bt = request_pool(w, b, np.unique(vis))
+            tk = w.topk_idx[b:b + 1]
+        else:
+            pool, bt = request_pool(w, b)
+            tk = None
+        hs = [h for _, h in items]
+        o, l, _ = oracle.mla_decode(w.fmt, pool, ql[b:b + 1], qr[b:b + 1], bt,
+                                    w.seq_lens[b:b + 1], w.scale, topk_idx=tk,
+                                    pairs=[(0, h) for h in hs], nthreads=nthreads)
+        for (i, _), oo, ll in zip(items, o, l):
+            outs[i] = oo
+            lses[i] = ll
+    return outs, lses
+
+
+def assert_decode_close(out_gpu: np.ndarray, lse_gpu: np.ndarray, out_ref: np.ndarray,
+                        lse_ref: np.ndarray, what: str = ""):
+    """out_*: [n, 512], lse_*: [n]; empty rows (lse = -inf) must be exactly zero / -inf."""
+    out_gpu = np.asarray(out_gpu, dtype=np.float64).reshape(-1, synth.D_C)
+    out_ref = np.asarray(out_ref, dtype=np.float64).reshape(-1, synth.D_C)
+    lse_gpu = np.asarray(lse_gpu, dtype=np.float64).reshape(-1)
+    lse_ref = np.asarray(lse_ref, dtype=np.float64).reshape(-1)
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse_gpu), empty), f"{what}: empty-set rows differ"
+    assert np.all(out_gpu[empty] == 0), f"{what}: empty rows not zero"
+    ne = ~empty
+    if not ne.any():
+        return
+    err = np.abs(out_gpu[ne] - out_ref[ne])
+    assert np.all(np.isfinite(out_gpu[ne])), f"{what}: non-finite outputs"
+    assert err.max() <= OUT_ABS, f"{what}: max |out err| {err.max():.3e}"
+    lerr = np.abs(lse_gpu[ne] - lse_ref[ne])
+    assert lerr.max() <= LSE_ABS, f"{what}: max |lse err| {lerr.max():.3e}"
+    rel = np.linalg.norm(out_gpu[ne] - out_ref[ne], axis=1) / np.linalg.norm(out_ref[ne], axis=1)
+    assert rel.max() <= OUT_REL, f"{what}: max normwise rel err {rel.max():.3e}"

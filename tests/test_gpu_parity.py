@@ -1,0 +1,207 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on identical seeded inputs.
+
+Bit-exact: cache bytes written by mla_cache_append (both formats) and the E4M3 conversion.
+Tolerance (tests/parity_util.py): decode outputs and log-sum-exps.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import mla_latent_kv_decode_gb300 as mla
+from mla_latent_kv_decode_gb300 import harness, synth
+from parity_util import (assert_decode_close, oracle_decode_pairs, oracle_pool)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    mla.load()
+    t.cuda.init()
+    return t
+
+
+def _custom(name, fmt, seq_lens, seed, topk_idx=None, shuffle=True, appended=0):
+    seq = np.asarray(seq_lens, dtype=np.int32)
+    pages = int(((seq.astype(np.int64) + 63) // 64).sum())
+    perm = synth.permutation(seed, synth.STREAM_PERM, pages) if shuffle else None
+    bt, total = synth._block_table(seq, perm)
+    return synth.Workload(name, fmt, len(seq), 128, seed, seq, bt, total,
+                          topk_idx=None if topk_idx is None else np.asarray(topk_idx, np.int32),
+                          appended=appended)
+
+
+def _run_full_compare(torch, w, what, replicas=1):
+    dw = harness.DeviceWorkload(w, gen="host")
+    dw.append()
+    out, lse = dw.decode()
+    assert mla.check_status() == 0
+    # cache bytes: bit-exact against the oracle's encoder on the same rows
+    ref_pool = oracle_pool(w)
+    gpu_pool = dw.pools[0].cpu().numpy()
+    assert np.array_equal(gpu_pool, ref_pool), f"{what}: pool bytes differ"
+    ql, qr = w.queries()
+    ro, rl, _ = oracle.mla_decode(w.fmt, ref_pool, ql, qr, w.block_table, w.seq_lens, w.scale,
+                                  topk_idx=w.topk_idx)
+    go = out.float().cpu().numpy().reshape(-1, 512)
+    gl = lse.cpu().numpy().reshape(-1)
+    assert_decode_close(go, gl, ro, rl, what)
+    return dw
+
+
+def test_tiny_dense_full(torch):
+    """B=1, 4,096 tokens, contiguous pages (the whole small workload, every output)."""
+    _run_full_compare(torch, synth.make_workload("tiny_dense"), "tiny_dense")
+
+
+def test_ragged_paged_batch_edges(torch):
+    """Ragged lengths around the 64-token page and tile edges, shuffled pages, one empty request."""
+    w = _custom("ragged", 0, [1, 63, 64, 65, 127, 0, 1000, 3000], seed=21)
+    _run_full_compare(torch, w, "ragged bf16")
+
+
+def test_split_kv_long_request(torch):
+    """One long request split across many work units and merged (split-KV + LSE merge)."""
+    w = _custom("long", 0, [20000], seed=22)
+    _run_full_compare(torch, w, "long bf16")
+
+
+def test_fp8_mixed_batch_with_append(torch):
+    w = _custom("fp8", 1, [300, 64, 1, 777], seed=23, appended=64)
+    _run_full_compare(torch, w, "fp8 mixed")
+
+
+def test_topk_sparse_with_padding(torch):
+    seed = 24
+    seq = [5000, 700, 4097]
+    K = 300
+    idx = np.stack([synth.sorted_distinct_sample(seed, synth.STREAM_TOPK, b, n, K)
+                    for b, n in enumerate(seq)])
+    idx[1, -20:] = -1          # padding entries
+    idx[2, -5:] = 4097 + np.arange(5)   # at/after seq_len: skipped
+    for fmt in (0, 1):
+        w = _custom(f"topk{fmt}", fmt, seq, seed=seed, topk_idx=idx)
+        _run_full_compare(torch, w, f"topk fmt={fmt}")
+
+
+def test_topk_all_padding_and_empty(torch):
+    w = _custom("topk_empty", 1, [100, 0], seed=25, topk_idx=np.full((2, 64), -1, np.int32))
+    _run_full_compare(torch, w, "topk all padding")
+
+
+def test_combine_matches_oracle(torch):
+    rng = np.random.default_rng(31)
+    S, B, H = 5, 2, 128
+    o = rng.normal(size=(S, B, H, 512)).astype(np.float32)
+    l = rng.normal(size=(S, B, H)).astype(np.float32) * 3
+    l[1, 0, :] = -np.inf            # one empty part
+    l[:, 1, 7] = -np.inf            # one all-empty row
+    out, lse = mla.combine(torch.from_numpy(o).cuda(), torch.from_numpy(l).cuda())
+    go = out.float().cpu().numpy()
+    gl = lse.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            ro, rl = oracle.combine(o[:, b, h], l[:, b, h])
+            if np.isneginf(rl):
+                assert np.isneginf(gl[b, h]) and np.all(go[b, h] == 0)
+                continue
+            assert abs(gl[b, h] - rl) <= 1e-5
+            assert np.abs(go[b, h] - ro).max() <= 1e-2 * max(1.0, np.abs(ro).max())
+
+
+def test_bounds_error_is_reported(torch):
+    w = _custom("bounds", 0, [200], seed=26)
+    dw = harness.DeviceWorkload(w, gen="host")
+    bt = dw.block_table.clone()
+    bt[0, 1] = w.num_pages + 5          # a page outside the pool
+    mla.decode(w.fmt, dw.pools[0], w.num_pages, dw.q_lat, dw.q_rope, bt, dw.seq_lens,
+               w.max_seq_len, w.scale)
+    assert mla.check_status() == 2      # MLA_ERR_BOUNDS, and cleared
+    assert mla.check_status() == 0
+    # an append slot past the pool is reported and not written
+    c, r = dw.rows(0, 0, 1)
+    before = dw.pools[0].clone()
+    mla.cache_append(w.fmt, dw.pools[0], w.num_pages, c, r,
+                     torch.tensor([w.num_pages * 64], dtype=torch.int32, device="cuda"))
+    assert mla.check_status() == 2
+    assert torch.equal(before, dw.pools[0])
+
+
+def test_generator_device_twin_is_bit_exact(torch):
+    w = synth.make_workload("paged_batch", B=2, seq_len=1200)
+    dw_host = harness.DeviceWorkload(w, gen="host")
+    dw_dev = harness.DeviceWorkload(w, gen="device")
+    assert torch.equal(dw_host.pools[0], dw_dev.pools[0])
+    c1, r1 = dw_host.rows(1, 5, 300)
+    c2, r2 = dw_dev.rows(1, 5, 300)
+    assert torch.equal(c1, c2) and torch.equal(r1, r2)
+
+
+def test_e4m3_conversion_exhaustive(torch):
+    """Every fp32 value in [-512, 512]: the device conversion equals the oracle encoder."""
+    limit = 0x44000000                     # bit pattern of 512.0
+    chunk = 1 << 27
+    nth = oracle.max_threads()
+    for sign in (0, 0x80000000):
+        for start in range(0, limit + 1, chunk):
+            end = min(limit + 1, start + chunk)
+            bits = np.arange(start, end, dtype=np.uint32) | np.uint32(sign)
+            x = bits.view(np.float32)
+            ref = oracle.e4m3_encode_array(x, nthreads=nth)
+            got = mla.e4m3_encode(torch.from_numpy(x).cuda()).cpu().numpy()
+            bad = np.nonzero(got != ref)[0]
+            assert bad.size == 0, (f"first mismatch x={x[bad[0]]!r} gpu={got[bad[0]]:#x} "
+                                   f"oracle={ref[bad[0]]:#x}")
+
+
+# --------------------------------------------------------------------------------------------
+# The five workloads at full size, in the launch configuration the benchmark times; the oracle
+# computes sampled (request, head) outputs one by one.
+# --------------------------------------------------------------------------------------------
+
+def _sampled(torch, name, pairs):
+    w = synth.make_workload(name)
+    dw = harness.DeviceWorkload(w)
+    dw.append()
+    out, lse = dw.decode()
+    assert mla.check_status() == 0
+    # sampled cache records are bit-exact against the oracle encoder
+    rng = np.random.default_rng(0)
+    pool = dw.pools[0]
+    rb = mla.record_bytes(w.fmt)
+    for b in {p[0] for p in pairs}:
+        ts = rng.integers(0, int(w.seq_lens[b]), 4)
+        c, r = synth.kv_rows_at(w.seed, b, ts)
+        ref = oracle.new_pool(w.fmt, 1)
+        oracle.cache_append(w.fmt, ref, c, r, np.arange(len(ts), dtype=np.int32))
+        for i, t in enumerate(ts):
+            s = int(w.block_table[b, t // 64]) * 64 + int(t) % 64
+            got = pool[s * rb:(s + 1) * rb].cpu().numpy()
+            assert np.array_equal(got, ref[i * rb:(i + 1) * rb]), f"{name}: record ({b},{t})"
+    ro, rl = oracle_decode_pairs(w, pairs)
+    go = np.stack([out[b, h].float().cpu().numpy() for b, h in pairs])
+    gl = np.array([float(lse[b, h]) for b, h in pairs])
+    assert_decode_close(go, gl, ro, rl, name)
+    # all outputs finite, all lse finite (every request sees positions)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_full_tiny_dense(torch):
+    _sampled(torch, "tiny_dense", [(0, 0), (0, 77), (0, 127)])
+
+
+def test_full_paged_batch(torch):
+    _sampled(torch, "paged_batch", [(0, 3), (13, 64), (31, 127), (31, 0)])
+
+
+def test_full_long_context(torch):
+    _sampled(torch, "long_context", [(0, 0), (0, 50), (0, 127)])
+
+
+def test_full_fp8_batch(torch):
+    _sampled(torch, "fp8_batch", [(0, 1), (40, 90), (63, 127)])
+
+
+def test_full_topk_sparse(torch):
+    _sampled(torch, "topk_sparse", [(0, 5), (33, 64), (63, 127)])
