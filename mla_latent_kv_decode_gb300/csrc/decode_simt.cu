@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a, int
 
 }  // namespace
 
-DecodePlan plan_decode(int fmt, int B, int max_seq_len, int topk, int sms) {
+DecodePlan plan_decode_simt(int fmt, int B, int max_seq_len, int topk, int sms) {
     (void)fmt;
     DecodePlan p;
     const int L = topk > 0 ? topk : max_seq_len;
@@ -196,7 +196,7 @@ DecodePlan plan_decode(int fmt, int B, int max_seq_len, int topk, int sms) {
     return p;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
     const int smem = (int)sizeof(SimtSmem);
     static bool attr_set[64] = {};
     int dev = 0;

@@ -29,7 +29,7 @@ struct DevCtl {
     uint32_t pad;
 };
 
-constexpr uint32_t kDefaultWaitLimit = 1u << 26;   // ~ seconds of polling, never reached normally
+constexpr uint32_t kDefaultWaitLimit = 1u << 20;   // far above any real wait; bounds a lost signal
 
 __device__ __forceinline__ void record_error(DevCtl* ctl, int code, int detail) {
     if (atomicCAS(&ctl->status, 0, code) == 0) ctl->detail = detail;
@@ -77,7 +77,19 @@ struct DecodeArgs {
     DevCtl* ctl;
 };
 
-DecodePlan plan_decode(int fmt, int B, int max_seq_len, int topk, int sms);
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+// Tensor-core path (bf16 dense) and CUDA-core path (FP8 mixed and top-k for now).
+DecodePlan plan_decode_tc(int fmt, int B, int max_seq_len, int topk, int sms);
+cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+DecodePlan plan_decode_simt(int fmt, int B, int max_seq_len, int topk, int sms);
+cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+
+inline bool use_tc(int fmt, int topk) { return fmt == MLA_KV_BF16 && topk == 0; }
+inline DecodePlan plan_decode(int fmt, int B, int max_seq_len, int topk, int sms) {
+    return use_tc(fmt, topk) ? plan_decode_tc(fmt, B, max_seq_len, topk, sms)
+                             : plan_decode_simt(fmt, B, max_seq_len, topk, sms);
+}
+inline cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+    return use_tc(a.fmt, a.topk) ? launch_decode_tc(a, p, st) : launch_decode_simt(a, p, st);
+}
 
 }  // namespace mla
