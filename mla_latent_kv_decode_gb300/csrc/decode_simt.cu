@@ -196,7 +196,12 @@ DecodePlan plan_decode_simt(int fmt, int B, int max_seq_len, int topk, int sms) 
     return p;
 }
 
-cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+cudaError_t launch_decode_simt(const DecodeArgs& args, const DecodePlan& p, cudaStream_t st) {
+    DecodeArgs a = args;
+    if (p.splits > 1) {
+        a.o_part = static_cast<float*>(a.workspace);
+        a.lse_part = a.o_part + (size_t)p.splits * a.B * kHeads * kDc;
+    }
     const int smem = (int)sizeof(SimtSmem);
     static bool attr_set[64] = {};
     int dev = 0;

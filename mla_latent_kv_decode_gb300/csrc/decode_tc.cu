@@ -9,18 +9,29 @@
 // V = the first 512 columns of the same rows.
 //
 // Capacity drives the design.  O (128 x 512 fp32) fills all 512 columns of one SM's tensor memory
-// and Q (128 x 576 bf16, 144 KB) most of its shared memory, so one work unit runs on a cluster of
-// two CTAs, r = 0, 1.  CTA r owns latent dims [256 r, 256 r + 256) and rope dims [32 r, 32 r + 32):
+// and Q (128 x 576 bf16, 144 KB) most of its shared memory, so the work runs on clusters of two
+// CTAs, r = 0, 1.  CTA r owns latent dims [256 r, 256 r + 256) and rope dims [32 r, 32 r + 32):
 //   * it streams only its 288 columns of every cached row (576 B per position) through a
 //     5-stage TMA ring, and holds only its half of Q (72 KB);
 //   * S_r = Q_r K_r^T is a partial score over its 288 dims (18 MMAs of 128x32x16 per tile);
 //   * the 128 softmax threads (one per head) send S_r to the peer CTA through distributed shared
-//     memory (st.async, 16 KB per tile), add the peer's part: both CTAs then hold the same fp32
-//     scores, bit for bit, and take identical softmax decisions;
+//     memory (st.async, 16 KB per tile) and add the peer's part: both CTAs then hold the same
+//     fp32 scores, bit for bit, and take identical softmax decisions;
 //   * P (bf16) goes to shared memory and O_r[128 x 256] += P V_r (2 MMAs of 128x256x16), V_r being
 //     the latent half already in the stage: nothing is loaded twice and no FLOP is repeated.
 // The online softmax runs in the log2 domain with a lazily updated running max (O is rescaled only
 // when a row max grows by more than 2^8), so the common tile never touches O.
+//
+// Scheduling: the grid is a fixed set of C clusters (at most one per SM pair).  The tiles of all
+// requests form one stream of W tiles; cluster c takes tiles [c W / C, (c + 1) W / C), so every
+// cluster gets the same work whatever the length mix.  A cluster walks its range request by
+// request ("segments"); a segment that covers a whole request writes the final output, one cut
+// by a range boundary writes a partial (normalised output + lse) into slot 2c (the range's first
+// segment) or 2c + 1 (its last), and a small merge kernel combines the partials of cut requests.
+//
+// Pipelining: QK runs two tiles ahead of PV (3 score buffers in TMEM), the softmax threads read and
+// send the scores of tile i + 1 before they finish tile i (hiding the exchange latency), and the
+// next request's Q is loaded as soon as the last QK of the previous one has completed.
 //
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner), warps 2-5
 // softmax / exchange / epilogue (thread = head = TMEM lane).  Every wait is bounded: on expiry the
@@ -38,13 +49,16 @@ using namespace ptx;
 
 constexpr int kT = 32;                 // positions per tile
 constexpr int kNS = 5;                 // KV ring stages
+constexpr int kNSB = 3;                // score buffers in TMEM
+constexpr int kQKAhead = 2;            // QK of tile i + 2 may run before PV of tile i
 constexpr int kThreads = 192;
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256)
-constexpr uint32_t kTmemS = 256;       // S buffers: [256 + 32 k, 256 + 32 k + 32), k = 0, 1
+constexpr uint32_t kTmemS = 256;       // score buffer k: columns [256 + 32 k, 288 + 32 k)
 constexpr uint32_t kDrainLimit = 1u << 20;
+constexpr int kMinTilesPerCluster = 8;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] bf16, SW128
@@ -60,8 +74,9 @@ constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 73728
 constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 165888
 constexpr int kOffP = kOffX + 2 * kXBytes;             // 198656
 constexpr int kOffBar = kOffP + 2 * kPBytes;           // 215040
-constexpr int kNumBars = 2 * kNS + 2 + 2 * 6;
-constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 64 + 1024;   // + alignment slack
+constexpr int kNumBars = 2 * kNS + 2 * kNSB + 13;
+constexpr int kOffSched = kOffBar + 8 * kNumBars;      // scan scratch: kThreads int32
+constexpr int kSmemBytes = kOffSched + 4 * kThreads + 64 + 1024;   // + alignment slack
 
 constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;       // 73728 per CTA
 
@@ -70,36 +85,47 @@ struct TcParams {
     const int32_t* seq_lens;
     __nv_bfloat16* out;
     float* lse;
-    float* o_part;
-    float* lse_part;
+    float* o_part;          // [2C][128][512]
+    float* lse_part;        // [2C][128]
+    int32_t* meta;          // tile_start[B], then W
     DevCtl* ctl;
     int64_t num_pages;
     int max_pages;
     int max_seq_len;
     int B;
-    int chunk;
-    int splits;
-    float scale_log2;     // scale * log2(e)
+    float scale_log2;       // scale * log2(e)
 };
 
 struct Bars {
-    uint32_t kv_full[kNS], kv_empty[kNS], q_full, mma_drain;
-    uint32_t s_full[2], s_empty[2], p_full[2], p_empty[2], x_full[2], x_free[2];
+    uint32_t kv_full, kv_empty;   // arrays of kNS
+    uint32_t s_full, s_empty;     // arrays of kNSB
+    uint32_t p_full, p_empty, x_full, x_free;   // arrays of 2
+    uint32_t q_full, q_empty, o_full, o_free, mma_drain;
+    __device__ __forceinline__ uint32_t kvf(int i) const { return kv_full + 8 * i; }
+    __device__ __forceinline__ uint32_t kve(int i) const { return kv_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t sf(int i) const { return s_full + 8 * i; }
+    __device__ __forceinline__ uint32_t se(int i) const { return s_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t pf(int i) const { return p_full + 8 * i; }
+    __device__ __forceinline__ uint32_t pe(int i) const { return p_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
+    __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
 };
 
-__device__ __forceinline__ Bars make_bars(uint32_t base) {
+__device__ __forceinline__ Bars make_bars(uint32_t a) {
     Bars b;
-    uint32_t a = base;
-    for (int i = 0; i < kNS; ++i) b.kv_full[i] = a, a += 8;
-    for (int i = 0; i < kNS; ++i) b.kv_empty[i] = a, a += 8;
-    b.q_full = a, a += 8;
-    b.mma_drain = a, a += 8;
-    for (int i = 0; i < 2; ++i) b.s_full[i] = a, a += 8;
-    for (int i = 0; i < 2; ++i) b.s_empty[i] = a, a += 8;
-    for (int i = 0; i < 2; ++i) b.p_full[i] = a, a += 8;
-    for (int i = 0; i < 2; ++i) b.p_empty[i] = a, a += 8;
-    for (int i = 0; i < 2; ++i) b.x_full[i] = a, a += 8;
-    for (int i = 0; i < 2; ++i) b.x_free[i] = a, a += 8;
+    b.kv_full = a; a += 8 * kNS;
+    b.kv_empty = a; a += 8 * kNS;
+    b.s_full = a; a += 8 * kNSB;
+    b.s_empty = a; a += 8 * kNSB;
+    b.p_full = a; a += 16;
+    b.p_empty = a; a += 16;
+    b.x_full = a; a += 16;
+    b.x_free = a; a += 16;
+    b.q_full = a; a += 8;
+    b.q_empty = a; a += 8;
+    b.o_full = a; a += 8;
+    b.o_free = a; a += 8;
+    b.mma_drain = a; a += 8;
     return b;
 }
 
@@ -113,6 +139,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ int clamp_len(int n, int max_len) {
+    return n < 0 ? 0 : (n > max_len ? max_len : n);
+}
+
+// Walks the tiles of one cluster's range: request b, tile t of that request (nt tiles in all).
+struct Cursor {
+    const int32_t* seq_lens;
+    int max_len, B;
+    int b, t, nt, n;         // n = visible positions of request b
+    long long g, g_end;      // global tile index, end of range
+    __device__ __forceinline__ void load_req() {
+        n = clamp_len(seq_lens[b], max_len);
+        nt = (n + kT - 1) / kT;
+    }
+    __device__ __forceinline__ void init(const int32_t* sl, int ml, int B_, int b0, int t0,
+                                         long long g0, long long g1) {
+        seq_lens = sl, max_len = ml, B = B_, b = b0, t = t0, g = g0, g_end = g1;
+        if (g < g_end) load_req();
+        else n = nt = 0;
+    }
+    __device__ __forceinline__ bool first(long long g_begin) const { return t == 0 || g == g_begin; }
+    __device__ __forceinline__ bool last() const { return t == nt - 1 || g == g_end - 1; }
+    __device__ __forceinline__ void next() {
+        ++g;
+        ++t;
+        if (g >= g_end) return;
+        while (t >= nt && b + 1 < B) {
+            ++b;
+            t = 0;
+            load_req();
+        }
+    }
+};
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                      const __grid_constant__ CUtensorMap tm_qrope,
@@ -123,44 +183,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
     __shared__ uint32_t s_tmem_base;
     __shared__ volatile int s_abort;
+    __shared__ int s_start_b, s_start_t;
+    __shared__ long long s_W;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t r = cluster_rank();
     const uint32_t peer = r ^ 1u;
-    const int unit = blockIdx.x >> 1;
-    const int b = unit / p.splits;
-    const int split = unit % p.splits;
+    const int c = blockIdx.x >> 1;
+    const int C = gridDim.x >> 1;
     const uint32_t wait_limit = p.ctl->wait_limit;
 
     const uint32_t sbase = smem_u32(sm);
     const Bars bars = make_bars(sbase + kOffBar);
+    int* scan = reinterpret_cast<int*>(sm + kOffSched);
 
-    int n_b = p.seq_lens[b];
-    if (n_b < 0 || n_b > p.max_seq_len) {
-        if (tid == 0 && r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, b);
-        n_b = n_b < 0 ? 0 : p.max_seq_len;
+    // ---- schedule: W = sum_b ceil(n_b / 32); this cluster's tiles [g_begin, g_end) ----
+    const int per = (p.B + kThreads - 1) / kThreads;
+    const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+    int my_tiles = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int raw = p.seq_lens[b];
+        if ((raw < 0 || raw > p.max_seq_len) && r == 0 && c == 0) record_error(p.ctl, MLA_ERR_BOUNDS, b);
+        my_tiles += (clamp_len(raw, p.max_seq_len) + kT - 1) / kT;
     }
-    const int e0 = split * p.chunk;
-    const int e1 = min(n_b, e0 + p.chunk);
-    const int n_tiles = e1 > e0 ? (e1 - e0 + kT - 1) / kT : 0;
-
+    scan[tid] = my_tiles;
     if (tid == 0) {
         s_abort = 0;
+        s_start_b = p.B;
+        s_start_t = 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long acc = 0;
+        for (int i = 0; i < kThreads; ++i) {
+            const int v = scan[i];
+            scan[i] = (int)acc;
+            acc += v;
+        }
+        s_W = acc;
+    }
+    __syncthreads();
+    const long long W = s_W;
+    const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
+    {
+        long long pre = scan[tid];
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int nt = (clamp_len(p.seq_lens[b], p.max_seq_len) + kT - 1) / kT;
+            if (c == 0 && r == 0) p.meta[b] = (int)pre;
+            if (g_begin < g_end && g_begin >= pre && g_begin < pre + nt) {
+                s_start_b = b;
+                s_start_t = (int)(g_begin - pre);
+            }
+            pre += nt;
+        }
+        if (c == 0 && r == 0 && tid == kThreads - 1) p.meta[p.B] = (int)W;
+    }
+
+    if (tid == 0) {
         for (int i = 0; i < kNS; ++i) {
-            mbar_init(bars.kv_full[i], 1);
-            mbar_init(bars.kv_empty[i], 1);
+            mbar_init(bars.kvf(i), 1);
+            mbar_init(bars.kve(i), 1);
+        }
+        for (int i = 0; i < kNSB; ++i) {
+            mbar_init(bars.sf(i), 1);
+            mbar_init(bars.se(i), 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.pf(i), 128);
+            mbar_init(bars.pe(i), 1);
+            mbar_init(bars.xf(i), 1);
+            mbar_init(bars.xe(i), 4);   // one remote arrive per peer softmax warp
         }
         mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        mbar_init(bars.o_full, 1);
+        mbar_init(bars.o_free, 128);
         mbar_init(bars.mma_drain, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bars.s_full[i], 1);
-            mbar_init(bars.s_empty[i], 128);
-            mbar_init(bars.p_full[i], 128);
-            mbar_init(bars.p_empty[i], 1);
-            mbar_init(bars.x_full[i], 1);
-            mbar_init(bars.x_free[i], 4);   // one remote arrive per peer softmax warp
-        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -172,102 +271,134 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the peer's barriers are initialised before any remote arrive / st.async
     const uint32_t tmem = s_tmem_base;
+    const int n_local = (int)(g_end - g_begin);   // tiles of this cluster
+    const int start_b = s_start_b, start_t = s_start_t;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && n_local > 0) {
             tma_prefetch_desc(&tm_qlat);
             tma_prefetch_desc(&tm_qrope);
             tma_prefetch_desc(&tm_kv_lat);
             tma_prefetch_desc(&tm_kv_rope);
-            const int qrow = b * kHeads;
-            mbar_arrive_expect_tx(bars.q_full, kQBytes);
-            for (int k = 0; k < 4; ++k)
-                tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
-                            (int)r * kHalfLat + 64 * k, qrow);
-            tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
+            Cursor cu;
+            cu.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
+            int seg = 0, issued = 0;
+            for (int i = 0; i < n_local; ++i, cu.next()) {
                 if (s_abort) break;
-                const int s = j % kNS;
-                if (!mbar_wait(bars.kv_empty[s], ((j / kNS) & 1) ^ 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 1);
+                if (cu.first(g_begin)) {
+                    if (seg > 0 && !mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit)) {
+                        fail(p.ctl, &s_abort, 1);
+                        break;
+                    }
+                    const int qrow = cu.b * kHeads;
+                    mbar_arrive_expect_tx(bars.q_full, kQBytes);
+                    for (int k = 0; k < 4; ++k)
+                        tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
+                                    (int)r * kHalfLat + 64 * k, qrow);
+                    tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
+                    ++seg;
+                }
+                const int s = i % kNS;
+                if (!mbar_wait(bars.kve(s), ((i / kNS) & 1) ^ 1, wait_limit)) {
+                    fail(p.ctl, &s_abort, 2);
                     break;
                 }
-                const int pos0 = e0 + j * kT;
-                const int page = p.block_table[(size_t)b * p.max_pages + pos0 / kPage];
+                const int pos0 = cu.t * kT;
+                const int page = p.block_table[(size_t)cu.b * p.max_pages + pos0 / kPage];
                 int row = -2 * kPage;   // outside the pool: the tile reads as zeros
                 if (page >= 0 && page < p.num_pages) row = page * kPage + pos0 % kPage;
                 else if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
                 const uint32_t st = sbase + kOffKv + s * kStageBytes;
-                mbar_arrive_expect_tx(bars.kv_full[s], kStageBytes);
+                mbar_arrive_expect_tx(bars.kvf(s), kStageBytes);
                 for (int k = 0; k < 4; ++k)
-                    tma_load_2d(st + k * kKvLatChunk, &tm_kv_lat, bars.kv_full[s],
+                    tma_load_2d(st + k * kKvLatChunk, &tm_kv_lat, bars.kvf(s),
                                 (int)r * kHalfLat + 64 * k, row);
-                tma_load_2d(st + 4 * kKvLatChunk, &tm_kv_rope, bars.kv_full[s],
-                            kDc + (int)r * kHalfRope, row);
-                issued = j + 1;
+                tma_load_2d(st + 4 * kKvLatChunk, &tm_kv_rope, bars.kvf(s), kDc + (int)r * kHalfRope,
+                            row);
+                issued = i + 1;
             }
-            // drain: the last (up to kNS) loads must land before this CTA may exit
+            // drain: every load issued lands before this CTA may exit
             for (int j = max(0, issued - kNS); j < issued; ++j)
-                mbar_wait(bars.kv_full[j % kNS], (j / kNS) & 1, kDrainLimit);
-            if (!mbar_wait(bars.q_full, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 9);
+                mbar_wait(bars.kvf(j % kNS), (j / kNS) & 1, kDrainLimit);
+            if (seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && n_local > 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, kT, 0, 0);
             constexpr uint32_t id_pv = idesc_bf16(128, kHalfLat, 0, 1);
             const uint32_t q_lat = sbase + kOffQ, q_rope = sbase + kOffQRope;
-            bool ok = mbar_wait(bars.q_full, 0, wait_limit);
-            if (!ok) fail(p.ctl, &s_abort, 2);
-            auto issue_pv = [&](int i) -> bool {
-                const int pb = i & 1;
-                if (!mbar_wait(bars.p_full[pb], (i >> 1) & 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 3);
-                    return false;
+            Cursor cq, cp;
+            cq.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
+            cp = cq;
+            int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
+            uint32_t polls = 0;
+            // Poll both queues: issue the next QK (up to kQKAhead tiles ahead of PV) when its
+            // inputs are ready, else the next PV when its P is ready, so that neither a late KV
+            // stage nor the next request's Q can hold back a PV.
+            while (ip < n_local && !s_abort) {
+                if (iq < n_local && iq <= ip + kQKAhead) {
+                    const int s = iq % kNS, sb = iq % kNSB;
+                    const bool ready = (!cq.first(g_begin) || mbar_try_wait(bars.q_full, seg_q & 1)) &&
+                                       mbar_try_wait(bars.kvf(s), (iq / kNS) & 1) &&
+                                       mbar_try_wait(bars.se(sb), ((iq / kNSB) & 1) ^ 1);
+                    if (ready) {
+                    tc_fence_after();
+                    const uint32_t st = sbase + kOffKv + s * kStageBytes;
+                    const uint32_t d = tmem + kTmemS + sb * kT;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(d, smem_desc(q_lat + k * kQLatChunk + kk * 32, 16, 1024, kSw128),
+                                        smem_desc(st + k * kKvLatChunk + kk * 32, 16, 1024, kSw128),
+                                        id_qk, (k | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_bf16_ss(d, smem_desc(q_rope + kk * 32, 16, 512, kSw64),
+                                    smem_desc(st + 4 * kKvLatChunk + kk * 32, 16, 512, kSw64), id_qk, 1u);
+                    mma_commit(bars.sf(sb));
+                    if (cq.last()) {
+                        mma_commit(bars.q_empty);
+                        ++seg_q;
+                    }
+                    cq.next();
+                    ++iq;
+                    polls = 0;
+                    continue;
+                    }
                 }
+                // PV of tile ip
+                const bool seg_first = cp.first(g_begin);
+                const int pb = ip & 1;
+                const bool pv_ready = (!seg_first || seg_p == 0 || mbar_try_wait(bars.o_free, (seg_p - 1) & 1)) &&
+                                      mbar_try_wait(bars.pf(pb), (ip >> 1) & 1);
+                if (!pv_ready) {
+                    if (++polls > wait_limit) {
+                        fail(p.ctl, &s_abort, 6);
+                        break;
+                    }
+                    continue;
+                }
+                polls = 0;
                 tc_fence_after();
                 const uint32_t pa = sbase + kOffP + pb * kPBytes;
-                const uint32_t v = sbase + kOffKv + (i % kNS) * kStageBytes;
+                const uint32_t v = sbase + kOffKv + (ip % kNS) * kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
                     mma_bf16_ss(tmem + kTmemO, smem_desc(pa + kk * 32, 16, 512, kSw64),
                                 smem_desc(v + kk * 16 * 128, kKvLatChunk, 1024, kSw128), id_pv,
-                                (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bars.p_empty[pb]);
-                mma_commit(bars.kv_empty[i % kNS]);
-                return true;
-            };
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (s_abort) break;
-                const int s = j % kNS, sb = j & 1;
-                if (!mbar_wait(bars.kv_full[s], (j / kNS) & 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 4);
-                    break;
+                                (!seg_first || kk > 0) ? 1u : 0u);
+                mma_commit(bars.pe(pb));
+                mma_commit(bars.kve(ip % kNS));
+                if (cp.last()) {
+                    mma_commit(bars.o_full);
+                    ++seg_p;
                 }
-                if (j >= 2 && !mbar_wait(bars.s_empty[sb], ((j >> 1) & 1) ^ 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 5);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t st = sbase + kOffKv + s * kStageBytes;
-                const uint32_t d = tmem + kTmemS + sb * kT;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(d, smem_desc(q_lat + k * kQLatChunk + kk * 32, 16, 1024, kSw128),
-                                    smem_desc(st + k * kKvLatChunk + kk * 32, 16, 1024, kSw128),
-                                    id_qk, (k | kk) != 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_bf16_ss(d, smem_desc(q_rope + kk * 32, 16, 512, kSw64),
-                                smem_desc(st + 4 * kKvLatChunk + kk * 32, 16, 512, kSw64), id_qk, 1u);
-                mma_commit(bars.s_full[sb]);
-                if (j >= 1 && !issue_pv(j - 1)) break;
-                if (j == n_tiles - 1) issue_pv(j);
+                cp.next();
+                ++ip;
             }
         }
         __syncwarp();
@@ -276,19 +407,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int lg = warp & 3;                 // TMEM lane group this warp may access
         const int h = lg * 32 + lane;            // head = TMEM lane
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-        const uint32_t x_local = sbase + kOffX;
-        const uint32_t x_remote = mapa(x_local, peer);
-        const uint32_t xfull_remote[2] = {mapa(bars.x_full[0], peer), mapa(bars.x_full[1], peer)};
-        const uint32_t xfree_remote[2] = {mapa(bars.x_free[0], peer), mapa(bars.x_free[1], peer)};
+        const uint32_t x_remote = mapa(sbase + kOffX, peer);
+        const uint32_t xfull_remote = mapa(bars.x_full, peer);
+        const uint32_t xfree_remote = mapa(bars.x_free, peer);
         const bool leader = (tid == 64);
         float m_used = -INFINITY, l_run = 0.f;
         float s_own[kT], s_next[kT];
 
-        // read S_j of this CTA from TMEM and send it to the peer
-        auto load_and_send = [&](int j, float (&dst)[kT]) -> bool {
-            const int sb = j & 1;
-            if (!mbar_wait(bars.s_full[sb], (j >> 1) & 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 6);
+        // read this CTA's partial scores of local tile i from TMEM and send them to the peer
+        auto load_and_send = [&](int i, float (&dst)[kT]) -> bool {
+            const int sb = i % kNSB, xb = i & 1;
+            if (!mbar_wait(bars.sf(sb), (i / kNSB) & 1, wait_limit)) {
+                fail(p.ctl, &s_abort, 7);
                 return false;
             }
             tc_fence_after();
@@ -296,34 +426,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + lane_off + kTmemS + sb * kT, v);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(bars.s_empty[sb]);
+            mbar_arrive(bars.se(sb));
 #pragma unroll
             for (int t = 0; t < kT; ++t) dst[t] = __uint_as_float(v[t]);
-            if (!mbar_wait(bars.x_free[sb], ((j >> 1) & 1) ^ 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 7);
+            if (!mbar_wait(bars.xe(xb), ((i >> 1) & 1) ^ 1, wait_limit)) {
+                fail(p.ctl, &s_abort, 8);
                 return false;
             }
 #pragma unroll
             for (int g = 0; g < kT / 4; ++g)
-                st_async_v4(x_remote + sb * kXBytes + (g * 128 + h) * 16, xfull_remote[sb],
+                st_async_v4(x_remote + xb * kXBytes + (g * 128 + h) * 16, xfull_remote + 8 * xb,
                             v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
             return true;
         };
 
+        Cursor cu;
+        cu.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
+        int seg = 0;
+        bool cut_front = false;
         bool ok = true;
-        if (n_tiles > 0) ok = load_and_send(0, s_own);
-        for (int j = 0; ok && j < n_tiles; ++j) {
+        if (n_local > 0) ok = load_and_send(0, s_own);
+        for (int i = 0; ok && i < n_local; ++i, cu.next()) {
             if (s_abort) break;
-            const int sb = j & 1;
-            if (j + 1 < n_tiles && !load_and_send(j + 1, s_next)) break;
-            // peer's partial scores of tile j
-            if (leader) mbar_arrive_expect_tx(bars.x_full[sb], kXBytes);
-            if (!mbar_wait(bars.x_full[sb], (j >> 1) & 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 8);
+            const int xb = i & 1, pb = i & 1;
+            // send the next tile's scores early (hides the exchange latency), except across a
+            // request boundary where the next QK waits for the next request's Q
+            const bool send_early = i + 1 < n_local && !cu.last();
+            if (send_early && !load_and_send(i + 1, s_next)) break;
+            const bool first = cu.first(g_begin);
+            if (first) {
+                m_used = -INFINITY;
+                l_run = 0.f;
+                cut_front = cu.t > 0;   // the request started before this cluster's range
+            }
+            // peer's partial scores of tile i
+            if (leader) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
+            if (!mbar_wait(bars.xf(xb), (i >> 1) & 1, wait_limit)) {
+                fail(p.ctl, &s_abort, 9);
                 break;
             }
             float x[kT];
-            const uint8_t* xp = sm + kOffX + sb * kXBytes;
+            const uint8_t* xp = sm + kOffX + xb * kXBytes;
 #pragma unroll
             for (int g = 0; g < kT / 4; ++g) {
                 const float4 q = *reinterpret_cast<const float4*>(xp + (g * 128 + h) * 16);
@@ -333,13 +476,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 x[4 * g + 3] = s_own[4 * g + 3] + q.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(xfree_remote[sb]);
+            if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * xb);
 
             // visibility of the tile's positions
-            const int pos0 = e0 + j * kT;
-            const int page = p.block_table[(size_t)b * p.max_pages + pos0 / kPage];
+            const int pos0 = cu.t * kT;
+            const int page = p.block_table[(size_t)cu.b * p.max_pages + pos0 / kPage];
             const bool page_ok = page >= 0 && page < p.num_pages;
-            const int nvalid = page_ok ? min(kT, e1 - pos0) : 0;
+            const int nvalid = page_ok ? min(kT, cu.n - pos0) : 0;
             float mt = -INFINITY;
 #pragma unroll
             for (int t = 0; t < kT; ++t) {
@@ -349,26 +492,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // lazy running max: rescale O only when the row max grows by more than 2^8
             const bool need = mt > m_used + 8.0f;
             const float m_new = need ? mt : m_used;
-            if (__any_sync(0xffffffffu, need) && j > 0) {
-                if (!mbar_wait(bars.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, wait_limit)) {
+            if (!first && __any_sync(0xffffffffu, need)) {
+                if (!mbar_wait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, wait_limit)) {
                     fail(p.ctl, &s_abort, 10);
                     break;
                 }
                 tc_fence_after();
                 const float alpha = need ? exp2f(m_used - m_new) : 1.0f;
 #pragma unroll 1
-                for (int c = 0; c < kHalfLat / 32; ++c) {
+                for (int cc = 0; cc < kHalfLat / 32; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + kTmemO + 32 * c, o);
+                    tmem_ld32(tmem + lane_off + kTmemO + 32 * cc, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tmem + lane_off + kTmemO + 32 * c, o);
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st32(tmem + lane_off + kTmemO + 32 * cc, o);
                 }
                 tmem_wait_st();
                 l_run *= alpha;
-            } else if (need) {
-                l_run = 0.f;    // first tile: nothing accumulated yet
             }
             m_used = m_new;
             float psum = 0.f;
@@ -381,81 +522,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pk[t / 2] = pack_bf16x2(p0, p1);
             }
             l_run += psum;
-            // positions past the end of the unit in a live page: zero their V rows so that
+            // positions past the end of the request in a live page: zero their V rows so that
             // 0 * (stale bytes) cannot poison O
             if (page_ok && nvalid < kT) {
-                uint8_t* st = sm + kOffKv + (j % kNS) * kStageBytes;
+                uint8_t* st = sm + kOffKv + (i % kNS) * kStageBytes;
                 const int nrows = kT - nvalid;
-                for (int i = tid - 64; i < nrows * 4 * 8; i += 128) {
-                    const int row = nvalid + i / 32, k = (i / 8) % 4, part = i % 8;
+                for (int e = tid - 64; e < nrows * 4 * 8; e += 128) {
+                    const int row = nvalid + e / 32, k = (e / 8) % 4, part = e % 8;
                     *reinterpret_cast<uint4*>(st + k * kKvLatChunk + row * 128 + part * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
             }
-            // P row h (64 bytes) into the SW64 K-major buffer once PV_{j-2} has released it
-            if (j >= 2 && !mbar_wait(bars.p_empty[sb], ((j - 2) >> 1) & 1, wait_limit)) {
+            // P row h (64 bytes) into the SW64 K-major buffer once PV of tile i - 2 released it
+            if (i >= 2 && !mbar_wait(bars.pe(pb), ((i - 2) >> 1) & 1, wait_limit)) {
                 fail(p.ctl, &s_abort, 11);
                 break;
             }
-            uint8_t* pbuf = sm + kOffP + sb * kPBytes;
+            uint8_t* pbuf = sm + kOffP + pb * kPBytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int pc = c ^ ((h >> 1) & 3);
+            for (int cc = 0; cc < 4; ++cc) {
+                const int pc = cc ^ ((h >> 1) & 3);
                 *reinterpret_cast<uint4*>(pbuf + h * 64 + pc * 16) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bars.p_full[sb]);
+            mbar_arrive(bars.pf(pb));
+
+            if (cu.last()) {
+                // ------------------------------------------------------ segment epilogue
+                const bool partial = cut_front || cu.t < cu.nt - 1;
+                const int slot = 2 * c + (seg == 0 ? 0 : 1);
+                if (!mbar_wait(bars.o_full, seg & 1, wait_limit)) {
+                    fail(p.ctl, &s_abort, 12);
+                    break;
+                }
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.0f / l_run : 0.0f;
+                const float L = l_run > 0.f ? (m_used + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+                const size_t row = (size_t)cu.b * kHeads + h;
+#pragma unroll 1
+                for (int cc = 0; cc < kHalfLat / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + kTmemO + 32 * cc, o);
+                    tmem_wait_ld();
+                    const int col = (int)r * kHalfLat + 32 * cc;
+                    if (!partial) {
+                        uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(
+                                pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                                 __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                    }
+                }
+                if (r == 0) {
+                    if (!partial) p.lse[row] = L;
+                    else p.lse_part[(size_t)slot * kHeads + h] = L;
+                }
+                tc_fence_before();
+                mbar_arrive(bars.o_free);
+                ++seg;
+            }
+            if (i + 1 < n_local && !send_early && !load_and_send(i + 1, s_next)) break;
 #pragma unroll
             for (int t = 0; t < kT; ++t) s_own[t] = s_next[t];
-        }
-
-        // ---------------------------------------------------------------- epilogue
-        if (n_tiles > 0 && !s_abort) {
-            const int jl = n_tiles - 1;
-            if (!mbar_wait(bars.p_empty[jl & 1], (jl >> 1) & 1, wait_limit)) fail(p.ctl, &s_abort, 12);
-            tc_fence_after();
-        }
-        const float inv = l_run > 0.f ? 1.0f / l_run : 0.0f;
-        const float L = l_run > 0.f ? (m_used + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-        const size_t row = (size_t)b * kHeads + h;
-        const size_t BH = (size_t)p.B * kHeads;
-#pragma unroll 1
-        for (int c = 0; c < kHalfLat / 32; ++c) {
-            uint32_t o[32];
-            if (n_tiles > 0 && !s_abort) {
-                tmem_ld32(tmem + lane_off + kTmemO + 32 * c, o);
-                tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0u;
-            }
-            const int col = (int)r * kHalfLat + 32 * c;
-            if (p.splits == 1) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
-                                        pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
-                                        pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
-                                        pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
-            } else {
-                float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)split * BH + row) * kDc + col);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                         __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-            }
-        }
-        if (r == 0) {
-            if (p.splits == 1) p.lse[row] = L;
-            else p.lse_part[(size_t)split * BH + row] = L;
         }
     }
 
     // ---------------------------------------------------------------------- teardown
-    if (warp == 1 && lane == 0 && n_tiles > 0) {
+    if (warp == 1 && lane == 0 && n_local > 0) {
         // all MMAs issued by this thread are complete once this barrier flips
         mma_commit(bars.mma_drain);
         if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 13);
@@ -467,6 +611,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the peer no longer writes into this CTA's shared memory
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Merge of the partials of requests cut by cluster range boundaries.  Block (request b, head h);
+// a request that lies inside one range was finished by the decode kernel and is skipped.  The
+// partial of request b made by cluster c sits in slot 2c when b reaches back to c's range start,
+// else (b starts inside c's range and runs past its end) in slot 2c + 1.
+__global__ void __launch_bounds__(128) merge_slots_kernel(const float* __restrict__ o_part,
+                                                          const float* __restrict__ lse_part,
+                                                          const int32_t* __restrict__ meta, int B, int C,
+                                                          __nv_bfloat16* __restrict__ out,
+                                                          float* __restrict__ lse) {
+    const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
+    const long long W = meta[B];
+    const long long T0 = meta[b], T1 = (b + 1 < B) ? meta[b + 1] : W;
+    if (T1 <= T0 || W <= 0) return;   // no tiles: the decode kernel wrote nothing to merge
+    int c_lo = (int)((T0 * C) / W);
+    while (c_lo > 0 && (long long)c_lo * W / C > T0) --c_lo;
+    while (c_lo + 1 < C && (long long)(c_lo + 1) * W / C <= T0) ++c_lo;
+    int c_hi = c_lo;
+    while (c_hi + 1 < C && (long long)(c_hi + 1) * W / C < T1) ++c_hi;
+    if (c_hi == c_lo && (long long)c_lo * W / C <= T0) {
+        // the whole request lies in one range unless that range begins inside it (cut at front)
+        return;
+    }
+    float m = -INFINITY;
+    for (int cc = c_lo; cc <= c_hi; ++cc) {
+        const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
+        if (re <= rb) continue;
+        const int slot = 2 * cc + (T0 <= rb ? 0 : 1);
+        m = fmaxf(m, lse_part[(size_t)slot * kHeads + h]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = -INFINITY;
+    if (m != -INFINITY) {
+        float l = 0.f;
+        for (int cc = c_lo; cc <= c_hi; ++cc) {
+            const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
+            if (re <= rb) continue;
+            const int slot = 2 * cc + (T0 <= rb ? 0 : 1);
+            l += expf(lse_part[(size_t)slot * kHeads + h] - m);
+        }
+        L = m + logf(l);
+        for (int cc = c_lo; cc <= c_hi; ++cc) {
+            const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
+            if (re <= rb) continue;
+            const int slot = 2 * cc + (T0 <= rb ? 0 : 1);
+            const float w = expf(lse_part[(size_t)slot * kHeads + h] - L);
+            if (w == 0.f) continue;
+            const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)slot * kHeads + h) * kDc)[threadIdx.x];
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
+        }
+    }
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x, acc.y);
+    packed.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc)[threadIdx.x] = packed;
+    if (threadIdx.x == 0) lse[(size_t)b * kHeads + h] = L;
+}
+
+// Requests with no visible position get zeros and lse = -inf (they own no tiles).
+__global__ void __launch_bounds__(128) empty_rows_kernel(const int32_t* __restrict__ seq_lens,
+                                                         int max_len, __nv_bfloat16* __restrict__ out,
+                                                         float* __restrict__ lse) {
+    const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
+    if (clamp_len(seq_lens[b], max_len) > 0) return;
+    reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc)[threadIdx.x] = make_uint2(0u, 0u);
+    if (threadIdx.x == 0) lse[(size_t)b * kHeads + h] = -INFINITY;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -494,28 +708,28 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int clusters_for(int B, int max_seq_len, int sms) {
+    const long long w_max = (long long)B * ((max_seq_len + kT - 1) / kT);
+    long long c = sms / 2;
+    const long long by_work = (w_max + kMinTilesPerCluster - 1) / kMinTilesPerCluster;
+    if (by_work < c) c = by_work;
+    return c < 1 ? 1 : (int)c;
+}
+
 }  // namespace
 
-// Split plan of the tensor-core path: a work unit is (request, chunk of positions) and runs on
-// one 2-CTA cluster; units per request are chosen so that the grid fills the SM pairs.
+// Workspace of the tensor-core path: 2 partial slots per cluster (fp32 [128][512] + lse [128]),
+// then the tile offsets of the requests and the tile total (int32 [B + 1]).
 DecodePlan plan_decode_tc(int fmt, int B, int max_seq_len, int topk, int sms) {
     (void)fmt;
+    (void)topk;
     DecodePlan p;
-    const int L = topk > 0 ? topk : max_seq_len;
-    const int pairs = sms / 2 > 0 ? sms / 2 : 1;
-    int S = (pairs + B - 1) / B;
-    const int max_s = (L + 63) / 64;
-    if (S > max_s) S = max_s;
-    if (S < 1) S = 1;
-    int chunk = (L + S - 1) / S;
-    chunk = (chunk + 63) / 64 * 64;
-    if (chunk < 64) chunk = 64;
-    S = (L + chunk - 1) / chunk;
-    if (S < 1) S = 1;
-    p.splits = S;
-    p.chunk = chunk;
-    p.workspace = S > 1 ? (size_t)S * B * kHeads * (kDc + 1) * sizeof(float) : 0;
-    p.launches = S > 1 ? 2 : 1;
+    const int C = clusters_for(B, max_seq_len, sms);
+    p.splits = C;
+    p.chunk = 0;
+    p.workspace = (size_t)2 * C * kHeads * (kDc + 1) * sizeof(float) + (size_t)(B + 1) * sizeof(int32_t);
+    p.workspace = (p.workspace + 255) / 256 * 256;
+    p.launches = 3;
     return p;
 }
 
@@ -542,28 +756,32 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
         !encode_2d(&tm_kv_rope, a.pool, kDk, kv_rows, kBf16RecordBytes, 32, kT,
                    CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
+    const int C = plan.splits;
+    float* o_part = static_cast<float*>(a.workspace);
+    float* lse_part = o_part + (size_t)2 * C * kHeads * kDc;
+    int32_t* meta = reinterpret_cast<int32_t*>(lse_part + (size_t)2 * C * kHeads);
     TcParams p;
     p.block_table = a.block_table;
     p.seq_lens = a.seq_lens;
     p.out = a.out;
     p.lse = a.lse;
-    p.o_part = a.o_part;
-    p.lse_part = a.lse_part;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.meta = meta;
     p.ctl = a.ctl;
     p.num_pages = a.num_pages;
     p.max_pages = a.max_pages;
     p.max_seq_len = a.max_seq_len;
     p.B = a.B;
-    p.chunk = plan.chunk;
-    p.splits = plan.splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const int64_t ctas = 2LL * a.B * plan.splits;
-    if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
-    decode_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_kv_lat,
-                                                                    tm_kv_rope, p);
+    const int64_t blocks = (int64_t)a.B * kHeads;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    empty_rows_kernel<<<(unsigned)blocks, 128, 0, st>>>(a.seq_lens, a.max_seq_len, a.out, a.lse);
+    decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope, p);
     e = cudaGetLastError();
-    if (e != cudaSuccess || plan.splits == 1) return e;
-    return launch_combine(a.o_part, a.lse_part, plan.splits, a.B, kHeads, a.out, a.lse, st);
+    if (e != cudaSuccess) return e;
+    merge_slots_kernel<<<(unsigned)blocks, 128, 0, st>>>(o_part, lse_part, meta, a.B, C, a.out, a.lse);
+    return cudaGetLastError();
 }
 
 }  // namespace mla

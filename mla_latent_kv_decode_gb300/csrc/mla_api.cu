@@ -148,13 +148,11 @@ mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const vo
     a.lse = lse;
     a.o_part = nullptr;
     a.lse_part = nullptr;
+    a.workspace = workspace;
     a.ctl = ctl;
-    if (plan.workspace > 0) {
-        if (!workspace || workspace_bytes < plan.workspace || !aligned(workspace, 256))
-            return MLA_ERR_INVALID;
-        a.o_part = static_cast<float*>(workspace);
-        a.lse_part = a.o_part + (size_t)plan.splits * B * kHeads * kDc;
-    }
+    if (plan.workspace > 0 &&
+        (!workspace || workspace_bytes < plan.workspace || !aligned(workspace, 256)))
+        return MLA_ERR_INVALID;
     return from_cuda(launch_decode(a, plan, stream));
 }
 

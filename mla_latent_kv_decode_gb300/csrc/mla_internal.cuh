@@ -72,8 +72,9 @@ struct DecodeArgs {
     float scale;
     __nv_bfloat16* out;
     float* lse;
-    float* o_part;         // [S, B, H, 512] when splits > 1
-    float* lse_part;       // [S, B, H]
+    float* o_part;         // simt path: [S, B, H, 512] when splits > 1
+    float* lse_part;       // simt path: [S, B, H]
+    void* workspace;       // caller scratch of at least plan.workspace bytes
     DevCtl* ctl;
 };
 
