@@ -4,38 +4,43 @@
 // 3.9 MB to 890 B per Token", Fig. 4 (1), Fig. 5 (2), Fig. 6 (2)):
 //     s_t = scale * (q_lat[h] . c_t + q_rope[h] . k_rope_t)
 //     out[h] = sum_t softmax(s)_t c_t,   lse[h] = ln sum_t exp(s_t).
-// All 128 heads share each cached latent row, so per 32-position tile the work is two dense
-// contractions: S[128 x 32] = Q[128 x 576] K^T and O[128 x 512] += P[128 x 32] V[32 x 512], with
-// V = the first 512 columns of the same rows.
+// All 128 heads share each cached latent row, so per 64-position tile (one cache page) the work is
+// two dense contractions: S[128 x 64] = Q[128 x 576] K^T and O[128 x 512] += P[128 x 64] V[64 x 512],
+// V being the first 512 columns of the same rows.
 //
 // Capacity drives the design.  O (128 x 512 fp32) fills all 512 columns of one SM's tensor memory
 // and Q (128 x 576 bf16, 144 KB) most of its shared memory, so the work runs on clusters of two
 // CTAs, r = 0, 1.  CTA r owns latent dims [256 r, 256 r + 256) and rope dims [32 r, 32 r + 32):
-//   * it streams only its 288 columns of every cached row (576 B per position) through a
-//     5-stage TMA ring, and holds only its half of Q (72 KB);
-//   * S_r = Q_r K_r^T is a partial score over its 288 dims (18 MMAs of 128x32x16 per tile);
-//   * the 128 softmax threads (one per head) send S_r to the peer CTA through distributed shared
-//     memory (st.async, 16 KB per tile) and add the peer's part: both CTAs then hold the same
-//     fp32 scores, bit for bit, and take identical softmax decisions;
-//   * P (bf16) goes to shared memory and O_r[128 x 256] += P V_r (2 MMAs of 128x256x16), V_r being
-//     the latent half already in the stage: nothing is loaded twice and no FLOP is repeated.
-// The online softmax runs in the log2 domain with a lazily updated running max (O is rescaled only
-// when a row max grows by more than 2^8), so the common tile never touches O.
+//   * it streams only its 288 columns of every cached row (576 B per position) through a 3-page
+//     TMA ring, and holds only its half of Q (72 KB);
+//   * S_r = Q_r K_r^T is a partial score over its 288 dims (18 MMAs of 128x64x16 per page);
+//   * the softmax threads send S_r to the peer CTA through distributed shared memory (st.async,
+//     32 KB per page) and add the peer's part: both CTAs then hold the same fp32 scores, bit for
+//     bit, and take identical softmax decisions;
+//   * P (bf16) is written to tensor memory and O_r[128 x 256] += P V_r runs as 4 MMAs of
+//     128x256x16 with P read from tensor memory, V_r being the latent half already in the stage:
+//     nothing is loaded twice and no FLOP is repeated.
+// The online softmax runs in the log2 domain with a lazily updated running max: the max of a
+// segment's first page is kept until a later score exceeds it by 2^16, so the common page needs
+// no row reduction and never touches O; a block-wide vote detects the rare page that does.
 //
-// Scheduling: the grid is a fixed set of C clusters (at most one per SM pair).  The tiles of all
+// Tensor memory (512 columns): O_r [0, 256), three score buffers [256 + 64 k), two P buffers
+// [448 + 32 k) (64 bf16 per lane in 32 columns).
+//
+// Scheduling: the grid is a fixed set of C clusters (at most one per SM pair).  The pages of all
 // requests form one stream of W tiles; cluster c takes tiles [c W / C, (c + 1) W / C), so every
 // cluster gets the same work whatever the length mix.  A cluster walks its range request by
 // request ("segments"); a segment that covers a whole request writes the final output, one cut
 // by a range boundary writes a partial (normalised output + lse) into slot 2c (the range's first
 // segment) or 2c + 1 (its last), and a small merge kernel combines the partials of cut requests.
 //
-// Pipelining: QK runs two tiles ahead of PV (3 score buffers in TMEM), the softmax threads read and
-// send the scores of tile i + 1 before they finish tile i (hiding the exchange latency), and the
-// next request's Q is loaded as soon as the last QK of the previous one has completed.
+// Pipelining: QK runs two pages ahead of PV (3 score buffers), the TMA ring three pages ahead, and
+// the next request's Q is loaded as soon as the last QK of the previous one has completed.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner), warps 2-5
-// softmax / exchange / epilogue (thread = head = TMEM lane).  Every wait is bounded: on expiry the
-// kernel records MLA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM, returns.
+// Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner), warps 2-17
+// softmax / exchange / epilogue: thread = head = TMEM lane, four warps share each 32-lane group
+// and take 16 positions of the page each.  Every wait is bounded: on expiry the kernel records
+// MLA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,36 +52,39 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kT = 32;                 // positions per tile
-constexpr int kNS = 5;                 // KV ring stages
+constexpr int kT = 64;                 // positions per tile = one cache page
+constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 3;                // score buffers in TMEM
 constexpr int kQKAhead = 2;            // QK of tile i + 2 may run before PV of tile i
-constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 512;   // 16 softmax warps
+constexpr int kSlice = kT / 4;         // positions per softmax warp
+constexpr int kThreads = 64 + kSoftmaxThreads;
+constexpr float kLazySlack = 16.0f;    // running max kept until a row max exceeds it by 2^16
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256)
-constexpr uint32_t kTmemS = 256;       // score buffer k: columns [256 + 32 k, 288 + 32 k)
+constexpr uint32_t kTmemS = 256;       // score buffer k: columns [256 + 64 k, 320 + 64 k)
+constexpr uint32_t kTmemP = 448;       // P buffer k: columns [448 + 32 k, 480 + 32 k)
 constexpr uint32_t kDrainLimit = 1u << 20;
-constexpr int kMinTilesPerCluster = 8;
+constexpr int kMinTilesPerCluster = 4;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] bf16, SW128
 constexpr int kQRopeBytes = 128 * 64;                  // [128 heads x 32 dims] bf16, SW64
-constexpr int kKvLatChunk = kT * 128;                  // [32 pos x 64 dims], SW128
-constexpr int kKvRope = kT * 64;                       // [32 pos x 32 dims], SW64
-constexpr int kStageBytes = 4 * kKvLatChunk + kKvRope;  // 18432
-constexpr int kXBytes = 128 * kT * 4;                  // peer partial scores, fp32 [8][128][4]
-constexpr int kPBytes = 128 * kT * 2;                  // P [128 heads x 32 pos] bf16, SW64
+constexpr int kKvLatChunk = kT * 128;                  // [64 pos x 64 dims], SW128
+constexpr int kKvRope = kT * 64;                       // [64 pos x 32 dims], SW64
+constexpr int kStageBytes = 4 * kKvLatChunk + kKvRope;  // 36864
+constexpr int kXBytes = 128 * kT * 4;                  // peer partial scores, fp32 [16][128][4]
 constexpr int kOffQ = 0;
 constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
 constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 73728
-constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 165888
-constexpr int kOffP = kOffX + 2 * kXBytes;             // 198656
-constexpr int kOffBar = kOffP + 2 * kPBytes;           // 215040
-constexpr int kNumBars = 2 * kNS + 2 * kNSB + 13;
-constexpr int kOffSched = kOffBar + 8 * kNumBars;      // scan scratch: kThreads int32
-constexpr int kSmemBytes = kOffSched + 4 * kThreads + 64 + 1024;   // + alignment slack
+constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 184320
+constexpr int kOffBar = kOffX + kXBytes;               // 217088
+constexpr int kNumBars = 2 * kNS + 2 * kNSB + 4 + 2 + 5;
+constexpr int kOffSched = kOffBar + 8 * kNumBars;
+constexpr int kOffRed = kOffSched + 64;                // per-head exchange between slices [4][128]
+constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 64 + 1024;   // + alignment slack
 
 constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;       // 73728 per CTA
 
@@ -99,7 +107,8 @@ struct TcParams {
 struct Bars {
     uint32_t kv_full, kv_empty;   // arrays of kNS
     uint32_t s_full, s_empty;     // arrays of kNSB
-    uint32_t p_full, p_empty, x_full, x_free;   // arrays of 2
+    uint32_t p_full, p_empty;     // arrays of 2
+    uint32_t x_full, x_free;
     uint32_t q_full, q_empty, o_full, o_free, mma_drain;
     __device__ __forceinline__ uint32_t kvf(int i) const { return kv_full + 8 * i; }
     __device__ __forceinline__ uint32_t kve(int i) const { return kv_empty + 8 * i; }
@@ -107,8 +116,6 @@ struct Bars {
     __device__ __forceinline__ uint32_t se(int i) const { return s_empty + 8 * i; }
     __device__ __forceinline__ uint32_t pf(int i) const { return p_full + 8 * i; }
     __device__ __forceinline__ uint32_t pe(int i) const { return p_empty + 8 * i; }
-    __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
-    __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
 };
 
 __device__ __forceinline__ Bars make_bars(uint32_t a) {
@@ -119,8 +126,8 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.s_empty = a; a += 8 * kNSB;
     b.p_full = a; a += 16;
     b.p_empty = a; a += 16;
-    b.x_full = a; a += 16;
-    b.x_free = a; a += 16;
+    b.x_full = a; a += 8;
+    b.x_free = a; a += 8;
     b.q_full = a; a += 8;
     b.q_empty = a; a += 8;
     b.o_full = a; a += 8;
@@ -143,11 +150,11 @@ __device__ __forceinline__ int clamp_len(int n, int max_len) {
     return n < 0 ? 0 : (n > max_len ? max_len : n);
 }
 
-// Walks the tiles of one cluster's range: request b, tile t of that request (nt tiles in all).
+// Walks the tiles of one cluster's range: request b, tile (page) t of that request.
 struct Cursor {
     const int32_t* seq_lens;
     int max_len, B;
-    int b, t, nt, n;         // n = visible positions of request b
+    int b, t, nt, n;         // n = visible positions of request b, nt = its tiles
     long long g, g_end;      // global tile index, end of range
     __device__ __forceinline__ void load_req() {
         n = clamp_len(seq_lens[b], max_len);
@@ -196,69 +203,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const uint32_t sbase = smem_u32(sm);
     const Bars bars = make_bars(sbase + kOffBar);
-    int* scan = reinterpret_cast<int*>(sm + kOffSched);
 
-    // ---- schedule: W = sum_b ceil(n_b / 32); this cluster's tiles [g_begin, g_end) ----
-    const int per = (p.B + kThreads - 1) / kThreads;
-    const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
-    int my_tiles = 0;
-    for (int b = b_lo; b < b_hi; ++b) {
-        const int raw = p.seq_lens[b];
-        if ((raw < 0 || raw > p.max_seq_len) && r == 0 && c == 0) record_error(p.ctl, MLA_ERR_BOUNDS, b);
-        my_tiles += (clamp_len(raw, p.max_seq_len) + kT - 1) / kT;
-    }
-    scan[tid] = my_tiles;
+    // ---- schedule (warp 0): W = sum_b ceil(n_b / 64); this cluster's tiles [g_begin, g_end) ----
     if (tid == 0) {
         s_abort = 0;
         s_start_b = p.B;
         s_start_t = 0;
     }
     __syncthreads();
-    if (tid == 0) {
-        long long acc = 0;
-        for (int i = 0; i < kThreads; ++i) {
-            const int v = scan[i];
-            scan[i] = (int)acc;
-            acc += v;
+    if (warp == 0) {
+        const int per = (p.B + 31) / 32;
+        const int b_lo = min(p.B, lane * per), b_hi = min(p.B, b_lo + per);
+        long long mine = 0;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int raw = p.seq_lens[b];
+            if ((raw < 0 || raw > p.max_seq_len) && r == 0 && c == 0) record_error(p.ctl, MLA_ERR_BOUNDS, b);
+            mine += (clamp_len(raw, p.max_seq_len) + kT - 1) / kT;
         }
-        s_W = acc;
-    }
-    __syncthreads();
-    const long long W = s_W;
-    const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
-    {
-        long long pre = scan[tid];
+        long long incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const long long W = __shfl_sync(0xffffffffu, incl, 31);
+        const long long gb = (long long)c * W / C;
+        long long pre = incl - mine;
         for (int b = b_lo; b < b_hi; ++b) {
             const int nt = (clamp_len(p.seq_lens[b], p.max_seq_len) + kT - 1) / kT;
             if (c == 0 && r == 0) p.meta[b] = (int)pre;
-            if (g_begin < g_end && g_begin >= pre && g_begin < pre + nt) {
+            if (gb < W && gb >= pre && gb < pre + nt) {
                 s_start_b = b;
-                s_start_t = (int)(g_begin - pre);
+                s_start_t = (int)(gb - pre);
             }
             pre += nt;
         }
-        if (c == 0 && r == 0 && tid == kThreads - 1) p.meta[p.B] = (int)W;
+        if (lane == 31) {
+            s_W = W;
+            if (c == 0 && r == 0) p.meta[p.B] = (int)W;
+        }
     }
 
-    if (tid == 0) {
+    if (tid == 32) {
         for (int i = 0; i < kNS; ++i) {
             mbar_init(bars.kvf(i), 1);
             mbar_init(bars.kve(i), 1);
         }
         for (int i = 0; i < kNSB; ++i) {
             mbar_init(bars.sf(i), 1);
-            mbar_init(bars.se(i), 128);
+            mbar_init(bars.se(i), kSoftmaxThreads / 32);   // one arrive per softmax warp
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bars.pf(i), 128);
+            mbar_init(bars.pf(i), kSoftmaxThreads / 32);
             mbar_init(bars.pe(i), 1);
-            mbar_init(bars.xf(i), 1);
-            mbar_init(bars.xe(i), 4);   // one remote arrive per peer softmax warp
         }
+        mbar_init(bars.x_full, 1);
+        mbar_init(bars.x_free, kSoftmaxThreads / 32);   // one remote arrive per peer softmax warp
         mbar_init(bars.q_full, 1);
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.o_full, 1);
-        mbar_init(bars.o_free, 128);
+        mbar_init(bars.o_free, kSoftmaxThreads / 32);
         mbar_init(bars.mma_drain, 1);
         fence_mbar_init();
     }
@@ -271,6 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the peer's barriers are initialised before any remote arrive / st.async
     const uint32_t tmem = s_tmem_base;
+    const long long W = s_W;
+    const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
     const int n_local = (int)(g_end - g_begin);   // tiles of this cluster
     const int start_b = s_start_b, start_t = s_start_t;
 
@@ -304,10 +310,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fail(p.ctl, &s_abort, 2);
                     break;
                 }
-                const int pos0 = cu.t * kT;
-                const int page = p.block_table[(size_t)cu.b * p.max_pages + pos0 / kPage];
+                const int page = p.block_table[(size_t)cu.b * p.max_pages + cu.t];
                 int row = -2 * kPage;   // outside the pool: the tile reads as zeros
-                if (page >= 0 && page < p.num_pages) row = page * kPage + pos0 % kPage;
+                if (page >= 0 && page < p.num_pages) row = page * kPage;
                 else if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
                 const uint32_t st = sbase + kOffKv + s * kStageBytes;
                 mbar_arrive_expect_tx(bars.kvf(s), kStageBytes);
@@ -341,40 +346,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             while (ip < n_local && !s_abort) {
                 if (iq < n_local && iq <= ip + kQKAhead) {
                     const int s = iq % kNS, sb = iq % kNSB;
-                    const bool ready = (!cq.first(g_begin) || mbar_try_wait(bars.q_full, seg_q & 1)) &&
-                                       mbar_try_wait(bars.kvf(s), (iq / kNS) & 1) &&
-                                       mbar_try_wait(bars.se(sb), ((iq / kNSB) & 1) ^ 1);
+                    const bool ready = (!cq.first(g_begin) || mbar_test(bars.q_full, seg_q & 1)) &&
+                                       mbar_test(bars.kvf(s), (iq / kNS) & 1) &&
+                                       mbar_test(bars.se(sb), ((iq / kNSB) & 1) ^ 1);
                     if (ready) {
-                    tc_fence_after();
-                    const uint32_t st = sbase + kOffKv + s * kStageBytes;
-                    const uint32_t d = tmem + kTmemS + sb * kT;
+                        tc_fence_after();
+                        const uint32_t st = sbase + kOffKv + s * kStageBytes;
+                        const uint32_t d = tmem + kTmemS + sb * kT;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                        for (int k = 0; k < 4; ++k)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(d, smem_desc(q_lat + k * kQLatChunk + kk * 32, 16, 1024, kSw128),
-                                        smem_desc(st + k * kKvLatChunk + kk * 32, 16, 1024, kSw128),
-                                        id_qk, (k | kk) != 0 ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss(d, smem_desc(q_lat + k * kQLatChunk + kk * 32, 16, 1024, kSw128),
+                                            smem_desc(st + k * kKvLatChunk + kk * 32, 16, 1024, kSw128),
+                                            id_qk, (k | kk) != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
-                        mma_bf16_ss(d, smem_desc(q_rope + kk * 32, 16, 512, kSw64),
-                                    smem_desc(st + 4 * kKvLatChunk + kk * 32, 16, 512, kSw64), id_qk, 1u);
-                    mma_commit(bars.sf(sb));
-                    if (cq.last()) {
-                        mma_commit(bars.q_empty);
-                        ++seg_q;
-                    }
-                    cq.next();
-                    ++iq;
-                    polls = 0;
-                    continue;
+                        for (int kk = 0; kk < 2; ++kk)
+                            mma_bf16_ss(d, smem_desc(q_rope + kk * 32, 16, 512, kSw64),
+                                        smem_desc(st + 4 * kKvLatChunk + kk * 32, 16, 512, kSw64), id_qk, 1u);
+                        mma_commit(bars.sf(sb));
+                        if (cq.last()) {
+                            mma_commit(bars.q_empty);
+                            ++seg_q;
+                        }
+                        cq.next();
+                        ++iq;
+                        polls = 0;
+                        continue;
                     }
                 }
-                // PV of tile ip
+                // PV of tile ip: O_r += P (tensor memory) x V_r (stage, MN-major)
                 const bool seg_first = cp.first(g_begin);
                 const int pb = ip & 1;
-                const bool pv_ready = (!seg_first || seg_p == 0 || mbar_try_wait(bars.o_free, (seg_p - 1) & 1)) &&
-                                      mbar_try_wait(bars.pf(pb), (ip >> 1) & 1);
+                const bool pv_ready = (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
+                                      mbar_test(bars.pf(pb), (ip >> 1) & 1);
                 if (!pv_ready) {
                     if (++polls > wait_limit) {
                         fail(p.ctl, &s_abort, 6);
@@ -384,11 +389,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 polls = 0;
                 tc_fence_after();
-                const uint32_t pa = sbase + kOffP + pb * kPBytes;
                 const uint32_t v = sbase + kOffKv + (ip % kNS) * kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_bf16_ss(tmem + kTmemO, smem_desc(pa + kk * 32, 16, 512, kSw64),
+                    mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 32 * pb + 8 * kk,
                                 smem_desc(v + kk * 16 * 128, kKvLatChunk, 1024, kSw128), id_pv,
                                 (!seg_first || kk > 0) ? 1u : 0u);
                 mma_commit(bars.pe(pb));
@@ -404,197 +408,198 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ softmax warps
-        const int lg = warp & 3;                 // TMEM lane group this warp may access
-        const int h = lg * 32 + lane;            // head = TMEM lane
+        // 16 warps.  Lane group lg = warp % 4: the TMEM lanes the warp may access, i.e. heads
+        // 32 lg .. 32 lg + 31 (thread = head).  Slice ts = (warp - 2) / 4: positions
+        // 16 ts .. 16 ts + 15 of every page, and O columns 64 ts .. 64 ts + 63 in corrections and
+        // epilogues.
+        //
+        // The 16 warps meet at named barriers, which cannot time out, so this loop never leaves
+        // early: after a failed (bounded) wait it keeps executing every barrier but skips the
+        // work, and waits return at once.  Wait results are made warp-uniform before any
+        // warp-collective tcgen05 instruction.
+        const int lg = warp & 3;
+        const int ts = (warp - 2) >> 2;
+        const int h = lg * 32 + lane;
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
         const uint32_t x_remote = mapa(sbase + kOffX, peer);
         const uint32_t xfull_remote = mapa(bars.x_full, peer);
         const uint32_t xfree_remote = mapa(bars.x_free, peer);
         const bool leader = (tid == 64);
-        float m_used = -INFINITY, l_run = 0.f;
-        float s_own[kT], s_next[kT];
+        float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][128 heads]
+        float m_used = -INFINITY, l_part = 0.f;
 
-        // read this CTA's partial scores of local tile i from TMEM and send them to the peer
-        auto load_and_send = [&](int i, float (&dst)[kT]) -> bool {
-            const int sb = i % kNSB, xb = i & 1;
-            if (!mbar_wait(bars.sf(sb), (i / kNSB) & 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 7);
-                return false;
-            }
-            tc_fence_after();
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + kTmemS + sb * kT, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bars.se(sb));
-#pragma unroll
-            for (int t = 0; t < kT; ++t) dst[t] = __uint_as_float(v[t]);
-            if (!mbar_wait(bars.xe(xb), ((i >> 1) & 1) ^ 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 8);
-                return false;
-            }
-#pragma unroll
-            for (int g = 0; g < kT / 4; ++g)
-                st_async_v4(x_remote + xb * kXBytes + (g * 128 + h) * 16, xfull_remote + 8 * xb,
-                            v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-            return true;
+        auto wwait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+            bool ok = !s_abort && mbar_wait(bar, parity, wait_limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0) fail(p.ctl, &s_abort, where);
+            return ok;
         };
 
         Cursor cu;
         cu.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
         int seg = 0;
         bool cut_front = false;
-        bool ok = true;
-        if (n_local > 0) ok = load_and_send(0, s_own);
-        for (int i = 0; ok && i < n_local; ++i, cu.next()) {
-            if (s_abort) break;
-            const int xb = i & 1, pb = i & 1;
-            // send the next tile's scores early (hides the exchange latency), except across a
-            // request boundary where the next QK waits for the next request's Q
-            const bool send_early = i + 1 < n_local && !cu.last();
-            if (send_early && !load_and_send(i + 1, s_next)) break;
+        for (int i = 0; i < n_local; ++i, cu.next()) {
+            const int sb = i % kNSB, pb = i & 1;
             const bool first = cu.first(g_begin);
             if (first) {
                 m_used = -INFINITY;
-                l_run = 0.f;
+                l_part = 0.f;
                 cut_front = cu.t > 0;   // the request started before this cluster's range
             }
-            // peer's partial scores of tile i
-            if (leader) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
-            if (!mbar_wait(bars.xf(xb), (i >> 1) & 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 9);
-                break;
-            }
-            float x[kT];
-            const uint8_t* xp = sm + kOffX + xb * kXBytes;
-#pragma unroll
-            for (int g = 0; g < kT / 4; ++g) {
-                const float4 q = *reinterpret_cast<const float4*>(xp + (g * 128 + h) * 16);
-                x[4 * g] = s_own[4 * g] + q.x;
-                x[4 * g + 1] = s_own[4 * g + 1] + q.y;
-                x[4 * g + 2] = s_own[4 * g + 2] + q.z;
-                x[4 * g + 3] = s_own[4 * g + 3] + q.w;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(xfree_remote + 8 * xb);
-
-            // visibility of the tile's positions
-            const int pos0 = cu.t * kT;
-            const int page = p.block_table[(size_t)cu.b * p.max_pages + pos0 / kPage];
-            const bool page_ok = page >= 0 && page < p.num_pages;
-            const int nvalid = page_ok ? min(kT, cu.n - pos0) : 0;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int t = 0; t < kT; ++t) {
-                x[t] = t < nvalid ? x[t] * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[t]);
-            }
-            // lazy running max: rescale O only when the row max grows by more than 2^8
-            const bool need = mt > m_used + 8.0f;
-            const float m_new = need ? mt : m_used;
-            if (!first && __any_sync(0xffffffffu, need)) {
-                if (!mbar_wait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 10);
-                    break;
-                }
+            // this CTA's partial scores of the warp's 16 positions: TMEM -> registers -> peer
+            uint32_t v[16];
+            const bool sok = wwait(bars.sf(sb), (i / kNSB) & 1, 7);
+            if (sok) {
                 tc_fence_after();
-                const float alpha = need ? exp2f(m_used - m_new) : 1.0f;
-#pragma unroll 1
-                for (int cc = 0; cc < kHalfLat / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + kTmemO + 32 * cc, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    tmem_st32(tmem + lane_off + kTmemO + 32 * cc, o);
-                }
-                tmem_wait_st();
-                l_run *= alpha;
+                tmem_ld16(tmem + lane_off + kTmemS + sb * kT + kSlice * ts, v);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.se(sb));
             }
-            m_used = m_new;
-            float psum = 0.f;
-            uint32_t pk[kT / 2];
+            if (wwait(bars.x_free, (i & 1) ^ 1, 8)) {
 #pragma unroll
-            for (int t = 0; t < kT; t += 2) {
-                const float p0 = m_used == -INFINITY ? 0.f : exp2f(x[t] - m_used);
-                const float p1 = m_used == -INFINITY ? 0.f : exp2f(x[t + 1] - m_used);
+                for (int g = 0; g < 4; ++g)
+                    st_async_v4(x_remote + ((4 * ts + g) * 128 + h) * 16, xfull_remote, v[4 * g],
+                                v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            }
+            // full scores = own partial + the peer's (the same fp32 sum in both CTAs, so both
+            // take identical decisions)
+            if (leader && !s_abort) mbar_arrive_expect_tx(bars.x_full, kXBytes);
+            const bool xok = wwait(bars.x_full, i & 1, 9);
+            const int nv = min(kT, cu.n - cu.t * kT) - kSlice * ts;   // valid positions here
+            float x[16];
+            float mx = -INFINITY;
+            const uint8_t* xp = sm + kOffX;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * 128 + h) * 16);
+                x[4 * g] = __uint_as_float(v[4 * g]) + q.x;
+                x[4 * g + 1] = __uint_as_float(v[4 * g + 1]) + q.y;
+                x[4 * g + 2] = __uint_as_float(v[4 * g + 2]) + q.z;
+                x[4 * g + 3] = __uint_as_float(v[4 * g + 3]) + q.w;
+            }
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                if (t < nv) mx = fmaxf(mx, x[t]);
+            // every loaded value has been consumed: hand the exchange buffer back to the peer
+            __syncwarp();
+            if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote);
+            const float mx2 = mx * p.scale_log2;
+            const bool need = first || mx2 > m_used + kLazySlack;
+            if (bar_red_or(1, kSoftmaxThreads, need)) {
+                // rare path (and every segment start): exact page row max over the four slices,
+                // new running max where it grew past the slack, O and partial sums rescaled
+                red[ts * 128 + h] = mx2;
+                named_bar_sync(2, kSoftmaxThreads);
+                const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
+                const bool grow = first || tmax > m_used + kLazySlack;
+                const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
+                if (!first) {
+                    const float alpha = grow ? ex2(m_used - m_new) : 1.0f;
+                    if (__any_sync(0xffffffffu, grow) && wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const uint32_t col = kTmemO + 64 * ts + 32 * cc;
+                            uint32_t o[32];
+                            tmem_ld32(tmem + lane_off + col, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                            tmem_st32(tmem + lane_off + col, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    l_part *= alpha;
+                }
+                m_used = m_new;
+                named_bar_sync(2, kSoftmaxThreads);   // red[] is free again
+            }
+            // P = 2^(x * scale * log2 e - m) for this warp's positions, packed to bf16
+            const float nm = -m_used;
+            float psum = 0.f;
+            uint32_t pk[8];
+#pragma unroll
+            for (int t = 0; t < 16; t += 2) {
+                float p0 = 0.f, p1 = 0.f;
+                if (m_used != -INFINITY) {
+                    p0 = t < nv ? ex2(fmaf(x[t], p.scale_log2, nm)) : 0.f;
+                    p1 = t + 1 < nv ? ex2(fmaf(x[t + 1], p.scale_log2, nm)) : 0.f;
+                }
                 psum += p0 + p1;
                 pk[t / 2] = pack_bf16x2(p0, p1);
             }
-            l_run += psum;
-            // positions past the end of the request in a live page: zero their V rows so that
-            // 0 * (stale bytes) cannot poison O
-            if (page_ok && nvalid < kT) {
+            l_part += psum;
+            // positions past the end of the request: zero their V rows so that 0 * (stale bytes)
+            // cannot poison O (QK of this page has completed, PV has not started)
+            const int nvalid = min(kT, cu.n - cu.t * kT);
+            if (nvalid < kT && sok) {
                 uint8_t* st = sm + kOffKv + (i % kNS) * kStageBytes;
                 const int nrows = kT - nvalid;
-                for (int e = tid - 64; e < nrows * 4 * 8; e += 128) {
+                for (int e = tid - 64; e < nrows * 4 * 8; e += kSoftmaxThreads) {
                     const int row = nvalid + e / 32, k = (e / 8) % 4, part = e % 8;
                     *reinterpret_cast<uint4*>(st + k * kKvLatChunk + row * 128 + part * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            // P row h (64 bytes) into the SW64 K-major buffer once PV of tile i - 2 released it
-            if (i >= 2 && !mbar_wait(bars.pe(pb), ((i - 2) >> 1) & 1, wait_limit)) {
-                fail(p.ctl, &s_abort, 11);
-                break;
+            // P of this warp's 16 positions into tensor memory once PV of tile i - 2 released it
+            if (i < 2 || wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11)) {
+                tmem_st8(tmem + lane_off + kTmemP + 32 * pb + 8 * ts, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
             }
-            uint8_t* pbuf = sm + kOffP + pb * kPBytes;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int pc = cc ^ ((h >> 1) & 3);
-                *reinterpret_cast<uint4*>(pbuf + h * 64 + pc * 16) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bars.pf(pb));
 
             if (cu.last()) {
                 // ------------------------------------------------------ segment epilogue
                 const bool partial = cut_front || cu.t < cu.nt - 1;
                 const int slot = 2 * c + (seg == 0 ? 0 : 1);
-                if (!mbar_wait(bars.o_full, seg & 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 12);
-                    break;
-                }
-                tc_fence_after();
-                const float inv = l_run > 0.f ? 1.0f / l_run : 0.0f;
-                const float L = l_run > 0.f ? (m_used + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-                const size_t row = (size_t)cu.b * kHeads + h;
+                red[ts * 128 + h] = l_part;
+                named_bar_sync(2, kSoftmaxThreads);
+                const float l_row = (red[h] + red[128 + h]) + (red[256 + h] + red[384 + h]);
+                named_bar_sync(2, kSoftmaxThreads);
+                if (wwait(bars.o_full, seg & 1, 12)) {
+                    tc_fence_after();
+                    const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
+                    const float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
+                    const size_t row = (size_t)cu.b * kHeads + h;
 #pragma unroll 1
-                for (int cc = 0; cc < kHalfLat / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + kTmemO + 32 * cc, o);
-                    tmem_wait_ld();
-                    const int col = (int)r * kHalfLat + 32 * cc;
-                    if (!partial) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tmem + lane_off + kTmemO + 64 * ts + 32 * cc, o);
+                        tmem_wait_ld();
+                        const int col = (int)r * kHalfLat + 64 * ts + 32 * cc;
+                        if (!partial) {
+                            uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[k] = make_uint4(
-                                pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
+                            for (int k = 0; k < 4; ++k)
+                                dst[k] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                                 __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                            for (int k = 0; k < 8; ++k)
+                                dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                                     __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                        }
                     }
+                    if (r == 0 && ts == 0) {
+                        if (!partial) p.lse[row] = L;
+                        else p.lse_part[(size_t)slot * kHeads + h] = L;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.o_free);
                 }
-                if (r == 0) {
-                    if (!partial) p.lse[row] = L;
-                    else p.lse_part[(size_t)slot * kHeads + h] = L;
-                }
-                tc_fence_before();
-                mbar_arrive(bars.o_free);
                 ++seg;
             }
-            if (i + 1 < n_local && !send_early && !load_and_send(i + 1, s_next)) break;
-#pragma unroll
-            for (int t = 0; t < kT; ++t) s_own[t] = s_next[t];
         }
     }
 
@@ -624,17 +629,14 @@ __global__ void __launch_bounds__(128) merge_slots_kernel(const float* __restric
                                                           float* __restrict__ lse) {
     const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
     const long long W = meta[B];
-    const long long T0 = meta[b], T1 = (b + 1 < B) ? meta[b + 1] : W;
-    if (T1 <= T0 || W <= 0) return;   // no tiles: the decode kernel wrote nothing to merge
+    const long long T0 = meta[b], T1 = meta[b + 1];
+    if (T1 <= T0 || W <= 0) return;   // no tiles: nothing to merge
     int c_lo = (int)((T0 * C) / W);
     while (c_lo > 0 && (long long)c_lo * W / C > T0) --c_lo;
     while (c_lo + 1 < C && (long long)(c_lo + 1) * W / C <= T0) ++c_lo;
     int c_hi = c_lo;
     while (c_hi + 1 < C && (long long)(c_hi + 1) * W / C < T1) ++c_hi;
-    if (c_hi == c_lo && (long long)c_lo * W / C <= T0) {
-        // the whole request lies in one range unless that range begins inside it (cut at front)
-        return;
-    }
+    if (c_hi == c_lo) return;         // the whole request lies in one range: already final
     float m = -INFINITY;
     for (int cc = c_lo; cc <= c_hi; ++cc) {
         const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
