@@ -40,8 +40,8 @@ L2_BYTES = 126 * 2 ** 20
 # DRAM bytes per decode launch from an ncu capture, keyed by the sha256 of the decode kernel
 # sources it was taken on; any change to those sources makes the entry stale (traffic = null).
 NCU_TRAFFIC = {}
-DECODE_SOURCES = ["mla_latent_kv_decode_gb300/csrc/decode_simt.cu",
-                  "mla_latent_kv_decode_gb300/csrc/combine.cu"]
+DECODE_SOURCES = ["mla_latent_kv_decode_gb300/csrc/decode_tc.cu",
+                  "mla_latent_kv_decode_gb300/csrc/tc_ptx.cuh"]
 
 
 def _sources_hash() -> str:
