@@ -119,6 +119,34 @@ mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const vo
                       int32_t topk, int32_t B, int32_t H, float scale, void* out, float* lse,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* mla_decode without a caller-provided workspace (this entry point has no counterpart in the
+ * pages; it is a convenience of this library).
+ *
+ * For callers that cannot allocate device memory at the point where they decode: a plug-in
+ * running inside a host application that owns every device allocation, or a serving loop that
+ * must not allocate (cudaMalloc synchronises the device and may fail under memory pressure)
+ * once it is running.  Such a caller still owns and passes all inputs and outputs; the split-KV
+ * scratch comes from a static device array of MLA_STATIC_WORKSPACE_BYTES that every GPU holds
+ * from the first use of this library until the process exits.  Nothing is allocated: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Arguments, results and errors are those of mla_decode (without workspace/workspace_bytes).
+ * Additionally returns MLA_ERR_UNSUPPORTED, before launching anything, when
+ * mla_decode_workspace_bytes(fmt, B, H, max_seq_len, topk) exceeds MLA_STATIC_WORKSPACE_BYTES.
+ *
+ * The first call on a device, with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any stream capture.  All
+ * calls on a device share the one array, which keeps whatever the last call left in it (the
+ * decode writes every scratch byte it reads, so nothing has to start at zero).  Calls whose
+ * executions overlap on the GPU (on different streams, or from different threads) race on the
+ * array: order them, e.g. on one stream. */
+#define MLA_STATIC_WORKSPACE_BYTES ((size_t)48 << 20)
+mla_status mla_decode_noalloc(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
+                              const void* q_rope, const int32_t* block_table, int32_t max_pages,
+                              const int32_t* seq_lens, int32_t max_seq_len,
+                              const int32_t* topk_idx, int32_t topk, int32_t B, int32_t H,
+                              float scale, void* out, float* lse, cudaStream_t stream);
+
 /* Split-KV merge: S partial results of the same queries over disjoint position sets.
  *   o_part  : device fp32 [S, B, H, 512] normalised partial outputs.
  *   lse_part: device fp32 [S, B, H] partial log-sum-exps (-inf for an empty part).

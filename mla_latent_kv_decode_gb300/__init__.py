@@ -63,6 +63,9 @@ def load():
         lib.mla_decode.argtypes = [i32, P, i64, P, P, P, i32, P, i32, P, i32, i32, i32, f32, P, P,
                                    P, sz, P]
         lib.mla_decode.restype = ctypes.c_int
+        lib.mla_decode_noalloc.argtypes = [i32, P, i64, P, P, P, i32, P, i32, P, i32, i32, i32, f32,
+                                           P, P, P]
+        lib.mla_decode_noalloc.restype = ctypes.c_int
         lib.mla_combine.argtypes = [P, P, i32, i32, i32, P, P, P]
         lib.mla_combine.restype = ctypes.c_int
         lib.mla_check_status.argtypes = [P]
@@ -165,6 +168,31 @@ def decode(fmt: int, pool, num_pages: int, q_lat, q_rope, block_table, seq_lens,
         _dev_ptr(lse, "lse", torch.float32, (B, H)),
         _dev_ptr(workspace, "workspace"), ws_bytes, _stream_ptr(stream))
     _check(rc, "mla_decode")
+    return out, lse
+
+
+def decode_noalloc(fmt: int, pool, num_pages: int, q_lat, q_rope, block_table, seq_lens,
+                   max_seq_len: int, scale: float, topk_idx=None, out=None, lse=None, stream=None):
+    """decode() for callers that cannot allocate device memory while decoding: the split-KV
+    scratch is the library's static device array (include/mla.h, mla_decode_noalloc) instead of a
+    workspace tensor.  Outputs must be passed in by such callers; calls must not overlap."""
+    torch = _torch()
+    B, H, _ = q_lat.shape
+    if out is None:
+        out = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=q_lat.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q_lat.device)
+    topk = 0 if topk_idx is None else int(topk_idx.shape[1])
+    rc = load().mla_decode_noalloc(
+        int(fmt), _dev_ptr(pool, "pool", torch.uint8), int(num_pages),
+        _dev_ptr(q_lat, "q_lat", torch.bfloat16, (B, H, D_C)),
+        _dev_ptr(q_rope, "q_rope", torch.bfloat16, (B, H, D_R)),
+        _dev_ptr(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev_ptr(seq_lens, "seq_lens", torch.int32, (B,)), int(max_seq_len),
+        _dev_ptr(topk_idx, "topk_idx", torch.int32), topk, int(B), int(H), float(scale),
+        _dev_ptr(out, "out", torch.bfloat16, (B, H, D_C)),
+        _dev_ptr(lse, "lse", torch.float32, (B, H)), _stream_ptr(stream))
+    _check(rc, "mla_decode_noalloc")
     return out, lse
 
 

@@ -156,6 +156,48 @@ mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const vo
     return from_cuda(launch_decode(a, plan, stream));
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Decode with a static scratch array, for callers that cannot allocate device memory (see mla.h).
+// ------------------------------------------------------------------------------------------------
+namespace {
+// The split-KV scratch of mla_decode_noalloc.  In host code this name is only a stand-in for the
+// device array: its device address comes from cudaGetSymbolAddress, once per device.
+__device__ __align__(256) unsigned char g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {};
+
+void* static_workspace_for_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
+        g_static_ptr[dev] = p;
+    }
+    return g_static_ptr[dev];
+}
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_noalloc(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
+                              const void* q_rope, const int32_t* block_table, int32_t max_pages,
+                              const int32_t* seq_lens, int32_t max_seq_len,
+                              const int32_t* topk_idx, int32_t topk, int32_t B, int32_t H,
+                              float scale, void* out, float* lse, cudaStream_t stream) {
+    if (B > 0 && H == kHeads && fmt_ok(fmt) && max_seq_len >= 0 && topk >= 0 &&
+        mla_decode_workspace_bytes(fmt, B, H, max_seq_len, topk) > MLA_STATIC_WORKSPACE_BYTES)
+        return MLA_ERR_UNSUPPORTED;
+    void* ws = static_workspace_for_current_device();
+    if (!ws) return MLA_ERR_CUDA;
+    return mla_decode(fmt, pool, num_pages, q_lat, q_rope, block_table, max_pages, seq_lens,
+                      max_seq_len, topk_idx, topk, B, H, scale, out, lse, ws,
+                      MLA_STATIC_WORKSPACE_BYTES, stream);
+}
+
 mla_status mla_combine(const float* o_part, const float* lse_part, int32_t S, int32_t B, int32_t H,
                        void* out, float* lse, cudaStream_t stream) {
     if (S <= 0 || B < 0 || H <= 0) return MLA_ERR_INVALID;
