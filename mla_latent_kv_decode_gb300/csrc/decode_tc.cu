@@ -13,16 +13,19 @@
 // CTAs, r = 0, 1.  CTA r owns latent dims [256 r, 256 r + 256) and rope dims [32 r, 32 r + 32):
 //   * it streams only its 288 columns of every cached row (576 B per position) through a 3-page
 //     TMA ring, and holds only its half of Q (72 KB);
-//   * S_r = Q_r K_r^T is a partial score over its 288 dims (18 MMAs of 128x64x16 per page);
-//   * the softmax threads send S_r to the peer CTA through distributed shared memory (st.async,
-//     32 KB per page) and add the peer's part: both CTAs then hold the same fp32 scores, bit for
-//     bit, and take identical softmax decisions;
-//   * P (bf16) is written to tensor memory and O_r[128 x 256] += P V_r runs as 4 MMAs of
-//     128x256x16 with P read from tensor memory, V_r being the latent half already in the stage:
-//     nothing is loaded twice and no FLOP is repeated.
+//   * S_r = Q_r K_r^T is a partial score over its 288 dims, for all 128 heads (18 MMAs of
+//     128x64x16 per page);
+//   * O_r[128 x 256] += P V_r (4 MMAs of 128x256x16, P read from tensor memory), V_r being the
+//     latent half already in the stage: nothing is loaded twice and no FLOP is repeated.
+// The softmax is split by heads: CTA r finishes heads [64 r, 64 r + 64) ("owned" heads).  Per page
+// it receives the peer's partial scores of its owned heads (16 KB fp32) through distributed shared
+// memory, computes P for them, and sends that P (8 KB bf16) back, so that each CTA ends up with P
+// for all 128 heads in its tensor memory.  That halves both the exchange and the exponentials
+// against exchanging all scores.
 // The online softmax runs in the log2 domain with a lazily updated running max: the max of a
 // segment's first page is kept until a later score exceeds it by 2^16, so the common page needs
-// no row reduction and never touches O; a block-wide vote detects the rare page that does.
+// no row reduction and never touches O; a vote among the warps sharing a head detects the rare
+// page that does, and the rescale factor travels with P to the peer.
 //
 // Tensor memory (512 columns): O_r [0, 256), three score buffers [256 + 64 k), two P buffers
 // [448 + 32 k) (64 bf16 per lane in 32 columns).
@@ -32,15 +35,14 @@
 // cluster gets the same work whatever the length mix.  A cluster walks its range request by
 // request ("segments"); a segment that covers a whole request writes the final output, one cut
 // by a range boundary writes a partial (normalised output + lse) into slot 2c (the range's first
-// segment) or 2c + 1 (its last), and a small merge kernel combines the partials of cut requests.
+// segment) or 2c + 1 (its last), and a merge kernel combines the partials of cut requests.
 //
-// Pipelining: QK runs two pages ahead of PV (3 score buffers), the TMA ring three pages ahead, and
-// the next request's Q is loaded as soon as the last QK of the previous one has completed.
-//
-// Warp roles (576 threads): warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner), warps 2-17
-// softmax / exchange / epilogue: thread = head = TMEM lane, four warps share each 32-lane group
-// and take 16 positions of the page each.  Every wait is bounded: on expiry the kernel records
-// MLA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM and returns.
+// Warp roles (576 threads): warp 0 TMA producer; warp 1 MMA issuer (+ TMEM owner); warps 2-17:
+// thread = head = TMEM lane, four warps per 32-lane group, 16 positions of a page each.  The 8
+// warps on the owned heads' lanes run the softmax ("owners"); the 8 on the other heads' lanes
+// ("agents") forward this CTA's partial scores of those heads to the peer, place the P the peer
+// sends back into tensor memory and finish those O rows.  Every wait is bounded: on expiry the
+// kernel records MLA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM, returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -56,12 +58,13 @@ constexpr int kT = 64;                 // positions per tile = one cache page
 constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 3;                // score buffers in TMEM
 constexpr int kQKAhead = 2;            // QK of tile i + 2 may run before PV of tile i
-constexpr int kSoftmaxThreads = 512;   // 16 softmax warps
-constexpr int kSlice = kT / 4;         // positions per softmax warp
+constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
+constexpr int kSlice = kT / 4;         // positions per warp
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr float kLazySlack = 16.0f;    // running max kept until a row max exceeds it by 2^16
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
+constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256)
 constexpr uint32_t kTmemS = 256;       // score buffer k: columns [256 + 64 k, 320 + 64 k)
@@ -75,16 +78,19 @@ constexpr int kQRopeBytes = 128 * 64;                  // [128 heads x 32 dims] 
 constexpr int kKvLatChunk = kT * 128;                  // [64 pos x 64 dims], SW128
 constexpr int kKvRope = kT * 64;                       // [64 pos x 32 dims], SW64
 constexpr int kStageBytes = 4 * kKvLatChunk + kKvRope;  // 36864
-constexpr int kXBytes = 128 * kT * 4;                  // peer partial scores, fp32 [16][128][4]
+constexpr int kXBytes = kOwned * kT * 4;               // peer partial scores of owned heads, fp32
+constexpr int kPInBytes = kOwned * kT * 2;             // peer's P of its owned heads, bf16
+constexpr int kPInMsg = kPInBytes + kOwned * 4;        // + one rescale factor per head
 constexpr int kOffQ = 0;
 constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
 constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 73728
-constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 184320
-constexpr int kOffBar = kOffX + kXBytes;               // 217088
-constexpr int kNumBars = 2 * kNS + 2 * kNSB + 4 + 2 + 5;
-constexpr int kOffSched = kOffBar + 8 * kNumBars;
-constexpr int kOffRed = kOffSched + 64;                // per-head exchange between slices [4][128]
-constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 64 + 1024;   // + alignment slack
+constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 184320: 2 buffers [16][64][16 B]
+constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 217088: [8][64][16 B] + alpha[64]
+constexpr int kOffLIn = kOffPIn + kPInMsg;             // 225536: 2 x l[64] of the peer's heads
+constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 226048
+constexpr int kNumBars = 2 * kNS + 2 * kNSB + 4 + 4 + 2 + 2 + 5;
+constexpr int kOffRed = kOffBar + 8 * kNumBars;        // per-head exchange between slices [4][128]
+constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 1024;   // + alignment slack
 
 constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;       // 73728 per CTA
 
@@ -95,7 +101,7 @@ struct TcParams {
     float* lse;
     float* o_part;          // [2C][128][512]
     float* lse_part;        // [2C][128]
-    int32_t* meta;          // tile_start[B], then W
+    int32_t* meta;          // per request: first partial slot, last cluster (2 x int32)
     DevCtl* ctl;
     int64_t num_pages;
     int max_pages;
@@ -108,7 +114,9 @@ struct Bars {
     uint32_t kv_full, kv_empty;   // arrays of kNS
     uint32_t s_full, s_empty;     // arrays of kNSB
     uint32_t p_full, p_empty;     // arrays of 2
-    uint32_t x_full, x_free;
+    uint32_t x_full, x_free;      // arrays of 2
+    uint32_t pin_full, pin_free;
+    uint32_t l_full;              // array of 2
     uint32_t q_full, q_empty, o_full, o_free, mma_drain;
     __device__ __forceinline__ uint32_t kvf(int i) const { return kv_full + 8 * i; }
     __device__ __forceinline__ uint32_t kve(int i) const { return kv_empty + 8 * i; }
@@ -116,6 +124,9 @@ struct Bars {
     __device__ __forceinline__ uint32_t se(int i) const { return s_empty + 8 * i; }
     __device__ __forceinline__ uint32_t pf(int i) const { return p_full + 8 * i; }
     __device__ __forceinline__ uint32_t pe(int i) const { return p_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
+    __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
+    __device__ __forceinline__ uint32_t lf(int i) const { return l_full + 8 * i; }
 };
 
 __device__ __forceinline__ Bars make_bars(uint32_t a) {
@@ -126,8 +137,11 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.s_empty = a; a += 8 * kNSB;
     b.p_full = a; a += 16;
     b.p_empty = a; a += 16;
-    b.x_full = a; a += 8;
-    b.x_free = a; a += 8;
+    b.x_full = a; a += 16;
+    b.x_free = a; a += 16;
+    b.pin_full = a; a += 8;
+    b.pin_free = a; a += 8;
+    b.l_full = a; a += 16;
     b.q_full = a; a += 8;
     b.q_empty = a; a += 8;
     b.o_full = a; a += 8;
@@ -180,6 +194,14 @@ struct Cursor {
     }
 };
 
+// 16 bytes (4 x b32) into the peer's shared memory, completing tx-bytes on its barrier.
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t remote_bar, uint32_t v) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     remote_addr),
+                 "r"(v), "r"(remote_bar)
+                 : "memory");
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                      const __grid_constant__ CUtensorMap tm_qrope,
@@ -204,7 +226,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(sm);
     const Bars bars = make_bars(sbase + kOffBar);
 
-    // ---- schedule (warp 0): W = sum_b ceil(n_b / 64); this cluster's tiles [g_begin, g_end) ----
+    // ---- schedule (warp 0): W = sum_b ceil(n_b / 64); this cluster's tiles [g_begin, g_end).
+    // Cluster 0 also records, per request, where its partials are: the first slot and the last
+    // cluster of the ranges it touches (first slot -1: no tiles).
     if (tid == 0) {
         s_abort = 0;
         s_start_b = p.B;
@@ -231,17 +255,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         long long pre = incl - mine;
         for (int b = b_lo; b < b_hi; ++b) {
             const int nt = (clamp_len(p.seq_lens[b], p.max_seq_len) + kT - 1) / kT;
-            if (c == 0 && r == 0) p.meta[b] = (int)pre;
+            if (c == 0 && r == 0) {
+                int first_slot = -1, c_hi = -1;
+                if (nt > 0) {
+                    // the clusters whose ranges hold tiles pre .. pre + nt - 1
+                    long long lo = ((pre + 1) * C + W - 1) / W - 1;
+                    long long hi = ((pre + nt) * C + W - 1) / W - 1;
+                    lo = lo < 0 ? 0 : (lo > C - 1 ? C - 1 : lo);
+                    hi = hi < lo ? lo : (hi > C - 1 ? C - 1 : hi);
+                    first_slot = 2 * (int)lo + ((lo * W / C) == pre ? 0 : 1);
+                    c_hi = (int)hi;
+                }
+                p.meta[2 * b] = first_slot;
+                p.meta[2 * b + 1] = c_hi;
+            }
             if (gb < W && gb >= pre && gb < pre + nt) {
                 s_start_b = b;
                 s_start_t = (int)(gb - pre);
             }
             pre += nt;
         }
-        if (lane == 31) {
-            s_W = W;
-            if (c == 0 && r == 0) p.meta[p.B] = (int)W;
-        }
+        if (lane == 31) s_W = W;
     }
 
     if (tid == 32) {
@@ -256,9 +290,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.pf(i), kSoftmaxThreads / 32);
             mbar_init(bars.pe(i), 1);
+            mbar_init(bars.xf(i), 1);
+            mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
+            mbar_init(bars.lf(i), 1);
         }
-        mbar_init(bars.x_full, 1);
-        mbar_init(bars.x_free, kSoftmaxThreads / 32);   // one remote arrive per peer softmax warp
+        mbar_init(bars.pin_full, 1);
+        mbar_init(bars.pin_free, 8);     // one remote arrive per peer agent warp
         mbar_init(bars.q_full, 1);
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.o_full, 1);
@@ -279,6 +316,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
     const int n_local = (int)(g_end - g_begin);   // tiles of this cluster
     const int start_b = s_start_b, start_t = s_start_t;
+
+    if (n_local == 0 && warp >= 2) {
+        // an empty range: its partial slots must not contribute to any merge
+        const int h = tid - 64;
+        if (r == 0 && h < kHeads) {
+            p.lse_part[(size_t)(2 * c) * kHeads + h] = -INFINITY;
+            p.lse_part[(size_t)(2 * c + 1) * kHeads + h] = -INFINITY;
+        }
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -407,26 +453,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------------ softmax warps
-        // 16 warps.  Lane group lg = warp % 4: the TMEM lanes the warp may access, i.e. heads
-        // 32 lg .. 32 lg + 31 (thread = head).  Slice ts = (warp - 2) / 4: positions
-        // 16 ts .. 16 ts + 15 of every page, and O columns 64 ts .. 64 ts + 63 in corrections and
-        // epilogues.
+        // ------------------------------------------------------------------ owners and agents
+        // Lane group lg = warp % 4 (the TMEM lanes this warp may access: heads 32 lg .. 32 lg + 31,
+        // thread = head), slice ts = (warp - 2) / 4 (positions 16 ts .. 16 ts + 15 of a page, and
+        // O columns 64 ts .. 64 ts + 63 in corrections and epilogues).  Lane groups 2r, 2r + 1
+        // hold the owned heads.
         //
-        // The 16 warps meet at named barriers, which cannot time out, so this loop never leaves
-        // early: after a failed (bounded) wait it keeps executing every barrier but skips the
-        // work, and waits return at once.  Wait results are made warp-uniform before any
-        // warp-collective tcgen05 instruction.
+        // The four owner warps of a lane group meet at named barriers (ids 1 + lg, 5 + lg, 128
+        // threads), which cannot time out, so these loops never leave early: after a failed
+        // (bounded) wait they keep executing every barrier but skip the work, and waits return at
+        // once.  Wait results are made warp-uniform before any warp-collective tcgen05 instruction.
         const int lg = warp & 3;
         const int ts = (warp - 2) >> 2;
         const int h = lg * 32 + lane;
+        const bool owner = (lg >> 1) == (int)r;
+        const int hh = h & (kOwned - 1);   // index among the owning CTA's heads
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-        const uint32_t x_remote = mapa(sbase + kOffX, peer);
-        const uint32_t xfull_remote = mapa(bars.x_full, peer);
-        const uint32_t xfree_remote = mapa(bars.x_free, peer);
-        const bool leader = (tid == 64);
         float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][128 heads]
-        float m_used = -INFINITY, l_part = 0.f;
 
         auto wwait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
             bool ok = !s_abort && mbar_wait(bar, parity, wait_limit);
@@ -435,170 +478,257 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             return ok;
         };
 
+        // this CTA's partial scores of page i for the warp's 16 positions (TMEM -> registers)
+        auto load_s = [&](int i, uint32_t (&v)[16]) -> bool {
+            const int sb = i % kNSB;
+            if (!wwait(bars.sf(sb), (i / kNSB) & 1, 7)) return false;
+            tc_fence_after();
+            tmem_ld16(tmem + lane_off + kTmemS + sb * kT + kSlice * ts, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.se(sb));
+            return true;
+        };
+
+        // O rows of this warp (its 64 columns) times alpha, once PV of page i - 1 has completed
+        auto rescale_o = [&](int i, float alpha) {
+            if (!wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) return;
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                const uint32_t col = kTmemO + 64 * ts + 32 * cc;
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + col, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                tmem_st32(tmem + lane_off + col, o);
+            }
+            tmem_wait_st();
+        };
+
+        // the warp's 16 P values of page i into tensor memory, then P ready for the MMA
+        auto store_p = [&](int i, const uint32_t (&pk)[8]) {
+            const int pb = i & 1;
+            if (i >= 2 && !wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11)) return;
+            tmem_st8(tmem + lane_off + kTmemP + 32 * pb + 8 * ts, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
+        };
+
+        // O rows of this warp normalised by l (row sum) into the output or a partial slot
+        auto epilogue_rows = [&](int seg, const Cursor& cu, bool partial, float l_row) {
+            const int slot = 2 * c + (seg == 0 ? 0 : 1);
+            if (!wwait(bars.o_full, seg & 1, 12)) return;
+            tc_fence_after();
+            const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
+            const size_t row = (size_t)cu.b * kHeads + h;
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + kTmemO + 64 * ts + 32 * cc, o);
+                tmem_wait_ld();
+                const int col = (int)r * kHalfLat + 64 * ts + 32 * cc;
+                if (!partial) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.o_free);
+        };
+
         Cursor cu;
         cu.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
         int seg = 0;
         bool cut_front = false;
-        for (int i = 0; i < n_local; ++i, cu.next()) {
-            const int sb = i % kNSB, pb = i & 1;
-            const bool first = cu.first(g_begin);
-            if (first) {
-                m_used = -INFINITY;
-                l_part = 0.f;
-                cut_front = cu.t > 0;   // the request started before this cluster's range
-            }
-            // this CTA's partial scores of the warp's 16 positions: TMEM -> registers -> peer
-            uint32_t v[16];
-            const bool sok = wwait(bars.sf(sb), (i / kNSB) & 1, 7);
-            if (sok) {
-                tc_fence_after();
-                tmem_ld16(tmem + lane_off + kTmemS + sb * kT + kSlice * ts, v);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.se(sb));
-            }
-            if (wwait(bars.x_free, (i & 1) ^ 1, 8)) {
+
+        if (!owner) {
+            // ------------------------------------------------------------ agents
+            const uint32_t x_remote = mapa(sbase + kOffX, peer);
+            const uint32_t xfull_remote = mapa(bars.x_full, peer);
+            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
+            const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
+            // forward this CTA's partial scores of page i (the peer's heads) to the peer
+            auto forward = [&](int i) {
+                uint32_t v[16];
+                if (!load_s(i, v)) return;
+                const int xb = i & 1;
+                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) return;
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                    st_async_v4(x_remote + ((4 * ts + g) * 128 + h) * 16, xfull_remote, v[4 * g],
-                                v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-            }
-            // full scores = own partial + the peer's (the same fp32 sum in both CTAs, so both
-            // take identical decisions)
-            if (leader && !s_abort) mbar_arrive_expect_tx(bars.x_full, kXBytes);
-            const bool xok = wwait(bars.x_full, i & 1, 9);
-            const int nv = min(kT, cu.n - cu.t * kT) - kSlice * ts;   // valid positions here
-            float x[16];
-            float mx = -INFINITY;
-            const uint8_t* xp = sm + kOffX;
+                    st_async_v4(x_remote + xb * kXBytes + ((4 * ts + g) * kOwned + hh) * 16,
+                                xfull_remote + 8 * xb, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            };
+            if (n_local > 0) forward(0);
+            for (int i = 0; i < n_local; ++i, cu.next()) {
+                if (i + 1 < n_local) forward(i + 1);
+                const bool first = cu.first(g_begin);
+                if (first) cut_front = cu.t > 0;
+                // the peer's P of its heads for page i, and its rescale factors
+                if (lead && !s_abort) mbar_arrive_expect_tx(bars.pin_full, kPInMsg);
+                const bool ok = wwait(bars.pin_full, i & 1, 13);
+                uint32_t pk[8];
+                const uint8_t* pin = sm + kOffPIn;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * 128 + h) * 16);
-                x[4 * g] = __uint_as_float(v[4 * g]) + q.x;
-                x[4 * g + 1] = __uint_as_float(v[4 * g + 1]) + q.y;
-                x[4 * g + 2] = __uint_as_float(v[4 * g + 2]) + q.z;
-                x[4 * g + 3] = __uint_as_float(v[4 * g + 3]) + q.w;
-            }
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-                if (t < nv) mx = fmaxf(mx, x[t]);
-            // every loaded value has been consumed: hand the exchange buffer back to the peer
-            __syncwarp();
-            if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote);
-            const float mx2 = mx * p.scale_log2;
-            const bool need = first || mx2 > m_used + kLazySlack;
-            if (bar_red_or(1, kSoftmaxThreads, need)) {
-                // rare path (and every segment start): exact page row max over the four slices,
-                // new running max where it grew past the slack, O and partial sums rescaled
-                red[ts * 128 + h] = mx2;
-                named_bar_sync(2, kSoftmaxThreads);
-                const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
-                const bool grow = first || tmax > m_used + kLazySlack;
-                const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
-                if (!first) {
-                    const float alpha = grow ? ex2(m_used - m_new) : 1.0f;
-                    if (__any_sync(0xffffffffu, grow) && wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) {
-                        tc_fence_after();
-#pragma unroll 1
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const uint32_t col = kTmemO + 64 * ts + 32 * cc;
-                            uint32_t o[32];
-                            tmem_ld32(tmem + lane_off + col, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                            tmem_st32(tmem + lane_off + col, o);
-                        }
-                        tmem_wait_st();
-                    }
-                    l_part *= alpha;
+                for (int g = 0; g < 2; ++g) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(pin + ((2 * ts + g) * kOwned + hh) * 16);
+                    pk[4 * g] = q.x;
+                    pk[4 * g + 1] = q.y;
+                    pk[4 * g + 2] = q.z;
+                    pk[4 * g + 3] = q.w;
                 }
-                m_used = m_new;
-                named_bar_sync(2, kSoftmaxThreads);   // red[] is free again
-            }
-            // P = 2^(x * scale * log2 e - m) for this warp's positions, packed to bf16
-            const float nm = -m_used;
-            float psum = 0.f;
-            uint32_t pk[8];
-#pragma unroll
-            for (int t = 0; t < 16; t += 2) {
-                float p0 = 0.f, p1 = 0.f;
-                if (m_used != -INFINITY) {
-                    p0 = t < nv ? ex2(fmaf(x[t], p.scale_log2, nm)) : 0.f;
-                    p1 = t + 1 < nv ? ex2(fmaf(x[t + 1], p.scale_log2, nm)) : 0.f;
-                }
-                psum += p0 + p1;
-                pk[t / 2] = pack_bf16x2(p0, p1);
-            }
-            l_part += psum;
-            // positions past the end of the request: zero their V rows so that 0 * (stale bytes)
-            // cannot poison O (QK of this page has completed, PV has not started)
-            const int nvalid = min(kT, cu.n - cu.t * kT);
-            if (nvalid < kT && sok) {
-                uint8_t* st = sm + kOffKv + (i % kNS) * kStageBytes;
-                const int nrows = kT - nvalid;
-                for (int e = tid - 64; e < nrows * 4 * 8; e += kSoftmaxThreads) {
-                    const int row = nvalid + e / 32, k = (e / 8) % 4, part = e % 8;
-                    *reinterpret_cast<uint4*>(st + k * kKvLatChunk + row * 128 + part * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            // P of this warp's 16 positions into tensor memory once PV of tile i - 2 released it
-            if (i < 2 || wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11)) {
-                tmem_st8(tmem + lane_off + kTmemP + 32 * pb + 8 * ts, pk);
-                tmem_wait_st();
-                tc_fence_before();
+                const float alpha = reinterpret_cast<const float*>(pin + kPInBytes)[hh];
                 __syncwarp();
-                if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
-            }
-
-            if (cu.last()) {
-                // ------------------------------------------------------ segment epilogue
-                const bool partial = cut_front || cu.t < cu.nt - 1;
-                const int slot = 2 * c + (seg == 0 ? 0 : 1);
-                red[ts * 128 + h] = l_part;
-                named_bar_sync(2, kSoftmaxThreads);
-                const float l_row = (red[h] + red[128 + h]) + (red[256 + h] + red[384 + h]);
-                named_bar_sync(2, kSoftmaxThreads);
-                if (wwait(bars.o_full, seg & 1, 12)) {
-                    tc_fence_after();
-                    const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
-                    const float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
-                    const size_t row = (size_t)cu.b * kHeads + h;
-#pragma unroll 1
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_off + kTmemO + 64 * ts + 32 * cc, o);
-                        tmem_wait_ld();
-                        const int col = (int)r * kHalfLat + 64 * ts + 32 * cc;
-                        if (!partial) {
-                            uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                dst[k] = make_uint4(
-                                    pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
-                        } else {
-                            float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
-#pragma unroll
-                            for (int k = 0; k < 8; ++k)
-                                dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                                     __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
-                        }
-                    }
-                    if (r == 0 && ts == 0) {
-                        if (!partial) p.lse[row] = L;
-                        else p.lse_part[(size_t)slot * kHeads + h] = L;
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars.o_free);
+                if (lane == 0 && ok) mbar_arrive_remote_relaxed(pinfree_remote);
+                if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha);
+                store_p(i, pk);
+                if (cu.last()) {
+                    const bool partial = cut_front || cu.t < cu.nt - 1;
+                    // the row sums of these heads, sent by the peer's owners
+                    if (lead && !s_abort) mbar_arrive_expect_tx(bars.lf(seg & 1), kOwned * 4);
+                    const bool lok = wwait(bars.lf(seg & 1), (seg >> 1) & 1, 14);
+                    const float l_row = lok ? reinterpret_cast<const float*>(sm + kOffLIn)[(seg & 1) * kOwned + hh] : 0.f;
+                    epilogue_rows(seg, cu, partial, l_row);
+                    ++seg;
                 }
-                ++seg;
+            }
+        } else {
+            // ------------------------------------------------------------ owners
+            const uint32_t pin_remote = mapa(sbase + kOffPIn, peer);
+            const uint32_t pinfull_remote = mapa(bars.pin_full, peer);
+            const uint32_t xfree_remote = mapa(bars.x_free, peer);
+            const uint32_t lin_remote = mapa(sbase + kOffLIn, peer);
+            const uint32_t lfull_remote = mapa(bars.l_full, peer);
+            const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
+            const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
+            float m_used = -INFINITY, l_part = 0.f;
+            for (int i = 0; i < n_local; ++i, cu.next()) {
+                const int xb = i & 1;
+                const bool first = cu.first(g_begin);
+                if (first) {
+                    m_used = -INFINITY;
+                    l_part = 0.f;
+                    cut_front = cu.t > 0;   // the request started before this cluster's range
+                }
+                uint32_t v[16];
+                const bool sok = load_s(i, v);
+                // the peer's partial scores of these heads for page i
+                if (lead && !s_abort) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
+                const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
+                const int nv = min(kT, cu.n - cu.t * kT) - kSlice * ts;   // valid positions here
+                float x[16];
+                float mx = -INFINITY;
+                const uint8_t* xp = sm + kOffX + xb * kXBytes;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * kOwned + hh) * 16);
+                    x[4 * g] = (__uint_as_float(v[4 * g]) + q.x) * p.scale_log2;
+                    x[4 * g + 1] = (__uint_as_float(v[4 * g + 1]) + q.y) * p.scale_log2;
+                    x[4 * g + 2] = (__uint_as_float(v[4 * g + 2]) + q.z) * p.scale_log2;
+                    x[4 * g + 3] = (__uint_as_float(v[4 * g + 3]) + q.w) * p.scale_log2;
+                }
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    if (t < nv) mx = fmaxf(mx, x[t]);
+                // every loaded value has been consumed: hand the exchange buffer back to the peer
+                __syncwarp();
+                if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote + 8 * xb);
+                float alpha = 1.0f;
+                const bool need = first || mx > m_used + kLazySlack;
+                if (bar_red_or(bar_vote, 128, need)) {
+                    // rare path (and every segment start): exact page row max over the four
+                    // slices, new running max where it grew past the slack, O rescaled here and,
+                    // through alpha sent with P, in the peer
+                    red[ts * 128 + h] = mx;
+                    named_bar_sync(bar_sync, 128);
+                    const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
+                    const bool grow = first || tmax > m_used + kLazySlack;
+                    const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
+                    if (!first) {
+                        alpha = grow ? ex2(m_used - m_new) : 1.0f;
+                        if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha);
+                        l_part *= alpha;
+                    }
+                    m_used = m_new;
+                    named_bar_sync(bar_sync, 128);   // red[] rows of this lane group are free again
+                }
+                // P = 2^(x - m) for this warp's positions, packed to bf16
+                float psum = 0.f;
+                uint32_t pk[8];
+#pragma unroll
+                for (int t = 0; t < 16; t += 2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    if (m_used != -INFINITY) {
+                        p0 = t < nv ? ex2(x[t] - m_used) : 0.f;
+                        p1 = t + 1 < nv ? ex2(x[t + 1] - m_used) : 0.f;
+                    }
+                    psum += p0 + p1;
+                    pk[t / 2] = pack_bf16x2(p0, p1);
+                }
+                l_part += psum;
+                // positions past the end of the request: zero their V rows so that
+                // 0 * (stale bytes) cannot poison O (QK of this page has completed, PV has not
+                // started); the owner warps of both lane groups share the rows
+                const int nvalid = min(kT, cu.n - cu.t * kT);
+                if (nvalid < kT && sok) {
+                    uint8_t* st = sm + kOffKv + (i % kNS) * kStageBytes;
+                    const int nrows = kT - nvalid;
+                    const int ot = (lg & 1) * 128 + ts * 32 + lane;   // 0 .. 255 over the owners
+                    for (int e = ot; e < nrows * 4 * 8; e += 256) {
+                        const int row = nvalid + e / 32, k = (e / 8) % 4, part = e % 8;
+                        *reinterpret_cast<uint4*>(st + k * kKvLatChunk + row * 128 + part * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                // P of these heads to the peer (its P input), once it has taken the previous one
+                if (wwait(bars.pin_free, (i & 1) ^ 1, 15)) {
+#pragma unroll
+                    for (int g = 0; g < 2; ++g)
+                        st_async_v4(pin_remote + ((2 * ts + g) * kOwned + hh) * 16, pinfull_remote,
+                                    pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+                    if (ts == 0)
+                        st_async_b32(pin_remote + kPInBytes + hh * 4, pinfull_remote, __float_as_uint(alpha));
+                }
+                store_p(i, pk);
+
+                if (cu.last()) {
+                    // ------------------------------------------------------ segment epilogue
+                    const bool partial = cut_front || cu.t < cu.nt - 1;
+                    red[ts * 128 + h] = l_part;
+                    named_bar_sync(bar_sync, 128);
+                    const float l_row = (red[h] + red[128 + h]) + (red[256 + h] + red[384 + h]);
+                    named_bar_sync(bar_sync, 128);
+                    // the row sums of these heads to the peer, which finishes its O rows of them
+                    if (ts == 0 && !s_abort)
+                        st_async_b32(lin_remote + ((seg & 1) * kOwned + hh) * 4,
+                                     lfull_remote + 8 * (seg & 1), __float_as_uint(l_row));
+                    const float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
+                    if (ts == 0) {
+                        const size_t row = (size_t)cu.b * kHeads + h;
+                        if (!partial) p.lse[row] = L;
+                        else p.lse_part[(size_t)(2 * c + (seg == 0 ? 0 : 1)) * kHeads + h] = L;
+                    }
+                    epilogue_rows(seg, cu, partial, l_row);
+                    ++seg;
+                }
             }
         }
     }
@@ -607,7 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1 && lane == 0 && n_local > 0) {
         // all MMAs issued by this thread are complete once this barrier flips
         mma_commit(bars.mma_drain);
-        if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 13);
+        if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
     }
     __syncwarp();
     if (s_abort) __nanosleep(100000);   // let any in-flight distributed-shared-memory stores land
@@ -618,54 +748,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge of the partials of requests cut by cluster range boundaries.  Block (request b, head h);
-// a request that lies inside one range was finished by the decode kernel and is skipped.  The
-// partial of request b made by cluster c sits in slot 2c when b reaches back to c's range start,
-// else (b starts inside c's range and runs past its end) in slot 2c + 1.
+// Finish of mla_decode: requests cut by cluster range boundaries get their partials merged,
+// requests with no visible position get zeros and lse = -inf; the rest were finished by the
+// decode kernel.  Block (request b, head h).  Request b's partials sit in slot first (2 c_lo or
+// 2 c_lo + 1) and slots 2c for the following clusters c up to c_hi.
 __global__ void __launch_bounds__(128) merge_slots_kernel(const float* __restrict__ o_part,
                                                           const float* __restrict__ lse_part,
-                                                          const int32_t* __restrict__ meta, int B, int C,
+                                                          const int32_t* __restrict__ meta,
                                                           __nv_bfloat16* __restrict__ out,
                                                           float* __restrict__ lse) {
     const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
-    const long long W = meta[B];
-    const long long T0 = meta[b], T1 = meta[b + 1];
-    if (T1 <= T0 || W <= 0) return;   // no tiles: nothing to merge
-    int c_lo = (int)((T0 * C) / W);
-    while (c_lo > 0 && (long long)c_lo * W / C > T0) --c_lo;
-    while (c_lo + 1 < C && (long long)(c_lo + 1) * W / C <= T0) ++c_lo;
-    int c_hi = c_lo;
-    while (c_hi + 1 < C && (long long)(c_hi + 1) * W / C < T1) ++c_hi;
-    if (c_hi == c_lo) return;         // the whole request lies in one range: already final
-    float m = -INFINITY;
-    for (int cc = c_lo; cc <= c_hi; ++cc) {
-        const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
-        if (re <= rb) continue;
-        const int slot = 2 * cc + (T0 <= rb ? 0 : 1);
-        m = fmaxf(m, lse_part[(size_t)slot * kHeads + h]);
-    }
+    const int first = meta[2 * b], c_hi = meta[2 * b + 1];
+    const int c_lo = first >> 1;
+    if (first >= 0 && c_hi == c_lo) return;   // inside one range: already final
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;
-    if (m != -INFINITY) {
-        float l = 0.f;
-        for (int cc = c_lo; cc <= c_hi; ++cc) {
-            const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
-            if (re <= rb) continue;
-            const int slot = 2 * cc + (T0 <= rb ? 0 : 1);
-            l += expf(lse_part[(size_t)slot * kHeads + h] - m);
+    if (first >= 0) {
+        const int n = c_hi - c_lo + 1;
+        float m = -INFINITY;
+        for (int k = 0; k < n; ++k) {
+            const int slot = k == 0 ? first : 2 * (c_lo + k);
+            m = fmaxf(m, lse_part[(size_t)slot * kHeads + h]);
         }
-        L = m + logf(l);
-        for (int cc = c_lo; cc <= c_hi; ++cc) {
-            const long long rb = (long long)cc * W / C, re = (long long)(cc + 1) * W / C;
-            if (re <= rb) continue;
-            const int slot = 2 * cc + (T0 <= rb ? 0 : 1);
-            const float w = expf(lse_part[(size_t)slot * kHeads + h] - L);
-            if (w == 0.f) continue;
-            const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)slot * kHeads + h) * kDc)[threadIdx.x];
-            acc.x += w * o.x;
-            acc.y += w * o.y;
-            acc.z += w * o.z;
-            acc.w += w * o.w;
+        if (m != -INFINITY) {
+            float l = 0.f;
+            for (int k = 0; k < n; ++k) {
+                const int slot = k == 0 ? first : 2 * (c_lo + k);
+                l += expf(lse_part[(size_t)slot * kHeads + h] - m);
+            }
+            L = m + logf(l);
+            for (int k = 0; k < n; ++k) {
+                const int slot = k == 0 ? first : 2 * (c_lo + k);
+                const float w = expf(lse_part[(size_t)slot * kHeads + h] - L);
+                if (w == 0.f) continue;
+                const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)slot * kHeads + h) * kDc)[threadIdx.x];
+                acc.x += w * o.x;
+                acc.y += w * o.y;
+                acc.z += w * o.z;
+                acc.w += w * o.w;
+            }
         }
     }
     uint2 packed;
@@ -673,16 +794,6 @@ __global__ void __launch_bounds__(128) merge_slots_kernel(const float* __restric
     packed.y = pack_bf16x2(acc.z, acc.w);
     reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc)[threadIdx.x] = packed;
     if (threadIdx.x == 0) lse[(size_t)b * kHeads + h] = L;
-}
-
-// Requests with no visible position get zeros and lse = -inf (they own no tiles).
-__global__ void __launch_bounds__(128) empty_rows_kernel(const int32_t* __restrict__ seq_lens,
-                                                         int max_len, __nv_bfloat16* __restrict__ out,
-                                                         float* __restrict__ lse) {
-    const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
-    if (clamp_len(seq_lens[b], max_len) > 0) return;
-    reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc)[threadIdx.x] = make_uint2(0u, 0u);
-    if (threadIdx.x == 0) lse[(size_t)b * kHeads + h] = -INFINITY;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -721,7 +832,7 @@ int clusters_for(int B, int max_seq_len, int sms) {
 }  // namespace
 
 // Workspace of the tensor-core path: 2 partial slots per cluster (fp32 [128][512] + lse [128]),
-// then the tile offsets of the requests and the tile total (int32 [B + 1]).
+// then per request its first partial slot and last cluster (int32 [B][2]).
 DecodePlan plan_decode_tc(int fmt, int B, int max_seq_len, int topk, int sms) {
     (void)fmt;
     (void)topk;
@@ -729,9 +840,9 @@ DecodePlan plan_decode_tc(int fmt, int B, int max_seq_len, int topk, int sms) {
     const int C = clusters_for(B, max_seq_len, sms);
     p.splits = C;
     p.chunk = 0;
-    p.workspace = (size_t)2 * C * kHeads * (kDc + 1) * sizeof(float) + (size_t)(B + 1) * sizeof(int32_t);
+    p.workspace = (size_t)2 * C * kHeads * (kDc + 1) * sizeof(float) + (size_t)2 * B * sizeof(int32_t);
     p.workspace = (p.workspace + 255) / 256 * 256;
-    p.launches = 3;
+    p.launches = 2;
     return p;
 }
 
@@ -778,11 +889,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const int64_t blocks = (int64_t)a.B * kHeads;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-    empty_rows_kernel<<<(unsigned)blocks, 128, 0, st>>>(a.seq_lens, a.max_seq_len, a.out, a.lse);
     decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    merge_slots_kernel<<<(unsigned)blocks, 128, 0, st>>>(o_part, lse_part, meta, a.B, C, a.out, a.lse);
+    merge_slots_kernel<<<(unsigned)blocks, 128, 0, st>>>(o_part, lse_part, meta, a.out, a.lse);
     return cudaGetLastError();
 }
 
