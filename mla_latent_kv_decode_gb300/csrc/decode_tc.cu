@@ -377,10 +377,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_local > 0) {
+        // The whole warp runs this loop so that its operands stay warp-uniform (cheap to issue);
+        // one elected lane issues each MMA and commit.
+        if (n_local > 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, kT, 0, 0);
             constexpr uint32_t id_pv = idesc_bf16(128, kHalfLat, 0, 1);
-            const uint32_t q_lat = sbase + kOffQ, q_rope = sbase + kOffQRope;
+            // descriptor words: the low word carries the start address (bits 4..17 of the shared
+            // address), so an offset inside a buffer is a 32-bit add to a masked base; the high
+            // word (stride, version, swizzle) is constant
+            const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
+            const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
+            const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
+            const uint32_t lat_lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
+            const uint32_t rope_lo = (uint32_t)smem_desc(0, 16, 512, kSw64);
+            const uint32_t v_lo = (uint32_t)smem_desc(0, kKvLatChunk, 1024, kSw128);
+            const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
+            const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
             Cursor cq, cp;
             cq.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
             cp = cq;
@@ -388,33 +400,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t polls = 0;
             // Poll both queues: issue the next QK (up to kQKAhead tiles ahead of PV) when its
             // inputs are ready, else the next PV when its P is ready, so that neither a late KV
-            // stage nor the next request's Q can hold back a PV.
-            while (ip < n_local && !s_abort) {
+            // stage nor the next request's Q can hold back a PV.  Lane 0's view of the barriers
+            // decides for the warp.
+            while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
                 if (iq < n_local && iq <= ip + kQKAhead) {
                     const int s = iq % kNS, sb = iq % kNSB;
-                    const bool ready = (!cq.first(g_begin) || mbar_test(bars.q_full, seg_q & 1)) &&
-                                       mbar_test(bars.kvf(s), (iq / kNS) & 1) &&
-                                       mbar_test(bars.se(sb), ((iq / kNSB) & 1) ^ 1);
+                    const bool ready = __shfl_sync(
+                        0xffffffffu,
+                        (!cq.first(g_begin) || mbar_test(bars.q_full, seg_q & 1)) &&
+                            mbar_test(bars.kvf(s), (iq / kNS) & 1) &&
+                            mbar_test(bars.se(sb), ((iq / kNSB) & 1) ^ 1),
+                        0);
                     if (ready) {
                         tc_fence_after();
-                        const uint32_t st = sbase + kOffKv + s * kStageBytes;
+                        const uint32_t st_lo = ((sbase + kOffKv + s * kStageBytes) >> 4) & 0x3FFF;
                         const uint32_t d = tmem + kTmemS + sb * kT;
+                        if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
+                            for (int k = 0; k < 4; ++k)
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16_ss(d, smem_desc(q_lat + k * kQLatChunk + kk * 32, 16, 1024, kSw128),
-                                            smem_desc(st + k * kKvLatChunk + kk * 32, 16, 1024, kSw128),
-                                            id_qk, (k | kk) != 0 ? 1u : 0u);
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_bf16_ss(d, lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
+                                                lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
+                                                id_qk, (k | kk) != 0 ? 1u : 0u);
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-                            mma_bf16_ss(d, smem_desc(q_rope + kk * 32, 16, 512, kSw64),
-                                        smem_desc(st + 4 * kKvLatChunk + kk * 32, 16, 512, kSw64), id_qk, 1u);
-                        mma_commit(bars.sf(sb));
-                        if (cq.last()) {
-                            mma_commit(bars.q_empty);
-                            ++seg_q;
+                            for (int kk = 0; kk < 2; ++kk)
+                                mma_bf16_ss(d, rope_hi | (qr_lo + kk * 2),
+                                            rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
+                                            id_qk, 1u);
+                            mma_commit(bars.sf(sb));
+                            if (cq.last()) mma_commit(bars.q_empty);
                         }
+                        __syncwarp();
+                        if (cq.last()) ++seg_q;
                         cq.next();
                         ++iq;
                         polls = 0;
@@ -424,29 +442,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // PV of tile ip: O_r += P (tensor memory) x V_r (stage, MN-major)
                 const bool seg_first = cp.first(g_begin);
                 const int pb = ip & 1;
-                const bool pv_ready = (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
-                                      mbar_test(bars.pf(pb), (ip >> 1) & 1);
+                const bool pv_ready = __shfl_sync(
+                    0xffffffffu,
+                    (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
+                        mbar_test(bars.pf(pb), (ip >> 1) & 1),
+                    0);
                 if (!pv_ready) {
                     if (++polls > wait_limit) {
-                        fail(p.ctl, &s_abort, 6);
+                        if (lane == 0) fail(p.ctl, &s_abort, 6);
                         break;
                     }
                     continue;
                 }
                 polls = 0;
                 tc_fence_after();
-                const uint32_t v = sbase + kOffKv + (ip % kNS) * kStageBytes;
+                const uint32_t v = ((sbase + kOffKv + (ip % kNS) * kStageBytes) >> 4) & 0x3FFF;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
-                    mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 32 * pb + 8 * kk,
-                                smem_desc(v + kk * 16 * 128, kKvLatChunk, 1024, kSw128), id_pv,
-                                (!seg_first || kk > 0) ? 1u : 0u);
-                mma_commit(bars.pe(pb));
-                mma_commit(bars.kve(ip % kNS));
-                if (cp.last()) {
-                    mma_commit(bars.o_full);
-                    ++seg_p;
+                    for (int kk = 0; kk < kT / 16; ++kk)
+                        mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 32 * pb + 8 * kk,
+                                    v_hi | (v + v_lo + ((kk * 16 * 128) >> 4)), id_pv,
+                                    (!seg_first || kk > 0) ? 1u : 0u);
+                    mma_commit(bars.pe(pb));
+                    mma_commit(bars.kve(ip % kNS));
+                    if (cp.last()) mma_commit(bars.o_full);
                 }
+                __syncwarp();
+                if (cp.last()) ++seg_p;
                 cp.next();
                 ++ip;
             }
@@ -634,7 +656,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
                 const int nv = min(kT, cu.n - cu.t * kT) - kSlice * ts;   // valid positions here
                 float x[16];
-                float mx = -INFINITY;
                 const uint8_t* xp = sm + kOffX + xb * kXBytes;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
@@ -644,18 +665,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     x[4 * g + 2] = (__uint_as_float(v[4 * g + 2]) + q.z) * p.scale_log2;
                     x[4 * g + 3] = (__uint_as_float(v[4 * g + 3]) + q.w) * p.scale_log2;
                 }
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (t < nv) mx = fmaxf(mx, x[t]);
                 // every loaded value has been consumed: hand the exchange buffer back to the peer
                 __syncwarp();
                 if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote + 8 * xb);
+                // P = 2^(x - m) for this warp's positions, packed to bf16, with the running max m.
+                // m is kept while every P of a row stays at most 2^16, so the common page needs no
+                // row max: a thread whose 16 P sum past 2^16 (or not to a finite value) votes for
+                // the rare path, as does every segment start.  There the exact page row max over
+                // the four slices raises m where it exceeds m by more than the slack, O is rescaled
+                // here and, through alpha sent with P, in the peer, and P is computed again.
                 float alpha = 1.0f;
-                const bool need = first || mx > m_used + kLazySlack;
+                float psum;
+                uint32_t pk[8];
+                auto exp_page = [&]() {
+                    psum = 0.f;
+#pragma unroll
+                    for (int t = 0; t < 16; t += 2) {
+                        float p0 = 0.f, p1 = 0.f;
+                        if (m_used != -INFINITY) {
+                            p0 = t < nv ? ex2(x[t] - m_used) : 0.f;
+                            p1 = t + 1 < nv ? ex2(x[t + 1] - m_used) : 0.f;
+                        }
+                        psum += p0 + p1;
+                        pk[t / 2] = pack_bf16x2(p0, p1);
+                    }
+                };
+                exp_page();
+                const bool need = first || !(psum <= 65536.0f);
                 if (bar_red_or(bar_vote, 128, need)) {
-                    // rare path (and every segment start): exact page row max over the four
-                    // slices, new running max where it grew past the slack, O rescaled here and,
-                    // through alpha sent with P, in the peer
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if (t < nv) mx = fmaxf(mx, x[t]);
                     red[ts * 128 + h] = mx;
                     named_bar_sync(bar_sync, 128);
                     const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
@@ -668,19 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     m_used = m_new;
                     named_bar_sync(bar_sync, 128);   // red[] rows of this lane group are free again
-                }
-                // P = 2^(x - m) for this warp's positions, packed to bf16
-                float psum = 0.f;
-                uint32_t pk[8];
-#pragma unroll
-                for (int t = 0; t < 16; t += 2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    if (m_used != -INFINITY) {
-                        p0 = t < nv ? ex2(x[t] - m_used) : 0.f;
-                        p1 = t + 1 < nv ? ex2(x[t + 1] - m_used) : 0.f;
-                    }
-                    psum += p0 + p1;
-                    pk[t / 2] = pack_bf16x2(p0, p1);
+                    exp_page();
                 }
                 l_part += psum;
                 // positions past the end of the request: zero their V rows so that
@@ -734,10 +763,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------------- teardown
-    if (warp == 1 && lane == 0 && n_local > 0) {
-        // all MMAs issued by this thread are complete once this barrier flips
-        mma_commit(bars.mma_drain);
-        if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
+    if (warp == 1 && n_local > 0) {
+        __syncwarp();
+        // all MMAs issued by the elected lane (the lowest active one, as in the loop) are complete
+        // once this barrier flips
+        if (elect_one()) {
+            mma_commit(bars.mma_drain);
+            if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
+        }
     }
     __syncwarp();
     if (s_abort) __nanosleep(100000);   // let any in-flight distributed-shared-memory stores land
