@@ -1,0 +1,143 @@
+// decode_common.cuh -- pieces shared by the tensor-core decode kernels: the balanced tile
+// schedule over a batch, the cursor that walks a cluster's tiles request by request, and small
+// device helpers.
+#pragma once
+
+#include <cuda.h>
+
+#include "mla_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace dc {
+
+constexpr int kT = 64;                  // positions per tile (a cache page, or 64 top-k entries)
+constexpr int kMinTilesPerCluster = 4;
+
+__device__ __forceinline__ void fail(DevCtl* ctl, volatile int* abort_flag, int where) {
+    *abort_flag = 1;
+    record_error(ctl, MLA_ERR_TIMEOUT, where);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ int clamp_len(int n, int max_len) {
+    return n < 0 ? 0 : (n > max_len ? max_len : n);
+}
+
+// Tiles of request b: its visible positions in pages of 64 (dense), or its top-k list in groups
+// of 64 entries (sparse: the list length is the same for every request).
+__device__ __forceinline__ int tiles_of(int n, int topk) {
+    return topk > 0 ? (topk + kT - 1) / kT : (n + kT - 1) / kT;
+}
+
+// Walks the tiles of one cluster's range: request b, tile t of that request, local tile index j
+// of n_loc.  Six ints (the request table and limits are passed in), as several copies stay live in
+// the softmax warps' registers.
+struct Cursor {
+    int b, t, nt, n;   // request, its tile, its tiles, its visible positions
+    int j, n_loc;      // local tile index, tiles in the range
+    __device__ __forceinline__ void load_req(const int32_t* seq_lens, int max_len, int topk) {
+        n = clamp_len(seq_lens[b], max_len);
+        nt = tiles_of(n, topk);
+    }
+    __device__ __forceinline__ void init(const int32_t* seq_lens, int max_len, int topk, int b0, int t0,
+                                         int n_local) {
+        b = b0, t = t0, j = 0, n_loc = n_local;
+        if (n_loc > 0) load_req(seq_lens, max_len, topk);
+        else n = nt = 0;
+    }
+    __device__ __forceinline__ bool first() const { return t == 0 || j == 0; }
+    __device__ __forceinline__ bool last() const { return t == nt - 1 || j == n_loc - 1; }
+    __device__ __forceinline__ void next(const int32_t* seq_lens, int max_len, int B, int topk) {
+        ++j;
+        ++t;
+        if (j >= n_loc) return;
+        while (t >= nt && b + 1 < B) {
+            ++b;
+            t = 0;
+            load_req(seq_lens, max_len, topk);
+        }
+    }
+};
+
+// The balanced schedule, run by one warp of every CTA: W = sum over requests of their tiles;
+// cluster c of C takes tiles [c W / C, (c + 1) W / C).  Returns W and this cluster's first tile
+// (request, tile).  Cluster 0's rank-0 CTA also records, per request, where its partials are:
+// meta[2b] = the first partial slot (2 c_lo or 2 c_lo + 1; -1 for a request with no tiles),
+// meta[2b + 1] = the last cluster whose range holds one of its tiles.
+__device__ __forceinline__ void schedule_warp(const int32_t* seq_lens, int max_len, int B, int topk,
+                                              int c, int C, bool record, int32_t* meta, DevCtl* ctl,
+                                              long long* W_out, int* start_b, int* start_t) {
+    const int lane = threadIdx.x & 31;
+    const int per = (B + 31) / 32;
+    const int b_lo = min(B, lane * per), b_hi = min(B, b_lo + per);
+    long long mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int raw = seq_lens[b];
+        if ((raw < 0 || raw > max_len) && record) record_error(ctl, MLA_ERR_BOUNDS, b);
+        mine += tiles_of(clamp_len(raw, max_len), topk);
+    }
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const long long W = __shfl_sync(0xffffffffu, incl, 31);
+    const long long gb = (long long)c * W / C;
+    long long pre = incl - mine;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int nt = tiles_of(clamp_len(seq_lens[b], max_len), topk);
+        if (record) {
+            int first_slot = -1, c_hi = -1;
+            if (nt > 0) {
+                // the clusters whose ranges hold tiles pre .. pre + nt - 1
+                long long lo = ((pre + 1) * C + W - 1) / W - 1;
+                long long hi = ((pre + nt) * C + W - 1) / W - 1;
+                lo = lo < 0 ? 0 : (lo > C - 1 ? C - 1 : lo);
+                hi = hi < lo ? lo : (hi > C - 1 ? C - 1 : hi);
+                first_slot = 2 * (int)lo + ((lo * W / C) == pre ? 0 : 1);
+                c_hi = (int)hi;
+            }
+            meta[2 * b] = first_slot;
+            meta[2 * b + 1] = c_hi;
+        }
+        if (gb < W && gb >= pre && gb < pre + nt) {
+            *start_b = b;
+            *start_t = (int)(gb - pre);
+        }
+        pre += nt;
+    }
+    if (lane == 31) *W_out = W;
+}
+
+// 4 bytes into the peer's shared memory, completing tx-bytes on its barrier.
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t remote_bar, uint32_t v) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     remote_addr),
+                 "r"(v), "r"(remote_bar)
+                 : "memory");
+}
+
+// Clusters for a batch: at most one per SM pair, at least kMinTilesPerCluster tiles each.
+inline int clusters_for_tiles(long long w_max, int sms) {
+    long long c = sms / 2;
+    const long long by_work = (w_max + kMinTilesPerCluster - 1) / kMinTilesPerCluster;
+    if (by_work < c) c = by_work;
+    return c < 1 ? 1 : (int)c;
+}
+
+}  // namespace dc
+
+// Shared by the tensor-core decode kernels (defined in decode_tc.cu).
+__global__ void merge_slots_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                                   const int32_t* __restrict__ meta, __nv_bfloat16* __restrict__ out,
+                                   float* __restrict__ lse);
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+
+}  // namespace mla

@@ -1,0 +1,886 @@
+// decode_gather.cu -- tensor-core absorbed MLA decode over rows the kernel gathers itself: the
+// FP8 mixed cache (dense) and the top-k sparse path (both cache formats).
+//
+// It computes what decode_tc.cu computes ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token",
+// Fig. 4 (1), Fig. 5 (2), Fig. 6 (2)) and shares its organisation: clusters of two CTAs that
+// split the latent and rope dims (CTA r: latent [256 r, 256 r + 256), rope [32 r, 32 r + 32)),
+// the softmax split by heads between the pair (owners finish heads [64 r, 64 r + 64), agents
+// forward this CTA's partial scores of the other heads and place the P the peer sends back), the
+// lazily updated running max, the balanced tile schedule and the partial merge.  What differs is
+// where a tile's rows come from and how FP8 scales enter:
+//   * a tile is 64 rows: the positions of one cache page (dense), or 64 consecutive entries of a
+//     request's top-k list (sparse: only listed positions enter the softmax, same page, Fig. 8
+//     and the DSA description on that page).  Rows outside the request (past its length, padding
+//     entries, entries >= N_b) are masked and read as zeros;
+//   * the agent warps load each row's bytes of this CTA's half from global memory and write them
+//     into a shared-memory tile in the MMA operand layouts: bf16 latent [64 x 256] (128-byte
+//     swizzle), bf16 rope [64 x 32] (64-byte swizzle), the two fp32 group scales per row and a
+//     64-bit mask of valid rows;
+//   * FP8 records (512 e4m3 codes, one fp32 scale per 128 dims, 64 bf16 rope dims; the 656-byte
+//     layout of the same page's FP8 section) convert exactly: every e4m3 value is a bf16 value.
+//     The scale of each 128-dim group is applied in fp32 where the group meets the other factor:
+//     on the scores, S = s_a S_a + s_b S_b + S_rope with one tensor-memory accumulator per group,
+//     and on P, O_g += (P s_g) V_g for the PV of group g.  P s_g goes to the MMA as a pair of bf16
+//     values, hi = bf16(P s_g) and lo = bf16(P s_g - hi), each with its own MMA: one bf16 rounding
+//     of the scaled P (2^-9) would shift a row that dominates the softmax by that much, next to the
+//     output's own bf16 rounding.  BF16 records take scale 1.
+//
+// Tensor memory (all 512 columns): O_r [0, 256), S_a [256, 320), S_b [320, 384),
+// S_rope [384, 448), P_a [448, 480), P_b [480, 512) (the hi parts; 64 bf16 per lane in 32
+// columns).  Shared memory: Q half (72 KB, TMA), two converted tiles (36 KB each), the lo parts of
+// P s_g (2 x 16 KB, the MMA's K-major layout), exchange buffers.
+//
+// Warp roles (576 threads): warp 0 Q loads (TMA); warp 1 MMA issuer (+ TMEM owner); warps 2-17:
+// thread = head = TMEM lane, four warps per 32-lane group, 16 positions of a tile each; the 8
+// warps on the owned heads' lanes run the softmax, the other 8 ("agents") forward partial scores,
+// place the peer's P, finish those O rows and load and convert the tiles.  Every wait is bounded:
+// on expiry the kernel records MLA_ERR_TIMEOUT, stops issuing, drains its MMAs, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "decode_common.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+using namespace dc;
+
+constexpr int kNC = 2;                 // converted tile slots
+constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
+constexpr int kSlice = kT / 4;         // positions per warp
+constexpr int kThreads = 64 + kSoftmaxThreads;
+constexpr float kLazySlack = 15.0f;    // running max kept until a row max exceeds it by 2^15
+constexpr float kPMax = 32768.0f;      // 2^15: P stays within fp16 range
+constexpr int kHalfLat = 256;          // latent dims per CTA
+constexpr int kHalfRope = 32;          // rope dims per CTA
+constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256); group a [0, 128), group b [128, 256)
+constexpr uint32_t kTmemSa = 256;      // score accumulators of this CTA's two latent groups
+constexpr uint32_t kTmemSb = 320;
+constexpr uint32_t kTmemSr = 384;      // ... and of its rope dims
+constexpr uint32_t kTmemPa = 448;      // P times the group scales
+constexpr uint32_t kTmemPb = 480;
+constexpr uint32_t kDrainLimit = 1u << 20;
+
+// shared-memory layout (bytes from a 1024-aligned base)
+constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] bf16, SW128
+constexpr int kQRopeBytes = 128 * 64;                  // [128 heads x 32 dims] bf16, SW64
+constexpr int kKvLatChunk = kT * 128;                  // [64 rows x 64 dims], SW128
+constexpr int kConvBytes = 4 * kKvLatChunk + kT * 64;  // latent + rope [64 rows x 32 dims], SW64
+constexpr int kPLoBytes = 128 * kT * 2;                // lo part of P s_g [128 heads x 64 pos], SW128
+constexpr int kXBytes = kOwned * kT * 4;               // peer partial scores of owned heads, fp32
+constexpr int kPInBytes = kOwned * kT * 2;             // peer's P of its owned heads, fp16
+constexpr int kPInMsg = kPInBytes + kOwned * 4;        // + one rescale factor per head
+constexpr int kOffQ = 0;
+constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
+constexpr int kOffConv = kOffQRope + kQRopeBytes;      // 73728
+constexpr int kOffPLo = kOffConv + kNC * kConvBytes;  // 147456: groups a, b
+constexpr int kOffScale = kOffPLo + 2 * kPLoBytes;     // 180224: [kNC][64 rows][2] fp32
+constexpr int kOffMask = kOffScale + kNC * kT * 2 * 4; // 181248: [kNC][2] uint32 valid rows
+constexpr int kOffX = kOffMask + 32;                   // 181280: 2 buffers [16][64][16 B]
+constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 214048: [8][64][16 B] + alpha[64]
+constexpr int kOffLIn = kOffPIn + kPInMsg;             // 222496: 2 x l[64] of the peer's heads
+constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 223008
+constexpr int kNumBars = 2 * kNC + 4 + 2 + 2 + 2 + 2 + 5;
+constexpr int kOffRed = (kOffBar + 8 * kNumBars + 15) & ~15;   // per-head exchange between slices [4][128]
+constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 1024;       // + alignment slack
+
+constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;     // 73728 per CTA
+
+struct GatherParams {
+    const uint8_t* pool;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* topk_idx;   // [B][topk] or null (dense)
+    __nv_bfloat16* out;
+    float* lse;
+    float* o_part;             // [2C][128][512]
+    float* lse_part;           // [2C][128]
+    int32_t* meta;             // per request: first partial slot, last cluster (2 x int32)
+    DevCtl* ctl;
+    int64_t num_pages;
+    int max_pages;
+    int max_seq_len;
+    int topk;
+    int B;
+    int fp8;                   // 1: 656-byte FP8 records, 0: 1152-byte BF16 records
+    float scale_log2;          // scale * log2(e)
+};
+
+struct Bars {
+    uint32_t c_full, c_empty;     // arrays of kNC
+    uint32_t s_full, s_empty, p_full, p_empty;
+    uint32_t x_full, x_free;      // arrays of 2
+    uint32_t pin_full, pin_free;
+    uint32_t l_full;              // array of 2
+    uint32_t q_full, q_empty, o_full, o_free, mma_drain;
+    __device__ __forceinline__ uint32_t cf(int i) const { return c_full + 8 * i; }
+    __device__ __forceinline__ uint32_t ce(int i) const { return c_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
+    __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
+    __device__ __forceinline__ uint32_t lf(int i) const { return l_full + 8 * i; }
+};
+
+__device__ __forceinline__ Bars make_bars(uint32_t a) {
+    Bars b;
+    b.c_full = a; a += 8 * kNC;
+    b.c_empty = a; a += 8 * kNC;
+    b.s_full = a; a += 8;
+    b.s_empty = a; a += 8;
+    b.p_full = a; a += 8;
+    b.p_empty = a; a += 8;
+    b.x_full = a; a += 16;
+    b.x_free = a; a += 16;
+    b.pin_full = a; a += 8;
+    b.pin_free = a; a += 8;
+    b.l_full = a; a += 16;
+    b.q_full = a; a += 8;
+    b.q_empty = a; a += 8;
+    b.o_full = a; a += 8;
+    b.o_free = a; a += 8;
+    b.mma_drain = a; a += 8;
+    return b;
+}
+
+// 16 e4m3 codes (OCP 8-bit floating point, bias 7) to 16 bf16 values, exactly: each code goes
+// to f16 and then to fp32, both exact, and every such value is a bf16 value.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t (&o)[8]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __half2_raw hr =
+                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[k] >> (16 * j)) & 0xFFFFu), __NV_E4M3);
+            __half2 h2;
+            *reinterpret_cast<__half2_raw*>(&h2) = hr;
+            const float2 f = __half22float2(h2);
+            o[2 * k + j] = pack_bf16x2(f.x, f.y);
+        }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_gather_kernel(const __grid_constant__ CUtensorMap tm_qlat,
+                         const __grid_constant__ CUtensorMap tm_qrope, GatherParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ uint32_t s_tmem_base;
+    __shared__ volatile int s_abort;
+    __shared__ int s_start_b, s_start_t;
+    __shared__ long long s_W;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t r = cluster_rank();
+    const uint32_t peer = r ^ 1u;
+    const int c = blockIdx.x >> 1;
+    const int C = gridDim.x >> 1;
+    const uint32_t wait_limit = p.ctl->wait_limit;
+
+    const uint32_t sbase = smem_u32(sm);
+    const Bars bars = make_bars(sbase + kOffBar);
+
+    if (tid == 0) {
+        s_abort = 0;
+        s_start_b = p.B;
+        s_start_t = 0;
+    }
+    __syncthreads();
+    if (warp == 0)
+        schedule_warp(p.seq_lens, p.max_seq_len, p.B, p.topk, c, C, c == 0 && r == 0, p.meta, p.ctl,
+                      &s_W, &s_start_b, &s_start_t);
+
+    if (tid == 32) {
+        for (int i = 0; i < kNC; ++i) {
+            mbar_init(bars.cf(i), 8);    // one arrive per agent warp once its rows are written
+            mbar_init(bars.ce(i), 1);
+        }
+        mbar_init(bars.s_full, 1);
+        mbar_init(bars.s_empty, kSoftmaxThreads / 32);   // one arrive per softmax warp
+        mbar_init(bars.p_full, kSoftmaxThreads / 32);
+        mbar_init(bars.p_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.xf(i), 1);
+            mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
+            mbar_init(bars.lf(i), 1);
+        }
+        mbar_init(bars.pin_full, 1);
+        mbar_init(bars.pin_free, 8);     // one remote arrive per peer agent warp
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        mbar_init(bars.o_full, 1);
+        mbar_init(bars.o_free, kSoftmaxThreads / 32);
+        mbar_init(bars.mma_drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&s_tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();   // the peer's barriers are initialised before any remote arrive / st.async
+    const uint32_t tmem = s_tmem_base;
+    const long long W = s_W;
+    const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
+    const int n_local = (int)(g_end - g_begin);   // tiles of this cluster
+    const int start_b = s_start_b, start_t = s_start_t;
+
+    if (n_local == 0 && warp >= 2) {
+        // an empty range: its partial slots must not contribute to any merge
+        const int h = tid - 64;
+        if (r == 0 && h < kHeads) {
+            p.lse_part[(size_t)(2 * c) * kHeads + h] = -INFINITY;
+            p.lse_part[(size_t)(2 * c + 1) * kHeads + h] = -INFINITY;
+        }
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ Q loads (TMA)
+        if (lane == 0 && n_local > 0) {
+            tma_prefetch_desc(&tm_qlat);
+            tma_prefetch_desc(&tm_qrope);
+            Cursor cu;
+            cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+            int seg = 0;
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+                if (s_abort) break;
+                if (!cu.first()) continue;
+                if (seg > 0 && !mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit)) {
+                    fail(p.ctl, &s_abort, 1);
+                    break;
+                }
+                const int qrow = cu.b * kHeads;
+                mbar_arrive_expect_tx(bars.q_full, kQBytes);
+                for (int k = 0; k < 4; ++k)
+                    tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
+                                (int)r * kHalfLat + 64 * k, qrow);
+                tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
+                ++seg;
+            }
+            // drain: the last Q load lands before this CTA may exit
+            if (seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        // The whole warp runs this loop so that its operands stay warp-uniform; one elected lane
+        // issues each MMA and commit.  QK of a tile: 8 MMAs per latent group into that group's
+        // accumulator, 2 rope MMAs; PV: per group, 4 pairs of MMAs of 128x128x16, the hi and lo
+        // parts of P times the group's scales.  One score set and one P set in tensor memory: QK of tile i + 1 follows the
+        // softmax's reads of tile i's scores, P of tile i + 1 follows PV of tile i.
+        if (n_local > 0) {
+            constexpr uint32_t id_qk = idesc_bf16(128, kT, 0, 0);
+            constexpr uint32_t id_pv = idesc_bf16(128, 128, 0, 1);
+            const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
+            const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
+            const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
+            const uint32_t lat_lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
+            const uint32_t rope_lo = (uint32_t)smem_desc(0, 16, 512, kSw64);
+            const uint32_t v_lo = (uint32_t)smem_desc(0, kKvLatChunk, 1024, kSw128);
+            const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
+            const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
+            Cursor cq, cp;
+            cq.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+            cp = cq;
+            int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
+            uint32_t polls = 0;
+            while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
+                if (iq < n_local && iq <= ip + 1) {
+                    const int s = iq % kNC;
+                    const bool ready = __shfl_sync(
+                        0xffffffffu,
+                        (!cq.first() || mbar_test(bars.q_full, seg_q & 1)) &&
+                            mbar_test(bars.cf(s), (iq / kNC) & 1) && mbar_test(bars.s_empty, (iq & 1) ^ 1),
+                        0);
+                    if (ready) {
+                        tc_fence_after();
+                        const uint32_t st_lo = ((sbase + kOffConv + s * kConvBytes) >> 4) & 0x3FFF;
+                        if (elect_one()) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_bf16_ss(tmem + (k < 2 ? kTmemSa : kTmemSb),
+                                                lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
+                                                lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
+                                                id_qk, ((k & 1) | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk)
+                                mma_bf16_ss(tmem + kTmemSr, rope_hi | (qr_lo + kk * 2),
+                                            rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
+                                            id_qk, kk != 0 ? 1u : 0u);
+                            mma_commit(bars.s_full);
+                            if (cq.last()) mma_commit(bars.q_empty);
+                        }
+                        __syncwarp();
+                        if (cq.last()) ++seg_q;
+                        cq.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                        ++iq;
+                        polls = 0;
+                        continue;
+                    }
+                }
+                const bool seg_first = cp.first();
+                const bool pv_ready = __shfl_sync(
+                    0xffffffffu,
+                    (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
+                        mbar_test(bars.p_full, ip & 1),
+                    0);
+                if (!pv_ready) {
+                    if (++polls > wait_limit) {
+                        if (lane == 0) fail(p.ctl, &s_abort, 6);
+                        break;
+                    }
+                    continue;
+                }
+                polls = 0;
+                tc_fence_after();
+                const uint32_t v = ((sbase + kOffConv + (ip % kNC) * kConvBytes) >> 4) & 0x3FFF;
+                const uint32_t plo = ((sbase + kOffPLo) >> 4) & 0x3FFF;
+                if (elect_one()) {
+#pragma unroll
+                    for (int g = 0; g < 2; ++g)
+#pragma unroll
+                        for (int kk = 0; kk < kT / 16; ++kk) {
+                            const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
+                            mma_bf16_ts(tmem + kTmemO + 128 * g, tmem + (g == 0 ? kTmemPa : kTmemPb) + 8 * kk, vd,
+                                        id_pv, (!seg_first || kk > 0) ? 1u : 0u);
+                            mma_bf16_ss(tmem + kTmemO + 128 * g,
+                                        lat_hi | (plo + lat_lo + ((g * kPLoBytes + kk * 32) >> 4)), vd, id_pv, 1u);
+                        }
+                    mma_commit(bars.p_empty);
+                    mma_commit(bars.ce(ip % kNC));
+                    if (cp.last()) mma_commit(bars.o_full);
+                }
+                __syncwarp();
+                if (cp.last()) ++seg_p;
+                cp.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                ++ip;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ owners and agents
+        // Lane group lg = warp % 4 (the TMEM lanes this warp may access: heads 32 lg .. 32 lg + 31,
+        // thread = head), slice ts = (warp - 2) / 4 (positions 16 ts .. 16 ts + 15 of a tile, and
+        // O columns 64 ts .. 64 ts + 63 in corrections and epilogues).  Lane groups 2r, 2r + 1
+        // hold the owned heads.
+        //
+        // The four owner warps of a lane group meet at named barriers (ids 1 + lg, 5 + lg, 128
+        // threads), which cannot time out, so these loops never leave early: after a failed
+        // (bounded) wait they keep executing every barrier but skip the work, and waits return at
+        // once.  Wait results are made warp-uniform before any warp-collective tcgen05 instruction.
+        const int lg = warp & 3;
+        const int ts = (warp - 2) >> 2;
+        const int h = lg * 32 + lane;
+        const bool owner = (lg >> 1) == (int)r;
+        const int hh = h & (kOwned - 1);   // index among the owning CTA's heads
+        const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+        float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][128 heads]
+        const int rec_bytes = p.fp8 ? kFp8RecordBytes : kBf16RecordBytes;
+
+        auto wwait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+            bool ok = !s_abort && mbar_wait(bar, parity, wait_limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0) fail(p.ctl, &s_abort, where);
+            return ok;
+        };
+
+        // group scales of the warp's 16 positions of tile i: float4 k holds (s_a, s_b) of
+        // positions 16 ts + 2k and 16 ts + 2k + 1
+        auto scales_of = [&](int i) -> const float4* {
+            return reinterpret_cast<const float4*>(sm + kOffScale) + (i % kNC) * (kT / 2) + 8 * ts;
+        };
+
+        // this CTA's partial scores of tile i for the warp's 16 positions: s_a S_a + s_b S_b + S_rope
+        // (the tile's scales and mask, written by the agents, are read once its slot is complete)
+        auto load_s = [&](int i, float (&v)[16]) -> bool {
+            if (!wwait(bars.cf(i % kNC), (i / kNC) & 1, 18)) return false;
+            if (!wwait(bars.s_full, i & 1, 7)) return false;
+            const float4* sc = scales_of(i);
+            tc_fence_after();
+            {
+                uint32_t a[16], b[16];
+                tmem_ld16(tmem + lane_off + kTmemSa + kSlice * ts, a);
+                tmem_ld16(tmem + lane_off + kTmemSb + kSlice * ts, b);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float4 q = sc[k];
+                    v[2 * k] = fmaf(q.x, __uint_as_float(a[2 * k]), q.y * __uint_as_float(b[2 * k]));
+                    v[2 * k + 1] = fmaf(q.z, __uint_as_float(a[2 * k + 1]), q.w * __uint_as_float(b[2 * k + 1]));
+                }
+            }
+            {
+                uint32_t e[16];
+                tmem_ld16(tmem + lane_off + kTmemSr + kSlice * ts, e);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] += __uint_as_float(e[t]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.s_empty);
+            return true;
+        };
+
+        // O rows of this warp (its 64 columns) times alpha, once PV of tile i - 1 has completed
+        auto rescale_o = [&](int i, float alpha) {
+            if (!wwait(bars.p_empty, (i - 1) & 1, 10)) return;
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                const uint32_t col = kTmemO + 64 * ts + 32 * cc;
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + col, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                tmem_st32(tmem + lane_off + col, o);
+            }
+            tmem_wait_st();
+        };
+
+        // the warp's 16 P values of tile i (fp16 pairs, so that the one rounding that matters
+        // is the bf16 one of P s_g) times each group's scales into tensor memory, once PV of
+        // tile i - 1 has completed, then P ready for the MMA
+        auto store_p = [&](int i, const uint32_t (&pk)[8]) {
+            if (i >= 1 && !wwait(bars.p_empty, (i - 1) & 1, 11)) return;
+            const float4* sc = scales_of(i);
+            uint32_t pa[8], pb[8], la[8], lb[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 q = sc[k];
+                __half2 h2;
+                *reinterpret_cast<uint32_t*>(&h2) = pk[k];
+                const float2 pf = __half22float2(h2);
+                const float xa0 = pf.x * q.x, xa1 = pf.y * q.z, xb0 = pf.x * q.y, xb1 = pf.y * q.w;
+                pa[k] = pack_bf16x2(xa0, xa1);
+                pb[k] = pack_bf16x2(xb0, xb1);
+                la[k] = pack_bf16x2(xa0 - __uint_as_float(pa[k] << 16), xa1 - __uint_as_float(pa[k] & 0xFFFF0000u));
+                lb[k] = pack_bf16x2(xb0 - __uint_as_float(pb[k] << 16), xb1 - __uint_as_float(pb[k] & 0xFFFF0000u));
+            }
+            tmem_st8(tmem + lane_off + kTmemPa + 8 * ts, pa);
+            tmem_st8(tmem + lane_off + kTmemPb + 8 * ts, pb);
+            // lo parts: row h, 16-byte chunks 2 ts and 2 ts + 1 of the 128-byte row (chunk c at
+            // c ^ (h % 8), 128-byte swizzle)
+            {
+                uint8_t* ra = sm + kOffPLo + h * 128;
+                uint8_t* rb = ra + kPLoBytes;
+                const int c0 = ((2 * ts) ^ (h & 7)) << 4, c1 = ((2 * ts + 1) ^ (h & 7)) << 4;
+                st_shared_v4(ra + c0, la[0], la[1], la[2], la[3]);
+                st_shared_v4(ra + c1, la[4], la[5], la[6], la[7]);
+                st_shared_v4(rb + c0, lb[0], lb[1], lb[2], lb[3]);
+                st_shared_v4(rb + c1, lb[4], lb[5], lb[6], lb[7]);
+                fence_proxy_async_smem();
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && !s_abort) mbar_arrive(bars.p_full);
+        };
+
+        // O rows of this warp normalised by l (row sum) into the output or a partial slot
+        auto epilogue_rows = [&](int seg, const Cursor& cu, bool partial, float l_row) {
+            const int slot = 2 * c + (seg == 0 ? 0 : 1);
+            if (!wwait(bars.o_full, seg & 1, 12)) return;
+            tc_fence_after();
+            const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
+            const size_t row = (size_t)cu.b * kHeads + h;
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + kTmemO + 64 * ts + 32 * cc, o);
+                tmem_wait_ld();
+                const int col = (int)r * kHalfLat + 64 * ts + 32 * cc;
+                if (!partial) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.o_free);
+        };
+
+        Cursor cu;
+        cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+        int seg = 0;
+        bool cut_front = false;
+
+        if (!owner) {
+            // ------------------------------------------------------------ agents
+            const uint32_t x_remote = mapa(sbase + kOffX, peer);
+            const uint32_t xfull_remote = mapa(bars.x_full, peer);
+            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
+            const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
+            const int at = ((lg & 1) * 4 + ts) * 32 + lane;   // 0 .. 255 over the agents
+
+            // the record of row `row` of the tile at cursor cj, or null when the row is outside
+            // the request (it then reads as zeros)
+            auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* {
+                int pos = cj.t * kT + row;
+                if (p.topk > 0) {
+                    if (pos >= p.topk) return nullptr;
+                    pos = p.topk_idx[(size_t)cj.b * p.topk + pos];
+                    if (pos < 0) return nullptr;
+                }
+                if (pos >= cj.n) return nullptr;
+                const int page = p.block_table[(size_t)cj.b * p.max_pages + (pos >> 6)];
+                if (page < 0 || page >= p.num_pages) {
+                    if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
+                    return nullptr;
+                }
+                return p.pool + ((size_t)page * kPage + (pos & (kPage - 1))) * rec_bytes;
+            };
+
+            // Tile j (cursor cj) into conversion slot j % kNC once PV of tile j - kNC is done:
+            // this CTA's half of every row, converted to the MMA layouts, its group scales and the
+            // mask of valid rows.
+            auto prepare = [&](int j, const Cursor& cj) {
+                const int slot = j % kNC;
+                if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
+                uint8_t* lat = sm + kOffConv + slot * kConvBytes;
+                uint8_t* rope = lat + 4 * kKvLatChunk;
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                if (p.fp8) {
+                    // 64 rows x 16 chunks of 16 codes; this thread converts chunks at + 256 k
+                    uint4 raw[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = at + 256 * k, row = e >> 4, ch = e & 15;
+                        const uint8_t* rec = row_record(cj, row);
+                        raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + kHalfLat * (int)r + 16 * ch)) : zero;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = at + 256 * k, row = e >> 4, ch = e & 15;
+                        uint32_t o[8];
+                        e4m3x16_to_bf16(raw[k], o);
+                        // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte parts
+                        // 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
+                        uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
+                        const int s0 = 2 * (ch & 3);
+                        st_shared_v4(dst + ((s0 ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        st_shared_v4(dst + (((s0 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
+                    }
+                } else {
+                    // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint4 raw[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int e = at + 256 * (4 * half + k), row = e >> 5, ch = e & 31;
+                            const uint8_t* rec = row_record(cj, row);
+                            raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int e = at + 256 * (4 * half + k), row = e >> 5, ch = e & 31;
+                            st_shared_v4(lat + (ch >> 3) * kKvLatChunk + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
+                                         raw[k].x, raw[k].y, raw[k].z, raw[k].w);
+                        }
+                    }
+                }
+                {
+                    // rope: 64 rows x 4 chunks of 8 dims, 64-byte swizzle
+                    const int row = at >> 2, c4 = at & 3;
+                    const uint8_t* rec = row_record(cj, row);
+                    const int rope_off = (p.fp8 ? kFp8RopeOff : 2 * kDc) + 2 * kHalfRope * (int)r;
+                    const uint4 raw = rec ? __ldg(reinterpret_cast<const uint4*>(rec + rope_off + 16 * c4)) : zero;
+                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), raw.x, raw.y, raw.z, raw.w);
+                }
+                if (at < kT) {
+                    // the row's two group scales (1 for bf16 records) and the valid-row mask
+                    const uint8_t* rec = row_record(cj, at);
+                    float2 s2 = make_float2(1.f, 1.f);
+                    if (p.fp8) s2 = rec ? __ldg(reinterpret_cast<const float2*>(rec + kFp8ScaleOff + 8 * (int)r))
+                                        : make_float2(0.f, 0.f);
+                    reinterpret_cast<float2*>(sm + kOffScale)[slot * kT + at] = s2;
+                    const uint32_t m = __ballot_sync(0xffffffffu, rec != nullptr);
+                    if (lane == 0) reinterpret_cast<uint32_t*>(sm + kOffMask)[2 * slot + (at >> 5)] = m;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.cf(slot));
+            };
+
+            // forward this CTA's partial scores of tile i (the peer's heads) to the peer
+            auto forward = [&](int i) {
+                float v[16];
+                if (!load_s(i, v)) return;
+                const int xb = i & 1;
+                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) return;
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    st_async_v4(x_remote + xb * kXBytes + ((4 * ts + g) * kOwned + hh) * 16,
+                                xfull_remote + 8 * xb, __float_as_uint(v[4 * g]), __float_as_uint(v[4 * g + 1]),
+                                __float_as_uint(v[4 * g + 2]), __float_as_uint(v[4 * g + 3]));
+            };
+
+            Cursor cpr = cu;   // next tile to prepare
+            int i_pr = 0;
+            auto prepare_until = [&](int upto) {
+                for (; i_pr < upto && i_pr < n_local; ++i_pr, cpr.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) prepare(i_pr, cpr);
+            };
+            prepare_until(2);
+            if (n_local > 0) forward(0);
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+                if (i + 1 < n_local) forward(i + 1);
+                const bool first = cu.first();
+                if (first) cut_front = cu.t > 0;
+                // the peer's P of its heads for tile i, and its rescale factors
+                if (lead && !s_abort) mbar_arrive_expect_tx(bars.pin_full, kPInMsg);
+                const bool ok = wwait(bars.pin_full, i & 1, 13);
+                uint32_t pk[8];
+                const uint8_t* pin = sm + kOffPIn;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(pin + ((2 * ts + g) * kOwned + hh) * 16);
+                    pk[4 * g] = q.x;
+                    pk[4 * g + 1] = q.y;
+                    pk[4 * g + 2] = q.z;
+                    pk[4 * g + 3] = q.w;
+                }
+                const float alpha = reinterpret_cast<const float*>(pin + kPInBytes)[hh];
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive_remote_relaxed(pinfree_remote);
+                if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha);
+                store_p(i, pk);
+                prepare_until(i + 3);
+                if (cu.last()) {
+                    const bool partial = cut_front || cu.t < cu.nt - 1;
+                    // the row sums of these heads, sent by the peer's owners
+                    if (lead && !s_abort) mbar_arrive_expect_tx(bars.lf(seg & 1), kOwned * 4);
+                    const bool lok = wwait(bars.lf(seg & 1), (seg >> 1) & 1, 14);
+                    const float l_row = lok ? reinterpret_cast<const float*>(sm + kOffLIn)[(seg & 1) * kOwned + hh] : 0.f;
+                    epilogue_rows(seg, cu, partial, l_row);
+                    ++seg;
+                }
+            }
+        } else {
+            // ------------------------------------------------------------ owners
+            const uint32_t pin_remote = mapa(sbase + kOffPIn, peer);
+            const uint32_t pinfull_remote = mapa(bars.pin_full, peer);
+            const uint32_t xfree_remote = mapa(bars.x_free, peer);
+            const uint32_t lin_remote = mapa(sbase + kOffLIn, peer);
+            const uint32_t lfull_remote = mapa(bars.l_full, peer);
+            const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
+            const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
+            float m_used = -INFINITY, l_part = 0.f;
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+                const int xb = i & 1;
+                const bool first = cu.first();
+                if (first) {
+                    m_used = -INFINITY;
+                    l_part = 0.f;
+                    cut_front = cu.t > 0;   // the request started before this cluster's range
+                }
+                float v[16];
+                load_s(i, v);
+                // valid rows of this warp's 16 positions
+                const uint32_t vmask =
+                    (reinterpret_cast<const uint32_t*>(sm + kOffMask)[2 * (i % kNC) + (ts >> 1)] >> (16 * (ts & 1))) & 0xFFFFu;
+                // the peer's partial scores of these heads for tile i
+                if (lead && !s_abort) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
+                const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
+                float x[16];
+                const uint8_t* xp = sm + kOffX + xb * kXBytes;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * kOwned + hh) * 16);
+                    x[4 * g] = (v[4 * g] + q.x) * p.scale_log2;
+                    x[4 * g + 1] = (v[4 * g + 1] + q.y) * p.scale_log2;
+                    x[4 * g + 2] = (v[4 * g + 2] + q.z) * p.scale_log2;
+                    x[4 * g + 3] = (v[4 * g + 3] + q.w) * p.scale_log2;
+                }
+                // every loaded value has been consumed: hand the exchange buffer back to the peer
+                __syncwarp();
+                if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote + 8 * xb);
+                // P = 2^(x - m) with the running max m (rows outside the request give 0).  m is
+                // kept while every P of a row stays at most 2^15: a thread whose 16 P sum past
+                // 2^15 (or not to a finite value) votes for the rare path, as does every segment
+                // start and a row with no visible position yet.  There the exact row max over the
+                // four slices raises m where it exceeds m by more than the slack, O is rescaled
+                // here and, through alpha sent with P, in the peer, and P is computed again.
+                float alpha = 1.0f;
+                float psum;
+                uint32_t pk[8];
+                auto exp_tile = [&]() {
+                    psum = 0.f;
+#pragma unroll
+                    for (int t = 0; t < 16; t += 2) {
+                        const bool live = m_used != -INFINITY;
+                        const float p0 = (live && ((vmask >> t) & 1)) ? ex2(x[t] - m_used) : 0.f;
+                        const float p1 = (live && ((vmask >> (t + 1)) & 1)) ? ex2(x[t + 1] - m_used) : 0.f;
+                        psum += p0 + p1;
+                        const __half2 h2 = __floats2half2_rn(p0, p1);
+                        pk[t / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                };
+                exp_tile();
+                const bool need = first || m_used == -INFINITY || !(psum <= kPMax);
+                if (bar_red_or(bar_vote, 128, need)) {
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if ((vmask >> t) & 1) mx = fmaxf(mx, x[t]);
+                    red[ts * 128 + h] = mx;
+                    named_bar_sync(bar_sync, 128);
+                    const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
+                    const bool grow = first || tmax > m_used + kLazySlack;
+                    const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
+                    if (!first) {
+                        alpha = grow ? ex2(m_used - m_new) : 1.0f;
+                        if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha);
+                        l_part *= alpha;
+                    }
+                    m_used = m_new;
+                    named_bar_sync(bar_sync, 128);   // red[] rows of this lane group are free again
+                    exp_tile();
+                }
+                l_part += psum;
+                // P of these heads (fp16, before the group scales) to the peer, once it has taken
+                // the previous one; both CTAs apply their group scales to these values
+                if (wwait(bars.pin_free, (i & 1) ^ 1, 15)) {
+#pragma unroll
+                    for (int g = 0; g < 2; ++g)
+                        st_async_v4(pin_remote + ((2 * ts + g) * kOwned + hh) * 16, pinfull_remote,
+                                    pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+                    if (ts == 0)
+                        st_async_b32(pin_remote + kPInBytes + hh * 4, pinfull_remote, __float_as_uint(alpha));
+                }
+                store_p(i, pk);
+
+                if (cu.last()) {
+                    // ------------------------------------------------------ segment epilogue
+                    const bool partial = cut_front || cu.t < cu.nt - 1;
+                    red[ts * 128 + h] = l_part;
+                    named_bar_sync(bar_sync, 128);
+                    const float l_row = (red[h] + red[128 + h]) + (red[256 + h] + red[384 + h]);
+                    named_bar_sync(bar_sync, 128);
+                    // the row sums of these heads to the peer, which finishes its O rows of them
+                    if (ts == 0 && !s_abort)
+                        st_async_b32(lin_remote + ((seg & 1) * kOwned + hh) * 4,
+                                     lfull_remote + 8 * (seg & 1), __float_as_uint(l_row));
+                    const float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
+                    if (ts == 0) {
+                        const size_t row = (size_t)cu.b * kHeads + h;
+                        if (!partial) p.lse[row] = L;
+                        else p.lse_part[(size_t)(2 * c + (seg == 0 ? 0 : 1)) * kHeads + h] = L;
+                    }
+                    epilogue_rows(seg, cu, partial, l_row);
+                    ++seg;
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    if (warp == 1 && n_local > 0) {
+        __syncwarp();
+        // all MMAs issued by the elected lane (the lowest active one, as in the loop) are complete
+        // once this barrier flips
+        if (elect_one()) {
+            mma_commit(bars.mma_drain);
+            if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
+        }
+    }
+    __syncwarp();
+    if (s_abort) __nanosleep(100000);   // let any in-flight distributed-shared-memory stores land
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();   // the peer no longer writes into this CTA's shared memory
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+// Same workspace as the dense bf16 kernel: 2 partial slots per cluster (fp32 [128][512] + lse
+// [128]), then per request its first partial slot and last cluster (int32 [B][2]).
+DecodePlan plan_decode_gather(int fmt, int B, int max_seq_len, int topk, int sms) {
+    (void)fmt;
+    DecodePlan p;
+    const long long per_req = topk > 0 ? (topk + kT - 1) / kT : (max_seq_len + kT - 1) / kT;
+    const int C = clusters_for_tiles((long long)B * per_req, sms);
+    p.splits = C;
+    p.workspace = (size_t)2 * C * kHeads * (kDc + 1) * sizeof(float) + (size_t)2 * B * sizeof(int32_t);
+    p.workspace = (p.workspace + 255) / 256 * 256;
+    p.launches = 2;
+    return p;
+}
+
+cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(decode_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    CUtensorMap tm_qlat, tm_qrope;
+    const uint64_t qrows = (uint64_t)a.B * kHeads;
+    if (!encode_2d(&tm_qlat, a.q_lat, kDc, qrows, kDc * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tm_qrope, a.q_rope, kDr, qrows, kDr * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    const int C = plan.splits;
+    float* o_part = static_cast<float*>(a.workspace);
+    float* lse_part = o_part + (size_t)2 * C * kHeads * kDc;
+    int32_t* meta = reinterpret_cast<int32_t*>(lse_part + (size_t)2 * C * kHeads);
+    GatherParams p;
+    p.pool = a.pool;
+    p.block_table = a.block_table;
+    p.seq_lens = a.seq_lens;
+    p.topk_idx = a.topk > 0 ? a.topk_idx : nullptr;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.o_part = o_part;
+    p.lse_part = lse_part;
+    p.meta = meta;
+    p.ctl = a.ctl;
+    p.num_pages = a.num_pages;
+    p.max_pages = a.max_pages;
+    p.max_seq_len = a.max_seq_len;
+    p.topk = a.topk_idx != nullptr ? a.topk : 0;
+    p.B = a.B;
+    p.fp8 = a.fmt == MLA_KV_FP8_MIXED ? 1 : 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const int64_t blocks = (int64_t)a.B * kHeads;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    decode_gather_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    merge_slots_kernel<<<(unsigned)blocks, 128, 0, st>>>(o_part, lse_part, meta, a.out, a.lse);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

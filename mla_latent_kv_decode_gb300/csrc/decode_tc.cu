@@ -46,15 +46,14 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include "mla_internal.cuh"
-#include "tc_ptx.cuh"
+#include "decode_common.cuh"
 
 namespace mla {
 namespace {
 
 using namespace ptx;
+using namespace dc;
 
-constexpr int kT = 64;                 // positions per tile = one cache page
 constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 3;                // score buffers in TMEM
 constexpr int kQKAhead = 2;            // QK of tile i + 2 may run before PV of tile i
@@ -70,7 +69,6 @@ constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256)
 constexpr uint32_t kTmemS = 256;       // score buffer k: columns [256 + 64 k, 320 + 64 k)
 constexpr uint32_t kTmemP = 448;       // P buffer k: columns [448 + 32 k, 480 + 32 k)
 constexpr uint32_t kDrainLimit = 1u << 20;
-constexpr int kMinTilesPerCluster = 4;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] bf16, SW128
@@ -150,58 +148,6 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     return b;
 }
 
-__device__ __forceinline__ void fail(DevCtl* ctl, volatile int* abort_flag, int where) {
-    *abort_flag = 1;
-    record_error(ctl, MLA_ERR_TIMEOUT, where);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ int clamp_len(int n, int max_len) {
-    return n < 0 ? 0 : (n > max_len ? max_len : n);
-}
-
-// Walks the tiles of one cluster's range: request b, tile (page) t of that request.
-struct Cursor {
-    const int32_t* seq_lens;
-    int max_len, B;
-    int b, t, nt, n;         // n = visible positions of request b, nt = its tiles
-    long long g, g_end;      // global tile index, end of range
-    __device__ __forceinline__ void load_req() {
-        n = clamp_len(seq_lens[b], max_len);
-        nt = (n + kT - 1) / kT;
-    }
-    __device__ __forceinline__ void init(const int32_t* sl, int ml, int B_, int b0, int t0,
-                                         long long g0, long long g1) {
-        seq_lens = sl, max_len = ml, B = B_, b = b0, t = t0, g = g0, g_end = g1;
-        if (g < g_end) load_req();
-        else n = nt = 0;
-    }
-    __device__ __forceinline__ bool first(long long g_begin) const { return t == 0 || g == g_begin; }
-    __device__ __forceinline__ bool last() const { return t == nt - 1 || g == g_end - 1; }
-    __device__ __forceinline__ void next() {
-        ++g;
-        ++t;
-        if (g >= g_end) return;
-        while (t >= nt && b + 1 < B) {
-            ++b;
-            t = 0;
-            load_req();
-        }
-    }
-};
-
-// 16 bytes (4 x b32) into the peer's shared memory, completing tx-bytes on its barrier.
-__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t remote_bar, uint32_t v) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                     remote_addr),
-                 "r"(v), "r"(remote_bar)
-                 : "memory");
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                      const __grid_constant__ CUtensorMap tm_qrope,
@@ -235,48 +181,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s_start_t = 0;
     }
     __syncthreads();
-    if (warp == 0) {
-        const int per = (p.B + 31) / 32;
-        const int b_lo = min(p.B, lane * per), b_hi = min(p.B, b_lo + per);
-        long long mine = 0;
-        for (int b = b_lo; b < b_hi; ++b) {
-            const int raw = p.seq_lens[b];
-            if ((raw < 0 || raw > p.max_seq_len) && r == 0 && c == 0) record_error(p.ctl, MLA_ERR_BOUNDS, b);
-            mine += (clamp_len(raw, p.max_seq_len) + kT - 1) / kT;
-        }
-        long long incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const long long W = __shfl_sync(0xffffffffu, incl, 31);
-        const long long gb = (long long)c * W / C;
-        long long pre = incl - mine;
-        for (int b = b_lo; b < b_hi; ++b) {
-            const int nt = (clamp_len(p.seq_lens[b], p.max_seq_len) + kT - 1) / kT;
-            if (c == 0 && r == 0) {
-                int first_slot = -1, c_hi = -1;
-                if (nt > 0) {
-                    // the clusters whose ranges hold tiles pre .. pre + nt - 1
-                    long long lo = ((pre + 1) * C + W - 1) / W - 1;
-                    long long hi = ((pre + nt) * C + W - 1) / W - 1;
-                    lo = lo < 0 ? 0 : (lo > C - 1 ? C - 1 : lo);
-                    hi = hi < lo ? lo : (hi > C - 1 ? C - 1 : hi);
-                    first_slot = 2 * (int)lo + ((lo * W / C) == pre ? 0 : 1);
-                    c_hi = (int)hi;
-                }
-                p.meta[2 * b] = first_slot;
-                p.meta[2 * b + 1] = c_hi;
-            }
-            if (gb < W && gb >= pre && gb < pre + nt) {
-                s_start_b = b;
-                s_start_t = (int)(gb - pre);
-            }
-            pre += nt;
-        }
-        if (lane == 31) s_W = W;
-    }
+    if (warp == 0)
+        schedule_warp(p.seq_lens, p.max_seq_len, p.B, 0, c, C, c == 0 && r == 0, p.meta, p.ctl, &s_W,
+                      &s_start_b, &s_start_t);
 
     if (tid == 32) {
         for (int i = 0; i < kNS; ++i) {
@@ -334,11 +241,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_kv_lat);
             tma_prefetch_desc(&tm_kv_rope);
             Cursor cu;
-            cu.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
+            cu.init(p.seq_lens, p.max_seq_len, 0, start_b, start_t, n_local);
             int seg = 0, issued = 0;
-            for (int i = 0; i < n_local; ++i, cu.next()) {
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
                 if (s_abort) break;
-                if (cu.first(g_begin)) {
+                if (cu.first()) {
                     if (seg > 0 && !mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit)) {
                         fail(p.ctl, &s_abort, 1);
                         break;
@@ -394,7 +301,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
             const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
             Cursor cq, cp;
-            cq.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
+            cq.init(p.seq_lens, p.max_seq_len, 0, start_b, start_t, n_local);
             cp = cq;
             int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
             uint32_t polls = 0;
@@ -407,7 +314,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int s = iq % kNS, sb = iq % kNSB;
                     const bool ready = __shfl_sync(
                         0xffffffffu,
-                        (!cq.first(g_begin) || mbar_test(bars.q_full, seg_q & 1)) &&
+                        (!cq.first() || mbar_test(bars.q_full, seg_q & 1)) &&
                             mbar_test(bars.kvf(s), (iq / kNS) & 1) &&
                             mbar_test(bars.se(sb), ((iq / kNSB) & 1) ^ 1),
                         0);
@@ -433,14 +340,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                         if (cq.last()) ++seg_q;
-                        cq.next();
+                        cq.next(p.seq_lens, p.max_seq_len, p.B, 0);
                         ++iq;
                         polls = 0;
                         continue;
                     }
                 }
                 // PV of tile ip: O_r += P (tensor memory) x V_r (stage, MN-major)
-                const bool seg_first = cp.first(g_begin);
+                const bool seg_first = cp.first();
                 const int pb = ip & 1;
                 const bool pv_ready = __shfl_sync(
                     0xffffffffu,
@@ -469,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (cp.last()) ++seg_p;
-                cp.next();
+                cp.next(p.seq_lens, p.max_seq_len, p.B, 0);
                 ++ip;
             }
         }
@@ -577,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         };
 
         Cursor cu;
-        cu.init(p.seq_lens, p.max_seq_len, p.B, start_b, start_t, g_begin, g_end);
+        cu.init(p.seq_lens, p.max_seq_len, 0, start_b, start_t, n_local);
         int seg = 0;
         bool cut_front = false;
 
@@ -599,9 +506,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 xfull_remote + 8 * xb, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
             };
             if (n_local > 0) forward(0);
-            for (int i = 0; i < n_local; ++i, cu.next()) {
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
                 if (i + 1 < n_local) forward(i + 1);
-                const bool first = cu.first(g_begin);
+                const bool first = cu.first();
                 if (first) cut_front = cu.t > 0;
                 // the peer's P of its heads for page i, and its rescale factors
                 if (lead && !s_abort) mbar_arrive_expect_tx(bars.pin_full, kPInMsg);
@@ -641,9 +548,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
             float m_used = -INFINITY, l_part = 0.f;
-            for (int i = 0; i < n_local; ++i, cu.next()) {
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
                 const int xb = i & 1;
-                const bool first = cu.first(g_begin);
+                const bool first = cu.first();
                 if (first) {
                     m_used = -INFINITY;
                     l_part = 0.f;
@@ -781,6 +688,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+}  // namespace
+
 // Finish of mla_decode: requests cut by cluster range boundaries get their partials merged,
 // requests with no visible position get zeros and lse = -inf; the rest were finished by the
 // decode kernel.  Block (request b, head h).  Request b's partials sit in slot first (2 c_lo or
@@ -829,7 +738,7 @@ __global__ void __launch_bounds__(128) merge_slots_kernel(const float* __restric
     if (threadIdx.x == 0) lse[(size_t)b * kHeads + h] = L;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         cudaDriverEntryPointQueryResult q;
@@ -854,15 +763,6 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int clusters_for(int B, int max_seq_len, int sms) {
-    const long long w_max = (long long)B * ((max_seq_len + kT - 1) / kT);
-    long long c = sms / 2;
-    const long long by_work = (w_max + kMinTilesPerCluster - 1) / kMinTilesPerCluster;
-    if (by_work < c) c = by_work;
-    return c < 1 ? 1 : (int)c;
-}
-
-}  // namespace
 
 // Workspace of the tensor-core path: 2 partial slots per cluster (fp32 [128][512] + lse [128]),
 // then per request its first partial slot and last cluster (int32 [B][2]).
@@ -870,9 +770,8 @@ DecodePlan plan_decode_tc(int fmt, int B, int max_seq_len, int topk, int sms) {
     (void)fmt;
     (void)topk;
     DecodePlan p;
-    const int C = clusters_for(B, max_seq_len, sms);
+    const int C = clusters_for_tiles((long long)B * ((max_seq_len + kT - 1) / kT), sms);
     p.splits = C;
-    p.chunk = 0;
     p.workspace = (size_t)2 * C * kHeads * (kDc + 1) * sizeof(float) + (size_t)2 * B * sizeof(int32_t);
     p.workspace = (p.workspace + 255) / 256 * 256;
     p.launches = 2;

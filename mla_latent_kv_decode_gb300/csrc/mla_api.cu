@@ -146,8 +146,6 @@ mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const vo
     a.scale = scale;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
-    a.o_part = nullptr;
-    a.lse_part = nullptr;
     a.workspace = workspace;
     a.ctl = ctl;
     if (plan.workspace > 0 &&

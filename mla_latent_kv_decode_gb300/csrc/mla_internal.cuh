@@ -50,9 +50,8 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int S, in
 
 // Split-KV plan of one decode call.
 struct DecodePlan {
-    int splits;            // S: work units per request along the visible positions
-    int chunk;             // positions per unit (multiple of 64 for dense, of 32 for sparse)
-    size_t workspace;      // bytes of (o_part, lse_part) needed; 0 when splits == 1
+    int splits;            // C: clusters of the launch (two partial slots each)
+    size_t workspace;      // bytes of the partial slots and the per-request merge table
     int launches;          // kernels one decode call launches
 };
 
@@ -72,25 +71,26 @@ struct DecodeArgs {
     float scale;
     __nv_bfloat16* out;
     float* lse;
-    float* o_part;         // simt path: [S, B, H, 512] when splits > 1
-    float* lse_part;       // simt path: [S, B, H]
     void* workspace;       // caller scratch of at least plan.workspace bytes
     DevCtl* ctl;
 };
 
-// Tensor-core path (bf16 dense) and CUDA-core path (FP8 mixed and top-k for now).
+// Tensor-core paths: bf16 dense pages (decode_tc.cu), FP8 records and top-k lists (decode_gather.cu).
 DecodePlan plan_decode_tc(int fmt, int B, int max_seq_len, int topk, int sms);
 cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
-DecodePlan plan_decode_simt(int fmt, int B, int max_seq_len, int topk, int sms);
-cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
 
-inline bool use_tc(int fmt, int topk) { return fmt == MLA_KV_BF16 && topk == 0; }
+DecodePlan plan_decode_gather(int fmt, int B, int max_seq_len, int topk, int sms);
+cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+
+// bf16 dense pages: TMA-fed tensor-core kernel; FP8 records or a top-k list: the tensor-core
+// kernel that gathers and converts rows itself.
+inline bool use_tma_path(int fmt, int topk) { return fmt == MLA_KV_BF16 && topk == 0; }
 inline DecodePlan plan_decode(int fmt, int B, int max_seq_len, int topk, int sms) {
-    return use_tc(fmt, topk) ? plan_decode_tc(fmt, B, max_seq_len, topk, sms)
-                             : plan_decode_simt(fmt, B, max_seq_len, topk, sms);
+    return use_tma_path(fmt, topk) ? plan_decode_tc(fmt, B, max_seq_len, topk, sms)
+                                   : plan_decode_gather(fmt, B, max_seq_len, topk, sms);
 }
 inline cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
-    return use_tc(a.fmt, a.topk) ? launch_decode_tc(a, p, st) : launch_decode_simt(a, p, st);
+    return use_tma_path(a.fmt, a.topk) ? launch_decode_tc(a, p, st) : launch_decode_gather(a, p, st);
 }
 
 }  // namespace mla
