@@ -647,6 +647,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             auto prepare_until = [&](int upto) {
                 for (; i_pr < upto && i_pr < n_local; ++i_pr, cpr.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) prepare(i_pr, cpr);
             };
+            // L2 prefetch of the rows of tile i + 5 during iteration i (tile i + 2 is prepared in
+            // iteration i, so prefetches run three iterations ahead): thread `at` covers part
+            // at / 64 (latent bytes, rope, scales) of row at % 64.  Its address comes from the
+            // index loads of the iteration before, so their latency overlaps an iteration.
+            const int pf_row = at & (kT - 1), pf_part = at >> 6;
+            const uint32_t pf_bytes = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
+            const int pf_off = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) * (int)r
+                                            : (pf_part == 1 ? (p.fp8 ? kFp8RopeOff : 2 * kDc) + 64 * (int)r : kFp8ScaleOff);
+            const bool pf_on = pf_part < (p.fp8 ? 3 : 2);
+            Cursor cpf = cu;   // the tile whose prefetch address is computed next (tiles 0, 1 are
+            int i_pf = 0;      // prepared at once)
+            for (; i_pf < 2 && i_pf < n_local; ++i_pf) cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+            const uint8_t* pf_rec = nullptr;
+            auto prefetch_step = [&]() {
+                if (pf_rec) prefetch_l2(pf_rec + pf_off, pf_bytes);
+                pf_rec = nullptr;
+                if (i_pf < n_local) {
+                    if (pf_on) pf_rec = row_record(cpf, pf_row);
+                    ++i_pf;
+                    cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                }
+            };
+            for (int k = 0; k < 4; ++k) prefetch_step();   // tiles 2, 3, 4 prefetched, 5 addressed
             prepare_until(2);
             if (n_local > 0) forward(0);
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
@@ -672,6 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha);
                 store_p(i, pk);
                 prepare_until(i + 3);
+                prefetch_step();
                 if (cu.last()) {
                     const bool partial = cut_front || cu.t < cu.nt - 1;
                     // the row sums of these heads, sent by the peer's owners
