@@ -37,10 +37,18 @@ METRIC = "MLA decode KV GB/s, TFLOP/s and % of GB300 roofline; decode tokens/s a
 UNIT = "KV GB/s"
 L2_BYTES = 126 * 2 ** 20
 
-# DRAM bytes per decode launch from an ncu capture, keyed by the sha256 of the decode kernel
-# sources it was taken on; any change to those sources makes the entry stale (traffic = null).
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per decode-kernel launch from an ncu capture, keyed by the sha256 of
+# the decode kernel sources it was taken on and the workload; any change to those sources makes the
+# entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
+# profiles/decode_gather_fp8_batch.md.
+NCU_TRAFFIC = {
+    ("6d63f2ca00bc97f4", "paged_batch"): 178_591_744,
+    ("6d63f2ca00bc97f4", "fp8_batch"): 1_416_535_640,
+}
 DECODE_SOURCES = ["mla_latent_kv_decode_gb300/csrc/decode_tc.cu",
+                  "mla_latent_kv_decode_gb300/csrc/decode_gather.cu",
+                  "mla_latent_kv_decode_gb300/csrc/decode_common.cuh",
+                  "mla_latent_kv_decode_gb300/csrc/mla_internal.cuh",
                   "mla_latent_kv_decode_gb300/csrc/tc_ptx.cuh"]
 
 
@@ -303,8 +311,22 @@ def run_ours(args):
     peaks = _peaks()
     dec_s = dec_ms / 1e3
     achieved = alg_bytes / dec_s / 1e9
-    traffic = NCU_TRAFFIC.get(_sources_hash())
-    launches_per_step = 1 + int(mla.load().mla_decode_launches(w.fmt, w.B, w.H, w.max_seq_len, 0))
+    traffic = NCU_TRAFFIC.get((_sources_hash(), w.name))
+    topk = 0 if w.topk_idx is None else int(w.topk_idx.shape[1])
+    launches_per_step = 1 + int(mla.load().mla_decode_launches(w.fmt, w.B, w.H, w.max_seq_len, topk))
+    # the bound of the call: HBM unless its flops at the dense bf16 peak take longer than its
+    # bytes at the HBM peak (the FP8 batch: q stays bf16, the cache bytes halve)
+    tensor_bound = flops / (peaks["bf16_tflops_sustained"] * 1e12) > alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        roofline = {"bound": "tensor", "achieved": round(flops / dec_s / 1e12, 2),
+                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": round(flops / dec_s / 1e12 / peaks["bf16_tflops_sustained"], 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    roofline.update({"traffic": traffic, "peak_source": peaks["source"], "kernel": "mla_decode call",
+                     "ms_per_launch": round(dec_ms, 6), "bytes_per_launch": alg_bytes,
+                     "flops_per_launch": flops})
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
@@ -319,11 +341,7 @@ def run_ours(args):
         "decode_tokens_per_s": round(world * w.B / step_s, 1),
         "tflops": round(world * flops / step_s / 1e12, 3),
         "step_frac_of_hbm_roofline": round((alg_bytes / (peaks['hbm_gbs'] * 1e9)) / step_s, 4),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "peak_source": peaks["source"],
-                     "kernel": "mla_decode call", "ms_per_launch": round(dec_ms, 6),
-                     "bytes_per_launch": alg_bytes},
+        "roofline": roofline,
         "tensor_util": {"achieved_tflops": round(flops / dec_s / 1e12, 2),
                         "peak": peaks["bf16_tflops_sustained"],
                         "frac": round(flops / dec_s / 1e12 / peaks["bf16_tflops_sustained"], 4)},
