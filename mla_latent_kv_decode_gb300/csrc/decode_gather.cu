@@ -562,10 +562,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // mask of valid rows.
             auto prepare = [&](int j, const Cursor& cj) {
                 const int slot = j % kNC;
-                if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
                 uint8_t* lat = sm + kOffConv + slot * kConvBytes;
                 uint8_t* rope = lat + 4 * kKvLatChunk;
                 const uint4 zero = make_uint4(0, 0, 0, 0);
+                // the row loads go out first, so that their latency overlaps the wait for the slot
+                const int rope_off = (p.fp8 ? kFp8RopeOff : 2 * kDc) + 2 * kHalfRope * (int)r;
+                const uint8_t* rrec = row_record(cj, at >> 2);
+                const uint4 rraw = rrec ? __ldg(reinterpret_cast<const uint4*>(rrec + rope_off + 16 * (at & 3))) : zero;
+                const uint8_t* srec = at < kT ? row_record(cj, at) : nullptr;
+                float2 s2 = make_float2(1.f, 1.f);
+                if (p.fp8 && at < kT)
+                    s2 = srec ? __ldg(reinterpret_cast<const float2*>(srec + kFp8ScaleOff + 8 * (int)r)) : make_float2(0.f, 0.f);
                 if (p.fp8) {
                     // 64 rows x 16 chunks of 16 codes; this thread converts chunks at + 256 k
                     uint4 raw[4];
@@ -575,6 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint8_t* rec = row_record(cj, row);
                         raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + kHalfLat * (int)r + 16 * ch)) : zero;
                     }
+                    if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int e = at + 256 * k, row = e >> 4, ch = e & 15;
@@ -589,14 +597,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k
+                    // (the first half loaded before the wait)
+                    uint4 raw[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = at + 256 * k, row = e >> 5, ch = e & 31;
+                        const uint8_t* rec = row_record(cj, row);
+                        raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
+                    }
+                    if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        uint4 raw[4];
+                        if (half == 1) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int e = at + 256 * (4 * half + k), row = e >> 5, ch = e & 31;
-                            const uint8_t* rec = row_record(cj, row);
-                            raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
+                            for (int k = 0; k < 4; ++k) {
+                                const int e = at + 256 * (4 + k), row = e >> 5, ch = e & 31;
+                                const uint8_t* rec = row_record(cj, row);
+                                raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
+                            }
                         }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -609,19 +627,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 {
                     // rope: 64 rows x 4 chunks of 8 dims, 64-byte swizzle
                     const int row = at >> 2, c4 = at & 3;
-                    const uint8_t* rec = row_record(cj, row);
-                    const int rope_off = (p.fp8 ? kFp8RopeOff : 2 * kDc) + 2 * kHalfRope * (int)r;
-                    const uint4 raw = rec ? __ldg(reinterpret_cast<const uint4*>(rec + rope_off + 16 * c4)) : zero;
-                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), raw.x, raw.y, raw.z, raw.w);
+                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
                 }
                 if (at < kT) {
                     // the row's two group scales (1 for bf16 records) and the valid-row mask
-                    const uint8_t* rec = row_record(cj, at);
-                    float2 s2 = make_float2(1.f, 1.f);
-                    if (p.fp8) s2 = rec ? __ldg(reinterpret_cast<const float2*>(rec + kFp8ScaleOff + 8 * (int)r))
-                                        : make_float2(0.f, 0.f);
                     reinterpret_cast<float2*>(sm + kOffScale)[slot * kT + at] = s2;
-                    const uint32_t m = __ballot_sync(0xffffffffu, rec != nullptr);
+                    const uint32_t m = __ballot_sync(0xffffffffu, srec != nullptr);
                     if (lane == 0) reinterpret_cast<uint32_t*>(sm + kOffMask)[2 * slot + (at >> 5)] = m;
                 }
                 fence_proxy_async_smem();
