@@ -57,7 +57,9 @@ using namespace dc;
 constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 3;                // score buffers in TMEM
 constexpr int kQKAhead = 2;            // QK of tile i + 2 may run before PV of tile i
-constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
+constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners, 4 forwarders, 4 receivers
+constexpr int kScoreReaders = 12;      // owners and forwarders read each score buffer
+constexpr int kPWriters = 12;          // owners and receivers write P and finish O rows
 constexpr int kSlice = kT / 4;         // positions per warp
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr float kLazySlack = 16.0f;    // running max kept until a row max exceeds it by 2^16
@@ -192,21 +194,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kNSB; ++i) {
             mbar_init(bars.sf(i), 1);
-            mbar_init(bars.se(i), kSoftmaxThreads / 32);   // one arrive per softmax warp
+            mbar_init(bars.se(i), kScoreReaders);   // one arrive per warp reading scores
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bars.pf(i), kSoftmaxThreads / 32);
+            mbar_init(bars.pf(i), kPWriters);       // one arrive per warp writing P
             mbar_init(bars.pe(i), 1);
             mbar_init(bars.xf(i), 1);
             mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
             mbar_init(bars.lf(i), 1);
         }
         mbar_init(bars.pin_full, 1);
-        mbar_init(bars.pin_free, 8);     // one remote arrive per peer agent warp
+        mbar_init(bars.pin_free, 4);     // one remote arrive per peer receiver warp
         mbar_init(bars.q_full, 1);
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.o_full, 1);
-        mbar_init(bars.o_free, kSoftmaxThreads / 32);
+        mbar_init(bars.o_free, kPWriters);   // one arrive per warp finishing O rows
         mbar_init(bars.mma_drain, 1);
         fence_mbar_init();
     }
@@ -420,13 +422,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        // O rows of this warp (its 64 columns) times alpha, once PV of page i - 1 has completed
-        auto rescale_o = [&](int i, float alpha) {
+        // O rows of this warp (columns [col0, col0 + 32 n)) times alpha, once PV of page i - 1
+        // has completed
+        auto rescale_o = [&](int i, float alpha, int col0, int n) {
             if (!wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) return;
             tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const uint32_t col = kTmemO + 64 * ts + 32 * cc;
+            for (int cc = 0; cc < n; ++cc) {
+                const uint32_t col = kTmemO + col0 + 32 * cc;
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_off + col, o);
                 tmem_wait_ld();
@@ -448,19 +451,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
         };
 
-        // O rows of this warp normalised by l (row sum) into the output or a partial slot
-        auto epilogue_rows = [&](int seg, const Cursor& cu, bool partial, float l_row) {
+        // O rows of this warp (columns [col0, col0 + 32 n)) normalised by l (row sum) into the
+        // output or a partial slot
+        auto epilogue_rows = [&](int seg, const Cursor& cu, bool partial, float l_row, int col0, int n) {
             const int slot = 2 * c + (seg == 0 ? 0 : 1);
             if (!wwait(bars.o_full, seg & 1, 12)) return;
             tc_fence_after();
             const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
             const size_t row = (size_t)cu.b * kHeads + h;
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < n; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kTmemO + 64 * ts + 32 * cc, o);
+                tmem_ld32(tmem + lane_off + kTmemO + col0 + 32 * cc, o);
                 tmem_wait_ld();
-                const int col = (int)r * kHalfLat + 64 * ts + 32 * cc;
+                const int col = (int)r * kHalfLat + col0 + 32 * cc;
                 if (!partial) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
 #pragma unroll
@@ -488,36 +492,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int seg = 0;
         bool cut_front = false;
 
-        if (!owner) {
-            // ------------------------------------------------------------ agents
+        if (!owner && ts < 2) {
+            // ------------------------------------------------------------ forwarders
+            // this CTA's partial scores of the peer's heads to the peer, 32 positions per warp
             const uint32_t x_remote = mapa(sbase + kOffX, peer);
             const uint32_t xfull_remote = mapa(bars.x_full, peer);
-            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
-            const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
-            // forward this CTA's partial scores of page i (the peer's heads) to the peer
-            auto forward = [&](int i) {
-                uint32_t v[16];
-                if (!load_s(i, v)) return;
+            for (int i = 0; i < n_local; ++i) {
+                const int sb = i % kNSB;
+                if (!wwait(bars.sf(sb), (i / kNSB) & 1, 7)) continue;
+                uint32_t v[32];
+                tc_fence_after();
+                tmem_ld32(tmem + lane_off + kTmemS + sb * kT + 32 * ts, v);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.se(sb));
                 const int xb = i & 1;
-                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) return;
+                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) continue;
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    st_async_v4(x_remote + xb * kXBytes + ((4 * ts + g) * kOwned + hh) * 16,
+                for (int g = 0; g < 8; ++g)
+                    st_async_v4(x_remote + xb * kXBytes + ((8 * ts + g) * kOwned + hh) * 16,
                                 xfull_remote + 8 * xb, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-            };
-            if (n_local > 0) forward(0);
+            }
+        } else if (!owner) {
+            // ------------------------------------------------------------ receivers
+            // the peer's P of its heads into tensor memory (32 positions per warp), the rescales
+            // it asks for, and those O rows' epilogue (128 columns per warp)
+            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
+            const int rts = ts - 2;
+            const bool lead = (rts == 0 && lg == 2 * (int)peer && lane == 0);
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
-                if (i + 1 < n_local) forward(i + 1);
                 const bool first = cu.first();
                 if (first) cut_front = cu.t > 0;
-                // the peer's P of its heads for page i, and its rescale factors
                 if (lead && !s_abort) mbar_arrive_expect_tx(bars.pin_full, kPInMsg);
                 const bool ok = wwait(bars.pin_full, i & 1, 13);
-                uint32_t pk[8];
+                uint32_t pk[16];
                 const uint8_t* pin = sm + kOffPIn;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const uint4 q = *reinterpret_cast<const uint4*>(pin + ((2 * ts + g) * kOwned + hh) * 16);
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(pin + ((4 * rts + g) * kOwned + hh) * 16);
                     pk[4 * g] = q.x;
                     pk[4 * g + 1] = q.y;
                     pk[4 * g + 2] = q.z;
@@ -526,15 +539,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float alpha = reinterpret_cast<const float*>(pin + kPInBytes)[hh];
                 __syncwarp();
                 if (lane == 0 && ok) mbar_arrive_remote_relaxed(pinfree_remote);
-                if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha);
-                store_p(i, pk);
+                if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha, 128 * rts, 4);
+                const int pb = i & 1;
+                if (!(i >= 2 && !wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11))) {
+                    tmem_st16(tmem + lane_off + kTmemP + 32 * pb + 16 * rts, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
+                }
                 if (cu.last()) {
                     const bool partial = cut_front || cu.t < cu.nt - 1;
                     // the row sums of these heads, sent by the peer's owners
                     if (lead && !s_abort) mbar_arrive_expect_tx(bars.lf(seg & 1), kOwned * 4);
                     const bool lok = wwait(bars.lf(seg & 1), (seg >> 1) & 1, 14);
                     const float l_row = lok ? reinterpret_cast<const float*>(sm + kOffLIn)[(seg & 1) * kOwned + hh] : 0.f;
-                    epilogue_rows(seg, cu, partial, l_row);
+                    epilogue_rows(seg, cu, partial, l_row, 128 * rts, 4);
                     ++seg;
                 }
             }
@@ -611,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
                     if (!first) {
                         alpha = grow ? ex2(m_used - m_new) : 1.0f;
-                        if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha);
+                        if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha, 64 * ts, 2);
                         l_part *= alpha;
                     }
                     m_used = m_new;
@@ -662,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (!partial) p.lse[row] = L;
                         else p.lse_part[(size_t)(2 * c + (seg == 0 ? 0 : 1)) * kHeads + h] = L;
                     }
-                    epilogue_rows(seg, cu, partial, l_row);
+                    epilogue_rows(seg, cu, partial, l_row, 64 * ts, 2);
                     ++seg;
                 }
             }
