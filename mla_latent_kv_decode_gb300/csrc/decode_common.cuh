@@ -123,6 +123,10 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t remo
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
 // Clusters for a batch: at most one per SM pair, at least kMinTilesPerCluster tiles each.
 inline int clusters_for_tiles(long long w_max, int sms) {
     long long c = sms / 2;

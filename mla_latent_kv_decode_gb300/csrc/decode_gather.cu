@@ -163,10 +163,6 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t (&o)[8])
         }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_gather_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                          const __grid_constant__ CUtensorMap tm_qrope, GatherParams p) {

@@ -11,24 +11,30 @@
 // Capacity drives the design.  O (128 x 512 fp32) fills all 512 columns of one SM's tensor memory
 // and Q (128 x 576 bf16, 144 KB) most of its shared memory, so the work runs on clusters of two
 // CTAs, r = 0, 1.  CTA r owns latent dims [256 r, 256 r + 256) and rope dims [32 r, 32 r + 32):
-//   * it streams only its 288 columns of every cached row (576 B per position) through a 3-page
-//     TMA ring, and holds only its half of Q (72 KB);
-//   * S_r = Q_r K_r^T is a partial score over its 288 dims, for all 128 heads (18 MMAs of
-//     128x64x16 per page);
-//   * O_r[128 x 256] += P V_r (4 MMAs of 128x256x16, P read from tensor memory), V_r being the
+//   * it streams only its 288 columns of every cached row (576 B per position) through a 4-page
+//     TMA ring, and holds only its half of Q: the latent part in tensor memory (written by the
+//     softmax warps, which read it from global memory once per request), the rope part in shared
+//     memory;
+//   * S_r = Q_r K_r^T is a partial score over its 288 dims, for all 128 heads (16 MMAs of
+//     128x64x16 with Q from tensor memory and 2 with Q from shared memory per page);
+//   * O_r[128 x 256] += P V_r (4 MMAs of 128x256x16, P and V from shared memory), V_r being the
 //     latent half already in the stage: nothing is loaded twice and no FLOP is repeated.
 // The softmax is split by heads: CTA r finishes heads [64 r, 64 r + 64) ("owned" heads).  Per page
 // it receives the peer's partial scores of its owned heads (16 KB fp32) through distributed shared
-// memory, computes P for them, and sends that P (8 KB bf16) back, so that each CTA ends up with P
-// for all 128 heads in its tensor memory.  That halves both the exchange and the exponentials
-// against exchanging all scores.
+// memory, computes P for them into its own P buffer and copies those rows (8 KB bf16, one bulk
+// copy per 32 heads) into the peer's, so that each CTA ends up with P for all 128 heads.  That
+// halves both the exchange and the exponentials against exchanging all scores.  Each CTA's MMA
+// issuer signals the completion of its PV to both CTAs (the buffer is free once both are done).
 // The online softmax runs in the log2 domain with a lazily updated running max: the max of a
 // segment's first page is kept until a later score exceeds it by 2^16, so the common page needs
 // no row reduction and never touches O; a vote among the warps sharing a head detects the rare
-// page that does, and the rescale factor travels with P to the peer.
+// page that does.  Its rescale factors travel with P; the peer's MMA issuer reads them and, when
+// one differs from 1, has that CTA's receiver warps rescale those O rows before the page's PV.
+// O is normalised by the sum of the bf16 P values the PV multiplied (the weights sum to one
+// exactly), the log-sum-exp uses the sum of the fp32 values.
 //
-// Tensor memory (512 columns): O_r [0, 256), three score buffers [256 + 64 k), two P buffers
-// [448 + 32 k) (64 bf16 per lane in 32 columns).
+// Tensor memory (512 columns): O_r [0, 256), two score buffers [256 + 64 k), Q_r latent
+// [384, 512) (two bf16 per column).
 //
 // Scheduling: the grid is a fixed set of C clusters (at most one per SM pair).  The pages of all
 // requests form one stream of W tiles; cluster c takes tiles [c W / C, (c + 1) W / C), so every
@@ -39,9 +45,9 @@
 //
 // Warp roles (576 threads): warp 0 TMA producer; warp 1 MMA issuer (+ TMEM owner); warps 2-17:
 // thread = head = TMEM lane, four warps per 32-lane group, 16 positions of a page each.  The 8
-// warps on the owned heads' lanes run the softmax ("owners"); the 8 on the other heads' lanes
-// ("agents") forward this CTA's partial scores of those heads to the peer, place the P the peer
-// sends back into tensor memory and finish those O rows.  Every wait is bounded: on expiry the
+// warps on the owned heads' lanes run the softmax ("owners"); on the other heads' lanes four
+// "forwarders" send this CTA's partial scores of those heads to the peer and four "receivers"
+// apply the rare rescales and finish those O rows.  Every wait is bounded: on expiry the
 // kernel records MLA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM, returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -54,12 +60,13 @@ namespace {
 using namespace ptx;
 using namespace dc;
 
-constexpr int kNS = 3;                 // KV ring stages (pages)
-constexpr int kNSB = 3;                // score buffers in TMEM
-constexpr int kQKAhead = 2;            // QK of tile i + 2 may run before PV of tile i
+constexpr int kNS = 4;                 // KV ring stages (pages)
+constexpr int kNSB = 2;                // score buffers in TMEM (read early in a page's chain)
+constexpr int kQKAhead = kNS - 1;      // QK may run this many tiles ahead of PV
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners, 4 forwarders, 4 receivers
 constexpr int kScoreReaders = 12;      // owners and forwarders read each score buffer
-constexpr int kPWriters = 12;          // owners and receivers write P and finish O rows
+constexpr int kOwnerWarps = 8;         // write P and finish the owned heads' O rows
+constexpr int kORowWarps = 12;         // owners and receivers finish O rows
 constexpr int kSlice = kT / 4;         // positions per warp
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr float kLazySlack = 16.0f;    // running max kept until a row max exceeds it by 2^16
@@ -69,32 +76,34 @@ constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256)
 constexpr uint32_t kTmemS = 256;       // score buffer k: columns [256 + 64 k, 320 + 64 k)
-constexpr uint32_t kTmemP = 448;       // P buffer k: columns [448 + 32 k, 480 + 32 k)
+constexpr uint32_t kTmemQ = 384;       // Q_r latent: columns [384, 512), two bf16 per column
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] bf16, SW128
 constexpr int kQRopeBytes = 128 * 64;                  // [128 heads x 32 dims] bf16, SW64
 constexpr int kKvLatChunk = kT * 128;                  // [64 pos x 64 dims], SW128
 constexpr int kKvRope = kT * 64;                       // [64 pos x 32 dims], SW64
 constexpr int kStageBytes = 4 * kKvLatChunk + kKvRope;  // 36864
 constexpr int kXBytes = kOwned * kT * 4;               // peer partial scores of owned heads, fp32
-constexpr int kPInBytes = kOwned * kT * 2;             // peer's P of its owned heads, bf16
-constexpr int kPInMsg = kPInBytes + kOwned * 4;        // + one rescale factor per head
-constexpr int kOffQ = 0;
-constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
-constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 73728
-constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 184320: 2 buffers [16][64][16 B]
-constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 217088: [8][64][16 B] + alpha[64]
-constexpr int kOffLIn = kOffPIn + kPInMsg;             // 225536: 2 x l[64] of the peer's heads
-constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 226048
-constexpr int kNumBars = 2 * kNS + 2 * kNSB + 4 + 4 + 2 + 2 + 5;
+constexpr int kPBytes = 128 * kT * 2;                  // P [128 heads x 64 pos] bf16, SW128
+constexpr int kPMsgBytes = 2 * (32 * 128 + 32 * 4);    // the peer's P rows and rescale factors
+constexpr int kOffQRope = 0;
+constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 8192
+constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 155648: 2 buffers [16][64][16 B]
+constexpr int kOffP = kOffX + 2 * kXBytes;             // 188416: 2 P buffers
+constexpr int kOffAlphaIn = kOffP + 2 * kPBytes;       // 221184: 2 x alpha[64] of the peer's heads
+constexpr int kOffAlphaOut = kOffAlphaIn + 2 * kOwned * 4;   // 221696: 2 x alpha[64], owned heads
+constexpr int kOffLIn = kOffAlphaOut + 2 * kOwned * 4; // 222208: 2 x l[64] of the peer's heads
+constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 222720
+constexpr int kNumBars = 2 * kNS + 2 * kNSB + 4 + 4 + 2 + 5 + 2;
 constexpr int kOffRed = kOffBar + 8 * kNumBars;        // per-head exchange between slices [4][128]
 constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+static_assert(kOffP % 1024 == 0 && kPBytes % 1024 == 0, "P buffers on 128-byte swizzle atoms");
 
-constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;       // 73728 per CTA
 
 struct TcParams {
+    const __nv_bfloat16* q_lat;   // [B][128][512]
     const int32_t* block_table;
     const int32_t* seq_lens;
     __nv_bfloat16* out;
@@ -115,9 +124,9 @@ struct Bars {
     uint32_t s_full, s_empty;     // arrays of kNSB
     uint32_t p_full, p_empty;     // arrays of 2
     uint32_t x_full, x_free;      // arrays of 2
-    uint32_t pin_full, pin_free;
     uint32_t l_full;              // array of 2
     uint32_t q_full, q_empty, o_full, o_free, mma_drain;
+    uint32_t resc_req, resc;      // a rescale of the peer's heads' O rows: asked, done
     __device__ __forceinline__ uint32_t kvf(int i) const { return kv_full + 8 * i; }
     __device__ __forceinline__ uint32_t kve(int i) const { return kv_empty + 8 * i; }
     __device__ __forceinline__ uint32_t sf(int i) const { return s_full + 8 * i; }
@@ -139,14 +148,14 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.p_empty = a; a += 16;
     b.x_full = a; a += 16;
     b.x_free = a; a += 16;
-    b.pin_full = a; a += 8;
-    b.pin_free = a; a += 8;
     b.l_full = a; a += 16;
     b.q_full = a; a += 8;
     b.q_empty = a; a += 8;
     b.o_full = a; a += 8;
     b.o_free = a; a += 8;
     b.mma_drain = a; a += 8;
+    b.resc_req = a; a += 8;
+    b.resc = a; a += 8;
     return b;
 }
 
@@ -162,6 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __shared__ volatile int s_abort;
     __shared__ int s_start_b, s_start_t;
     __shared__ long long s_W;
+    __shared__ volatile int s_resc_page;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -197,19 +207,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bars.se(i), kScoreReaders);   // one arrive per warp reading scores
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bars.pf(i), kPWriters);       // one arrive per warp writing P
-            mbar_init(bars.pe(i), 1);
+            // P ready: one arrive per owner warp (one of them with the peer's bytes)
+            mbar_init(bars.pf(i), kOwnerWarps);
+            mbar_init(bars.pe(i), 2);    // the PV completion of both CTAs of the pair
             mbar_init(bars.xf(i), 1);
             mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
             mbar_init(bars.lf(i), 1);
         }
-        mbar_init(bars.pin_full, 1);
-        mbar_init(bars.pin_free, 4);     // one remote arrive per peer receiver warp
-        mbar_init(bars.q_full, 1);
+        // per segment: the producer's rope copy (with its bytes) and every score-reading warp's
+        // share of the latent half in tensor memory
+        mbar_init(bars.q_full, 1 + kScoreReaders);
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.o_full, 1);
-        mbar_init(bars.o_free, kPWriters);   // one arrive per warp finishing O rows
+        mbar_init(bars.o_free, kORowWarps);   // one arrive per warp finishing O rows
         mbar_init(bars.mma_drain, 1);
+        mbar_init(bars.resc_req, 1);
+        mbar_init(bars.resc, 4);             // one arrive per receiver warp
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -253,10 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const int qrow = cu.b * kHeads;
-                    mbar_arrive_expect_tx(bars.q_full, kQBytes);
-                    for (int k = 0; k < 4; ++k)
-                        tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
-                                    (int)r * kHalfLat + 64 * k, qrow);
+                    mbar_arrive_expect_tx(bars.q_full, kQRopeBytes);
                     tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
                     ++seg;
                 }
@@ -277,6 +287,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tma_load_2d(st + 4 * kKvLatChunk, &tm_kv_rope, bars.kvf(s), kDc + (int)r * kHalfRope,
                             row);
                 issued = i + 1;
+                if (cu.last() && i + 1 < n_local) {
+                    // the next request's latent Q, which the softmax warps read into tensor memory
+                    // once this segment's QKs are done, into L2
+                    Cursor cn = cu;
+                    cn.next(p.seq_lens, p.max_seq_len, p.B, 0);
+                    for (int k = 0; k < 4; ++k)
+                        tma_prefetch_l2_2d(&tm_qlat, (int)r * kHalfLat + 64 * k, cn.b * kHeads);
+                }
             }
             // drain: every load issued lands before this CTA may exit
             for (int j = max(0, issued - kNS); j < issued; ++j)
@@ -300,12 +318,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lat_lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
             const uint32_t rope_lo = (uint32_t)smem_desc(0, 16, 512, kSw64);
             const uint32_t v_lo = (uint32_t)smem_desc(0, kKvLatChunk, 1024, kSw128);
-            const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
             const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
             Cursor cq, cp;
             cq.init(p.seq_lens, p.max_seq_len, 0, start_b, start_t, n_local);
             cp = cq;
             int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
+            int asked = -1, n_resc = 0;
+            bool grow = false;
             uint32_t polls = 0;
             // Poll both queues: issue the next QK (up to kQKAhead tiles ahead of PV) when its
             // inputs are ready, else the next PV when its P is ready, so that neither a late KV
@@ -329,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             for (int k = 0; k < 4; ++k)
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
-                                    mma_bf16_ss(d, lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
+                                    mma_bf16_ts(d, tmem + kTmemQ + 32 * k + 8 * kk,
                                                 lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
                                                 id_qk, (k | kk) != 0 ? 1u : 0u);
 #pragma unroll
@@ -348,14 +367,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         continue;
                     }
                 }
-                // PV of tile ip: O_r += P (tensor memory) x V_r (stage, MN-major)
+                // PV of tile ip: O_r += P (shared memory, K-major) x V_r (stage, MN-major)
                 const bool seg_first = cp.first();
                 const int pb = ip & 1;
-                const bool pv_ready = __shfl_sync(
+                bool pv_ready = __shfl_sync(
                     0xffffffffu,
                     (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
                         mbar_test(bars.pf(pb), (ip >> 1) & 1),
                     0);
+                if (pv_ready) {
+                    if (asked != ip) {
+                        // a running max of the peer's heads grew on this page (rescale factor
+                        // != 1): the receivers rescale those O rows here before this PV
+                        const float* al = reinterpret_cast<const float*>(sm + kOffAlphaIn) + pb * kOwned;
+                        grow = __any_sync(0xffffffffu, al[lane] != 1.0f || al[lane + 32] != 1.0f);
+                        if (grow && lane == 0) {
+                            s_resc_page = ip;
+                            mbar_arrive(bars.resc_req);
+                        }
+                        asked = ip;
+                    }
+                    if (grow) pv_ready = __shfl_sync(0xffffffffu, mbar_test(bars.resc, n_resc & 1), 0);
+                }
                 if (!pv_ready) {
                     if (++polls > wait_limit) {
                         if (lane == 0) fail(p.ctl, &s_abort, 6);
@@ -364,15 +397,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 polls = 0;
+                if (grow) {
+                    ++n_resc;
+                    grow = false;
+                }
                 tc_fence_after();
                 const uint32_t v = ((sbase + kOffKv + (ip % kNS) * kStageBytes) >> 4) & 0x3FFF;
+                const uint32_t pa = ((sbase + kOffP + pb * kPBytes) >> 4) & 0x3FFF;
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < kT / 16; ++kk)
-                        mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 32 * pb + 8 * kk,
+                        mma_bf16_ss(tmem + kTmemO, lat_hi | (pa + lat_lo + ((kk * 32) >> 4)),
                                     v_hi | (v + v_lo + ((kk * 16 * 128) >> 4)), id_pv,
                                     (!seg_first || kk > 0) ? 1u : 0u);
-                    mma_commit(bars.pe(pb));
+                    // P buffer pb is free once both CTAs' PV of this page is done (each CTA's
+                    // owners write their rows into both)
+                    mma_commit_mc(bars.pe(pb), 0x3);
                     mma_commit(bars.kve(ip % kNS));
                     if (cp.last()) mma_commit(bars.o_full);
                 }
@@ -403,10 +443,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][128 heads]
 
         auto wwait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+            // common case first: the phase is complete by the first try
+            if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
             bool ok = !s_abort && mbar_wait(bar, parity, wait_limit);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && lane == 0) fail(p.ctl, &s_abort, where);
             return ok;
+        };
+
+        // Q_r latent of request b into tensor memory: columns [c0, c0 + 32 n) of this warp's 32
+        // lanes (two bf16 per column, lower dim in the low half: the order of the dims in memory),
+        // then this warp's share of the segment's Q is in place
+        auto load_q = [&](int b, int c0, int n) {
+            if (__any_sync(0xffffffffu, s_abort)) return;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.q_lat + ((size_t)b * kHeads + h) * kDc + (int)r * kHalfLat + 2 * c0);
+#pragma unroll 1
+            for (int half = 0; half < n; ++half) {
+                uint32_t q[32];   // 64 dims: all eight loads in flight before the store
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 v = __ldg(src + 8 * half + k);
+                    q[4 * k] = v.x;
+                    q[4 * k + 1] = v.y;
+                    q[4 * k + 2] = v.z;
+                    q[4 * k + 3] = v.w;
+                }
+                tmem_st32(tmem + lane_off + kTmemQ + c0 + 32 * half, q);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.q_full);
         };
 
         // this CTA's partial scores of page i for the warp's 16 positions (TMEM -> registers)
@@ -438,17 +506,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_st32(tmem + lane_off + col, o);
             }
             tmem_wait_st();
-        };
-
-        // the warp's 16 P values of page i into tensor memory, then P ready for the MMA
-        auto store_p = [&](int i, const uint32_t (&pk)[8]) {
-            const int pb = i & 1;
-            if (i >= 2 && !wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11)) return;
-            tmem_st8(tmem + lane_off + kTmemP + 32 * pb + 8 * ts, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
         };
 
         // O rows of this warp (columns [col0, col0 + 32 n)) normalised by l (row sum) into the
@@ -497,7 +554,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // this CTA's partial scores of the peer's heads to the peer, 32 positions per warp
             const uint32_t x_remote = mapa(sbase + kOffX, peer);
             const uint32_t xfull_remote = mapa(bars.x_full, peer);
-            for (int i = 0; i < n_local; ++i) {
+            if (n_local > 0) load_q(cu.b, 64 * ts, 2);
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
                 const int sb = i % kNSB;
                 if (!wwait(bars.sf(sb), (i / kNSB) & 1, 7)) continue;
                 uint32_t v[32];
@@ -508,76 +566,98 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.se(sb));
                 const int xb = i & 1;
-                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) continue;
+                // already in log2 units (times scale log2(e)): the owner adds its own part with an FMA
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    st_async_v4(x_remote + xb * kXBytes + ((8 * ts + g) * kOwned + hh) * 16,
-                                xfull_remote + 8 * xb, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+                for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * p.scale_log2);
+                if (wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) {
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        st_async_v4(x_remote + xb * kXBytes + ((8 * ts + g) * kOwned + hh) * 16,
+                                    xfull_remote + 8 * xb, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+                }
+                if (cu.last() && i + 1 < n_local) {
+                    // the segment's QKs are done: the next request's Q, this warp's 64 columns
+                    Cursor cn = cu;
+                    cn.next(p.seq_lens, p.max_seq_len, p.B, 0);
+                    load_q(cn.b, 64 * ts, 2);
+                }
             }
         } else if (!owner) {
             // ------------------------------------------------------------ receivers
-            // the peer's P of its heads into tensor memory (32 positions per warp), the rescales
-            // it asks for, and those O rows' epilogue (128 columns per warp)
-            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
+            // this CTA's O rows of the peer's heads: the rare rescales the MMA issuer asks for (a
+            // running max of those heads grew by more than the slack) and each segment's
+            // epilogue, 128 columns per warp
             const int rts = ts - 2;
             const bool lead = (rts == 0 && lg == 2 * (int)peer && lane == 0);
+            int n_req = 0;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
-                const bool first = cu.first();
-                if (first) cut_front = cu.t > 0;
-                if (lead && !s_abort) mbar_arrive_expect_tx(bars.pin_full, kPInMsg);
-                const bool ok = wwait(bars.pin_full, i & 1, 13);
-                uint32_t pk[16];
-                const uint8_t* pin = sm + kOffPIn;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint4 q = *reinterpret_cast<const uint4*>(pin + ((4 * rts + g) * kOwned + hh) * 16);
-                    pk[4 * g] = q.x;
-                    pk[4 * g + 1] = q.y;
-                    pk[4 * g + 2] = q.z;
-                    pk[4 * g + 3] = q.w;
+                if (cu.first()) cut_front = cu.t > 0;
+                if (!cu.last()) continue;
+                // until the segment's last PV completes, its rescales in page order (a request
+                // always names a page of this segment: its PV waits for the rescale, and the
+                // next segment's PVs wait for this segment's epilogue)
+                uint32_t polls = 0;
+                while (!__any_sync(0xffffffffu, s_abort)) {
+                    if (__shfl_sync(0xffffffffu, mbar_test(bars.o_full, seg & 1), 0)) break;
+                    if (__shfl_sync(0xffffffffu, mbar_test(bars.resc_req, n_req & 1), 0)) {
+                        const int ir = s_resc_page;
+                        ++n_req;
+                        const float alpha =
+                            reinterpret_cast<const float*>(sm + kOffAlphaIn)[(ir & 1) * kOwned + hh];
+                        rescale_o(ir, alpha, 128 * rts, 4);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.resc);
+                        polls = 0;
+                        continue;
+                    }
+                    if (++polls > wait_limit) {
+                        if (lane == 0) fail(p.ctl, &s_abort, 13);
+                        break;
+                    }
+                    __nanosleep(32);
                 }
-                const float alpha = reinterpret_cast<const float*>(pin + kPInBytes)[hh];
-                __syncwarp();
-                if (lane == 0 && ok) mbar_arrive_remote_relaxed(pinfree_remote);
-                if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha, 128 * rts, 4);
-                const int pb = i & 1;
-                if (!(i >= 2 && !wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11))) {
-                    tmem_st16(tmem + lane_off + kTmemP + 32 * pb + 16 * rts, pk);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0 && !s_abort) mbar_arrive(bars.pf(pb));
-                }
-                if (cu.last()) {
-                    const bool partial = cut_front || cu.t < cu.nt - 1;
-                    // the row sums of these heads, sent by the peer's owners
-                    if (lead && !s_abort) mbar_arrive_expect_tx(bars.lf(seg & 1), kOwned * 4);
-                    const bool lok = wwait(bars.lf(seg & 1), (seg >> 1) & 1, 14);
-                    const float l_row = lok ? reinterpret_cast<const float*>(sm + kOffLIn)[(seg & 1) * kOwned + hh] : 0.f;
-                    epilogue_rows(seg, cu, partial, l_row, 128 * rts, 4);
-                    ++seg;
-                }
+                const bool partial = cut_front || cu.t < cu.nt - 1;
+                // the row sums of these heads, sent by the peer's owners
+                if (lead && !s_abort) mbar_arrive_expect_tx(bars.lf(seg & 1), kOwned * 4);
+                const bool lok = wwait(bars.lf(seg & 1), (seg >> 1) & 1, 14);
+                const float l_row = lok ? reinterpret_cast<const float*>(sm + kOffLIn)[(seg & 1) * kOwned + hh] : 0.f;
+                epilogue_rows(seg, cu, partial, l_row, 128 * rts, 4);
+                ++seg;
             }
         } else {
             // ------------------------------------------------------------ owners
-            const uint32_t pin_remote = mapa(sbase + kOffPIn, peer);
-            const uint32_t pinfull_remote = mapa(bars.pin_full, peer);
+            const uint32_t p_remote = mapa(sbase + kOffP, peer);
+            const uint32_t ain_remote = mapa(sbase + kOffAlphaIn, peer);
+            const uint32_t pfull_remote = mapa(bars.p_full, peer);
             const uint32_t xfree_remote = mapa(bars.x_free, peer);
             const uint32_t lin_remote = mapa(sbase + kOffLIn, peer);
             const uint32_t lfull_remote = mapa(bars.l_full, peer);
             const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
-            float m_used = -INFINITY, l_part = 0.f;
+            // row sums of P: l_part of the fp32 values (the log-sum-exp), lr_part of the bf16 values
+            // the PV multiplies (the output's normaliser, so that the weights applied to the rows
+            // sum to one exactly; with a running max below the true max the dominant P carries a
+            // bf16 rounding that would otherwise show in the output)
+            float m_used = -INFINITY, l_part = 0.f, lr_part = 0.f;
+            if (n_local > 0) load_q(cu.b, 32 * ts, 1);
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
                 const int xb = i & 1;
                 const bool first = cu.first();
                 if (first) {
                     m_used = -INFINITY;
                     l_part = 0.f;
+                    lr_part = 0.f;
                     cut_front = cu.t > 0;   // the request started before this cluster's range
                 }
                 uint32_t v[16];
                 const bool sok = load_s(i, v);
+                if (cu.last() && i + 1 < n_local) {
+                    // the segment's QKs are done: the next request's Q, this warp's 32 columns
+                    Cursor cn = cu;
+                    cn.next(p.seq_lens, p.max_seq_len, p.B, 0);
+                    load_q(cn.b, 32 * ts, 1);
+                }
                 // the peer's partial scores of these heads for page i
                 if (lead && !s_abort) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
                 const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
@@ -587,10 +667,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * kOwned + hh) * 16);
-                    x[4 * g] = (__uint_as_float(v[4 * g]) + q.x) * p.scale_log2;
-                    x[4 * g + 1] = (__uint_as_float(v[4 * g + 1]) + q.y) * p.scale_log2;
-                    x[4 * g + 2] = (__uint_as_float(v[4 * g + 2]) + q.z) * p.scale_log2;
-                    x[4 * g + 3] = (__uint_as_float(v[4 * g + 3]) + q.w) * p.scale_log2;
+                    x[4 * g] = fmaf(__uint_as_float(v[4 * g]), p.scale_log2, q.x);
+                    x[4 * g + 1] = fmaf(__uint_as_float(v[4 * g + 1]), p.scale_log2, q.y);
+                    x[4 * g + 2] = fmaf(__uint_as_float(v[4 * g + 2]), p.scale_log2, q.z);
+                    x[4 * g + 3] = fmaf(__uint_as_float(v[4 * g + 3]), p.scale_log2, q.w);
+                }
+                // positions past the end of the request take no weight
+                if (nv < 16) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if (t >= nv) x[t] = -INFINITY;
                 }
                 // every loaded value has been consumed: hand the exchange buffer back to the peer
                 __syncwarp();
@@ -601,29 +687,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // the rare path, as does every segment start.  There the exact page row max over
                 // the four slices raises m where it exceeds m by more than the slack, O is rescaled
                 // here and, through alpha sent with P, in the peer, and P is computed again.
+                // both CTAs' PV of page i - 2 has completed: P buffer i % 2 is free here and there
+                const int pb = i & 1;
+                const bool pok = i < 2 || wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11);
                 float alpha = 1.0f;
-                float psum;
+                float psum, prsum;
                 uint32_t pk[8];
+                // this warp's 16 P of its lane's row: 16-byte chunks 2 ts, 2 ts + 1 of the 128-byte
+                // row (chunk c stored at c ^ (row % 8): 128-byte swizzle), and the rescale factor
+                const int lrow = lg * 32 + lane;   // P row = TMEM lane
+                uint8_t* prow = sm + kOffP + pb * kPBytes + lrow * 128;
+                auto write_p = [&]() {
+                    if (!pok) return;
+                    st_shared_v4(prow + (((2 * ts) ^ (lrow & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                    st_shared_v4(prow + (((2 * ts + 1) ^ (lrow & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+                    if (ts == 0) reinterpret_cast<float*>(sm + kOffAlphaOut)[pb * kOwned + hh] = alpha;
+                    fence_proxy_async_smem();
+                };
+                // (m = -inf only before a segment's first page has set it: P is then recomputed)
                 auto exp_page = [&]() {
-                    psum = 0.f;
+                    const float m = m_used == -INFINITY ? INFINITY : m_used;
+                    float s0 = 0.f, s1 = 0.f, r0 = 0.f, r1 = 0.f;
 #pragma unroll
                     for (int t = 0; t < 16; t += 2) {
-                        float p0 = 0.f, p1 = 0.f;
-                        if (m_used != -INFINITY) {
-                            p0 = t < nv ? ex2(x[t] - m_used) : 0.f;
-                            p1 = t + 1 < nv ? ex2(x[t + 1] - m_used) : 0.f;
-                        }
-                        psum += p0 + p1;
+                        const float p0 = ex2(x[t] - m), p1 = ex2(x[t + 1] - m);
+                        s0 += p0;
+                        s1 += p1;
                         pk[t / 2] = pack_bf16x2(p0, p1);
+                        r0 += __uint_as_float(pk[t / 2] << 16);
+                        r1 += __uint_as_float(pk[t / 2] & 0xFFFF0000u);
                     }
+                    psum = s0 + s1;
+                    prsum = r0 + r1;
                 };
                 exp_page();
+                write_p();
                 const bool need = first || !(psum <= 65536.0f);
                 if (bar_red_or(bar_vote, 128, need)) {
                     float mx = -INFINITY;
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        if (t < nv) mx = fmaxf(mx, x[t]);
+                    for (int t = 0; t < 16; ++t) mx = fmaxf(mx, x[t]);
                     red[ts * 128 + h] = mx;
                     named_bar_sync(bar_sync, 128);
                     const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
@@ -633,12 +736,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         alpha = grow ? ex2(m_used - m_new) : 1.0f;
                         if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha, 64 * ts, 2);
                         l_part *= alpha;
+                        lr_part *= alpha;
                     }
                     m_used = m_new;
-                    named_bar_sync(bar_sync, 128);   // red[] rows of this lane group are free again
                     exp_page();
+                    write_p();
+                    // red[] rows of this lane group are free again, its final P rows in place
+                    named_bar_sync(bar_sync, 128);
                 }
                 l_part += psum;
+                lr_part += prsum;
                 // positions past the end of the request: zero their V rows so that
                 // 0 * (stale bytes) cannot poison O (QK of this page has completed, PV has not
                 // started); the owner warps of both lane groups share the rows
@@ -654,35 +761,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();
                 }
-                // P of these heads to the peer (its P input), once it has taken the previous one
-                if (wwait(bars.pin_free, (i & 1) ^ 1, 15)) {
-#pragma unroll
-                    for (int g = 0; g < 2; ++g)
-                        st_async_v4(pin_remote + ((2 * ts + g) * kOwned + hh) * 16, pinfull_remote,
-                                    pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-                    if (ts == 0)
-                        st_async_b32(pin_remote + kPInBytes + hh * 4, pinfull_remote, __float_as_uint(alpha));
+                // the lane group's P rows and rescale factors (all four warps wrote theirs before
+                // the vote or the barrier after the recompute) into the peer's P buffer
+                if (ts == 0 && lane == 0 && pok && !s_abort) {
+                    const uint32_t off = pb * kPBytes + lg * 32 * 128;
+                    bulk_copy_s2c(p_remote + off, sbase + kOffP + off, 32 * 128, pfull_remote + 8 * pb);
+                    const uint32_t aoff = (pb * kOwned + (lg & 1) * 32) * 4;
+                    bulk_copy_s2c(ain_remote + aoff, sbase + kOffAlphaOut + aoff, 32 * 4, pfull_remote + 8 * pb);
                 }
-                store_p(i, pk);
+                // P ready for this CTA's PV (the lead arrival also expects the peer's bytes)
+                __syncwarp();
+                if (lane == 0 && pok && !s_abort) {
+                    if (lead) mbar_arrive_expect_tx(bars.pf(pb), kPMsgBytes);
+                    else mbar_arrive(bars.pf(pb));
+                }
 
                 if (cu.last()) {
                     // ------------------------------------------------------ segment epilogue
                     const bool partial = cut_front || cu.t < cu.nt - 1;
+                    // (the other CTA's heads' entries of red[] hold the second sum)
                     red[ts * 128 + h] = l_part;
+                    red[ts * 128 + (h ^ kOwned)] = lr_part;
                     named_bar_sync(bar_sync, 128);
                     const float l_row = (red[h] + red[128 + h]) + (red[256 + h] + red[384 + h]);
+                    const int hr = h ^ kOwned;
+                    const float lr_row = (red[hr] + red[128 + hr]) + (red[256 + hr] + red[384 + hr]);
                     named_bar_sync(bar_sync, 128);
-                    // the row sums of these heads to the peer, which finishes its O rows of them
+                    // the normalisers of these heads to the peer, which finishes its O rows of them
                     if (ts == 0 && !s_abort)
                         st_async_b32(lin_remote + ((seg & 1) * kOwned + hh) * 4,
-                                     lfull_remote + 8 * (seg & 1), __float_as_uint(l_row));
+                                     lfull_remote + 8 * (seg & 1), __float_as_uint(lr_row));
                     const float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
                     if (ts == 0) {
                         const size_t row = (size_t)cu.b * kHeads + h;
                         if (!partial) p.lse[row] = L;
                         else p.lse_part[(size_t)(2 * c + (seg == 0 ? 0 : 1)) * kHeads + h] = L;
                     }
-                    epilogue_rows(seg, cu, partial, l_row, 64 * ts, 2);
+                    epilogue_rows(seg, cu, partial, lr_row, 64 * ts, 2);
                     ++seg;
                 }
             }
@@ -697,6 +812,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (elect_one()) {
             mma_commit(bars.mma_drain);
             if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
+            // the peer's PV completion signals of the last two pages have landed here
+            if (!s_abort)
+                for (int j = max(0, n_local - 2); j < n_local; ++j)
+                    mbar_wait(bars.pe(j & 1), (j >> 1) & 1, kDrainLimit);
         }
     }
     __syncwarp();
@@ -826,6 +945,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
     float* lse_part = o_part + (size_t)2 * C * kHeads * kDc;
     int32_t* meta = reinterpret_cast<int32_t*>(lse_part + (size_t)2 * C * kHeads);
     TcParams p;
+    p.q_lat = a.q_lat;
     p.block_table = a.block_table;
     p.seq_lens = a.seq_lens;
     p.out = a.out;

@@ -122,6 +122,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// Prefetch a 2D tile into L2 (no shared memory written, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (tcgen05.mma operands, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -177,6 +185,16 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// Arrive once on the barrier at shared-memory offset `bar` of every CTA in `cta_mask` (cluster
+// ranks) when all MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
         : "memory");
 }
 
@@ -307,6 +325,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t remot
         "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
             remote_addr),
         "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+        : "memory");
+}
+
+// Bulk copy (async proxy) of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory to a shared::cluster address, completing the bytes on the barrier `bar` of
+// the destination CTA.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "r"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 

@@ -22,14 +22,14 @@ def torch():
     return t
 
 
-def _custom(name, fmt, seq_lens, seed, topk_idx=None, shuffle=True, appended=0):
+def _custom(name, fmt, seq_lens, seed, topk_idx=None, shuffle=True, appended=0, scale=None):
     seq = np.asarray(seq_lens, dtype=np.int32)
     pages = int(((seq.astype(np.int64) + 63) // 64).sum())
     perm = synth.permutation(seed, synth.STREAM_PERM, pages) if shuffle else None
     bt, total = synth._block_table(seq, perm)
     return synth.Workload(name, fmt, len(seq), 128, seed, seq, bt, total,
                           topk_idx=None if topk_idx is None else np.asarray(topk_idx, np.int32),
-                          appended=appended)
+                          appended=appended, scale=synth.SCALE if scale is None else scale)
 
 
 def _run_full_compare(torch, w, what, replicas=1):
@@ -70,6 +70,16 @@ def test_split_kv_long_request(torch):
 def test_fp8_mixed_batch_with_append(torch):
     w = _custom("fp8", 1, [300, 64, 1, 777], seed=23, appended=64)
     _run_full_compare(torch, w, "fp8 mixed")
+
+
+def test_running_max_growth(torch):
+    """Scores spread wide (softmax scale 4 instead of 1/sqrt(192)): a head's running max grows by
+    more than the kernels' lazy-max slack (2^16) on most pages (about 360 growth events over the
+    128 heads of the 4,096-token request), so O rows are rescaled mid-segment on both CTAs of a
+    pair, and requests split across clusters merge partials with very different maxima."""
+    for fmt in (0, 1):
+        w = _custom(f"growth{fmt}", fmt, [4096, 3000, 130, 8000, 65], seed=26, scale=4.0)
+        _run_full_compare(torch, w, f"running-max growth fmt={fmt}")
 
 
 def test_topk_sparse_with_padding(torch):
