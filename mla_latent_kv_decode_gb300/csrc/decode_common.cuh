@@ -137,10 +137,10 @@ inline int clusters_for_tiles(long long w_max, int sms) {
 
 }  // namespace dc
 
-// Shared by the tensor-core decode kernels (defined in decode_tc.cu).
-__global__ void merge_slots_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                                   const int32_t* __restrict__ meta, __nv_bfloat16* __restrict__ out,
-                                   float* __restrict__ lse);
+// Shared by the tensor-core decode kernels (defined in decode_tc.cu): the merge of split
+// requests' partial slots into the output (B requests, C clusters), on stream st.
+cudaError_t launch_merge_slots(const float* o_part, const float* lse_part, const int32_t* meta,
+                               __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st);
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
 

@@ -905,13 +905,10 @@ cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cu
     p.B = a.B;
     p.fp8 = a.fmt == MLA_KV_FP8_MIXED ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const int64_t blocks = (int64_t)a.B * kHeads;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     decode_gather_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    merge_slots_kernel<<<(unsigned)blocks, 128, 0, st>>>(o_part, lse_part, meta, a.out, a.lse);
-    return cudaGetLastError();
+    return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st);
 }
 
 }  // namespace mla

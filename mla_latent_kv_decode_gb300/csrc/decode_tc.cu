@@ -687,9 +687,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // the rare path, as does every segment start.  There the exact page row max over
                 // the four slices raises m where it exceeds m by more than the slack, O is rescaled
                 // here and, through alpha sent with P, in the peer, and P is computed again.
-                // both CTAs' PV of page i - 2 has completed: P buffer i % 2 is free here and there
                 const int pb = i & 1;
-                const bool pok = i < 2 || wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11);
+                bool pok = true;   // P buffer pb is free (checked once P is computed)
                 float alpha = 1.0f;
                 float psum, prsum;
                 uint32_t pk[8];
@@ -721,6 +720,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     prsum = r0 + r1;
                 };
                 exp_page();
+                // both CTAs' PV of page i - 2 has completed: P buffer i % 2 is free here and there
+                pok = i < 2 || wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11);
                 write_p();
                 const bool need = first || !(psum <= 65536.0f);
                 if (bar_red_or(bar_vote, 128, need)) {
@@ -831,50 +832,133 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Finish of mla_decode: requests cut by cluster range boundaries get their partials merged,
 // requests with no visible position get zeros and lse = -inf; the rest were finished by the
-// decode kernel.  Block (request b, head h).  Request b's partials sit in slot first (2 c_lo or
-// 2 c_lo + 1) and slots 2c for the following clusters c up to c_hi.
-__global__ void __launch_bounds__(128) merge_slots_kernel(const float* __restrict__ o_part,
-                                                          const float* __restrict__ lse_part,
-                                                          const int32_t* __restrict__ meta,
-                                                          __nv_bfloat16* __restrict__ out,
-                                                          float* __restrict__ lse) {
-    const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
-    const int first = meta[2 * b], c_hi = meta[2 * b + 1];
+// decode kernel.  Request b's partials sit in slot first (2 c_lo or 2 c_lo + 1) and slots 2c for
+// the following clusters c up to c_hi.  Two shapes, both built so that the loads of a step are
+// independent (a few memory latencies in all rather than one per slot):
+//   * wide (few slots per request, many requests): block (b, heads 8 g .. 8 g + 7), warp = head;
+//     lanes take slots for the log-sum-exp, then columns for the weighted row sum;
+//   * deep (many slots, few requests): block (b, h); every warp forms the log-sum-exp, warp w
+//     accumulates slots w, w + 8, ... over the whole row and shared memory sums the eight rows.
+__device__ __forceinline__ float merge_lse(const float* __restrict__ lse_part, int first, int c_lo, int n,
+                                           int h, int lane) {
+    float m = -INFINITY;
+    for (int k = lane; k < n; k += 32)
+        m = fmaxf(m, __ldg(lse_part + (size_t)(k == 0 ? first : 2 * (c_lo + k)) * kHeads + h));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (m == -INFINITY) return -INFINITY;
+    float l = 0.f;
+    for (int k = lane; k < n; k += 32)
+        l += expf(__ldg(lse_part + (size_t)(k == 0 ? first : 2 * (c_lo + k)) * kHeads + h) - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    return m + logf(l);
+}
+
+// acc (this lane's columns 4 lane + 128 j of row h) += the weighted rows of slots k0, k0 + dk, ...
+__device__ __forceinline__ void merge_rows(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                                           int first, int c_lo, int n, int k0, int dk, int h, int lane,
+                                           float L, float4 (&acc)[4]) {
+#pragma unroll 4
+    for (int k = k0; k < n; k += dk) {
+        const int slot = k == 0 ? first : 2 * (c_lo + k);
+        const float w = expf(__ldg(lse_part + (size_t)slot * kHeads + h) - L);
+        const float4* src = reinterpret_cast<const float4*>(o_part + ((size_t)slot * kHeads + h) * kDc) + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 o = __ldg(src + 32 * j);
+            acc[j].x += w * o.x;
+            acc[j].y += w * o.y;
+            acc[j].z += w * o.z;
+            acc[j].w += w * o.w;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) merge_wide_kernel(const float* __restrict__ o_part,
+                                                         const float* __restrict__ lse_part,
+                                                         const int32_t* __restrict__ meta,
+                                                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    const int b = blockIdx.x >> 4;
+    const int lane = threadIdx.x & 31;
+    const int h = (blockIdx.x & 15) * 8 + (threadIdx.x >> 5);
+    const int first = __ldg(meta + 2 * b), c_hi = __ldg(meta + 2 * b + 1);
     const int c_lo = first >> 1;
     if (first >= 0 && c_hi == c_lo) return;   // inside one range: already final
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;
     if (first >= 0) {
         const int n = c_hi - c_lo + 1;
-        float m = -INFINITY;
-        for (int k = 0; k < n; ++k) {
-            const int slot = k == 0 ? first : 2 * (c_lo + k);
-            m = fmaxf(m, lse_part[(size_t)slot * kHeads + h]);
-        }
-        if (m != -INFINITY) {
-            float l = 0.f;
-            for (int k = 0; k < n; ++k) {
-                const int slot = k == 0 ? first : 2 * (c_lo + k);
-                l += expf(lse_part[(size_t)slot * kHeads + h] - m);
-            }
-            L = m + logf(l);
-            for (int k = 0; k < n; ++k) {
-                const int slot = k == 0 ? first : 2 * (c_lo + k);
-                const float w = expf(lse_part[(size_t)slot * kHeads + h] - L);
-                if (w == 0.f) continue;
-                const float4 o = reinterpret_cast<const float4*>(o_part + ((size_t)slot * kHeads + h) * kDc)[threadIdx.x];
-                acc.x += w * o.x;
-                acc.y += w * o.y;
-                acc.z += w * o.z;
-                acc.w += w * o.w;
-            }
-        }
+        L = merge_lse(lse_part, first, c_lo, n, h, lane);
+        if (L != -INFINITY) merge_rows(o_part, lse_part, first, c_lo, n, 0, 1, h, lane, L, acc);
     }
-    uint2 packed;
-    packed.x = pack_bf16x2(acc.x, acc.y);
-    packed.y = pack_bf16x2(acc.z, acc.w);
-    reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc)[threadIdx.x] = packed;
+    uint2* dst = reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc) + lane;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint2 packed;
+        packed.x = pack_bf16x2(acc[j].x, acc[j].y);
+        packed.y = pack_bf16x2(acc[j].z, acc[j].w);
+        dst[32 * j] = packed;
+    }
+    if (lane == 0) lse[(size_t)b * kHeads + h] = L;
+}
+
+__global__ void __launch_bounds__(256) merge_deep_kernel(const float* __restrict__ o_part,
+                                                         const float* __restrict__ lse_part,
+                                                         const int32_t* __restrict__ meta,
+                                                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    __shared__ float4 red[8][kDc / 4];
+    const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int first = __ldg(meta + 2 * b), c_hi = __ldg(meta + 2 * b + 1);
+    const int c_lo = first >> 1;
+    if (first >= 0 && c_hi == c_lo) return;   // inside one range: already final (whole block)
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = -INFINITY;
+    if (first >= 0) {
+        const int n = c_hi - c_lo + 1;
+        L = merge_lse(lse_part, first, c_lo, n, h, lane);
+        if (L != -INFINITY) merge_rows(o_part, lse_part, first, c_lo, n, warp, 8, h, lane, L, acc);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) red[warp][lane + 32 * j] = acc[j];
+    __syncthreads();
+    if (threadIdx.x < kDc / 4) {
+        float4 t = red[0][threadIdx.x];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            const float4 u = red[w][threadIdx.x];
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(t.x, t.y);
+        packed.y = pack_bf16x2(t.z, t.w);
+        reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc)[threadIdx.x] = packed;
+    }
     if (threadIdx.x == 0) lse[(size_t)b * kHeads + h] = L;
+}
+
+cudaError_t launch_merge_slots(const float* o_part, const float* lse_part, const int32_t* meta,
+                               __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st) {
+    if (B <= 0) return cudaSuccess;
+    // a request spans about C / B + 1 cluster ranges
+    if ((C + B - 1) / B + 1 <= 8) {
+        const int64_t blocks = (int64_t)B * (kHeads / 8);
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        merge_wide_kernel<<<(unsigned)blocks, 256, 0, st>>>(o_part, lse_part, meta, out, lse);
+    } else {
+        const int64_t blocks = (int64_t)B * kHeads;
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        merge_deep_kernel<<<(unsigned)blocks, 256, 0, st>>>(o_part, lse_part, meta, out, lse);
+    }
+    return cudaGetLastError();
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -959,13 +1043,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
     p.max_seq_len = a.max_seq_len;
     p.B = a.B;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const int64_t blocks = (int64_t)a.B * kHeads;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    merge_slots_kernel<<<(unsigned)blocks, 128, 0, st>>>(o_part, lse_part, meta, a.out, a.lse);
-    return cudaGetLastError();
+    return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st);
 }
 
 }  // namespace mla
