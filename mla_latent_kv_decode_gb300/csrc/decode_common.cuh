@@ -142,6 +142,7 @@ inline int clusters_for_tiles(long long w_max, int sms) {
 cudaError_t launch_merge_slots(const float* o_part, const float* lse_part, const int32_t* meta,
                                __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st);
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
-               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 }  // namespace mla

@@ -60,8 +60,9 @@ namespace {
 using namespace ptx;
 using namespace dc;
 
-constexpr int kNS = 4;                 // KV ring stages (pages)
+constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 2;                // score buffers in TMEM (read early in a page's chain)
+constexpr int kNP = 2;                 // P buffers in shared memory (held until both PVs are done)
 constexpr int kQKAhead = kNS - 1;      // QK may run this many tiles ahead of PV
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners, 4 forwarders, 4 receivers
 constexpr int kScoreReaders = 12;      // owners and forwarders read each score buffer
@@ -90,12 +91,15 @@ constexpr int kPMsgBytes = 2 * (32 * 128 + 32 * 4);    // the peer's P rows and 
 constexpr int kOffQRope = 0;
 constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 8192
 constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 155648: 2 buffers [16][64][16 B]
-constexpr int kOffP = kOffX + 2 * kXBytes;             // 188416: 2 P buffers
-constexpr int kOffAlphaIn = kOffP + 2 * kPBytes;       // 221184: 2 x alpha[64] of the peer's heads
-constexpr int kOffAlphaOut = kOffAlphaIn + 2 * kOwned * 4;   // 221696: 2 x alpha[64], owned heads
-constexpr int kOffLIn = kOffAlphaOut + 2 * kOwned * 4; // 222208: 2 x l[64] of the peer's heads
-constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 222720
-constexpr int kNumBars = 2 * kNS + 2 * kNSB + 4 + 4 + 2 + 5 + 2;
+constexpr int kOffP = kOffX + 2 * kXBytes;             // kNP P buffers
+constexpr int kOffAlphaIn = kOffP + kNP * kPBytes;     // kNP x alpha[64] of the peer's heads
+constexpr int kOffAlphaOut = kOffAlphaIn + kNP * kOwned * 4;   // kNP x alpha[64], owned heads
+constexpr int kOffLIn = kOffAlphaOut + kNP * kOwned * 4;  // 2 x l[64] of the peer's heads
+// epilogue staging, 2 KB per softmax warp: [32 rows x 64 B], 64-byte swizzle (the TMA store box)
+constexpr int kOffStage = (kOffLIn + 2 * kOwned * 4 + 1023) / 1024 * 1024;
+constexpr int kStageOut = 2048;
+constexpr int kOffBar = kOffStage + 16 * kStageOut;
+constexpr int kNumBars = 2 * kNS + 2 * kNSB + 2 * kNP + 4 + 2 + 5 + 2;
 constexpr int kOffRed = kOffBar + 8 * kNumBars;        // per-head exchange between slices [4][128]
 constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -122,7 +126,7 @@ struct TcParams {
 struct Bars {
     uint32_t kv_full, kv_empty;   // arrays of kNS
     uint32_t s_full, s_empty;     // arrays of kNSB
-    uint32_t p_full, p_empty;     // arrays of 2
+    uint32_t p_full, p_empty;     // arrays of kNP
     uint32_t x_full, x_free;      // arrays of 2
     uint32_t l_full;              // array of 2
     uint32_t q_full, q_empty, o_full, o_free, mma_drain;
@@ -144,8 +148,8 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.kv_empty = a; a += 8 * kNS;
     b.s_full = a; a += 8 * kNSB;
     b.s_empty = a; a += 8 * kNSB;
-    b.p_full = a; a += 16;
-    b.p_empty = a; a += 16;
+    b.p_full = a; a += 8 * kNP;
+    b.p_empty = a; a += 8 * kNP;
     b.x_full = a; a += 16;
     b.x_free = a; a += 16;
     b.l_full = a; a += 16;
@@ -163,7 +167,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                      const __grid_constant__ CUtensorMap tm_qrope,
                      const __grid_constant__ CUtensorMap tm_kv_lat,
-                     const __grid_constant__ CUtensorMap tm_kv_rope, TcParams p) {
+                     const __grid_constant__ CUtensorMap tm_kv_rope,
+                     const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_opart,
+                     TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -206,10 +212,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bars.sf(i), 1);
             mbar_init(bars.se(i), kScoreReaders);   // one arrive per warp reading scores
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNP; ++i) {
             // P ready: one arrive per owner warp (one of them with the peer's bytes)
             mbar_init(bars.pf(i), kOwnerWarps);
             mbar_init(bars.pe(i), 2);    // the PV completion of both CTAs of the pair
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bars.xf(i), 1);
             mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
             mbar_init(bars.lf(i), 1);
@@ -369,11 +377,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 // PV of tile ip: O_r += P (shared memory, K-major) x V_r (stage, MN-major)
                 const bool seg_first = cp.first();
-                const int pb = ip & 1;
+                const int pb = ip % kNP;
                 bool pv_ready = __shfl_sync(
                     0xffffffffu,
                     (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
-                        mbar_test(bars.pf(pb), (ip >> 1) & 1),
+                        mbar_test(bars.pf(pb), (ip / kNP) & 1),
                     0);
                 if (pv_ready) {
                     if (asked != ip) {
@@ -493,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // O rows of this warp (columns [col0, col0 + 32 n)) times alpha, once PV of page i - 1
         // has completed
         auto rescale_o = [&](int i, float alpha, int col0, int n) {
-            if (!wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) return;
+            if (!wwait(bars.pe((i - 1) % kNP), ((i - 1) / kNP) & 1, 10)) return;
             tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < n; ++cc) {
@@ -509,39 +517,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         };
 
         // O rows of this warp (columns [col0, col0 + 32 n)) normalised by l (row sum) into the
-        // output or a partial slot
+        // output (bf16) or a partial slot (fp32).  The rows go out through the warp's staging
+        // buffer and TMA stores of [32 rows x 64 B] boxes (a thread holds one row, so direct
+        // stores would touch 32 lines per instruction); O is released to the next segment's PV
+        // once its last columns are in registers.
         auto epilogue_rows = [&](int seg, const Cursor& cu, bool partial, float l_row, int col0, int n) {
             const int slot = 2 * c + (seg == 0 ? 0 : 1);
-            if (!wwait(bars.o_full, seg & 1, 12)) return;
-            tc_fence_after();
-            const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
-            const size_t row = (size_t)cu.b * kHeads + h;
+            const bool ok = wwait(bars.o_full, seg & 1, 12);
+            if (ok) {
+                tc_fence_after();
+                const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
+                uint8_t* stg = sm + kOffStage + (warp - 2) * kStageOut;
+                const uint32_t stg_s = sbase + kOffStage + (warp - 2) * kStageOut;
+                uint8_t* srow = stg + lane * 64;
+                const int sw = (lane >> 1) & 3;   // 64-byte swizzle: chunk j at j ^ sw
+                const int row0 = (partial ? slot : cu.b) * kHeads + lg * 32;
+                auto put = [&](const CUtensorMap* m, int x, const uint32_t (&w)[16]) {
+                    if (lane == 0) bulk_wait_read0();   // the previous box has left the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_shared_v4(srow + ((j ^ sw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tma_store_2d(m, stg_s, x, row0);
+                };
 #pragma unroll 1
-            for (int cc = 0; cc < n; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kTmemO + col0 + 32 * cc, o);
-                tmem_wait_ld();
-                const int col = (int)r * kHalfLat + col0 + 32 * cc;
-                if (!partial) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
+                for (int cc = 0; cc < n; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + kTmemO + col0 + 32 * cc, o);
+                    tmem_wait_ld();
+                    if (cc == n - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.o_free);
+                    }
+                    const int col = (int)r * kHalfLat + col0 + 32 * cc;
+                    uint32_t w[16];
+                    if (!partial) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
+                        for (int k = 0; k < 16; ++k)
+                            w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+                        put(&tm_out, col, w);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(__uint_as_float(o[16 * hf + k]) * inv);
+                            put(&tm_opart, col + 16 * hf, w);
+                        }
+                    }
                 }
+            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.o_free);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.o_free);
         };
 
         Cursor cu;
@@ -603,7 +634,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int ir = s_resc_page;
                         ++n_req;
                         const float alpha =
-                            reinterpret_cast<const float*>(sm + kOffAlphaIn)[(ir & 1) * kOwned + hh];
+                            reinterpret_cast<const float*>(sm + kOffAlphaIn)[(ir % kNP) * kOwned + hh];
                         rescale_o(ir, alpha, 128 * rts, 4);
                         tc_fence_before();
                         __syncwarp();
@@ -687,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // the rare path, as does every segment start.  There the exact page row max over
                 // the four slices raises m where it exceeds m by more than the slack, O is rescaled
                 // here and, through alpha sent with P, in the peer, and P is computed again.
-                const int pb = i & 1;
+                const int pb = i % kNP;
                 bool pok = true;   // P buffer pb is free (checked once P is computed)
                 float alpha = 1.0f;
                 float psum, prsum;
@@ -720,8 +751,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     prsum = r0 + r1;
                 };
                 exp_page();
-                // both CTAs' PV of page i - 2 has completed: P buffer i % 2 is free here and there
-                pok = i < 2 || wwait(bars.pe(pb), ((i - 2) >> 1) & 1, 11);
+                // both CTAs' PV of page i - kNP has completed: P buffer pb is free here and there
+                pok = i < kNP || wwait(bars.pe(pb), ((i - kNP) / kNP) & 1, 11);
                 write_p();
                 const bool need = first || !(psum <= 65536.0f);
                 if (bar_red_or(bar_vote, 128, need)) {
@@ -806,6 +837,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------------- teardown
+    bulk_wait0();   // this thread's epilogue stores have completed
     if (warp == 1 && n_local > 0) {
         __syncwarp();
         // all MMAs issued by the elected lane (the lowest active one, as in the loop) are complete
@@ -813,10 +845,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (elect_one()) {
             mma_commit(bars.mma_drain);
             if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
-            // the peer's PV completion signals of the last two pages have landed here
+            // the peer's PV completion signals of the last kNP pages have landed here
             if (!s_abort)
-                for (int j = max(0, n_local - 2); j < n_local; ++j)
-                    mbar_wait(bars.pe(j & 1), (j >> 1) & 1, kDrainLimit);
+                for (int j = max(0, n_local - kNP); j < n_local; ++j)
+                    mbar_wait(bars.pe(j % kNP), (j / kNP) & 1, kDrainLimit);
         }
     }
     __syncwarp();
@@ -974,14 +1006,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
-               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+               uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw, CUtensorMapDataType dt) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+    return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1014,7 +1046,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    CUtensorMap tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope;
+    CUtensorMap tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope, tm_out, tm_opart;
     const uint64_t qrows = (uint64_t)a.B * kHeads;
     const uint64_t kv_rows = (uint64_t)a.num_pages * kPage;
     if (!encode_2d(&tm_qlat, a.q_lat, kDc, qrows, kDc * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1028,6 +1060,11 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
     float* o_part = static_cast<float*>(a.workspace);
     float* lse_part = o_part + (size_t)2 * C * kHeads * kDc;
     int32_t* meta = reinterpret_cast<int32_t*>(lse_part + (size_t)2 * C * kHeads);
+    // epilogue boxes: 32 rows x 32 bf16 of the output, 32 rows x 16 fp32 of a partial slot
+    if (!encode_2d(&tm_out, a.out, kDc, qrows, kDc * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_2d(&tm_opart, o_part, kDc, (uint64_t)2 * C * kHeads, kDc * 4, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+        return cudaErrorInvalidValue;
     TcParams p;
     p.q_lat = a.q_lat;
     p.block_table = a.block_table;
@@ -1043,7 +1080,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& plan, cudaSt
     p.max_seq_len = a.max_seq_len;
     p.B = a.B;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope, p);
+    decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_kv_lat, tm_kv_rope, tm_out,
+                                                         tm_opart, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st);
