@@ -837,7 +837,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------------- teardown
-    bulk_wait0();   // this thread's epilogue stores have completed
+    bulk_wait_read0();   // this thread's epilogue stores have read their staging buffers
     if (warp == 1 && n_local > 0) {
         __syncwarp();
         // all MMAs issued by the elected lane (the lowest active one, as in the loop) are complete
