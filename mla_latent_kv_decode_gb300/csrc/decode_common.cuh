@@ -64,14 +64,24 @@ struct Cursor {
     }
 };
 
-// The balanced schedule, run by one warp of every CTA: W = sum over requests of their tiles;
-// cluster c of C takes tiles [c W / C, (c + 1) W / C).  Returns W and this cluster's first tile
-// (request, tile).  Cluster 0's rank-0 CTA also records, per request, where its partials are:
-// meta[2b] = the first partial slot (2 c_lo or 2 c_lo + 1; -1 for a request with no tiles),
-// meta[2b + 1] = the last cluster whose range holds one of its tiles.
+// Cluster of stream index x when cluster c of C owns [floor(c W / C), floor((c + 1) W / C)).
+__device__ __forceinline__ int cluster_of(long long x, long long W, int C) {
+    long long c = ((x + 1) * C + W - 1) / W - 1;
+    return (int)(c < 0 ? 0 : (c > C - 1 ? C - 1 : c));
+}
+
+// The balanced schedule, run by one warp of every CTA.  The requests form one stream in which
+// request b > 0 takes seg_cost "start" units followed by its tiles (a request with no tiles takes
+// none; request 0 starts with the kernel): the units stand for the fixed cost of starting a
+// segment inside a cluster's range (the epilogue of the one before, the new request's first
+// page), so that a cluster whose range holds more request starts gets fewer tiles.  With W units in all, cluster c takes units [c W / C, (c + 1) W / C) and processes
+// the tiles among them.  Returns this cluster's tile count and first tile (request, tile).
+// Cluster 0's rank-0 CTA also records, per request, where its partials are: meta[2b] = the first
+// partial slot (2 c_lo if the request is that cluster's first segment, else 2 c_lo + 1; -1 for a
+// request with no tiles), meta[2b + 1] = the last cluster whose range holds one of its tiles.
 __device__ __forceinline__ void schedule_warp(const int32_t* seq_lens, int max_len, int B, int topk,
-                                              int c, int C, bool record, int32_t* meta, DevCtl* ctl,
-                                              long long* W_out, int* start_b, int* start_t) {
+                                              int seg_cost, int c, int C, bool record, int32_t* meta,
+                                              DevCtl* ctl, int* n_local, int* start_b, int* start_t) {
     const int lane = threadIdx.x & 31;
     const int per = (B + 31) / 32;
     const int b_lo = min(B, lane * per), b_hi = min(B, b_lo + per);
@@ -79,7 +89,8 @@ __device__ __forceinline__ void schedule_warp(const int32_t* seq_lens, int max_l
     for (int b = b_lo; b < b_hi; ++b) {
         const int raw = seq_lens[b];
         if ((raw < 0 || raw > max_len) && record) record_error(ctl, MLA_ERR_BOUNDS, b);
-        mine += tiles_of(clamp_len(raw, max_len), topk);
+        const int nt = tiles_of(clamp_len(raw, max_len), topk);
+        mine += nt > 0 ? nt + (b > 0 ? seg_cost : 0) : 0;
     }
     long long incl = mine;
 #pragma unroll
@@ -88,31 +99,56 @@ __device__ __forceinline__ void schedule_warp(const int32_t* seq_lens, int max_l
         if (lane >= o) incl += v;
     }
     const long long W = __shfl_sync(0xffffffffu, incl, 31);
-    const long long gb = (long long)c * W / C;
-    long long pre = incl - mine;
+    const long long g0 = (long long)c * W / C, g1 = (long long)(c + 1) * W / C;
+    long long v = incl - mine;   // start unit of request b
+    int cnt = 0, fb = B, ft = 0;
     for (int b = b_lo; b < b_hi; ++b) {
         const int nt = tiles_of(clamp_len(seq_lens[b], max_len), topk);
-        if (record) {
-            int first_slot = -1, c_hi = -1;
-            if (nt > 0) {
-                // the clusters whose ranges hold tiles pre .. pre + nt - 1
-                long long lo = ((pre + 1) * C + W - 1) / W - 1;
-                long long hi = ((pre + nt) * C + W - 1) / W - 1;
-                lo = lo < 0 ? 0 : (lo > C - 1 ? C - 1 : lo);
-                hi = hi < lo ? lo : (hi > C - 1 ? C - 1 : hi);
-                first_slot = 2 * (int)lo + ((lo * W / C) == pre ? 0 : 1);
-                c_hi = (int)hi;
+        if (nt == 0) {
+            if (record) {
+                meta[2 * b] = -1;
+                meta[2 * b + 1] = -1;
             }
-            meta[2 * b] = first_slot;
-            meta[2 * b + 1] = c_hi;
+            continue;
         }
-        if (gb < W && gb >= pre && gb < pre + nt) {
-            *start_b = b;
-            *start_t = (int)(gb - pre);
+        const int sc = b > 0 ? seg_cost : 0;
+        const long long t0 = v + sc;   // unit of the request's tile 0
+        // tiles t with t0 + t in [g0, g1)
+        const long long lo_t = g0 - t0 < 0 ? 0 : (g0 - t0 > nt ? nt : g0 - t0);
+        const long long hi_t = g1 - t0 < 0 ? 0 : (g1 - t0 > nt ? nt : g1 - t0);
+        if (hi_t > lo_t) {
+            if (fb == B) {
+                fb = b;
+                ft = (int)lo_t;
+            }
+            cnt += (int)(hi_t - lo_t);
         }
-        pre += nt;
+        if (record) {
+            const int clo = cluster_of(t0, W, C), chi = cluster_of(t0 + nt - 1, W, C);
+            // the request is cluster clo's first segment iff clo's range starts at or after the
+            // request's start units (the unit before them is the previous request's last tile)
+            const bool starts = (long long)clo * W / C >= v;
+            meta[2 * b] = 2 * clo + (starts ? 0 : 1);
+            meta[2 * b + 1] = chi;
+        }
+        v += nt + sc;
     }
-    if (lane == 31) *W_out = W;
+    // the first request (lowest b) with tiles in range, and the total
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const int ob = __shfl_xor_sync(0xffffffffu, fb, o);
+        const int ot = __shfl_xor_sync(0xffffffffu, ft, o);
+        if (ob < fb) {
+            fb = ob;
+            ft = ot;
+        }
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    }
+    if (lane == 0) {
+        *n_local = cnt;
+        *start_b = fb;
+        *start_t = ft;
+    }
 }
 
 // 4 bytes into the peer's shared memory, completing tx-bytes on its barrier.

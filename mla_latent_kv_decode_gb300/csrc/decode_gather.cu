@@ -48,6 +48,7 @@ namespace {
 using namespace ptx;
 using namespace dc;
 
+constexpr int kSegCost = 1;           // a segment start costs about one tile (schedule units)
 constexpr int kNC = 2;                 // converted tile slots
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
 constexpr int kSlice = kT / 4;         // positions per warp
@@ -172,7 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __shared__ uint32_t s_tmem_base;
     __shared__ volatile int s_abort;
     __shared__ int s_start_b, s_start_t;
-    __shared__ long long s_W;
+    __shared__ int s_n_local;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -189,11 +190,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s_abort = 0;
         s_start_b = p.B;
         s_start_t = 0;
+        s_n_local = 0;
     }
     __syncthreads();
     if (warp == 0)
-        schedule_warp(p.seq_lens, p.max_seq_len, p.B, p.topk, c, C, c == 0 && r == 0, p.meta, p.ctl,
-                      &s_W, &s_start_b, &s_start_t);
+        schedule_warp(p.seq_lens, p.max_seq_len, p.B, p.topk, kSegCost, c, C, c == 0 && r == 0, p.meta,
+                      p.ctl, &s_n_local, &s_start_b, &s_start_t);
 
     if (tid == 32) {
         for (int i = 0; i < kNC; ++i) {
@@ -227,9 +229,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the peer's barriers are initialised before any remote arrive / st.async
     const uint32_t tmem = s_tmem_base;
-    const long long W = s_W;
-    const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
-    const int n_local = (int)(g_end - g_begin);   // tiles of this cluster
+    const int n_local = s_n_local;   // tiles of this cluster
     const int start_b = s_start_b, start_t = s_start_t;
 
     if (n_local == 0 && warp >= 2) {

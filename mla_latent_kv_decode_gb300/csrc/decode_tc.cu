@@ -63,6 +63,7 @@ using namespace dc;
 constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 2;                // score buffers in TMEM (read early in a page's chain)
 constexpr int kNP = 2;                 // P buffers in shared memory (held until both PVs are done)
+constexpr int kSegCost = 4;           // a segment start costs about four pages (schedule units)
 constexpr int kQKAhead = kNS - 1;      // QK may run this many tiles ahead of PV
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners, 4 forwarders, 4 receivers
 constexpr int kScoreReaders = 12;      // owners and forwarders read each score buffer
@@ -176,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __shared__ uint32_t s_tmem_base;
     __shared__ volatile int s_abort;
     __shared__ int s_start_b, s_start_t;
-    __shared__ long long s_W;
+    __shared__ int s_n_local;
     __shared__ volatile int s_resc_page;
 
     const int tid = threadIdx.x;
@@ -197,11 +198,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s_abort = 0;
         s_start_b = p.B;
         s_start_t = 0;
+        s_n_local = 0;
     }
     __syncthreads();
     if (warp == 0)
-        schedule_warp(p.seq_lens, p.max_seq_len, p.B, 0, c, C, c == 0 && r == 0, p.meta, p.ctl, &s_W,
-                      &s_start_b, &s_start_t);
+        schedule_warp(p.seq_lens, p.max_seq_len, p.B, 0, kSegCost, c, C, c == 0 && r == 0, p.meta, p.ctl,
+                      &s_n_local, &s_start_b, &s_start_t);
 
     if (tid == 32) {
         for (int i = 0; i < kNS; ++i) {
@@ -242,9 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the peer's barriers are initialised before any remote arrive / st.async
     const uint32_t tmem = s_tmem_base;
-    const long long W = s_W;
-    const long long g_begin = (long long)c * W / C, g_end = (long long)(c + 1) * W / C;
-    const int n_local = (int)(g_end - g_begin);   // tiles of this cluster
+    const int n_local = s_n_local;   // tiles of this cluster
     const int start_b = s_start_b, start_t = s_start_t;
 
     if (n_local == 0 && warp >= 2) {
