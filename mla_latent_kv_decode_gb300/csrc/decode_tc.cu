@@ -63,6 +63,7 @@ using namespace dc;
 constexpr int kNS = 3;                 // KV ring stages (pages)
 constexpr int kNSB = 2;                // score buffers in TMEM (read early in a page's chain)
 constexpr int kNP = 2;                 // P buffers in shared memory (held until both PVs are done)
+constexpr int kNX = 2;                 // partial-score exchange buffers
 constexpr int kSegCost = 4;           // a segment start costs about four pages (schedule units)
 constexpr int kQKAhead = kNS - 1;      // QK may run this many tiles ahead of PV
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners, 4 forwarders, 4 receivers
@@ -92,15 +93,15 @@ constexpr int kPMsgBytes = 2 * (32 * 128 + 32 * 4);    // the peer's P rows and 
 constexpr int kOffQRope = 0;
 constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 8192
 constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 155648: 2 buffers [16][64][16 B]
-constexpr int kOffP = kOffX + 2 * kXBytes;             // kNP P buffers
+constexpr int kOffP = kOffX + kNX * kXBytes;           // kNP P buffers
 constexpr int kOffAlphaIn = kOffP + kNP * kPBytes;     // kNP x alpha[64] of the peer's heads
 constexpr int kOffAlphaOut = kOffAlphaIn + kNP * kOwned * 4;   // kNP x alpha[64], owned heads
 constexpr int kOffLIn = kOffAlphaOut + kNP * kOwned * 4;  // 2 x l[64] of the peer's heads
 // epilogue staging, 2 KB per softmax warp: [32 rows x 64 B], 64-byte swizzle (the TMA store box)
 constexpr int kOffStage = (kOffLIn + 2 * kOwned * 4 + 1023) / 1024 * 1024;
 constexpr int kStageOut = 2048;
-constexpr int kOffBar = kOffStage + 16 * kStageOut;
-constexpr int kNumBars = 2 * kNS + 2 * kNSB + 2 * kNP + 4 + 2 + 5 + 2;
+constexpr int kOffBar = kOffStage + 12 * kStageOut;   // owners and receivers
+constexpr int kNumBars = 2 * kNS + 2 * kNSB + 2 * kNP + 2 * kNX + 2 + 5 + 2;
 constexpr int kOffRed = kOffBar + 8 * kNumBars;        // per-head exchange between slices [4][128]
 constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -128,7 +129,7 @@ struct Bars {
     uint32_t kv_full, kv_empty;   // arrays of kNS
     uint32_t s_full, s_empty;     // arrays of kNSB
     uint32_t p_full, p_empty;     // arrays of kNP
-    uint32_t x_full, x_free;      // arrays of 2
+    uint32_t x_full, x_free;      // arrays of kNX
     uint32_t l_full;              // array of 2
     uint32_t q_full, q_empty, o_full, o_free, mma_drain;
     uint32_t resc_req, resc;      // a rescale of the peer's heads' O rows: asked, done
@@ -151,8 +152,8 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.s_empty = a; a += 8 * kNSB;
     b.p_full = a; a += 8 * kNP;
     b.p_empty = a; a += 8 * kNP;
-    b.x_full = a; a += 16;
-    b.x_free = a; a += 16;
+    b.x_full = a; a += 8 * kNX;
+    b.x_free = a; a += 8 * kNX;
     b.l_full = a; a += 16;
     b.q_full = a; a += 8;
     b.q_empty = a; a += 8;
@@ -219,11 +220,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bars.pf(i), kOwnerWarps);
             mbar_init(bars.pe(i), 2);    // the PV completion of both CTAs of the pair
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNX; ++i) {
             mbar_init(bars.xf(i), 1);
             mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
-            mbar_init(bars.lf(i), 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(bars.lf(i), 1);
         // per segment: the producer's rope copy (with its bytes) and every score-reading warp's
         // share of the latent half in tensor memory
         mbar_init(bars.q_full, 1 + kScoreReaders);
@@ -527,8 +528,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (ok) {
                 tc_fence_after();
                 const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
-                uint8_t* stg = sm + kOffStage + (warp - 2) * kStageOut;
-                const uint32_t stg_s = sbase + kOffStage + (warp - 2) * kStageOut;
+                const int si = owner ? (lg & 1) * 4 + ts : 8 + (lg & 1) * 2 + (ts - 2);   // staging buffer
+                uint8_t* stg = sm + kOffStage + si * kStageOut;
+                const uint32_t stg_s = sbase + kOffStage + si * kStageOut;
                 uint8_t* srow = stg + lane * 64;
                 const int sw = (lane >> 1) & 3;   // 64-byte swizzle: chunk j at j ^ sw
                 const int row0 = (partial ? slot : cu.b) * kHeads + lg * 32;
@@ -596,11 +598,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.se(sb));
-                const int xb = i & 1;
+                const int xb = i % kNX;
                 // already in log2 units (times scale log2(e)): the owner adds its own part with an FMA
 #pragma unroll
                 for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * p.scale_log2);
-                if (wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) {
+                if (wwait(bars.xe(xb), ((i / kNX) & 1) ^ 1, 8)) {
 #pragma unroll
                     for (int g = 0; g < 8; ++g)
                         st_async_v4(x_remote + xb * kXBytes + ((8 * ts + g) * kOwned + hh) * 16,
@@ -673,7 +675,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY, l_part = 0.f, lr_part = 0.f;
             if (n_local > 0) load_q(cu.b, 32 * ts, 1);
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, 0)) {
-                const int xb = i & 1;
+                const int xb = i % kNX;
                 const bool first = cu.first();
                 if (first) {
                     m_used = -INFINITY;
@@ -691,7 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 // the peer's partial scores of these heads for page i
                 if (lead && !s_abort) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
-                const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
+                const bool xok = wwait(bars.xf(xb), (i / kNX) & 1, 9);
                 const int nv = min(kT, cu.n - cu.t * kT) - kSlice * ts;   // valid positions here
                 float x[16];
                 const uint8_t* xp = sm + kOffX + xb * kXBytes;
