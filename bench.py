@@ -42,8 +42,8 @@ L2_BYTES = 126 * 2 ** 20
 # entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
 # profiles/decode_gather_fp8_batch.md.
 NCU_TRAFFIC = {
-    ("6d63f2ca00bc97f4", "paged_batch"): 178_591_744,
-    ("6d63f2ca00bc97f4", "fp8_batch"): 1_416_535_640,
+    ("ed6f880eca010d0c", "paged_batch"): 178_216_192,
+    ("ed6f880eca010d0c", "fp8_batch"): 1_414_786_472,
 }
 DECODE_SOURCES = ["mla_latent_kv_decode_gb300/csrc/decode_tc.cu",
                   "mla_latent_kv_decode_gb300/csrc/decode_gather.cu",
