@@ -72,6 +72,28 @@ def test_fp8_mixed_batch_with_append(torch):
     _run_full_compare(torch, w, "fp8 mixed")
 
 
+def test_many_requests_mixed_lengths(torch):
+    """40 requests (empty, one-token, page-edge and long ones interleaved): the tile stream with
+    its per-request start cost, ranges that begin or end inside a request's start units, and
+    the merge of requests cut into a few pieces (warp-per-head shape)."""
+    rng = np.random.default_rng(27)
+    seq = rng.integers(0, 6000, size=40)
+    seq[::7] = 0
+    seq[3::11] = 1
+    seq[5::13] = 64
+    for fmt in (0, 1):
+        w = _custom(f"many{fmt}", fmt, seq, seed=27)
+        _run_full_compare(torch, w, f"many requests fmt={fmt}")
+
+
+def test_few_long_requests_deep_merge(torch):
+    """Three long requests of different lengths: each is cut into many pieces, merged by the
+    block-per-head shape, with one empty request between them."""
+    for fmt in (0, 1):
+        w = _custom(f"few{fmt}", fmt, [17000, 0, 9000, 25001], seed=28)
+        _run_full_compare(torch, w, f"few long requests fmt={fmt}")
+
+
 def test_running_max_growth(torch):
     """Scores spread wide (softmax scale 4 instead of 1/sqrt(192)): a head's running max grows by
     more than the kernels' lazy-max slack (2^16) on most pages (about 360 growth events over the
