@@ -71,6 +71,19 @@ def _load():
             lib.oracle_mla_decode.restype = ctypes.c_int
             lib.oracle_combine.argtypes = [P, P, i32, i64, P, P]
             lib.oracle_combine.restype = None
+            lib.oracle_index_page_bytes.argtypes = []
+            lib.oracle_index_page_bytes.restype = i64
+            lib.oracle_index_append.argtypes = [P, i64, P, P, i64]
+            lib.oracle_index_append.restype = i64
+            lib.oracle_index_read.argtypes = [P, i64, P]
+            lib.oracle_index_read.restype = None
+            lib.oracle_index_score.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int]
+            lib.oracle_index_score.restype = f64
+            lib.oracle_indexer_scores.argtypes = [P, i64, P, P, ctypes.c_int, P, i32, P, i32, i64, P,
+                                                  ctypes.c_int]
+            lib.oracle_indexer_scores.restype = ctypes.c_int
+            lib.oracle_topk.argtypes = [P, i64, P, i32, i32, P, ctypes.c_int]
+            lib.oracle_topk.restype = None
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -216,3 +229,79 @@ def combine(o_part: np.ndarray, lse_part: np.ndarray):
     lse = np.empty(1, dtype=np.float64)
     _load().oracle_combine(_ptr(o_part), _ptr(lse_part), S, D, _ptr(out), _ptr(lse))
     return out, float(lse[0])
+
+
+# ------------------------------------------------------------------------------------------
+# DSA lightning indexer and top-k selection ("DeepSeek's KV Cache: From 3.9 MB to 890 B per
+# Token", "DSA: three things the indexer builds" (Fig. 8), "The score that picks positions"
+# (Fig. 9), "Calculating V3.2's KV cache" (search key, 132 B)).
+# ------------------------------------------------------------------------------------------
+IDX_DIM = 128
+IDX_HEADS = 64
+
+
+def index_page_bytes() -> int:
+    """Bytes of one 64-token page of the index-key pool (64 x (128 codes + 4-byte scale))."""
+    return int(_load().oracle_index_page_bytes())
+
+
+def new_index_pool(num_pages: int) -> np.ndarray:
+    return np.zeros(num_pages * index_page_bytes(), dtype=np.uint8)
+
+
+def index_append(pool: np.ndarray, k: np.ndarray, slot: np.ndarray) -> int:
+    """Quantise T search keys (bf16 bits k[T,128]) into ``pool`` at ``slot``; returns the number of
+    rows whose slot lies outside the pool."""
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    T = slot.shape[0]
+    assert k.shape == (T, IDX_DIM)
+    num_pages = pool.size // index_page_bytes()
+    return int(_load().oracle_index_append(_ptr(pool), num_pages, _ptr(k), _ptr(slot), T))
+
+
+def index_read(pool: np.ndarray, slot: int) -> np.ndarray:
+    """The search key of one cached token, exact doubles [128]."""
+    k = np.empty(IDX_DIM, dtype=np.float64)
+    _load().oracle_index_read(_ptr(pool), int(slot), _ptr(k))
+    return k
+
+
+def index_score(q: np.ndarray, w: np.ndarray, k: np.ndarray) -> float:
+    """sum_j w[j] ReLU(q[j] . k) for one query q[heads, dim] (fp64) and one key k[dim]."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    heads, dim = q.shape
+    assert w.shape == (heads,) and k.shape == (dim,)
+    return float(_load().oracle_index_score(_ptr(q), _ptr(w), _ptr(k), heads, dim))
+
+
+def indexer_scores(pool: np.ndarray, q: np.ndarray, w: np.ndarray, block_table: np.ndarray,
+                   seq_lens: np.ndarray, ld: int, nthreads: int = 0) -> np.ndarray:
+    """Scores float64[B, ld] of each request's query (bf16 bits q[B,heads,128], fp32 w[B,heads])
+    at every visible position; -inf from seq_lens[b] on."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, heads, dim = q.shape
+    assert dim == IDX_DIM and w.shape == (B, heads)
+    out = np.empty((B, ld), dtype=np.float64)
+    num_pages = pool.size // index_page_bytes()
+    rc = _load().oracle_indexer_scores(_ptr(pool), num_pages, _ptr(q), _ptr(w), heads, _ptr(block_table),
+                                       block_table.shape[1], _ptr(seq_lens), B, ld, _ptr(out), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_indexer_scores: a visible position maps outside the pool")
+    return out
+
+
+def topk(scores: np.ndarray, seq_lens: np.ndarray, K: int, nthreads: int = 0) -> np.ndarray:
+    """int32[B, K]: per row, the K highest scores among positions < seq_lens[b] (a tie goes to the
+    lower position), in increasing position order, -1 past the picks."""
+    scores = np.ascontiguousarray(scores, dtype=np.float64)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, ld = scores.shape
+    idx = np.empty((B, K), dtype=np.int32)
+    _load().oracle_topk(_ptr(scores), ld, _ptr(seq_lens), B, K, _ptr(idx), nthreads)
+    return idx

@@ -336,6 +336,143 @@ void oracle_combine(const float* o_part, const float* lse_part, int32_t S, int64
     *lse = L;
 }
 
+/* ---------------------------------------------------------------------------------------- */
+/* DSA lightning indexer and top-k selection                                                */
+/* ([KV] "DSA: three things the indexer builds" (Fig. 8), "The score that picks positions"   */
+/* (Fig. 9), "Calculating V3.2's KV cache" (search key, 132 B))                              */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Index-key page of this library's pool: the 64 tokens' 128 E4M3 codes (token-major, 8,192 B)
+ * followed by their 64 fp32 scales (256 B), 8,448 B per page = 64 x 132 B: the search key is
+ * "128 FP8 values with one FP32 scale for all 128 dimensions", quantised entirely ([KV]
+ * "Calculating V3.2's KV cache").  The scale rule is the main cache's: absmax / 448. */
+#define ORACLE_IDX_DIM 128
+#define ORACLE_IDX_PAGE_BYTES (ORACLE_PAGE * (ORACLE_IDX_DIM + 4))
+
+int64_t oracle_index_page_bytes(void) { return ORACLE_IDX_PAGE_BYTES; }
+
+/* Write T search keys (bf16 bits k[T,128]) at `slot` (page * 64 + row; < 0 skipped).  Returns the
+ * number of rows whose slot is outside the pool (not written). */
+int64_t oracle_index_append(uint8_t* pool, int64_t num_pages, const uint16_t* k, const int32_t* slot,
+                            int64_t T) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < T; ++i) {
+        int64_t sl = slot[i];
+        if (sl < 0) continue;
+        if (sl >= num_pages * ORACLE_PAGE) { ++bad; continue; }
+        uint8_t* page = pool + (sl / ORACLE_PAGE) * ORACLE_IDX_PAGE_BYTES;
+        int64_t row = sl % ORACLE_PAGE;
+        const uint16_t* x = k + i * ORACLE_IDX_DIM;
+        float amax = 0.0f;
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d) {
+            float v = fabsf((float)oracle_bf16_to_f64(x[d]));
+            if (v > amax) amax = v;
+        }
+        float s = amax / 448.0f;
+        for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+            page[row * ORACLE_IDX_DIM + d] = (amax == 0.0f) ? 0 : oracle_e4m3_encode((float)oracle_bf16_to_f64(x[d]) / s);
+        memcpy(page + ORACLE_PAGE * ORACLE_IDX_DIM + 4 * row, &s, 4);
+    }
+    return bad;
+}
+
+/* The search key of one cached token as exact doubles: k[d] = e4m3_value(code[d]) * s. */
+void oracle_index_read(const uint8_t* pool, int64_t slot, double* k) {
+    const uint8_t* page = pool + (slot / ORACLE_PAGE) * ORACLE_IDX_PAGE_BYTES;
+    int64_t row = slot % ORACLE_PAGE;
+    float s;
+    memcpy(&s, page + ORACLE_PAGE * ORACLE_IDX_DIM + 4 * row, 4);
+    for (int d = 0; d < ORACLE_IDX_DIM; ++d) k[d] = oracle_e4m3_decode(page[row * ORACLE_IDX_DIM + d]) * (double)s;
+}
+
+/* Indexer score of one query (heads x dim, fp64) against one key (dim):
+ *     I = sum_j w[j] * ReLU(q[j] . k)
+ * ([KV] "The score that picks positions": "for each head, take the dot product of the query
+ * and the shared key, apply ReLU, and multiply the result by the head weight; then sum over
+ * all heads").  Written for any head count and width. */
+double oracle_index_score(const double* q, const double* w, const double* k, int heads, int dim) {
+    double I = 0.0;
+    for (int j = 0; j < heads; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < dim; ++d) dot += q[(int64_t)j * dim + d] * k[d];
+        I += w[j] * (dot > 0.0 ? dot : 0.0);
+    }
+    return I;
+}
+
+/* Scores of request b's query (q bf16 bits [B, heads, 128], w fp32 [B, heads]) at every visible
+ * position t < seq_lens[b] (clamped to [0, ld]) of the paged index pool; scores[b * ld + t].
+ * Positions from seq_lens[b] on are set to -inf (not visible).  Returns 1 if a visible position
+ * maps outside the pool, else 0. */
+int oracle_indexer_scores(const uint8_t* pool, int64_t num_pages, const uint16_t* q, const float* w,
+                          int heads, const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                          int32_t B, int64_t ld, double* scores, int nthreads) {
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+#endif
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t n = seq_lens[b];
+        if (n < 0) n = 0;
+        if (n > ld) n = ld;
+        double* qd = (double*)malloc(sizeof(double) * (size_t)heads * ORACLE_IDX_DIM);
+        double* wd = (double*)malloc(sizeof(double) * (size_t)heads);
+        double k[ORACLE_IDX_DIM];
+        for (int64_t e = 0; e < (int64_t)heads * ORACLE_IDX_DIM; ++e)
+            qd[e] = oracle_bf16_to_f64(q[(int64_t)b * heads * ORACLE_IDX_DIM + e]);
+        for (int j = 0; j < heads; ++j) wd[j] = (double)w[(int64_t)b * heads + j];
+        for (int64_t t = 0; t < ld; ++t) {
+            if (t >= n) { scores[(int64_t)b * ld + t] = -INFINITY; continue; }
+            int64_t page = block_table[(int64_t)b * max_pages + t / ORACLE_PAGE];
+            if (page < 0 || page >= num_pages) { err = 1; scores[(int64_t)b * ld + t] = NAN; continue; }
+            oracle_index_read(pool, page * ORACLE_PAGE + t % ORACLE_PAGE, k);
+            scores[(int64_t)b * ld + t] = oracle_index_score(qd, wd, k, heads, ORACLE_IDX_DIM);
+        }
+        free(qd);
+        free(wd);
+    }
+    return err;
+}
+
+/* Top-k selection of one row: among positions t < n, the K with the highest scores, a tie going
+ * to the lower position; written to idx[0 .. K) in increasing position order, -1 past the
+ * min(K, n) picks ([KV] "The score that picks positions": "each row picks up to 2,048
+ * highest-scoring positions among the positions that query can see").  Plain selection: K passes
+ * over the row, each taking the best position not taken yet (the tie rule is the order of the
+ * comparison), then a sort of the picks. */
+void oracle_topk_row(const double* scores, int64_t n, int32_t K, int32_t* idx) {
+    int32_t m = (int32_t)(n < K ? n : K);
+    unsigned char* taken = (unsigned char*)calloc((size_t)(n > 0 ? n : 1), 1);
+    for (int32_t r = 0; r < m; ++r) {
+        int64_t best = -1;
+        for (int64_t t = 0; t < n; ++t) {
+            if (taken[t]) continue;
+            if (best < 0 || scores[t] > scores[best]) best = t;   /* strict: ties keep the lower t */
+        }
+        if (best >= 0) taken[best] = 1;
+    }
+    int32_t c = 0;
+    for (int64_t t = 0; t < n; ++t)
+        if (taken[t]) idx[c++] = (int32_t)t;
+    for (; c < K; ++c) idx[c] = -1;
+    free(taken);
+}
+
+void oracle_topk(const double* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K, int32_t* idx,
+                 int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+#endif
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t n = seq_lens[b];
+        if (n < 0) n = 0;
+        if (n > ld) n = ld;
+        oracle_topk_row(scores + (int64_t)b * ld, n, K, idx + (int64_t)b * K);
+    }
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

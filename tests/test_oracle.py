@@ -491,3 +491,133 @@ def test_workload_recipes():
         idx = w5.topk_idx[b]
         assert len(set(idx.tolist())) == 256 and np.all(np.diff(idx) > 0)
         assert idx.min() >= 0 and idx.max() < 4096
+
+
+# ------------------------------------------------------------------------------------------
+# DSA lightning indexer and top-k selection: "DeepSeek's KV Cache: From 3.9 MB to 890 B per
+# Token", sections "DSA: three things the indexer builds" (Fig. 8), "The score that picks
+# positions" (Fig. 9) and "Calculating V3.2's KV cache" (search key, 132 B).
+# ------------------------------------------------------------------------------------------
+
+def _bf16_bits(x):
+    return synth._bf16_rne(np.asarray(x, dtype=np.float32))
+
+
+def test_index_page_bytes_closed_form():
+    # "Search key, 132 B": 128 FP8 values + one fp32 scale, per token; 64 tokens per page
+    assert oracle.index_page_bytes() == 64 * (128 + 4) == 8448
+
+
+def test_index_score_hand_example():
+    # two heads, three dims: head 0's dot is 2 - 2 + 0 = 0 (ReLU keeps 0), head 1's is
+    # 0 + 1 + 3 = 4, so I = 0.5 * 0 + 2 * 4 = 8; a key that makes both dots negative scores 0
+    q = np.array([[1.0, -2.0, 0.0], [0.0, 1.0, 1.0]])
+    w = np.array([0.5, 2.0])
+    assert oracle.index_score(q, w, np.array([2.0, 1.0, 3.0])) == 8.0
+    assert oracle.index_score(q, w, np.array([-1.0, 1.0, -2.0])) == 0.0
+    # a negative head weight counts against the position (the score is not a probability)
+    assert oracle.index_score(q, np.array([0.5, -2.0]), np.array([2.0, 1.0, 3.0])) == -8.0
+
+
+def test_index_score_invariants():
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((64, 128))
+    k = rng.standard_normal(128)
+    w1, w2 = rng.standard_normal(64), rng.standard_normal(64)
+    I = lambda qq, ww, kk: oracle.index_score(qq, ww, kk)
+    # linear in the head weights
+    assert abs(I(q, w1 + w2, k) - (I(q, w1, k) + I(q, w2, k))) < 1e-9
+    # positively homogeneous in the query (ReLU commutes with a positive factor)
+    assert abs(I(2.5 * q, w1, k) - 2.5 * I(q, w1, k)) < 1e-9
+    # ReLU(x) + ReLU(-x) = |x|: the scores of k and -k add up to the weighted absolute dots
+    dots = q @ k
+    assert abs(I(q, w1, k) + I(q, w1, -k) - float(np.sum(w1 * np.abs(dots)))) < 1e-9
+
+
+def test_index_append_codec_and_layout():
+    rng = np.random.default_rng(42)
+    T = 40
+    x = rng.standard_normal((T, 128)).astype(np.float32) * rng.uniform(0.01, 30, (T, 1)).astype(np.float32)
+    x[3] = 0.0                                   # an all-zero key
+    bits = _bf16_bits(x)
+    xf = oracle.bf16_to_f64(bits).reshape(T, 128)
+    pool = oracle.new_index_pool(2)
+    slot = np.arange(T, dtype=np.int32) * 3 % 128  # rows scattered over both pages
+    assert oracle.index_append(pool, bits, slot) == 0
+    page_bytes = oracle.index_page_bytes()
+    for i in range(T):
+        k = oracle.index_read(pool, int(slot[i]))
+        amax = np.float32(np.max(np.abs(xf[i].astype(np.float32))))
+        s = np.float32(amax / np.float32(448.0))
+        # the scale sits after the page's 64 x 128 codes, row-major
+        pg, row = divmod(int(slot[i]), 64)
+        stored = np.frombuffer(pool[pg * page_bytes + 8192 + 4 * row: pg * page_bytes + 8192 + 4 * row + 4].tobytes(),
+                               dtype=np.float32)[0]
+        assert stored == s
+        if amax == 0:
+            assert np.all(k == 0.0)
+            continue
+        j = int(np.argmax(np.abs(xf[i])))
+        assert abs(k[j]) == 448.0 * float(s)         # the largest magnitude maps to +-448
+        nz = np.abs(xf[i]) >= 2.0 ** -6 * float(s)   # normal E4M3 range
+        assert np.all(np.abs(k[nz] - xf[i][nz]) <= 2.0 ** -4 * np.abs(xf[i][nz]) + 1e-30)
+        assert np.all(np.abs(k[~nz] - xf[i][~nz]) <= 2.0 ** -10 * float(s) + 1e-30)
+    # other rows untouched, an out-of-pool slot reported
+    untouched = np.setdiff1d(np.arange(128), slot)
+    for t in untouched[:5]:
+        assert np.all(oracle.index_read(pool, int(t)) == 0.0)
+    assert oracle.index_append(pool, bits[:1], np.array([128], np.int32)) == 1
+
+
+def test_indexer_scores_through_pages_and_visibility():
+    rng = np.random.default_rng(43)
+    B, heads, n_pages = 2, 64, 5
+    keys = _bf16_bits(rng.standard_normal((n_pages * 64, 128)).astype(np.float32))
+    pool = oracle.new_index_pool(n_pages)
+    oracle.index_append(pool, keys, np.arange(n_pages * 64, dtype=np.int32))
+    q = _bf16_bits(rng.standard_normal((B, heads, 128)).astype(np.float32))
+    w = rng.standard_normal((B, heads)).astype(np.float32)
+    bt = np.array([[3, 0, 4], [1, 2, -1]], np.int32)
+    seq = np.array([150, 70], np.int32)
+    sc = oracle.indexer_scores(pool, q, w, bt, seq, ld=192)
+    qd = oracle.bf16_to_f64(q).reshape(B, heads, 128)
+    for b in range(B):
+        for t in (0, 63, 64, int(seq[b]) - 1):
+            k = oracle.index_read(pool, int(bt[b, t // 64]) * 64 + t % 64)
+            assert sc[b, t] == oracle.index_score(qd[b], w[b].astype(np.float64), k)
+        assert np.all(np.isneginf(sc[b, seq[b]:]))
+    # permuting the pages together with the block table leaves every score unchanged
+    perm = np.array([4, 2, 0, 1, 3])
+    pool2 = oracle.new_index_pool(n_pages)
+    pb = oracle.index_page_bytes()
+    for new, old in enumerate(perm):
+        pool2[new * pb:(new + 1) * pb] = pool[old * pb:(old + 1) * pb]
+    inv = np.argsort(perm)
+    bt2 = np.where(bt >= 0, inv[np.maximum(bt, 0)], -1).astype(np.int32)
+    assert np.array_equal(oracle.indexer_scores(pool2, q, w, bt2, seq, ld=192), sc)
+
+
+def _topk_lexsort(scores, n, K):
+    # independent statement of the selection: order by (score descending, position ascending)
+    t = np.arange(n)
+    order = np.lexsort((t, -scores[:n]))
+    pick = np.sort(order[:min(K, n)])
+    return np.concatenate([pick, -np.ones(K - pick.size, dtype=np.int64)]).astype(np.int32)
+
+
+def test_topk_selection():
+    rng = np.random.default_rng(44)
+    ld = 300
+    sc = rng.standard_normal((5, ld))
+    sc[1, ::3] = 0.5            # many ties at the cut
+    sc[2, :] = 1.0              # all tied: the lowest positions win
+    seq = np.array([300, 250, 100, 7, 0], np.int32)
+    for K in (1, 16, 64, 120, 300):
+        idx = oracle.topk(sc, seq, K)
+        for b in range(5):
+            ref = _topk_lexsort(sc[b], int(seq[b]), K)
+            assert np.array_equal(idx[b], ref), (K, b)
+            picks = idx[b][idx[b] >= 0]
+            assert np.all(np.diff(picks) > 0) and np.all(picks < seq[b])
+            assert picks.size == min(K, int(seq[b]))
+    assert np.array_equal(oracle.topk(sc, seq, 64)[2], np.arange(64))
