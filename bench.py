@@ -204,6 +204,37 @@ def run_reference(args):
     return 0
 
 
+def run_indexer_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from mla_latent_kv_decode_gb300 import synth
+    import oracle
+    oracle.build()
+    w = synth.make_index_workload()
+    nth = os.cpu_count() or 1
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_indexer_requests(w, budget / 4, nth)
+    keys, sec, req = 0, 0.0, 0
+    for _ in range(args.steps):
+        k, s_, d = _oracle_indexer_requests(w, budget, nth)
+        keys, sec, req = keys + k, sec + s_, req + d
+    value = keys * 132 / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "search-key GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "topk": w.K, "description": w.description},
+            "cpu_baseline": {"value": round(value, 6), "unit": "search-key GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: whole queries of the {w.name} workload for ~{budget:.1f} s; "
+                                       f"{req} queries, {keys} keys in total"},
+            "e2e": {"value": round(value, 6), "unit": "search-key GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------------------------
 # Our arm
 # ----------------------------------------------------------------------------------------------
@@ -358,6 +389,205 @@ def run_ours(args):
     return 0
 
 
+def run_indexer(args):
+    """The DSA lightning-indexer step (search-key scores of every cached position, then top-k per
+    query) on the indexer_topk workload: one graph of mla_indexer_score + mla_topk_select."""
+    import torch
+    import mla_latent_kv_decode_gb300 as mla
+    from mla_latent_kv_decode_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    mla.load()
+    w = synth.make_index_workload()
+    pool = torch.zeros(mla.index_pool_bytes(w.num_pages), dtype=torch.uint8, device="cuda")
+    chunk = 1 << 15
+    kbuf = torch.empty((chunk, mla.INDEX_DIM), dtype=torch.bfloat16, device="cuda")
+    for b in range(w.B):
+        n = int(w.seq_lens[b])
+        for t0 in range(0, n, chunk):
+            t1 = min(n, t0 + chunk)
+            synth.gpu_normal_bf16(kbuf.data_ptr(), t1 - t0, w.seed, synth.STREAM_IDX_K,
+                                  (b * synth.KV_ROW_STRIDE + t0) * mla.INDEX_DIM, mla.INDEX_DIM, mla.INDEX_DIM)
+            slot = torch.from_numpy(w.slots(b, t0, t1)).cuda()
+            mla.index_append(pool, w.num_pages, kbuf[:t1 - t0], slot)
+    q = torch.from_numpy(synth.index_queries(w.seed, w.B).view(np.int16)).cuda().view(torch.bfloat16)
+    wt = torch.from_numpy(synth.index_weights(w.seed, w.B)).cuda()
+    bt = torch.from_numpy(w.block_table).cuda()
+    sl = torch.from_numpy(w.seq_lens).cuda()
+    ld = w.max_seq_len
+    scores = torch.empty((w.B, ld), dtype=torch.float32, device="cuda")
+    idx = torch.empty((w.B, w.K), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        mla.indexer_score(pool, w.num_pages, q, wt, bt, sl, ld, scores=scores)
+        mla.topk_select(scores, sl, w.K, topk_idx=idx)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    rc = mla.check_status()
+    if rc != 0:
+        raise mla.MlaError(rc, "warm-up")
+    graphs = {}
+    for name, fn in (("step", step),
+                     ("score", lambda: mla.indexer_score(pool, w.num_pages, q, wt, bt, sl, ld, scores=scores)),
+                     ("topk", lambda: mla.topk_select(scores, sl, w.K, topk_idx=idx))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[name] = g
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graphs["step"].replay()
+    barrier()
+
+    def timed(g, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                g.replay()
+            e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) / n
+
+    steps = min(args.steps, 500)
+    ms = timed(graphs["step"], steps)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    score_ms = timed(graphs["score"], max(10, steps // 2))
+    topk_ms = timed(graphs["topk"], max(10, steps // 2))
+    clocks = sampler.stop()
+    rc = mla.check_status()
+    if rc != 0:
+        raise mla.MlaError(rc, "timed region")
+
+    # end to end: queries, weights, tables host -> device, the step, the picks device -> host
+    host = {k: v.cpu().pin_memory() for k, v in (("q", q), ("w", wt), ("bt", bt), ("sl", sl))}
+    dev = {"q": q, "w": wt, "bt": bt, "sl": sl}
+    idx_h = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = idx_h.numel() * idx_h.element_size()
+
+    def one():
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        step()
+        idx_h.copy_(idx, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+    barrier()
+    e_steps = max(3, min(steps, 100))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            one()
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+
+    keys = int(w.seq_lens.astype(np.int64).sum())
+    key_bytes = keys * 132
+    alg_bytes = (key_bytes + w.B * 64 * 128 * 2 + w.B * 64 * 4 + w.B * w.K * 4 + w.block_table.size * 4
+                 + w.B * 4)
+    flops = 2 * 64 * 128 * keys
+    peaks = _peaks()
+    s = ms / 1e3
+    tensor_bound = flops / (peaks["bf16_tflops_sustained"] * 1e12) > alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    achieved = alg_bytes / s / 1e9
+    if tensor_bound:
+        roofline = {"bound": "tensor", "achieved": round(flops / s / 1e12, 2), "peak": peaks["bf16_tflops_sustained"],
+                    "unit": "TFLOP/s", "frac": round(flops / s / 1e12 / peaks["bf16_tflops_sustained"], 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    roofline.update({"traffic": NCU_TRAFFIC.get((_sources_hash(), w.name)), "peak_source": peaks["source"],
+                     "kernel": "mla_indexer_score + mla_topk_select", "ms_per_launch": round(ms, 6),
+                     "bytes_per_launch": alg_bytes, "flops_per_launch": flops,
+                     "score_ms": round(score_ms, 6), "topk_ms": round(topk_ms, 6),
+                     "score_frac_of_hbm": round(key_bytes / (score_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)})
+    line = {
+        "metric": METRIC, "value": round(world * key_bytes / s / 1e9, 3), "unit": "search-key GB/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "indexer_heads": 64, "indexer_dim": 128, "topk": w.K,
+                   "description": w.description, "step": "mla_indexer_score + mla_topk_select",
+                   "l2": f"inputs larger than L2: a {key_bytes / 2**30:.2f} GiB search-key pool",
+                   "parallelism": f"replicas x{world}"},
+        "queries_per_s": round(world * w.B / s, 1),
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": round(world * key_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "search-key GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": steps * 2,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = indexer_cpu_baseline(w, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def _oracle_indexer_requests(w, budget_s: float, nthreads: int):
+    """The oracle's scores and top-k of whole requests of the indexer workload until the budget."""
+    import oracle
+    from mla_latent_kv_decode_gb300 import synth
+    q = synth.index_queries(w.seed, w.B)
+    wt = synth.index_weights(w.seed, w.B)
+    done, keys, spent = 0, 0, 0.0
+    while done < w.B and (spent < budget_s or done == 0):
+        b = done
+        n = int(w.seq_lens[b])
+        pages = (n + 63) // 64
+        pool = oracle.new_index_pool(pages)
+        oracle.index_append(pool, synth.index_keys(w.seed, b, 0, n), np.arange(n, dtype=np.int32))
+        bt = np.arange(pages, dtype=np.int32)[None]
+        t0 = time.perf_counter()
+        sc = oracle.indexer_scores(pool, q[b:b + 1], wt[b:b + 1], bt, w.seq_lens[b:b + 1], n, nthreads)
+        oracle.topk(sc, w.seq_lens[b:b + 1], w.K, nthreads)
+        spent += time.perf_counter() - t0
+        keys += n
+        done += 1
+    return keys, spent, done
+
+
+def indexer_cpu_baseline(w, budget_s: float = 12.0):
+    import oracle
+    nth = os.cpu_count() or 1
+    oracle.build()
+    keys, spent, done = _oracle_indexer_requests(w, budget_s, nth)
+    return {"value": round(keys * 132 / spent / 1e9, 6), "unit": "search-key GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.B} queries of the {w.name} workload (scores of all {keys} keys, top-{w.K}), "
+                      f"{spent:.1f} s of fp64 oracle time (one thread per query)"}
+
+
 def run_e2e(args, dw, torch, mla, stream, barrier, dist):
     """Same metric through the public API with pinned host buffers: every step copies its inputs
     (queries, block table, seq_lens, new rows and slots) host->device, runs append + decode, and
@@ -412,7 +642,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="paged_batch",
-                    choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse"])
+                    choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse",
+                             "indexer_topk"])
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0 = enough to exceed L2 3x)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -420,7 +651,11 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
+        if args.workload == "indexer_topk":
+            return run_indexer_reference(args)
         return run_reference(args)
+    if args.workload == "indexer_topk":
+        return run_indexer(args)
     return run_ours(args)
 
 

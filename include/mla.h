@@ -174,6 +174,58 @@ mla_status mla_set_wait_limit(uint32_t iterations);
  * the conversion against an independent encoder (OCP OFP8 specification, format E4M3). */
 mla_status mla_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * DSA lightning indexer ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token", sections "DSA:
+ * three things the indexer builds" (Fig. 8), "The score that picks positions" (Fig. 9) and
+ * "Calculating V3.2's KV cache" (search key)).  The indexer ranks the positions a query may read:
+ *     I(t, s) = sum_j w(t, j) * ReLU(q(t, j) . k(s)),  j < 64 indexer heads, 128 dims,
+ * and each query keeps its (up to) K highest-scoring visible positions; the result is the
+ * topk_idx of mla_decode.
+ * ------------------------------------------------------------------------------------------ */
+#define MLA_INDEX_HEADS 64
+#define MLA_INDEX_DIM 128
+/* One 64-token page of the search-key pool: the 64 keys' 128 E4M3 codes (token-major, 8,192 B)
+ * followed by their 64 fp32 scales (256 B): 132 B per token, "128 FP8 values with one FP32 scale
+ * for all 128 dimensions". */
+#define MLA_INDEX_PAGE_BYTES 8448
+
+/* Write T search keys into the search-key pool.
+ *   pool       : device, num_pages * MLA_INDEX_PAGE_BYTES bytes, 16-byte aligned; slot s is row
+ *                s % 64 of page s / 64 (the pages can share the main cache's block_table).
+ *   k_index    : device bf16 [T, 128]  search key of each new token.
+ *   slot       : device int32 [T]      destination slot; negative skips the row; a slot >=
+ *                num_pages * 64 is not written and records MLA_ERR_BOUNDS.
+ * Per key: amax = max |x|, s = amax / 448 (fp32, correctly rounded), code = E4M3(x / s) rounded
+ * to nearest even and saturated to +-448; amax = 0 gives s = 0 and zero codes.  Only the listed
+ * slots change.  MLA_ERR_INVALID for null pointers, T < 0 or a misaligned pointer. */
+mla_status mla_index_append(void* pool, int64_t num_pages, const void* k_index, const int32_t* slot,
+                            int64_t T, cudaStream_t stream);
+
+/* Indexer scores of B queries at every visible position.
+ *   pool, num_pages : the search-key pool written by mla_index_append.
+ *   q_index    : device bf16 [B, 64, 128]  indexer query of each head.
+ *   w_index    : device fp32 [B, 64]       head weights (any sign; not a probability).
+ *   block_table, max_pages, seq_lens, max_seq_len : as in mla_decode (position t of request b is
+ *                row t % 64 of page block_table[b][t / 64]; positions t < seq_lens[b] are visible).
+ *   scores     : device fp32 [B, max_seq_len]; scores[b][t] = I(b, t) for t < seq_lens[b]; the
+ *                rest of each row is not written.
+ * The dot products are bf16 x bf16 (E4M3 codes convert to bf16 exactly) with fp32 accumulation;
+ * the key scale multiplies after the ReLU (it is >= 0).  A visible position whose page is
+ * outside the pool scores as an all-zero key and records MLA_ERR_BOUNDS.  MLA_ERR_INVALID for
+ * null or misaligned pointers, B < 0, max_pages < 1 or max_seq_len > max_pages * 64. */
+mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_index, const float* w_index,
+                             const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                             int32_t B, int32_t max_seq_len, float* scores, cudaStream_t stream);
+
+/* Top-k selection per row: among positions t < seq_lens[b] (clamped to [0, ld]) of row b of
+ * `scores` (device fp32 [B, ld]), the K highest scores, a tie going to the lower position
+ * ("each row picks up to 2,048 highest-scoring positions among the positions that query can
+ * see"), written to topk_idx[b] (device int32 [B, K]) in increasing position order and padded
+ * with -1 past the min(K, seq_lens[b]) picks: directly the topk_idx of mla_decode.  Scores must
+ * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, K < 1 or ld < 0. */
+mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
+                           int32_t* topk_idx, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

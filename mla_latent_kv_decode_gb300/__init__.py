@@ -76,6 +76,12 @@ def load():
         lib.mla_set_wait_limit.restype = ctypes.c_int
         lib.mla_e4m3_encode.argtypes = [P, P, i64, P]
         lib.mla_e4m3_encode.restype = ctypes.c_int
+        lib.mla_index_append.argtypes = [P, i64, P, P, i64, P]
+        lib.mla_index_append.restype = ctypes.c_int
+        lib.mla_indexer_score.argtypes = [P, i64, P, P, P, i32, P, i32, i32, P, P]
+        lib.mla_indexer_score.restype = ctypes.c_int
+        lib.mla_topk_select.argtypes = [P, i64, P, i32, i32, P, P]
+        lib.mla_topk_select.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -229,3 +235,54 @@ def e4m3_encode(x, codes=None, stream=None):
                                 int(x.numel()), _stream_ptr(stream))
     _check(rc, "mla_e4m3_encode")
     return codes
+
+
+# DSA lightning indexer: search-key pool, indexer scores, top-k selection (include/mla.h).
+INDEX_HEADS = 64
+INDEX_DIM = 128
+INDEX_PAGE_BYTES = 8448
+
+
+def index_pool_bytes(num_pages: int) -> int:
+    return num_pages * INDEX_PAGE_BYTES
+
+
+def index_append(pool, num_pages: int, k_index, slot, stream=None) -> None:
+    """Quantise T search keys (bf16 k_index[T,128]) into the search-key pool at int32 ``slot[T]``."""
+    torch = _torch()
+    T = int(slot.shape[0])
+    rc = load().mla_index_append(_dev_ptr(pool, "pool", torch.uint8), int(num_pages),
+                                 _dev_ptr(k_index, "k_index", torch.bfloat16, (T, INDEX_DIM)),
+                                 _dev_ptr(slot, "slot", torch.int32), T, _stream_ptr(stream))
+    _check(rc, "mla_index_append")
+
+
+def indexer_score(pool, num_pages: int, q_index, w_index, block_table, seq_lens, max_seq_len: int,
+                  scores=None, stream=None):
+    """fp32 scores[B, max_seq_len] of the queries (bf16 q_index[B,64,128], fp32 w_index[B,64])."""
+    torch = _torch()
+    B = int(q_index.shape[0])
+    if scores is None:
+        scores = torch.empty((B, max_seq_len), dtype=torch.float32, device=q_index.device)
+    rc = load().mla_indexer_score(_dev_ptr(pool, "pool", torch.uint8), int(num_pages),
+                                  _dev_ptr(q_index, "q_index", torch.bfloat16, (B, INDEX_HEADS, INDEX_DIM)),
+                                  _dev_ptr(w_index, "w_index", torch.float32, (B, INDEX_HEADS)),
+                                  _dev_ptr(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+                                  _dev_ptr(seq_lens, "seq_lens", torch.int32, (B,)), B, int(max_seq_len),
+                                  _dev_ptr(scores, "scores", torch.float32, (B, max_seq_len)), _stream_ptr(stream))
+    _check(rc, "mla_indexer_score")
+    return scores
+
+
+def topk_select(scores, seq_lens, K: int, topk_idx=None, stream=None):
+    """int32 topk_idx[B, K]: per row the K highest scores among positions < seq_lens[b], in
+    increasing position order, -1 past the picks."""
+    torch = _torch()
+    B, ld = scores.shape
+    if topk_idx is None:
+        topk_idx = torch.empty((B, K), dtype=torch.int32, device=scores.device)
+    rc = load().mla_topk_select(_dev_ptr(scores, "scores", torch.float32), int(ld),
+                                _dev_ptr(seq_lens, "seq_lens", torch.int32, (B,)), int(B), int(K),
+                                _dev_ptr(topk_idx, "topk_idx", torch.int32, (B, K)), _stream_ptr(stream))
+    _check(rc, "mla_topk_select")
+    return topk_idx

@@ -4,6 +4,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "mla_internal.cuh"
 #include "tc_ptx.cuh"
@@ -161,6 +163,23 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t remo
 
 __device__ __forceinline__ void st_shared_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+// 16 e4m3 codes (OCP 8-bit floating point, bias 7) to 16 bf16 values, exactly: each code goes
+// to f16 and then to fp32, both exact, and every such value is a bf16 value.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t (&o)[8]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __half2_raw hr =
+                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[k] >> (16 * j)) & 0xFFFFu), __NV_E4M3);
+            __half2 h2;
+            *reinterpret_cast<__half2_raw*>(&h2) = hr;
+            const float2 f = __half22float2(h2);
+            o[2 * k + j] = pack_bf16x2(f.x, f.y);
+        }
 }
 
 // Clusters for a batch: at most one per SM pair, at least kMinTilesPerCluster tiles each.

@@ -91,6 +91,48 @@ mla_status mla_cache_append(int32_t fmt, void* pool, int64_t num_pages, const vo
                                          stream));
 }
 
+mla_status mla_index_append(void* pool, int64_t num_pages, const void* k_index, const int32_t* slot,
+                            int64_t T, cudaStream_t stream) {
+    if (T < 0 || num_pages < 0) return MLA_ERR_INVALID;
+    if (T == 0) return MLA_OK;
+    if (!pool || !k_index || !slot) return MLA_ERR_INVALID;
+    if (!aligned(pool, 16) || !aligned(k_index, 16) || !aligned(slot, 4)) return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_index_append(static_cast<uint8_t*>(pool), num_pages,
+                                         static_cast<const __nv_bfloat16*>(k_index), slot, T, ctl, stream));
+}
+
+mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_index, const float* w_index,
+                             const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                             int32_t B, int32_t max_seq_len, float* scores, cudaStream_t stream) {
+    if (B < 0 || num_pages < 0 || max_pages < 1 || max_seq_len < 0 ||
+        (int64_t)max_seq_len > (int64_t)max_pages * kPage)
+        return MLA_ERR_INVALID;
+    if (B == 0 || max_seq_len == 0) return MLA_OK;
+    if (!pool || !q_index || !w_index || !block_table || !seq_lens || !scores) return MLA_ERR_INVALID;
+    if (!aligned(pool, 16) || !aligned(q_index, 16) || !aligned(w_index, 4) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(scores, 4))
+        return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_indexer_score(static_cast<const uint8_t*>(pool), num_pages,
+                                          static_cast<const __nv_bfloat16*>(q_index), w_index, block_table,
+                                          max_pages, seq_lens, B, max_seq_len, scores, ctl, stream));
+}
+
+mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
+                           int32_t* topk_idx, cudaStream_t stream) {
+    if (B < 0 || K < 1 || ld < 0) return MLA_ERR_INVALID;
+    if (B == 0) return MLA_OK;
+    if (!scores || !seq_lens || !topk_idx) return MLA_ERR_INVALID;
+    if (!aligned(scores, 4) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4)) return MLA_ERR_INVALID;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_topk_select(scores, ld, seq_lens, B, K, topk_idx, stream));
+}
+
 size_t mla_decode_workspace_bytes(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len,
                                   int32_t topk) {
     if (!fmt_ok(fmt) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;

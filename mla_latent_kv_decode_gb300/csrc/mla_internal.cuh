@@ -48,6 +48,15 @@ cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaSt
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int S, int B, int H,
                            __nv_bfloat16* out, float* lse, cudaStream_t st);
 
+// DSA lightning indexer (indexer.cu).
+cudaError_t launch_index_append(uint8_t* pool, int64_t num_pages, const __nv_bfloat16* k, const int32_t* slot,
+                                int64_t T, DevCtl* ctl, cudaStream_t st);
+cudaError_t launch_indexer_score(const uint8_t* pool, int64_t num_pages, const __nv_bfloat16* q, const float* w,
+                                 const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                                 int max_seq_len, float* scores, DevCtl* ctl, cudaStream_t st);
+cudaError_t launch_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int B, int K,
+                               int32_t* idx, cudaStream_t st);
+
 // Split-KV plan of one decode call.
 struct DecodePlan {
     int splits;            // C: clusters of the launch (two partial slots each)

@@ -26,6 +26,9 @@ Workloads (one MLA layer each; H = 128 heads, 64-token pages, scale = 1/sqrt(192
   fp8_batch     B=64, 32,768 tokens each (32,704 prefilled + 64 appended), FP8 mixed cache
   topk_sparse   B=64, 131,072 tokens each, FP8 mixed cache, 2,048 distinct sorted positions
                 per request drawn uniformly from [0, seq_len)
+
+DSA lightning-indexer inputs (64 indexer heads x 128 dims): search keys, queries and head
+weights from their own streams (``index_keys``, ``index_queries``, ``index_weights``).
 """
 from __future__ import annotations
 
@@ -45,6 +48,9 @@ STREAM_KV = 2
 STREAM_SEQ = 4
 STREAM_PERM = 5
 STREAM_TOPK = 6
+STREAM_IDX_K = 7          # DSA indexer search keys
+STREAM_IDX_Q = 8          # DSA indexer queries
+STREAM_IDX_W = 9          # DSA indexer head weights
 
 D_C = 512
 D_R = 64
@@ -135,6 +141,61 @@ def uniform_int(seed: int, stream: int, count: int, lo: int, hi: int) -> np.ndar
     """count integers uniform in [lo, hi] (inclusive), by modulo of the 64-bit words."""
     w = u64(seed, stream, 0, count)
     return (lo + (w % np.uint64(hi - lo + 1)).astype(np.int64)).astype(np.int64)
+
+
+IDX_HEADS = 64
+IDX_DIM = 128
+
+
+def index_keys(seed: int, b: int, t0: int, t1: int) -> np.ndarray:
+    """Search keys of request b, positions t0..t1-1: bf16 bits [n, 128]."""
+    n = t1 - t0
+    return normal_bf16(seed, STREAM_IDX_K, (b * KV_ROW_STRIDE + t0) * IDX_DIM, n * IDX_DIM).reshape(n, IDX_DIM)
+
+
+def index_queries(seed: int, B: int) -> np.ndarray:
+    """Indexer queries: bf16 bits [B, 64, 128]."""
+    return normal_bf16(seed, STREAM_IDX_Q, 0, B * IDX_HEADS * IDX_DIM).reshape(B, IDX_HEADS, IDX_DIM)
+
+
+def index_weights(seed: int, B: int) -> np.ndarray:
+    """Indexer head weights: fp32 [B, 64] (both signs)."""
+    return normal_f32(seed, STREAM_IDX_W, 0, B * IDX_HEADS).reshape(B, IDX_HEADS)
+
+
+@dataclass
+class IndexWorkload:
+    """DSA lightning-indexer workload: B queries over their own search-key pools."""
+    name: str
+    B: int
+    seed: int
+    seq_lens: np.ndarray          # int32[B]
+    block_table: np.ndarray       # int32[B, max_pages]
+    num_pages: int
+    K: int
+    description: str = ""
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.B else 0
+
+    def slots(self, b: int, t0: int, t1: int) -> np.ndarray:
+        t = np.arange(t0, t1, dtype=np.int64)
+        return (self.block_table[b, t // PAGE].astype(np.int64) * PAGE + t % PAGE).astype(np.int32)
+
+
+def make_index_workload(name: str = "indexer_topk", seed: int | None = None, B: int | None = None,
+                        seq_len: int | None = None, K: int = 2048) -> IndexWorkload:
+    """indexer_topk: B=64 queries, 131,072 cached search keys each (2,048 shuffled pages per
+    request, 132 B per key), top-2,048 selection -- the step that produces topk_sparse's lists."""
+    seed = 0x4D4C41 + 6 if seed is None else seed
+    B = B or 64
+    N = seq_len or 131072
+    seq = np.full(B, N, dtype=np.int32)
+    pages = int(((seq.astype(np.int64) + PAGE - 1) // PAGE).sum())
+    bt, total = _block_table(seq, permutation(seed, STREAM_PERM, pages))
+    return IndexWorkload(name, B, seed, seq, bt, total, K,
+                         f"B={B}, {N} search keys each (FP8, 132 B), 64 indexer heads x 128 dims, top-{K}")
 
 
 def permutation(seed: int, stream: int, n: int) -> np.ndarray:
