@@ -411,7 +411,7 @@ def run_indexer(args):
         torch.cuda.synchronize()
 
     mla.load()
-    w = synth.make_index_workload()
+    w = synth.make_index_workload(B=args.index_batch)
     pool = torch.zeros(mla.index_pool_bytes(w.num_pages), dtype=torch.uint8, device="cuda")
     chunk = 1 << 15
     kbuf = torch.empty((chunk, mla.INDEX_DIM), dtype=torch.bfloat16, device="cuda")
@@ -644,6 +644,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="paged_batch",
                     choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse",
                              "indexer_topk"])
+    ap.add_argument("--index-batch", type=int, default=64,
+                    help="indexer_topk: queries per step (64 is the workload; smaller for profiling)")
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0 = enough to exceed L2 3x)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -3,10 +3,10 @@
  * for NVIDIA GB300 (sm_103a).
  *
  * What is computed.  Each cached token of one layer is a latent record [c_KV (512) | k_rope (64)]
- * ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token", Fig. 3: "What stays in the cache is
- * C^KV (512 dimensions) and K^R (64 dimensions)").  For a new token, every head h brings a query
- * already absorbed into the latent space, q_lat[h] = Q^C_h (W^UK_h)^T (512), and a rotary query
- * q_rope[h] (64) (same page, Fig. 5 (2) "Absorb").  Decode scores every visible position t,
+ * ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token", Fig. 3: the cache keeps only the
+ * 512-dim latent C^KV and the 64-dim rotary key K^R of each token).  For a new token, every
+ * head h brings a query already absorbed into the latent space, q_lat[h] = Q^C_h (W^UK_h)^T
+ * (512), and a rotary query q_rope[h] (64) (same page, Fig. 5 (2) "Absorb").  Decode scores every visible position t,
  *     s_t = scale * (q_lat[h] . c_t + q_rope[h] . k_rope_t)              (Fig. 4 (1); scale is
  *                                                                        1/sqrt(d_k + d_r))
  * and returns the absorbed value path U_h = sum_t softmax(s)_t c_t (Fig. 6 (2)) together with
@@ -209,9 +209,11 @@ mla_status mla_index_append(void* pool, int64_t num_pages, const void* k_index, 
  *                row t % 64 of page block_table[b][t / 64]; positions t < seq_lens[b] are visible).
  *   scores     : device fp32 [B, max_seq_len]; scores[b][t] = I(b, t) for t < seq_lens[b]; the
  *                rest of each row is not written.
- * The dot products are bf16 x bf16 (E4M3 codes convert to bf16 exactly) with fp32 accumulation;
- * the key scale multiplies after the ReLU (it is >= 0).  A visible position whose page is
- * outside the pool scores as an all-zero key and records MLA_ERR_BOUNDS.  MLA_ERR_INVALID for
+ * The dot products have exact products and fp32 accumulation (E4M3 codes convert to f16 exactly;
+ * per head, q is scaled by a power of two into f16 range and the head weight by its inverse, so
+ * every bf16 q element within 2^31 of its head's largest magnitude is exact); the key scale
+ * multiplies after the ReLU (it is >= 0).  A visible position whose page is outside the pool
+ * records MLA_ERR_BOUNDS (its score is then unspecified; no memory outside the pool is read).  MLA_ERR_INVALID for
  * null or misaligned pointers, B < 0, max_pages < 1 or max_seq_len > max_pages * 64. */
 mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_index, const float* w_index,
                              const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
@@ -219,9 +221,9 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
 
 /* Top-k selection per row: among positions t < seq_lens[b] (clamped to [0, ld]) of row b of
  * `scores` (device fp32 [B, ld]), the K highest scores, a tie going to the lower position
- * ("each row picks up to 2,048 highest-scoring positions among the positions that query can
- * see"), written to topk_idx[b] (device int32 [B, K]) in increasing position order and padded
- * with -1 past the min(K, seq_lens[b]) picks: directly the topk_idx of mla_decode.  Scores must
+ * (section "The score that picks positions": every query keeps at most 2,048 of the positions
+ * visible to it, those with the largest scores), written to topk_idx[b] (device int32
+ * [B, K]) in increasing position order and padded with -1 past the min(K, seq_lens[b]) picks: directly the topk_idx of mla_decode.  Scores must
  * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, K < 1 or ld < 0. */
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream);

@@ -199,5 +199,8 @@ cudaError_t launch_merge_slots(const float* o_part, const float* lse_part, const
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw,
                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+// 3D tiled tensor map (dims innermost first, byte strides of dims 1 and 2).
+bool encode_3d(CUtensorMap* m, const void* base, const uint64_t dims[3], const uint64_t strides_bytes[2],
+               const uint32_t box[3], CUtensorMapSwizzle sw, CUtensorMapDataType dt);
 
 }  // namespace mla

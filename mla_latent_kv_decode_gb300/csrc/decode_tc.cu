@@ -1020,6 +1020,17 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_3d(CUtensorMap* m, const void* base, const uint64_t dims[3], const uint64_t strides_bytes[2],
+               const uint32_t box[3], CUtensorMapSwizzle sw, CUtensorMapDataType dt) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+    cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Workspace of the tensor-core path: 2 partial slots per cluster (fp32 [128][512] + lse [128]),
 // then per request its first partial slot and last cluster (int32 [B][2]).

@@ -193,8 +193,8 @@ int64_t oracle_cache_append(int fmt, uint8_t* pool, int64_t num_pages, const uin
 
 /* Read one record back as exact doubles: c[512], kr[64].
  * FP8 mixed: c[k] = e4m3_value(code[k]) * s_{k / 128}, exact in double (at most 4 + 24
- * significant bits); the scale "brings values stored at low precision back to their
- * original size" ([KV] "KV cache per token at a glance"). */
+ * significant bits); multiplying by the scale restores the magnitude that the low-precision
+ * codes were divided down from ([KV] "KV cache per token at a glance"). */
 void oracle_read_record(int fmt, const uint8_t* pool, int64_t slot, double* c, double* kr) {
     int64_t rb = oracle_record_bytes(fmt);
     const uint8_t* rec = pool + slot * rb;
@@ -343,9 +343,9 @@ void oracle_combine(const float* o_part, const float* lse_part, int32_t S, int64
 /* ---------------------------------------------------------------------------------------- */
 
 /* Index-key page of this library's pool: the 64 tokens' 128 E4M3 codes (token-major, 8,192 B)
- * followed by their 64 fp32 scales (256 B), 8,448 B per page = 64 x 132 B: the search key is
- * "128 FP8 values with one FP32 scale for all 128 dimensions", quantised entirely ([KV]
- * "Calculating V3.2's KV cache").  The scale rule is the main cache's: absmax / 448. */
+ * followed by their 64 fp32 scales (256 B), 8,448 B per page = 64 x 132 B: a search key is 128
+ * FP8 codes sharing a single fp32 scale, every dimension quantised, the rotary ones included
+ * ([KV] "Calculating V3.2's KV cache").  The scale rule is the main cache's: absmax / 448. */
 #define ORACLE_IDX_DIM 128
 #define ORACLE_IDX_PAGE_BYTES (ORACLE_PAGE * (ORACLE_IDX_DIM + 4))
 
@@ -387,9 +387,8 @@ void oracle_index_read(const uint8_t* pool, int64_t slot, double* k) {
 
 /* Indexer score of one query (heads x dim, fp64) against one key (dim):
  *     I = sum_j w[j] * ReLU(q[j] . k)
- * ([KV] "The score that picks positions": "for each head, take the dot product of the query
- * and the shared key, apply ReLU, and multiply the result by the head weight; then sum over
- * all heads").  Written for any head count and width. */
+ * ([KV] "The score that picks positions": per head, the query-key dot product goes through a
+ * ReLU and is weighted by that head's weight; the weighted terms add up over the heads).  Written for any head count and width. */
 double oracle_index_score(const double* q, const double* w, const double* k, int heads, int dim) {
     double I = 0.0;
     for (int j = 0; j < heads; ++j) {
@@ -437,8 +436,8 @@ int oracle_indexer_scores(const uint8_t* pool, int64_t num_pages, const uint16_t
 
 /* Top-k selection of one row: among positions t < n, the K with the highest scores, a tie going
  * to the lower position; written to idx[0 .. K) in increasing position order, -1 past the
- * min(K, n) picks ([KV] "The score that picks positions": "each row picks up to 2,048
- * highest-scoring positions among the positions that query can see").  Plain selection: K passes
+ * min(K, n) picks ([KV] "The score that picks positions": a query keeps at most 2,048 of the
+ * positions it can see, those that score highest).  Plain selection: K passes
  * over the row, each taking the best position not taken yet (the tie rule is the order of the
  * comparison), then a sort of the picks. */
 void oracle_topk_row(const double* scores, int64_t n, int32_t K, int32_t* idx) {

@@ -122,6 +122,38 @@ def test_indexer_scores_and_topk(torch, seq):
         assert np.array_equal(got, exp), K
 
 
+def test_indexer_scores_subnormal_codes(torch):
+    """Keys whose codes are almost all E4M3 subnormals (one dim holds the absmax, the others are
+    ~1e-5 of it) against queries that give that dim no weight: the score is then the subnormal
+    codes' contribution alone, so the bound below leaves no room for a code converted wrongly."""
+    rng = np.random.default_rng(55)
+    T, num_pages = 200, 4
+    x = rng.uniform(-0.03, 0.03, (T, 128)).astype(np.float32)
+    x[:, 0] = rng.uniform(500, 2000, T).astype(np.float32) * rng.choice([-1, 1], T)
+    x[5, 1:] = 0.0
+    bits = synth._bf16_rne(x)
+    slot = np.arange(T, dtype=np.int32)
+    host = oracle.new_index_pool(num_pages)
+    oracle.index_append(host, bits, slot)
+    k0 = oracle.index_read(host, 0)
+    assert np.count_nonzero(np.abs(k0[1:]) < np.abs(k0[0]) * 2.0 ** -6 / 448 * 1.0001) > 100
+    dev = torch.zeros(mla.index_pool_bytes(num_pages), dtype=torch.uint8, device="cuda")
+    mla.index_append(dev, num_pages, _bits_tensor(torch, bits), torch.from_numpy(slot).cuda())
+    q = synth._bf16_rne(rng.standard_normal((1, 64, 128)).astype(np.float32))
+    q[:, :, 0] = 0
+    w = rng.uniform(-1, 1, (1, 64)).astype(np.float32)
+    bt = np.arange(num_pages, dtype=np.int32)[None]
+    seq = np.array([T], np.int32)
+    scores = mla.indexer_score(dev, num_pages, _bits_tensor(torch, q), torch.from_numpy(w).cuda(),
+                               torch.from_numpy(bt).cuda(), torch.from_numpy(seq).cuda(), T)
+    assert mla.check_status() == 0
+    gs = scores.cpu().numpy().astype(np.float64)[0]
+    ref = oracle.indexer_scores(host, q, w, bt, seq, T)[0]
+    bound = _score_bound(host, q, w, bt, seq, T)[0]
+    assert np.count_nonzero(ref) > T // 2
+    assert np.all(np.abs(gs - ref) <= bound), float(np.max(np.abs(gs - ref) - bound))
+
+
 def test_topk_ties_and_edges(torch):
     rng = np.random.default_rng(53)
     B, ld = 6, 9000
