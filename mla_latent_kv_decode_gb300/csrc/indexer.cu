@@ -10,15 +10,15 @@
 // their 64 fp32 scales (one per key, absmax / 448, the main cache's rule); the codes of a page are
 // kept together so that every key starts on a 16-byte boundary.
 //
-// Scores: the keys of 128 positions (two pages) against one request's 64 head queries are one
-// tensor-core contraction D[128 x 64] = codes[128 x 128] . q^T (f16 operands, exact products,
+// Scores: the keys of 256 positions (four pages) against one request's 64 head queries are two
+// tensor-core contractions D[128 x 64] = codes[128 x 128] . q^T (f16 operands, exact products,
 // fp32 accumulation in TMEM), and since a key's scale s >= 0,
 //   I = s * sum_j w_j max(D_j, 0).
-// One CTA per SM walks a balanced range of (request, 128-position) tiles.  A producer thread
-// loads whole pages into an 8-deep shared-memory ring by TMA; converter warps turn the E4M3 codes
-// into f16 straight in tensor memory (the MMA's A operand); one warp issues the MMAs; 4 warps
-// (thread = position = TMEM lane) finish the scores.  The pass is HBM-bound on the keys (132 B per
-// position).
+// One CTA per SM walks a balanced range of (request, 256-position) tiles.  Two producer threads
+// load whole pages into an 8-deep shared-memory ring by TMA; converter warps turn the E4M3 codes
+// into f16 straight in tensor memory (the MMA's A operand); one warp issues the MMAs; epilogue
+// warps (thread = position = TMEM lane) finish the scores.  The pass is HBM-bound on the keys
+// (132 B per position).
 //
 // Top-k: one CTA per request; a radix select on order-preserving keys of the fp32 scores (four
 // 8-bit digits, most significant first) finds the K-th largest, then an ordered compaction writes
@@ -37,7 +37,9 @@ constexpr int kIdxDim = MLA_INDEX_DIM;           // 128
 constexpr int kIdxHeads = MLA_INDEX_HEADS;       // 64
 constexpr int kIdxPageBytes = MLA_INDEX_PAGE_BYTES;   // 8448
 constexpr int kIdxScaleOff = kPage * kIdxDim;    // 8192: scales after the page's codes
-constexpr int kTile = 128;                       // positions per tile (two pages)
+constexpr int kTile = 256;                       // positions per tile (four pages)
+constexpr int kMH = kTile / 128;                 // its 128-position halves (one MMA row block each)
+constexpr int kTP = kTile / 64;                  // its pages
 
 // ------------------------------------------------------------------------------------ append
 
@@ -82,40 +84,51 @@ __global__ void __launch_bounds__(256) index_append_kernel(uint8_t* __restrict__
 
 // ------------------------------------------------------------------------------------ scores
 
-// Warp roles: 8 converter warps in two groups of 4 (group g converts the tiles i = g mod 2; warp
-// w of a group owns TMEM lanes 32 (w % 4) ..), 4 epilogue warps, the MMA issuer, the producer.
+// Warp roles: 8 converter warps and 8 epilogue warps, each in two groups of 4 (group g takes the
+// tiles i = g mod 2; warp w of a group owns TMEM lanes 32 (w % 4) ..), two MMA issuers (warps 16
+// and 19) and two producers (warps 17, 18), issuer / producer g for the tiles i = g mod 2.  A warp
+// runs on sub-partition warp % 4, so each sub-partition carries one single-thread role.
 constexpr int kConvWarps = 8;
-constexpr int kIssWarp = kConvWarps + 4;
-constexpr int kProdWarp = kConvWarps + 5;
-constexpr int kSThreads = 32 * (kConvWarps + 6);
-constexpr int kNR = 8;                           // raw page slots (tiles in flight)
-constexpr int kNS = 4;                           // q / scale / weight stages
-constexpr int kNA = 4;                           // A operands in tensor memory
+constexpr int kEpiWarps = 8;
+constexpr int kIssWarp = kConvWarps + kEpiWarps;   // even tiles; kIssWarp + 3: odd tiles
+constexpr int kProdWarp = kIssWarp + 1;
+constexpr int kSThreads = 32 * (kIssWarp + 4);
+constexpr int kNR = 4;                           // raw page slots (tiles in flight)
+constexpr int kNS = 8;                           // per-tile stages (scales, weights, tile info)
+constexpr int kNA = 2;                           // A operands in tensor memory
 constexpr int kND = 2;                           // accumulators in tensor memory
-constexpr int kLookup = 8;                       // tiles whose pages the producer looks up together
-// raw slot: the tile's two pages' codes (64 rows x 128 B each, 128-byte swizzle) then their scales
-constexpr int kSlotScales = 2 * kPage * kIdxDim;       // 16384
-constexpr int kSlot = 17408;                            // 16384 + 2 x 256 rounded to 1 KB
-// stage: q as the MMA's B operand ([64 heads x 64 dims] f16 per chunk, two chunks, SW128),
-// the tile's 128 key scales, the 64 head weights, request / first position / count
+constexpr int kLookup = 2;                       // tiles whose pages a producer looks up together
+// raw slot: the tile's four pages whole, each as 66 rows of 128 B (64 rows of codes, then the 64
+// scales) with the 128-byte swizzle, at 9 KB apart
+constexpr int kPageRows = kIdxPageBytes / 128;          // 66
+constexpr int kSlotPage = 9216;
+constexpr int kSlot = kTP * kSlotPage;
+// q slot (one per request in flight, two): q as the MMA's B operand ([64 heads x 64 dims] f16
+// per chunk, two chunks, SW128), then the 64 rescaled head weights
 constexpr int kQChunk = kIdxHeads * 128;
-constexpr int kStQ = 0;
-constexpr int kStScale = 2 * kQChunk;                   // 16384
-constexpr int kStW = kStScale + kTile * 4;              // 16896
-constexpr int kStMeta = kStW + kIdxHeads * 4;           // 17152
-constexpr int kStage = 17408;
-constexpr int kSOffStage = kNR * kSlot;                 // 139264
-constexpr int kSOffEntry = kSOffStage + kNS * kStage;   // 208896: per raw slot {b, base, cnt, -}
+constexpr int kQW = 2 * kQChunk;                        // 16384
+constexpr int kQSlot = 17408;
+// stage: the tile's 256 key scales, its 64 head weights, {request, first position, count, flags}
+constexpr int kStScale = 0;
+constexpr int kStW = kTile * 4;                         // 1024
+constexpr int kStMeta = kStW + kIdxHeads * 4;           // 1280
+constexpr int kStage = 1296;
+constexpr int kSOffQ = kNR * kSlot;                     // 147456
+constexpr int kSOffStage = kSOffQ + 2 * kQSlot;         // 182272
+constexpr int kSOffEntry = kSOffStage + kNS * kStage;   // per raw slot {b, base, cnt, flags}
 constexpr int kSOffBar = kSOffEntry + kNR * 16;
-constexpr int kNBars = 2 * kNR + 2 * kNS + kNA + 2 * kND + 1;
+constexpr int kNBars = 2 * kNR + 2 * kNS + kNA + 2 * kND + 4 + 2;
 constexpr int kSSmem = kSOffBar + 8 * kNBars + 1024;
-constexpr uint32_t kSTmemCols = 512;                    // A: 4 x 64 columns, D: 2 x 64 columns
-constexpr uint32_t kTmemD = 64 * kNA;
-static_assert(kSlotScales + 2 * 256 <= kSlot && kSlot % 1024 == 0, "raw slot");
-static_assert(kStMeta + 16 <= kStage && kStage % 1024 == 0, "stage layout");
+constexpr uint32_t kSTmemCols = 512;                    // A: 2 x 128 columns, D: 2 x 128 columns
+constexpr uint32_t kTmemD = 64 * kMH * kNA;
+// tile flags: request ordinal within the CTA's range (bits 0..27), first / last tile of the request
+constexpr int kFirst = 1 << 28, kLast = 1 << 29, kOrdMask = (1 << 28) - 1;
+static_assert(kPageRows * 128 == kIdxPageBytes && kIdxPageBytes <= kSlotPage && kSlotPage % 1024 == 0, "raw slot");
+static_assert(kQW + kIdxHeads * 4 <= kQSlot && kQSlot % 1024 == 0 && kSOffQ % 1024 == 0, "q slot");
+static_assert(kStMeta + 16 <= kStage && kStage % 16 == 0, "stage layout");
 static_assert(kSSmem <= 232448, "shared memory");
-static_assert(kNR % 2 == 0 && kNS % 2 == 0 && kNA % 2 == 0, "rings shared by two converter groups");
-static_assert(kTmemD + 64 * kND <= kSTmemCols, "tensor memory");
+static_assert(kNR % 2 == 0 && kNS % 2 == 0 && kNA % 2 == 0 && kND % 2 == 0, "rings shared by two groups");
+static_assert(kTmemD + 64 * kMH * kND <= kSTmemCols, "tensor memory");
 
 struct ScoreParams {
     const uint8_t* pool;
@@ -132,16 +145,16 @@ struct ScoreParams {
     int B;
 };
 
-__device__ __forceinline__ int tiles128(int n) { return (n + kTile - 1) / kTile; }
+__device__ __forceinline__ int tiles_n(int n) { return (n + kTile - 1) / kTile; }
 
-// Balanced contiguous range of the (request, 128-position tile) stream for CTA c of C; run by one
+// Balanced contiguous range of the (request, 256-position tile) stream for CTA c of C; run by one
 // warp.  Returns the first tile and the tile count through shared memory.
 __device__ void score_schedule(const ScoreParams& p, int c, int C, int* s_b, int* s_t, int* s_n) {
     const int lane = threadIdx.x & 31;
     const int per = (p.B + 31) / 32;
     const int b_lo = min(p.B, lane * per), b_hi = min(p.B, b_lo + per);
     long long mine = 0;
-    for (int b = b_lo; b < b_hi; ++b) mine += tiles128(clamp_len(p.seq_lens[b], p.max_seq_len));
+    for (int b = b_lo; b < b_hi; ++b) mine += tiles_n(clamp_len(p.seq_lens[b], p.max_seq_len));
     long long incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -152,7 +165,7 @@ __device__ void score_schedule(const ScoreParams& p, int c, int C, int* s_b, int
     const long long g0 = (long long)c * W / C, g1 = (long long)(c + 1) * W / C;
     long long pre = incl - mine;
     for (int b = b_lo; b < b_hi; ++b) {
-        const int nt = tiles128(clamp_len(p.seq_lens[b], p.max_seq_len));
+        const int nt = tiles_n(clamp_len(p.seq_lens[b], p.max_seq_len));
         if (g0 < W && g0 >= pre && g0 < pre + nt) {
             *s_b = b;
             *s_t = (int)(g0 - pre);
@@ -166,7 +179,7 @@ struct TileCursor {
     int b, t, nt, n;
     __device__ __forceinline__ void load(const ScoreParams& p) {
         n = clamp_len(p.seq_lens[b], p.max_seq_len);
-        nt = tiles128(n);
+        nt = tiles_n(n);
     }
     __device__ __forceinline__ void next(const ScoreParams& p) {
         ++t;
@@ -197,16 +210,22 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
     return v;
 }
 
-// Scores of a balanced range of (request, 128-position) tiles per CTA.
-//   producer: looks up each tile's two pages (checked) and loads them whole into a raw slot (the
-//             codes by a 3D tensor map with a 128-byte swizzle, the scales by a bulk copy);
+// Scores of a balanced range of (request, 256-position) tiles per CTA.
+//   producers: look up each tile's four pages (checked) and load each whole into a raw slot by one
+//             TMA copy (a 3D tensor map: 66 rows of 128 B per page, 128-byte swizzle); they walk
+//             the whole tile stream, so they also number the requests and mark each request's
+//             first and last tile;
 //   converters: E4M3 codes -> f16 (exact) straight into tensor memory as the MMA's A operand
-//             (row = position, two dims per column), key scales into the stage, and on a request
-//             change the request's q (scaled per head by 2^e into [2^14, 2^15) of f16, the head
-//             weight by 2^-e: the products w ReLU(q . k) are unchanged, and every bf16 q element
-//             not 2^31 below its head's largest is exact in f16);
-//   issuer:   D[128 x 64] = A[128 x 128] . q^T, eight K=16 MMAs;
-//   epilogue: thread = position = TMEM lane: I = s * sum_j w_j max(D_j, 0).
+//             (row = position, two dims per column); key scales, head weights and tile info into
+//             the tile's stage; on a request's first tile, that request's q into a q slot (scaled
+//             per head by 2^e into [2^14, 2^15) of f16, the head weight by 2^-e: the products
+//             w ReLU(q . k) are unchanged, and every bf16 q element not 2^31 below its head's
+//             largest is exact in f16);
+//   issuers:  D[128 x 64] = A[128 x 128] . q^T for each half of the tile, eight K=16 MMAs each; each walks the tile
+//             stream and, at the end of each request, commits the release of its q slot (the slot
+//             is free once both issuers' MMAs up to there are done);
+//   epilogue: thread = position = TMEM lane: I = s * sum_j w_j max(D_j, 0), two groups of 4 warps
+//             on alternate tiles.
 __global__ void __launch_bounds__(kSThreads, 1)
     indexer_score_kernel(const __grid_constant__ CUtensorMap tm_codes, ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -218,16 +237,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar0 = sbase + kSOffBar;
-    auto raw_full = [&](int r) { return bar0 + 8 * r; };
-    auto raw_empty = [&](int r) { return bar0 + 8 * (kNR + r); };
-    auto full = [&](int s) { return bar0 + 8 * (2 * kNR + s); };
-    auto empty = [&](int s) { return bar0 + 8 * (2 * kNR + kNS + s); };
-    auto afree = [&](int a) { return bar0 + 8 * (2 * kNR + 2 * kNS + a); };
-    auto dfull = [&](int d) { return bar0 + 8 * (2 * kNR + 2 * kNS + kNA + d); };
-    auto dfree = [&](int d) { return bar0 + 8 * (2 * kNR + 2 * kNS + kNA + kND + d); };
-    const uint32_t drain = bar0 + 8 * (kNBars - 1);
+    auto raw_full = [&](int r) { return bar0 + 8 * r; };                   // producer -> converters
+    auto raw_empty = [&](int r) { return bar0 + 8 * (kNR + r); };          // converters -> producer
+    auto full = [&](int s) { return bar0 + 8 * (2 * kNR + s); };           // converters -> issuer, epilogue
+    auto sempty = [&](int s) { return bar0 + 8 * (2 * kNR + kNS + s); };   // epilogue -> converters
+    auto afree = [&](int a) { return bar0 + 8 * (2 * kNR + 2 * kNS + a); };            // MMA -> converters
+    auto dfull = [&](int d) { return bar0 + 8 * (2 * kNR + 2 * kNS + kNA + d); };      // MMA -> epilogue
+    auto dfree = [&](int d) { return bar0 + 8 * (2 * kNR + 2 * kNS + kNA + kND + d); };   // epilogue -> MMA
+    auto qfull = [&](int q) { return bar0 + 8 * (2 * kNR + 2 * kNS + kNA + 2 * kND + q); };     // q slot written
+    auto qempty = [&](int q) { return bar0 + 8 * (2 * kNR + 2 * kNS + kNA + 2 * kND + 2 + q); };   // q slot free
     int4* entry = reinterpret_cast<int4*>(sm + kSOffEntry);
     const uint32_t wait_limit = p.ctl->wait_limit;
+    auto swait = [](uint32_t bar, uint32_t parity, uint32_t limit) { return mbar_wait(bar, parity, limit); };
 
     if (tid == 0) {
         s_abort = 0;
@@ -244,14 +265,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         for (int s = 0; s < kNS; ++s) {
             mbar_init(full(s), 4);
-            mbar_init(empty(s), 1 + 4);
+            mbar_init(sempty(s), 4);
         }
         for (int a = 0; a < kNA; ++a) mbar_init(afree(a), 1);
         for (int d = 0; d < kND; ++d) {
             mbar_init(dfull(d), 1);
             mbar_init(dfree(d), 4);
         }
-        mbar_init(drain, 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(qfull(q), 4);
+            mbar_init(qempty(q), 2);   // both issuers, at the request's end
+        }
+        mbar_init(bar0 + 8 * (kNBars - 2), 1);   // the issuers' drains
+        mbar_init(bar0 + 8 * (kNBars - 1), 1);
         fence_mbar_init();
     }
     if (warp == kIssWarp) {
@@ -270,135 +296,160 @@ __global__ void __launch_bounds__(kSThreads, 1)
         record_error(p.ctl, MLA_ERR_TIMEOUT, 40 + where);
     };
 
-    if (warp == kProdWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0 && n_local > 0) {
+    if (warp == kProdWarp || warp == kProdWarp + 1) {
+        // ------------------------------------------------------------ producers
+        // Producer pw loads the tiles j = pw, pw + 2, ..; its cursor walks every tile, counting
+        // request changes.  The block-table lookups of its next kLookup tiles are in flight while
+        // the current ones are issued.
+        const int pw = warp - kProdWarp;
+        if (lane == 0 && pw < n_local) {
             TileCursor pf;
             pf.b = s_b0;
             pf.t = s_t0;
             pf.load(p);
-            int issued = 0;
-            for (int j0 = 0; j0 < n_local && !s_abort; j0 += kLookup) {
-                const int jn = min(kLookup, n_local - j0);
-                int eb[kLookup], ebase[kLookup], ecnt[kLookup], pg0[kLookup], pg1[kLookup];
+            int ord = 0, prev_b = -1;   // request ordinal of the cursor's tile; request before it
+            auto step = [&](int j) {    // cursor from tile j to tile j + 1 (j + 1 < n_local)
+                prev_b = pf.b;
+                pf.next(p);
+                if (pf.b != prev_b) ++ord;
+            };
+            if (pw == 1) step(0);
+            struct Batch {
+                int b[kLookup], base[kLookup], cnt[kLookup], flags[kLookup], pg[kLookup][kTP];
+            };
+            // tiles j0, j0 + 2, .. of this producer (cursor at tile j0; left at the tile after)
+            auto fill = [&](Batch& x, int j0) {
 #pragma unroll
                 for (int k = 0; k < kLookup; ++k) {
-                    eb[k] = pf.b;
-                    ebase[k] = pf.t * kTile;
-                    ecnt[k] = min(kTile, pf.n - ebase[k]);
-                    if (k + 1 < jn) pf.next(p);
-                }
+                    const int j = j0 + 2 * k;
 #pragma unroll
-                for (int k = 0; k < kLookup; ++k) {   // the lookups go out together
-                    pg0[k] = pg1[k] = -1;
-                    if (k < jn) {
-                        const int32_t* row = p.block_table + (size_t)eb[k] * p.max_pages + (ebase[k] >> 6);
-                        pg0[k] = row[0];
-                        if (ecnt[k] > 64) pg1[k] = row[1];
+                    for (int h = 0; h < kTP; ++h) x.pg[k][h] = -1;
+                    x.b[k] = pf.b;
+                    x.base[k] = pf.t * kTile;
+                    x.cnt[k] = min(kTile, pf.n - x.base[k]);
+                    x.flags[k] = ord | (prev_b != pf.b ? kFirst : 0);
+                    if (j < n_local) {
+                        const int32_t* row = p.block_table + (size_t)x.b[k] * p.max_pages + (x.base[k] >> 6);
+#pragma unroll
+                        for (int h = 0; h < kTP; ++h)
+                            if (x.cnt[k] > 64 * h) x.pg[k][h] = row[h];
+                        if (j + 1 < n_local) {
+                            step(j);
+                            if (pf.b != x.b[k]) x.flags[k] |= kLast;
+                            if (j + 2 < n_local) step(j + 1);
+                        } else {
+                            x.flags[k] |= kLast;
+                        }
                     }
                 }
-                bool ok = true;
+            };
+            Batch cur, nxt;
+            int issued_hi = -1;   // the last tile issued
+            fill(cur, pw);
+            bool ok = true;
+            for (int j0 = pw; ok && j0 < n_local && !s_abort; j0 += 2 * kLookup) {
+                if (j0 + 2 * kLookup < n_local) fill(nxt, j0 + 2 * kLookup);
 #pragma unroll
                 for (int k = 0; k < kLookup; ++k) {
-                    if (k >= jn || !ok) continue;
-                    const int j = j0 + k, r = j % kNR;
-                    if (j >= kNR && !mbar_wait(raw_empty(r), ((j / kNR) - 1) & 1, wait_limit)) {
+                    const int j = j0 + 2 * k, r = j % kNR;
+                    if (j >= n_local || !ok) continue;
+                    if (j >= kNR && !swait(raw_empty(r), ((j / kNR) - 1) & 1, wait_limit)) {
                         fail(4);
                         ok = false;
                         continue;
                     }
-                    int pg[2] = {pg0[k], pg1[k]};
+                    int pg[kTP];
                     uint32_t bytes = 0;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h == 1 && ecnt[k] <= 64) continue;
+                    for (int h = 0; h < kTP; ++h) {
+                        pg[h] = cur.pg[k][h];
+                        if (cur.cnt[k] <= 64 * h) continue;
                         if (pg[h] < 0 || pg[h] >= p.num_pages) {
                             record_error(p.ctl, MLA_ERR_BOUNDS, pg[h]);
                             pg[h] = -1;
                         } else {
-                            bytes += kPage * kIdxDim + kPage * 4;
+                            bytes += kIdxPageBytes;
                         }
                     }
-                    entry[r] = make_int4(eb[k], ebase[k], ecnt[k], 0);
+                    entry[r] = make_int4(cur.b[k], cur.base[k], cur.cnt[k], cur.flags[k]);
                     const uint32_t slot = sbase + r * kSlot;
                     mbar_arrive_expect_tx(raw_full(r), bytes);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (pg[h] < 0) continue;
-                        tma_load_3d(slot + h * kPage * kIdxDim, &tm_codes, raw_full(r), 0, 0, pg[h]);
-                        bulk_load(slot + kSlotScales + h * 256, p.pool + (size_t)pg[h] * kIdxPageBytes + kIdxScaleOff,
-                                  kPage * 4, raw_full(r));
-                    }
-                    issued = j + 1;
+                    for (int h = 0; h < kTP; ++h)
+                        if (pg[h] >= 0) tma_load_3d(slot + h * kSlotPage, &tm_codes, raw_full(r), 0, 0, pg[h]);
+                    issued_hi = j;
                 }
-                if (!ok) break;
-                if (j0 + jn < n_local) pf.next(p);
+                cur = nxt;
             }
             // nothing of this CTA's copies is left in flight when it exits
-            for (int j = max(0, issued - kNR); j < issued; ++j)
-                if (!mbar_wait(raw_full(j % kNR), (j / kNR) & 1, wait_limit)) fail(6);
+            for (int j = issued_hi; j >= 0 && j > issued_hi - kNR; j -= 2)
+                if (!swait(raw_full(j % kNR), (j / kNR) & 1, wait_limit)) fail(6);
         }
         __syncwarp();
     } else if (warp < kConvWarps) {
         // ------------------------------------------------------------ converters
         const int g = warp >> 2, q4 = warp & 3;
         const int gt = tid & 127;             // thread within the group
-        const int pp = q4 * 32 + lane;        // position = TMEM lane
-        const int h = pp >> 6, rr = pp & 63;  // page of the tile, row of the page
+        const int pp = q4 * 32 + lane;        // position within each half = TMEM lane
+        const int rr = pp & 63;               // row of the page
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        int qh1 = -1, qh2 = -1;               // requests of this group's previous two tiles
         for (int i = g; i < n_local; i += 2) {
             if (s_abort) break;
             const int s = i % kNS, r = i % kNR, a = i % kNA;
-            if (!mbar_wait(raw_full(r), (i / kNR) & 1, wait_limit)) {
+            if (!swait(raw_full(r), (i / kNR) & 1, wait_limit)) {
                 if (lane == 0) fail(1);
                 break;
             }
             const int4 en = entry[r];
-            const uint32_t rowa = sbase + r * kSlot + h * kPage * kIdxDim + rr * kIdxDim;
-            uint4 u[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) u[c] = ld_shared_v4(rowa + ((c ^ (rr & 7)) << 4));
-            const float sc = *reinterpret_cast<const float*>(sm + r * kSlot + kSlotScales + h * 256 + rr * 4);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(raw_empty(r));
-            const bool new_q = qh2 != en.x;
-            qh2 = qh1;
-            qh1 = en.x;
-            if (i >= kNA && !mbar_wait(afree(a), ((i / kNA) - 1) & 1, wait_limit)) {
+            if (i >= kNA && !swait(afree(a), ((i / kNA) - 1) & 1, wait_limit)) {
                 if (lane == 0) fail(2);
                 break;
             }
             tc_fence_after();
+            float sc[kMH];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t o[32];
+            for (int m = 0; m < kMH; ++m) {
+                // position 128 m + pp: page 2 m + pp / 64, row rr
+                const int pgo = r * kSlot + (2 * m + (pp >> 6)) * kSlotPage;
+                const uint32_t rowa = sbase + pgo + rr * 128;
+                uint4 u[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = u[4 * half + c];
-                    o[8 * c + 0] = e4m3x2_to_f16x2(v.x);
-                    o[8 * c + 1] = e4m3x2_to_f16x2(v.x >> 16);
-                    o[8 * c + 2] = e4m3x2_to_f16x2(v.y);
-                    o[8 * c + 3] = e4m3x2_to_f16x2(v.y >> 16);
-                    o[8 * c + 4] = e4m3x2_to_f16x2(v.z);
-                    o[8 * c + 5] = e4m3x2_to_f16x2(v.z >> 16);
-                    o[8 * c + 6] = e4m3x2_to_f16x2(v.w);
-                    o[8 * c + 7] = e4m3x2_to_f16x2(v.w >> 16);
+                for (int c = 0; c < 8; ++c) u[c] = ld_shared_v4(rowa + ((c ^ (rr & 7)) << 4));
+                // scale rr: byte 4 rr of rows 64, 65 (unit (rr % 32) / 4, swizzled by the row)
+                sc[m] = *reinterpret_cast<const float*>(
+                    sm + pgo + (64 + (rr >> 5)) * 128 + ((((rr & 31) >> 2) ^ (rr >> 5)) << 4) + (rr & 3) * 4);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t o[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = u[4 * half + c];
+                        o[8 * c + 0] = e4m3x2_to_f16x2(v.x);
+                        o[8 * c + 1] = e4m3x2_to_f16x2(v.x >> 16);
+                        o[8 * c + 2] = e4m3x2_to_f16x2(v.y);
+                        o[8 * c + 3] = e4m3x2_to_f16x2(v.y >> 16);
+                        o[8 * c + 4] = e4m3x2_to_f16x2(v.z);
+                        o[8 * c + 5] = e4m3x2_to_f16x2(v.z >> 16);
+                        o[8 * c + 6] = e4m3x2_to_f16x2(v.w);
+                        o[8 * c + 7] = e4m3x2_to_f16x2(v.w >> 16);
+                    }
+                    tmem_st32(tmem + lane_off + 64 * (kMH * a + m) + 32 * half, o);
                 }
-                tmem_st32(tmem + lane_off + 64 * a + 32 * half, o);
             }
-            uint4 qv[8];
-            if (new_q) {
-                const uint4* qs = reinterpret_cast<const uint4*>(p.q + (size_t)en.x * kIdxHeads * kIdxDim);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(raw_empty(r));
+            const int ord = en.w & kOrdMask, qs = ord & 1;
+            uint8_t* qslot = sm + kSOffQ + qs * kQSlot;
+            if (en.w & kFirst) {
+                // this request's q into its slot, once the request two before has left it
+                uint4 qv[8];
+                const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (size_t)en.x * kIdxHeads * kIdxDim);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) qv[k] = __ldg(qs + gt + 128 * k);
-            }
-            if (i >= kNS && !mbar_wait(empty(s), ((i / kNS) - 1) & 1, wait_limit)) {
-                if (lane == 0) fail(3);
-                break;
-            }
-            uint8_t* st = sm + kSOffStage + s * kStage;
-            if (new_q) {
+                for (int k = 0; k < 8; ++k) qv[k] = __ldg(qsrc + gt + 128 * k);
+                if (ord >= 2 && !swait(qempty(qs), ((ord >> 1) - 1) & 1, wait_limit)) {
+                    if (lane == 0) fail(8);
+                    break;
+                }
                 // q unit gq (of 1024): head gq / 16, dims 8 (gq % 16) ..: chunk (gq % 16) / 8,
                 // unit gq % 8; the 16 units of a head sit in 16 consecutive lanes
 #pragma unroll
@@ -422,98 +473,142 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     uint32_t o[4];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) o[m] = f32x2_to_f16x2(f[2 * m] * up, f[2 * m + 1] * up);
-                    st_shared_v4(st + kStQ + (uq >> 3) * kQChunk + hd * 128 + (((uq & 7) ^ (hd & 7)) << 4), o[0],
-                                 o[1], o[2], o[3]);
+                    st_shared_v4(qslot + (uq >> 3) * kQChunk + hd * 128 + (((uq & 7) ^ (hd & 7)) << 4), o[0], o[1],
+                                 o[2], o[3]);
                     if (uq == 0) {
                         const float down = __uint_as_float((uint32_t)(127 - e) << 23);
-                        reinterpret_cast<float*>(st + kStW)[hd] = __ldg(p.w + (size_t)en.x * kIdxHeads + hd) * down;
+                        reinterpret_cast<float*>(qslot + kQW)[hd] = __ldg(p.w + (size_t)en.x * kIdxHeads + hd) * down;
                     }
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qfull(qs));
             }
-            reinterpret_cast<float*>(st + kStScale)[pp] = sc;
+            if (i >= kNS && !swait(sempty(s), ((i / kNS) - 1) & 1, wait_limit)) {
+                if (lane == 0) fail(3);
+                break;
+            }
+            if (!swait(qfull(qs), (ord >> 1) & 1, wait_limit)) {   // the request's weights
+                if (lane == 0) fail(9);
+                break;
+            }
+            uint8_t* st = sm + kSOffStage + s * kStage;
+#pragma unroll
+            for (int m = 0; m < kMH; ++m) reinterpret_cast<float*>(st + kStScale)[128 * m + pp] = sc[m];
+            if (gt < kIdxHeads)
+                reinterpret_cast<float*>(st + kStW)[gt] = reinterpret_cast<const float*>(qslot + kQW)[gt];
             if (gt == 0) *reinterpret_cast<int4*>(st + kStMeta) = en;
             tmem_wait_st();
             tc_fence_before();
-            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full(s));
         }
-    } else if (warp == kIssWarp) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kIssWarp || warp == kIssWarp + 3) {
+        // ------------------------------------------------------------ MMA issuers
         constexpr uint32_t idesc = idesc_f16(128, kIdxHeads, 0, 0);
         const uint64_t hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
         const uint32_t lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
+        const int ig = warp == kIssWarp ? 0 : 1;
+        const uint32_t drain = bar0 + 8 * (kNBars - 2 + ig);
+        TileCursor ic;
+        ic.b = s_b0;
+        ic.t = s_t0;
+        if (n_local > 0) ic.load(p);
+        int ord = 0, ready_ord = -1;   // request ordinal of tile i; the last one whose q was seen
         for (int i = 0; i < n_local; ++i) {
             if (__any_sync(0xffffffffu, s_abort)) break;
-            const int s = i % kNS, a = i % kNA, d = i % kND;
-            bool ok = mbar_wait(full(s), (i / kNS) & 1, wait_limit);
-            ok = ok && (i < kND || mbar_wait(dfree(d), ((i / kND) - 1) & 1, wait_limit));
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) fail(5);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t b_lo = ((sbase + kSOffStage + s * kStage + kStQ) >> 4) & 0x3FFF;
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < kIdxDim / 16; ++kk) {
-                    const uint32_t off_b = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
-                    mma_bf16_ts(tmem + kTmemD + 64 * d, tmem + 64 * a + 8 * kk, hi | (b_lo + lo + off_b), idesc,
-                                kk > 0 ? 1u : 0u);
+            if ((i & 1) == ig) {
+                const int s = i % kNS, a = i % kNA, d = i % kND, qs = ord & 1;
+                bool ok = swait(full(s), (i / kNS) & 1, wait_limit);
+                if (ord != ready_ord) {
+                    ok = ok && swait(qfull(qs), (ord >> 1) & 1, wait_limit);
+                    ready_ord = ord;
                 }
-                mma_commit(dfull(d));
-                mma_commit(empty(s));
-                mma_commit(afree(a));
+                ok = ok && (i < kND || swait(dfree(d), ((i / kND) - 1) & 1, wait_limit));
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) fail(5);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t b_lo = ((sbase + kSOffQ + qs * kQSlot) >> 4) & 0x3FFF;
+                if (elect_one()) {
+#pragma unroll
+                    for (int m = 0; m < kMH; ++m)
+#pragma unroll
+                        for (int kk = 0; kk < kIdxDim / 16; ++kk) {
+                            const uint32_t off_b = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
+                            mma_bf16_ts(tmem + kTmemD + 64 * (kMH * d + m), tmem + 64 * (kMH * a + m) + 8 * kk,
+                                        hi | (b_lo + lo + off_b), idesc, kk > 0 ? 1u : 0u);
+                        }
+                    mma_commit(dfull(d));
+                    mma_commit(afree(a));
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            const int b = ic.b;
+            if (i + 1 < n_local) ic.next(p);
+            if (i + 1 == n_local || ic.b != b) {   // the request of tile i ends here
+                if (elect_one()) mma_commit(qempty(ord & 1));
+                __syncwarp();
+                ++ord;
+            }
         }
         __syncwarp();
         if (elect_one()) {
             mma_commit(drain);
-            mbar_wait(drain, 0, wait_limit);
+            swait(drain, 0, wait_limit);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q4 = warp & 3;            // TMEM lanes 32 q4 .. 32 q4 + 31
-        const int pp = q4 * 32 + lane;      // position within the tile
+        const int eg = (warp - kConvWarps) >> 2, q4 = warp & 3;   // group; TMEM lanes 32 q4 ..
+        const int pp = q4 * 32 + lane;                            // position within the tile
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        for (int i = 0; i < n_local; ++i) {
+        for (int i = eg; i < n_local; i += 2) {
             const int s = i % kNS, d = i % kND;
-            bool ok = !s_abort && mbar_wait(dfull(d), (i / kND) & 1, wait_limit);
-            ok = ok && mbar_wait(full(s), (i / kNS) & 1, wait_limit);   // the stage's scales, weights
+            bool ok = !s_abort && swait(dfull(d), (i / kND) & 1, wait_limit);
+            ok = ok && swait(full(s), (i / kNS) & 1, wait_limit);   // the stage's scales, weights
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) fail(7);
                 break;
             }
             tc_fence_after();
-            uint32_t a[32], b[32];
-            tmem_ld32(tmem + lane_off + kTmemD + 64 * d, a);
-            tmem_ld32(tmem + lane_off + kTmemD + 64 * d + 32, b);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dfree(d));
             const uint8_t* st = sm + kSOffStage + s * kStage;
             const float4* wv = reinterpret_cast<const float4*>(st + kStW);
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 wa = wv[j], wb = wv[8 + j];
-                acc0 = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * j]), 0.f), acc0);
-                acc0 = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * j + 1]), 0.f), acc0);
-                acc0 = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * j + 2]), 0.f), acc0);
-                acc0 = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * j + 3]), 0.f), acc0);
-                acc1 = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * j]), 0.f), acc1);
-                acc1 = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * j + 1]), 0.f), acc1);
-                acc1 = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * j + 2]), 0.f), acc1);
-                acc1 = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * j + 3]), 0.f), acc1);
-            }
-            const float score = reinterpret_cast<const float*>(st + kStScale)[pp] * (acc0 + acc1) + 0.0f;   // (-0 -> +0)
             const int4 meta = *reinterpret_cast<const int4*>(st + kStMeta);
+            float score[kMH];
+#pragma unroll
+            for (int m = 0; m < kMH; ++m) {
+                uint32_t a[32], b[32];
+                tmem_ld32(tmem + lane_off + kTmemD + 64 * (kMH * d + m), a);
+                tmem_ld32(tmem + lane_off + kTmemD + 64 * (kMH * d + m) + 32, b);
+                tmem_wait_ld();
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 wa = wv[j], wb = wv[8 + j];
+                    acc[0] = fmaf(wa.x, fmaxf(__uint_as_float(a[4 * j]), 0.f), acc[0]);
+                    acc[1] = fmaf(wa.y, fmaxf(__uint_as_float(a[4 * j + 1]), 0.f), acc[1]);
+                    acc[2] = fmaf(wa.z, fmaxf(__uint_as_float(a[4 * j + 2]), 0.f), acc[2]);
+                    acc[3] = fmaf(wa.w, fmaxf(__uint_as_float(a[4 * j + 3]), 0.f), acc[3]);
+                    acc[0] = fmaf(wb.x, fmaxf(__uint_as_float(b[4 * j]), 0.f), acc[0]);
+                    acc[1] = fmaf(wb.y, fmaxf(__uint_as_float(b[4 * j + 1]), 0.f), acc[1]);
+                    acc[2] = fmaf(wb.z, fmaxf(__uint_as_float(b[4 * j + 2]), 0.f), acc[2]);
+                    acc[3] = fmaf(wb.w, fmaxf(__uint_as_float(b[4 * j + 3]), 0.f), acc[3]);
+                }
+                score[m] = reinterpret_cast<const float*>(st + kStScale)[128 * m + pp] *
+                               ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                           0.0f;   // (-0 -> +0)
+            }
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty(s));
-            if (pp < meta.z) p.scores[(size_t)meta.x * p.ld + meta.y + pp] = score;
+            if (lane == 0) {
+                mbar_arrive(dfree(d));
+                mbar_arrive(sempty(s));
+            }
+#pragma unroll
+            for (int m = 0; m < kMH; ++m)
+                if (128 * m + pp < meta.z) p.scores[(size_t)meta.x * p.ld + meta.y + 128 * m + pp] = score[m];
         }
     }
 
@@ -684,11 +779,12 @@ cudaError_t launch_indexer_score(const uint8_t* pool, int64_t num_pages, const _
     int sms = num_sms();
     if (sms <= 0) sms = 152;
     const int C = (int)(max_tiles < sms ? (max_tiles < 1 ? 1 : max_tiles) : sms);
-    // codes of page z, row y, byte x: pool + z * 8448 + y * 128 + x
+    // page z as 66 rows y of 128 bytes x (64 rows of codes, then the scales): pool + z * 8448 +
+    // y * 128 + x
     CUtensorMap tm;
-    const uint64_t dims[3] = {(uint64_t)kIdxDim, (uint64_t)kPage, (uint64_t)(num_pages > 0 ? num_pages : 1)};
-    const uint64_t strides[2] = {(uint64_t)kIdxDim, (uint64_t)kIdxPageBytes};
-    const uint32_t box[3] = {(uint32_t)kIdxDim, (uint32_t)kPage, 1u};
+    const uint64_t dims[3] = {128u, (uint64_t)kPageRows, (uint64_t)(num_pages > 0 ? num_pages : 1)};
+    const uint64_t strides[2] = {128u, (uint64_t)kIdxPageBytes};
+    const uint32_t box[3] = {128u, (uint32_t)kPageRows, 1u};
     if (!encode_3d(&tm, pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8))
         return cudaErrorInvalidValue;
     indexer_score_kernel<<<C, kSThreads, kSSmem, st>>>(tm, p);

@@ -91,6 +91,27 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// The same, letting the thread sleep up to `ns` nanoseconds inside the instruction while the
+// phase is incomplete (a waiting warp then takes no issue slots from the warps doing work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with sleeping polls (at most limit polls of up to ns each).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint32_t limit, uint32_t ns) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait_sleep(bar, parity, ns)) return true;
+    return false;
+}
+
 // Bounded wait for the phase with the given parity to complete: false after `limit` polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i)
