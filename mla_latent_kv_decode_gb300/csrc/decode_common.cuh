@@ -165,21 +165,27 @@ __device__ __forceinline__ void st_shared_v4(uint8_t* p, uint32_t a, uint32_t b,
     *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
 
-// 16 e4m3 codes (OCP 8-bit floating point, bias 7) to 16 bf16 values, exactly: each code goes
-// to f16 and then to fp32, both exact, and every such value is a bf16 value.
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t (&o)[8]) {
+// Two fp32 values to an f16 pair (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A bf16 pair to an f16 pair: exact for magnitudes in the f16 normal range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// 16 e4m3 codes (OCP 8-bit floating point, bias 7) to 16 f16 values, exactly: every e4m3 value
+// (normal or subnormal, at most 448) is an f16 value.
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 c, uint32_t (&o)[8]) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const __half2_raw hr =
-                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[k] >> (16 * j)) & 0xFFFFu), __NV_E4M3);
-            __half2 h2;
-            *reinterpret_cast<__half2_raw*>(&h2) = hr;
-            const float2 f = __half22float2(h2);
-            o[2 * k + j] = pack_bf16x2(f.x, f.y);
-        }
+        for (int j = 0; j < 2; ++j)
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * k + j]) : "h"((uint16_t)(w[k] >> (16 * j))));
 }
 
 // Clusters for a batch: at most one per SM pair, at least kMinTilesPerCluster tiles each.

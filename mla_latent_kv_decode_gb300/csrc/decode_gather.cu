@@ -12,31 +12,36 @@
 //     request's top-k list (sparse: only listed positions enter the softmax, same page, Fig. 8
 //     and the DSA description on that page).  Rows outside the request (past its length, padding
 //     entries, entries >= N_b) are masked and read as zeros;
-//   * the agent warps load each row's bytes of this CTA's half from global memory and write them
-//     into a shared-memory tile in the MMA operand layouts: bf16 latent [64 x 256] (128-byte
-//     swizzle), bf16 rope [64 x 32] (64-byte swizzle), the two fp32 group scales per row and a
-//     64-bit mask of valid rows;
+//   * FP8 records: a producer warp copies each tile's raw bytes of this CTA's half into a
+//     conversion slot as soon as PV has released it (a page: three TMA boxes; top-k rows: three
+//     bulk copies per row), with the row's four group scales and a 64-bit mask of valid rows; the
+//     agent warps then convert the slot in place into the MMA operand layouts: latent [64 x 256]
+//     (128-byte swizzle), rope [64 x 32] (64-byte swizzle), zeros for rows outside the request;
+//   * bf16 records (top-k only) are loaded by the agents from global memory straight into those
+//     layouts;
 //   * FP8 records (512 e4m3 codes, one fp32 scale per 128 dims, 64 bf16 rope dims; the 656-byte
-//     layout of the same page's FP8 section) convert exactly: every e4m3 value is a bf16 value.
-//     The scale of each 128-dim group is applied in fp32 where the group meets the other factor:
-//     on the scores, S = s_a S_a + s_b S_b + S_rope with one tensor-memory accumulator per group,
-//     and on P, O_g += (P s_g) V_g for the PV of group g.  P s_g goes to the MMA as a pair of bf16
-//     values, hi = bf16(P s_g) and lo = bf16(P s_g - hi), each with its own MMA: one bf16 rounding
-//     of the scaled P (2^-9) would shift a row that dominates the softmax by that much, next to the
-//     output's own bf16 rounding.  BF16 records take scale 1.
+//     layout of the same page's FP8 section) convert exactly to f16: every e4m3 value is an f16
+//     value, and the MMAs of the latent dims run on f16 operands (this CTA's half of the latent
+//     query is converted from bf16 to f16 in place once per request, exact for |q| in the f16
+//     normal range).  The scale of each 128-dim group is applied in fp32 where the group meets
+//     the other factor: on the scores, S = s_a S_a + s_b S_b + S_rope with one tensor-memory
+//     accumulator per group, and on P, O_g += (P s_g) V_g for the PV of group g, with P s_g
+//     rounded once to f16 (2^-11).  The running max is kept within 2^8 of every P here, so P s_g
+//     stays finite for group scales below 255 (absmax below 114,000).  BF16 records take scale 1
+//     and bf16 operands throughout.
 //
 // Tensor memory (all 512 columns): O_r [0, 256), S_a [256, 320), S_b [320, 384),
-// S_rope [384, 448), P_a [448, 480), P_b [480, 512) (the hi parts; 64 bf16 per lane in 32
-// columns).  Shared memory: Q half (72 KB, TMA), two converted tiles (36 KB each), the lo parts of
-// P s_g (2 x 16 KB, the MMA's K-major layout), exchange buffers.
+// S_rope [384, 448), P_a [448, 480), P_b [480, 512) (64 16-bit values per lane in 32 columns).
+// Shared memory: Q half (72 KB, TMA), three converted tiles (36 KB each), exchange buffers.
 //
-// Warp roles (576 threads): warp 0 Q loads (TMA); warp 1 MMA issuer (+ TMEM owner); warps 2-17:
-// thread = head = TMEM lane, four warps per 32-lane group, 16 positions of a tile each; the 8
-// warps on the owned heads' lanes run the softmax, the other 8 ("agents") forward partial scores,
-// place the peer's P, finish those O rows and load and convert the tiles.  Every wait is bounded:
-// on expiry the kernel records MLA_ERR_TIMEOUT, stops issuing, drains its MMAs, frees TMEM and
-// returns.
+// Warp roles (608 threads): warp 0 Q loads (TMA) and the f16 conversion of Q; warp 1 MMA issuer
+// (+ TMEM owner); warps 2-17: thread = head = TMEM lane, four warps per 32-lane group, 16
+// positions of a tile each; the 8 warps on the owned heads' lanes run the softmax, the other 8
+// ("agents") forward partial scores, convert the tiles, place the peer's P and finish those O
+// rows; warp 18 loads the FP8 tiles.  Every wait is bounded: on expiry the kernel records MLA_ERR_TIMEOUT, stops
+// issuing, drains its MMAs, frees TMEM and returns.
 #include <cuda.h>
+#include <cstring>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -49,12 +54,16 @@ using namespace ptx;
 using namespace dc;
 
 constexpr int kSegCost = 1;           // a segment start costs about one tile (schedule units)
-constexpr int kNC = 2;                 // converted tile slots
+constexpr int kNC = 3;                 // converted tile slots
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
 constexpr int kSlice = kT / 4;         // positions per warp
-constexpr int kThreads = 64 + kSoftmaxThreads;
-constexpr float kLazySlack = 15.0f;    // running max kept until a row max exceeds it by 2^15
-constexpr float kPMax = 32768.0f;      // 2^15: P stays within fp16 range
+constexpr int kProducerWarp = 2 + kSoftmaxThreads / 32;   // warp 18: FP8 tile loads
+constexpr int kThreads = 64 + kSoftmaxThreads + 32;
+constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps
+// the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
+// range of the exchange (bf16 records); 2^8 keeps P s_g within f16 range for s_g < 255 (FP8)
+constexpr float kLazySlackBf16 = 15.0f;
+constexpr float kLazySlackFp8 = 8.0f;
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
 constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
@@ -72,25 +81,28 @@ constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] 
 constexpr int kQRopeBytes = 128 * 64;                  // [128 heads x 32 dims] bf16, SW64
 constexpr int kKvLatChunk = kT * 128;                  // [64 rows x 64 dims], SW128
 constexpr int kConvBytes = 4 * kKvLatChunk + kT * 64;  // latent + rope [64 rows x 32 dims], SW64
-constexpr int kPLoBytes = 128 * kT * 2;                // lo part of P s_g [128 heads x 64 pos], SW128
 constexpr int kXBytes = kOwned * kT * 4;               // peer partial scores of owned heads, fp32
 constexpr int kPInBytes = kOwned * kT * 2;             // peer's P of its owned heads, fp16
 constexpr int kPInMsg = kPInBytes + kOwned * 4;        // + one rescale factor per head
 constexpr int kOffQ = 0;
 constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
 constexpr int kOffConv = kOffQRope + kQRopeBytes;      // 73728
-constexpr int kOffPLo = kOffConv + kNC * kConvBytes;  // 147456: groups a, b
-constexpr int kOffScale = kOffPLo + 2 * kPLoBytes;     // 180224: [kNC][64 rows][2] fp32
-constexpr int kOffMask = kOffScale + kNC * kT * 2 * 4; // 181248: [kNC][2] uint32 valid rows
-constexpr int kOffX = kOffMask + 32;                   // 181280: 2 buffers [16][64][16 B]
-constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 214048: [8][64][16 B] + alpha[64]
-constexpr int kOffLIn = kOffPIn + kPInMsg;             // 222496: 2 x l[64] of the peer's heads
-constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 223008
-constexpr int kNumBars = 2 * kNC + 4 + 2 + 2 + 2 + 2 + 5;
-constexpr int kOffRed = (kOffBar + 8 * kNumBars + 15) & ~15;   // per-head exchange between slices [4][128]
-constexpr int kSmemBytes = kOffRed + 4 * 128 * 4 + 1024;       // + alignment slack
+constexpr int kScaleBytes = kT * 16;                   // per slot: [64 rows][4 groups] fp32
+constexpr int kOffScale = kOffConv + kNC * kConvBytes; // 184320: [kNC][64 rows][4] fp32
+constexpr int kOffMask = kOffScale + kNC * kScaleBytes; // 187392: [kNC][2] uint32 valid rows
+constexpr int kOffX = kOffMask + 32;                   // 187424: 2 buffers [16][64][16 B]
+constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 220192: [8][64][16 B] + alpha[64]
+constexpr int kOffLIn = kOffPIn + kPInMsg;             // 228640: 2 x l[64] of the peer's heads
+constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 229152
+constexpr int kNumBars = 3 * kNC + 4 + 2 + 2 + 2 + 2 + 6;
+constexpr int kOffRed = (kOffBar + 8 * kNumBars + 15) & ~15;   // owned heads' exchange between slices [4][64]
+constexpr int kSmemBytes = kOffRed + 4 * kOwned * 4 + 1024;    // + alignment slack
+// raw FP8 bytes of one tile and CTA: codes [64][256] at the slot's start, rope [64][64 B] at its
+// rope region, scales [64][16 B]
+constexpr uint32_t kRawTileBytes = kT * (kHalfLat + 2 * kHalfRope + 16);   // 21504
 
 constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;     // 73728 per CTA
+static_assert(kSmemBytes + 64 <= 232448, "shared memory above the 227 KB a CTA may use");
 
 struct GatherParams {
     const uint8_t* pool;
@@ -114,13 +126,15 @@ struct GatherParams {
 
 struct Bars {
     uint32_t c_full, c_empty;     // arrays of kNC
+    uint32_t r_full;              // array of kNC: raw FP8 bytes of a tile landed
     uint32_t s_full, s_empty, p_full, p_empty;
     uint32_t x_full, x_free;      // arrays of 2
     uint32_t pin_full, pin_free;
     uint32_t l_full;              // array of 2
-    uint32_t q_full, q_empty, o_full, o_free, mma_drain;
+    uint32_t q_full, q_ready, q_empty, o_full, o_free, mma_drain;
     __device__ __forceinline__ uint32_t cf(int i) const { return c_full + 8 * i; }
     __device__ __forceinline__ uint32_t ce(int i) const { return c_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t rf(int i) const { return r_full + 8 * i; }
     __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
     __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
     __device__ __forceinline__ uint32_t lf(int i) const { return l_full + 8 * i; }
@@ -130,6 +144,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     Bars b;
     b.c_full = a; a += 8 * kNC;
     b.c_empty = a; a += 8 * kNC;
+    b.r_full = a; a += 8 * kNC;
     b.s_full = a; a += 8;
     b.s_empty = a; a += 8;
     b.p_full = a; a += 8;
@@ -140,6 +155,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.pin_free = a; a += 8;
     b.l_full = a; a += 16;
     b.q_full = a; a += 8;
+    b.q_ready = a; a += 8;
     b.q_empty = a; a += 8;
     b.o_full = a; a += 8;
     b.o_free = a; a += 8;
@@ -149,7 +165,11 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_gather_kernel(const __grid_constant__ CUtensorMap tm_qlat,
-                         const __grid_constant__ CUtensorMap tm_qrope, GatherParams p) {
+                         const __grid_constant__ CUtensorMap tm_qrope,
+                         const __grid_constant__ CUtensorMap tm_codes,    // FP8 pool as bytes:
+                         const __grid_constant__ CUtensorMap tm_krope,    // boxes of 64 rows x 256,
+                         const __grid_constant__ CUtensorMap tm_scl,      // 64 and 16 bytes
+                         GatherParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -184,6 +204,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNC; ++i) {
             mbar_init(bars.cf(i), 8);    // one arrive per agent warp once its rows are written
             mbar_init(bars.ce(i), 1);
+            // dense FP8 tiles: the producer's one arrival with the TMA bytes; top-k FP8 tiles: one
+            // arrival per producer lane once its copies land, plus one after the mask is written
+            mbar_init(bars.rf(i), p.topk > 0 ? 33 : 1);
         }
         mbar_init(bars.s_full, 1);
         mbar_init(bars.s_empty, kSoftmaxThreads / 32);   // one arrive per softmax warp
@@ -197,6 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(bars.pin_full, 1);
         mbar_init(bars.pin_free, 8);     // one remote arrive per peer agent warp
         mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_ready, 1);
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.o_full, 1);
         mbar_init(bars.o_free, kSoftmaxThreads / 32);
@@ -215,6 +239,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int n_local = s_n_local;   // tiles of this cluster
     const int start_b = s_start_b, start_t = s_start_t;
 
+    // the record of row `row` of the tile at cursor cj, or null when the row is outside the
+    // request (it then reads as zeros); an out-of-pool page is recorded as MLA_ERR_BOUNDS
+    const int rec_bytes = p.fp8 ? kFp8RecordBytes : kBf16RecordBytes;
+    auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* {
+        int pos = cj.t * kT + row;
+        if (p.topk > 0) {
+            if (pos >= p.topk) return nullptr;
+            pos = p.topk_idx[(size_t)cj.b * p.topk + pos];
+            if (pos < 0) return nullptr;
+        }
+        if (pos >= cj.n) return nullptr;
+        const int page = p.block_table[(size_t)cj.b * p.max_pages + (pos >> 6)];
+        if (page < 0 || page >= p.num_pages) {
+            if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
+            return nullptr;
+        }
+        return p.pool + ((size_t)page * kPage + (pos & (kPage - 1))) * rec_bytes;
+    };
+
     if (n_local == 0 && warp >= 2) {
         // an empty range: its partial slots must not contribute to any merge
         const int h = tid - 64;
@@ -225,42 +268,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ Q loads (TMA)
+        // ------------------------------------------------------------------ Q loads (TMA) + f16
+        // FP8 records: once a request's Q half has landed, the whole warp converts its latent
+        // part from bf16 to f16 in place (the swizzle permutes whole 16-byte chunks, so each
+        // chunk keeps its place), then releases it to the MMA issuer.
+        Cursor cu;
         if (lane == 0 && n_local > 0) {
             tma_prefetch_desc(&tm_qlat);
             tma_prefetch_desc(&tm_qrope);
-            Cursor cu;
-            cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-            int seg = 0;
-            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-                if (s_abort) break;
-                if (!cu.first()) continue;
-                if (seg > 0 && !mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit)) {
-                    fail(p.ctl, &s_abort, 1);
-                    break;
-                }
+        }
+        cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+        int seg = 0;
+        for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+            if (!cu.first()) continue;
+            bool ok = !s_abort;
+            if (ok && seg > 0) ok = mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) fail(p.ctl, &s_abort, 1);
+                break;
+            }
+            if (lane == 0) {
                 const int qrow = cu.b * kHeads;
                 mbar_arrive_expect_tx(bars.q_full, kQBytes);
                 for (int k = 0; k < 4; ++k)
                     tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
                                 (int)r * kHalfLat + 64 * k, qrow);
                 tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
-                ++seg;
             }
-            // drain: the last Q load lands before this CTA may exit
-            if (seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
+            ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full, seg & 1, wait_limit));
+            if (!ok) {
+                if (lane == 0) fail(p.ctl, &s_abort, 19);
+                break;
+            }
+            if (p.fp8) {
+#pragma unroll 8
+                for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
+                    uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
+                    const uint4 v = *q;
+                    *q = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                    bf16x2_to_f16x2(v.w));
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.q_ready);
+            ++seg;
         }
+        // drain: the last Q load lands before this CTA may exit
+        if (lane == 0 && seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         // The whole warp runs this loop so that its operands stay warp-uniform; one elected lane
         // issues each MMA and commit.  QK of a tile: 8 MMAs per latent group into that group's
-        // accumulator, 2 rope MMAs; PV: per group, 4 pairs of MMAs of 128x128x16, the hi and lo
-        // parts of P times the group's scales.  One score set and one P set in tensor memory: QK of tile i + 1 follows the
-        // softmax's reads of tile i's scores, P of tile i + 1 follows PV of tile i.
+        // accumulator (f16 operands for FP8 records), 2 rope MMAs (bf16); PV: per group, 4 MMAs
+        // of 128x128x16 with P times the group's scales from tensor memory.  One score set and
+        // one P set in tensor memory: QK of tile i + 1 follows the softmax's reads of tile i's
+        // scores, P of tile i + 1 follows PV of tile i.
         if (n_local > 0) {
-            constexpr uint32_t id_qk = idesc_bf16(128, kT, 0, 0);
-            constexpr uint32_t id_pv = idesc_bf16(128, 128, 0, 1);
+            const uint32_t id_qk = p.fp8 ? idesc_f16(128, kT, 0, 0) : idesc_bf16(128, kT, 0, 0);
+            constexpr uint32_t id_qr = idesc_bf16(128, kT, 0, 0);
+            const uint32_t id_pv = p.fp8 ? idesc_f16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 1);
             const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
             const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
             const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
@@ -279,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int s = iq % kNC;
                     const bool ready = __shfl_sync(
                         0xffffffffu,
-                        (!cq.first() || mbar_test(bars.q_full, seg_q & 1)) &&
+                        (!cq.first() || mbar_test(bars.q_ready, seg_q & 1)) &&
                             mbar_test(bars.cf(s), (iq / kNC) & 1) && mbar_test(bars.s_empty, (iq & 1) ^ 1),
                         0);
                     if (ready) {
@@ -298,7 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             for (int kk = 0; kk < 2; ++kk)
                                 mma_bf16_ss(tmem + kTmemSr, rope_hi | (qr_lo + kk * 2),
                                             rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
-                                            id_qk, kk != 0 ? 1u : 0u);
+                                            id_qr, kk != 0 ? 1u : 0u);
                             mma_commit(bars.s_full);
                             if (cq.last()) mma_commit(bars.q_empty);
                         }
@@ -326,7 +395,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 polls = 0;
                 tc_fence_after();
                 const uint32_t v = ((sbase + kOffConv + (ip % kNC) * kConvBytes) >> 4) & 0x3FFF;
-                const uint32_t plo = ((sbase + kOffPLo) >> 4) & 0x3FFF;
                 if (elect_one()) {
 #pragma unroll
                     for (int g = 0; g < 2; ++g)
@@ -335,8 +403,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
                             mma_bf16_ts(tmem + kTmemO + 128 * g, tmem + (g == 0 ? kTmemPa : kTmemPb) + 8 * kk, vd,
                                         id_pv, (!seg_first || kk > 0) ? 1u : 0u);
-                            mma_bf16_ss(tmem + kTmemO + 128 * g,
-                                        lat_hi | (plo + lat_lo + ((g * kPLoBytes + kk * 32) >> 4)), vd, id_pv, 1u);
                         }
                     mma_commit(bars.p_empty);
                     mma_commit(bars.ce(ip % kNC));
@@ -346,6 +412,130 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (cp.last()) ++seg_p;
                 cp.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
                 ++ip;
+            }
+        }
+        __syncwarp();
+    } else if (warp == kProducerWarp) {
+        // ------------------------------------------------------------------ FP8 tile loads
+        // Tile j's raw bytes into conversion slot j % kNC once PV of tile j - kNC has released it,
+        // with the mask of valid rows (written before the arrival the agents wait on).  A dense
+        // tile is one page: three TMA boxes of its 64 rows (rows past the request's end are
+        // loaded and then zeroed by the agents).  A top-k tile: each lane copies its two rows with
+        // 16-byte cp.async (21 pieces per row: 16 of codes, the scales, 4 of rope) and arrives
+        // once they have landed.  Row lookups run one tile ahead, so that their latency overlaps
+        // the wait for the slot, and the rows of tile j + kPfAhead are prefetched into L2.
+        if (p.fp8 && n_local > 0) {
+            constexpr int kPfAhead = 3;
+            const bool dense = p.topk == 0;
+            if (dense && lane == 0) {
+                tma_prefetch_desc(&tm_codes);
+                tma_prefetch_desc(&tm_krope);
+                tma_prefetch_desc(&tm_scl);
+            }
+            Cursor cj, cpf;
+            cj.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+            cpf = cj;
+            int j_pf = 0;
+            const uint8_t* pf0 = nullptr;
+            const uint8_t* pf1 = nullptr;
+            // L2 prefetch of the rows looked up in the call before, then the lookup of tile j_pf
+            auto prefetch_step = [&]() {
+                if (dense) {
+                    if (pf0) {
+                        const int y = (int)((pf0 - p.pool) / kFp8RecordBytes);
+                        tma_prefetch_l2_2d(&tm_codes, kHalfLat * (int)r, y);
+                        tma_prefetch_l2_2d(&tm_krope, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
+                        tma_prefetch_l2_2d(&tm_scl, kFp8ScaleOff, y);
+                    }
+                } else {
+                    // the lines of the row's codes half and of its scales and rope
+                    const uint8_t* pq[2] = {pf0, pf1};
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        if (pq[q]) {
+                            prefetch_line_l2(pq[q] + kHalfLat * (int)r);
+                            prefetch_line_l2(pq[q] + kHalfLat * (int)r + 128);
+                            prefetch_line_l2(pq[q] + kFp8ScaleOff);
+                            prefetch_line_l2(pq[q] + kFp8RecordBytes - 16);
+                        }
+                }
+                pf0 = pf1 = nullptr;
+                if (j_pf < n_local) {
+                    if (!dense || lane == 0) pf0 = row_record(cpf, lane);
+                    if (!dense) pf1 = row_record(cpf, lane + 32);
+                    ++j_pf;
+                    cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                }
+            };
+            for (int k = 0; k < kPfAhead; ++k) prefetch_step();
+            const uint8_t* rec0 = row_record(cj, lane);
+            const uint8_t* rec1 = row_record(cj, lane + 32);
+            int issued = 0;
+            for (int j = 0; j < n_local; ++j) {
+                prefetch_step();
+                const int slot = j % kNC;
+                const uint32_t m0 = __ballot_sync(0xffffffffu, rec0 != nullptr);
+                const uint32_t m1 = __ballot_sync(0xffffffffu, rec1 != nullptr);
+                bool ok = !s_abort;
+                if (ok && j >= kNC) ok = mbar_wait(bars.ce(slot), ((j / kNC) - 1) & 1, wait_limit);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) fail(p.ctl, &s_abort, 20);
+                    break;
+                }
+                const uint32_t dst = sbase + kOffConv + slot * kConvBytes;
+                const uint32_t dst_rope = dst + 4 * kKvLatChunk;
+                const uint32_t dst_scl = sbase + kOffScale + slot * kScaleBytes;
+                const uint32_t bar = bars.rf(slot);
+                if (lane == 0) {
+                    uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * slot;
+                    mk[0] = m0;
+                    mk[1] = m1;
+                    if (dense) {
+                        if (m0 & 1u) {   // row 0 of a dense tile is visible unless its page is not
+                            const int y = (int)((rec0 - p.pool) / kFp8RecordBytes);
+                            mbar_arrive_expect_tx(bar, kRawTileBytes);
+                            tma_load_2d(dst, &tm_codes, bar, kHalfLat * (int)r, y);
+                            tma_load_2d(dst_rope, &tm_krope, bar, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
+                            tma_load_2d(dst_scl, &tm_scl, bar, kFp8ScaleOff, y);
+                        } else {
+                            mbar_arrive(bar);
+                        }
+                    } else {
+                        mbar_arrive(bar);
+                    }
+                }
+                if (!dense) {
+                    auto copy_row = [&](const uint8_t* rec, int row) {
+                        if (!rec) return;
+                        const uint8_t* cs = rec + kHalfLat * (int)r;
+#pragma unroll
+                        for (int k = 0; k < kHalfLat / 16; ++k) cp_async16(dst + row * kHalfLat + 16 * k, cs + 16 * k);
+                        cp_async16(dst_scl + row * 16, rec + kFp8ScaleOff);
+                        const uint8_t* rs = rec + kFp8RopeOff + 2 * kHalfRope * (int)r;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) cp_async16(dst_rope + row * 64 + 16 * k, rs + 16 * k);
+                    };
+                    copy_row(rec0, lane);
+                    copy_row(rec1, lane + 32);
+                    cp_async_arrive_noinc(bar);
+                }
+                __syncwarp();
+                ++issued;
+                cj.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                rec0 = rec1 = nullptr;
+                if (j + 1 < n_local) {
+                    rec0 = row_record(cj, lane);
+                    rec1 = row_record(cj, lane + 32);
+                }
+            }
+            // drain: the copies of the last tiles (one per slot) land before this CTA may exit
+            if (dense) {
+                if (lane == 0)
+                    for (int j = issued - 1; j >= 0 && j >= issued - kNC; --j)
+                        mbar_wait(bars.rf(j % kNC), (j / kNC) & 1, kDrainLimit);
+            } else {
+                cp_async_wait_all();
             }
         }
         __syncwarp();
@@ -366,8 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool owner = (lg >> 1) == (int)r;
         const int hh = h & (kOwned - 1);   // index among the owning CTA's heads
         const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-        float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][128 heads]
-        const int rec_bytes = p.fp8 ? kFp8RecordBytes : kBf16RecordBytes;
+        float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][64 owned heads]
 
         auto wwait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
             bool ok = !s_abort && mbar_wait(bar, parity, wait_limit);
@@ -376,10 +565,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             return ok;
         };
 
-        // group scales of the warp's 16 positions of tile i: float4 k holds (s_a, s_b) of
-        // positions 16 ts + 2k and 16 ts + 2k + 1
-        auto scales_of = [&](int i) -> const float4* {
-            return reinterpret_cast<const float4*>(sm + kOffScale) + (i % kNC) * (kT / 2) + 8 * ts;
+        // group scales of the warp's 16 positions of tile i: element 2 t is (s_a, s_b) of
+        // position 16 ts + t (each row holds the scales of all four groups)
+        auto scales_of = [&](int i) -> const float2* {
+            return reinterpret_cast<const float2*>(sm + kOffScale + (i % kNC) * kScaleBytes) + 32 * ts + (int)r;
         };
 
         // this CTA's partial scores of tile i for the warp's 16 positions: s_a S_a + s_b S_b + S_rope
@@ -387,7 +576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto load_s = [&](int i, float (&v)[16]) -> bool {
             if (!wwait(bars.cf(i % kNC), (i / kNC) & 1, 18)) return false;
             if (!wwait(bars.s_full, i & 1, 7)) return false;
-            const float4* sc = scales_of(i);
+            const float2* sc = scales_of(i);
             tc_fence_after();
             {
                 uint32_t a[16], b[16];
@@ -395,10 +584,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_ld16(tmem + lane_off + kTmemSb + kSlice * ts, b);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float4 q = sc[k];
-                    v[2 * k] = fmaf(q.x, __uint_as_float(a[2 * k]), q.y * __uint_as_float(b[2 * k]));
-                    v[2 * k + 1] = fmaf(q.z, __uint_as_float(a[2 * k + 1]), q.w * __uint_as_float(b[2 * k + 1]));
+                for (int t = 0; t < 16; ++t) {
+                    const float2 q = sc[2 * t];
+                    v[t] = fmaf(q.x, __uint_as_float(a[t]), q.y * __uint_as_float(b[t]));
                 }
             }
             {
@@ -431,39 +619,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_st();
         };
 
-        // the warp's 16 P values of tile i (fp16 pairs, so that the one rounding that matters
-        // is the bf16 one of P s_g) times each group's scales into tensor memory, once PV of
-        // tile i - 1 has completed, then P ready for the MMA
+        // the warp's 16 P values of tile i (fp16 pairs from the softmax) times each group's
+        // scales into tensor memory, once PV of tile i - 1 has completed, then P ready for the
+        // MMA: f16 (P s_g) for FP8 records, bf16 P for bf16 records (scale 1)
         auto store_p = [&](int i, const uint32_t (&pk)[8]) {
             if (i >= 1 && !wwait(bars.p_empty, (i - 1) & 1, 11)) return;
-            const float4* sc = scales_of(i);
-            uint32_t pa[8], pb[8], la[8], lb[8];
+            uint32_t pa[8], pb[8];
+            if (p.fp8) {
+                const float2* sc = scales_of(i);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float4 q = sc[k];
-                __half2 h2;
-                *reinterpret_cast<uint32_t*>(&h2) = pk[k];
-                const float2 pf = __half22float2(h2);
-                const float xa0 = pf.x * q.x, xa1 = pf.y * q.z, xb0 = pf.x * q.y, xb1 = pf.y * q.w;
-                pa[k] = pack_bf16x2(xa0, xa1);
-                pb[k] = pack_bf16x2(xb0, xb1);
-                la[k] = pack_bf16x2(xa0 - __uint_as_float(pa[k] << 16), xa1 - __uint_as_float(pa[k] & 0xFFFF0000u));
-                lb[k] = pack_bf16x2(xb0 - __uint_as_float(pb[k] << 16), xb1 - __uint_as_float(pb[k] & 0xFFFF0000u));
+                for (int k = 0; k < 8; ++k) {
+                    const float2 q0 = sc[4 * k], q1 = sc[4 * k + 2];
+                    __half2 h2;
+                    *reinterpret_cast<uint32_t*>(&h2) = pk[k];
+                    const float2 pf = __half22float2(h2);
+                    pa[k] = pack_f16x2(pf.x * q0.x, pf.y * q1.x);
+                    pb[k] = pack_f16x2(pf.x * q0.y, pf.y * q1.y);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    __half2 h2;
+                    *reinterpret_cast<uint32_t*>(&h2) = pk[k];
+                    const float2 pf = __half22float2(h2);
+                    pa[k] = pb[k] = pack_bf16x2(pf.x, pf.y);
+                }
             }
             tmem_st8(tmem + lane_off + kTmemPa + 8 * ts, pa);
             tmem_st8(tmem + lane_off + kTmemPb + 8 * ts, pb);
-            // lo parts: row h, 16-byte chunks 2 ts and 2 ts + 1 of the 128-byte row (chunk c at
-            // c ^ (h % 8), 128-byte swizzle)
-            {
-                uint8_t* ra = sm + kOffPLo + h * 128;
-                uint8_t* rb = ra + kPLoBytes;
-                const int c0 = ((2 * ts) ^ (h & 7)) << 4, c1 = ((2 * ts + 1) ^ (h & 7)) << 4;
-                st_shared_v4(ra + c0, la[0], la[1], la[2], la[3]);
-                st_shared_v4(ra + c1, la[4], la[5], la[6], la[7]);
-                st_shared_v4(rb + c0, lb[0], lb[1], lb[2], lb[3]);
-                st_shared_v4(rb + c1, lb[4], lb[5], lb[6], lb[7]);
-                fence_proxy_async_smem();
-            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -510,97 +693,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int seg = 0;
         bool cut_front = false;
 
-        if (!owner) {
-            // ------------------------------------------------------------ agents
-            const uint32_t x_remote = mapa(sbase + kOffX, peer);
-            const uint32_t xfull_remote = mapa(bars.x_full, peer);
-            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
-            const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
-            const int at = ((lg & 1) * 4 + ts) * 32 + lane;   // 0 .. 255 over the agents
-
-            // the record of row `row` of the tile at cursor cj, or null when the row is outside
-            // the request (it then reads as zeros)
-            auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* {
-                int pos = cj.t * kT + row;
-                if (p.topk > 0) {
-                    if (pos >= p.topk) return nullptr;
-                    pos = p.topk_idx[(size_t)cj.b * p.topk + pos];
-                    if (pos < 0) return nullptr;
+        // Tile preparation (called by the agents): thread `at` of the 256 agent threads.
+        const int at = ((lg & 1) * 4 + ts) * 32 + lane;
+        // Tile j (cursor cj) into conversion slot j % kNC: this CTA's half of every row in the
+        // MMA layouts, zeros for rows outside the request.  FP8 records: the producer warp has
+        // put the raw bytes into the slot (codes [64][256] at its start, rope [64][64 B] in its
+        // rope region, scales [64][16 B], the mask of valid rows); each agent thread reads its
+        // 16-byte pieces, all agents meet, and each writes its pieces converted.  bf16 records:
+        // the rows are loaded from global memory once PV of tile j - kNC has freed the slot.
+        auto prepare = [&](int j, const Cursor& cj) {
+            const int slot = j % kNC;
+            uint8_t* lat = sm + kOffConv + slot * kConvBytes;
+            uint8_t* rope = lat + 4 * kKvLatChunk;
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            if (p.fp8) {
+                const bool ok = wwait(bars.rf(slot), (j / kNC) & 1, 17);
+                const uint32_t* mk = reinterpret_cast<const uint32_t*>(sm + kOffMask) + 2 * slot;
+                const uint32_t mk0 = mk[0], mk1 = mk[1];
+                auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
+                uint4 raw[4], rraw = zero;
+                if (ok) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) raw[k] = *reinterpret_cast<const uint4*>(lat + (at + 256 * k) * 16);
+                    rraw = *reinterpret_cast<const uint4*>(rope + at * 16);
                 }
-                if (pos >= cj.n) return nullptr;
-                const int page = p.block_table[(size_t)cj.b * p.max_pages + (pos >> 6)];
-                if (page < 0 || page >= p.num_pages) {
-                    if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
-                    return nullptr;
-                }
-                return p.pool + ((size_t)page * kPage + (pos & (kPage - 1))) * rec_bytes;
-            };
-
-            // Tile j (cursor cj) into conversion slot j % kNC once PV of tile j - kNC is done:
-            // this CTA's half of every row, converted to the MMA layouts, its group scales and the
-            // mask of valid rows.
-            auto prepare = [&](int j, const Cursor& cj) {
-                const int slot = j % kNC;
-                uint8_t* lat = sm + kOffConv + slot * kConvBytes;
-                uint8_t* rope = lat + 4 * kKvLatChunk;
-                const uint4 zero = make_uint4(0, 0, 0, 0);
-                // the row loads go out first, so that their latency overlaps the wait for the slot
-                const int rope_off = (p.fp8 ? kFp8RopeOff : 2 * kDc) + 2 * kHalfRope * (int)r;
-                const uint8_t* rrec = row_record(cj, at >> 2);
-                const uint4 rraw = rrec ? __ldg(reinterpret_cast<const uint4*>(rrec + rope_off + 16 * (at & 3))) : zero;
-                const uint8_t* srec = at < kT ? row_record(cj, at) : nullptr;
-                float2 s2 = make_float2(1.f, 1.f);
-                if (p.fp8 && at < kT)
-                    s2 = srec ? __ldg(reinterpret_cast<const float2*>(srec + kFp8ScaleOff + 8 * (int)r)) : make_float2(0.f, 0.f);
-                if (p.fp8) {
-                    // 64 rows x 16 chunks of 16 codes; this thread converts chunks at + 256 k
-                    uint4 raw[4];
+                named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
+                if (ok) {
+                    // 64 rows x 16 chunks of 16 codes; piece at + 256 k is chunk ch of row `row`
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int e = at + 256 * k, row = e >> 4, ch = e & 15;
-                        const uint8_t* rec = row_record(cj, row);
-                        raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + kHalfLat * (int)r + 16 * ch)) : zero;
-                    }
-                    if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = at + 256 * k, row = e >> 4, ch = e & 15;
-                        uint32_t o[8];
-                        e4m3x16_to_bf16(raw[k], o);
-                        // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte parts
-                        // 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
+                        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if (valid(row)) e4m3x16_to_f16(raw[k], o);
+                        // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte
+                        // parts 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
                         uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
                         const int s0 = 2 * (ch & 3);
                         st_shared_v4(dst + ((s0 ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
                         st_shared_v4(dst + (((s0 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
                     }
-                } else {
-                    // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k
-                    // (the first half loaded before the wait)
-                    uint4 raw[4];
+                    // rope: 64 rows x 4 chunks of 8 dims, 64-byte swizzle
+                    const int row = at >> 2, c4 = at & 3;
+                    if (!valid(row)) rraw = zero;
+                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
+                    // scales of rows outside the request: zero (their P is zero)
+                    if (at < kT && !valid(at))
+                        *reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + at * 16) = zero;
+                }
+            } else {
+                // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k
+                // (the first half loaded before the wait)
+                const int rope_off = 2 * kDc + 2 * kHalfRope * (int)r;
+                const uint8_t* rrec = row_record(cj, at >> 2);
+                const uint4 rraw = rrec ? __ldg(reinterpret_cast<const uint4*>(rrec + rope_off + 16 * (at & 3))) : zero;
+                const uint8_t* srec = at < kT ? row_record(cj, at) : nullptr;
+                uint4 raw[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = at + 256 * k, row = e >> 5, ch = e & 31;
-                        const uint8_t* rec = row_record(cj, row);
-                        raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
-                    }
-                    if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
+                for (int k = 0; k < 4; ++k) {
+                    const int e = at + 256 * k, row = e >> 5, ch = e & 31;
+                    const uint8_t* rec = row_record(cj, row);
+                    raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
+                }
+                if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        if (half == 1) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const int e = at + 256 * (4 + k), row = e >> 5, ch = e & 31;
-                                const uint8_t* rec = row_record(cj, row);
-                                raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
-                            }
-                        }
+                for (int half = 0; half < 2; ++half) {
+                    if (half == 1) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const int e = at + 256 * (4 * half + k), row = e >> 5, ch = e & 31;
-                            st_shared_v4(lat + (ch >> 3) * kKvLatChunk + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
-                                         raw[k].x, raw[k].y, raw[k].z, raw[k].w);
+                            const int e = at + 256 * (4 + k), row = e >> 5, ch = e & 31;
+                            const uint8_t* rec = row_record(cj, row);
+                            raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
                         }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = at + 256 * (4 * half + k), row = e >> 5, ch = e & 31;
+                        st_shared_v4(lat + (ch >> 3) * kKvLatChunk + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
+                                     raw[k].x, raw[k].y, raw[k].z, raw[k].w);
                     }
                 }
                 {
@@ -609,15 +778,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
                 }
                 if (at < kT) {
-                    // the row's two group scales (1 for bf16 records) and the valid-row mask
-                    reinterpret_cast<float2*>(sm + kOffScale)[slot * kT + at] = s2;
+                    // the row's group scales (1 for bf16 records) and the valid-row mask
+                    reinterpret_cast<float2*>(sm + kOffScale + slot * kScaleBytes)[2 * at + (int)r] = make_float2(1.f, 1.f);
                     const uint32_t m = __ballot_sync(0xffffffffu, srec != nullptr);
                     if (lane == 0) reinterpret_cast<uint32_t*>(sm + kOffMask)[2 * slot + (at >> 5)] = m;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.cf(slot));
-            };
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.cf(slot));
+        };
+
+        Cursor cpr = cu;   // next tile to prepare
+        int i_pr = 0;
+        auto prepare_until = [&](int upto) {
+            for (; i_pr < upto && i_pr < n_local; ++i_pr, cpr.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) prepare(i_pr, cpr);
+        };
+        // L2 prefetch of the rows of tile i + 5 during iteration i (tile i + 2 is prepared in
+        // iteration i, so prefetches run three iterations ahead): thread `at` covers part
+        // at / 64 (latent bytes, rope, scales) of row at % 64.  Its address comes from the
+        // index loads of the iteration before, so their latency overlaps an iteration.
+        const int pf_row = at & (kT - 1), pf_part = at >> 6;
+        const uint32_t pf_bytes = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
+        const int pf_off = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) * (int)r
+                                        : (pf_part == 1 ? (p.fp8 ? kFp8RopeOff : 2 * kDc) + 64 * (int)r : kFp8ScaleOff);
+        const bool pf_on = !p.fp8 && pf_part < 2;   // FP8 tiles: the producer warp prefetches
+        Cursor cpf = cu;   // the tile whose prefetch address is computed next (tiles 0, 1 are
+        int i_pf = 0;      // prepared at once)
+        for (; i_pf < 2 && i_pf < n_local; ++i_pf) cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+        const uint8_t* pf_rec = nullptr;
+        auto prefetch_step = [&]() {
+            if (pf_rec) prefetch_l2(pf_rec + pf_off, pf_bytes);
+            pf_rec = nullptr;
+            if (i_pf < n_local) {
+                if (pf_on) pf_rec = row_record(cpf, pf_row);
+                ++i_pf;
+                cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+            }
+        };
+        if (!owner) {
+            // ------------------------------------------------------------ agents
+            const uint32_t x_remote = mapa(sbase + kOffX, peer);
+            const uint32_t xfull_remote = mapa(bars.x_full, peer);
+            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
+            const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
 
             // forward this CTA's partial scores of tile i (the peer's heads) to the peer
             auto forward = [&](int i) {
@@ -632,38 +836,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 __float_as_uint(v[4 * g + 2]), __float_as_uint(v[4 * g + 3]));
             };
 
-            Cursor cpr = cu;   // next tile to prepare
-            int i_pr = 0;
-            auto prepare_until = [&](int upto) {
-                for (; i_pr < upto && i_pr < n_local; ++i_pr, cpr.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) prepare(i_pr, cpr);
-            };
-            // L2 prefetch of the rows of tile i + 5 during iteration i (tile i + 2 is prepared in
-            // iteration i, so prefetches run three iterations ahead): thread `at` covers part
-            // at / 64 (latent bytes, rope, scales) of row at % 64.  Its address comes from the
-            // index loads of the iteration before, so their latency overlaps an iteration.
-            const int pf_row = at & (kT - 1), pf_part = at >> 6;
-            const uint32_t pf_bytes = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
-            const int pf_off = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) * (int)r
-                                            : (pf_part == 1 ? (p.fp8 ? kFp8RopeOff : 2 * kDc) + 64 * (int)r : kFp8ScaleOff);
-            const bool pf_on = pf_part < (p.fp8 ? 3 : 2);
-            Cursor cpf = cu;   // the tile whose prefetch address is computed next (tiles 0, 1 are
-            int i_pf = 0;      // prepared at once)
-            for (; i_pf < 2 && i_pf < n_local; ++i_pf) cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-            const uint8_t* pf_rec = nullptr;
-            auto prefetch_step = [&]() {
-                if (pf_rec) prefetch_l2(pf_rec + pf_off, pf_bytes);
-                pf_rec = nullptr;
-                if (i_pf < n_local) {
-                    if (pf_on) pf_rec = row_record(cpf, pf_row);
-                    ++i_pf;
-                    cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-            };
             for (int k = 0; k < 4; ++k) prefetch_step();   // tiles 2, 3, 4 prefetched, 5 addressed
             prepare_until(2);
             if (n_local > 0) forward(0);
+            // Iteration i: the peer's P of tile i into tensor memory (PV of tile i can then go),
+            // then this CTA's scores of tile i + 1 to the peer and tile i + 2 converted.
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-                if (i + 1 < n_local) forward(i + 1);
                 const bool first = cu.first();
                 if (first) cut_front = cu.t > 0;
                 // the peer's P of its heads for tile i, and its rescale factors
@@ -684,8 +862,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0 && ok) mbar_arrive_remote_relaxed(pinfree_remote);
                 if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha);
                 store_p(i, pk);
-                prepare_until(i + 3);
-                prefetch_step();
                 if (cu.last()) {
                     const bool partial = cut_front || cu.t < cu.nt - 1;
                     // the row sums of these heads, sent by the peer's owners
@@ -695,6 +871,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     epilogue_rows(seg, cu, partial, l_row);
                     ++seg;
                 }
+                if (i + 1 < n_local) forward(i + 1);
+                prepare_until(i + 3);
+                prefetch_step();
             }
         } else {
             // ------------------------------------------------------------ owners
@@ -705,6 +884,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lfull_remote = mapa(bars.l_full, peer);
             const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
+            const float slack = p.fp8 ? kLazySlackFp8 : kLazySlackBf16;
+            const float p_max = exp2f(slack);
             float m_used = -INFINITY, l_part = 0.f;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
                 const int xb = i & 1;
@@ -736,8 +917,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote + 8 * xb);
                 // P = 2^(x - m) with the running max m (rows outside the request give 0).  m is
-                // kept while every P of a row stays at most 2^15: a thread whose 16 P sum past
-                // 2^15 (or not to a finite value) votes for the rare path, as does every segment
+                // kept while every P of a row stays at most 2^slack: a thread whose 16 P sum past
+                // 2^slack (or not to a finite value) votes for the rare path, as does every segment
                 // start and a row with no visible position yet.  There the exact row max over the
                 // four slices raises m where it exceeds m by more than the slack, O is rescaled
                 // here and, through alpha sent with P, in the peer, and P is computed again.
@@ -757,16 +938,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 };
                 exp_tile();
-                const bool need = first || m_used == -INFINITY || !(psum <= kPMax);
+                const bool need = first || m_used == -INFINITY || !(psum <= p_max);
                 if (bar_red_or(bar_vote, 128, need)) {
                     float mx = -INFINITY;
 #pragma unroll
                     for (int t = 0; t < 16; ++t)
                         if ((vmask >> t) & 1) mx = fmaxf(mx, x[t]);
-                    red[ts * 128 + h] = mx;
+                    red[ts * kOwned + hh] = mx;
                     named_bar_sync(bar_sync, 128);
-                    const float tmax = fmaxf(fmaxf(red[h], red[128 + h]), fmaxf(red[256 + h], red[384 + h]));
-                    const bool grow = first || tmax > m_used + kLazySlack;
+                    const float tmax = fmaxf(fmaxf(red[hh], red[kOwned + hh]), fmaxf(red[2 * kOwned + hh], red[3 * kOwned + hh]));
+                    const bool grow = first || tmax > m_used + slack;
                     const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
                     if (!first) {
                         alpha = grow ? ex2(m_used - m_new) : 1.0f;
@@ -793,9 +974,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (cu.last()) {
                     // ------------------------------------------------------ segment epilogue
                     const bool partial = cut_front || cu.t < cu.nt - 1;
-                    red[ts * 128 + h] = l_part;
+                    red[ts * kOwned + hh] = l_part;
                     named_bar_sync(bar_sync, 128);
-                    const float l_row = (red[h] + red[128 + h]) + (red[256 + h] + red[384 + h]);
+                    const float l_row = (red[hh] + red[kOwned + hh]) + (red[2 * kOwned + hh] + red[3 * kOwned + hh]);
                     named_bar_sync(bar_sync, 128);
                     // the row sums of these heads to the peer, which finishes its O rows of them
                     if (ts == 0 && !s_abort)
@@ -861,11 +1042,26 @@ cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cu
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    CUtensorMap tm_qlat, tm_qrope;
+    CUtensorMap tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl;
     const uint64_t qrows = (uint64_t)a.B * kHeads;
     if (!encode_2d(&tm_qlat, a.q_lat, kDc, qrows, kDc * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tm_qrope, a.q_rope, kDr, qrows, kDr * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
+    std::memset(&tm_codes, 0, sizeof(tm_codes));
+    std::memset(&tm_krope, 0, sizeof(tm_krope));
+    std::memset(&tm_scl, 0, sizeof(tm_scl));
+    if (a.fmt == MLA_KV_FP8_MIXED && (a.topk_idx == nullptr || a.topk <= 0)) {
+        // the pool as rows of 656 bytes; a box is 64 rows (one page) of a record's byte range
+        const uint64_t rows = (uint64_t)a.num_pages * kPage;
+        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (!encode_2d(&tm_codes, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, kHalfLat, kT,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, u8) ||
+            !encode_2d(&tm_krope, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, 2 * kHalfRope, kT,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, u8) ||
+            !encode_2d(&tm_scl, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, 16, kT,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, u8))
+            return cudaErrorInvalidValue;
+    }
     const int C = plan.splits;
     float* o_part = static_cast<float*>(a.workspace);
     float* lse_part = o_part + (size_t)2 * C * kHeads * kDc;
@@ -888,7 +1084,7 @@ cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cu
     p.B = a.B;
     p.fp8 = a.fmt == MLA_KV_FP8_MIXED ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    decode_gather_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, p);
+    decode_gather_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st);
