@@ -37,27 +37,41 @@ METRIC = "MLA decode KV GB/s, TFLOP/s and % of GB300 roofline; decode tokens/s a
 UNIT = "KV GB/s"
 L2_BYTES = 126 * 2 ** 20
 
-# DRAM bytes (read + write) per decode-kernel launch from an ncu capture, keyed by the sha256 of
-# the decode kernel sources it was taken on and the workload; any change to those sources makes the
-# entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
-# profiles/decode_gather_fp8_batch.md.
-NCU_TRAFFIC = {
-    ("ed6f880eca010d0c", "paged_batch"): 178_216_192,
-    ("ed6f880eca010d0c", "fp8_batch"): 1_414_786_472,
+# DRAM bytes (read + write) per launch of each workload's dominant kernel from an ncu capture,
+# keyed by the sha256 of the sources that kernel is built from and the workload; any change to
+# those sources makes the entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
+# profiles/decode_gather_fp8_batch.md, profiles/indexer_score_indexer_topk.md.
+_HEADERS = ["mla_latent_kv_decode_gb300/csrc/decode_common.cuh",
+            "mla_latent_kv_decode_gb300/csrc/mla_internal.cuh",
+            "mla_latent_kv_decode_gb300/csrc/tc_ptx.cuh",
+            "include/mla.h"]
+KERNEL_SOURCES = {
+    "decode_tc": ["mla_latent_kv_decode_gb300/csrc/decode_tc.cu"] + _HEADERS,
+    "decode_gather": ["mla_latent_kv_decode_gb300/csrc/decode_gather.cu"] + _HEADERS,
+    "indexer_score": ["mla_latent_kv_decode_gb300/csrc/indexer.cu"] + _HEADERS,
 }
-DECODE_SOURCES = ["mla_latent_kv_decode_gb300/csrc/decode_tc.cu",
-                  "mla_latent_kv_decode_gb300/csrc/decode_gather.cu",
-                  "mla_latent_kv_decode_gb300/csrc/decode_common.cuh",
-                  "mla_latent_kv_decode_gb300/csrc/mla_internal.cuh",
-                  "mla_latent_kv_decode_gb300/csrc/tc_ptx.cuh"]
+WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_context": "decode_tc",
+                   "fp8_batch": "decode_gather", "topk_sparse": "decode_gather",
+                   "indexer_topk": "indexer_score"}
+NCU_TRAFFIC = {
+    ("4e0d25fe1eceffc4", "paged_batch"): 178_197_504,
+    ("4e0d25fe1eceffc4", "long_context"): 155_823_104,
+    ("a98ff32544de16c1", "fp8_batch"): 1_417_405_440,
+    ("a98ff32544de16c1", "topk_sparse"): 123_346_688,
+    ("97765f997c7c0cb6", "indexer_topk"): 1_144_415_232,
+}
 
 
-def _sources_hash() -> str:
+def _sources_hash(workload: str) -> str:
     h = hashlib.sha256()
-    for p in DECODE_SOURCES:
+    for p in KERNEL_SOURCES[WORKLOAD_KERNEL[workload]]:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def _traffic(workload: str):
+    return NCU_TRAFFIC.get((_sources_hash(workload), workload))
 
 
 def _peaks():
@@ -342,7 +356,7 @@ def run_ours(args):
     peaks = _peaks()
     dec_s = dec_ms / 1e3
     achieved = alg_bytes / dec_s / 1e9
-    traffic = NCU_TRAFFIC.get((_sources_hash(), w.name))
+    traffic = _traffic(w.name)
     topk = 0 if w.topk_idx is None else int(w.topk_idx.shape[1])
     launches_per_step = 1 + int(mla.load().mla_decode_launches(w.fmt, w.B, w.H, w.max_seq_len, topk))
     # the bound of the call: HBM unless its flops at the dense bf16 peak take longer than its
@@ -525,7 +539,7 @@ def run_indexer(args):
     else:
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roofline.update({"traffic": NCU_TRAFFIC.get((_sources_hash(), w.name)), "peak_source": peaks["source"],
+    roofline.update({"traffic": _traffic(w.name), "peak_source": peaks["source"],
                      "kernel": "mla_indexer_score + mla_topk_select", "ms_per_launch": round(ms, 6),
                      "bytes_per_launch": alg_bytes, "flops_per_launch": flops,
                      "score_ms": round(score_ms, 6), "topk_ms": round(topk_ms, 6),

@@ -120,7 +120,6 @@ struct GatherParams {
     int max_seq_len;
     int topk;
     int B;
-    int fp8;                   // 1: 656-byte FP8 records, 0: 1152-byte BF16 records
     float scale_log2;          // scale * log2(e)
 };
 
@@ -163,6 +162,9 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     return b;
 }
 
+// One instantiation per (record format, tile kind) in use: FP8 pages, FP8 top-k rows, bf16 top-k
+// rows (dense bf16 pages take decode_tc_kernel), so that each holds only its own paths.
+template <bool kFp8, bool kTopk>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_gather_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                          const __grid_constant__ CUtensorMap tm_qrope,
@@ -206,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bars.ce(i), 1);
             // dense FP8 tiles: the producer's one arrival with the TMA bytes; top-k FP8 tiles: one
             // arrival per producer lane once its copies land, plus one after the mask is written
-            mbar_init(bars.rf(i), p.topk > 0 ? 33 : 1);
+            mbar_init(bars.rf(i), kTopk ? 33 : 1);
         }
         mbar_init(bars.s_full, 1);
         mbar_init(bars.s_empty, kSoftmaxThreads / 32);   // one arrive per softmax warp
@@ -241,22 +243,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // the record of row `row` of the tile at cursor cj, or null when the row is outside the
     // request (it then reads as zeros); an out-of-pool page is recorded as MLA_ERR_BOUNDS
-    const int rec_bytes = p.fp8 ? kFp8RecordBytes : kBf16RecordBytes;
-    auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* {
+    // (two stages, so that several rows' index loads, then their page loads, can be in flight)
+    constexpr int rec_bytes = kFp8 ? kFp8RecordBytes : kBf16RecordBytes;
+    auto row_pos = [&](const Cursor& cj, int row) -> int {   // visible position of the row, or -1
         int pos = cj.t * kT + row;
-        if (p.topk > 0) {
-            if (pos >= p.topk) return nullptr;
-            pos = p.topk_idx[(size_t)cj.b * p.topk + pos];
-            if (pos < 0) return nullptr;
-        }
-        if (pos >= cj.n) return nullptr;
-        const int page = p.block_table[(size_t)cj.b * p.max_pages + (pos >> 6)];
+        if (kTopk) pos = pos < p.topk ? __ldg(p.topk_idx + (size_t)cj.b * p.topk + pos) : -1;
+        return pos >= 0 && pos < cj.n ? pos : -1;
+    };
+    auto page_of = [&](const Cursor& cj, int pos) -> int {
+        return pos >= 0 ? __ldg(p.block_table + (size_t)cj.b * p.max_pages + (pos >> 6)) : 0;
+    };
+    auto record_at = [&](int pos, int page) -> const uint8_t* {
+        if (pos < 0) return nullptr;
         if (page < 0 || page >= p.num_pages) {
             if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
             return nullptr;
         }
         return p.pool + ((size_t)page * kPage + (pos & (kPage - 1))) * rec_bytes;
     };
+    auto pos_record = [&](const Cursor& cj, int pos) -> const uint8_t* { return record_at(pos, page_of(cj, pos)); };
+    auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* { return pos_record(cj, row_pos(cj, row)); };
 
     if (n_local == 0 && warp >= 2) {
         // an empty range: its partial slots must not contribute to any merge
@@ -301,7 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) fail(p.ctl, &s_abort, 19);
                 break;
             }
-            if (p.fp8) {
+            if (kFp8) {
 #pragma unroll 8
                 for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
                     uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
@@ -327,9 +333,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // one P set in tensor memory: QK of tile i + 1 follows the softmax's reads of tile i's
         // scores, P of tile i + 1 follows PV of tile i.
         if (n_local > 0) {
-            const uint32_t id_qk = p.fp8 ? idesc_f16(128, kT, 0, 0) : idesc_bf16(128, kT, 0, 0);
+            constexpr uint32_t id_qk = kFp8 ? idesc_f16(128, kT, 0, 0) : idesc_bf16(128, kT, 0, 0);
             constexpr uint32_t id_qr = idesc_bf16(128, kT, 0, 0);
-            const uint32_t id_pv = p.fp8 ? idesc_f16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 1);
+            constexpr uint32_t id_pv = kFp8 ? idesc_f16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 1);
             const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
             const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
             const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
@@ -424,32 +430,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 16-byte cp.async (21 pieces per row: 16 of codes, the scales, 4 of rope) and arrives
         // once they have landed.  Row lookups run one tile ahead, so that their latency overlaps
         // the wait for the slot, and the rows of tile j + kPfAhead are prefetched into L2.
-        if (p.fp8 && n_local > 0) {
+        if (kFp8 && n_local > 0) {
             constexpr int kPfAhead = 3;
-            const bool dense = p.topk == 0;
+            constexpr bool dense = !kTopk;
             if (dense && lane == 0) {
                 tma_prefetch_desc(&tm_codes);
                 tma_prefetch_desc(&tm_krope);
                 tma_prefetch_desc(&tm_scl);
             }
-            Cursor cj, cpf;
+            Cursor cj, cpf;   // the next tile to load, and (dense) the next tile to prefetch into L2
             cj.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
             cpf = cj;
             int j_pf = 0;
-            const uint8_t* pf0 = nullptr;
-            const uint8_t* pf1 = nullptr;
-            // L2 prefetch of the rows looked up in the call before, then the lookup of tile j_pf
-            auto prefetch_step = [&]() {
+            // L2 prefetch of the rows of the records given (dense: lane 0 holds the page's row 0)
+            auto prefetch = [&](const uint8_t* f0, const uint8_t* f1) {
                 if (dense) {
-                    if (pf0) {
-                        const int y = (int)((pf0 - p.pool) / kFp8RecordBytes);
+                    if (f0) {
+                        const int y = (int)((f0 - p.pool) / kFp8RecordBytes);
                         tma_prefetch_l2_2d(&tm_codes, kHalfLat * (int)r, y);
                         tma_prefetch_l2_2d(&tm_krope, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
                         tma_prefetch_l2_2d(&tm_scl, kFp8ScaleOff, y);
                     }
                 } else {
                     // the lines of the row's codes half and of its scales and rope
-                    const uint8_t* pq[2] = {pf0, pf1};
+                    const uint8_t* pq[2] = {f0, f1};
 #pragma unroll
                     for (int q = 0; q < 2; ++q)
                         if (pq[q]) {
@@ -459,20 +463,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             prefetch_line_l2(pq[q] + kFp8RecordBytes - 16);
                         }
                 }
-                pf0 = pf1 = nullptr;
+            };
+            // Dense tiles: at the start of each iteration the page of tile j_pf (looked up by lane 0
+            // the iteration before) is prefetched and the page of the next tile to prefetch looked
+            // up; after a tile is issued, rows lane, lane + 32 of the next one are looked up.
+            const uint8_t* rec0 = nullptr;
+            const uint8_t* rec1 = nullptr;
+            const uint8_t* pf_page = nullptr;
+            auto prefetch_dense = [&]() {
+                prefetch(pf_page, nullptr);
+                pf_page = nullptr;
                 if (j_pf < n_local) {
-                    if (!dense || lane == 0) pf0 = row_record(cpf, lane);
-                    if (!dense) pf1 = row_record(cpf, lane + 32);
+                    if (lane == 0) pf_page = row_record(cpf, 0);
                     ++j_pf;
                     cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
                 }
             };
-            for (int k = 0; k < kPfAhead; ++k) prefetch_step();
-            const uint8_t* rec0 = row_record(cj, lane);
-            const uint8_t* rec1 = row_record(cj, lane + 32);
+            // Top-k tiles: a three-stage pipeline in which every load is consumed one iteration
+            // after it is issued: index loads of tile j + 3, page loads of tile j + 2, records of
+            // tile j + 1 (whose rows are then prefetched into L2), run after tile j is issued.
+            Cursor cB = cj, cA = cj;   // the tiles of the page and index stages
+            int jB = 0, jA = 0;
+            int ia0 = -1, ia1 = -1;    // index stage results (raw list entries)
+            int pb0 = -1, pb1 = -1, gb0 = 0, gb1 = 0;   // page stage results: positions, pages
+            auto stage_a = [&]() {
+                ia0 = ia1 = -1;
+                if (jA < n_local) {
+                    const int e0 = cA.t * kT + lane, e1 = e0 + 32;
+                    const size_t base = (size_t)cA.b * p.topk;
+                    ia0 = e0 < p.topk ? __ldg(p.topk_idx + base + e0) : -1;
+                    ia1 = e1 < p.topk ? __ldg(p.topk_idx + base + e1) : -1;
+                }
+            };
+            auto stage_b = [&]() {   // consumes the index stage of the same tile, then advances it
+                pb0 = pb1 = -1;
+                if (jB < n_local) {
+                    pb0 = ia0 >= 0 && ia0 < cB.n ? ia0 : -1;
+                    pb1 = ia1 >= 0 && ia1 < cB.n ? ia1 : -1;
+                    gb0 = page_of(cB, pb0);
+                    gb1 = page_of(cB, pb1);
+                    ++jB;
+                    cB.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                }
+                if (jA < n_local) {
+                    ++jA;
+                    cA.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                }
+                stage_a();
+            };
+            auto lookups_topk = [&](bool load_next) {   // records of the tile the page stage holds
+                rec0 = load_next ? record_at(pb0, gb0) : nullptr;
+                rec1 = load_next ? record_at(pb1, gb1) : nullptr;
+                prefetch(rec0, rec1);
+                stage_b();
+            };
+            if (dense) {
+                for (int k = 0; k < kPfAhead; ++k) prefetch_dense();
+                rec0 = row_record(cj, lane);
+                rec1 = row_record(cj, lane + 32);
+            } else {
+                stage_a();    // tile 0
+                stage_b();    // tile 0 pages, tile 1 indices
+                lookups_topk(true);
+            }
             int issued = 0;
             for (int j = 0; j < n_local; ++j) {
-                prefetch_step();
+                if (dense) prefetch_dense();
                 const int slot = j % kNC;
                 const uint32_t m0 = __ballot_sync(0xffffffffu, rec0 != nullptr);
                 const uint32_t m1 = __ballot_sync(0xffffffffu, rec1 != nullptr);
@@ -491,16 +547,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * slot;
                     mk[0] = m0;
                     mk[1] = m1;
-                    if (dense) {
-                        if (m0 & 1u) {   // row 0 of a dense tile is visible unless its page is not
-                            const int y = (int)((rec0 - p.pool) / kFp8RecordBytes);
-                            mbar_arrive_expect_tx(bar, kRawTileBytes);
-                            tma_load_2d(dst, &tm_codes, bar, kHalfLat * (int)r, y);
-                            tma_load_2d(dst_rope, &tm_krope, bar, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
-                            tma_load_2d(dst_scl, &tm_scl, bar, kFp8ScaleOff, y);
-                        } else {
-                            mbar_arrive(bar);
-                        }
+                    if (dense && (m0 & 1u)) {   // row 0 of a dense tile is visible unless its page is not
+                        const int y = (int)((rec0 - p.pool) / kFp8RecordBytes);
+                        mbar_arrive_expect_tx(bar, kRawTileBytes);
+                        tma_load_2d(dst, &tm_codes, bar, kHalfLat * (int)r, y);
+                        tma_load_2d(dst_rope, &tm_krope, bar, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
+                        tma_load_2d(dst_scl, &tm_scl, bar, kFp8ScaleOff, y);
                     } else {
                         mbar_arrive(bar);
                     }
@@ -523,10 +575,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 ++issued;
                 cj.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                rec0 = rec1 = nullptr;
-                if (j + 1 < n_local) {
-                    rec0 = row_record(cj, lane);
-                    rec1 = row_record(cj, lane + 32);
+                if (dense) {
+                    rec0 = rec1 = nullptr;
+                    if (j + 1 < n_local) {
+                        rec0 = row_record(cj, lane);
+                        rec1 = row_record(cj, lane + 32);
+                    }
+                } else {
+                    lookups_topk(j + 1 < n_local);
                 }
             }
             // drain: the copies of the last tiles (one per slot) land before this CTA may exit
@@ -625,7 +681,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto store_p = [&](int i, const uint32_t (&pk)[8]) {
             if (i >= 1 && !wwait(bars.p_empty, (i - 1) & 1, 11)) return;
             uint32_t pa[8], pb[8];
-            if (p.fp8) {
+            if (kFp8) {
                 const float2* sc = scales_of(i);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -706,7 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint8_t* lat = sm + kOffConv + slot * kConvBytes;
             uint8_t* rope = lat + 4 * kKvLatChunk;
             const uint4 zero = make_uint4(0, 0, 0, 0);
-            if (p.fp8) {
+            if (kFp8) {
                 const bool ok = wwait(bars.rf(slot), (j / kNC) & 1, 17);
                 const uint32_t* mk = reinterpret_cast<const uint32_t*>(sm + kOffMask) + 2 * slot;
                 const uint32_t mk0 = mk[0], mk1 = mk[1];
@@ -799,10 +855,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // at / 64 (latent bytes, rope, scales) of row at % 64.  Its address comes from the
         // index loads of the iteration before, so their latency overlaps an iteration.
         const int pf_row = at & (kT - 1), pf_part = at >> 6;
-        const uint32_t pf_bytes = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
-        const int pf_off = pf_part == 0 ? (p.fp8 ? kHalfLat : 2 * kHalfLat) * (int)r
-                                        : (pf_part == 1 ? (p.fp8 ? kFp8RopeOff : 2 * kDc) + 64 * (int)r : kFp8ScaleOff);
-        const bool pf_on = !p.fp8 && pf_part < 2;   // FP8 tiles: the producer warp prefetches
+        const uint32_t pf_bytes = pf_part == 0 ? (kFp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
+        const int pf_off = pf_part == 0 ? (kFp8 ? kHalfLat : 2 * kHalfLat) * (int)r
+                                        : (pf_part == 1 ? (kFp8 ? kFp8RopeOff : 2 * kDc) + 64 * (int)r : kFp8ScaleOff);
+        const bool pf_on = !kFp8 && pf_part < 2;   // FP8 tiles: the producer warp prefetches
         Cursor cpf = cu;   // the tile whose prefetch address is computed next (tiles 0, 1 are
         int i_pf = 0;      // prepared at once)
         for (; i_pf < 2 && i_pf < n_local; ++i_pf) cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
@@ -884,7 +940,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lfull_remote = mapa(bars.l_full, peer);
             const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
-            const float slack = p.fp8 ? kLazySlackFp8 : kLazySlackBf16;
+            constexpr float slack = kFp8 ? kLazySlackFp8 : kLazySlackBf16;
             const float p_max = exp2f(slack);
             float m_used = -INFINITY, l_part = 0.f;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
@@ -1031,16 +1087,22 @@ DecodePlan plan_decode_gather(int fmt, int B, int max_seq_len, int topk, int sms
 }
 
 cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st) {
-    static bool attr_set[64] = {};
+    const bool fp8 = a.fmt == MLA_KV_FP8_MIXED;
+    const bool topk = a.topk_idx != nullptr && a.topk > 0;
+    if (!fp8 && !topk) return cudaErrorInvalidValue;   // dense bf16 pages: decode_tc_kernel
+    const int mode = fp8 ? (topk ? 1 : 0) : 2;
+    auto* kernel = mode == 0 ? decode_gather_kernel<true, false>
+                 : mode == 1 ? decode_gather_kernel<true, true>
+                             : decode_gather_kernel<false, true>;
+    static bool attr_set[64][3] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+    if (!attr_set[dev][mode]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev][mode] = true;
     }
     CUtensorMap tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl;
     const uint64_t qrows = (uint64_t)a.B * kHeads;
@@ -1082,9 +1144,8 @@ cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cu
     p.max_seq_len = a.max_seq_len;
     p.topk = a.topk_idx != nullptr ? a.topk : 0;
     p.B = a.B;
-    p.fp8 = a.fmt == MLA_KV_FP8_MIXED ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    decode_gather_kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl, p);
+    kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st);
