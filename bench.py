@@ -74,6 +74,23 @@ def _traffic(workload: str):
     return NCU_TRAFFIC.get((_sources_hash(workload), workload))
 
 
+def max_over_ranks(ms: float, dist, device: str = "cuda") -> float:
+    """The slowest rank's time (every rank gets it), so that a job's value is the units all ranks
+    processed divided by the time the whole job took.  dist is torch.distributed or None."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: each of `world` ranks processes `units_per_rank` in `seconds` (the
+    max over ranks); replicas only, so per-rank work is fixed as ranks are added (weak scaling)."""
+    return world * units_per_rank / seconds
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -324,10 +341,7 @@ def run_ours(args):
         ev1.record(stream)
     barrier()
     ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
 
     # ---- decode-kernel timing (roofline): graphs of `reps` back-to-back decode calls ----
     n_dec = max(10, min(200, args.steps // reps + 1))
@@ -352,7 +366,7 @@ def run_ours(args):
     alg_bytes = dw.algorithmic_bytes()
     flops = dw.flops()
     step_s = ms / 1e3 / args.steps
-    value = world * kv_bytes / step_s / 1e9
+    value = job_value(world, kv_bytes, step_s) / 1e9
     peaks = _peaks()
     dec_s = dec_ms / 1e3
     achieved = alg_bytes / dec_s / 1e9
@@ -485,10 +499,7 @@ def run_indexer(args):
 
     steps = min(args.steps, 500)
     ms = timed(graphs["step"], steps)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     score_ms = timed(graphs["score"], max(10, steps // 2))
     topk_ms = timed(graphs["topk"], max(10, steps // 2))
     clocks = sampler.stop()
@@ -638,12 +649,9 @@ def run_e2e(args, dw, torch, mla, stream, barrier, dist):
         e1.record(stream)
     barrier()
     ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     world = 1 if dist is None else dist.get_world_size()
-    value = world * dw.kv_bytes() / (ms / 1e3 / steps) / 1e9
+    value = job_value(world, dw.kv_bytes(), ms / 1e3 / steps) / 1e9
     return {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(ms / steps, 4)}
