@@ -56,9 +56,9 @@ WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_
 NCU_TRAFFIC = {
     ("4e0d25fe1eceffc4", "paged_batch"): 178_197_504,
     ("4e0d25fe1eceffc4", "long_context"): 155_823_104,
-    ("a98ff32544de16c1", "fp8_batch"): 1_417_405_440,
-    ("a98ff32544de16c1", "topk_sparse"): 123_346_688,
-    ("97765f997c7c0cb6", "indexer_topk"): 1_144_415_232,
+    ("168287261a379162", "fp8_batch"): 1_415_478_784,
+    ("168287261a379162", "topk_sparse"): 122_264_576,
+    ("97765f997c7c0cb6", "indexer_topk"): 1_144_435_712,
 }
 
 
