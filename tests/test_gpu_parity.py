@@ -237,3 +237,41 @@ def test_full_fp8_batch(torch):
 
 def test_full_topk_sparse(torch):
     _sampled(torch, "topk_sparse", [(0, 5), (33, 64), (63, 127)])
+
+
+def test_zero_queries_average_the_latents(torch):
+    """q = 0: every visible position scores 0, so out is the plain mean of the visible latents and
+    lse = ln N (the oracle's zero-query special case), through pages, splits and both formats."""
+    for fmt in (0, 1):
+        w = _custom(f"zeroq{fmt}", fmt, [1, 64, 3001, 9000], seed=29)
+        dw = harness.DeviceWorkload(w, gen="host")
+        dw.q_lat.zero_()
+        dw.q_rope.zero_()
+        out, lse = dw.decode()
+        assert mla.check_status() == 0
+        pool = oracle_pool(w)
+        zl = np.zeros((w.B, 128, synth.D_C), dtype=np.uint16)
+        zr = np.zeros((w.B, 128, synth.D_R), dtype=np.uint16)
+        ro, rl, _ = oracle.mla_decode(w.fmt, pool, zl, zr, w.block_table, w.seq_lens, w.scale)
+        assert np.allclose(rl.reshape(w.B, 128), np.log(w.seq_lens.astype(np.float64))[:, None], atol=1e-12)
+        assert_decode_close(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().reshape(-1),
+                            ro, rl, f"zero queries fmt={fmt}")
+
+
+def test_topk_listing_every_position_equals_dense(torch):
+    """A top-k list holding every visible position (the top-k path's degenerate case) gives the
+    dense result: both paths against the oracle, and against each other."""
+    seq = [130, 1000, 64]
+    K = 1024
+    idx = np.full((len(seq), K), -1, np.int32)
+    for b, n in enumerate(seq):
+        idx[b, :n] = np.arange(n, dtype=np.int32)
+    for fmt in (0, 1):
+        wd = _custom(f"dense{fmt}", fmt, seq, seed=30)
+        wk = _custom(f"all{fmt}", fmt, seq, seed=30, topk_idx=idx)
+        dd = _run_full_compare(torch, wd, f"dense fmt={fmt}")
+        dk = _run_full_compare(torch, wk, f"top-k of every position fmt={fmt}")
+        od, ld = dd.decode()
+        ok, lk = dk.decode()
+        assert np.abs(od.float().cpu().numpy() - ok.float().cpu().numpy()).max() <= 1e-2
+        assert np.abs(ld.cpu().numpy() - lk.cpu().numpy()).max() <= 1e-3
