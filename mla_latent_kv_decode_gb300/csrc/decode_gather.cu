@@ -558,15 +558,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!dense) {
+                    // each lane copies its row's 16-byte pieces starting at piece `lane`, so that
+                    // the 32 lanes of one copy instruction write different banks
                     auto copy_row = [&](const uint8_t* rec, int row) {
                         if (!rec) return;
                         const uint8_t* cs = rec + kHalfLat * (int)r;
 #pragma unroll
-                        for (int k = 0; k < kHalfLat / 16; ++k) cp_async16(dst + row * kHalfLat + 16 * k, cs + 16 * k);
+                        for (int k = 0; k < kHalfLat / 16; ++k) {
+                            const int q = (k + lane) & (kHalfLat / 16 - 1);
+                            cp_async16(dst + row * kHalfLat + 16 * q, cs + 16 * q);
+                        }
                         cp_async16(dst_scl + row * 16, rec + kFp8ScaleOff);
                         const uint8_t* rs = rec + kFp8RopeOff + 2 * kHalfRope * (int)r;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) cp_async16(dst_rope + row * 64 + 16 * k, rs + 16 * k);
+                        for (int k = 0; k < 4; ++k) {
+                            const int q = (k + lane) & 3;
+                            cp_async16(dst_rope + row * 64 + 16 * q, rs + 16 * q);
+                        }
                     };
                     copy_row(rec0, lane);
                     copy_row(rec1, lane + 32);
