@@ -20,9 +20,11 @@
 // warps (thread = position = TMEM lane) finish the scores.  The pass is HBM-bound on the keys
 // (132 B per position).
 //
-// Top-k: one CTA per request; a radix select on order-preserving keys of the fp32 scores (four
-// 8-bit digits, most significant first) finds the K-th largest, then an ordered compaction writes
-// the positions above it and, of those equal to it, the lowest ones, in increasing position order.
+// Top-k: one cluster of two CTAs per request, each holding half the row; a radix select on
+// order-preserving keys of the fp32 scores (four 8-bit digits, most significant first, the two
+// halves' histograms summed through distributed shared memory) finds the K-th largest, then each
+// CTA writes its half's positions above it and, of those equal to it, the lowest ones, in
+// increasing position order.
 #include <cuda.h>
 
 #include "decode_common.cuh"
@@ -654,79 +656,106 @@ __device__ __forceinline__ int block_scan(int v, int* total, int* sh) {
     return r;
 }
 
-__global__ void __launch_bounds__(kKThreads) topk_select_kernel(const float* __restrict__ scores, int64_t ld,
-                                                                const int32_t* __restrict__ seq_lens,
-                                                                int K, int32_t* __restrict__ idx) {
-    __shared__ uint32_t hist[256];
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// One request per cluster of two CTAs; CTA q holds positions [q h, min(n, (q + 1) h)), h = the
+// row's first half rounded up.  The K-th largest key T is found one 8-bit digit at a time (most
+// significant first) from the sum of the two CTAs' histograms of their halves (read through
+// distributed shared memory; two histogram buffers, so one cluster barrier per digit suffices).
+// Each CTA also learns from the histograms how many keys above T and equal to T the first half
+// holds, which places the second CTA's output, and then compacts its half in position order
+// (the keys above T, and of the krem keys equal to T the lowest positions).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
+    topk_select_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ seq_lens, int K,
+                       int32_t* __restrict__ idx) {
+    __shared__ uint32_t hist[2][256];
+    __shared__ uint32_t phist[256];   // the peer's histogram of the current digit, copied
     __shared__ int sh[64];
     __shared__ uint32_t s_prefix, s_mask;
-    __shared__ int s_krem;
-    const int b = blockIdx.x, tid = threadIdx.x;
+    __shared__ int s_krem, s_above0, s_eq0;
+    const uint32_t q = cluster_rank();
+    const int b = blockIdx.x >> 1, tid = threadIdx.x;
     int64_t n = seq_lens[b];
     n = n < 0 ? 0 : (n > ld ? ld : n);
     const float* row = scores + (size_t)b * ld;
     int32_t* out = idx + (size_t)b * K;
     if (n <= K) {
-        for (int t = tid; t < K; t += kKThreads) out[t] = t < n ? t : -1;
-        return;
+        if (q == 0)
+            for (int t = tid; t < K; t += kKThreads) out[t] = t < n ? t : -1;
+        return;   // both CTAs of the cluster leave here
     }
+    const int64_t h = (n + 1) / 2;
+    const int64_t lo = q * h, hi = q == 0 ? h : n;
+    const uint32_t peer_hist = mapa(smem_u32(&hist[0][0]), q ^ 1u);
     if (tid == 0) {
         s_prefix = 0;
         s_mask = 0;
         s_krem = K;
+        s_above0 = 0;
+        s_eq0 = 0;
     }
-    // the K-th largest key, one 8-bit digit at a time (most significant first): krem counts the
-    // keys still to take among those matching the prefix
     for (int level = 0; level < 4; ++level) {
-        const int shift = 24 - 8 * level;
-        for (int j = tid; j < 256; j += kKThreads) hist[j] = 0;
+        const int shift = 24 - 8 * level, hb = level & 1;
+        for (int j = tid; j < 256; j += kKThreads) hist[hb][j] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
-        for (int64_t t = tid; t < n; t += kKThreads) {
+        for (int64_t t = lo + tid; t < hi; t += kKThreads) {
             const uint32_t key = order_key(row[t]);
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            if ((key & mask) == prefix) atomicAdd(&hist[hb][(key >> shift) & 255u], 1u);
         }
+        cluster_sync();   // both halves' histograms of this digit are complete
+        for (int j = tid; j < 256; j += kKThreads) phist[j] = ld_cluster_u32(peer_hist + 4u * (uint32_t)(hb * 256 + j));
         __syncthreads();
         if (tid == 0) {
-            int krem = s_krem;
+            int krem = s_krem, above0 = s_above0;
             int dsel = 0;
             for (int dg = 255; dg >= 0; --dg) {
-                const int c = (int)hist[dg];
+                const int mine = (int)hist[hb][dg], theirs = (int)phist[dg];
+                const int c = mine + theirs;
                 if (c >= krem) {
                     dsel = dg;
+                    if (level == 3) s_eq0 = q == 0 ? mine : theirs;
                     break;
                 }
                 krem -= c;
+                above0 += q == 0 ? mine : theirs;
             }
             s_krem = krem;
+            s_above0 = above0;
             s_prefix = prefix | ((uint32_t)dsel << shift);
             s_mask = mask | (255u << shift);
         }
         __syncthreads();
     }
+    cluster_sync();   // no CTA reads the other's histograms any more (it may exit)
     const uint32_t T = s_prefix;
     const int krem = s_krem;   // keys equal to T to take, lowest positions first
-    // ordered compaction, 4 consecutive positions per thread per round
-    int base = 0, eq_seen = 0;
-    for (int64_t c0 = 0; c0 < n; c0 += 4 * kKThreads) {
+    // ordered compaction of this half, 4 consecutive positions per thread per round
+    int base = q == 0 ? 0 : s_above0 + min(krem, s_eq0);
+    int eq_seen = q == 0 ? 0 : s_eq0;
+    for (int64_t c0 = lo; c0 < hi; c0 += 4 * kKThreads) {
         const int64_t t0 = c0 + 4 * tid;
         uint32_t key[4];
         int n_eq = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            key[e] = t0 + e < n ? order_key(row[t0 + e]) : 0u;
-            n_eq += (t0 + e < n && key[e] == T) ? 1 : 0;
+            key[e] = t0 + e < hi ? order_key(row[t0 + e]) : 0u;
+            n_eq += (t0 + e < hi && key[e] == T) ? 1 : 0;
         }
         int eq_total;
         const int eq_before = eq_seen + block_scan(n_eq, &eq_total, sh);
-        int take[4], n_take = 0, r = eq_before;
+        int take[4], n_take = 0, rk = eq_before;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const bool in = t0 + e < n;
+            const bool in = t0 + e < hi;
             const bool gt = in && key[e] > T;
             const bool eq = in && key[e] == T;
-            take[e] = gt || (eq && r < krem);
-            r += eq ? 1 : 0;
+            take[e] = gt || (eq && rk < krem);
+            rk += eq ? 1 : 0;
             n_take += take[e];
         }
         int take_total;
@@ -793,7 +822,7 @@ cudaError_t launch_indexer_score(const uint8_t* pool, int64_t num_pages, const _
 
 cudaError_t launch_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int B, int K,
                                int32_t* idx, cudaStream_t st) {
-    topk_select_kernel<<<B, kKThreads, 0, st>>>(scores, ld, seq_lens, K, idx);
+    topk_select_kernel<<<2 * B, kKThreads, 0, st>>>(scores, ld, seq_lens, K, idx);
     return cudaGetLastError();
 }
 
