@@ -56,9 +56,9 @@ WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_
 NCU_TRAFFIC = {
     ("4e0d25fe1eceffc4", "paged_batch"): 178_197_504,
     ("4e0d25fe1eceffc4", "long_context"): 155_823_104,
-    ("168287261a379162", "fp8_batch"): 1_415_478_784,
-    ("168287261a379162", "topk_sparse"): 122_264_576,
-    ("97765f997c7c0cb6", "indexer_topk"): 1_144_435_712,
+    ("728ed11da3a0569d", "fp8_batch"): 1_414_574_592,
+    ("728ed11da3a0569d", "topk_sparse"): 122_382_592,
+    ("a24c84afac1bba6c", "indexer_topk"): 1_144_571_392,
 }
 
 
