@@ -613,48 +613,97 @@ def indexer_cpu_baseline(w, budget_s: float = 12.0):
                       f"{spent:.1f} s of fp64 oracle time (one thread per query)"}
 
 
+def _pack(torch, tensors, device):
+    """One pinned host buffer and one device buffer holding `tensors` at 256-byte aligned offsets:
+    (host buffer, device buffer, device views with the tensors' dtypes and shapes)."""
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(total, dtype=torch.uint8, device=device)
+    views = []
+    for t, o in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        host[o:o + n].copy_(t.detach().contiguous().view(torch.uint8).reshape(-1).cpu())
+        views.append(dev[o:o + n].view(t.dtype).view(t.shape))
+    return host, dev, views
+
+
 def run_e2e(args, dw, torch, mla, stream, barrier, dist):
-    """Same metric through the public API with pinned host buffers: every step copies its inputs
-    (queries, block table, seq_lens, new rows and slots) host->device, runs append + decode, and
-    reads out + lse back."""
-    w = dw.w
-    host = {}
-    dev = {"q_lat": dw.q_lat, "q_rope": dw.q_rope, "block_table": dw.block_table,
-           "seq_lens": dw.seq_lens, "new_c": dw.new_c, "new_r": dw.new_r, "new_slot": dw.new_slot}
-    for k, v in dev.items():
-        host[k] = v.cpu().pin_memory()
-    out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
-    lse_h = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    """Same metric through the public API with pinned host buffers, as a serving loop runs it:
+    every step's inputs (queries, block table, seq_lens, new rows and slots, packed in one pinned
+    buffer) go host->device in one copy and its out + lse (one device buffer) come back in one
+    copy, on a copy stream, while the compute stream runs append + decode of the step before
+    (two input and two output buffers; events keep each buffer's writer after its last reader).
+    Every copy of every step is inside the timed region."""
+    names = [k for k in ("q_lat", "q_rope", "block_table", "seq_lens", "new_c", "new_r", "new_slot")
+             if getattr(dw, k) is not None]
+    saved = {k: getattr(dw, k) for k in names + ["out", "lse"]}
+    ins = [_pack(torch, [saved[k] for k in names], dw.device) for _ in range(2)]
+    outs = [_pack(torch, [saved["out"], saved["lse"]], dw.device) for _ in range(2)]
+    h2d = ins[0][0].numel()
+    d2h = outs[0][0].numel()
     steps = max(3, min(args.steps, 200))
+    # one copy stream for both directions: a second one (measured) helped the batch workloads by
+    # ~1.5 % and cost the long-context one ~10 % in host overhead
+    hstream = dstream = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]     # inputs of the slot landed
+    in_free = [ev(), ev()]      # the compute that read the slot's inputs is done
+    out_ready = [ev(), ev()]    # the compute that wrote the slot's outputs is done
+    out_free = [ev(), ev()]     # the copy that read the slot's outputs is done
 
-    def one(i):
-        for k in dev:
-            dev[k].copy_(host[k], non_blocking=True)
-        dw.step(i % dw.replicas)
-        out_h.copy_(dw.out, non_blocking=True)
-        lse_h.copy_(dw.lse, non_blocking=True)
+    def run(n):
+        with torch.cuda.stream(hstream):
+            ins[0][1].copy_(ins[0][0], non_blocking=True)
+            in_ready[0].record(hstream)
+        for i in range(n):
+            sl = i % 2
+            stream.wait_event(in_ready[sl])
+            if i >= 2:
+                stream.wait_event(out_free[sl])
+            for k, v in zip(names, ins[sl][2]):
+                setattr(dw, k, v)
+            dw.out, dw.lse = outs[sl][2]
+            with torch.cuda.stream(stream):
+                dw.step(i % dw.replicas)
+            in_free[sl].record(stream)
+            out_ready[sl].record(stream)
+            if i + 1 < n:
+                o = 1 - sl
+                if i >= 1:
+                    hstream.wait_event(in_free[o])
+                with torch.cuda.stream(hstream):
+                    ins[o][1].copy_(ins[o][0], non_blocking=True)
+                    in_ready[o].record(hstream)
+            dstream.wait_event(out_ready[sl])
+            with torch.cuda.stream(dstream):
+                outs[sl][0].copy_(outs[sl][1], non_blocking=True)
+                out_free[sl].record(dstream)
+        stream.wait_stream(hstream)
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            one(i)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
+    try:
+        run(3)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            one(i)
+        hstream.wait_stream(stream)
+        run(steps)
         e1.record(stream)
-    barrier()
+        barrier()
+    finally:
+        for k, v in saved.items():
+            setattr(dw, k, v)
     ms = e0.elapsed_time(e1)
     ms = max_over_ranks(ms, dist)
     world = 1 if dist is None else dist.get_world_size()
     value = job_value(world, dw.kv_bytes(), ms / 1e3 / steps) / 1e9
     return {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "ms_per_step": round(ms / steps, 4)}
+            "ms_per_step": round(ms / steps, 4),
+            "overlap": "inputs of step i+1 and outputs of step i copied while step i+1 / i compute"}
 
 
 def main(argv=None):
