@@ -112,7 +112,13 @@ int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_l
  *   lse        : device fp32 [B, H] = ln sum_t exp(s_t) (-inf if nothing is visible).
  *   workspace  : device scratch of at least mla_decode_workspace_bytes(...) bytes (may be NULL
  *                when that is 0); 256-byte aligned; its contents are clobbered.
- * A page index outside [0, num_pages) met while reading records MLA_ERR_BOUNDS. */
+ * A page index outside [0, num_pages) met while reading records MLA_ERR_BOUNDS.
+ * Arithmetic: scores and outputs accumulate in fp32 on the tensor cores.  bf16 records: bf16
+ * operands, P rounded once to bf16.  FP8 records: the E4M3 codes enter as f16 (exact), and so
+ * does q_lat, converted once per request (exact for |q| in [2^-14, 65504); smaller magnitudes
+ * lose low bits, larger ones overflow).  Each 128-dim group's scale multiplies in fp32: on that
+ * group's partial score, and on P as f16(P * scale).  The last stays finite for group scales
+ * below 255 (absmax below 114,000), because the running max is kept within 2^8 of every P. */
 mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
                       const void* q_rope, const int32_t* block_table, int32_t max_pages,
                       const int32_t* seq_lens, int32_t max_seq_len, const int32_t* topk_idx,
