@@ -21,10 +21,10 @@
 // (132 B per position).
 //
 // Top-k: one cluster of two CTAs per request, each holding half the row; a radix select on
-// order-preserving keys of the fp32 scores (four 8-bit digits, most significant first, the two
-// halves' histograms summed through distributed shared memory) finds the K-th largest, then each
-// CTA writes its half's positions above it and, of those equal to it, the lowest ones, in
-// increasing position order.
+// order-preserving keys of the fp32 scores (digits of 11, 11 and 10 bits, most significant first,
+// the two halves' histograms summed through distributed shared memory) finds the K-th largest,
+// then each warp writes the positions of its range of a half that are above it and, of those
+// equal to it, the lowest ones, in increasing position order.
 #include <cuda.h>
 
 #include "decode_common.cuh"
@@ -629,58 +629,66 @@ __device__ __forceinline__ uint32_t order_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // larger float, larger key
 }
 
-// Block-wide exclusive scan of v (1024 threads); returns the prefix, *total the sum.
-__device__ __forceinline__ int block_scan(int v, int* total, int* sh) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) sh[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int s = sh[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        sh[32 + lane] = s;
-    }
-    __syncthreads();
-    *total = sh[32 + 31];
-    const int r = (warp > 0 ? sh[32 + warp - 1] : 0) + x - v;
-    __syncthreads();
-    return r;
-}
-
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 
+constexpr int kKWarps = kKThreads / 32;
+constexpr int kKU = 8;   // loads in flight per thread in the passes over the row
+
+// One warp: the bin of hist[0, nb) holding the krem-th largest key (a larger bin holds larger
+// keys) and how many keys of that bin are still to take (1 <= krem <= the histogram's total).
+__device__ __forceinline__ void select_digit(const uint32_t* hist, int nb, int krem, uint32_t* d_out,
+                                             int* krem_out) {
+    const int lane = threadIdx.x & 31;
+    const int per = nb / 32;   // bins per lane, lane 31 holding the largest
+    int sum = 0;
+    for (int i = 0; i < per; ++i) sum += (int)hist[lane * per + i];
+    int incl = sum;            // keys in this lane's bins and above
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+    }
+    const int above = incl - sum;
+    if (above < krem && krem <= incl) {   // exactly one lane
+        int rem = krem - above;
+        for (int i = per - 1; i >= 0; --i) {
+            const int c = (int)hist[lane * per + i];
+            if (c >= rem) {
+                *d_out = (uint32_t)(lane * per + i);
+                *krem_out = rem;
+                break;
+            }
+            rem -= c;
+        }
+    }
+}
+
 // One request per cluster of two CTAs; CTA q holds positions [q h, min(n, (q + 1) h)), h = the
-// row's first half rounded up.  The K-th largest key T is found one 8-bit digit at a time (most
-// significant first) from the sum of the two CTAs' histograms of their halves (read through
-// distributed shared memory; two histogram buffers, so one cluster barrier per digit suffices).
-// Each CTA also learns from the histograms how many keys above T and equal to T the first half
-// holds, which places the second CTA's output, and then compacts its half in position order
-// (the keys above T, and of the krem keys equal to T the lowest positions).
+// row's first half rounded up.  The K-th largest key T is found one digit at a time (11, 11 and
+// 10 bits, most significant first) from the sum of the two CTAs' histograms of their halves
+// (the peer's read through distributed shared memory; two histogram buffers, so one cluster
+// barrier per digit suffices).  The histograms also give how many keys above T and equal to T the
+// first half holds, which places the second CTA's output.  Each warp of a CTA then owns a
+// contiguous range of its half: one pass counts the range's keys above and equal to T, and a
+// second writes its positions in order (the keys above T, and of the krem keys equal to T the
+// lowest positions).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
     topk_select_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ seq_lens, int K,
                        int32_t* __restrict__ idx) {
-    __shared__ uint32_t hist[2][256];
-    __shared__ uint32_t phist[256];   // the peer's histogram of the current digit, copied
-    __shared__ int sh[64];
-    __shared__ uint32_t s_prefix, s_mask;
-    __shared__ int s_krem, s_above0, s_eq0;
+    __shared__ uint32_t hist[2][2048];
+    __shared__ uint32_t comb[2048];   // both halves' counts of the current digit
+    __shared__ int wgt[kKWarps], weq[kKWarps];
+    __shared__ uint32_t s_prefix, s_mask, s_digit;
+    __shared__ int s_krem, s_krem_new, s_above0, s_eq0;
     const uint32_t q = cluster_rank();
-    const int b = blockIdx.x >> 1, tid = threadIdx.x;
-    int64_t n = seq_lens[b];
-    n = n < 0 ? 0 : (n > ld ? ld : n);
+    const int b = blockIdx.x >> 1, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int64_t n64 = seq_lens[b];
+    n64 = n64 < 0 ? 0 : (n64 > ld ? ld : n64);
+    const int n = (int)n64;
     const float* row = scores + (size_t)b * ld;
     int32_t* out = idx + (size_t)b * K;
     if (n <= K) {
@@ -688,8 +696,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
             for (int t = tid; t < K; t += kKThreads) out[t] = t < n ? t : -1;
         return;   // both CTAs of the cluster leave here
     }
-    const int64_t h = (n + 1) / 2;
-    const int64_t lo = q * h, hi = q == 0 ? h : n;
+    const int h = (n + 1) / 2;
+    const int lo = (int)q * h, hi = q == 0 ? h : n;
     const uint32_t peer_hist = mapa(smem_u32(&hist[0][0]), q ^ 1u);
     if (tid == 0) {
         s_prefix = 0;
@@ -698,73 +706,107 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
         s_above0 = 0;
         s_eq0 = 0;
     }
-    for (int level = 0; level < 4; ++level) {
-        const int shift = 24 - 8 * level, hb = level & 1;
-        for (int j = tid; j < 256; j += kKThreads) hist[hb][j] = 0;
+    for (int level = 0; level < 3; ++level) {
+        const int shift = level == 0 ? 21 : (level == 1 ? 10 : 0);
+        const int nb = level == 2 ? 1024 : 2048;
+        const int hb = level & 1;
+        for (int j = tid; j < 2048; j += kKThreads) hist[hb][j] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
-        for (int64_t t = lo + tid; t < hi; t += kKThreads) {
-            const uint32_t key = order_key(row[t]);
-            if ((key & mask) == prefix) atomicAdd(&hist[hb][(key >> shift) & 255u], 1u);
+        const int krem = s_krem;
+        for (int base = lo; base < hi; base += kKU * kKThreads) {
+            uint32_t key[kKU];
+#pragma unroll
+            for (int u = 0; u < kKU; ++u) {
+                const int t = base + u * kKThreads + tid;
+                key[u] = t < hi ? order_key(row[t]) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kKU; ++u)
+                if (base + u * kKThreads + tid < hi && (key[u] & mask) == prefix)
+                    atomicAdd(&hist[hb][(key[u] >> shift) & (uint32_t)(nb - 1)], 1u);
         }
         cluster_sync();   // both halves' histograms of this digit are complete
-        for (int j = tid; j < 256; j += kKThreads) phist[j] = ld_cluster_u32(peer_hist + 4u * (uint32_t)(hb * 256 + j));
+        for (int j = tid; j < nb; j += kKThreads)
+            comb[j] = hist[hb][j] + ld_cluster_u32(peer_hist + 4u * (uint32_t)(hb * 2048 + j));
         __syncthreads();
+        if (warp == 0) select_digit(comb, nb, krem, &s_digit, &s_krem_new);
+        __syncthreads();
+        const uint32_t d = s_digit;
+        // the first half's keys in bins above d (all above T), and at the last digit in bin d
+        int a0 = 0;
+        for (int j = (int)d + 1 + tid; j < nb; j += kKThreads)
+            a0 += (int)(q == 0 ? hist[hb][j] : comb[j] - hist[hb][j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+        if (lane == 0 && a0) atomicAdd(&s_above0, a0);
         if (tid == 0) {
-            int krem = s_krem, above0 = s_above0;
-            int dsel = 0;
-            for (int dg = 255; dg >= 0; --dg) {
-                const int mine = (int)hist[hb][dg], theirs = (int)phist[dg];
-                const int c = mine + theirs;
-                if (c >= krem) {
-                    dsel = dg;
-                    if (level == 3) s_eq0 = q == 0 ? mine : theirs;
-                    break;
-                }
-                krem -= c;
-                above0 += q == 0 ? mine : theirs;
-            }
-            s_krem = krem;
-            s_above0 = above0;
-            s_prefix = prefix | ((uint32_t)dsel << shift);
-            s_mask = mask | (255u << shift);
+            if (level == 2) s_eq0 = (int)(q == 0 ? hist[hb][d] : comb[d] - hist[hb][d]);
+            s_krem = s_krem_new;
+            s_prefix = prefix | (d << shift);
+            s_mask = mask | ((uint32_t)(nb - 1) << shift);
         }
         __syncthreads();
     }
     cluster_sync();   // no CTA reads the other's histograms any more (it may exit)
     const uint32_t T = s_prefix;
     const int krem = s_krem;   // keys equal to T to take, lowest positions first
-    // ordered compaction of this half, 4 consecutive positions per thread per round
-    int base = q == 0 ? 0 : s_above0 + min(krem, s_eq0);
-    int eq_seen = q == 0 ? 0 : s_eq0;
-    for (int64_t c0 = lo; c0 < hi; c0 += 4 * kKThreads) {
-        const int64_t t0 = c0 + 4 * tid;
-        uint32_t key[4];
-        int n_eq = 0;
+
+    // per warp range of this half: keys above T and equal to T
+    const unsigned lt = (1u << lane) - 1u;
+    const int L = (hi - lo + kKU * kKThreads - 1) / (kKU * kKThreads) * (kKU * 32);
+    const int r0 = lo + warp * L, r1 = min(hi, r0 + L);
+    int g = 0, e = 0;
+    for (int c0 = r0; c0 < r0 + L; c0 += 32 * kKU) {
+        uint32_t key[kKU];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            key[e] = t0 + e < hi ? order_key(row[t0 + e]) : 0u;
-            n_eq += (t0 + e < hi && key[e] == T) ? 1 : 0;
+        for (int u = 0; u < kKU; ++u) {
+            const int t = c0 + 32 * u + lane;
+            key[u] = t < r1 ? order_key(row[t]) : 0u;
         }
-        int eq_total;
-        const int eq_before = eq_seen + block_scan(n_eq, &eq_total, sh);
-        int take[4], n_take = 0, rk = eq_before;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const bool in = t0 + e < hi;
-            const bool gt = in && key[e] > T;
-            const bool eq = in && key[e] == T;
-            take[e] = gt || (eq && rk < krem);
-            rk += eq ? 1 : 0;
-            n_take += take[e];
+        for (int u = 0; u < kKU; ++u) {
+            const bool in = c0 + 32 * u + lane < r1;
+            g += (in && key[u] > T) ? 1 : 0;
+            e += (in && key[u] == T) ? 1 : 0;
         }
-        int take_total;
-        int w = base + block_scan(n_take, &take_total, sh);
+    }
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (take[e]) out[w++] = (int32_t)(t0 + e);
-        base += take_total;
-        eq_seen += eq_total;
+    for (int o = 16; o > 0; o >>= 1) {
+        g += __shfl_xor_sync(0xffffffffu, g, o);
+        e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (lane == 0) {
+        wgt[warp] = g;
+        weq[warp] = e;
+    }
+    __syncthreads();
+    int above = q == 0 ? 0 : s_above0, eq_before = q == 0 ? 0 : s_eq0;
+    for (int v = 0; v < warp; ++v) {
+        above += wgt[v];
+        eq_before += weq[v];
+    }
+    // ordered write: the keys above T before this range, and the equal ones (at most krem)
+    int o = above + min(krem, eq_before);
+    for (int c0 = r0; c0 < r0 + L; c0 += 32 * kKU) {
+        uint32_t key[kKU];
+#pragma unroll
+        for (int u = 0; u < kKU; ++u) {
+            const int t = c0 + 32 * u + lane;
+            key[u] = t < r1 ? order_key(row[t]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kKU; ++u) {
+            const int t = c0 + 32 * u + lane;
+            const bool in = t < r1;
+            const bool is_eq = in && key[u] == T;
+            const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
+            const bool take = (in && key[u] > T) || (is_eq && eq_before + __popc(eb & lt) < krem);
+            const unsigned tb = __ballot_sync(0xffffffffu, take);
+            if (take) out[o + __popc(tb & lt)] = t;
+            o += __popc(tb);
+            eq_before += __popc(eb);
+        }
     }
 }
 
