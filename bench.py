@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -38,8 +39,8 @@ UNIT = "KV GB/s"
 L2_BYTES = 126 * 2 ** 20
 
 # DRAM bytes (read + write) per launch of each workload's dominant kernel from an ncu capture,
-# keyed by the sha256 of the sources that kernel is built from and the workload; any change to
-# those sources makes the entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
+# keyed by the sha256 of the code (comments excluded) of the sources that kernel is built from and
+# the workload; any change to that code makes the entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
 # profiles/decode_gather_fp8_batch.md, profiles/indexer_score_indexer_topk.md.
 _HEADERS = ["mla_latent_kv_decode_gb300/csrc/decode_common.cuh",
             "mla_latent_kv_decode_gb300/csrc/mla_internal.cuh",
@@ -54,19 +55,27 @@ WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_
                    "fp8_batch": "decode_gather", "topk_sparse": "decode_gather",
                    "indexer_topk": "indexer_score"}
 NCU_TRAFFIC = {
-    ("4e0d25fe1eceffc4", "paged_batch"): 178_197_504,
-    ("4e0d25fe1eceffc4", "long_context"): 155_823_104,
-    ("728ed11da3a0569d", "fp8_batch"): 1_414_574_592,
-    ("728ed11da3a0569d", "topk_sparse"): 122_382_592,
-    ("a24c84afac1bba6c", "indexer_topk"): 1_144_571_392,
+    ("c9436f9a11212c15", "paged_batch"): 178_121_984,
+    ("c9436f9a11212c15", "long_context"): 155_761_152,
+    ("317d8c4c452e69fa", "fp8_batch"): 1_414_574_592,
+    ("317d8c4c452e69fa", "topk_sparse"): 122_382_592,
+    ("a650593e7d15f670", "indexer_topk"): 1_144_615_680,
 }
+
+
+def _code_only(text: str) -> str:
+    """The source without its comments and blank lines (a comment edit leaves the kernel as it
+    was; any change to code or constants does not)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
 def _sources_hash(workload: str) -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES[WORKLOAD_KERNEL[workload]]:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
