@@ -159,9 +159,10 @@ def decode(fmt: int, pool, num_pages: int, q_lat, q_rope, block_table, seq_lens,
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q_lat.device)
     topk = 0 if topk_idx is None else int(topk_idx.shape[1])
-    need = decode_workspace_bytes(fmt, B, max_seq_len, topk, H)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q_lat.device)
+    if workspace is None:   # (a caller's workspace is checked against the need by the library)
+        need = decode_workspace_bytes(fmt, B, max_seq_len, topk, H)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q_lat.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().mla_decode(
         int(fmt), _dev_ptr(pool, "pool", torch.uint8), int(num_pages),
