@@ -13,10 +13,11 @@
 //     and the DSA description on that page).  Rows outside the request (past its length, padding
 //     entries, entries >= N_b) are masked and read as zeros;
 //   * FP8 records: a producer warp copies each tile's raw bytes of this CTA's half into a
-//     conversion slot as soon as PV has released it (a page: three TMA boxes; top-k rows: three
-//     bulk copies per row), with the row's four group scales and a 64-bit mask of valid rows; the
-//     agent warps then convert the slot in place into the MMA operand layouts: latent [64 x 256]
-//     (128-byte swizzle), rope [64 x 32] (64-byte swizzle), zeros for rows outside the request;
+//     conversion slot as soon as PV has released it (a page: three TMA boxes; top-k rows: 21
+//     16-byte cp.async pieces per row, one row per lane), with the row's four group scales and a
+//     64-bit mask of valid rows; the agent warps then convert the slot in place into the MMA
+//     operand layouts: latent [64 x 256] (128-byte swizzle), rope [64 x 32] (64-byte swizzle),
+//     zeros for rows outside the request;
 //   * bf16 records (top-k only) are loaded by the agents from global memory straight into those
 //     layouts;
 //   * FP8 records (512 e4m3 codes, one fp32 scale per 128 dims, 64 bf16 rope dims; the 656-byte
@@ -38,8 +39,12 @@
 // (+ TMEM owner); warps 2-17: thread = head = TMEM lane, four warps per 32-lane group, 16
 // positions of a tile each; the 8 warps on the owned heads' lanes run the softmax, the other 8
 // ("agents") forward partial scores, convert the tiles, place the peer's P and finish those O
-// rows; warp 18 loads the FP8 tiles.  Every wait is bounded: on expiry the kernel records MLA_ERR_TIMEOUT, stops
-// issuing, drains its MMAs, frees TMEM and returns.
+// rows; warp 18 loads the FP8 tiles.  Every wait is bounded: on expiry the kernel records
+// MLA_ERR_TIMEOUT, stops issuing, drains its MMAs, frees TMEM and returns.
+//
+// The kernel is a template over (record format, tile kind), instantiated for FP8 pages, FP8 top-k
+// rows and bf16 top-k rows, so that each instantiation holds only its own paths (at 608 threads
+// a thread has 96 registers; the shared code spilled twice as much).
 #include <cuda.h>
 #include <cstring>
 #include <cuda_fp16.h>
