@@ -433,8 +433,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // tile is one page: three TMA boxes of its 64 rows (rows past the request's end are
         // loaded and then zeroed by the agents).  A top-k tile: each lane copies its two rows with
         // 16-byte cp.async (21 pieces per row: 16 of codes, the scales, 4 of rope) and arrives
-        // once they have landed.  Row lookups run one tile ahead, so that their latency overlaps
-        // the wait for the slot, and the rows of tile j + kPfAhead are prefetched into L2.
+        // once they have landed.  Pages: the next tile's rows are looked up after a tile is
+        // issued, and the page kPfAhead tiles ahead is prefetched into L2.  Top-k rows: index
+        // loads, page loads and records run as a three-stage pipeline (see below), and each
+        // tile's rows are prefetched into L2 one tile ahead of their copies.
         if (kFp8 && n_local > 0) {
             constexpr int kPfAhead = 3;
             constexpr bool dense = !kTopk;
@@ -863,10 +865,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto prepare_until = [&](int upto) {
             for (; i_pr < upto && i_pr < n_local; ++i_pr, cpr.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) prepare(i_pr, cpr);
         };
-        // L2 prefetch of the rows of tile i + 5 during iteration i (tile i + 2 is prepared in
-        // iteration i, so prefetches run three iterations ahead): thread `at` covers part
-        // at / 64 (latent bytes, rope, scales) of row at % 64.  Its address comes from the
-        // index loads of the iteration before, so their latency overlaps an iteration.
+        // bf16 records: L2 prefetch of the rows of tile i + 5 during iteration i (tile i + 2 is
+        // prepared in iteration i, so prefetches run three iterations ahead): thread `at` covers
+        // part at / 64 (latent bytes, rope) of row at % 64.  Its address comes from the index
+        // loads of the iteration before, so their latency overlaps an iteration.  (FP8 tiles are
+        // prefetched by warp 18.)
         const int pf_row = at & (kT - 1), pf_part = at >> 6;
         const uint32_t pf_bytes = pf_part == 0 ? (kFp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
         const int pf_off = pf_part == 0 ? (kFp8 ? kHalfLat : 2 * kHalfLat) * (int)r
