@@ -67,3 +67,38 @@ def test_synth_generator_library_loads():
     if not os.path.exists(os.path.join(os.path.dirname(mla.library_path()), "libmla_synth.so")):
         pytest.skip("not built")
     synth._load_gpu()
+
+
+def test_host_validation_of_the_other_entry_points(lib):
+    """Argument errors of the combine, indexer and top-k entry points are answered on the host
+    (MLA_ERR_INVALID = 1), and empty work returns MLA_OK, without a device."""
+    d = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    # mla_combine(o_part, lse_part, S, B, H, out, lse, stream)
+    assert lib.mla_combine(d, d, 0, 1, 128, d, d, None) == 1          # S < 1
+    assert lib.mla_combine(d, d, 2, 1, 0, d, d, None) == 1            # H < 1
+    assert lib.mla_combine(d, d, 2, -1, 128, d, d, None) == 1         # B < 0
+    assert lib.mla_combine(None, None, 2, 0, 128, None, None, None) == 0
+    assert lib.mla_combine(d, d, 2, 1, 128, odd, d, None) == 1        # out misaligned
+    assert lib.mla_combine(None, d, 2, 1, 128, d, d, None) == 1       # null partials
+    # mla_index_append(pool, num_pages, k_index, slot, T, stream)
+    assert lib.mla_index_append(d, 1, d, d, -1, None) == 1
+    assert lib.mla_index_append(d, -1, d, d, 1, None) == 1
+    assert lib.mla_index_append(None, 0, None, None, 0, None) == 0
+    assert lib.mla_index_append(odd, 1, d, d, 1, None) == 1
+    # mla_indexer_score(pool, num_pages, q, w, block_table, max_pages, seq_lens, B, max_seq_len,
+    #                   scores, stream)
+    assert lib.mla_indexer_score(d, 1, d, d, d, 1, d, -1, 64, d, None) == 1
+    assert lib.mla_indexer_score(d, 1, d, d, d, 0, d, 1, 0, d, None) == 1     # max_pages < 1
+    assert lib.mla_indexer_score(d, 1, d, d, d, 1, d, 1, 65, d, None) == 1    # beyond the table
+    assert lib.mla_indexer_score(None, 0, None, None, None, 1, None, 0, 64, None, None) == 0
+    assert lib.mla_indexer_score(d, 1, None, d, d, 1, d, 1, 64, d, None) == 1
+    # mla_topk_select(scores, ld, seq_lens, B, K, topk_idx, stream)
+    assert lib.mla_topk_select(d, 100, d, 1, 0, d, None) == 1          # K < 1
+    assert lib.mla_topk_select(d, -1, d, 1, 8, d, None) == 1           # ld < 0
+    assert lib.mla_topk_select(d, 100, d, -1, 8, d, None) == 1         # B < 0
+    assert lib.mla_topk_select(None, 100, None, 0, 8, None, None) == 0
+    assert lib.mla_topk_select(d, 100, d, 1, 8, odd, None) == 1        # misaligned output
+    # mla_decode_noalloc with H != 128 is rejected.  It looks up its static array before
+    # mla_decode's checks, so without a device the answer is MLA_ERR_CUDA, else MLA_ERR_INVALID.
+    assert lib.mla_decode_noalloc(0, d, 1, d, d, d, 1, d, 64, None, 0, 1, 64, 0.07, d, d, None) in (1, 4)
