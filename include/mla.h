@@ -230,7 +230,7 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
  * (section "The score that picks positions": every query keeps at most 2,048 of the positions
  * visible to it, those with the largest scores), written to topk_idx[b] (device int32
  * [B, K]) in increasing position order and padded with -1 past the min(K, seq_lens[b]) picks: directly the topk_idx of mla_decode.  Scores must
- * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, K < 1 or ld < 0. */
+ * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, B > 2^30, K < 1 or ld < 0. */
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream);
 

@@ -125,7 +125,7 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
 
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream) {
-    if (B < 0 || K < 1 || ld < 0) return MLA_ERR_INVALID;
+    if (B < 0 || B > (1 << 30) || K < 1 || ld < 0) return MLA_ERR_INVALID;   // two CTAs a request
     if (B == 0) return MLA_OK;
     if (!scores || !seq_lens || !topk_idx) return MLA_ERR_INVALID;
     if (!aligned(scores, 4) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4)) return MLA_ERR_INVALID;
