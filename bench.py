@@ -1,17 +1,21 @@
 #!/usr/bin/env python3
 """Benchmark of absorbed MLA decode over a paged latent cache on GB300.
 
-A step is one pass of the hot path over one batch: mla_cache_append of the newest token of
-every request (bf16 record) followed by mla_decode of the whole batch (page gather, scores,
-online softmax, weighted latent sum, split-KV merge).  Default workload: the batched paged
-decode (B=32, H=128, seq_lens uniform in [1024, 8192], 64-token pages shuffled in a shared pool,
-bf16 cache, scale 1/sqrt(192)).
+A step is one pass of the hot path over one batch: mla_cache_append of the tokens each request
+adds (quantised into the cache) followed by mla_decode of the whole batch (page gather, FP8
+dequantisation, scores, online softmax, weighted latent sum, split-KV merge).  The headline
+workload is the largest one that fits one GPU: the FP8 mixed cache, B=64 requests of 32,768
+positions each (32,704 prefilled + 64 appended per step), H=128, 64-token pages shuffled,
+scale 1/sqrt(192).  The same run measures the other four workloads (tiny dense, batched paged,
+long context, top-k sparse) and reports them under "configs".
 
 Timing: W warm-up steps, then exactly K steps bracketed by a barrier and a device synchronise,
 timed with CUDA events on the launching stream, max over ranks.  Each step is a CUDA graph of
 the two library calls (the calls take about as long as the kernels, so eager launches would
-time the host).  The inputs rotate over several identical pool replicas whose total exceeds L2,
-so every step reads its cache from HBM.
+time the host).  The inputs rotate over identical pool replicas whose touched bytes exceed L2
+three times, so every step reads its cache from HBM; the tiny workload is also timed with L2
+flushed before every call.  The decode call alone is timed over at least a second of
+back-to-back calls for the roofline figures.
 
 One JSON line on stdout (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
 """
@@ -40,8 +44,7 @@ L2_BYTES = 126 * 2 ** 20
 
 # DRAM bytes (read + write) per launch of each workload's dominant kernel from an ncu capture,
 # keyed by the sha256 of the code (comments excluded) of the sources that kernel is built from and
-# the workload; any change to that code makes the entry stale (traffic = null).  Captures: profiles/decode_tc_paged_batch.md,
-# profiles/decode_gather_fp8_batch.md, profiles/indexer_score_indexer_topk.md.
+# the workload; any change to that code makes the entry stale (traffic = null).
 _HEADERS = ["mla_latent_kv_decode_gb300/csrc/decode_common.cuh",
             "mla_latent_kv_decode_gb300/csrc/mla_internal.cuh",
             "mla_latent_kv_decode_gb300/csrc/tc_ptx.cuh",
@@ -210,6 +213,16 @@ def cpu_baseline(w, budget_s: float = 12.0):
                       f"({nth} OpenMP threads)"}
 
 
+def _reference_replicas(w):
+    """The replica count and pool size our arm uses for this workload (for an identical config)."""
+    rb = 1152 if w.fmt == 0 else 656
+    one_pool = w.num_pages * 64 * rb
+    kv = w.attended() * rb
+    need = -(-3 * L2_BYTES // max(kv, 1))
+    rep = 1 if need <= 1 else int(max(1, min(need + 1, 96, POOL_BUDGET // max(one_pool, 1))))
+    return rep, one_pool
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -232,8 +245,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(sec / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "kv_format": "bf16" if w.fmt == 0 else "fp8_mixed",
-                       "description": w.description},
+            "config": workload_config(w, *_reference_replicas(w)),
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": nth, "kind": "oracle",
                              "sample": f"each step: whole requests of the {w.name} workload "
                                        f"(all heads) for ~{budget:.1f} s; {req} requests, {tok} "
@@ -279,6 +291,139 @@ def run_indexer_reference(args):
 # Our arm
 # ----------------------------------------------------------------------------------------------
 
+HEADLINE = "fp8_batch"
+CONFIG_ORDER = ["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse"]
+POOL_BUDGET = 48 << 30        # device bytes the pool replicas of one workload may take
+
+
+def workload_config(w, replicas: int, one_pool: int, world: int = 1) -> dict:
+    """The config object of a workload's line (the same for both arms)."""
+    topk = 0 if w.topk_idx is None else int(w.topk_idx.shape[1])
+    return {"workload": w.name, "B": w.B, "H": w.H, "kv_format": "bf16" if w.fmt == 0 else "fp8_mixed",
+            "description": w.description, "topk": topk, "page_tokens": 64, "scale": w.scale,
+            "step": "cache_append of the tokens each request adds + mla_decode of the batch",
+            "l2": f"inputs larger than L2: {replicas} rotating pool replicas of {one_pool / 2**20:.0f} MiB"
+                  if replicas > 1 else "one pool, larger than L2",
+            "parallelism": f"replicas x{world}"}
+
+
+def _replicas(w, mla, kv_bytes: int) -> int:
+    """Pool replicas whose touched record bytes exceed L2 three times (within POOL_BUDGET)."""
+    one_pool = mla.pool_bytes(w.fmt, w.num_pages)
+    need = -(-3 * L2_BYTES // max(kv_bytes, 1))
+    if need <= 1:
+        return 1
+    return int(max(1, min(need + 1, 96, POOL_BUDGET // max(one_pool, 1))))
+
+
+def _roofline(dw, dec_ms: float, peaks: dict, burst: bool) -> dict:
+    """Roofline of one mla_decode call: its algorithmic bytes (or flops, where the flops at the
+    tensor peak take longer than the bytes at the HBM peak) over its measured duration."""
+    alg_bytes = dw.algorithmic_bytes()
+    flops = dw.flops()
+    dec_s = dec_ms / 1e3
+    tpeak = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    tensor_bound = flops / (tpeak * 1e12) > alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        r = {"bound": "tensor", "achieved": round(flops / dec_s / 1e12, 2), "peak": tpeak, "unit": "TFLOP/s",
+             "frac": round(flops / dec_s / 1e12 / tpeak, 4),
+             "peak_kind": "burst bf16 (graph of back-to-back calls timed alone)" if burst else "sustained bf16"}
+    else:
+        achieved = alg_bytes / dec_s / 1e9
+        r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    r.update({"traffic": _traffic(dw.w.name), "peak_source": peaks["source"], "kernel": "mla_decode call",
+              "ms_per_launch": round(dec_ms, 6), "bytes_per_launch": alg_bytes, "flops_per_launch": flops,
+              "hbm_frac": round(alg_bytes / dec_s / 1e9 / peaks["hbm_gbs"], 4),
+              "tensor_frac": round(flops / dec_s / 1e12 / tpeak, 4)})
+    return r
+
+
+class _Bench:
+    """One workload on the device: pool replicas, CUDA graphs of the step (append + decode) and
+    of back-to-back decode calls, and the timed legs."""
+
+    def __init__(self, name, args, torch, mla, harness, synth, stream, barrier, dist, replicas=None):
+        self.torch, self.mla, self.stream, self.barrier, self.dist = torch, mla, stream, barrier, dist
+        w = synth.make_workload(name)
+        self.w = w
+        kv = int(w.attended() * mla.record_bytes(w.fmt))
+        self.replicas = replicas if replicas is not None else (
+            _replicas(w, mla, kv) if args.replicas == 0 else args.replicas)
+        self.one_pool = mla.pool_bytes(w.fmt, w.num_pages)
+        skip = 1 if w.appended == 0 else w.appended
+        self.dw = dw = harness.DeviceWorkload(w, replicas=self.replicas, prefill_skip_last=skip)
+        dw.alloc_outputs()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):      # eager warm-up (also sets kernel attributes)
+            for r in range(self.replicas):
+                dw.step(r)
+        stream.synchronize()
+        rc = mla.check_status()
+        if rc != 0:
+            raise mla.MlaError(rc, f"warm-up {name}")
+        self.graphs = []
+        for r in range(self.replicas):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                dw.step(r)
+            self.graphs.append(g)
+        self.reps = 20
+        self.dec_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.dec_graph, stream=stream):
+            for i in range(self.reps):
+                dw.decode(i % self.replicas)
+
+    def _timed(self, fn):
+        torch = self.torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            fn()
+            e1.record(self.stream)
+        self.barrier()
+        return e0.elapsed_time(e1)
+
+    def steps(self, k: int, warmup: int) -> float:
+        """ms of exactly k steps after `warmup` untimed ones (max over ranks)."""
+        def run(n):
+            for i in range(n):
+                self.graphs[i % self.replicas].replay()
+        with self.torch.cuda.stream(self.stream):
+            run(warmup)
+        self.barrier()
+        return max_over_ranks(self._timed(lambda: run(k)), self.dist)
+
+    def decode_ms(self, min_seconds: float) -> float:
+        """Average ms of one decode call over graphs of back-to-back calls lasting at least
+        min_seconds (the estimate of one replay sizes the loop)."""
+        one = self._timed(lambda: self.dec_graph.replay())
+        n = max(10, int(min_seconds * 1e3 / max(one, 1e-3)) + 1)
+        def run():
+            for _ in range(n):
+                self.dec_graph.replay()
+        return self._timed(run) / (n * self.reps)
+
+    def cold_decode_ms(self, calls: int = 50) -> float:
+        """Average ms of one decode call with L2 flushed before each (a buffer twice the size of
+        L2 is written between calls; only the call itself is inside the events)."""
+        torch = self.torch
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=self.dw.device)
+        total = 0.0
+        for _ in range(calls):
+            with torch.cuda.stream(self.stream):
+                flush.fill_(1)
+            total += self._timed(lambda: self.dw.decode(0, self.stream))
+        del flush
+        return total / calls
+
+    def free(self):
+        del self.graphs, self.dec_graph, self.dw
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
 def run_ours(args):
     import torch
     import mla_latent_kv_decode_gb300 as mla
@@ -299,124 +444,79 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     mla.load()
-    w = synth.make_workload(args.workload)
-    one_pool = mla.pool_bytes(w.fmt, w.num_pages)
-    replicas = max(1, min(8, -(-3 * L2_BYTES // max(one_pool, 1)) + 1)) if args.replicas == 0 else args.replicas
-    skip = 1 if w.appended == 0 else w.appended
-    dw = harness.DeviceWorkload(w, replicas=replicas, prefill_skip_last=skip)
-    dw.alloc_outputs()
+    peaks = _peaks()
     stream = torch.cuda.Stream()
-    torch.cuda.synchronize()
-
-    # eager warm-up (also sets kernel attributes before capture)
-    with torch.cuda.stream(stream):
-        for r in range(replicas):
-            dw.step(r)
-    stream.synchronize()
-    rc = mla.check_status()
-    if rc != 0:
-        raise mla.MlaError(rc, "warm-up")
-
-    # one graph per replica: append + decode
-    graphs = []
-    for r in range(replicas):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            dw.step(r)
-        graphs.append(g)
-    dec_graphs = []
-    reps = 20
-    for r in range(replicas):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(reps):
-                dw.decode((r + i) % replicas)
-        dec_graphs.append(g)
-
     sampler = ClockSampler(local)
     sampler.start()
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % replicas].replay()
-    barrier()
+    headline = args.workload
+    others = [] if args.no_configs else [n for n in CONFIG_ORDER if n != headline]
 
-    # ---- timed region: exactly K steps ----
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % replicas].replay()
-        ev1.record(stream)
-    barrier()
-    ms = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms, dist)
-
-    # ---- decode-kernel timing (roofline): graphs of `reps` back-to-back decode calls ----
-    n_dec = max(10, min(200, args.steps // reps + 1))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(n_dec):
-            dec_graphs[i % replicas].replay()
-        e1.record(stream)
-    barrier()
-    dec_ms = e0.elapsed_time(e1) / (n_dec * reps)
-    clocks = sampler.stop()
+    # ---- the headline workload: exactly K timed steps, then the decode call alone ----
+    bh = _Bench(headline, args, torch, mla, harness, synth, stream, barrier, dist)
+    w, dw = bh.w, bh.dw
+    ms = bh.steps(args.steps, args.warmup)
+    dec_ms = bh.decode_ms(args.kernel_seconds)
     rc = mla.check_status()
     if rc != 0:
         raise mla.MlaError(rc, "timed region")
-
-    # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, dw, torch, mla, stream, barrier, dist)
 
     kv_bytes = dw.kv_bytes()
-    alg_bytes = dw.algorithmic_bytes()
     flops = dw.flops()
     step_s = ms / 1e3 / args.steps
     value = job_value(world, kv_bytes, step_s) / 1e9
-    peaks = _peaks()
-    dec_s = dec_ms / 1e3
-    achieved = alg_bytes / dec_s / 1e9
-    traffic = _traffic(w.name)
     topk = 0 if w.topk_idx is None else int(w.topk_idx.shape[1])
     launches_per_step = 1 + int(mla.load().mla_decode_launches(w.fmt, w.B, w.H, w.max_seq_len, topk))
-    # the bound of the call: HBM unless its flops at the dense bf16 peak take longer than its
-    # bytes at the HBM peak (the FP8 batch: q stays bf16, the cache bytes halve)
-    tensor_bound = flops / (peaks["bf16_tflops_sustained"] * 1e12) > alg_bytes / (peaks["hbm_gbs"] * 1e9)
-    if tensor_bound:
-        roofline = {"bound": "tensor", "achieved": round(flops / dec_s / 1e12, 2),
-                    "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": round(flops / dec_s / 1e12 / peaks["bf16_tflops_sustained"], 4)}
-    else:
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roofline.update({"traffic": traffic, "peak_source": peaks["source"], "kernel": "mla_decode call",
-                     "ms_per_launch": round(dec_ms, 6), "bytes_per_launch": alg_bytes,
-                     "flops_per_launch": flops})
+    roofline = _roofline(dw, dec_ms, peaks, burst=True)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "kv_format": "bf16" if w.fmt == 0 else "fp8_mixed",
-                   "seq_lens": "uniform in [1024, 8192]" if w.name == "paged_batch" else w.description,
-                   "attended_tokens": w.attended(), "page_tokens": 64, "scale": w.scale,
-                   "step": "cache_append of each request's newest token + mla_decode of the batch",
-                   "l2": f"inputs larger than L2: {replicas} rotating pool replicas of "
-                         f"{one_pool / 2**20:.0f} MiB", "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, bh.replicas, bh.one_pool, world),
         "decode_tokens_per_s": round(world * w.B / step_s, 1),
         "tflops": round(world * flops / step_s / 1e12, 3),
-        "step_frac_of_hbm_roofline": round((alg_bytes / (peaks['hbm_gbs'] * 1e9)) / step_s, 4),
+        "attended_tokens": w.attended(),
         "roofline": roofline,
-        "tensor_util": {"achieved_tflops": round(flops / dec_s / 1e12, 2),
-                        "peak": peaks["bf16_tflops_sustained"],
-                        "frac": round(flops / dec_s / 1e12 / peaks["bf16_tflops_sustained"], 4)},
-        "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step,
     }
+    bh.free()
+
+    # ---- the other workloads: the same legs, reported under "configs" ----
+    configs = {}
+    for name in others:
+        b = _Bench(name, args, torch, mla, harness, synth, stream, barrier, dist)
+        k = max(args.steps, 20)
+        c_ms = b.steps(k, max(args.warmup, 3))
+        c_dec = b.decode_ms(args.kernel_seconds)
+        rc = mla.check_status()
+        if rc != 0:
+            raise mla.MlaError(rc, f"timed region {name}")
+        c_e2e = run_e2e(args, b.dw, torch, mla, stream, barrier, dist)
+        entry = {"ms_per_step": round(c_ms / k, 6), "steps": k,
+                 "value": round(job_value(world, b.dw.kv_bytes(), c_ms / 1e3 / k) / 1e9, 3), "unit": UNIT,
+                 "ms_per_call": round(c_dec, 6),
+                 "decode_tokens_per_s": round(world * b.w.B / (c_dec / 1e3), 1),
+                 "roofline": _roofline(b.dw, c_dec, peaks, burst=True),
+                 "e2e": c_e2e,
+                 "config": workload_config(b.w, b.replicas, b.one_pool, world)}
+        b.free()
+        if name == "tiny_dense":
+            # 4.7 MB fits in L2: the figure above is hot (one pool, back-to-back); cold = L2
+            # flushed before every call
+            hot = _Bench(name, args, torch, mla, harness, synth, stream, barrier, dist, replicas=1)
+            cold_ms = hot.cold_decode_ms()
+            hot_ms = hot.decode_ms(min(args.kernel_seconds, 0.5))
+            entry["l2_hot"] = {"ms_per_call": round(hot_ms, 6), "roofline": _roofline(hot.dw, hot_ms, peaks, True),
+                               "how": "one pool, back-to-back calls (the 4.7 MB cache stays in L2)"}
+            entry["l2_cold"] = {"ms_per_call": round(cold_ms, 6), "roofline": _roofline(hot.dw, cold_ms, peaks, True),
+                                "how": f"{2 * L2_BYTES / 2**20:.0f} MiB written before each call, outside the events"}
+            hot.free()
+        configs[name] = entry
+    if configs:
+        line["configs"] = configs
+    line["clocks"] = sampler.stop()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
@@ -721,7 +821,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="paged_batch",
+    ap.add_argument("--workload", default=HEADLINE,
                     choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse",
                              "indexer_topk"])
     ap.add_argument("--index-batch", type=int, default=64,
@@ -729,6 +829,9 @@ def main(argv=None):
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0 = enough to exceed L2 3x)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--kernel-seconds", type=float, default=1.0,
+                    help="minimum length of the back-to-back decode timing of each workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -45,7 +45,9 @@ typedef enum {
     MLA_ERR_BOUNDS = 2,       /* a kernel met a page/slot index outside the pool             */
     MLA_ERR_TIMEOUT = 3,      /* a bounded wait inside a kernel ran out; the kernel returned */
     MLA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed                           */
-    MLA_ERR_UNSUPPORTED = 5   /* the device is not sm_103 / sm_100-family, or a size limit   */
+    MLA_ERR_UNSUPPORTED = 5,  /* the device is not sm_103 / sm_100-family, or a size limit   */
+    MLA_ERR_RANGE = 6         /* a kernel met a value outside the range its format's arithmetic
+                                 carries (see the FP8 notes of mla_decode)                   */
 } mla_status;
 
 typedef enum {
@@ -116,9 +118,11 @@ int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_l
  * Arithmetic: scores and outputs accumulate in fp32 on the tensor cores.  bf16 records: bf16
  * operands, P rounded once to bf16.  FP8 records: the E4M3 codes enter as f16 (exact), and so
  * does q_lat, converted once per request (exact for |q| in [2^-14, 65504); smaller magnitudes
- * lose low bits, larger ones overflow).  Each 128-dim group's scale multiplies in fp32: on that
- * group's partial score, and on P as f16(P * scale).  The last stays finite for group scales
- * below 255 (absmax below 114,000), because the running max is kept within 2^8 of every P. */
+ * lose low bits).  Each 128-dim group's scale multiplies in fp32: on that group's partial score,
+ * and on P as f16(P * scale), which stays finite for group scales up to 255 (absmax up to
+ * 114,240) because the running max is kept within 2^8 of every P.  Outside those two ranges the
+ * FP8 path does not compute: a q_lat element of magnitude 65520 or more (it would overflow f16),
+ * or a visible record with a group scale above 255 (or not finite), records MLA_ERR_RANGE. */
 mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
                       const void* q_rope, const int32_t* block_table, int32_t max_pages,
                       const int32_t* seq_lens, int32_t max_seq_len, const int32_t* topk_idx,
@@ -139,9 +143,12 @@ mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const vo
  * Arguments, results and errors are those of mla_decode (without workspace/workspace_bytes).
  * Additionally returns MLA_ERR_UNSUPPORTED, before launching anything, when
  * mla_decode_workspace_bytes(fmt, B, H, max_seq_len, topk) exceeds MLA_STATIC_WORKSPACE_BYTES.
+ * The order of the host checks: sizes and scale (MLA_ERR_INVALID), then B == 0 (MLA_OK, nothing
+ * touched), then the size limit (MLA_ERR_UNSUPPORTED), then the pointers (MLA_ERR_INVALID).
  *
- * The first call on a device, with that device current, looks up the array's device address
- * (cudaGetSymbolAddress) and keeps it; make that first call before any stream capture.  All
+ * The first call on a device that passes those checks, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it; make that first call before any
+ * stream capture.  All
  * calls on a device share the one array, which keeps whatever the last call left in it (the
  * decode writes every scratch byte it reads, so nothing has to start at zero).  Calls whose
  * executions overlap on the GPU (on different streams, or from different threads) race on the
@@ -230,7 +237,7 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
  * (section "The score that picks positions": every query keeps at most 2,048 of the positions
  * visible to it, those with the largest scores), written to topk_idx[b] (device int32
  * [B, K]) in increasing position order and padded with -1 past the min(K, seq_lens[b]) picks: directly the topk_idx of mla_decode.  Scores must
- * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, B > 2^30, K < 1 or ld < 0. */
+ * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, B >= 2^30, K < 1 or ld < 0. */
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream);
 

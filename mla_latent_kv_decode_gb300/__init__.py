@@ -24,7 +24,7 @@ HEADS = 128
 PAGE = 64
 
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID", 2: "MLA_ERR_BOUNDS", 3: "MLA_ERR_TIMEOUT",
-          4: "MLA_ERR_CUDA", 5: "MLA_ERR_UNSUPPORTED"}
+          4: "MLA_ERR_CUDA", 5: "MLA_ERR_UNSUPPORTED", 6: "MLA_ERR_RANGE"}
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
 _lock = threading.Lock()

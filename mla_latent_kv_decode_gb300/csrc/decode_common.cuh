@@ -177,6 +177,11 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
+// non-zero when either f16 half is an infinity or a NaN (exponent field all ones)
+__device__ __forceinline__ uint32_t f16x2_inf_or_nan(uint32_t v) {
+    return ((v & 0x7C00u) == 0x7C00u) | ((v & 0x7C000000u) == 0x7C000000u);
+}
+
 // 16 e4m3 codes (OCP 8-bit floating point, bias 7) to 16 f16 values, exactly: every e4m3 value
 // (normal or subnormal, at most 448) is an f16 value.
 __device__ __forceinline__ void e4m3x16_to_f16(const uint4 c, uint32_t (&o)[8]) {

@@ -69,6 +69,7 @@ constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps
 // range of the exchange (bf16 records); 2^8 keeps P s_g within f16 range for s_g < 255 (FP8)
 constexpr float kLazySlackBf16 = 15.0f;
 constexpr float kLazySlackFp8 = 8.0f;
+constexpr float kMaxGroupScale = 255.0f;   // 2^8 * 255 = 65280: P s_g stays a finite f16
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
 constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
@@ -313,14 +314,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             if (kFp8) {
+                // an element that overflows f16 (|q| >= 65520) is outside this path's range
+                uint32_t inf = 0;
 #pragma unroll 8
                 for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
                     uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
                     const uint4 v = *q;
-                    *q = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                    bf16x2_to_f16x2(v.w));
+                    const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                               bf16x2_to_f16x2(v.w));
+                    inf |= f16x2_inf_or_nan(f.x) | f16x2_inf_or_nan(f.y) | f16x2_inf_or_nan(f.z) |
+                           f16x2_inf_or_nan(f.w);
+                    *q = f;
                 }
                 fence_proxy_async_smem();
+                if (__any_sync(0xffffffffu, inf != 0) && lane == 0) record_error(p.ctl, MLA_ERR_RANGE, cu.b);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.q_ready);
@@ -807,9 +814,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int row = at >> 2, c4 = at & 3;
                     if (!valid(row)) rraw = zero;
                     st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
-                    // scales of rows outside the request: zero (their P is zero)
-                    if (at < kT && !valid(at))
-                        *reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + at * 16) = zero;
+                    // scales of rows outside the request: zero (their P is zero); a visible row
+                    // whose group scale is above 255 (or not finite) would overflow f16(P s_g)
+                    if (at < kT) {
+                        uint4* sc = reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + at * 16);
+                        if (!valid(at)) {
+                            *sc = zero;
+                        } else {
+                            const uint4 q = *sc;   // (a NaN fails every comparison)
+                            if (!(__uint_as_float(q.x) <= kMaxGroupScale) || !(__uint_as_float(q.y) <= kMaxGroupScale) ||
+                                !(__uint_as_float(q.z) <= kMaxGroupScale) || !(__uint_as_float(q.w) <= kMaxGroupScale))
+                                record_error(p.ctl, MLA_ERR_RANGE, cj.b);
+                        }
+                    }
                 }
             } else {
                 // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k

@@ -864,7 +864,7 @@ cudaError_t launch_indexer_score(const uint8_t* pool, int64_t num_pages, const _
 
 cudaError_t launch_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int B, int K,
                                int32_t* idx, cudaStream_t st) {
-    topk_select_kernel<<<2 * B, kKThreads, 0, st>>>(scores, ld, seq_lens, K, idx);
+    topk_select_kernel<<<dim3(2u * (unsigned)B), kKThreads, 0, st>>>(scores, ld, seq_lens, K, idx);
     return cudaGetLastError();
 }
 

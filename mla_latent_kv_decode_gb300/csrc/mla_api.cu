@@ -64,6 +64,32 @@ bool fmt_ok(int32_t fmt) { return fmt == MLA_KV_BF16 || fmt == MLA_KV_FP8_MIXED;
 mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 // The kernels are built for sm_103a only; any other device would fail at launch.
 bool device_supported() { return device_cc() == 103; }
+
+// mla_decode's checks of its sizes and scale (no pointer is looked at)
+mla_status decode_shape_status(int32_t fmt, int64_t num_pages, int32_t max_pages, int32_t max_seq_len,
+                               int32_t topk, int32_t B, int32_t H, float scale) {
+    if (!fmt_ok(fmt) || B < 0 || H != kHeads || num_pages < 0 || max_pages < 0 ||
+        max_seq_len < 0 || topk < 0)
+        return MLA_ERR_INVALID;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * kPage) return MLA_ERR_INVALID;
+    return MLA_OK;
+}
+
+// mla_decode's checks of its pointers (null, alignment, top-k list given iff topk > 0)
+mla_status decode_pointer_status(const void* pool, const void* q_lat, const void* q_rope,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 const int32_t* topk_idx, int32_t topk, const void* out,
+                                 const float* lse) {
+    if (!pool || !q_lat || !q_rope || !block_table || !seq_lens || !out || !lse)
+        return MLA_ERR_INVALID;
+    if ((topk_idx == nullptr) != (topk == 0)) return MLA_ERR_INVALID;
+    if (!aligned(pool, 128) || !aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(out, 16) ||
+        !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+        (topk_idx && !aligned(topk_idx, 4)))
+        return MLA_ERR_INVALID;
+    return MLA_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -125,7 +151,8 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
 
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream) {
-    if (B < 0 || B > (1 << 30) || K < 1 || ld < 0) return MLA_ERR_INVALID;   // two CTAs a request
+    // two CTAs a request: 2 B must stay below 2^31 (a grid dimension and an int)
+    if (B < 0 || B >= (1 << 30) || K < 1 || ld < 0) return MLA_ERR_INVALID;
     if (B == 0) return MLA_OK;
     if (!scores || !seq_lens || !topk_idx) return MLA_ERR_INVALID;
     if (!aligned(scores, 4) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4)) return MLA_ERR_INVALID;
@@ -154,20 +181,10 @@ mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const vo
                       const int32_t* seq_lens, int32_t max_seq_len, const int32_t* topk_idx,
                       int32_t topk, int32_t B, int32_t H, float scale, void* out, float* lse,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (!fmt_ok(fmt) || B < 0 || H != kHeads || num_pages < 0 || max_pages < 0 ||
-        max_seq_len < 0 || topk < 0)
-        return MLA_ERR_INVALID;
-    if (!(scale > 0.0f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
-    if ((int64_t)max_seq_len > (int64_t)max_pages * kPage) return MLA_ERR_INVALID;
-    if (B == 0) return MLA_OK;
-    if (!pool || !q_lat || !q_rope || !block_table || !seq_lens || !out || !lse)
-        return MLA_ERR_INVALID;
-    if (topk_idx == nullptr && topk != 0) return MLA_ERR_INVALID;
-    if (topk_idx != nullptr && topk == 0) return MLA_ERR_INVALID;
-    if (!aligned(pool, 128) || !aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(out, 16) ||
-        !aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
-        (topk_idx && !aligned(topk_idx, 4)))
-        return MLA_ERR_INVALID;
+    mla_status st = decode_shape_status(fmt, num_pages, max_pages, max_seq_len, topk, B, H, scale);
+    if (st != MLA_OK || B == 0) return st;
+    st = decode_pointer_status(pool, q_lat, q_rope, block_table, seq_lens, topk_idx, topk, out, lse);
+    if (st != MLA_OK) return st;
     DevCtl* ctl = device_ctl();
     if (!ctl) return MLA_ERR_CUDA;
     if (!device_supported()) return MLA_ERR_UNSUPPORTED;
@@ -228,9 +245,15 @@ mla_status mla_decode_noalloc(int32_t fmt, const void* pool, int64_t num_pages, 
                               const int32_t* seq_lens, int32_t max_seq_len,
                               const int32_t* topk_idx, int32_t topk, int32_t B, int32_t H,
                               float scale, void* out, float* lse, cudaStream_t stream) {
-    if (B > 0 && H == kHeads && fmt_ok(fmt) && max_seq_len >= 0 && topk >= 0 &&
-        mla_decode_workspace_bytes(fmt, B, H, max_seq_len, topk) > MLA_STATIC_WORKSPACE_BYTES)
+    // the checks of mla_decode first, and the size limit before the pointers, so that an
+    // over-size call is refused whatever it points at; the array is looked up only when a
+    // launch follows
+    mla_status st = decode_shape_status(fmt, num_pages, max_pages, max_seq_len, topk, B, H, scale);
+    if (st != MLA_OK || B == 0) return st;
+    if (mla_decode_workspace_bytes(fmt, B, H, max_seq_len, topk) > MLA_STATIC_WORKSPACE_BYTES)
         return MLA_ERR_UNSUPPORTED;
+    st = decode_pointer_status(pool, q_lat, q_rope, block_table, seq_lens, topk_idx, topk, out, lse);
+    if (st != MLA_OK) return st;
     void* ws = static_workspace_for_current_device();
     if (!ws) return MLA_ERR_CUDA;
     return mla_decode(fmt, pool, num_pages, q_lat, q_rope, block_table, max_pages, seq_lens,
@@ -274,6 +297,7 @@ const char* mla_status_string(mla_status s) {
         case MLA_ERR_TIMEOUT: return "bounded wait ran out inside a kernel";
         case MLA_ERR_CUDA: return "CUDA error";
         case MLA_ERR_UNSUPPORTED: return "unsupported device or size";
+        case MLA_ERR_RANGE: return "value outside the range of the format's arithmetic";
     }
     return "unknown status";
 }

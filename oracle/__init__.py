@@ -62,7 +62,7 @@ def _load():
             lib.oracle_attend.restype = None
             lib.oracle_record_bytes.argtypes = [ctypes.c_int]
             lib.oracle_record_bytes.restype = i64
-            lib.oracle_cache_append.argtypes = [ctypes.c_int, P, i64, P, P, P, i64]
+            lib.oracle_cache_append.argtypes = [ctypes.c_int, P, i64, P, P, P, i64, ctypes.c_int]
             lib.oracle_cache_append.restype = i64
             lib.oracle_read_record.argtypes = [ctypes.c_int, P, i64, P, P]
             lib.oracle_read_record.restype = None
@@ -84,6 +84,12 @@ def _load():
             lib.oracle_indexer_scores.restype = ctypes.c_int
             lib.oracle_topk.argtypes = [P, i64, P, i32, i32, P, ctypes.c_int]
             lib.oracle_topk.restype = None
+            lib.oracle_value_project.argtypes = [P, P, P] + [ctypes.c_int] * 5 + [P, P, ctypes.c_int]
+            lib.oracle_value_project.restype = None
+            lib.oracle_merge_value_output.argtypes = [P, P] + [ctypes.c_int] * 4 + [P, ctypes.c_int]
+            lib.oracle_merge_value_output.restype = None
+            lib.oracle_project_merged.argtypes = [P, P] + [ctypes.c_int] * 4 + [P, ctypes.c_int]
+            lib.oracle_project_merged.restype = None
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -157,10 +163,12 @@ def new_pool(fmt: int, num_pages: int) -> np.ndarray:
 
 
 def cache_append(fmt: int, pool: np.ndarray, c_kv: np.ndarray, k_rope: np.ndarray,
-                 slot: np.ndarray) -> int:
+                 slot: np.ndarray, nthreads: int = 0) -> int:
     """Write T tokens (bf16 bits c_kv[T,512], k_rope[T,64]) into ``pool`` at ``slot``.
 
-    Returns the number of rows whose slot lies outside the pool (not written).
+    Returns the number of rows whose slot lies outside the pool (not written).  Large appends
+    whose non-negative slots are all distinct are spread over ``nthreads`` threads (all host
+    threads for 0); otherwise rows are written one after another, in order.
     """
     c_kv = np.ascontiguousarray(c_kv, dtype=np.uint16)
     k_rope = np.ascontiguousarray(k_rope, dtype=np.uint16)
@@ -168,8 +176,13 @@ def cache_append(fmt: int, pool: np.ndarray, c_kv: np.ndarray, k_rope: np.ndarra
     T = slot.shape[0]
     assert c_kv.shape == (T, D_C) and k_rope.shape == (T, D_R)
     num_pages = pool.size // (PAGE * record_bytes(fmt))
+    nth = 1
+    if T >= 4096:
+        live = slot[slot >= 0]
+        if np.unique(live).size == live.size:
+            nth = nthreads if nthreads > 0 else max_threads()
     return int(_load().oracle_cache_append(fmt, _ptr(pool), num_pages, _ptr(c_kv), _ptr(k_rope),
-                                           _ptr(slot), T))
+                                           _ptr(slot), T, nth))
 
 
 def read_record(fmt: int, pool: np.ndarray, slot: int):
@@ -305,3 +318,50 @@ def topk(scores: np.ndarray, seq_lens: np.ndarray, K: int, nthreads: int = 0) ->
     idx = np.empty((B, K), dtype=np.int32)
     _load().oracle_topk(_ptr(scores), ld, _ptr(seq_lens), B, K, _ptr(idx), nthreads)
     return idx
+
+
+# ------------------------------------------------------------------------------------------
+# Value up-projection and output projection ("DeepSeek's KV Cache: From 3.9 MB to 890 B per
+# Token", section "Computing without expanding Key and Value", Fig. 6 (2) and (3)).
+# ------------------------------------------------------------------------------------------
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def value_project(u: np.ndarray, w_uv: np.ndarray, w_o: np.ndarray, nthreads: int = 0):
+    """Fig. 6 (2): Z_h = U_h W^UV_h and Y = sum_h Z_h W^O_h, in fp64.
+
+    u [B,H,dc], w_uv [H,dc,dv] (W^UV_h: dc rows, dv columns), w_o [H*dv, D] (W^O; rows h*dv ..
+    h*dv + dv - 1 are W^O_h).  Returns (z [B,H,dv], y [B,D])."""
+    u, w_uv, w_o = _f64(u), _f64(w_uv), _f64(w_o)
+    B, H, dc = u.shape
+    dv = w_uv.shape[2]
+    D = w_o.shape[1]
+    assert w_uv.shape == (H, dc, dv) and w_o.shape == (H * dv, D)
+    z = np.empty((B, H, dv))
+    y = np.empty((B, D))
+    _load().oracle_value_project(_ptr(u), _ptr(w_uv), _ptr(w_o), B, H, dc, dv, D, _ptr(z), _ptr(y), nthreads)
+    return z, y
+
+
+def merge_value_output(w_uv: np.ndarray, w_o: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """Fig. 6 (3): the pre-merged weight What^O_h = W^UV_h W^O_h, [H, dc, D] in fp64."""
+    w_uv, w_o = _f64(w_uv), _f64(w_o)
+    H, dc, dv = w_uv.shape
+    D = w_o.shape[1]
+    assert w_o.shape == (H * dv, D)
+    w_hat = np.empty((H, dc, D))
+    _load().oracle_merge_value_output(_ptr(w_uv), _ptr(w_o), H, dc, dv, D, _ptr(w_hat), nthreads)
+    return w_hat
+
+
+def project_merged(u: np.ndarray, w_hat: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """Y = sum_h U_h What^O_h (Fig. 6 (3)); u [B,H,dc], w_hat [H,dc,D] -> y [B,D]."""
+    u, w_hat = _f64(u), _f64(w_hat)
+    B, H, dc = u.shape
+    D = w_hat.shape[2]
+    assert w_hat.shape == (H, dc, D)
+    y = np.empty((B, D))
+    _load().oracle_project_merged(_ptr(u), _ptr(w_hat), B, H, dc, D, _ptr(y), nthreads)
+    return y

@@ -156,11 +156,17 @@ int64_t oracle_record_bytes(int fmt) {
  * largest magnitude maps onto the largest finite E4M3 value):
  *     amax = max |x| (fp32),  s_g = fl32(amax / 448),  code = E4M3_RNE_satfinite(fl32(x / s_g)),
  *     amax == 0 gives s_g = 0 and all-zero codes;  the 64 rope values stay bf16.
- * Returns the number of rows whose slot is outside the pool (those rows are not written). */
+ * Returns the number of rows whose slot is outside the pool (those rows are not written).
+ * Rows are independent; with nthreads > 1 they are written by that many threads, which the
+ * caller may ask for only when no two rows share a slot (the row order then cannot matter). */
 int64_t oracle_cache_append(int fmt, uint8_t* pool, int64_t num_pages, const uint16_t* c_kv,
-                            const uint16_t* k_rope, const int32_t* slot, int64_t T) {
+                            const uint16_t* k_rope, const int32_t* slot, int64_t T, int nthreads) {
     int64_t rb = oracle_record_bytes(fmt);
     int64_t bad = 0;
+#ifdef _OPENMP
+    if (nthreads > 1) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static) reduction(+ : bad) if (nthreads > 1)
+#endif
     for (int64_t i = 0; i < T; ++i) {
         int64_t sl = slot[i];
         if (sl < 0) continue;
@@ -273,12 +279,17 @@ int oracle_mla_decode(int fmt, const uint8_t* pool, int64_t num_pages,
         }
         double* K = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORACLE_DK);
         int bad = 0;
+        /* each row of K is read on its own: threads split the rows, nothing else */
+#ifdef _OPENMP
+        if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static) reduction(| : bad)
+#endif
         for (int64_t j = 0; j < n; ++j) {
             int64_t t = pos[j];
             int64_t pg = t / ORACLE_PAGE;
-            if (pg >= max_pages) { bad = 1; break; }
+            if (pg >= max_pages) { bad = 1; continue; }
             int64_t page = block_table[(int64_t)b * max_pages + pg];
-            if (page < 0 || page >= num_pages) { bad = 1; break; }
+            if (page < 0 || page >= num_pages) { bad = 1; continue; }
             oracle_read_record(fmt, pool, page * ORACLE_PAGE + t % ORACLE_PAGE,
                                K + j * ORACLE_DK, K + j * ORACLE_DK + ORACLE_DC);
         }
@@ -334,6 +345,82 @@ void oracle_combine(const float* o_part, const float* lse_part, int32_t S, int64
         for (int64_t j = 0; j < D; ++j) out[j] += w * (double)o_part[(int64_t)i * D + j];
     }
     *lse = L;
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Value up-projection and output projection ([KV] "Computing without expanding Key and      */
+/* Value", Fig. 6)                                                                           */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Fig. 6 (2), "Absorb": the decode output U_h of head h (the probability-weighted sum of the
+ * cached latent rows, dc wide) is multiplied by W^UV_h, which gives head h's value output
+ * Z_h = U_h W^UV_h (dv wide), and then by W^O_h, the block of dv rows of the output weight W^O
+ * that belongs to head h; the heads' contributions Y_h = Z_h W^O_h add up to the layer output
+ * Y (Fig. 4 (2): the heads' outputs, concatenated, times W^O).
+ *   u    [B][H][dc]
+ *   w_uv [H][dc][dv]   W^UV_h as in the figure: dc rows, dv columns
+ *   w_o  [H*dv][D]     W^O; row h*dv + j is row j of W^O_h
+ *   z    [B][H][dv]    out: Z_h
+ *   y    [B][D]        out: Y = sum_h Z_h W^O_h
+ * Threads (nthreads > 0) split the requests b; each output element is one plain sum. */
+void oracle_value_project(const double* u, const double* w_uv, const double* w_o, int B, int H, int dc,
+                          int dv, int D, double* z, double* y, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+#endif
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h)
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int k = 0; k < dc; ++k)
+                    acc += u[((int64_t)b * H + h) * dc + k] * w_uv[((int64_t)h * dc + k) * dv + j];
+                z[((int64_t)b * H + h) * dv + j] = acc;
+            }
+        for (int n = 0; n < D; ++n) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                for (int j = 0; j < dv; ++j)
+                    acc += z[((int64_t)b * H + h) * dv + j] * w_o[((int64_t)h * dv + j) * D + n];
+            y[(int64_t)b * D + n] = acc;
+        }
+    }
+}
+
+/* Fig. 6 (3), "Pre-merge the weights": W^UV_h and W^O_h are merged ahead of time into
+ * What^O_h = W^UV_h W^O_h (dc rows, D columns).   w_hat [H][dc][D]. */
+void oracle_merge_value_output(const double* w_uv, const double* w_o, int H, int dc, int dv, int D,
+                               double* w_hat, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+#endif
+    for (int h = 0; h < H; ++h)
+        for (int k = 0; k < dc; ++k)
+            for (int n = 0; n < D; ++n) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j)
+                    acc += w_uv[((int64_t)h * dc + k) * dv + j] * w_o[((int64_t)h * dv + j) * D + n];
+                w_hat[((int64_t)h * dc + k) * D + n] = acc;
+            }
+}
+
+/* Y = sum_h U_h What^O_h with the pre-merged weight (Fig. 6 (3)).  u [B][H][dc],
+ * w_hat [H][dc][D], y [B][D]. */
+void oracle_project_merged(const double* u, const double* w_hat, int B, int H, int dc, int D, double* y,
+                           int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+#endif
+    for (int b = 0; b < B; ++b)
+        for (int n = 0; n < D; ++n) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                for (int k = 0; k < dc; ++k)
+                    acc += u[((int64_t)b * H + h) * dc + k] * w_hat[((int64_t)h * dc + k) * D + n];
+            y[(int64_t)b * D + n] = acc;
+        }
 }
 
 /* ---------------------------------------------------------------------------------------- */

@@ -98,3 +98,39 @@ def assert_decode_close(out_gpu: np.ndarray, lse_gpu: np.ndarray, out_ref: np.nd
     assert lerr.max() <= LSE_ABS, f"{what}: max |lse err| {lerr.max():.3e}"
     rel = np.linalg.norm(out_gpu[ne] - out_ref[ne], axis=1) / np.linalg.norm(out_ref[ne], axis=1)
     assert rel.max() <= OUT_REL, f"{what}: max normwise rel err {rel.max():.3e}"
+
+
+def twin_rows(w: synth.Workload, b: int, t0: int, t1: int):
+    """bf16 bits (c_kv [n,512], k_rope [n,64]) of request b's positions t0..t1-1, drawn on the
+    device by the generator's twin (bit-exact with synth.kv_rows) and copied to the host: the
+    same inputs the host recipe gives, at a speed that suits the full-size workloads."""
+    import torch
+    n = t1 - t0
+    c = torch.empty((n, synth.D_C), dtype=torch.bfloat16, device="cuda")
+    r = torch.empty((n, synth.D_R), dtype=torch.bfloat16, device="cuda")
+    base = (b * synth.KV_ROW_STRIDE + t0) * synth.D_K
+    s = torch.cuda.current_stream().cuda_stream
+    synth.gpu_normal_bf16(c.data_ptr(), n, w.seed, synth.STREAM_KV, base, synth.D_C, synth.D_K, s)
+    synth.gpu_normal_bf16(r.data_ptr(), n, w.seed, synth.STREAM_KV, base + synth.D_C, synth.D_R,
+                          synth.D_K, s)
+    return (c.cpu().view(torch.int16).numpy().view(np.uint16),
+            r.cpu().view(torch.int16).numpy().view(np.uint16))
+
+
+def twin_rows_at(w: synth.Workload, b: int, positions: np.ndarray):
+    """twin_rows at arbitrary sorted positions of request b (drawn in ranges, then picked)."""
+    positions = np.asarray(positions, dtype=np.int64)
+    c = np.empty((positions.size, synth.D_C), dtype=np.uint16)
+    r = np.empty((positions.size, synth.D_R), dtype=np.uint16)
+    if positions.size == 0:
+        return c, r
+    span = 1 << 15
+    for t0 in range(0, int(positions.max()) + 1, span):
+        sel = np.nonzero((positions >= t0) & (positions < t0 + span))[0]
+        if sel.size == 0:
+            continue
+        t1 = int(positions[sel].max()) + 1
+        cc, rr = twin_rows(w, b, t0, t1)
+        c[sel] = cc[positions[sel] - t0]
+        r[sel] = rr[positions[sel] - t0]
+    return c, r

@@ -9,7 +9,8 @@ import pytest
 import oracle
 import mla_latent_kv_decode_gb300 as mla
 from mla_latent_kv_decode_gb300 import harness, synth
-from parity_util import (assert_decode_close, oracle_decode_pairs, oracle_pool)
+from parity_util import (assert_decode_close, oracle_decode_pairs, oracle_pool, twin_rows,
+                         twin_rows_at)
 
 pytestmark = pytest.mark.gpu
 
@@ -188,55 +189,77 @@ def test_e4m3_conversion_exhaustive(torch):
 
 
 # --------------------------------------------------------------------------------------------
-# The five workloads at full size, in the launch configuration the benchmark times; the oracle
-# computes sampled (request, head) outputs one by one.
+# The five workloads at full size, in the launch configuration the benchmark times: every
+# (request, head) output against the oracle, and the cache bytes bit-exact against the oracle's
+# encoder (the whole pool for the dense workloads, every listed record for the top-k one).  The
+# rows come from the input generator's device twin (bit-exact with the host recipe, checked by
+# test_generator_device_twin_is_bit_exact) and are copied to the host for the oracle.
 # --------------------------------------------------------------------------------------------
 
-def _sampled(torch, name, pairs):
+def _full_size(torch, name):
     w = synth.make_workload(name)
     dw = harness.DeviceWorkload(w)
     dw.append()
     out, lse = dw.decode()
     assert mla.check_status() == 0
-    # sampled cache records are bit-exact against the oracle encoder
-    rng = np.random.default_rng(0)
-    pool = dw.pools[0]
+    go = out.float().cpu().numpy().reshape(-1, 512)
+    gl = lse.cpu().numpy().reshape(-1)
+    assert np.isfinite(go).all() and np.isfinite(gl).all()   # every request sees positions
+    ql, qr = w.queries()
     rb = mla.record_bytes(w.fmt)
-    for b in {p[0] for p in pairs}:
-        ts = rng.integers(0, int(w.seq_lens[b]), 4)
-        c, r = synth.kv_rows_at(w.seed, b, ts)
-        ref = oracle.new_pool(w.fmt, 1)
-        oracle.cache_append(w.fmt, ref, c, r, np.arange(len(ts), dtype=np.int32))
-        for i, t in enumerate(ts):
-            s = int(w.block_table[b, t // 64]) * 64 + int(t) % 64
-            got = pool[s * rb:(s + 1) * rb].cpu().numpy()
-            assert np.array_equal(got, ref[i * rb:(i + 1) * rb]), f"{name}: record ({b},{t})"
-    ro, rl = oracle_decode_pairs(w, pairs)
-    go = np.stack([out[b, h].float().cpu().numpy() for b, h in pairs])
-    gl = np.array([float(lse[b, h]) for b, h in pairs])
-    assert_decode_close(go, gl, ro, rl, name)
-    # all outputs finite, all lse finite (every request sees positions)
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    if w.topk_idx is None:
+        ref_pool = oracle.new_pool(w.fmt, w.num_pages)
+        for b in range(w.B):
+            n = int(w.seq_lens[b])
+            for t0 in range(0, n, 1 << 15):
+                t1 = min(n, t0 + (1 << 15))
+                c, r = twin_rows(w, b, t0, t1)
+                assert oracle.cache_append(w.fmt, ref_pool, c, r, w.slots(b, t0, t1)) == 0
+        assert np.array_equal(dw.pools[0].cpu().numpy(), ref_pool), f"{name}: pool bytes differ"
+        del dw
+        ro, rl, _ = oracle.mla_decode(w.fmt, ref_pool, ql, qr, w.block_table, w.seq_lens, w.scale)
+        assert_decode_close(go, gl, ro, rl, name)
+        return
+    # top-k: each request's listed records (compared with the device pool's bytes at their slots)
+    # on a compact oracle pool of their own
+    pool_dev = dw.pools[0]
+    for b in range(w.B):
+        idx = w.topk_idx[b]
+        vis = np.unique(idx[(idx >= 0) & (idx < w.seq_lens[b])]).astype(np.int64)
+        c, r = twin_rows_at(w, b, vis)
+        pages = (int(w.seq_lens[b]) + 63) // 64
+        pool = oracle.new_pool(w.fmt, pages)
+        assert oracle.cache_append(w.fmt, pool, c, r, vis.astype(np.int32)) == 0
+        slots = torch.from_numpy(w.slots(b, 0, 0) if vis.size == 0 else
+                                 (w.block_table[b, vis // 64].astype(np.int64) * 64 + vis % 64)).cuda()
+        got = pool_dev.view(-1, rb)[slots].cpu().numpy()
+        want = pool.reshape(-1, rb)[vis]
+        assert np.array_equal(got, want), f"{name}: records of request {b} differ"
+        bt = np.arange(pages, dtype=np.int32)[None]
+        ro, rl, _ = oracle.mla_decode(w.fmt, pool, ql[b:b + 1], qr[b:b + 1], bt, w.seq_lens[b:b + 1],
+                                      w.scale, topk_idx=w.topk_idx[b:b + 1])
+        assert_decode_close(go[b * w.H:(b + 1) * w.H], gl[b * w.H:(b + 1) * w.H], ro, rl,
+                            f"{name} request {b}")
 
 
 def test_full_tiny_dense(torch):
-    _sampled(torch, "tiny_dense", [(0, 0), (0, 77), (0, 127)])
+    _full_size(torch, "tiny_dense")
 
 
 def test_full_paged_batch(torch):
-    _sampled(torch, "paged_batch", [(0, 3), (13, 64), (31, 127), (31, 0)])
+    _full_size(torch, "paged_batch")
 
 
 def test_full_long_context(torch):
-    _sampled(torch, "long_context", [(0, 0), (0, 50), (0, 127)])
+    _full_size(torch, "long_context")
 
 
 def test_full_fp8_batch(torch):
-    _sampled(torch, "fp8_batch", [(0, 1), (40, 90), (63, 127)])
+    _full_size(torch, "fp8_batch")
 
 
 def test_full_topk_sparse(torch):
-    _sampled(torch, "topk_sparse", [(0, 5), (33, 64), (63, 127)])
+    _full_size(torch, "topk_sparse")
 
 
 def test_zero_queries_average_the_latents(torch):

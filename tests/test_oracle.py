@@ -621,3 +621,65 @@ def test_topk_selection():
             assert np.all(np.diff(picks) > 0) and np.all(picks < seq[b])
             assert picks.size == min(K, int(seq[b]))
     assert np.array_equal(oracle.topk(sc, seq, 64)[2], np.arange(64))
+
+
+# ------------------------------------------------------------------------------------------
+# Value up-projection and output projection ("DeepSeek's KV Cache", section "Computing without
+# expanding Key and Value", Fig. 6 (1), (2), (3))
+# ------------------------------------------------------------------------------------------
+
+def test_value_project_hand_example():
+    """Two heads, dc = 2, dv = 1, D = 2, worked by hand:
+    U_0 = [1, 2], U_1 = [3, -1]; W^UV_0 = [[1], [1]], W^UV_1 = [[2], [0]]
+      -> Z_0 = 1 + 2 = 3, Z_1 = 6 + 0 = 6;
+    W^O_0 = [[1, 0]], W^O_1 = [[0, -1]] -> Y = 3 [1, 0] + 6 [0, -1] = [3, -6].
+    Pre-merged: What^O_0 = [[1, 0], [1, 0]], What^O_1 = [[0, -2], [0, 0]]."""
+    u = np.array([[[1.0, 2.0], [3.0, -1.0]]])
+    w_uv = np.array([[[1.0], [1.0]], [[2.0], [0.0]]])
+    w_o = np.array([[1.0, 0.0], [0.0, -1.0]])
+    z, y = oracle.value_project(u, w_uv, w_o)
+    assert z.reshape(-1).tolist() == [3.0, 6.0]
+    assert y.reshape(-1).tolist() == [3.0, -6.0]
+    w_hat = oracle.merge_value_output(w_uv, w_o)
+    assert w_hat.tolist() == [[[1.0, 0.0], [1.0, 0.0]], [[0.0, -2.0], [0.0, 0.0]]]
+    assert oracle.project_merged(u, w_hat).reshape(-1).tolist() == [3.0, -6.0]
+
+
+def test_value_project_three_orders_agree():
+    """Fig. 6: (1) expand V_h = C W^UV_h and weight it by the probabilities, (2) weight the
+    latent rows first (U_h) and multiply by W^UV_h and W^O_h, (3) multiply U_h by the pre-merged
+    What^O_h -- the same layer output (1e-9 relative in fp64).  (1) goes through the attention
+    core with the expanded values; the output weight of each head is its block of rows of W^O."""
+    rng = np.random.default_rng(61)
+    H, dc, dv, D, n, B = 3, 16, 4, 10, 9, 2
+    C = rng.normal(size=(n, dc))
+    w_uv = rng.normal(size=(H, dc, dv)) / 4
+    w_o = rng.normal(size=(H * dv, D)) / 2
+    q = rng.normal(size=(B, H, dc))
+    U = np.empty((B, H, dc))
+    Zx = np.empty((B, H, dv))
+    for b in range(B):
+        for h in range(H):
+            U[b, h], _ = oracle.attend(q[b, h], C, C, 0.3)
+            Zx[b, h], _ = oracle.attend(q[b, h], C, C @ w_uv[h], 0.3)
+    Y1 = np.stack([sum(Zx[b, h] @ w_o[h * dv:(h + 1) * dv] for h in range(H)) for b in range(B)])
+    z2, Y2 = oracle.value_project(U, w_uv, w_o)
+    Y3 = oracle.project_merged(U, oracle.merge_value_output(w_uv, w_o))
+    scale = np.abs(Y1).max()
+    assert np.abs(z2 - Zx).max() <= 1e-9 * np.abs(Zx).max()
+    assert np.abs(Y2 - Y1).max() <= 1e-9 * scale
+    assert np.abs(Y3 - Y1).max() <= 1e-9 * scale
+    # a head's rows of W^O taken from the wrong block change the result
+    w_o_swapped = np.concatenate([w_o[dv:2 * dv], w_o[:dv], w_o[2 * dv:]])
+    _, Yw = oracle.value_project(U, w_uv, w_o_swapped)
+    assert np.abs(Yw - Y1).max() > 1e-3 * scale
+
+
+def test_value_project_of_the_worked_example_output():
+    """With identity up-projection and output weights, the layer output is the worked example's
+    attention output ("What attention stores, and what DeepSeek changed", section "The four
+    numbers attention works with": out_3 = [0.610, 1.171, 0.610])."""
+    g, d, K, V, q = _worked()
+    out, _ = oracle.attend(q, K, V, 1.0 / math.sqrt(d))
+    _, y = oracle.value_project(out.reshape(1, 1, d), np.eye(d).reshape(1, d, d), np.eye(d))
+    np.testing.assert_allclose(y.reshape(-1), g["out"], atol=6e-4)
