@@ -424,6 +424,94 @@ class _Bench:
         self.torch.cuda.empty_cache()
 
 
+def measure_value_project(args, torch, mla, harness, stream, barrier, peaks, merged=False):
+    """The value up-projection and output projection of a decode batch (B=64, 128 heads, d_v 128,
+    hidden 5,120; Fig. 6 (2), or (3) with the merged weight): the call alone over >= the kernel
+    leg's seconds of back-to-back calls alternating two weight replicas (370 MB, or 1.3 GB merged,
+    larger than L2), and end to end with U copied in from pinned host memory and Y copied back."""
+    B, H, D = 64, 128, 5120
+    reps = [harness.ProjInputs(B, H, D, seed=0x4D4C41 + 7 + i, merged=merged) for i in range(2)]
+    z = torch.empty((2, B, H * mla.D_V), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((B, D), dtype=torch.bfloat16, device="cuda")
+
+    def call(p):
+        if merged:
+            mla.value_project_merged(p.u, p.w_hat_t, y=y)
+        else:
+            mla.value_project(p.u, p.w_uv_t, p.w_o_t, z=z, y=y)
+
+    with torch.cuda.stream(stream):
+        for p in reps:
+            call(p)
+    stream.synchronize()
+    rc = mla.check_status()
+    if rc != 0:
+        raise mla.MlaError(rc, "value projection warm-up")
+    n_in = 20
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_in):
+            call(reps[i % 2])
+
+    def timed(fn):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1)
+
+    one = timed(g.replay)
+    n = max(10, int(args.kernel_seconds * 1e3 / max(one, 1e-3)) + 1)
+
+    def loop():
+        for _ in range(n):
+            g.replay()
+    ms = timed(loop) / (n * n_in)
+    # end to end: U in from pinned host memory, the call, Y back, each step
+    u_h = reps[0].u.cpu().pin_memory()
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e_step(i):
+        p = reps[i % 2]
+        p.u.copy_(u_h, non_blocking=True)
+        call(p)
+        y_h.copy_(y, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+    barrier()
+    k = 50
+
+    def e2e_loop():
+        for i in range(k):
+            e2e_step(i)
+    e2e_ms = timed(e2e_loop) / k
+    rc = mla.check_status()
+    if rc != 0:
+        raise mla.MlaError(rc, "value projection timed region")
+    p = reps[0]
+    alg = p.algorithmic_bytes()
+    flops = p.flops()
+    gbs = alg / (ms / 1e3) / 1e9
+    entry = {"ms_per_call": round(ms, 6), "B": B, "H": H, "d_v": mla.D_V, "D": D,
+             "form": "merged weight (Fig. 6 (3))" if merged else "two products (Fig. 6 (2))",
+             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                          "peak_source": peaks["source"], "bytes_per_launch": alg, "flops_per_launch": flops,
+                          "tensor_frac": round(flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)},
+             "e2e": {"value": round(alg / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                     "h2d_bytes_per_step": int(u_h.numel() * 2), "d2h_bytes_per_step": int(y_h.numel() * 2),
+                     "steps": k},
+             "l2": "two weight replicas alternate (inputs larger than L2)"}
+    del reps, z, y, g
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
     import torch
     import mla_latent_kv_decode_gb300 as mla
@@ -514,6 +602,10 @@ def run_ours(args):
                                 "how": f"{2 * L2_BYTES / 2**20:.0f} MiB written before each call, outside the events"}
             hot.free()
         configs[name] = entry
+    if not args.no_configs:
+        configs["value_project"] = measure_value_project(args, torch, mla, harness, stream, barrier, peaks)
+        configs["value_project_merged"] = measure_value_project(args, torch, mla, harness, stream, barrier, peaks,
+                                                                merged=True)
     if configs:
         line["configs"] = configs
     line["clocks"] = sampler.stop()

@@ -241,6 +241,43 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Value up-projection and output projection of the decode output ("DeepSeek's KV Cache: From
+ * 3.9 MB to 890 B per Token", section "Computing without expanding Key and Value", Fig. 6).
+ * mla_decode returns per head the weighted latent sum U_h (512); what the layer adds to the
+ * residual stream is Y = sum_h (U_h W^UV_h) W^O_h, where W^UV_h (512 x 128) rebuilds head h's
+ * value width and W^O_h is head h's block of 128 rows of the output weight W^O (Fig. 6 (2)), or
+ * Y = sum_h U_h What^O_h with the pre-merged What^O_h = W^UV_h W^O_h (512 x D, Fig. 6 (3)).
+ * Weights are passed transposed, in the [output, input] layout, bf16.
+ * ------------------------------------------------------------------------------------------ */
+#define MLA_D_V 128
+
+/* Fig. 6 (2).
+ *   u      : device bf16 [B, H, 512]    U, e.g. mla_decode's out.
+ *   w_uv_t : device bf16 [H, 128, 512]  row j of head h is column j of W^UV_h.
+ *   w_o_t  : device bf16 [D, H * 128]   row n is column n of W^O (columns h * 128 .. h * 128 + 127
+ *                                        of a row belong to head h).
+ *   z      : device bf16 [2, B, H * 128], written: Z_h = U_h W^UV_h of every head, heads side by
+ *            side, as two planes whose sum carries Z: z[0] = bf16(Z), z[1] = bf16(Z - z[0]) (about
+ *            16 significant bits).  It is the intermediate of the two products.
+ *   y      : device bf16 [B, D]  Y.
+ * Products: bf16 operands, fp32 accumulation on the tensor cores; Z enters the second product as
+ * its two planes, whose two fp32 results are added; Y is rounded once to bf16.  The second
+ * product's reduction over H * 128 is split across up to 8 CTAs whose fp32 partial sums are added
+ * in a fixed order.  B >= 0 (B = 0 does nothing), 1 <= H <= 65535, D a positive multiple of 128,
+ * B <= 8,388,480; pointers 16-byte aligned; otherwise MLA_ERR_INVALID. */
+mla_status mla_value_project(const void* u, const void* w_uv_t, const void* w_o_t, int32_t B, int32_t H,
+                             int32_t D, void* z, void* y, cudaStream_t stream);
+
+/* Fig. 6 (3), with the merged weight.
+ *   u       : device bf16 [B, H, 512].
+ *   w_hat_t : device bf16 [D, H * 512]  row n, columns h * 512 .. h * 512 + 511, is column n of
+ *             What^O_h.
+ *   y       : device bf16 [B, D].
+ * Same arithmetic, limits and errors as mla_value_project (one product, no intermediate). */
+mla_status mla_value_project_merged(const void* u, const void* w_hat_t, int32_t B, int32_t H, int32_t D,
+                                    void* y, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

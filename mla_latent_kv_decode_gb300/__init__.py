@@ -82,6 +82,10 @@ def load():
         lib.mla_indexer_score.restype = ctypes.c_int
         lib.mla_topk_select.argtypes = [P, i64, P, i32, i32, P, P]
         lib.mla_topk_select.restype = ctypes.c_int
+        lib.mla_value_project.argtypes = [P, P, P, i32, i32, i32, P, P, P]
+        lib.mla_value_project.restype = ctypes.c_int
+        lib.mla_value_project_merged.argtypes = [P, P, P, i32, i32, i32, P, P]
+        lib.mla_value_project_merged.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -287,3 +291,41 @@ def topk_select(scores, seq_lens, K: int, topk_idx=None, stream=None):
                                 _dev_ptr(topk_idx, "topk_idx", torch.int32, (B, K)), _stream_ptr(stream))
     _check(rc, "mla_topk_select")
     return topk_idx
+
+
+# Value up-projection and output projection of the decode output (include/mla.h).
+D_V = 128
+
+
+def value_project(u, w_uv_t, w_o_t, z=None, y=None, stream=None):
+    """Y = sum_h (U_h W^UV_h) W^O_h: u bf16[B,H,512], w_uv_t bf16[H,128,512] (W^UV_h transposed),
+    w_o_t bf16[D,H*128] (W^O transposed).  Returns (y bf16[B,D], z bf16[2,B,H*128]: Z as hi and lo
+    planes)."""
+    torch = _torch()
+    B, H, _ = u.shape
+    D = int(w_o_t.shape[0])
+    if z is None:
+        z = torch.empty((2, B, H * D_V), dtype=torch.bfloat16, device=u.device)
+    if y is None:
+        y = torch.empty((B, D), dtype=torch.bfloat16, device=u.device)
+    rc = load().mla_value_project(_dev_ptr(u, "u", torch.bfloat16, (B, H, D_C)),
+                                  _dev_ptr(w_uv_t, "w_uv_t", torch.bfloat16, (H, D_V, D_C)),
+                                  _dev_ptr(w_o_t, "w_o_t", torch.bfloat16, (D, H * D_V)), int(B), int(H), D,
+                                  _dev_ptr(z, "z", torch.bfloat16, (2, B, H * D_V)),
+                                  _dev_ptr(y, "y", torch.bfloat16, (B, D)), _stream_ptr(stream))
+    _check(rc, "mla_value_project")
+    return y, z
+
+
+def value_project_merged(u, w_hat_t, y=None, stream=None):
+    """Y = sum_h U_h What^O_h with the pre-merged weight: u bf16[B,H,512], w_hat_t bf16[D,H*512]."""
+    torch = _torch()
+    B, H, _ = u.shape
+    D = int(w_hat_t.shape[0])
+    if y is None:
+        y = torch.empty((B, D), dtype=torch.bfloat16, device=u.device)
+    rc = load().mla_value_project_merged(_dev_ptr(u, "u", torch.bfloat16, (B, H, D_C)),
+                                         _dev_ptr(w_hat_t, "w_hat_t", torch.bfloat16, (D, H * D_C)), int(B),
+                                         int(H), D, _dev_ptr(y, "y", torch.bfloat16, (B, D)), _stream_ptr(stream))
+    _check(rc, "mla_value_project_merged")
+    return y

@@ -274,6 +274,46 @@ mla_status mla_combine(const float* o_part, const float* lse_part, int32_t S, in
                                     lse, stream));
 }
 
+namespace {
+mla_status value_project_status(const void* u, const void* w1, const void* w2, int32_t B, int32_t H, int32_t D,
+                                const void* y) {
+    if (B < 0 || H < 1 || H > 65535 || D < kDv || D % 128 != 0 || (int64_t)B > 65535LL * 128)
+        return MLA_ERR_INVALID;
+    if (B == 0) return MLA_OK;
+    if (!u || !w1 || !y) return MLA_ERR_INVALID;
+    if (!aligned(u, 16) || !aligned(w1, 16) || !aligned(y, 16) || (w2 && !aligned(w2, 16)))
+        return MLA_ERR_INVALID;
+    return MLA_OK;
+}
+}  // namespace
+
+mla_status mla_value_project(const void* u, const void* w_uv_t, const void* w_o_t, int32_t B, int32_t H,
+                             int32_t D, void* z, void* y, cudaStream_t stream) {
+    mla_status st = value_project_status(u, w_uv_t, w_o_t, B, H, D, y);
+    if (st != MLA_OK || B == 0) return st;
+    if (!w_o_t || !z || !aligned(z, 16)) return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_value_project(static_cast<const __nv_bfloat16*>(u),
+                                          static_cast<const __nv_bfloat16*>(w_uv_t),
+                                          static_cast<const __nv_bfloat16*>(w_o_t), B, H, D,
+                                          static_cast<__nv_bfloat16*>(z), static_cast<__nv_bfloat16*>(y), ctl,
+                                          stream));
+}
+
+mla_status mla_value_project_merged(const void* u, const void* w_hat_t, int32_t B, int32_t H, int32_t D,
+                                    void* y, cudaStream_t stream) {
+    mla_status st = value_project_status(u, w_hat_t, nullptr, B, H, D, y);
+    if (st != MLA_OK || B == 0) return st;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_value_project_merged(static_cast<const __nv_bfloat16*>(u),
+                                                 static_cast<const __nv_bfloat16*>(w_hat_t), B, H, D,
+                                                 static_cast<__nv_bfloat16*>(y), ctl, stream));
+}
+
 mla_status mla_check_status(cudaStream_t stream) {
     DevCtl* ctl = device_ctl();
     if (!ctl) return MLA_ERR_CUDA;

@@ -12,6 +12,7 @@ namespace mla {
 constexpr int kDc = MLA_D_C;                 // latent width
 constexpr int kDr = MLA_D_R;                 // rope width
 constexpr int kDk = kDc + kDr;               // 576 = score contraction length
+constexpr int kDv = MLA_D_V;                 // value width of one head (value up-projection)
 constexpr int kHeads = MLA_HEADS;
 constexpr int kPage = MLA_PAGE_TOKENS;
 constexpr int kBf16RecordBytes = kDk * 2;    // 1152
@@ -56,6 +57,13 @@ cudaError_t launch_indexer_score(const uint8_t* pool, int64_t num_pages, const _
                                  int max_seq_len, float* scores, DevCtl* ctl, cudaStream_t st);
 cudaError_t launch_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int B, int K,
                                int32_t* idx, cudaStream_t st);
+
+// Value up-projection and output projection (proj.cu).
+cudaError_t launch_value_project(const __nv_bfloat16* u, const __nv_bfloat16* w_uv_t, const __nv_bfloat16* w_o_t,
+                                 int B, int H, int D, __nv_bfloat16* z, __nv_bfloat16* y, DevCtl* ctl,
+                                 cudaStream_t st);
+cudaError_t launch_value_project_merged(const __nv_bfloat16* u, const __nv_bfloat16* w_hat_t, int B, int H, int D,
+                                        __nv_bfloat16* y, DevCtl* ctl, cudaStream_t st);
 
 // Split-KV plan of one decode call.
 struct DecodePlan {

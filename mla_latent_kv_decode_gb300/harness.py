@@ -151,3 +151,49 @@ class DeviceWorkload:
     def flops(self) -> int:
         """2 * H * (576 + 512) per attended position (scores + weighted sum)."""
         return int(2 * self.w.H * (synth.D_K + synth.D_C) * self.w.attended())
+
+
+class ProjInputs:
+    """Seeded inputs of the value up-projection and output projection on the device: U (unit
+    normal bf16), W^UV_h transposed (unit normal times 2^-4) and W^O transposed (unit normal
+    times 2^-7), drawn by the generator's device twin; the power-of-two factors are exact in
+    bf16 and give Z and Y a variance of about 2.  With merged=True the weight is instead a
+    stand-in for What^O transposed [D, H*512] (unit normal times 2^-8), for timing."""
+
+    def __init__(self, B: int, H: int = 128, D: int = 5120, seed: int = 0x4D4C41 + 7, merged: bool = False,
+                 device="cuda"):
+        import torch
+        self.B, self.H, self.D, self.seed = B, H, D, seed
+        dev = torch.device(device)
+        s = torch.cuda.current_stream().cuda_stream
+
+        def draw(shape, stream, scale):
+            t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+            n = t.numel()
+            row = shape[-1]
+            synth.gpu_normal_bf16(t.data_ptr(), n // row, seed, stream, 0, row, row, s)
+            if scale != 1.0:
+                t.mul_(scale)
+            return t
+
+        self.u = draw((B, H, synth.D_C), synth.STREAM_U, 1.0)
+        if merged:
+            self.w_hat_t = draw((D, H * synth.D_C), synth.STREAM_WO, 2.0 ** -8)
+        else:
+            self.w_uv_t = draw((H, mla.D_V, synth.D_C), synth.STREAM_WUV, 2.0 ** -4)
+            self.w_o_t = draw((D, H * mla.D_V), synth.STREAM_WO, 2.0 ** -7)
+        torch.cuda.synchronize()
+
+    def weight_bytes(self) -> int:
+        if hasattr(self, "w_hat_t"):
+            return self.w_hat_t.numel() * 2
+        return (self.w_uv_t.numel() + self.w_o_t.numel()) * 2
+
+    def algorithmic_bytes(self) -> int:
+        """Weights, U and Y: what one call must move (the intermediate Z is not counted)."""
+        return self.weight_bytes() + self.u.numel() * 2 + self.B * self.D * 2
+
+    def flops(self) -> int:
+        if hasattr(self, "w_hat_t"):
+            return 2 * self.B * self.H * synth.D_C * self.D
+        return 2 * self.B * self.H * mla.D_V * (synth.D_C + self.D)

@@ -51,6 +51,9 @@ STREAM_TOPK = 6
 STREAM_IDX_K = 7          # DSA indexer search keys
 STREAM_IDX_Q = 8          # DSA indexer queries
 STREAM_IDX_W = 9          # DSA indexer head weights
+STREAM_U = 10             # value projection: decode outputs U
+STREAM_WUV = 11           # value projection: W^UV
+STREAM_WO = 12            # value projection: W^O (or the merged weight)
 
 D_C = 512
 D_R = 64

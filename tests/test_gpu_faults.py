@@ -49,6 +49,7 @@ def test_fp8_path_reports_values_outside_its_range():
         w = synth.make_workload("fp8_batch", B=2, seq_len=300) if topk is None else \
             synth.make_workload("topk_sparse", B=2, seq_len=300, topk=topk)
         dw = harness.DeviceWorkload(w, gen="host")
+        dw.append()                                    # the tokens the workload appends
         dw.decode()
         assert mla.check_status() == 0
         q0 = dw.q_lat[1, 5, 17].clone()
