@@ -84,7 +84,7 @@ def load():
         lib.mla_topk_select.restype = ctypes.c_int
         lib.mla_value_project.argtypes = [P, P, P, i32, i32, i32, P, P, P]
         lib.mla_value_project.restype = ctypes.c_int
-        lib.mla_value_project_merged.argtypes = [P, P, P, i32, i32, i32, P, P]
+        lib.mla_value_project_merged.argtypes = [P, P, i32, i32, i32, P, P]
         lib.mla_value_project_merged.restype = ctypes.c_int
         _lib = lib
         return lib

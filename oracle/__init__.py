@@ -90,6 +90,23 @@ def _load():
             lib.oracle_merge_value_output.restype = None
             lib.oracle_project_merged.argtypes = [P, P] + [ctypes.c_int] * 4 + [P, ctypes.c_int]
             lib.oracle_project_merged.restype = None
+            lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_decode.restype = f64
+            lib.oracle_e2m1_encode.argtypes = [f32]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_shared_record_bytes.argtypes = [ctypes.c_int]
+            lib.oracle_shared_record_bytes.restype = i64
+            lib.oracle_shared_append.argtypes = [ctypes.c_int, P, i64, P, P, i64]
+            lib.oracle_shared_append.restype = i64
+            lib.oracle_shared_read.argtypes = [ctypes.c_int, P, i64, P]
+            lib.oracle_shared_read.restype = None
+            lib.oracle_attend_sink.argtypes = [P, P, i64, P, i64, i64, ctypes.c_int, ctypes.c_int, f64, f64, P, P]
+            lib.oracle_attend_sink.restype = None
+            lib.oracle_unrotate.argtypes = [P, P]
+            lib.oracle_unrotate.restype = None
+            lib.oracle_shared_kv_decode.argtypes = [ctypes.c_int, P, i64, P, P, i32, P, P, i32, i32, i32, f32, P, P,
+                                                    P, i64, P, P, ctypes.c_int]
+            lib.oracle_shared_kv_decode.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -365,3 +382,111 @@ def project_merged(u: np.ndarray, w_hat: np.ndarray, nthreads: int = 0) -> np.nd
     y = np.empty((B, D))
     _load().oracle_project_merged(_ptr(u), _ptr(w_hat), B, H, dc, D, _ptr(y), nthreads)
     return y
+
+
+# ------------------------------------------------------------------------------------------
+# Shared K = V decode over V4 / V4.1 main-KV entries ("DeepSeek's KV Cache: From 3.9 MB to 890 B
+# per Token", section "HCA: 128 tokens into one" (Fig. 15), "Calculating V4-Flash's KV cache",
+# "Calculating V4.1-Flash's KV cache").
+# ------------------------------------------------------------------------------------------
+V4_FP8 = 2       # 584 B: 448 E4M3 (one UE8M0 scale per 64) + 64 bf16 RoPE + 7 scales + 1 pad
+V41_FP4 = 3      # 288 B: 512 E2M1 (one E4M3 scale per 16)
+E_DIM = 512
+
+
+def e2m1_decode(code: int) -> float:
+    """OCP MX E2M1 value of one 4-bit code (exact)."""
+    return float(_load().oracle_e2m1_decode(int(code) & 0xF))
+
+
+def e2m1_encode(x: float) -> int:
+    """E2M1 round-to-nearest-even, saturating at +-6, of one fp32 value."""
+    return int(_load().oracle_e2m1_encode(float(np.float32(x))))
+
+
+def shared_record_bytes(fmt: int) -> int:
+    return int(_load().oracle_shared_record_bytes(int(fmt)))
+
+
+def new_shared_pool(fmt: int, num_pages: int) -> np.ndarray:
+    return np.zeros(num_pages * PAGE * shared_record_bytes(fmt), dtype=np.uint8)
+
+
+def shared_append(fmt: int, pool: np.ndarray, entry: np.ndarray, slot: np.ndarray) -> int:
+    """Quantise T entries (bf16 bits [T,512]) into ``pool`` at ``slot``; returns the number of rows
+    whose slot lies outside the pool."""
+    entry = np.ascontiguousarray(entry, dtype=np.uint16)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    T = slot.shape[0]
+    assert entry.shape == (T, E_DIM)
+    num_pages = pool.size // (PAGE * shared_record_bytes(fmt))
+    return int(_load().oracle_shared_append(int(fmt), _ptr(pool), num_pages, _ptr(entry), _ptr(slot), T))
+
+
+def shared_read(fmt: int, pool: np.ndarray, slot: int) -> np.ndarray:
+    """One cached entry as exact doubles [512]."""
+    e = np.empty(E_DIM, dtype=np.float64)
+    _load().oracle_shared_read(int(fmt), _ptr(pool), int(slot), _ptr(e))
+    return e
+
+
+def attend_sink(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, sink: float = -np.inf):
+    """Attention of one query with the sink exp(sink) in the softmax denominator (fp64):
+    returns (out[dv], lse) with lse = ln(sum_t exp(s_t) + exp(sink))."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    n, dk = K.shape
+    dv = V.shape[1]
+    out = np.empty(dv)
+    lse = np.empty(1)
+    _load().oracle_attend_sink(_ptr(q), _ptr(K), dk, _ptr(V), dv, n, dk, dv, float(scale), float(sink),
+                               _ptr(out), _ptr(lse))
+    return out, float(lse[0])
+
+
+def unrotate(o: np.ndarray, cos_sin: np.ndarray) -> np.ndarray:
+    """The last 64 dims of a 512-dim head output rotated back by the angles whose cosines and
+    sines cos_sin[0:32], cos_sin[32:64] gives (pairs 448 + 2i, 448 + 2i + 1)."""
+    o = _f64(o).copy()
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    assert o.shape == (E_DIM,) and cs.shape == (64,)
+    _load().oracle_unrotate(_ptr(o), _ptr(cs))
+    return o
+
+
+def shared_kv_decode(fmt: int, pool: np.ndarray, q: np.ndarray, block_table: np.ndarray,
+                     seq_lens: np.ndarray, scale: float, sink: np.ndarray | None = None,
+                     rope_cs: np.ndarray | None = None, topk_idx: np.ndarray | None = None, pairs=None,
+                     nthreads: int = 0):
+    """Shared K = V decode in fp64 for the (b, h) pairs given (all by default).  q bf16 bits
+    [B,H,512]; sink fp32 [H] or None; rope_cs fp32 [B,64] (cos then sin of the query position's
+    32 angles) or None.  Returns (out float64[n,512], lse float64[n])."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, H, _ = q.shape
+    if pairs is None:
+        pairs = np.stack(np.meshgrid(np.arange(B), np.arange(H), indexing="ij"), -1).reshape(-1, 2)
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    order = np.argsort(pairs[:, 0], kind="stable")
+    sp = np.ascontiguousarray(pairs[order])
+    n = sp.shape[0]
+    out = np.empty((n, E_DIM))
+    lse = np.empty(n)
+    topk = 0
+    if topk_idx is not None:
+        topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+        topk = topk_idx.shape[1]
+    sk = None if sink is None else np.ascontiguousarray(sink, dtype=np.float32)
+    cs = None if rope_cs is None else np.ascontiguousarray(rope_cs, dtype=np.float32)
+    num_pages = pool.size // (PAGE * shared_record_bytes(fmt))
+    rc = _load().oracle_shared_kv_decode(int(fmt), _ptr(pool), num_pages, _ptr(q), _ptr(block_table),
+                                         block_table.shape[1], _ptr(seq_lens), _ptr(topk_idx), topk, B, H,
+                                         float(np.float32(scale)), _ptr(sk), _ptr(cs), _ptr(sp), n, _ptr(out),
+                                         _ptr(lse), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_shared_kv_decode: a visible position maps outside the pool")
+    res_out = np.empty_like(out)
+    res_lse = np.empty_like(lse)
+    res_out[order] = out
+    res_lse[order] = lse
+    return res_out, res_lse

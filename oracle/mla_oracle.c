@@ -424,6 +424,272 @@ void oracle_project_merged(const double* u, const double* w_hat, int B, int H, i
 }
 
 /* ---------------------------------------------------------------------------------------- */
+/* Shared K = V decode over V4 / V4.1 main-KV entries ([KV] "HCA: 128 tokens into one",       */
+/* Fig. 15; "Calculating V4-Flash's KV cache"; "Calculating V4.1-Flash's KV cache")          */
+/* ---------------------------------------------------------------------------------------- */
+
+#define ORACLE_E 512          /* entry width c: one entry serves as Key and Value            */
+#define ORACLE_E_NOPE 448     /* V4: non-RoPE dims stored as E4M3                               */
+#define ORACLE_E_ROPE 64      /* the last 64 dims carry RoPE                                    */
+#define ORACLE_V4_GROUP 64    /* V4: one UE8M0 scale per 64 channels (7 scales + 1 pad byte)   */
+#define ORACLE_V41_GROUP 16   /* V4.1: one E4M3 scale per 16 channels                           */
+enum { ORACLE_V4_FP8 = 2, ORACLE_V41_FP4 = 3 };
+
+/* [OCP MX] E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no infinities or NaN.
+ * Normal (E > 0): 2^(E-1) * (1 + M/2); subnormal (E = 0): M/2.  Magnitudes 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6. */
+double oracle_e2m1_decode(uint8_t code) {
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* E2M1 of an fp32 value, round to nearest with ties to the even mantissa bit, saturating to 6.
+ * The non-negative codes 0..7 increase in value, so this is the nearest-code search of the E4M3
+ * encoder over eight codes. */
+uint8_t oracle_e2m1_encode(float x) {
+    uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    double a = fabs((double)x);
+    if (a >= 6.0) return sign | 0x7;
+    int lo = 0;
+    while (lo < 7 && oracle_e2m1_decode((uint8_t)(lo + 1)) <= a) ++lo;
+    if (lo == 7) return sign | 0x7;
+    double vlo = oracle_e2m1_decode((uint8_t)lo), vhi = oracle_e2m1_decode((uint8_t)(lo + 1));
+    int code;
+    if (a - vlo < vhi - a) code = lo;
+    else if (a - vlo > vhi - a) code = lo + 1;
+    else code = (lo & 1) ? lo + 1 : lo;
+    return sign | (uint8_t)code;
+}
+
+/* Bytes of one entry: V4 448 x 1 B (E4M3) + 64 x 2 B (bf16 RoPE) + 7 x 1 B (UE8M0) + 1 B pad =
+ * 584; V4.1 512 x 0.5 B (E2M1) + 32 x 1 B (E4M3 scales) = 288. */
+int64_t oracle_shared_record_bytes(int fmt) {
+    if (fmt == ORACLE_V4_FP8) return ORACLE_E_NOPE + 2 * ORACLE_E_ROPE + ORACLE_E_NOPE / ORACLE_V4_GROUP + 1;
+    if (fmt == ORACLE_V41_FP4) return ORACLE_E / 2 + ORACLE_E / ORACLE_V41_GROUP;
+    return -1;
+}
+
+/* Where each field of slot s lives.  V4 (this library's page layout; the pages give only the
+ * sizes): a 64-entry page holds all its entries' codes [64][448], then their RoPE dims [64][64]
+ * bf16, then their scale bytes [64][8] (7 UE8M0 + 1 pad), so that every field starts on a 16-byte
+ * boundary.  V4.1: entries one after another, [256 B of E2M1 pairs | 32 E4M3 scales]. */
+static void v4_fields(const uint8_t* pool, int64_t slot, const uint8_t** codes, const uint8_t** rope,
+                      const uint8_t** scales) {
+    const int64_t page = slot / ORACLE_PAGE, row = slot % ORACLE_PAGE;
+    const uint8_t* base = pool + page * ORACLE_PAGE * 584;
+    *codes = base + row * ORACLE_E_NOPE;
+    *rope = base + ORACLE_PAGE * ORACLE_E_NOPE + row * 2 * ORACLE_E_ROPE;
+    *scales = base + ORACLE_PAGE * (ORACLE_E_NOPE + 2 * ORACLE_E_ROPE) + row * 8;
+}
+
+/* Write T entries (bf16 bits [T][512]) at `slot` (< 0 skips; beyond the pool: counted, not
+ * written).
+ * V4 ("Calculating V4-Flash's KV cache": 448 non-RoPE dims in FP8 E4M3 with one UE8M0 scale per
+ * 64 channels, 64 RoPE dims in BF16): per group g of 64 non-RoPE dims, amax = max |x|; the scale
+ * is the power of two 2^e with the smallest integer e such that 448 * 2^e >= amax (so that no code
+ * saturates), stored as the byte e + 127 (e clamped to [-127, 127]; amax = 0 stores byte 0 and
+ * zero codes); code = E4M3_RNE_satfinite(fl32(x / 2^e)).  The RoPE dims are copied, the pad byte
+ * is 0.
+ * V4.1 ("Calculating V4.1-Flash's KV cache": all 512 dims in FP4 E2M1, the RoPE part included,
+ * one E4M3 scale per 16 channels): per group of 16 dims, s = E4M3_RNE_satfinite(fl32(amax / 6))
+ * (6 is E2M1's largest magnitude); code = E2M1_RNE_satfinite(fl32(x / value(s))), all codes 0
+ * when value(s) = 0.  Dims 2i and 2i + 1 share byte i, dim 2i in the low nibble. */
+int64_t oracle_shared_append(int fmt, uint8_t* pool, int64_t num_pages, const uint16_t* entry,
+                             const int32_t* slot, int64_t T) {
+    int64_t rb = oracle_shared_record_bytes(fmt);
+    int64_t bad = 0;
+    for (int64_t i = 0; i < T; ++i) {
+        int64_t sl = slot[i];
+        if (sl < 0) continue;
+        if (sl >= num_pages * ORACLE_PAGE) { ++bad; continue; }
+        const uint16_t* x = entry + i * ORACLE_E;
+        if (fmt == ORACLE_V4_FP8) {
+            const uint8_t *c0, *r0, *s0;
+            v4_fields(pool, sl, &c0, &r0, &s0);
+            uint8_t* codes = (uint8_t*)c0;
+            uint8_t* rope = (uint8_t*)r0;
+            uint8_t* scales = (uint8_t*)s0;
+            for (int g = 0; g < ORACLE_E_NOPE / ORACLE_V4_GROUP; ++g) {
+                double amax = 0.0;
+                for (int k = 0; k < ORACLE_V4_GROUP; ++k) {
+                    double v = fabs(oracle_bf16_to_f64(x[g * ORACLE_V4_GROUP + k]));
+                    if (v > amax) amax = v;
+                }
+                if (amax == 0.0) {
+                    scales[g] = 0;
+                    for (int k = 0; k < ORACLE_V4_GROUP; ++k) codes[g * ORACLE_V4_GROUP + k] = 0;
+                    continue;
+                }
+                int e = -127;
+                while (e < 127 && 448.0 * ldexp(1.0, e) < amax) ++e;
+                scales[g] = (uint8_t)(e + 127);
+                for (int k = 0; k < ORACLE_V4_GROUP; ++k) {
+                    float v = (float)oracle_bf16_to_f64(x[g * ORACLE_V4_GROUP + k]);
+                    codes[g * ORACLE_V4_GROUP + k] = oracle_e4m3_encode((float)((double)v / ldexp(1.0, e)));
+                }
+            }
+            scales[7] = 0;
+            memcpy(rope, x + ORACLE_E_NOPE, 2 * ORACLE_E_ROPE);
+        } else {
+            uint8_t* rec = pool + sl * rb;
+            for (int g = 0; g < ORACLE_E / ORACLE_V41_GROUP; ++g) {
+                float amax = 0.0f;
+                for (int k = 0; k < ORACLE_V41_GROUP; ++k) {
+                    float v = fabsf((float)oracle_bf16_to_f64(x[g * ORACLE_V41_GROUP + k]));
+                    if (v > amax) amax = v;
+                }
+                uint8_t sc = oracle_e4m3_encode(amax / 6.0f);
+                float sv = (float)oracle_e4m3_decode(sc);
+                rec[ORACLE_E / 2 + g] = sc;
+                for (int k = 0; k < ORACLE_V41_GROUP; k += 2) {
+                    float v0 = (float)oracle_bf16_to_f64(x[g * ORACLE_V41_GROUP + k]);
+                    float v1 = (float)oracle_bf16_to_f64(x[g * ORACLE_V41_GROUP + k + 1]);
+                    uint8_t q0 = sv == 0.0f ? 0 : oracle_e2m1_encode(v0 / sv);
+                    uint8_t q1 = sv == 0.0f ? 0 : oracle_e2m1_encode(v1 / sv);
+                    rec[(g * ORACLE_V41_GROUP + k) / 2] = (uint8_t)(q0 | (q1 << 4));
+                }
+            }
+        }
+    }
+    return bad;
+}
+
+/* One entry as exact doubles e[512]: V4 code * 2^(byte - 127) for the 448 non-RoPE dims, the
+ * bf16 RoPE dims widened; V4.1 E2M1 value * E4M3 scale value. */
+void oracle_shared_read(int fmt, const uint8_t* pool, int64_t slot, double* e) {
+    if (fmt == ORACLE_V4_FP8) {
+        const uint8_t *codes, *rope, *scales;
+        v4_fields(pool, slot, &codes, &rope, &scales);
+        for (int k = 0; k < ORACLE_E_NOPE; ++k)
+            e[k] = oracle_e4m3_decode(codes[k]) * ldexp(1.0, (int)scales[k / ORACLE_V4_GROUP] - 127);
+        for (int r = 0; r < ORACLE_E_ROPE; ++r) {
+            uint16_t b;
+            memcpy(&b, rope + 2 * r, 2);
+            e[ORACLE_E_NOPE + r] = oracle_bf16_to_f64(b);
+        }
+    } else {
+        const uint8_t* rec = pool + slot * oracle_shared_record_bytes(fmt);
+        for (int k = 0; k < ORACLE_E; ++k) {
+            uint8_t byte = rec[k / 2];
+            uint8_t q = (k & 1) ? (byte >> 4) : (byte & 0xF);
+            e[k] = oracle_e2m1_decode(q) * oracle_e4m3_decode(rec[ORACLE_E / 2 + k / ORACLE_V41_GROUP]);
+        }
+    }
+}
+
+/* Scaled dot-product attention of one query with a sink ([KV] Fig. 15 (2): the head adds
+ * exp(z') to the softmax denominator, so the weights on the real entries may sum to less than 1):
+ *   s_t = scale * (q . K_t);  L = sum_t exp(s_t) + exp(z');  out = sum_t (exp(s_t) / L) V_t;
+ *   lse = ln L.
+ * z' = -inf is no sink (plain attention).  n == 0: out = 0 and lse = z'.  Computed with
+ * m = max(z', max_t s_t) subtracted inside every exponential. */
+void oracle_attend_sink(const double* q, const double* K, int64_t ldk, const double* V, int64_t ldv, int64_t n,
+                        int dk, int dv, double scale, double sink, double* out, double* lse) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int j = 0; j < dv; ++j) out[j] = 0.0;
+    double m = sink;
+    for (int64_t t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int k = 0; k < dk; ++k) dot += q[k] * K[t * ldk + k];
+        s[t] = scale * dot;
+        if (s[t] > m) m = s[t];
+    }
+    if (m == -INFINITY) {   /* nothing visible and no sink */
+        *lse = -INFINITY;
+        free(s);
+        return;
+    }
+    double l = exp(sink - m);
+    for (int64_t t = 0; t < n; ++t) l += exp(s[t] - m);
+    for (int64_t t = 0; t < n; ++t) {
+        double p = exp(s[t] - m) / l;
+        for (int j = 0; j < dv; ++j) out[j] += p * V[t * ldv + j];
+    }
+    *lse = m + log(l);
+    free(s);
+}
+
+/* Inverse rotation of the last 64 dims of a head output by the query position ([KV] Fig. 15 (3):
+ * E serves as the Value with RoPE still applied, so the output's RoPE dims are rotated back by
+ * the current position t).  The rotation acts on the pairs (448 + 2i, 448 + 2i + 1), i < 32, by
+ * the angle theta_i of position t, given as cos_sin[i] = cos(theta_i), cos_sin[32 + i] =
+ * sin(theta_i); rotating back is rotating by -theta_i:
+ *   y0 = x0 cos + x1 sin,   y1 = -x0 sin + x1 cos. */
+void oracle_unrotate(double* o, const float* cos_sin) {
+    for (int i = 0; i < ORACLE_E_ROPE / 2; ++i) {
+        double c = cos_sin[i], sn = cos_sin[ORACLE_E_ROPE / 2 + i];
+        double x0 = o[ORACLE_E_NOPE + 2 * i], x1 = o[ORACLE_E_NOPE + 2 * i + 1];
+        o[ORACLE_E_NOPE + 2 * i] = x0 * c + x1 * sn;
+        o[ORACLE_E_NOPE + 2 * i + 1] = -x0 * sn + x1 * c;
+    }
+}
+
+/* Shared K = V decode ([KV] Fig. 15 (1)-(3)) for (request b, head h) pairs: the visible entries
+ * (dense: positions 0 .. seq_lens[b]-1; with topk_idx: the listed ones, as in oracle_mla_decode)
+ * serve as both Key and Value, E_t (512) read from the pool; s_t = scale * (q[b,h] . E_t); the
+ * softmax adds the sink exp(sink[h]) to its denominator (sink NULL: none); the output's last 64
+ * dims are rotated back by rope_cs[b] (NULL: not rotated).  lse = ln(sum_t exp(s_t) + exp(z')).
+ * Returns -1 if a visible position maps outside the pool (that pair's lse is NaN). */
+int oracle_shared_kv_decode(int fmt, const uint8_t* pool, int64_t num_pages, const uint16_t* q,
+                            const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                            const int32_t* topk_idx, int32_t topk, int32_t B, int32_t H, float scale,
+                            const float* sink, const float* rope_cs, const int32_t* pairs, int64_t n_pairs,
+                            double* out, double* lse, int nthreads) {
+    int rc = 0;
+    (void)B;
+    for (int64_t i0 = 0; i0 < n_pairs;) {
+        int32_t b = pairs[2 * i0];
+        int64_t i1 = i0;
+        while (i1 < n_pairs && pairs[2 * i1] == b) ++i1;
+        int64_t N = seq_lens[b], n = 0;
+        int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)((topk_idx ? topk : N) + 1));
+        if (topk_idx) {
+            for (int32_t j = 0; j < topk; ++j) {
+                int64_t t = topk_idx[(int64_t)b * topk + j];
+                if (t >= 0 && t < N) pos[n++] = t;
+            }
+        } else {
+            for (int64_t t = 0; t < N; ++t) pos[n++] = t;
+        }
+        double* E = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORACLE_E);
+        int bad = 0;
+#ifdef _OPENMP
+        if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static) reduction(| : bad)
+#endif
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t t = pos[j], pg = t / ORACLE_PAGE;
+            if (pg >= max_pages) { bad = 1; continue; }
+            int64_t page = block_table[(int64_t)b * max_pages + pg];
+            if (page < 0 || page >= num_pages) { bad = 1; continue; }
+            oracle_shared_read(fmt, pool, page * ORACLE_PAGE + t % ORACLE_PAGE, E + j * ORACLE_E);
+        }
+        if (bad) {
+            rc = -1;
+            for (int64_t i = i0; i < i1; ++i) lse[i] = NAN;
+        } else {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic)
+#endif
+            for (int64_t i = i0; i < i1; ++i) {
+                int32_t h = pairs[2 * i + 1];
+                double qd[ORACLE_E];
+                for (int k = 0; k < ORACLE_E; ++k) qd[k] = oracle_bf16_to_f64(q[((int64_t)b * H + h) * ORACLE_E + k]);
+                double z = sink ? (double)sink[h] : -INFINITY;
+                oracle_attend_sink(qd, E, ORACLE_E, E, ORACLE_E, n, ORACLE_E, ORACLE_E, (double)scale, z,
+                                   out + i * ORACLE_E, lse + i);
+                if (rope_cs) oracle_unrotate(out + i * ORACLE_E, rope_cs + (int64_t)b * ORACLE_E_ROPE);
+            }
+        }
+        free(E);
+        free(pos);
+        i0 = i1;
+    }
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------------------- */
 /* DSA lightning indexer and top-k selection                                                */
 /* ([KV] "DSA: three things the indexer builds" (Fig. 8), "The score that picks positions"   */
 /* (Fig. 9), "Calculating V3.2's KV cache" (search key, 132 B))                              */

@@ -2,9 +2,11 @@
 890 B per Token", section "Computing without expanding Key and Value", Fig. 6 (2) and (3)) with
 the fp64 oracle, through the C ABI.
 
-Tolerance: Y is bf16 of unit-variance-order values; every element within 1e-2 of the oracle, and
-per request ||gpu - oracle|| <= 1e-2 ||oracle||.  Z's two bf16 planes carry Z to about 16
-significant bits: |hi + lo - Z| <= 2^-14 |Z| + 1e-6 per element.
+Tolerance, from the arithmetic: Y is rounded once to bf16 (relative error at most 2^-9) after
+fp32 accumulation of products of bf16 values, with Z carried to about 16 significant bits; so
+every element within 2^-8 |Y| + 2^-12 of the oracle (twice the rounding bound, plus room for the
+accumulation), and per request ||gpu - oracle|| <= 1e-2 ||oracle||.  Z's two bf16 planes:
+|hi + lo - Z| <= 2^-14 |Z| + 1e-6 per element, and |lo| at most half a bf16 step of hi.
 """
 import numpy as np
 import pytest
@@ -15,7 +17,6 @@ from mla_latent_kv_decode_gb300 import harness
 
 pytestmark = pytest.mark.gpu
 
-Y_ABS = 1e-2
 Y_REL = 1e-2
 
 
@@ -26,7 +27,9 @@ def _np(t):
 def _check_y(y, ref, what):
     err = np.abs(y - ref)
     assert np.isfinite(y).all(), what
-    assert err.max() <= Y_ABS, f"{what}: max |y err| {err.max():.3e}"
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -12
+    worst = np.argmax(err - bound)
+    assert np.all(err <= bound), f"{what}: |y err| {err.flat[worst]:.3e} at |y| {np.abs(ref).flat[worst]:.3e}"
     rel = np.linalg.norm(y - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
     assert rel.max() <= Y_REL, f"{what}: normwise {rel.max():.3e}"
 
@@ -44,9 +47,8 @@ def _two_stage(B, H, D, seed):
     zsum = zz[0] + zz[1]
     zref = zr.reshape(B, H * mla.D_V)
     assert np.all(np.abs(zsum - zref) <= 2.0 ** -14 * np.abs(zref) + 1e-6), "Z planes"
-    # the hi plane is Z rounded to bf16: adding the lo plane does not change its rounding
-    import torch
-    assert torch.equal((z[0].float() + z[1].float()).to(torch.bfloat16), z[0])
+    # the lo plane is what the hi plane's rounding left: at most half a bf16 step of hi
+    assert np.all(np.abs(zz[1]) <= 2.0 ** -8 * np.abs(zz[0]) + 1e-30)
     return p, y
 
 
@@ -82,8 +84,11 @@ def test_value_project_merged_weight():
     y2, _ = mla.value_project(p.u, p.w_uv_t, p.w_o_t)
     assert mla.check_status() == 0
     _, yr = oracle.value_project(u, w_uv, w_o)
-    # the merged weight's bf16 rounding moves Y by a few 1e-3 at most
-    assert np.abs(_np(y3) - yr).max() <= 2e-2 and np.abs(_np(y2) - yr).max() <= Y_ABS
+    # the two GPU forms against the unrounded fp64 result: the merged weight's own bf16 rounding
+    # (2^-9 relative per element, averaging out over 65,536 terms) adds a little to the first
+    _check_y(_np(y2), yr, "two products vs fp64")
+    rel = np.linalg.norm(_np(y3) - yr) / np.linalg.norm(yr)
+    assert rel <= 1e-2, f"merged vs fp64 normwise {rel:.3e}"
 
 
 def test_value_project_empty_batch_and_bad_sizes():

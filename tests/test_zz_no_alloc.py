@@ -84,6 +84,8 @@ def test_noalloc_gather_paths_with_a_smaller_plan_between():
     for big in (big_dense, big_topk):
         dwb = harness.DeviceWorkload(big, gen="host")
         dws = harness.DeviceWorkload(small_dense, gen="host")
+        dwb.append()      # the tokens the workloads append (the FP8 batch's last 64 positions)
+        dws.append()
         ref_b = _workspace_reference(big, dwb)
         ref_s = _workspace_reference(small_dense, dws)
         o, l = _noalloc_outputs(lib, torch, big, dwb)
