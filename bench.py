@@ -51,7 +51,8 @@ _HEADERS = ["mla_latent_kv_decode_gb300/csrc/decode_common.cuh",
             "include/mla.h"]
 KERNEL_SOURCES = {
     "decode_tc": ["mla_latent_kv_decode_gb300/csrc/decode_tc.cu"] + _HEADERS,
-    "decode_gather": ["mla_latent_kv_decode_gb300/csrc/decode_gather.cu"] + _HEADERS,
+    "decode_gather": ["mla_latent_kv_decode_gb300/csrc/decode_gather.cu",
+                      "mla_latent_kv_decode_gb300/csrc/decode_gather.cuh"] + _HEADERS,
     "indexer_score": ["mla_latent_kv_decode_gb300/csrc/indexer.cu"] + _HEADERS,
 }
 WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_context": "decode_tc",

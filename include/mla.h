@@ -57,7 +57,18 @@ typedef enum {
     /* 656 B per token: 512 E4M3 latent codes, 4 fp32 scales (one per 128 latent dims),
      * 64 bf16 rope, in that order and without padding ("DeepSeek's KV Cache",
      * "Calculating V3.2's KV cache": 512 + 16 + 128 = 656 B). */
-    MLA_KV_FP8_MIXED = 1
+    MLA_KV_FP8_MIXED = 1,
+    /* Shared K = V entries ("DeepSeek's KV Cache", section "HCA: 128 tokens into one", Fig. 15: one
+     * 512-dim entry E per position serves as both Key and Value; its last 64 dims carry RoPE).
+     * Written by mla_shared_kv_append and read by mla_shared_kv_decode only.
+     * 584 B per entry ("Calculating V4-Flash's KV cache"): 448 E4M3 codes with one UE8M0 scale
+     * per 64 dims, 64 bf16 RoPE dims, 7 scale bytes + 1 pad byte.  A 64-entry page (37,376 B)
+     * holds its entries field by field: codes [64][448], then RoPE [64][64] bf16, then scale
+     * bytes [64][8], so that each field starts on a 16-byte boundary. */
+    MLA_KV_V4_FP8 = 2,
+    /* 288 B per entry ("Calculating V4.1-Flash's KV cache"): 512 E2M1 codes, two per byte (dim 2i
+     * in the low nibble), then 32 E4M3 scales, one per 16 dims; entries one after another. */
+    MLA_KV_V41_FP4 = 3
 } mla_kv_format;
 
 #define MLA_D_C 512
@@ -65,8 +76,8 @@ typedef enum {
 #define MLA_HEADS 128
 #define MLA_PAGE_TOKENS 64
 
-/* Bytes of one token's record: 1152 (MLA_KV_BF16) or 656 (MLA_KV_FP8_MIXED); 0 for an unknown
- * format.  Host only. */
+/* Bytes of one token's record: 1152 (MLA_KV_BF16), 656 (MLA_KV_FP8_MIXED), 584 (MLA_KV_V4_FP8)
+ * or 288 (MLA_KV_V41_FP4); 0 for an unknown format.  Host only. */
 size_t mla_record_bytes(int32_t fmt);
 
 /* Write T new tokens into the paged pool ("DeepSeek's KV Cache", Fig. 3: C^KV and K^R are what
@@ -240,6 +251,56 @@ mla_status mla_indexer_score(const void* pool, int64_t num_pages, const void* q_
  * not be NaN.  MLA_ERR_INVALID for null pointers, B < 0, B >= 2^30, K < 1 or ld < 0. */
 mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int32_t B, int32_t K,
                            int32_t* topk_idx, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Shared K = V decode over compressed V4 / V4.1 entries ("DeepSeek's KV Cache: From 3.9 MB to
+ * 890 B per Token", section "HCA: 128 tokens into one", Fig. 15).  Each visible entry E (512
+ * dims, the last 64 carrying RoPE) serves as both Key and Value; the softmax adds a per-head sink
+ * exp(z'_h) to its denominator (so the weights may sum to less than one); the output's last 64
+ * dims are rotated back by the query position (each entry's contribution then carries the
+ * relative rotation s - t):
+ *     s_t = scale * (q[h] . E_t)        L_h = sum_t exp(s_t) + exp(z'_h)
+ *     o[h] = sum_t (exp(s_t) / L_h) E_t,  then dims (448 + 2i, 448 + 2i + 1) rotated by -theta_i
+ *     lse[h] = ln L_h
+ * ------------------------------------------------------------------------------------------ */
+
+/* Write T entries into a pool of format MLA_KV_V4_FP8 or MLA_KV_V41_FP4.
+ *   pool  : device, num_pages * 64 * mla_record_bytes(fmt) bytes, 128-byte aligned (the page
+ *           layouts are given with the formats).
+ *   entry : device bf16 [T, 512]  the entries (dims 448..511: the RoPE part, already rotated).
+ *   slot  : device int32 [T]  page * 64 + row; negative skips the row; >= num_pages * 64 is not
+ *           written and records MLA_ERR_BOUNDS.
+ * V4: per 64-dim group of dims 0..447, amax = max |x| and the scale 2^e with the smallest integer e
+ * (clamped to [-127, 127]) such that 448 * 2^e >= amax, stored as the byte e + 127 (UE8M0); code =
+ * E4M3(x * 2^-e) rounded to nearest even (saturating); amax = 0 stores byte 0 and zero codes;
+ * dims 448..511 are stored as bf16; the pad byte is 0.
+ * V4.1: per 16-dim group, s = E4M3(amax / 6) (fp32 division correctly rounded, then rounded to
+ * nearest even, saturating); code = E2M1(x / value(s)) rounded to nearest even, saturating at 6
+ * (all zero when value(s) = 0).
+ * Only the listed slots change.  MLA_ERR_INVALID for another format, null or misaligned pointers or
+ * T < 0. */
+mla_status mla_shared_kv_append(int32_t fmt, void* pool, int64_t num_pages, const void* entry,
+                                const int32_t* slot, int64_t T, cudaStream_t stream);
+
+/* Shared K = V decode of B requests (the computation above).
+ *   fmt, pool, num_pages : the entries written by mla_shared_kv_append.
+ *   q          : device bf16 [B, H, 512]  queries (already normalised and rotated by the caller).
+ *   block_table, max_pages, seq_lens, max_seq_len, topk_idx, topk, B, H (== 128), scale : as in
+ *                mla_decode (scale is normally 1/sqrt(512)); top-k lists pick the visible entries.
+ *   sink       : device fp32 [128]  z'_h, or NULL for none (then L_h has no extra term).
+ *   rope_cs    : device fp32 [B, 64]  per request cos(theta_i) (i < 32) then sin(theta_i) of the
+ *                query position's RoPE angles, or NULL for no rotation.
+ *   out        : device bf16 [B, H, 512];  lse : device fp32 [B, H] (a request with no visible entry:
+ *                out = 0 and lse = z'_h, or -inf without a sink).
+ *   workspace  : mla_decode_workspace_bytes(fmt, B, H, max_seq_len, topk) bytes, 256-byte aligned.
+ * Arithmetic: every stored code converts exactly to bf16 (an E4M3 value times a power of two; an
+ * E2M1 value times an E4M3 value); q . E and P E accumulate in fp32 on the tensor cores with bf16
+ * operands and P rounded once to bf16.  Errors as mla_decode. */
+mla_status mla_shared_kv_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q,
+                                const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                                int32_t max_seq_len, const int32_t* topk_idx, int32_t topk, int32_t B,
+                                int32_t H, float scale, const float* sink, const float* rope_cs, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Value up-projection and output projection of the decode output ("DeepSeek's KV Cache: From

@@ -18,6 +18,8 @@ import threading
 
 BF16 = 0          # 1,152-byte record: [c_KV 512 bf16 | k_rope 64 bf16]
 FP8_MIXED = 1     # 656-byte record: [512 E4M3 | 4 fp32 scales | 64 bf16 rope]
+V4_FP8 = 2        # 584-byte shared K = V entry: 448 E4M3 (UE8M0 per 64) + 64 bf16 RoPE dims
+V41_FP4 = 3       # 288-byte shared K = V entry: 512 E2M1 + one E4M3 scale per 16 dims
 D_C = 512
 D_R = 64
 HEADS = 128
@@ -82,6 +84,11 @@ def load():
         lib.mla_indexer_score.restype = ctypes.c_int
         lib.mla_topk_select.argtypes = [P, i64, P, i32, i32, P, P]
         lib.mla_topk_select.restype = ctypes.c_int
+        lib.mla_shared_kv_append.argtypes = [i32, P, i64, P, P, i64, P]
+        lib.mla_shared_kv_append.restype = ctypes.c_int
+        lib.mla_shared_kv_decode.argtypes = [i32, P, i64, P, P, i32, P, i32, P, i32, i32, i32, f32, P, P, P, P,
+                                             P, sz, P]
+        lib.mla_shared_kv_decode.restype = ctypes.c_int
         lib.mla_value_project.argtypes = [P, P, P, i32, i32, i32, P, P, P]
         lib.mla_value_project.restype = ctypes.c_int
         lib.mla_value_project_merged.argtypes = [P, P, i32, i32, i32, P, P]
@@ -329,3 +336,46 @@ def value_project_merged(u, w_hat_t, y=None, stream=None):
                                          int(H), D, _dev_ptr(y, "y", torch.bfloat16, (B, D)), _stream_ptr(stream))
     _check(rc, "mla_value_project_merged")
     return y
+
+
+# Shared K = V decode over V4 / V4.1 entries (include/mla.h).
+E_DIM = 512
+
+
+def shared_kv_append(fmt: int, pool, num_pages: int, entry, slot, stream=None) -> None:
+    """Quantise T entries (bf16 entry[T,512]) into a V4 / V4.1 pool at int32 ``slot[T]``."""
+    torch = _torch()
+    T = int(slot.shape[0])
+    rc = load().mla_shared_kv_append(int(fmt), _dev_ptr(pool, "pool", torch.uint8), int(num_pages),
+                                     _dev_ptr(entry, "entry", torch.bfloat16, (T, E_DIM)),
+                                     _dev_ptr(slot, "slot", torch.int32), T, _stream_ptr(stream))
+    _check(rc, "mla_shared_kv_append")
+
+
+def shared_kv_decode(fmt: int, pool, num_pages: int, q, block_table, seq_lens, max_seq_len: int,
+                     scale: float, sink=None, rope_cs=None, topk_idx=None, out=None, lse=None, workspace=None,
+                     stream=None):
+    """Shared K = V decode; returns (out bf16[B,H,512], lse fp32[B,H])."""
+    torch = _torch()
+    B, H, _ = q.shape
+    if out is None:
+        out = torch.empty((B, H, E_DIM), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    topk = 0 if topk_idx is None else int(topk_idx.shape[1])
+    if workspace is None:
+        need = decode_workspace_bytes(fmt, B, max_seq_len, topk, H)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().mla_shared_kv_decode(
+        int(fmt), _dev_ptr(pool, "pool", torch.uint8), int(num_pages),
+        _dev_ptr(q, "q", torch.bfloat16, (B, H, E_DIM)),
+        _dev_ptr(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev_ptr(seq_lens, "seq_lens", torch.int32, (B,)), int(max_seq_len),
+        _dev_ptr(topk_idx, "topk_idx", torch.int32), topk, int(B), int(H), float(scale),
+        _dev_ptr(sink, "sink", torch.float32, (H,)), _dev_ptr(rope_cs, "rope_cs", torch.float32, (B, 64)),
+        _dev_ptr(out, "out", torch.bfloat16, (B, H, E_DIM)), _dev_ptr(lse, "lse", torch.float32, (B, H)),
+        _dev_ptr(workspace, "workspace"), ws_bytes, _stream_ptr(stream))
+    _check(rc, "mla_shared_kv_decode")
+    return out, lse

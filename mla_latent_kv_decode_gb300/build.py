@@ -13,8 +13,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 
-LIBMLA_SOURCES = ["mla_api.cu", "append.cu", "combine.cu", "decode_tc.cu", "decode_gather.cu", "indexer.cu",
-                  "proj.cu"]
+LIBMLA_SOURCES = ["mla_api.cu", "append.cu", "combine.cu", "decode_tc.cu", "decode_gather.cu", "decode_shared.cu",
+                  "indexer.cu", "proj.cu"]
 SYNTH_SOURCES = ["synth.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

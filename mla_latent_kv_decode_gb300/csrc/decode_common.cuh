@@ -201,12 +201,51 @@ inline int clusters_for_tiles(long long w_max, int sms) {
     return c < 1 ? 1 : (int)c;
 }
 
+// One E4M3 code (the low byte of `code`) as a float, exactly.
+__device__ __forceinline__ float e4m3_to_float(uint32_t code) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)(code & 0xFFu)));
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// 16 e4m3 codes times a power-of-two scale to 16 bf16 values (pairs, low half first), exactly:
+// an E4M3 value has at most 4 significant bits and the scale only moves its exponent.
+__device__ __forceinline__ void e4m3x16_scaled_bf16(const uint4 c, float s, uint32_t (&o)[8]) {
+    uint32_t h[8];
+    e4m3x16_to_f16(c, h);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
+        o[k] = pack_bf16x2(f.x * s, f.y * s);
+    }
+}
+
+// 32 E2M1 codes (16 bytes; byte i holds dims 2i in its low and 2i + 1 in its high nibble) times an
+// E4M3 scale value (s0 for bytes 0-7, s1 for bytes 8-15) to 32 bf16 values, exactly: an E2M1 value
+// times an E4M3 value has at most 5 significant bits, well inside bf16's range.
+__device__ __forceinline__ void e2m1x32_scaled_bf16(const uint4 c, float s0, float s1, uint32_t (&o)[16]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t h;
+            asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+                : "=r"(h)
+                : "r"((w[k] >> (8 * j)) & 0xFFu));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+            const float sc = k < 2 ? s0 : s1;
+            o[4 * k + j] = pack_bf16x2(f.x * sc, f.y * sc);
+        }
+}
+
 }  // namespace dc
 
 // Shared by the tensor-core decode kernels (defined in decode_tc.cu): the merge of split
 // requests' partial slots into the output (B requests, C clusters), on stream st.
 cudaError_t launch_merge_slots(const float* o_part, const float* lse_part, const int32_t* meta,
-                               __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st);
+                               __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st,
+                               const float* sink = nullptr);
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
                uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw,
                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);

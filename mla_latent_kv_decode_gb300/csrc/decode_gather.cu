@@ -1,1109 +1,8 @@
-// decode_gather.cu -- tensor-core absorbed MLA decode over rows the kernel gathers itself: the
-// FP8 mixed cache (dense) and the top-k sparse path (both cache formats).
-//
-// It computes what decode_tc.cu computes ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token",
-// Fig. 4 (1), Fig. 5 (2), Fig. 6 (2)) and shares its organisation: clusters of two CTAs that
-// split the latent and rope dims (CTA r: latent [256 r, 256 r + 256), rope [32 r, 32 r + 32)),
-// the softmax split by heads between the pair (owners finish heads [64 r, 64 r + 64), agents
-// forward this CTA's partial scores of the other heads and place the P the peer sends back), the
-// lazily updated running max, the balanced tile schedule and the partial merge.  What differs is
-// where a tile's rows come from and how FP8 scales enter:
-//   * a tile is 64 rows: the positions of one cache page (dense), or 64 consecutive entries of a
-//     request's top-k list (sparse: only listed positions enter the softmax, same page, Fig. 8
-//     and the DSA description on that page).  Rows outside the request (past its length, padding
-//     entries, entries >= N_b) are masked and read as zeros;
-//   * FP8 records: a producer warp copies each tile's raw bytes of this CTA's half into a
-//     conversion slot as soon as PV has released it (a page: three TMA boxes; top-k rows: 21
-//     16-byte cp.async pieces per row, one row per lane), with the row's four group scales and a
-//     64-bit mask of valid rows; the agent warps then convert the slot in place into the MMA
-//     operand layouts: latent [64 x 256] (128-byte swizzle), rope [64 x 32] (64-byte swizzle),
-//     zeros for rows outside the request;
-//   * bf16 records (top-k only) are loaded by the agents from global memory straight into those
-//     layouts;
-//   * FP8 records (512 e4m3 codes, one fp32 scale per 128 dims, 64 bf16 rope dims; the 656-byte
-//     layout of the same page's FP8 section) convert exactly to f16: every e4m3 value is an f16
-//     value, and the MMAs of the latent dims run on f16 operands (this CTA's half of the latent
-//     query is converted from bf16 to f16 in place once per request, exact for |q| in the f16
-//     normal range).  The scale of each 128-dim group is applied in fp32 where the group meets
-//     the other factor: on the scores, S = s_a S_a + s_b S_b + S_rope with one tensor-memory
-//     accumulator per group, and on P, O_g += (P s_g) V_g for the PV of group g, with P s_g
-//     rounded once to f16 (2^-11).  The running max is kept within 2^8 of every P here, so P s_g
-//     stays finite for group scales below 255 (absmax below 114,000).  BF16 records take scale 1
-//     and bf16 operands throughout.
-//
-// Tensor memory (all 512 columns): O_r [0, 256), S_a [256, 320), S_b [320, 384),
-// S_rope [384, 448), P_a [448, 480), P_b [480, 512) (64 16-bit values per lane in 32 columns).
-// Shared memory: Q half (72 KB, TMA), three converted tiles (36 KB each), exchange buffers.
-//
-// Warp roles (608 threads): warp 0 Q loads (TMA) and the f16 conversion of Q; warp 1 MMA issuer
-// (+ TMEM owner); warps 2-17: thread = head = TMEM lane, four warps per 32-lane group, 16
-// positions of a tile each; the 8 warps on the owned heads' lanes run the softmax, the other 8
-// ("agents") forward partial scores, convert the tiles, place the peer's P and finish those O
-// rows; warp 18 loads the FP8 tiles.  Every wait is bounded: on expiry the kernel records
-// MLA_ERR_TIMEOUT, stops issuing, drains its MMAs, frees TMEM and returns.
-//
-// The kernel is a template over (record format, tile kind), instantiated for FP8 pages, FP8 top-k
-// rows and bf16 top-k rows, so that each instantiation holds only its own paths (at 608 threads
-// a thread has 96 registers; the shared code spilled twice as much).
-#include <cuda.h>
-#include <cstring>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-
-#include "decode_common.cuh"
+// decode_gather.cu -- instantiations of the gather decode kernel (decode_gather.cuh) for the MLA
+// record formats: FP8 mixed pages, FP8 mixed top-k rows and bf16 top-k rows; its plan and launch.
+#include "decode_gather.cuh"
 
 namespace mla {
-namespace {
-
-using namespace ptx;
-using namespace dc;
-
-constexpr int kSegCost = 1;           // a segment start costs about one tile (schedule units)
-constexpr int kNC = 3;                 // converted tile slots
-constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
-constexpr int kSlice = kT / 4;         // positions per warp
-constexpr int kProducerWarp = 2 + kSoftmaxThreads / 32;   // warp 18: FP8 tile loads
-constexpr int kThreads = 64 + kSoftmaxThreads + 32;
-constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps
-// the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
-// range of the exchange (bf16 records); 2^8 keeps P s_g within f16 range for s_g < 255 (FP8)
-constexpr float kLazySlackBf16 = 15.0f;
-constexpr float kLazySlackFp8 = 8.0f;
-constexpr float kMaxGroupScale = 255.0f;   // 2^8 * 255 = 65280: P s_g stays a finite f16
-constexpr int kHalfLat = 256;          // latent dims per CTA
-constexpr int kHalfRope = 32;          // rope dims per CTA
-constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256); group a [0, 128), group b [128, 256)
-constexpr uint32_t kTmemSa = 256;      // score accumulators of this CTA's two latent groups
-constexpr uint32_t kTmemSb = 320;
-constexpr uint32_t kTmemSr = 384;      // ... and of its rope dims
-constexpr uint32_t kTmemPa = 448;      // P times the group scales
-constexpr uint32_t kTmemPb = 480;
-constexpr uint32_t kDrainLimit = 1u << 20;
-
-// shared-memory layout (bytes from a 1024-aligned base)
-constexpr int kQLatChunk = 128 * 128;                  // [128 heads x 64 dims] bf16, SW128
-constexpr int kQRopeBytes = 128 * 64;                  // [128 heads x 32 dims] bf16, SW64
-constexpr int kKvLatChunk = kT * 128;                  // [64 rows x 64 dims], SW128
-constexpr int kConvBytes = 4 * kKvLatChunk + kT * 64;  // latent + rope [64 rows x 32 dims], SW64
-constexpr int kXBytes = kOwned * kT * 4;               // peer partial scores of owned heads, fp32
-constexpr int kPInBytes = kOwned * kT * 2;             // peer's P of its owned heads, fp16
-constexpr int kPInMsg = kPInBytes + kOwned * 4;        // + one rescale factor per head
-constexpr int kOffQ = 0;
-constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
-constexpr int kOffConv = kOffQRope + kQRopeBytes;      // 73728
-constexpr int kScaleBytes = kT * 16;                   // per slot: [64 rows][4 groups] fp32
-constexpr int kOffScale = kOffConv + kNC * kConvBytes; // 184320: [kNC][64 rows][4] fp32
-constexpr int kOffMask = kOffScale + kNC * kScaleBytes; // 187392: [kNC][2] uint32 valid rows
-constexpr int kOffX = kOffMask + 32;                   // 187424: 2 buffers [16][64][16 B]
-constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 220192: [8][64][16 B] + alpha[64]
-constexpr int kOffLIn = kOffPIn + kPInMsg;             // 228640: 2 x l[64] of the peer's heads
-constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 229152
-constexpr int kNumBars = 3 * kNC + 4 + 2 + 2 + 2 + 2 + 6;
-constexpr int kOffRed = (kOffBar + 8 * kNumBars + 15) & ~15;   // owned heads' exchange between slices [4][64]
-constexpr int kSmemBytes = kOffRed + 4 * kOwned * 4 + 1024;    // + alignment slack
-// raw FP8 bytes of one tile and CTA: codes [64][256] at the slot's start, rope [64][64 B] at its
-// rope region, scales [64][16 B]
-constexpr uint32_t kRawTileBytes = kT * (kHalfLat + 2 * kHalfRope + 16);   // 21504
-
-constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;     // 73728 per CTA
-static_assert(kSmemBytes + 64 <= 232448, "shared memory above the 227 KB a CTA may use");
-
-struct GatherParams {
-    const uint8_t* pool;
-    const int32_t* block_table;
-    const int32_t* seq_lens;
-    const int32_t* topk_idx;   // [B][topk] or null (dense)
-    __nv_bfloat16* out;
-    float* lse;
-    float* o_part;             // [2C][128][512]
-    float* lse_part;           // [2C][128]
-    int32_t* meta;             // per request: first partial slot, last cluster (2 x int32)
-    DevCtl* ctl;
-    int64_t num_pages;
-    int max_pages;
-    int max_seq_len;
-    int topk;
-    int B;
-    float scale_log2;          // scale * log2(e)
-};
-
-struct Bars {
-    uint32_t c_full, c_empty;     // arrays of kNC
-    uint32_t r_full;              // array of kNC: raw FP8 bytes of a tile landed
-    uint32_t s_full, s_empty, p_full, p_empty;
-    uint32_t x_full, x_free;      // arrays of 2
-    uint32_t pin_full, pin_free;
-    uint32_t l_full;              // array of 2
-    uint32_t q_full, q_ready, q_empty, o_full, o_free, mma_drain;
-    __device__ __forceinline__ uint32_t cf(int i) const { return c_full + 8 * i; }
-    __device__ __forceinline__ uint32_t ce(int i) const { return c_empty + 8 * i; }
-    __device__ __forceinline__ uint32_t rf(int i) const { return r_full + 8 * i; }
-    __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
-    __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
-    __device__ __forceinline__ uint32_t lf(int i) const { return l_full + 8 * i; }
-};
-
-__device__ __forceinline__ Bars make_bars(uint32_t a) {
-    Bars b;
-    b.c_full = a; a += 8 * kNC;
-    b.c_empty = a; a += 8 * kNC;
-    b.r_full = a; a += 8 * kNC;
-    b.s_full = a; a += 8;
-    b.s_empty = a; a += 8;
-    b.p_full = a; a += 8;
-    b.p_empty = a; a += 8;
-    b.x_full = a; a += 16;
-    b.x_free = a; a += 16;
-    b.pin_full = a; a += 8;
-    b.pin_free = a; a += 8;
-    b.l_full = a; a += 16;
-    b.q_full = a; a += 8;
-    b.q_ready = a; a += 8;
-    b.q_empty = a; a += 8;
-    b.o_full = a; a += 8;
-    b.o_free = a; a += 8;
-    b.mma_drain = a; a += 8;
-    return b;
-}
-
-// One instantiation per (record format, tile kind) in use: FP8 pages, FP8 top-k rows, bf16 top-k
-// rows (dense bf16 pages take decode_tc_kernel), so that each holds only its own paths.
-template <bool kFp8, bool kTopk>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_gather_kernel(const __grid_constant__ CUtensorMap tm_qlat,
-                         const __grid_constant__ CUtensorMap tm_qrope,
-                         const __grid_constant__ CUtensorMap tm_codes,    // FP8 pool as bytes:
-                         const __grid_constant__ CUtensorMap tm_krope,    // boxes of 64 rows x 256,
-                         const __grid_constant__ CUtensorMap tm_scl,      // 64 and 16 bytes
-                         GatherParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-    __shared__ uint32_t s_tmem_base;
-    __shared__ volatile int s_abort;
-    __shared__ int s_start_b, s_start_t;
-    __shared__ int s_n_local;
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const uint32_t r = cluster_rank();
-    const uint32_t peer = r ^ 1u;
-    const int c = blockIdx.x >> 1;
-    const int C = gridDim.x >> 1;
-    const uint32_t wait_limit = p.ctl->wait_limit;
-
-    const uint32_t sbase = smem_u32(sm);
-    const Bars bars = make_bars(sbase + kOffBar);
-
-    if (tid == 0) {
-        s_abort = 0;
-        s_start_b = p.B;
-        s_start_t = 0;
-        s_n_local = 0;
-    }
-    __syncthreads();
-    if (warp == 0)
-        schedule_warp(p.seq_lens, p.max_seq_len, p.B, p.topk, kSegCost, c, C, c == 0 && r == 0, p.meta,
-                      p.ctl, &s_n_local, &s_start_b, &s_start_t);
-
-    if (tid == 32) {
-        for (int i = 0; i < kNC; ++i) {
-            mbar_init(bars.cf(i), 8);    // one arrive per agent warp once its rows are written
-            mbar_init(bars.ce(i), 1);
-            // dense FP8 tiles: the producer's one arrival with the TMA bytes; top-k FP8 tiles: one
-            // arrival per producer lane once its copies land, plus one after the mask is written
-            mbar_init(bars.rf(i), kTopk ? 33 : 1);
-        }
-        mbar_init(bars.s_full, 1);
-        mbar_init(bars.s_empty, kSoftmaxThreads / 32);   // one arrive per softmax warp
-        mbar_init(bars.p_full, kSoftmaxThreads / 32);
-        mbar_init(bars.p_empty, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bars.xf(i), 1);
-            mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
-            mbar_init(bars.lf(i), 1);
-        }
-        mbar_init(bars.pin_full, 1);
-        mbar_init(bars.pin_free, 8);     // one remote arrive per peer agent warp
-        mbar_init(bars.q_full, 1);
-        mbar_init(bars.q_ready, 1);
-        mbar_init(bars.q_empty, 1);
-        mbar_init(bars.o_full, 1);
-        mbar_init(bars.o_free, kSoftmaxThreads / 32);
-        mbar_init(bars.mma_drain, 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&s_tmem_base), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    cluster_sync();   // the peer's barriers are initialised before any remote arrive / st.async
-    const uint32_t tmem = s_tmem_base;
-    const int n_local = s_n_local;   // tiles of this cluster
-    const int start_b = s_start_b, start_t = s_start_t;
-
-    // the record of row `row` of the tile at cursor cj, or null when the row is outside the
-    // request (it then reads as zeros); an out-of-pool page is recorded as MLA_ERR_BOUNDS
-    // (two stages, so that several rows' index loads, then their page loads, can be in flight)
-    constexpr int rec_bytes = kFp8 ? kFp8RecordBytes : kBf16RecordBytes;
-    auto row_pos = [&](const Cursor& cj, int row) -> int {   // visible position of the row, or -1
-        int pos = cj.t * kT + row;
-        if (kTopk) pos = pos < p.topk ? __ldg(p.topk_idx + (size_t)cj.b * p.topk + pos) : -1;
-        return pos >= 0 && pos < cj.n ? pos : -1;
-    };
-    auto page_of = [&](const Cursor& cj, int pos) -> int {
-        return pos >= 0 ? __ldg(p.block_table + (size_t)cj.b * p.max_pages + (pos >> 6)) : 0;
-    };
-    auto record_at = [&](int pos, int page) -> const uint8_t* {
-        if (pos < 0) return nullptr;
-        if (page < 0 || page >= p.num_pages) {
-            if (r == 0) record_error(p.ctl, MLA_ERR_BOUNDS, page);
-            return nullptr;
-        }
-        return p.pool + ((size_t)page * kPage + (pos & (kPage - 1))) * rec_bytes;
-    };
-    auto pos_record = [&](const Cursor& cj, int pos) -> const uint8_t* { return record_at(pos, page_of(cj, pos)); };
-    auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* { return pos_record(cj, row_pos(cj, row)); };
-
-    if (n_local == 0 && warp >= 2) {
-        // an empty range: its partial slots must not contribute to any merge
-        const int h = tid - 64;
-        if (r == 0 && h < kHeads) {
-            p.lse_part[(size_t)(2 * c) * kHeads + h] = -INFINITY;
-            p.lse_part[(size_t)(2 * c + 1) * kHeads + h] = -INFINITY;
-        }
-    }
-
-    if (warp == 0) {
-        // ------------------------------------------------------------------ Q loads (TMA) + f16
-        // FP8 records: once a request's Q half has landed, the whole warp converts its latent
-        // part from bf16 to f16 in place (the swizzle permutes whole 16-byte chunks, so each
-        // chunk keeps its place), then releases it to the MMA issuer.
-        Cursor cu;
-        if (lane == 0 && n_local > 0) {
-            tma_prefetch_desc(&tm_qlat);
-            tma_prefetch_desc(&tm_qrope);
-        }
-        cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-        int seg = 0;
-        for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-            if (!cu.first()) continue;
-            bool ok = !s_abort;
-            if (ok && seg > 0) ok = mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) fail(p.ctl, &s_abort, 1);
-                break;
-            }
-            if (lane == 0) {
-                const int qrow = cu.b * kHeads;
-                mbar_arrive_expect_tx(bars.q_full, kQBytes);
-                for (int k = 0; k < 4; ++k)
-                    tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
-                                (int)r * kHalfLat + 64 * k, qrow);
-                tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full, seg & 1, wait_limit));
-            if (!ok) {
-                if (lane == 0) fail(p.ctl, &s_abort, 19);
-                break;
-            }
-            if (kFp8) {
-                // an element that overflows f16 (|q| >= 65520) is outside this path's range
-                uint32_t inf = 0;
-#pragma unroll 8
-                for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
-                    uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
-                    const uint4 v = *q;
-                    const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                               bf16x2_to_f16x2(v.w));
-                    inf |= f16x2_inf_or_nan(f.x) | f16x2_inf_or_nan(f.y) | f16x2_inf_or_nan(f.z) |
-                           f16x2_inf_or_nan(f.w);
-                    *q = f;
-                }
-                fence_proxy_async_smem();
-                if (__any_sync(0xffffffffu, inf != 0) && lane == 0) record_error(p.ctl, MLA_ERR_RANGE, cu.b);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.q_ready);
-            ++seg;
-        }
-        // drain: the last Q load lands before this CTA may exit
-        if (lane == 0 && seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop so that its operands stay warp-uniform; one elected lane
-        // issues each MMA and commit.  QK of a tile: 8 MMAs per latent group into that group's
-        // accumulator (f16 operands for FP8 records), 2 rope MMAs (bf16); PV: per group, 4 MMAs
-        // of 128x128x16 with P times the group's scales from tensor memory.  One score set and
-        // one P set in tensor memory: QK of tile i + 1 follows the softmax's reads of tile i's
-        // scores, P of tile i + 1 follows PV of tile i.
-        if (n_local > 0) {
-            constexpr uint32_t id_qk = kFp8 ? idesc_f16(128, kT, 0, 0) : idesc_bf16(128, kT, 0, 0);
-            constexpr uint32_t id_qr = idesc_bf16(128, kT, 0, 0);
-            constexpr uint32_t id_pv = kFp8 ? idesc_f16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 1);
-            const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
-            const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
-            const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
-            const uint32_t lat_lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
-            const uint32_t rope_lo = (uint32_t)smem_desc(0, 16, 512, kSw64);
-            const uint32_t v_lo = (uint32_t)smem_desc(0, kKvLatChunk, 1024, kSw128);
-            const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
-            const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
-            Cursor cq, cp;
-            cq.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-            cp = cq;
-            int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
-            uint32_t polls = 0;
-            while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
-                if (iq < n_local && iq <= ip + 1) {
-                    const int s = iq % kNC;
-                    const bool ready = __shfl_sync(
-                        0xffffffffu,
-                        (!cq.first() || mbar_test(bars.q_ready, seg_q & 1)) &&
-                            mbar_test(bars.cf(s), (iq / kNC) & 1) && mbar_test(bars.s_empty, (iq & 1) ^ 1),
-                        0);
-                    if (ready) {
-                        tc_fence_after();
-                        const uint32_t st_lo = ((sbase + kOffConv + s * kConvBytes) >> 4) & 0x3FFF;
-                        if (elect_one()) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    mma_bf16_ss(tmem + (k < 2 ? kTmemSa : kTmemSb),
-                                                lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
-                                                lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qk, ((k & 1) | kk) != 0 ? 1u : 0u);
-#pragma unroll
-                            for (int kk = 0; kk < 2; ++kk)
-                                mma_bf16_ss(tmem + kTmemSr, rope_hi | (qr_lo + kk * 2),
-                                            rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
-                                            id_qr, kk != 0 ? 1u : 0u);
-                            mma_commit(bars.s_full);
-                            if (cq.last()) mma_commit(bars.q_empty);
-                        }
-                        __syncwarp();
-                        if (cq.last()) ++seg_q;
-                        cq.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                        ++iq;
-                        polls = 0;
-                        continue;
-                    }
-                }
-                const bool seg_first = cp.first();
-                const bool pv_ready = __shfl_sync(
-                    0xffffffffu,
-                    (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
-                        mbar_test(bars.p_full, ip & 1),
-                    0);
-                if (!pv_ready) {
-                    if (++polls > wait_limit) {
-                        if (lane == 0) fail(p.ctl, &s_abort, 6);
-                        break;
-                    }
-                    continue;
-                }
-                polls = 0;
-                tc_fence_after();
-                const uint32_t v = ((sbase + kOffConv + (ip % kNC) * kConvBytes) >> 4) & 0x3FFF;
-                if (elect_one()) {
-#pragma unroll
-                    for (int g = 0; g < 2; ++g)
-#pragma unroll
-                        for (int kk = 0; kk < kT / 16; ++kk) {
-                            const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
-                            mma_bf16_ts(tmem + kTmemO + 128 * g, tmem + (g == 0 ? kTmemPa : kTmemPb) + 8 * kk, vd,
-                                        id_pv, (!seg_first || kk > 0) ? 1u : 0u);
-                        }
-                    mma_commit(bars.p_empty);
-                    mma_commit(bars.ce(ip % kNC));
-                    if (cp.last()) mma_commit(bars.o_full);
-                }
-                __syncwarp();
-                if (cp.last()) ++seg_p;
-                cp.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                ++ip;
-            }
-        }
-        __syncwarp();
-    } else if (warp == kProducerWarp) {
-        // ------------------------------------------------------------------ FP8 tile loads
-        // Tile j's raw bytes into conversion slot j % kNC once PV of tile j - kNC has released it,
-        // with the mask of valid rows (written before the arrival the agents wait on).  A dense
-        // tile is one page: three TMA boxes of its 64 rows (rows past the request's end are
-        // loaded and then zeroed by the agents).  A top-k tile: each lane copies its two rows with
-        // 16-byte cp.async (21 pieces per row: 16 of codes, the scales, 4 of rope) and arrives
-        // once they have landed.  Pages: the next tile's rows are looked up after a tile is
-        // issued, and the page kPfAhead tiles ahead is prefetched into L2.  Top-k rows: index
-        // loads, page loads and records run as a three-stage pipeline (see below), and each
-        // tile's rows are prefetched into L2 one tile ahead of their copies.
-        if (kFp8 && n_local > 0) {
-            constexpr int kPfAhead = 3;
-            constexpr bool dense = !kTopk;
-            if (dense && lane == 0) {
-                tma_prefetch_desc(&tm_codes);
-                tma_prefetch_desc(&tm_krope);
-                tma_prefetch_desc(&tm_scl);
-            }
-            Cursor cj, cpf;   // the next tile to load, and (dense) the next tile to prefetch into L2
-            cj.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-            cpf = cj;
-            int j_pf = 0;
-            // L2 prefetch of the rows of the records given (dense: lane 0 holds the page's row 0)
-            auto prefetch = [&](const uint8_t* f0, const uint8_t* f1) {
-                if (dense) {
-                    if (f0) {
-                        const int y = (int)((f0 - p.pool) / kFp8RecordBytes);
-                        tma_prefetch_l2_2d(&tm_codes, kHalfLat * (int)r, y);
-                        tma_prefetch_l2_2d(&tm_krope, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
-                        tma_prefetch_l2_2d(&tm_scl, kFp8ScaleOff, y);
-                    }
-                } else {
-                    // the lines of the row's codes half and of its scales and rope
-                    const uint8_t* pq[2] = {f0, f1};
-#pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        if (pq[q]) {
-                            prefetch_line_l2(pq[q] + kHalfLat * (int)r);
-                            prefetch_line_l2(pq[q] + kHalfLat * (int)r + 128);
-                            prefetch_line_l2(pq[q] + kFp8ScaleOff);
-                            prefetch_line_l2(pq[q] + kFp8RecordBytes - 16);
-                        }
-                }
-            };
-            // Dense tiles: at the start of each iteration the page of tile j_pf (looked up by lane 0
-            // the iteration before) is prefetched and the page of the next tile to prefetch looked
-            // up; after a tile is issued, rows lane, lane + 32 of the next one are looked up.
-            const uint8_t* rec0 = nullptr;
-            const uint8_t* rec1 = nullptr;
-            const uint8_t* pf_page = nullptr;
-            auto prefetch_dense = [&]() {
-                prefetch(pf_page, nullptr);
-                pf_page = nullptr;
-                if (j_pf < n_local) {
-                    if (lane == 0) pf_page = row_record(cpf, 0);
-                    ++j_pf;
-                    cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-            };
-            // Top-k tiles: a three-stage pipeline in which every load is consumed one iteration
-            // after it is issued: index loads of tile j + 3, page loads of tile j + 2, records of
-            // tile j + 1 (whose rows are then prefetched into L2), run after tile j is issued.
-            Cursor cB = cj, cA = cj;   // the tiles of the page and index stages
-            int jB = 0, jA = 0;
-            int ia0 = -1, ia1 = -1;    // index stage results (raw list entries)
-            int pb0 = -1, pb1 = -1, gb0 = 0, gb1 = 0;   // page stage results: positions, pages
-            auto stage_a = [&]() {
-                ia0 = ia1 = -1;
-                if (jA < n_local) {
-                    const int e0 = cA.t * kT + lane, e1 = e0 + 32;
-                    const size_t base = (size_t)cA.b * p.topk;
-                    ia0 = e0 < p.topk ? __ldg(p.topk_idx + base + e0) : -1;
-                    ia1 = e1 < p.topk ? __ldg(p.topk_idx + base + e1) : -1;
-                }
-            };
-            auto stage_b = [&]() {   // consumes the index stage of the same tile, then advances it
-                pb0 = pb1 = -1;
-                if (jB < n_local) {
-                    pb0 = ia0 >= 0 && ia0 < cB.n ? ia0 : -1;
-                    pb1 = ia1 >= 0 && ia1 < cB.n ? ia1 : -1;
-                    gb0 = page_of(cB, pb0);
-                    gb1 = page_of(cB, pb1);
-                    ++jB;
-                    cB.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-                if (jA < n_local) {
-                    ++jA;
-                    cA.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-                stage_a();
-            };
-            auto lookups_topk = [&](bool load_next) {   // records of the tile the page stage holds
-                rec0 = load_next ? record_at(pb0, gb0) : nullptr;
-                rec1 = load_next ? record_at(pb1, gb1) : nullptr;
-                prefetch(rec0, rec1);
-                stage_b();
-            };
-            if (dense) {
-                for (int k = 0; k < kPfAhead; ++k) prefetch_dense();
-                rec0 = row_record(cj, lane);
-                rec1 = row_record(cj, lane + 32);
-            } else {
-                stage_a();    // tile 0
-                stage_b();    // tile 0 pages, tile 1 indices
-                lookups_topk(true);
-            }
-            int issued = 0;
-            for (int j = 0; j < n_local; ++j) {
-                if (dense) prefetch_dense();
-                const int slot = j % kNC;
-                const uint32_t m0 = __ballot_sync(0xffffffffu, rec0 != nullptr);
-                const uint32_t m1 = __ballot_sync(0xffffffffu, rec1 != nullptr);
-                bool ok = !s_abort;
-                if (ok && j >= kNC) ok = mbar_wait(bars.ce(slot), ((j / kNC) - 1) & 1, wait_limit);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) {
-                    if (lane == 0) fail(p.ctl, &s_abort, 20);
-                    break;
-                }
-                const uint32_t dst = sbase + kOffConv + slot * kConvBytes;
-                const uint32_t dst_rope = dst + 4 * kKvLatChunk;
-                const uint32_t dst_scl = sbase + kOffScale + slot * kScaleBytes;
-                const uint32_t bar = bars.rf(slot);
-                if (lane == 0) {
-                    uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * slot;
-                    mk[0] = m0;
-                    mk[1] = m1;
-                    if (dense && (m0 & 1u)) {   // row 0 of a dense tile is visible unless its page is not
-                        const int y = (int)((rec0 - p.pool) / kFp8RecordBytes);
-                        mbar_arrive_expect_tx(bar, kRawTileBytes);
-                        tma_load_2d(dst, &tm_codes, bar, kHalfLat * (int)r, y);
-                        tma_load_2d(dst_rope, &tm_krope, bar, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
-                        tma_load_2d(dst_scl, &tm_scl, bar, kFp8ScaleOff, y);
-                    } else {
-                        mbar_arrive(bar);
-                    }
-                }
-                if (!dense) {
-                    // each lane copies its row's 16-byte pieces starting at piece `lane`, so that
-                    // the 32 lanes of one copy instruction write different banks
-                    auto copy_row = [&](const uint8_t* rec, int row) {
-                        if (!rec) return;
-                        const uint8_t* cs = rec + kHalfLat * (int)r;
-#pragma unroll
-                        for (int k = 0; k < kHalfLat / 16; ++k) {
-                            const int q = (k + lane) & (kHalfLat / 16 - 1);
-                            cp_async16(dst + row * kHalfLat + 16 * q, cs + 16 * q);
-                        }
-                        cp_async16(dst_scl + row * 16, rec + kFp8ScaleOff);
-                        const uint8_t* rs = rec + kFp8RopeOff + 2 * kHalfRope * (int)r;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int q = (k + lane) & 3;
-                            cp_async16(dst_rope + row * 64 + 16 * q, rs + 16 * q);
-                        }
-                    };
-                    copy_row(rec0, lane);
-                    copy_row(rec1, lane + 32);
-                    cp_async_arrive_noinc(bar);
-                }
-                __syncwarp();
-                ++issued;
-                cj.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                if (dense) {
-                    rec0 = rec1 = nullptr;
-                    if (j + 1 < n_local) {
-                        rec0 = row_record(cj, lane);
-                        rec1 = row_record(cj, lane + 32);
-                    }
-                } else {
-                    lookups_topk(j + 1 < n_local);
-                }
-            }
-            // drain: the copies of the last tiles (one per slot) land before this CTA may exit
-            if (dense) {
-                if (lane == 0)
-                    for (int j = issued - 1; j >= 0 && j >= issued - kNC; --j)
-                        mbar_wait(bars.rf(j % kNC), (j / kNC) & 1, kDrainLimit);
-            } else {
-                cp_async_wait_all();
-            }
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------------ owners and agents
-        // Lane group lg = warp % 4 (the TMEM lanes this warp may access: heads 32 lg .. 32 lg + 31,
-        // thread = head), slice ts = (warp - 2) / 4 (positions 16 ts .. 16 ts + 15 of a tile, and
-        // O columns 64 ts .. 64 ts + 63 in corrections and epilogues).  Lane groups 2r, 2r + 1
-        // hold the owned heads.
-        //
-        // The four owner warps of a lane group meet at named barriers (ids 1 + lg, 5 + lg, 128
-        // threads), which cannot time out, so these loops never leave early: after a failed
-        // (bounded) wait they keep executing every barrier but skip the work, and waits return at
-        // once.  Wait results are made warp-uniform before any warp-collective tcgen05 instruction.
-        const int lg = warp & 3;
-        const int ts = (warp - 2) >> 2;
-        const int h = lg * 32 + lane;
-        const bool owner = (lg >> 1) == (int)r;
-        const int hh = h & (kOwned - 1);   // index among the owning CTA's heads
-        const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-        float* red = reinterpret_cast<float*>(sm + kOffRed);   // [4 slices][64 owned heads]
-
-        auto wwait = [&](uint32_t bar, uint32_t parity, int where) -> bool {
-            bool ok = !s_abort && mbar_wait(bar, parity, wait_limit);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok && lane == 0) fail(p.ctl, &s_abort, where);
-            return ok;
-        };
-
-        // group scales of the warp's 16 positions of tile i: element 2 t is (s_a, s_b) of
-        // position 16 ts + t (each row holds the scales of all four groups)
-        auto scales_of = [&](int i) -> const float2* {
-            return reinterpret_cast<const float2*>(sm + kOffScale + (i % kNC) * kScaleBytes) + 32 * ts + (int)r;
-        };
-
-        // this CTA's partial scores of tile i for the warp's 16 positions: s_a S_a + s_b S_b + S_rope
-        // (the tile's scales and mask, written by the agents, are read once its slot is complete)
-        auto load_s = [&](int i, float (&v)[16]) -> bool {
-            if (!wwait(bars.cf(i % kNC), (i / kNC) & 1, 18)) return false;
-            if (!wwait(bars.s_full, i & 1, 7)) return false;
-            const float2* sc = scales_of(i);
-            tc_fence_after();
-            {
-                uint32_t a[16], b[16];
-                tmem_ld16(tmem + lane_off + kTmemSa + kSlice * ts, a);
-                tmem_ld16(tmem + lane_off + kTmemSb + kSlice * ts, b);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float2 q = sc[2 * t];
-                    v[t] = fmaf(q.x, __uint_as_float(a[t]), q.y * __uint_as_float(b[t]));
-                }
-            }
-            {
-                uint32_t e[16];
-                tmem_ld16(tmem + lane_off + kTmemSr + kSlice * ts, e);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] += __uint_as_float(e[t]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.s_empty);
-            return true;
-        };
-
-        // O rows of this warp (its 64 columns) times alpha, once PV of tile i - 1 has completed
-        auto rescale_o = [&](int i, float alpha) {
-            if (!wwait(bars.p_empty, (i - 1) & 1, 10)) return;
-            tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const uint32_t col = kTmemO + 64 * ts + 32 * cc;
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + col, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                tmem_st32(tmem + lane_off + col, o);
-            }
-            tmem_wait_st();
-        };
-
-        // the warp's 16 P values of tile i (fp16 pairs from the softmax) times each group's
-        // scales into tensor memory, once PV of tile i - 1 has completed, then P ready for the
-        // MMA: f16 (P s_g) for FP8 records, bf16 P for bf16 records (scale 1)
-        auto store_p = [&](int i, const uint32_t (&pk)[8]) {
-            if (i >= 1 && !wwait(bars.p_empty, (i - 1) & 1, 11)) return;
-            uint32_t pa[8], pb[8];
-            if (kFp8) {
-                const float2* sc = scales_of(i);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 q0 = sc[4 * k], q1 = sc[4 * k + 2];
-                    __half2 h2;
-                    *reinterpret_cast<uint32_t*>(&h2) = pk[k];
-                    const float2 pf = __half22float2(h2);
-                    pa[k] = pack_f16x2(pf.x * q0.x, pf.y * q1.x);
-                    pb[k] = pack_f16x2(pf.x * q0.y, pf.y * q1.y);
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    __half2 h2;
-                    *reinterpret_cast<uint32_t*>(&h2) = pk[k];
-                    const float2 pf = __half22float2(h2);
-                    pa[k] = pb[k] = pack_bf16x2(pf.x, pf.y);
-                }
-            }
-            tmem_st8(tmem + lane_off + kTmemPa + 8 * ts, pa);
-            tmem_st8(tmem + lane_off + kTmemPb + 8 * ts, pb);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && !s_abort) mbar_arrive(bars.p_full);
-        };
-
-        // O rows of this warp normalised by l (row sum) into the output or a partial slot
-        auto epilogue_rows = [&](int seg, const Cursor& cu, bool partial, float l_row) {
-            const int slot = 2 * c + (seg == 0 ? 0 : 1);
-            if (!wwait(bars.o_full, seg & 1, 12)) return;
-            tc_fence_after();
-            const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
-            const size_t row = (size_t)cu.b * kHeads + h;
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kTmemO + 64 * ts + 32 * cc, o);
-                tmem_wait_ld();
-                const int col = (int)r * kHalfLat + 64 * ts + 32 * cc;
-                if (!partial) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.o_free);
-        };
-
-        Cursor cu;
-        cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-        int seg = 0;
-        bool cut_front = false;
-
-        // Tile preparation (called by the agents): thread `at` of the 256 agent threads.
-        const int at = ((lg & 1) * 4 + ts) * 32 + lane;
-        // Tile j (cursor cj) into conversion slot j % kNC: this CTA's half of every row in the
-        // MMA layouts, zeros for rows outside the request.  FP8 records: the producer warp has
-        // put the raw bytes into the slot (codes [64][256] at its start, rope [64][64 B] in its
-        // rope region, scales [64][16 B], the mask of valid rows); each agent thread reads its
-        // 16-byte pieces, all agents meet, and each writes its pieces converted.  bf16 records:
-        // the rows are loaded from global memory once PV of tile j - kNC has freed the slot.
-        auto prepare = [&](int j, const Cursor& cj) {
-            const int slot = j % kNC;
-            uint8_t* lat = sm + kOffConv + slot * kConvBytes;
-            uint8_t* rope = lat + 4 * kKvLatChunk;
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            if (kFp8) {
-                const bool ok = wwait(bars.rf(slot), (j / kNC) & 1, 17);
-                const uint32_t* mk = reinterpret_cast<const uint32_t*>(sm + kOffMask) + 2 * slot;
-                const uint32_t mk0 = mk[0], mk1 = mk[1];
-                auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
-                uint4 raw[4], rraw = zero;
-                if (ok) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) raw[k] = *reinterpret_cast<const uint4*>(lat + (at + 256 * k) * 16);
-                    rraw = *reinterpret_cast<const uint4*>(rope + at * 16);
-                }
-                named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
-                if (ok) {
-                    // 64 rows x 16 chunks of 16 codes; piece at + 256 k is chunk ch of row `row`
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = at + 256 * k, row = e >> 4, ch = e & 15;
-                        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                        if (valid(row)) e4m3x16_to_f16(raw[k], o);
-                        // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte
-                        // parts 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
-                        uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
-                        const int s0 = 2 * (ch & 3);
-                        st_shared_v4(dst + ((s0 ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
-                        st_shared_v4(dst + (((s0 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
-                    }
-                    // rope: 64 rows x 4 chunks of 8 dims, 64-byte swizzle
-                    const int row = at >> 2, c4 = at & 3;
-                    if (!valid(row)) rraw = zero;
-                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
-                    // scales of rows outside the request: zero (their P is zero); a visible row
-                    // whose group scale is above 255 (or not finite) would overflow f16(P s_g)
-                    if (at < kT) {
-                        uint4* sc = reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + at * 16);
-                        if (!valid(at)) {
-                            *sc = zero;
-                        } else {
-                            const uint4 q = *sc;   // (a NaN fails every comparison)
-                            if (!(__uint_as_float(q.x) <= kMaxGroupScale) || !(__uint_as_float(q.y) <= kMaxGroupScale) ||
-                                !(__uint_as_float(q.z) <= kMaxGroupScale) || !(__uint_as_float(q.w) <= kMaxGroupScale))
-                                record_error(p.ctl, MLA_ERR_RANGE, cj.b);
-                        }
-                    }
-                }
-            } else {
-                // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k
-                // (the first half loaded before the wait)
-                const int rope_off = 2 * kDc + 2 * kHalfRope * (int)r;
-                const uint8_t* rrec = row_record(cj, at >> 2);
-                const uint4 rraw = rrec ? __ldg(reinterpret_cast<const uint4*>(rrec + rope_off + 16 * (at & 3))) : zero;
-                const uint8_t* srec = at < kT ? row_record(cj, at) : nullptr;
-                uint4 raw[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = at + 256 * k, row = e >> 5, ch = e & 31;
-                    const uint8_t* rec = row_record(cj, row);
-                    raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
-                }
-                if (j >= kNC && !wwait(bars.ce(slot), ((j / kNC) - 1) & 1, 17)) return;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    if (half == 1) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int e = at + 256 * (4 + k), row = e >> 5, ch = e & 31;
-                            const uint8_t* rec = row_record(cj, row);
-                            raw[k] = rec ? __ldg(reinterpret_cast<const uint4*>(rec + 2 * kHalfLat * (int)r + 16 * ch)) : zero;
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = at + 256 * (4 * half + k), row = e >> 5, ch = e & 31;
-                        st_shared_v4(lat + (ch >> 3) * kKvLatChunk + row * 128 + (((ch & 7) ^ (row & 7)) << 4),
-                                     raw[k].x, raw[k].y, raw[k].z, raw[k].w);
-                    }
-                }
-                {
-                    // rope: 64 rows x 4 chunks of 8 dims, 64-byte swizzle
-                    const int row = at >> 2, c4 = at & 3;
-                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
-                }
-                if (at < kT) {
-                    // the row's group scales (1 for bf16 records) and the valid-row mask
-                    reinterpret_cast<float2*>(sm + kOffScale + slot * kScaleBytes)[2 * at + (int)r] = make_float2(1.f, 1.f);
-                    const uint32_t m = __ballot_sync(0xffffffffu, srec != nullptr);
-                    if (lane == 0) reinterpret_cast<uint32_t*>(sm + kOffMask)[2 * slot + (at >> 5)] = m;
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.cf(slot));
-        };
-
-        Cursor cpr = cu;   // next tile to prepare
-        int i_pr = 0;
-        auto prepare_until = [&](int upto) {
-            for (; i_pr < upto && i_pr < n_local; ++i_pr, cpr.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) prepare(i_pr, cpr);
-        };
-        // bf16 records: L2 prefetch of the rows of tile i + 5 during iteration i (tile i + 2 is
-        // prepared in iteration i, so prefetches run three iterations ahead): thread `at` covers
-        // part at / 64 (latent bytes, rope) of row at % 64.  Its address comes from the index
-        // loads of the iteration before, so their latency overlaps an iteration.  (FP8 tiles are
-        // prefetched by warp 18.)
-        const int pf_row = at & (kT - 1), pf_part = at >> 6;
-        const uint32_t pf_bytes = pf_part == 0 ? (kFp8 ? kHalfLat : 2 * kHalfLat) : (pf_part == 1 ? 64 : 16);
-        const int pf_off = pf_part == 0 ? (kFp8 ? kHalfLat : 2 * kHalfLat) * (int)r
-                                        : (pf_part == 1 ? (kFp8 ? kFp8RopeOff : 2 * kDc) + 64 * (int)r : kFp8ScaleOff);
-        const bool pf_on = !kFp8 && pf_part < 2;   // FP8 tiles: the producer warp prefetches
-        Cursor cpf = cu;   // the tile whose prefetch address is computed next (tiles 0, 1 are
-        int i_pf = 0;      // prepared at once)
-        for (; i_pf < 2 && i_pf < n_local; ++i_pf) cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-        const uint8_t* pf_rec = nullptr;
-        auto prefetch_step = [&]() {
-            if (pf_rec) prefetch_l2(pf_rec + pf_off, pf_bytes);
-            pf_rec = nullptr;
-            if (i_pf < n_local) {
-                if (pf_on) pf_rec = row_record(cpf, pf_row);
-                ++i_pf;
-                cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-            }
-        };
-        if (!owner) {
-            // ------------------------------------------------------------ agents
-            const uint32_t x_remote = mapa(sbase + kOffX, peer);
-            const uint32_t xfull_remote = mapa(bars.x_full, peer);
-            const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
-            const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
-
-            // forward this CTA's partial scores of tile i (the peer's heads) to the peer
-            auto forward = [&](int i) {
-                float v[16];
-                if (!load_s(i, v)) return;
-                const int xb = i & 1;
-                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) return;
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    st_async_v4(x_remote + xb * kXBytes + ((4 * ts + g) * kOwned + hh) * 16,
-                                xfull_remote + 8 * xb, __float_as_uint(v[4 * g]), __float_as_uint(v[4 * g + 1]),
-                                __float_as_uint(v[4 * g + 2]), __float_as_uint(v[4 * g + 3]));
-            };
-
-            for (int k = 0; k < 4; ++k) prefetch_step();   // tiles 2, 3, 4 prefetched, 5 addressed
-            prepare_until(2);
-            if (n_local > 0) forward(0);
-            // Iteration i: the peer's P of tile i into tensor memory (PV of tile i can then go),
-            // then this CTA's scores of tile i + 1 to the peer and tile i + 2 converted.
-            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-                const bool first = cu.first();
-                if (first) cut_front = cu.t > 0;
-                // the peer's P of its heads for tile i, and its rescale factors
-                if (lead && !s_abort) mbar_arrive_expect_tx(bars.pin_full, kPInMsg);
-                const bool ok = wwait(bars.pin_full, i & 1, 13);
-                uint32_t pk[8];
-                const uint8_t* pin = sm + kOffPIn;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const uint4 q = *reinterpret_cast<const uint4*>(pin + ((2 * ts + g) * kOwned + hh) * 16);
-                    pk[4 * g] = q.x;
-                    pk[4 * g + 1] = q.y;
-                    pk[4 * g + 2] = q.z;
-                    pk[4 * g + 3] = q.w;
-                }
-                const float alpha = reinterpret_cast<const float*>(pin + kPInBytes)[hh];
-                __syncwarp();
-                if (lane == 0 && ok) mbar_arrive_remote_relaxed(pinfree_remote);
-                if (!first && __any_sync(0xffffffffu, ok && alpha != 1.0f)) rescale_o(i, alpha);
-                store_p(i, pk);
-                if (cu.last()) {
-                    const bool partial = cut_front || cu.t < cu.nt - 1;
-                    // the row sums of these heads, sent by the peer's owners
-                    if (lead && !s_abort) mbar_arrive_expect_tx(bars.lf(seg & 1), kOwned * 4);
-                    const bool lok = wwait(bars.lf(seg & 1), (seg >> 1) & 1, 14);
-                    const float l_row = lok ? reinterpret_cast<const float*>(sm + kOffLIn)[(seg & 1) * kOwned + hh] : 0.f;
-                    epilogue_rows(seg, cu, partial, l_row);
-                    ++seg;
-                }
-                if (i + 1 < n_local) forward(i + 1);
-                prepare_until(i + 3);
-                prefetch_step();
-            }
-        } else {
-            // ------------------------------------------------------------ owners
-            const uint32_t pin_remote = mapa(sbase + kOffPIn, peer);
-            const uint32_t pinfull_remote = mapa(bars.pin_full, peer);
-            const uint32_t xfree_remote = mapa(bars.x_free, peer);
-            const uint32_t lin_remote = mapa(sbase + kOffLIn, peer);
-            const uint32_t lfull_remote = mapa(bars.l_full, peer);
-            const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
-            const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
-            constexpr float slack = kFp8 ? kLazySlackFp8 : kLazySlackBf16;
-            const float p_max = exp2f(slack);
-            float m_used = -INFINITY, l_part = 0.f;
-            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-                const int xb = i & 1;
-                const bool first = cu.first();
-                if (first) {
-                    m_used = -INFINITY;
-                    l_part = 0.f;
-                    cut_front = cu.t > 0;   // the request started before this cluster's range
-                }
-                float v[16];
-                load_s(i, v);
-                // valid rows of this warp's 16 positions
-                const uint32_t vmask =
-                    (reinterpret_cast<const uint32_t*>(sm + kOffMask)[2 * (i % kNC) + (ts >> 1)] >> (16 * (ts & 1))) & 0xFFFFu;
-                // the peer's partial scores of these heads for tile i
-                if (lead && !s_abort) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
-                const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
-                float x[16];
-                const uint8_t* xp = sm + kOffX + xb * kXBytes;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * kOwned + hh) * 16);
-                    x[4 * g] = (v[4 * g] + q.x) * p.scale_log2;
-                    x[4 * g + 1] = (v[4 * g + 1] + q.y) * p.scale_log2;
-                    x[4 * g + 2] = (v[4 * g + 2] + q.z) * p.scale_log2;
-                    x[4 * g + 3] = (v[4 * g + 3] + q.w) * p.scale_log2;
-                }
-                // every loaded value has been consumed: hand the exchange buffer back to the peer
-                __syncwarp();
-                if (lane == 0 && xok) mbar_arrive_remote_relaxed(xfree_remote + 8 * xb);
-                // P = 2^(x - m) with the running max m (rows outside the request give 0).  m is
-                // kept while every P of a row stays at most 2^slack: a thread whose 16 P sum past
-                // 2^slack (or not to a finite value) votes for the rare path, as does every segment
-                // start and a row with no visible position yet.  There the exact row max over the
-                // four slices raises m where it exceeds m by more than the slack, O is rescaled
-                // here and, through alpha sent with P, in the peer, and P is computed again.
-                float alpha = 1.0f;
-                float psum;
-                uint32_t pk[8];
-                auto exp_tile = [&]() {
-                    psum = 0.f;
-#pragma unroll
-                    for (int t = 0; t < 16; t += 2) {
-                        const bool live = m_used != -INFINITY;
-                        const float p0 = (live && ((vmask >> t) & 1)) ? ex2(x[t] - m_used) : 0.f;
-                        const float p1 = (live && ((vmask >> (t + 1)) & 1)) ? ex2(x[t + 1] - m_used) : 0.f;
-                        psum += p0 + p1;
-                        const __half2 h2 = __floats2half2_rn(p0, p1);
-                        pk[t / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-                    }
-                };
-                exp_tile();
-                const bool need = first || m_used == -INFINITY || !(psum <= p_max);
-                if (bar_red_or(bar_vote, 128, need)) {
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        if ((vmask >> t) & 1) mx = fmaxf(mx, x[t]);
-                    red[ts * kOwned + hh] = mx;
-                    named_bar_sync(bar_sync, 128);
-                    const float tmax = fmaxf(fmaxf(red[hh], red[kOwned + hh]), fmaxf(red[2 * kOwned + hh], red[3 * kOwned + hh]));
-                    const bool grow = first || tmax > m_used + slack;
-                    const float m_new = grow ? (first ? tmax : fmaxf(tmax, m_used)) : m_used;
-                    if (!first) {
-                        alpha = grow ? ex2(m_used - m_new) : 1.0f;
-                        if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha);
-                        l_part *= alpha;
-                    }
-                    m_used = m_new;
-                    named_bar_sync(bar_sync, 128);   // red[] rows of this lane group are free again
-                    exp_tile();
-                }
-                l_part += psum;
-                // P of these heads (fp16, before the group scales) to the peer, once it has taken
-                // the previous one; both CTAs apply their group scales to these values
-                if (wwait(bars.pin_free, (i & 1) ^ 1, 15)) {
-#pragma unroll
-                    for (int g = 0; g < 2; ++g)
-                        st_async_v4(pin_remote + ((2 * ts + g) * kOwned + hh) * 16, pinfull_remote,
-                                    pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-                    if (ts == 0)
-                        st_async_b32(pin_remote + kPInBytes + hh * 4, pinfull_remote, __float_as_uint(alpha));
-                }
-                store_p(i, pk);
-
-                if (cu.last()) {
-                    // ------------------------------------------------------ segment epilogue
-                    const bool partial = cut_front || cu.t < cu.nt - 1;
-                    red[ts * kOwned + hh] = l_part;
-                    named_bar_sync(bar_sync, 128);
-                    const float l_row = (red[hh] + red[kOwned + hh]) + (red[2 * kOwned + hh] + red[3 * kOwned + hh]);
-                    named_bar_sync(bar_sync, 128);
-                    // the row sums of these heads to the peer, which finishes its O rows of them
-                    if (ts == 0 && !s_abort)
-                        st_async_b32(lin_remote + ((seg & 1) * kOwned + hh) * 4,
-                                     lfull_remote + 8 * (seg & 1), __float_as_uint(l_row));
-                    const float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
-                    if (ts == 0) {
-                        const size_t row = (size_t)cu.b * kHeads + h;
-                        if (!partial) p.lse[row] = L;
-                        else p.lse_part[(size_t)(2 * c + (seg == 0 ? 0 : 1)) * kHeads + h] = L;
-                    }
-                    epilogue_rows(seg, cu, partial, l_row);
-                    ++seg;
-                }
-            }
-        }
-    }
-
-    // ---------------------------------------------------------------------- teardown
-    if (warp == 1 && n_local > 0) {
-        __syncwarp();
-        // all MMAs issued by the elected lane (the lowest active one, as in the loop) are complete
-        // once this barrier flips
-        if (elect_one()) {
-            mma_commit(bars.mma_drain);
-            if (!mbar_wait(bars.mma_drain, 0, kDrainLimit)) record_error(p.ctl, MLA_ERR_TIMEOUT, 16);
-        }
-    }
-    __syncwarp();
-    if (s_abort) __nanosleep(100000);   // let any in-flight distributed-shared-memory stores land
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    cluster_sync();   // the peer no longer writes into this CTA's shared memory
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
-
-}  // namespace
 
 // Same workspace as the dense bf16 kernel: 2 partial slots per cluster (fp32 [128][512] + lse
 // [128]), then per request its first partial slot and last cluster (int32 [B][2]).
@@ -1120,68 +19,13 @@ DecodePlan plan_decode_gather(int fmt, int B, int max_seq_len, int topk, int sms
 }
 
 cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t st) {
-    const bool fp8 = a.fmt == MLA_KV_FP8_MIXED;
     const bool topk = a.topk_idx != nullptr && a.topk > 0;
-    if (!fp8 && !topk) return cudaErrorInvalidValue;   // dense bf16 pages: decode_tc_kernel
-    const int mode = fp8 ? (topk ? 1 : 0) : 2;
-    auto* kernel = mode == 0 ? decode_gather_kernel<true, false>
-                 : mode == 1 ? decode_gather_kernel<true, true>
-                             : decode_gather_kernel<false, true>;
-    static bool attr_set[64][3] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev][mode]) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev][mode] = true;
-    }
-    CUtensorMap tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl;
-    const uint64_t qrows = (uint64_t)a.B * kHeads;
-    if (!encode_2d(&tm_qlat, a.q_lat, kDc, qrows, kDc * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tm_qrope, a.q_rope, kDr, qrows, kDr * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
-        return cudaErrorInvalidValue;
-    std::memset(&tm_codes, 0, sizeof(tm_codes));
-    std::memset(&tm_krope, 0, sizeof(tm_krope));
-    std::memset(&tm_scl, 0, sizeof(tm_scl));
-    if (a.fmt == MLA_KV_FP8_MIXED && (a.topk_idx == nullptr || a.topk <= 0)) {
-        // the pool as rows of 656 bytes; a box is 64 rows (one page) of a record's byte range
-        const uint64_t rows = (uint64_t)a.num_pages * kPage;
-        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-        if (!encode_2d(&tm_codes, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, kHalfLat, kT,
-                       CU_TENSOR_MAP_SWIZZLE_NONE, u8) ||
-            !encode_2d(&tm_krope, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, 2 * kHalfRope, kT,
-                       CU_TENSOR_MAP_SWIZZLE_NONE, u8) ||
-            !encode_2d(&tm_scl, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, 16, kT,
-                       CU_TENSOR_MAP_SWIZZLE_NONE, u8))
-            return cudaErrorInvalidValue;
-    }
-    const int C = plan.splits;
-    float* o_part = static_cast<float*>(a.workspace);
-    float* lse_part = o_part + (size_t)2 * C * kHeads * kDc;
-    int32_t* meta = reinterpret_cast<int32_t*>(lse_part + (size_t)2 * C * kHeads);
-    GatherParams p;
-    p.pool = a.pool;
-    p.block_table = a.block_table;
-    p.seq_lens = a.seq_lens;
-    p.topk_idx = a.topk > 0 ? a.topk_idx : nullptr;
-    p.out = a.out;
-    p.lse = a.lse;
-    p.o_part = o_part;
-    p.lse_part = lse_part;
-    p.meta = meta;
-    p.ctl = a.ctl;
-    p.num_pages = a.num_pages;
-    p.max_pages = a.max_pages;
-    p.max_seq_len = a.max_seq_len;
-    p.topk = a.topk_idx != nullptr ? a.topk : 0;
-    p.B = a.B;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
-    kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st);
+    if (a.fmt == MLA_KV_V4_FP8 || a.fmt == MLA_KV_V41_FP4) return launch_decode_shared(a, plan, st);
+    if (a.fmt == MLA_KV_FP8_MIXED)
+        return topk ? launch_gather_instance<MLA_KV_FP8_MIXED, true>(a, plan, st)
+                    : launch_gather_instance<MLA_KV_FP8_MIXED, false>(a, plan, st);
+    if (!topk) return cudaErrorInvalidValue;   // dense bf16 pages: decode_tc_kernel
+    return launch_gather_instance<MLA_KV_BF16, true>(a, plan, st);
 }
 
 }  // namespace mla

@@ -874,14 +874,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 //   * deep (many slots, few requests): block (b, h); every warp forms the log-sum-exp, warp w
 //     accumulates slots w, w + 8, ... over the whole row and shared memory sums the eight rows.
 __device__ __forceinline__ float merge_lse(const float* __restrict__ lse_part, int first, int c_lo, int n,
-                                           int h, int lane) {
-    float m = -INFINITY;
+                                           int h, int lane, float z) {
+    // z: the head's sink (shared K = V entries; -inf for none), one more term of the sum
+    float m = z;
     for (int k = lane; k < n; k += 32)
         m = fmaxf(m, __ldg(lse_part + (size_t)(k == 0 ? first : 2 * (c_lo + k)) * kHeads + h));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (m == -INFINITY) return -INFINITY;
-    float l = 0.f;
+    float l = lane == 0 && z != -INFINITY ? expf(z - m) : 0.f;
     for (int k = lane; k < n; k += 32)
         l += expf(__ldg(lse_part + (size_t)(k == 0 ? first : 2 * (c_lo + k)) * kHeads + h) - m);
 #pragma unroll
@@ -912,7 +913,8 @@ __device__ __forceinline__ void merge_rows(const float* __restrict__ o_part, con
 __global__ void __launch_bounds__(256) merge_wide_kernel(const float* __restrict__ o_part,
                                                          const float* __restrict__ lse_part,
                                                          const int32_t* __restrict__ meta,
-                                                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                                                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                         const float* __restrict__ sink) {
     const int b = blockIdx.x >> 4;
     const int lane = threadIdx.x & 31;
     const int h = (blockIdx.x & 15) * 8 + (threadIdx.x >> 5);
@@ -922,10 +924,11 @@ __global__ void __launch_bounds__(256) merge_wide_kernel(const float* __restrict
     float4 acc[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = -INFINITY;
+    const float z = sink != nullptr ? __ldg(sink + h) : -INFINITY;
+    float L = z;   // no visible position: lse = ln exp(z') (-inf without a sink)
     if (first >= 0) {
         const int n = c_hi - c_lo + 1;
-        L = merge_lse(lse_part, first, c_lo, n, h, lane);
+        L = merge_lse(lse_part, first, c_lo, n, h, lane, z);
         if (L != -INFINITY) merge_rows(o_part, lse_part, first, c_lo, n, 0, 1, h, lane, L, acc);
     }
     uint2* dst = reinterpret_cast<uint2*>(out + ((size_t)b * kHeads + h) * kDc) + lane;
@@ -942,7 +945,8 @@ __global__ void __launch_bounds__(256) merge_wide_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) merge_deep_kernel(const float* __restrict__ o_part,
                                                          const float* __restrict__ lse_part,
                                                          const int32_t* __restrict__ meta,
-                                                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                                                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                         const float* __restrict__ sink) {
     __shared__ float4 red[8][kDc / 4];
     const int b = blockIdx.x / kHeads, h = blockIdx.x % kHeads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -952,10 +956,11 @@ __global__ void __launch_bounds__(256) merge_deep_kernel(const float* __restrict
     float4 acc[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = -INFINITY;
+    const float z = sink != nullptr ? __ldg(sink + h) : -INFINITY;
+    float L = z;   // no visible position: lse = ln exp(z') (-inf without a sink)
     if (first >= 0) {
         const int n = c_hi - c_lo + 1;
-        L = merge_lse(lse_part, first, c_lo, n, h, lane);
+        L = merge_lse(lse_part, first, c_lo, n, h, lane, z);
         if (L != -INFINITY) merge_rows(o_part, lse_part, first, c_lo, n, warp, 8, h, lane, L, acc);
     }
 #pragma unroll
@@ -980,17 +985,17 @@ __global__ void __launch_bounds__(256) merge_deep_kernel(const float* __restrict
 }
 
 cudaError_t launch_merge_slots(const float* o_part, const float* lse_part, const int32_t* meta,
-                               __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st) {
+                               __nv_bfloat16* out, float* lse, int B, int C, cudaStream_t st, const float* sink) {
     if (B <= 0) return cudaSuccess;
     // a request spans about C / B + 1 cluster ranges
     if ((C + B - 1) / B + 1 <= 8) {
         const int64_t blocks = (int64_t)B * (kHeads / 8);
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        merge_wide_kernel<<<(unsigned)blocks, 256, 0, st>>>(o_part, lse_part, meta, out, lse);
+        merge_wide_kernel<<<(unsigned)blocks, 256, 0, st>>>(o_part, lse_part, meta, out, lse, sink);
     } else {
         const int64_t blocks = (int64_t)B * kHeads;
         if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        merge_deep_kernel<<<(unsigned)blocks, 256, 0, st>>>(o_part, lse_part, meta, out, lse);
+        merge_deep_kernel<<<(unsigned)blocks, 256, 0, st>>>(o_part, lse_part, meta, out, lse, sink);
     }
     return cudaGetLastError();
 }

@@ -61,14 +61,15 @@ using namespace mla;
 namespace {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool fmt_ok(int32_t fmt) { return fmt == MLA_KV_BF16 || fmt == MLA_KV_FP8_MIXED; }
+bool shared_fmt_ok(int32_t fmt) { return fmt == MLA_KV_V4_FP8 || fmt == MLA_KV_V41_FP4; }
 mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 // The kernels are built for sm_103a only; any other device would fail at launch.
 bool device_supported() { return device_cc() == 103; }
 
 // mla_decode's checks of its sizes and scale (no pointer is looked at)
 mla_status decode_shape_status(int32_t fmt, int64_t num_pages, int32_t max_pages, int32_t max_seq_len,
-                               int32_t topk, int32_t B, int32_t H, float scale) {
-    if (!fmt_ok(fmt) || B < 0 || H != kHeads || num_pages < 0 || max_pages < 0 ||
+                               int32_t topk, int32_t B, int32_t H, float scale, bool shared = false) {
+    if (!(shared ? shared_fmt_ok(fmt) : fmt_ok(fmt)) || B < 0 || H != kHeads || num_pages < 0 || max_pages < 0 ||
         max_seq_len < 0 || topk < 0)
         return MLA_ERR_INVALID;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
@@ -97,6 +98,8 @@ extern "C" {
 size_t mla_record_bytes(int32_t fmt) {
     if (fmt == MLA_KV_BF16) return kBf16RecordBytes;
     if (fmt == MLA_KV_FP8_MIXED) return kFp8RecordBytes;
+    if (fmt == MLA_KV_V4_FP8) return kV4EntryBytes;
+    if (fmt == MLA_KV_V41_FP4) return kV41EntryBytes;
     return 0;
 }
 
@@ -162,7 +165,7 @@ mla_status mla_topk_select(const float* scores, int64_t ld, const int32_t* seq_l
 
 size_t mla_decode_workspace_bytes(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len,
                                   int32_t topk) {
-    if (!fmt_ok(fmt) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;
+    if (!(fmt_ok(fmt) || shared_fmt_ok(fmt)) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;
     int sms = num_sms();
     if (sms <= 0) sms = 152;
     return plan_decode(fmt, B, max_seq_len, topk, sms).workspace;
@@ -170,7 +173,7 @@ size_t mla_decode_workspace_bytes(int32_t fmt, int32_t B, int32_t H, int32_t max
 
 int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_len,
                             int32_t topk) {
-    if (!fmt_ok(fmt) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;
+    if (!(fmt_ok(fmt) || shared_fmt_ok(fmt)) || B <= 0 || H != kHeads || max_seq_len < 0 || topk < 0) return 0;
     int sms = num_sms();
     if (sms <= 0) sms = 152;
     return plan_decode(fmt, B, max_seq_len, topk, sms).launches;
@@ -272,6 +275,60 @@ mla_status mla_combine(const float* o_part, const float* lse_part, int32_t S, in
     if (!device_supported()) return MLA_ERR_UNSUPPORTED;
     return from_cuda(launch_combine(o_part, lse_part, S, B, H, static_cast<__nv_bfloat16*>(out),
                                     lse, stream));
+}
+
+mla_status mla_shared_kv_append(int32_t fmt, void* pool, int64_t num_pages, const void* entry,
+                                const int32_t* slot, int64_t T, cudaStream_t stream) {
+    if (!shared_fmt_ok(fmt) || T < 0 || num_pages < 0) return MLA_ERR_INVALID;
+    if (T == 0) return MLA_OK;
+    if (!pool || !entry || !slot) return MLA_ERR_INVALID;
+    if (!aligned(pool, 128) || !aligned(entry, 16) || !aligned(slot, 4)) return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    return from_cuda(launch_shared_append(fmt, static_cast<uint8_t*>(pool), num_pages,
+                                          static_cast<const __nv_bfloat16*>(entry), slot, T, ctl, stream));
+}
+
+mla_status mla_shared_kv_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q,
+                                const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                                int32_t max_seq_len, const int32_t* topk_idx, int32_t topk, int32_t B,
+                                int32_t H, float scale, const float* sink, const float* rope_cs, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    mla_status st = decode_shape_status(fmt, num_pages, max_pages, max_seq_len, topk, B, H, scale, true);
+    if (st != MLA_OK || B == 0) return st;
+    // (q takes the place of q_lat; there is no separate rotary query)
+    st = decode_pointer_status(pool, q, q, block_table, seq_lens, topk_idx, topk, out, lse);
+    if (st != MLA_OK) return st;
+    if ((sink && !aligned(sink, 4)) || (rope_cs && !aligned(rope_cs, 4))) return MLA_ERR_INVALID;
+    DevCtl* ctl = device_ctl();
+    if (!ctl) return MLA_ERR_CUDA;
+    if (!device_supported()) return MLA_ERR_UNSUPPORTED;
+    DecodePlan plan = plan_decode_gather(fmt, B, max_seq_len, topk, num_sms());
+    DecodeArgs a;
+    a.fmt = fmt;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.num_pages = num_pages;
+    a.q_lat = static_cast<const __nv_bfloat16*>(q);
+    a.q_rope = nullptr;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.max_seq_len = max_seq_len;
+    a.topk_idx = topk_idx;
+    a.topk = topk;
+    a.B = B;
+    a.scale = scale;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.workspace = workspace;
+    a.ctl = ctl;
+    a.sink = sink;
+    a.rope_cs = rope_cs;
+    if (plan.workspace > 0 &&
+        (!workspace || workspace_bytes < plan.workspace || !aligned(workspace, 256)))
+        return MLA_ERR_INVALID;
+    return from_cuda(launch_decode_gather(a, plan, stream));
 }
 
 namespace {

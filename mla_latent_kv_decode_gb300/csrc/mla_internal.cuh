@@ -20,6 +20,15 @@ constexpr int kFp8RecordBytes = kDc + 16 + kDr * 2;   // 656
 constexpr int kFp8Group = 128;
 constexpr int kFp8ScaleOff = kDc;            // 4 fp32 scales after the 512 codes
 constexpr int kFp8RopeOff = kDc + 16;        // 64 bf16 rope after the scales
+// Shared K = V entries (512 dims, the last 64 carry RoPE)
+constexpr int kE = 512;
+constexpr int kENope = 448;                  // V4: E4M3 dims, one UE8M0 scale per 64
+constexpr int kV4EntryBytes = 584;
+constexpr int kV4PageBytes = kPage * kV4EntryBytes;          // 37,376: codes, RoPE, scales by field
+constexpr int kV4RopeOff = kPage * kENope;                   // 28,672: RoPE [64][128 B]
+constexpr int kV4ScaleOff = kPage * (kENope + 128);          // 36,864: scale bytes [64][8]
+constexpr int kV41EntryBytes = 288;          // V4.1: 256 B of E2M1 pairs, 32 E4M3 scales
+constexpr int kV41ScaleOff = 256;
 
 // Per-device control block living in device global memory (one per device; its address is
 // taken with cudaGetSymbolAddress and passed to every kernel).
@@ -46,6 +55,8 @@ cudaError_t launch_cache_append(int fmt, uint8_t* pool, int64_t num_pages,
                                 const __nv_bfloat16* c_kv, const __nv_bfloat16* k_rope,
                                 const int32_t* slot, int64_t T, DevCtl* ctl, cudaStream_t st);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t st);
+cudaError_t launch_shared_append(int fmt, uint8_t* pool, int64_t num_pages, const __nv_bfloat16* entry,
+                                 const int32_t* slot, int64_t T, DevCtl* ctl, cudaStream_t st);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int S, int B, int H,
                            __nv_bfloat16* out, float* lse, cudaStream_t st);
 
@@ -90,6 +101,8 @@ struct DecodeArgs {
     float* lse;
     void* workspace;       // caller scratch of at least plan.workspace bytes
     DevCtl* ctl;
+    const float* sink = nullptr;      // shared K = V entries: per-head sink z' [128] (or null)
+    const float* rope_cs = nullptr;   // shared K = V entries: [B][64] cos, sin of the query angles (or null)
 };
 
 // Tensor-core paths: bf16 dense pages (decode_tc.cu), FP8 records and top-k lists (decode_gather.cu).
@@ -98,6 +111,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStrea
 
 DecodePlan plan_decode_gather(int fmt, int B, int max_seq_len, int topk, int sms);
 cudaError_t launch_decode_gather(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+cudaError_t launch_decode_shared(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);   // decode_shared.cu
 
 // bf16 dense pages: TMA-fed tensor-core kernel; FP8 records or a top-k list: the tensor-core
 // kernel that gathers and converts rows itself.

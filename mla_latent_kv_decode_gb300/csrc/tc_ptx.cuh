@@ -198,6 +198,18 @@ __device__ __forceinline__ void bulk_wait0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 8-byte asynchronous copy global -> shared (both addresses 8-byte aligned).
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Prefetch a 3D tile into L2.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+
 // Prefetch a 2D tile into L2 (no shared memory written, nothing to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

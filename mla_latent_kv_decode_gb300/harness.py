@@ -197,3 +197,108 @@ class ProjInputs:
         if hasattr(self, "w_hat_t"):
             return 2 * self.B * self.H * synth.D_C * self.D
         return 2 * self.B * self.H * mla.D_V * (synth.D_C + self.D)
+
+
+class SharedDeviceWorkload:
+    """The device tensors of a shared K = V workload (synth.SharedWorkload): pool replicas filled
+    through shared_kv_append, queries, sinks, RoPE cos/sin, tables; the entries each step appends
+    (the newest of every request)."""
+
+    def __init__(self, w: synth.SharedWorkload, device="cuda", replicas: int = 1, gen: str = "auto",
+                 appended: int = 1):
+        import torch
+        self.torch = torch
+        self.w = w
+        self.device = torch.device(device)
+        self.replicas = replicas
+        self.pool_bytes = w.num_pages * synth.PAGE * mla.record_bytes(w.fmt)
+        self.pools = [torch.zeros(self.pool_bytes, dtype=torch.uint8, device=self.device) for _ in range(replicas)]
+        self.q = bf16_tensor(torch, w.queries(), self.device)
+        sk = w.sink()
+        cs = w.rope_cs()
+        self.sink = None if sk is None else torch.from_numpy(sk).to(self.device)
+        self.rope_cs = None if cs is None else torch.from_numpy(cs).to(self.device)
+        self.block_table = _t(torch, w.block_table, self.device, torch.int32)
+        self.seq_lens = _t(torch, w.seq_lens, self.device, torch.int32)
+        self.topk_idx = None if w.topk_idx is None else _t(torch, w.topk_idx, self.device, torch.int32)
+        total = int(w.seq_lens.astype(np.int64).sum()) * synth.E_DIM
+        self.gen = gen if gen != "auto" else ("host" if total <= HOST_GEN_LIMIT else "device")
+        self.appended = appended
+        self._fill()
+        cs_, ss = [], []
+        for b in range(w.B):
+            n = int(w.seq_lens[b])
+            t0 = max(0, n - appended)
+            if t0 < n:
+                cs_.append(self.entries(b, t0, n))
+                ss.append(_t(torch, w.slots(b, t0, n), self.device, torch.int32))
+        self.new_e = torch.cat(cs_).contiguous() if cs_ else None
+        self.new_slot = torch.cat(ss).contiguous() if ss else None
+
+    def entries(self, b: int, t0: int, t1: int):
+        torch = self.torch
+        if self.gen == "host":
+            return bf16_tensor(torch, synth.shared_entries(self.w.seed, b, t0, t1), self.device)
+        n = t1 - t0
+        e = torch.empty((n, synth.E_DIM), dtype=torch.bfloat16, device=self.device)
+        synth.gpu_normal_bf16(e.data_ptr(), n, self.w.seed, synth.STREAM_KV, (b * synth.KV_ROW_STRIDE + t0) * synth.E_DIM,
+                              synth.E_DIM, synth.E_DIM, torch.cuda.current_stream().cuda_stream)
+        return e
+
+    def _fill(self):
+        w = self.w
+        chunk = 1 << 16
+        for b in range(w.B):
+            n = int(w.seq_lens[b]) - self.appended
+            for t0 in range(0, max(n, 0), chunk):
+                t1 = min(n, t0 + chunk)
+                e = self.entries(b, t0, t1)
+                sl = _t(self.torch, w.slots(b, t0, t1), self.device, self.torch.int32)
+                for pool in self.pools:
+                    mla.shared_kv_append(w.fmt, pool, w.num_pages, e, sl)
+        rc = mla.check_status()
+        if rc != 0:
+            raise mla.MlaError(rc, "entry fill")
+
+    def append(self, replica: int = 0, stream=None):
+        if self.new_slot is not None:
+            mla.shared_kv_append(self.w.fmt, self.pools[replica], self.w.num_pages, self.new_e, self.new_slot,
+                                 stream=stream)
+
+    def alloc_outputs(self):
+        torch = self.torch
+        w = self.w
+        self.out = torch.empty((w.B, w.H, synth.E_DIM), dtype=torch.bfloat16, device=self.device)
+        self.lse = torch.empty((w.B, w.H), dtype=torch.float32, device=self.device)
+        need = mla.decode_workspace_bytes(w.fmt, w.B, w.max_seq_len, 0 if w.topk_idx is None else w.topk_idx.shape[1])
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        return self.out, self.lse
+
+    def decode(self, replica: int = 0, stream=None):
+        w = self.w
+        if not hasattr(self, "out"):
+            self.alloc_outputs()
+        return mla.shared_kv_decode(w.fmt, self.pools[replica], w.num_pages, self.q, self.block_table,
+                                    self.seq_lens, w.max_seq_len, w.scale, sink=self.sink, rope_cs=self.rope_cs,
+                                    topk_idx=self.topk_idx, out=self.out, lse=self.lse, workspace=self.workspace,
+                                    stream=stream)
+
+    def step(self, replica: int = 0, stream=None):
+        self.append(replica, stream)
+        return self.decode(replica, stream)
+
+    def kv_bytes(self) -> int:
+        return int(self.w.attended() * mla.record_bytes(self.w.fmt))
+
+    def algorithmic_bytes(self) -> int:
+        """Attended entries, q, out, lse, sinks, cos/sin, tables."""
+        w = self.w
+        b = self.kv_bytes() + w.B * w.H * (synth.E_DIM * 2 * 2 + 4) + w.H * 4 + w.B * 64 * 4
+        b += w.B * 4 + w.block_table.size * 4
+        if w.topk_idx is not None:
+            b += w.topk_idx.size * 4
+        return int(b)
+
+    def flops(self) -> int:
+        """2 * H * (512 + 512) per attended entry (scores + weighted sum)."""
+        return int(2 * self.w.H * 2 * synth.E_DIM * self.w.attended())

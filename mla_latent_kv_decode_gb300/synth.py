@@ -54,6 +54,8 @@ STREAM_IDX_W = 9          # DSA indexer head weights
 STREAM_U = 10             # value projection: decode outputs U
 STREAM_WUV = 11           # value projection: W^UV
 STREAM_WO = 12            # value projection: W^O (or the merged weight)
+STREAM_SINK = 13          # shared K = V decode: per-head sinks
+STREAM_ANGLE = 14         # shared K = V decode: the query positions' RoPE angles
 
 D_C = 512
 D_R = 64
@@ -359,3 +361,105 @@ def gpu_normal_bf16(dst_ptr: int, rows: int, seed: int, stream: int, first_index
                                        ctypes.c_void_p(cuda_stream))
     if rc != 0:
         raise RuntimeError(f"synth_normal_bf16 failed with CUDA error {rc}")
+
+
+# ----------------------------------------------------------------------------------------------
+# Shared K = V entries (V4 / V4.1 formats): 512-dim entries, queries, sinks, RoPE angles
+# ----------------------------------------------------------------------------------------------
+E_DIM = 512
+
+
+def shared_entries(seed: int, b: int, t0: int, t1: int) -> np.ndarray:
+    """Entries of request b, positions t0..t1-1: bf16 bits [n, 512] (unit normal)."""
+    n = t1 - t0
+    return normal_bf16(seed, STREAM_KV, (b * KV_ROW_STRIDE + t0) * E_DIM, n * E_DIM).reshape(n, E_DIM)
+
+
+def shared_queries(seed: int, B: int, H: int = H_DEFAULT) -> np.ndarray:
+    """Queries bf16 bits [B, H, 512]."""
+    return normal_bf16(seed, STREAM_Q, 0, B * H * E_DIM).reshape(B, H, E_DIM)
+
+
+def sinks(seed: int, H: int = H_DEFAULT) -> np.ndarray:
+    """Per-head sink values z' (fp32 [H], unit normal)."""
+    return normal_f32(seed, STREAM_SINK, 0, H)
+
+
+def rope_cos_sin(seed: int, B: int) -> np.ndarray:
+    """Per request the cos and sin of 32 angles drawn uniformly in [0, 2 pi): fp32 [B, 64] (cos
+    first).  The decode only rotates by the angles it is given, so uniform angles exercise it as
+    well as any position's."""
+    w = u64(seed, STREAM_ANGLE, 0, B * 32).reshape(B, 32)
+    ang = (w >> np.uint64(11)).astype(np.float64) * (2.0 * math.pi / float(1 << 53))
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+@dataclass
+class SharedWorkload:
+    """B requests over a pool of shared K = V entries (format V4 = 2 or V4.1 = 3)."""
+    name: str
+    fmt: int
+    B: int
+    H: int
+    seed: int
+    seq_lens: np.ndarray
+    block_table: np.ndarray
+    num_pages: int
+    scale: float = float(np.float32(1.0 / math.sqrt(512.0)))
+    topk_idx: np.ndarray | None = None
+    use_sink: bool = True
+    use_rope: bool = True
+    description: str = ""
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.B else 0
+
+    def slots(self, b: int, t0: int, t1: int) -> np.ndarray:
+        t = np.arange(t0, t1, dtype=np.int64)
+        return (self.block_table[b, t // PAGE].astype(np.int64) * PAGE + t % PAGE).astype(np.int32)
+
+    def attended(self) -> int:
+        if self.topk_idx is None:
+            return int(self.seq_lens.astype(np.int64).sum())
+        n = 0
+        for b in range(self.B):
+            idx = self.topk_idx[b]
+            n += int(((idx >= 0) & (idx < self.seq_lens[b])).sum())
+        return n
+
+    def queries(self):
+        return shared_queries(self.seed, self.B, self.H)
+
+    def sink(self):
+        return sinks(self.seed, self.H) if self.use_sink else None
+
+    def rope_cs(self):
+        return rope_cos_sin(self.seed, self.B) if self.use_rope else None
+
+
+def make_shared_workload(name: str, fmt: int | None = None, seq_lens=None, seed: int | None = None,
+                         topk_idx=None, shuffle: bool = True, use_sink: bool = True,
+                         use_rope: bool = True) -> SharedWorkload:
+    """v4_batch / v41_batch: B=64 requests of 32,768 entries each (V4 584-B or V4.1 288-B entries),
+    shuffled pages, per-head sinks, RoPE rotated back; or a custom batch (seq_lens, top-k lists)."""
+    if fmt is None:
+        fmt = {"v4_batch": 2, "v41_batch": 3}[name]
+    if seed is None:
+        seed = 0x4D4C41 + 10 + fmt
+    if seq_lens is None:
+        seq_lens = np.full(64, 32768, dtype=np.int32)
+    seq = np.asarray(seq_lens, dtype=np.int32)
+    pages = int(((seq.astype(np.int64) + PAGE - 1) // PAGE).sum())
+    perm = permutation(seed, STREAM_PERM, pages) if shuffle else None
+    bt, total = _block_table(seq, perm)
+    label = "V4 584-B" if fmt == 2 else "V4.1 288-B"
+    return SharedWorkload(name, fmt, len(seq), H_DEFAULT, seed, seq, bt, total,
+                          topk_idx=None if topk_idx is None else np.asarray(topk_idx, np.int32),
+                          use_sink=use_sink, use_rope=use_rope,
+                          description=f"B={len(seq)}, {int(seq.max()) if len(seq) else 0} entries max, {label} "
+                                      f"shared K = V entries, shuffled pages")

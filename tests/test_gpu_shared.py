@@ -1,0 +1,125 @@
+"""Parity of the shared K = V path ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token", section
+"HCA: 128 tokens into one", Fig. 15; entry formats of "Calculating V4-Flash's KV cache" and
+"Calculating V4.1-Flash's KV cache") with the fp64 oracle, through the C ABI.
+
+Bit-exact: the pool bytes written by mla_shared_kv_append (both formats).  Tolerance: the decode
+bar of tests/parity_util.py (outputs 1e-2 absolute and 1e-2 normwise per (request, head), lse
+1e-3).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import mla_latent_kv_decode_gb300 as mla
+from mla_latent_kv_decode_gb300 import harness, synth
+from parity_util import assert_decode_close
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [(2, "v4"), (3, "v41")]
+
+
+def _oracle_pool(w, upto=None):
+    pool = oracle.new_shared_pool(w.fmt, w.num_pages)
+    for b in range(w.B):
+        n = int(w.seq_lens[b] if upto is None else upto[b])
+        if n > 0:
+            assert oracle.shared_append(w.fmt, pool, synth.shared_entries(w.seed, b, 0, n), w.slots(b, 0, n)) == 0
+    return pool
+
+
+def _run(w, what):
+    dw = harness.SharedDeviceWorkload(w, gen="host")
+    dw.append()
+    out, lse = dw.decode()
+    assert mla.check_status() == 0
+    pool = _oracle_pool(w)
+    assert np.array_equal(dw.pools[0].cpu().numpy(), pool), f"{what}: pool bytes differ"
+    ro, rl = oracle.shared_kv_decode(w.fmt, pool, w.queries(), w.block_table, w.seq_lens, w.scale,
+                                     sink=w.sink(), rope_cs=w.rope_cs(), topk_idx=w.topk_idx)
+    go = out.float().cpu().numpy().reshape(-1, 512)
+    gl = lse.cpu().numpy().reshape(-1)
+    if w.use_sink:
+        # a request with nothing visible: zeros and lse = z'
+        sk = np.tile(w.sink(), w.B)
+        empty = np.isclose(rl, sk) & np.all(ro == 0, axis=1)
+        assert np.all(go[empty] == 0) and np.allclose(gl[empty], sk[empty])
+        keep = ~empty
+        assert_decode_close(go[keep], gl[keep], ro[keep], rl[keep], what)
+    else:
+        assert_decode_close(go, gl, ro, rl, what)
+    return dw
+
+
+@pytest.mark.parametrize("fmt,tag", FORMATS)
+def test_shared_ragged_batch(fmt, tag):
+    """Ragged lengths around page edges, an empty request, shuffled pages; sinks and rotation."""
+    w = synth.make_shared_workload(f"ragged_{tag}", fmt=fmt, seq_lens=[1, 63, 64, 65, 0, 700, 3000], seed=41 + fmt)
+    _run(w, f"ragged {tag}")
+
+
+@pytest.mark.parametrize("fmt,tag", FORMATS)
+def test_shared_without_sink_or_rotation(fmt, tag):
+    w = synth.make_shared_workload(f"plain_{tag}", fmt=fmt, seq_lens=[500, 129, 2000], seed=43 + fmt,
+                                   use_sink=False, use_rope=False)
+    _run(w, f"plain {tag}")
+
+
+@pytest.mark.parametrize("fmt,tag", FORMATS)
+def test_shared_long_requests_split_and_merged(fmt, tag):
+    """Requests long enough to be cut across many clusters: partials are rotated back in place
+    and the merge adds the sink once."""
+    w = synth.make_shared_workload(f"long_{tag}", fmt=fmt, seq_lens=[20000, 9000, 0, 33], seed=45 + fmt)
+    _run(w, f"long {tag}")
+
+
+@pytest.mark.parametrize("fmt,tag", FORMATS)
+def test_shared_topk_rows(fmt, tag):
+    """Top-k lists (the entries a CSA layer's indexer picks): padding, entries past the length,
+    a list of every position equal to the dense result."""
+    seed = 47 + fmt
+    seq = [5000, 700, 4097, 90]
+    K = 300
+    idx = np.stack([synth.sorted_distinct_sample(seed, synth.STREAM_TOPK, b, n, K) for b, n in enumerate(seq)])
+    idx[1, -20:] = -1
+    idx[2, -5:] = 4097 + np.arange(5)
+    w = synth.make_shared_workload(f"topk_{tag}", fmt=fmt, seq_lens=seq, seed=seed, topk_idx=idx)
+    _run(w, f"topk {tag}")
+    seq = [130, 64]
+    full = np.full((2, 192), -1, np.int32)
+    for b, n in enumerate(seq):
+        full[b, :n] = np.arange(n)
+    wd = synth.make_shared_workload(f"dense_{tag}", fmt=fmt, seq_lens=seq, seed=seed + 1)
+    wk = synth.make_shared_workload(f"all_{tag}", fmt=fmt, seq_lens=seq, seed=seed + 1, topk_idx=full)
+    od, ld = _run(wd, f"dense {tag}").decode()
+    ok, lk = _run(wk, f"all {tag}").decode()
+    assert np.abs(od.float().cpu().numpy() - ok.float().cpu().numpy()).max() <= 1e-2
+    assert np.abs(ld.cpu().numpy() - lk.cpu().numpy()).max() <= 1e-3
+
+
+def test_shared_append_codec_edges():
+    """Groups at the edges of both codecs, bit-exact against the oracle's encoders: zero groups, a
+    group whose amax is exactly 448 * 2^e, huge and tiny magnitudes, values on E2M1 midpoints."""
+    import torch
+    rng = np.random.default_rng(49)
+    T = 4096
+    x = rng.normal(size=(T, 512)).astype(np.float32)
+    x[0] = 0.0
+    x[1, :64] = 448.0
+    x[2] *= 1e30
+    x[3] *= 1e-30
+    x[4, :16] = np.array([6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25, -6, -5, -3.5, -2.5, -1.75, -1.25, -0.75, -0.25])
+    x[5:] *= np.exp2(rng.integers(-20, 20, size=(T - 5, 1))).astype(np.float32)
+    bits = synth._bf16_rne(x)
+    e = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    slot = rng.permutation(T).astype(np.int32)
+    for fmt in (2, 3):
+        pages = T // 64
+        pool = torch.zeros(pages * 64 * mla.record_bytes(fmt), dtype=torch.uint8, device="cuda")
+        mla.shared_kv_append(fmt, pool, pages, e, torch.from_numpy(slot).cuda())
+        assert mla.check_status() == 0
+        ref = oracle.new_shared_pool(fmt, pages)
+        assert oracle.shared_append(fmt, ref, bits, slot) == 0
+        got = pool.cpu().numpy()
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, f"fmt {fmt}: first differing byte {bad[:4]} gpu {got[bad[:4]]} oracle {ref[bad[:4]]}"
