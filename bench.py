@@ -293,14 +293,16 @@ def run_indexer_reference(args):
 # ----------------------------------------------------------------------------------------------
 
 HEADLINE = "fp8_batch"
-CONFIG_ORDER = ["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse"]
+CONFIG_ORDER = ["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse", "v4_batch", "v41_batch"]
+SHARED_WORKLOADS = ("v4_batch", "v41_batch")
+KV_FORMAT_NAMES = {0: "bf16", 1: "fp8_mixed", 2: "v4_fp8_584B", 3: "v41_fp4_288B"}
 POOL_BUDGET = 48 << 30        # device bytes the pool replicas of one workload may take
 
 
 def workload_config(w, replicas: int, one_pool: int, world: int = 1) -> dict:
     """The config object of a workload's line (the same for both arms)."""
     topk = 0 if w.topk_idx is None else int(w.topk_idx.shape[1])
-    return {"workload": w.name, "B": w.B, "H": w.H, "kv_format": "bf16" if w.fmt == 0 else "fp8_mixed",
+    return {"workload": w.name, "B": w.B, "H": w.H, "kv_format": KV_FORMAT_NAMES[w.fmt],
             "description": w.description, "topk": topk, "page_tokens": 64, "scale": w.scale,
             "step": "cache_append of the tokens each request adds + mla_decode of the batch",
             "l2": f"inputs larger than L2: {replicas} rotating pool replicas of {one_pool / 2**20:.0f} MiB"
@@ -346,14 +348,18 @@ class _Bench:
 
     def __init__(self, name, args, torch, mla, harness, synth, stream, barrier, dist, replicas=None):
         self.torch, self.mla, self.stream, self.barrier, self.dist = torch, mla, stream, barrier, dist
-        w = synth.make_workload(name)
+        shared = name in SHARED_WORKLOADS
+        w = synth.make_shared_workload(name) if shared else synth.make_workload(name)
         self.w = w
         kv = int(w.attended() * mla.record_bytes(w.fmt))
         self.replicas = replicas if replicas is not None else (
             _replicas(w, mla, kv) if args.replicas == 0 else args.replicas)
         self.one_pool = mla.pool_bytes(w.fmt, w.num_pages)
-        skip = 1 if w.appended == 0 else w.appended
-        self.dw = dw = harness.DeviceWorkload(w, replicas=self.replicas, prefill_skip_last=skip)
+        if shared:
+            self.dw = dw = harness.SharedDeviceWorkload(w, replicas=self.replicas, appended=1)
+        else:
+            skip = 1 if w.appended == 0 else w.appended
+            self.dw = dw = harness.DeviceWorkload(w, replicas=self.replicas, prefill_skip_last=skip)
         dw.alloc_outputs()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):      # eager warm-up (also sets kernel attributes)
@@ -839,8 +845,8 @@ def run_e2e(args, dw, torch, mla, stream, barrier, dist):
     copy, on a copy stream, while the compute stream runs append + decode of the step before
     (two input and two output buffers; events keep each buffer's writer after its last reader).
     Every copy of every step is inside the timed region."""
-    names = [k for k in ("q_lat", "q_rope", "block_table", "seq_lens", "new_c", "new_r", "new_slot")
-             if getattr(dw, k) is not None]
+    names = [k for k in ("q_lat", "q_rope", "q", "sink", "rope_cs", "block_table", "seq_lens", "new_c", "new_r",
+                         "new_e", "new_slot") if getattr(dw, k, None) is not None]
     saved = {k: getattr(dw, k) for k in names + ["out", "lse"]}
     ins = [_pack(torch, [saved[k] for k in names], dw.device) for _ in range(2)]
     outs = [_pack(torch, [saved["out"], saved["lse"]], dw.device) for _ in range(2)]
@@ -916,7 +922,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
                     choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse",
-                             "indexer_topk"])
+                             "indexer_topk", "v4_batch", "v41_batch"])
     ap.add_argument("--index-batch", type=int, default=64,
                     help="indexer_topk: queries per step (64 is the workload; smaller for profiling)")
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0 = enough to exceed L2 3x)")
@@ -929,6 +935,8 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
+        if args.workload in SHARED_WORKLOADS:
+            ap.error("the reference arm times the MLA workloads and the indexer")
         if args.workload == "indexer_topk":
             return run_indexer_reference(args)
         return run_reference(args)

@@ -78,7 +78,7 @@ def test_shared_topk_rows(fmt, tag):
     """Top-k lists (the entries a CSA layer's indexer picks): padding, entries past the length,
     a list of every position equal to the dense result."""
     seed = 47 + fmt
-    seq = [5000, 700, 4097, 90]
+    seq = [5000, 700, 4097, 310]
     K = 300
     idx = np.stack([synth.sorted_distinct_sample(seed, synth.STREAM_TOPK, b, n, K) for b, n in enumerate(seq)])
     idx[1, -20:] = -1
