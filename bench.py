@@ -54,10 +54,12 @@ KERNEL_SOURCES = {
     "decode_gather": ["mla_latent_kv_decode_gb300/csrc/decode_gather.cu",
                       "mla_latent_kv_decode_gb300/csrc/decode_gather.cuh"] + _HEADERS,
     "indexer_score": ["mla_latent_kv_decode_gb300/csrc/indexer.cu"] + _HEADERS,
+    "proj": ["mla_latent_kv_decode_gb300/csrc/proj.cu"] + _HEADERS,
 }
 WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_context": "decode_tc",
                    "fp8_batch": "decode_gather", "topk_sparse": "decode_gather",
-                   "indexer_topk": "indexer_score"}
+                   "v4_batch": "decode_gather", "v41_batch": "decode_gather",
+                   "indexer_topk": "indexer_score", "value_project": "proj", "value_project_merged": "proj"}
 NCU_TRAFFIC = {
     ("c9436f9a11212c15", "paged_batch"): 178_121_984,
     ("c9436f9a11212c15", "long_context"): 155_761_152,
@@ -506,7 +508,8 @@ def measure_value_project(args, torch, mla, harness, stream, barrier, peaks, mer
     entry = {"ms_per_call": round(ms, 6), "B": B, "H": H, "d_v": mla.D_V, "D": D,
              "form": "merged weight (Fig. 6 (3))" if merged else "two products (Fig. 6 (2))",
              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                          "frac": round(gbs / peaks["hbm_gbs"], 4),
+                          "traffic": _traffic("value_project_merged" if merged else "value_project"),
                           "peak_source": peaks["source"], "bytes_per_launch": alg, "flops_per_launch": flops,
                           "tensor_frac": round(flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)},
              "e2e": {"value": round(alg / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
@@ -517,6 +520,24 @@ def measure_value_project(args, torch, mla, harness, stream, barrier, peaks, mer
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return entry
+
+
+def run_value_project(args):
+    """The value up-projection and output projection alone (one line, for profiling it): the
+    measurement of measure_value_project, with the clocks of its run."""
+    import torch
+    import mla_latent_kv_decode_gb300 as mla
+    from mla_latent_kv_decode_gb300 import harness
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    mla.load()
+    stream = torch.cuda.Stream()
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    sampler.start()
+    entry = measure_value_project(args, torch, mla, harness, stream, torch.cuda.synchronize, _peaks(),
+                                  merged=args.workload == "value_project_merged")
+    entry["clocks"] = sampler.stop()
+    print(json.dumps({"metric": METRIC, "workload": args.workload, **entry}), flush=True)
+    return 0
 
 
 def run_ours(args):
@@ -922,7 +943,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
                     choices=["tiny_dense", "paged_batch", "long_context", "fp8_batch", "topk_sparse",
-                             "indexer_topk", "v4_batch", "v41_batch"])
+                             "indexer_topk", "v4_batch", "v41_batch", "value_project", "value_project_merged"])
     ap.add_argument("--index-batch", type=int, default=64,
                     help="indexer_topk: queries per step (64 is the workload; smaller for profiling)")
     ap.add_argument("--replicas", type=int, default=0, help="pool replicas (0 = enough to exceed L2 3x)")
@@ -935,13 +956,15 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
-        if args.workload in SHARED_WORKLOADS:
+        if args.workload in SHARED_WORKLOADS or args.workload.startswith("value_project"):
             ap.error("the reference arm times the MLA workloads and the indexer")
         if args.workload == "indexer_topk":
             return run_indexer_reference(args)
         return run_reference(args)
     if args.workload == "indexer_topk":
         return run_indexer(args)
+    if args.workload in ("value_project", "value_project_merged"):
+        return run_value_project(args)
     return run_ours(args)
 
 
