@@ -61,11 +61,16 @@ WORKLOAD_KERNEL = {"tiny_dense": "decode_tc", "paged_batch": "decode_tc", "long_
                    "v4_batch": "decode_gather", "v41_batch": "decode_gather",
                    "indexer_topk": "indexer_score", "value_project": "proj", "value_project_merged": "proj"}
 NCU_TRAFFIC = {
-    ("c9436f9a11212c15", "paged_batch"): 178_121_984,
-    ("c9436f9a11212c15", "long_context"): 155_761_152,
-    ("317d8c4c452e69fa", "fp8_batch"): 1_414_574_592,
-    ("317d8c4c452e69fa", "topk_sparse"): 122_382_592,
-    ("a650593e7d15f670", "indexer_topk"): 1_144_615_680,
+    ("a6a81cb6175a2d16", "tiny_dense"): 4_939_008,
+    ("a6a81cb6175a2d16", "paged_batch"): 176_497_152,
+    ("a6a81cb6175a2d16", "long_context"): 154_273_024,
+    ("7ec042eae824bb42", "fp8_batch"): 1_412_751_232,
+    ("7ec042eae824bb42", "topk_sparse"): 120_461_056,
+    ("7ec042eae824bb42", "v4_batch"): 1_259_511_552,
+    ("7ec042eae824bb42", "v41_batch"): 636_540_672,
+    ("1a7398fbc27d89ce", "indexer_topk"): 1_142_927_360,
+    ("4257ceba335e021a", "value_project"): 197_980_416,
+    ("4257ceba335e021a", "value_project_merged"): 681_876_352,
 }
 
 
