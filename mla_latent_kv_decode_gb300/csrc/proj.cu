@@ -41,12 +41,11 @@ constexpr int kBK = 64;               // K per stage: one 128-byte swizzle row o
 constexpr int kMaxNB = 128;           // requests per tile
 constexpr int kPThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kMaxStages = 8;
-constexpr int kSlotStride = 20;       // floats per row of a reduction slot (16 + 4: no bank conflicts)
-constexpr int kSlotBytes = kBM * kSlotStride * 4;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kDrainLimit = 1u << 20;
 constexpr int kRingBudget = 200 * 1024;
+constexpr int kPrefetchChunks = 24;   // stage-2 weight chunks (16 KB each) per CTA prefetched by stage 1
 
 enum Epi : int { kEpiZ = 0, kEpiYPair = 1, kEpiY = 2 };
 
@@ -64,6 +63,14 @@ struct ProjParams {
     int64_t out_plane;   // kEpiZ: elements from the hi plane to the lo plane
     __nv_bfloat16* out;
     DevCtl* ctl;
+    // kEpiZ: the next product's weight boxes to prefetch into L2 while this one runs (one CTA per
+    // CTA of the next launch: its output tile and the first chunks of its K share)
+    int pf_tiles;        // output tiles of the next product (0: no prefetch)
+    int pf_split;        // its cluster size
+    int pf_k_chunks;     // its K / 64
+    int pf_chunks;       // chunks to prefetch per CTA
+    bool wait_prior;     // this launch depends on the previous one (programmatic): wait before
+                         // reading the activations
 };
 
 __device__ __forceinline__ uint32_t cluster_size() {
@@ -78,10 +85,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int kEpi>
 __global__ void __launch_bounds__(kPThreads, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                     ProjParams p) {
+                     const __grid_constant__ CUtensorMap tm_next, ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -135,16 +149,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
             tma_prefetch_desc(&tm_b);
+            // the weights of the first ring's worth of chunks go out at once; when this launch
+            // depends on the one before (its activations are that launch's output), the
+            // activations wait for it, the weights do not
+            const int first = nck < p.stages ? nck : p.stages;
+            for (int i = 0; i < first; ++i) {
+                mbar_arrive_expect_tx(full(i), p.stage_bytes);
+                tma_load_2d(a_dst(i), &tm_a, full(i), (c0 + i) * kBK, a_row);
+            }
+            if (p.wait_prior) grid_dependency_wait();
             for (int i = 0; i < nck; ++i) {
                 const int s = i % p.stages;
                 if (i >= p.stages && !mbar_wait(empty(s), ((i / p.stages) - 1) & 1, wait_limit)) {
                     s_abort = 1;
                     record_error(p.ctl, MLA_ERR_TIMEOUT, 60);
                 }
-                if (s_abort) break;
+                if (s_abort) {
+                    // the weight boxes already issued still land on their barriers: count them in
+                    issued = i > first ? i : first;
+                    break;
+                }
                 const int kx = (c0 + i) * kBK;
-                mbar_arrive_expect_tx(full(s), p.stage_bytes);
-                tma_load_2d(a_dst(s), &tm_a, full(s), kx, a_row);
+                if (i >= first) {
+                    mbar_arrive_expect_tx(full(s), p.stage_bytes);
+                    tma_load_2d(a_dst(s), &tm_a, full(s), kx, a_row);
+                }
                 if (kEpi == kEpiYPair) {
                     tma_load_3d(b_dst(s), &tm_b, full(s), b_col0 + kx, b0, 0);
                     tma_load_3d(b_dst(s) + (uint32_t)p.nb * 128u, &tm_b, full(s), b_col0 + kx, b0, 1);
@@ -153,6 +182,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 ++issued;
             }
+            // the next product's first weight chunks into L2 (its launch waits for this one)
+            if (kEpi == kEpiZ && p.pf_tiles > 0) {
+                const int cta = (int)(blockIdx.z * gridDim.y + blockIdx.y) * (int)gridDim.x + (int)blockIdx.x;
+                const int n_next = p.pf_tiles * p.pf_split;
+                const int per_cta_z = (n_next + (int)(gridDim.x * gridDim.y * gridDim.z) - 1) /
+                                      (int)(gridDim.x * gridDim.y * gridDim.z);
+                for (int q = cta * per_cta_z; q < (cta + 1) * per_cta_z && q < n_next; ++q) {
+                    const int tile = q / p.pf_split, rr = q % p.pf_split;
+                    const int per2 = p.pf_k_chunks / p.pf_split, ex2 = p.pf_k_chunks % p.pf_split;
+                    const int k0 = rr * per2 + (rr < ex2 ? rr : ex2);
+                    for (int c = 0; c < p.pf_chunks && c < per2; ++c)
+                        tma_prefetch_l2_2d(&tm_next, (k0 + c) * kBK, tile * kBM);
+                }
+            }
+            grid_launch_dependents();
             // drain: every issued copy lands before the ring is reused or the CTA exits
             for (int i = issued - 1; i >= 0 && i >= issued - p.stages; --i)
                 mbar_wait(full(i % p.stages), (i / p.stages) & 1, kDrainLimit);
@@ -216,92 +260,87 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tc_fence_after();
     }
 
-    // Partial sums of the cluster into rank 0, 16 columns a round through two slot buffers:
-    // ranks 1 .. S-1 write their columns into their own slot of rank 0's buffer (j & 1), then
-    // every thread of the cluster meets; rank 0 adds the slots, in rank order, to its own
-    // columns in tensor memory.  The barrier of round j + 1 follows rank 0's reads of round j,
-    // so round j + 2 may overwrite that buffer.  The first barrier: every CTA's main loop is
-    // over (rank 0's ring is no longer written by TMA).
+    // The cluster's partial sums, in one exchange: the accumulator's columns are cut into units of
+    // 16 requests (for kEpiYPair a unit is its hi column block and its lo column block), CTA q of
+    // the cluster owns units [u_of(q), u_of(q + 1)); every CTA writes its partials of the other
+    // CTAs' units into their slot buffers through distributed shared memory (slot: the sender's
+    // rank among the others), all threads of the cluster meet, and each CTA adds, in rank order,
+    // the partials of its own units to its own and writes those outputs.  The first barrier: every
+    // CTA's main loop is over (the ring, where the slots live, is no longer written by TMA).
+    const int units = (kEpi == kEpiYPair ? p.nb : p.n_mma) / 16;
+    auto u_of = [&](int q) { return q * units / (int)S; };
+    const int blocks = kEpi == kEpiYPair ? 2 : 1;                  // column blocks per unit
+    const int max_units = (units + (int)S - 1) / (int)S;
+    const int slot_stride = blocks * 16 * max_units + 4;          // floats per slot row (+4: banks)
+    const int slot_floats = kBM * slot_stride;
+    auto col_of = [&](int u, int blk) { return blk == 0 ? 16 * u : p.nb + 16 * u; };
     if (S > 1) {
-        const int rounds = (p.n_mma + 15) / 16;
-        const uint32_t slots = sbase;   // the ring, free once the main loop is over
-        const uint32_t slots_remote = mapa(slots, 0);
         tc_fence_before();
         __syncthreads();
         cluster_sync();
-        for (int j = 0; j <= rounds; ++j) {
-            if (epi && have_acc && j < rounds && r != 0) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_off + 16 * j, v);
-                tmem_wait_ld();
-                const uint32_t dst = slots_remote + (uint32_t)(((j & 1) * (int)(S - 1) + (int)r - 1) * kSlotBytes) +
-                                     (uint32_t)(m * kSlotStride * 4);
+        if (epi && have_acc) {
+            for (int q = 0; q < (int)S; ++q) {
+                if (q == (int)r) continue;
+                const int slot = (int)r < q ? (int)r : (int)r - 1;
+                const uint32_t base = mapa(sbase, (uint32_t)q) +
+                                      (uint32_t)((slot * slot_floats + m * slot_stride) * 4);
+                for (int u = u_of(q); u < u_of(q + 1); ++u)
+                    for (int blk = 0; blk < blocks; ++blk) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_off + col_of(u, blk), v);
+                        tmem_wait_ld();
+                        const uint32_t dst = base + (uint32_t)(((blk * max_units + (u - u_of(q))) * 16) * 4);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_cluster_v4(dst + 16 * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                        for (int t = 0; t < 4; ++t)
+                            st_cluster_v4(dst + 16 * t, __uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
+                                          __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]));
+                    }
             }
-            if (epi && have_acc && j >= 1 && r == 0) {
-                const int jj = j - 1;
+        }
+        __syncwarp();
+        cluster_sync();
+    }
+
+    if (epi && have_acc) {
+        const int64_t col = (int64_t)z * p.out_cols_per_z + (int64_t)mt * kBM + m;
+        __nv_bfloat16* out = p.out + (int64_t)b0 * p.out_ld + col;
+        const int nvalid = min(p.nb, p.B - b0);
+        for (int u = u_of((int)r); u < u_of((int)r + 1); ++u) {
+            if (16 * u >= nvalid) break;
+            float acc[2][16];
+            for (int blk = 0; blk < blocks; ++blk) {
                 uint32_t v[16];
-                tmem_ld16(tmem + lane_off + 16 * jj, v);
+                tmem_ld16(tmem + lane_off + col_of(u, blk), v);
                 tmem_wait_ld();
-                float acc[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) acc[t] = __uint_as_float(v[t]);
+                for (int t = 0; t < 16; ++t) acc[blk][t] = __uint_as_float(v[t]);
                 for (int q = 1; q < (int)S; ++q) {
                     const float4* src = reinterpret_cast<const float4*>(
-                        sm + ((jj & 1) * (int)(S - 1) + q - 1) * kSlotBytes + m * kSlotStride * 4);
+                        sm + ((q - 1) * slot_floats + m * slot_stride + (blk * max_units + (u - u_of((int)r))) * 16) * 4);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const float4 x = src[t];
-                        acc[4 * t] += x.x;
-                        acc[4 * t + 1] += x.y;
-                        acc[4 * t + 2] += x.z;
-                        acc[4 * t + 3] += x.w;
+                        acc[blk][4 * t] += x.x;
+                        acc[blk][4 * t + 1] += x.y;
+                        acc[blk][4 * t + 2] += x.z;
+                        acc[blk][4 * t + 3] += x.w;
                     }
                 }
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(acc[t]);
-                tmem_st16(tmem + lane_off + 16 * jj, v);
-                tmem_wait_st();
             }
-            __syncwarp();
-            cluster_sync();
-        }
-    }
-
-    if (epi && have_acc && r == 0) {
-        const int nvalid = min(p.nb, p.B - b0);
-        const int64_t col = (int64_t)z * p.out_cols_per_z + (int64_t)mt * kBM + m;
-        __nv_bfloat16* out = p.out + (int64_t)b0 * p.out_ld + col;
-        for (int c = 0; c < nvalid; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_off + c, v);
-            tmem_wait_ld();
-            if (kEpi == kEpiYPair) {
-                uint32_t w[16];
-                tmem_ld16(tmem + lane_off + p.nb + c, w);
-                tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (c + t < nvalid)
-                        out[(int64_t)(c + t) * p.out_ld] =
-                            __float2bfloat16_rn(__uint_as_float(v[t]) + __uint_as_float(w[t]));
-            } else if (kEpi == kEpiZ) {
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (c + t < nvalid) {
-                        const float x = __uint_as_float(v[t]);
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-                        const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-                        out[(int64_t)(c + t) * p.out_ld] = hi;
-                        out[p.out_plane + (int64_t)(c + t) * p.out_ld] = lo;
-                    }
-            } else {
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (c + t < nvalid) out[(int64_t)(c + t) * p.out_ld] = __float2bfloat16_rn(__uint_as_float(v[t]));
+            for (int t = 0; t < 16; ++t) {
+                const int b = 16 * u + t;
+                if (b >= nvalid) break;
+                __nv_bfloat16* o = out + (int64_t)b * p.out_ld;
+                if (kEpi == kEpiYPair) {
+                    *o = __float2bfloat16_rn(acc[0][t] + acc[1][t]);
+                } else if (kEpi == kEpiZ) {
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(acc[0][t]);
+                    *o = hi;
+                    o[p.out_plane] = __float2bfloat16_rn(acc[0][t] - __bfloat162float(hi));
+                } else {
+                    *o = __float2bfloat16_rn(acc[0][t]);
+                }
             }
         }
     }
@@ -324,21 +363,31 @@ int pick_split(int tiles, int k_chunks, int sms) {
     return s < 1 ? 1 : s;
 }
 
+int split_of(int tiles, int k_chunks) {
+    int sms = num_sms();
+    if (sms <= 0) sms = 152;
+    return pick_split(tiles, k_chunks, sms);
+}
+
 template <int kEpi>
-cudaError_t launch_proj(const CUtensorMap& tm_a, const CUtensorMap& tm_b, ProjParams p, int m_tiles, int n_tiles,
-                        int zdim, cudaStream_t st) {
+cudaError_t launch_proj(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_next, ProjParams p,
+                        int m_tiles, int n_tiles, int zdim, bool programmatic, cudaStream_t st) {
     auto* kernel = proj_gemm_kernel<kEpi>;
     const int b_rows = kEpi == kEpiYPair ? 2 * p.nb : p.n_mma;
     p.stage_bytes = kABytes + (uint32_t)b_rows * 128u;
     p.stages = kRingBudget / (int)p.stage_bytes;
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) return cudaErrorInvalidValue;
-    int sms = num_sms();
-    if (sms <= 0) sms = 152;
-    const int S = pick_split(m_tiles * n_tiles * zdim, p.k_chunks, sms);
+    const int S = split_of(m_tiles * n_tiles * zdim, p.k_chunks);
     size_t smem = (size_t)p.stages * p.stage_bytes + 1024;
-    const size_t slot_need = (size_t)2 * (S - 1) * kSlotBytes + 1024;
+    // the reduction's slots (they reuse the ring once the main loop is over)
+    const int units = (kEpi == kEpiYPair ? p.nb : p.n_mma) / 16;
+    const int max_units = (units + S - 1) / S;
+    const size_t slot_need =
+        (size_t)(S - 1) * kBM * ((kEpi == kEpiYPair ? 2 : 1) * 16 * max_units + 4) * 4 + 1024;
     if (slot_need > smem) smem = slot_need;
+    if (smem > (size_t)kRingBudget + 2048) return cudaErrorInvalidValue;
+    p.wait_prior = programmatic;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -356,14 +405,18 @@ cudaError_t launch_proj(const CUtensorMap& tm_a, const CUtensorMap& tm_b, ProjPa
     cfg.blockDim = dim3(kPThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the launch may begin before the previous one on the stream ends; its producer waits for that
+    // one (griddepcontrol.wait) before it reads the activations the previous launch wrote
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kernel, tm_a, tm_b, p);
+    cfg.numAttrs = programmatic ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tm_a, tm_b, tm_next, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -379,6 +432,9 @@ cudaError_t launch_value_project(const __nv_bfloat16* u, const __nv_bfloat16* w_
     const int nt = (B + kMaxNB - 1) / kMaxNB;
     const int bt = B < kMaxNB ? B : kMaxNB;
     const uint64_t hk = (uint64_t)H * kDv;   // stage 2 K: the heads' outputs side by side
+    CUtensorMap tm_w_o;                       // stage 2's weight: W^O^T [D x H*128]
+    if (!encode_2d(&tm_w_o, w_o_t, hk, (uint64_t)D, hk * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     {
         // stage 1: A = W^UV_h^T rows [h*128, h*128 + 128) of [H*128 x 512]; B = U [B x H*512]
         CUtensorMap tm_a, tm_b;
@@ -399,19 +455,24 @@ cudaError_t launch_value_project(const __nv_bfloat16* u, const __nv_bfloat16* w_
         p.out_plane = (int64_t)B * (int64_t)hk;
         p.out = z;
         p.ctl = ctl;
-        cudaError_t e = launch_proj<kEpiZ>(tm_a, tm_b, p, 1, nt, H, st);
+        // while it runs (it is latency-bound), the stage-2 CTAs' first weight chunks go into L2
+        p.pf_tiles = (D / kBM) * nt;
+        p.pf_split = split_of(p.pf_tiles, (int)(hk / kBK));
+        p.pf_k_chunks = (int)(hk / kBK);
+        p.pf_chunks = kPrefetchChunks;
+        cudaError_t e = launch_proj<kEpiZ>(tm_a, tm_b, tm_w_o, p, 1, nt, H, false, st);
         if (e != cudaSuccess) return e;
     }
     {
         // stage 2: A = W^O^T [D x H*128]; B = the hi and lo planes of Z, [2][B][H*128] (each plane's
-        // box a multiple of 16 rows, so that the lo columns start on a 16-column boundary)
-        CUtensorMap tm_a, tm_b;
+        // box a multiple of 16 rows, so that the lo columns start on a 16-column boundary); launched
+        // so that it may start while stage 1 finishes
+        CUtensorMap tm_b;
         const int nb = round_up(bt, 16);
         const uint64_t dims[3] = {hk, (uint64_t)B, 2};
         const uint64_t strides[2] = {hk * 2, (uint64_t)B * hk * 2};
         const uint32_t box[3] = {(uint32_t)kBK, (uint32_t)nb, 1};
-        if (!encode_2d(&tm_a, w_o_t, hk, (uint64_t)D, hk * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_3d(&tm_b, z, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        if (!encode_3d(&tm_b, z, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
             return cudaErrorInvalidValue;
         ProjParams p = {};
         p.k_chunks = (int)(hk / kBK);
@@ -421,7 +482,7 @@ cudaError_t launch_value_project(const __nv_bfloat16* u, const __nv_bfloat16* w_
         p.out_ld = D;
         p.out = y;
         p.ctl = ctl;
-        return launch_proj<kEpiYPair>(tm_a, tm_b, p, D / kBM, nt, 1, st);
+        return launch_proj<kEpiYPair>(tm_w_o, tm_b, tm_w_o, p, D / kBM, nt, 1, true, st);
     }
 }
 
@@ -444,7 +505,7 @@ cudaError_t launch_value_project_merged(const __nv_bfloat16* u, const __nv_bfloa
     p.out_ld = D;
     p.out = y;
     p.ctl = ctl;
-    return launch_proj<kEpiY>(tm_a, tm_b, p, D / kBM, nt, 1, st);
+    return launch_proj<kEpiY>(tm_a, tm_b, tm_a, p, D / kBM, nt, 1, false, st);
 }
 
 }  // namespace mla
