@@ -44,8 +44,8 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kDrainLimit = 1u << 20;
-constexpr int kRingBudget = 200 * 1024;
-constexpr int kPrefetchChunks = 24;   // stage-2 weight chunks (16 KB each) per CTA prefetched by stage 1
+constexpr int kRingBudget = 104 * 1024;   // two CTAs fit on an SM (tensor memory: 2 x 256 columns)
+constexpr int kPrefetchChunks = 12;   // stage-2 weight chunks (16 KB each) per CTA prefetched by stage 1
 
 enum Epi : int { kEpiZ = 0, kEpiYPair = 1, kEpiY = 2 };
 
@@ -93,7 +93,7 @@ __device__ __forceinline__ void grid_launch_dependents() {
 }
 
 template <int kEpi>
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 2)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_next, ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -353,20 +353,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Cluster size along K: about one CTA per SM for the tiles given, at most 8, at most one share
-// per K chunk.
+// Cluster size along K: about 1.35 CTAs per SM for the tiles given (two fit on an SM, and a sweep
+// of the merged product at 40 tiles ran best with clusters of 5: 5.9 TB/s, against 4.5 TB/s with
+// one CTA per SM and 3.9 TB/s at 7), at most 8, at most one share per K chunk.
 int pick_split(int tiles, int k_chunks, int sms) {
-    int s = tiles > 0 ? sms / tiles : 1;
+    int s = tiles > 0 ? (27 * sms) / (20 * tiles) : 1;
     if (s < 1) s = 1;
     if (s > 8) s = 8;
     if (s > k_chunks) s = k_chunks;
     return s < 1 ? 1 : s;
 }
 
-int split_of(int tiles, int k_chunks) {
+// Shared memory of the reduction's slots for a cluster of S (they reuse the ring).
+size_t slot_bytes(bool pair, int units, int S) {
+    const int max_units = (units + S - 1) / S;
+    return (size_t)(S - 1) * kBM * ((pair ? 2 : 1) * 16 * max_units + 4) * 4 + 1024;
+}
+
+// The cluster size of a launch: pick_split, lowered until the reduction's slots fit.
+int split_of(int tiles, int k_chunks, bool pair, int units) {
     int sms = num_sms();
     if (sms <= 0) sms = 152;
-    return pick_split(tiles, k_chunks, sms);
+    int S = pick_split(tiles, k_chunks, sms);
+    while (S > 1 && slot_bytes(pair, units, S) > (size_t)kRingBudget + 1024) --S;
+    return S;
 }
 
 template <int kEpi>
@@ -378,13 +388,11 @@ cudaError_t launch_proj(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
     p.stages = kRingBudget / (int)p.stage_bytes;
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) return cudaErrorInvalidValue;
-    const int S = split_of(m_tiles * n_tiles * zdim, p.k_chunks);
+    const int units = (kEpi == kEpiYPair ? p.nb : p.n_mma) / 16;
+    const int S = split_of(m_tiles * n_tiles * zdim, p.k_chunks, kEpi == kEpiYPair, units);
     size_t smem = (size_t)p.stages * p.stage_bytes + 1024;
     // the reduction's slots (they reuse the ring once the main loop is over)
-    const int units = (kEpi == kEpiYPair ? p.nb : p.n_mma) / 16;
-    const int max_units = (units + S - 1) / S;
-    const size_t slot_need =
-        (size_t)(S - 1) * kBM * ((kEpi == kEpiYPair ? 2 : 1) * 16 * max_units + 4) * 4 + 1024;
+    const size_t slot_need = slot_bytes(kEpi == kEpiYPair, units, S);
     if (slot_need > smem) smem = slot_need;
     if (smem > (size_t)kRingBudget + 2048) return cudaErrorInvalidValue;
     p.wait_prior = programmatic;
@@ -457,7 +465,7 @@ cudaError_t launch_value_project(const __nv_bfloat16* u, const __nv_bfloat16* w_
         p.ctl = ctl;
         // while it runs (it is latency-bound), the stage-2 CTAs' first weight chunks go into L2
         p.pf_tiles = (D / kBM) * nt;
-        p.pf_split = split_of(p.pf_tiles, (int)(hk / kBK));
+        p.pf_split = split_of(p.pf_tiles, (int)(hk / kBK), true, round_up(bt, 16) / 16);
         p.pf_k_chunks = (int)(hk / kBK);
         p.pf_chunks = kPrefetchChunks;
         cudaError_t e = launch_proj<kEpiZ>(tm_a, tm_b, tm_w_o, p, 1, nt, H, false, st);
