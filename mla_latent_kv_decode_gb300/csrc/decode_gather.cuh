@@ -71,19 +71,15 @@ constexpr int kThreads = 64 + kSoftmaxThreads + 32;
 constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps
 // the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
 // range of the exchange (bf16 records); 2^8 keeps P s_g within f16 range for s_g < 255 (FP8)
-constexpr float kLazySlackBf16 = 15.0f;
-constexpr float kLazySlackFp8 = 8.0f;
-constexpr float kMaxGroupScale = 255.0f;   // 2^8 * 255 = 65280: P s_g stays a finite f16
+constexpr float kLazySlack = 15.0f;
+constexpr float kMaxGroupScale = 146.0f;   // 448 * 146 = 65,408: every code * s_g is a finite f16
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
 constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256); group a [0, 128), group b [128, 256)
-constexpr uint32_t kTmemSa = 256;      // score accumulators of this CTA's two latent groups
-constexpr uint32_t kTmemSb = 320;
-constexpr uint32_t kTmemSr = 384;      // ... and of its rope dims
-constexpr uint32_t kTmemPa = 448;      // P times the group scales
-constexpr uint32_t kTmemPb = 480;
+constexpr uint32_t kTmemS = 256;       // two score accumulators [64 columns each]: tile i uses i & 1
+constexpr uint32_t kTmemP = 384;       // two P buffers [32 columns each: 64 16-bit values a lane]
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 // shared-memory layout (bytes from a 1024-aligned base)
@@ -104,7 +100,7 @@ constexpr int kOffX = kOffMask + 32;                   // 187424: 2 buffers [16]
 constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 220192: [8][64][16 B] + alpha[64]
 constexpr int kOffLIn = kOffPIn + kPInMsg;             // 228640: 2 x l[64] of the peer's heads
 constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 229152
-constexpr int kNumBars = 3 * kNC + 4 + 2 + 2 + 2 + 2 + 6;
+constexpr int kNumBars = 3 * kNC + 8 + 2 + 2 + 2 + 2 + 6;
 constexpr int kOffRed = (kOffBar + 8 * kNumBars + 15) & ~15;   // owned heads' exchange between slices [4][64]
 constexpr int kSmemBytes = kOffRed + 4 * kOwned * 4 + 1024;    // + alignment slack
 // raw FP8 bytes of one tile and CTA: codes [64][256] at the slot's start, rope [64][64 B] at its
@@ -138,7 +134,7 @@ struct GatherParams {
 struct Bars {
     uint32_t c_full, c_empty;     // arrays of kNC
     uint32_t r_full;              // array of kNC: raw FP8 bytes of a tile landed
-    uint32_t s_full, s_empty, p_full, p_empty;
+    uint32_t s_full, s_empty, p_full, p_empty;   // arrays of 2 (score and P buffers)
     uint32_t x_full, x_free;      // arrays of 2
     uint32_t pin_full, pin_free;
     uint32_t l_full;              // array of 2
@@ -149,6 +145,10 @@ struct Bars {
     __device__ __forceinline__ uint32_t xf(int i) const { return x_full + 8 * i; }
     __device__ __forceinline__ uint32_t xe(int i) const { return x_free + 8 * i; }
     __device__ __forceinline__ uint32_t lf(int i) const { return l_full + 8 * i; }
+    __device__ __forceinline__ uint32_t sf(int i) const { return s_full + 8 * i; }
+    __device__ __forceinline__ uint32_t se(int i) const { return s_empty + 8 * i; }
+    __device__ __forceinline__ uint32_t pf(int i) const { return p_full + 8 * i; }
+    __device__ __forceinline__ uint32_t pe(int i) const { return p_empty + 8 * i; }
 };
 
 __device__ __forceinline__ Bars make_bars(uint32_t a) {
@@ -156,10 +156,10 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.c_full = a; a += 8 * kNC;
     b.c_empty = a; a += 8 * kNC;
     b.r_full = a; a += 8 * kNC;
-    b.s_full = a; a += 8;
-    b.s_empty = a; a += 8;
-    b.p_full = a; a += 8;
-    b.p_empty = a; a += 8;
+    b.s_full = a; a += 16;
+    b.s_empty = a; a += 16;
+    b.p_full = a; a += 16;
+    b.p_empty = a; a += 16;
     b.x_full = a; a += 16;
     b.x_free = a; a += 16;
     b.pin_full = a; a += 8;
@@ -228,10 +228,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // arrival per producer lane once its copies land, plus one after the mask is written
             mbar_init(bars.rf(i), kTopk ? 33 : 1);
         }
-        mbar_init(bars.s_full, 1);
-        mbar_init(bars.s_empty, kSoftmaxThreads / 32);   // one arrive per softmax warp
-        mbar_init(bars.p_full, kSoftmaxThreads / 32);
-        mbar_init(bars.p_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.sf(i), 1);
+            mbar_init(bars.se(i), kSoftmaxThreads / 32);   // one arrive per softmax warp
+            mbar_init(bars.pf(i), kSoftmaxThreads / 32);
+            mbar_init(bars.pe(i), 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.xf(i), 1);
             mbar_init(bars.xe(i), 8);    // one remote arrive per peer owner warp
@@ -376,33 +378,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
             uint32_t polls = 0;
             while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
-                if (iq < n_local && iq <= ip + 1) {
+                if (iq < n_local && iq <= ip + 2) {   // QK up to two tiles ahead of PV (two score buffers)
                     const int s = iq % kNC;
+                    const int sb = iq & 1;
                     const bool ready = __shfl_sync(
                         0xffffffffu,
                         (!cq.first() || mbar_test(bars.q_ready, seg_q & 1)) &&
-                            mbar_test(bars.cf(s), (iq / kNC) & 1) && mbar_test(bars.s_empty, (iq & 1) ^ 1),
+                            mbar_test(bars.cf(s), (iq / kNC) & 1) &&
+                            mbar_test(bars.se(sb), ((iq >> 1) & 1) ^ 1),
                         0);
                     if (ready) {
                         tc_fence_after();
                         const uint32_t st_lo = ((sbase + kOffConv + s * kConvBytes) >> 4) & 0x3FFF;
                         if (elect_one()) {
+                            const uint32_t sacc = tmem + kTmemS + 64 * sb;
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
-                                    mma_bf16_ss(tmem + (k < 2 ? kTmemSa : kTmemSb),
-                                                lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
+                                    mma_bf16_ss(sacc, lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
                                                 lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qk, ((k & 1) | kk) != 0 ? 1u : 0u);
+                                                id_qk, (k | kk) != 0 ? 1u : 0u);
                             if (!kShared) {
 #pragma unroll
                                 for (int kk = 0; kk < 2; ++kk)
-                                    mma_bf16_ss(tmem + kTmemSr, rope_hi | (qr_lo + kk * 2),
+                                    mma_bf16_ss(sacc, rope_hi | (qr_lo + kk * 2),
                                                 rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qr, kk != 0 ? 1u : 0u);
+                                                id_qr, 1u);
                             }
-                            mma_commit(bars.s_full);
+                            mma_commit(bars.sf(sb));
                             if (cq.last()) mma_commit(bars.q_empty);
                         }
                         __syncwarp();
@@ -417,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool pv_ready = __shfl_sync(
                     0xffffffffu,
                     (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
-                        mbar_test(bars.p_full, ip & 1),
+                        mbar_test(bars.pf(ip & 1), (ip >> 1) & 1),
                     0);
                 if (!pv_ready) {
                     if (++polls > wait_limit) {
@@ -435,10 +439,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < kT / 16; ++kk) {
                             const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
-                            mma_bf16_ts(tmem + kTmemO + 128 * g, tmem + (g == 0 ? kTmemPa : kTmemPb) + 8 * kk, vd,
+                            mma_bf16_ts(tmem + kTmemO + 128 * g, tmem + kTmemP + 32 * (ip & 1) + 8 * kk, vd,
                                         id_pv, (!seg_first || kk > 0) ? 1u : 0u);
                         }
-                    mma_commit(bars.p_empty);
+                    mma_commit(bars.pe(ip & 1));
                     mma_commit(bars.ce(ip % kNC));
                     if (cp.last()) mma_commit(bars.o_full);
                 }
@@ -727,46 +731,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             return ok;
         };
 
-        // group scales of the warp's 16 positions of tile i: element 2 t is (s_a, s_b) of
-        // position 16 ts + t (each row holds the scales of all four groups)
-        auto scales_of = [&](int i) -> const float2* {
-            return reinterpret_cast<const float2*>(sm + kOffScale + (i % kNC) * kScaleBytes) + 32 * ts + (int)r;
-        };
-
-        // this CTA's partial scores of tile i for the warp's 16 positions: s_a S_a + s_b S_b + S_rope
-        // (the tile's scales and mask, written by the agents, are read once its slot is complete)
+        // this CTA's partial scores of tile i for the warp's 16 positions (score buffer i & 1; the
+        // tile's mask, written with its slot, is read once the slot is complete)
         auto load_s = [&](int i, float (&v)[16]) -> bool {
             if (!wwait(bars.cf(i % kNC), (i / kNC) & 1, 18)) return false;
-            if (!wwait(bars.s_full, i & 1, 7)) return false;
-            const float2* sc = scales_of(i);
+            if (!wwait(bars.sf(i & 1), (i >> 1) & 1, 7)) return false;
             tc_fence_after();
-            {
-                uint32_t a[16], b[16];
-                tmem_ld16(tmem + lane_off + kTmemSa + kSlice * ts, a);
-                tmem_ld16(tmem + lane_off + kTmemSb + kSlice * ts, b);
-                tmem_wait_ld();
+            uint32_t a[16];
+            tmem_ld16(tmem + lane_off + kTmemS + 64 * (i & 1) + kSlice * ts, a);
+            tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float2 q = sc[2 * t];
-                    v[t] = fmaf(q.x, __uint_as_float(a[t]), q.y * __uint_as_float(b[t]));
-                }
-            }
-            if (!kShared) {
-                uint32_t e[16];
-                tmem_ld16(tmem + lane_off + kTmemSr + kSlice * ts, e);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] += __uint_as_float(e[t]);
-            }
+            for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(a[t]);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.s_empty);
+            if (lane == 0) mbar_arrive(bars.se(i & 1));
             return true;
         };
 
         // O rows of this warp (its 64 columns) times alpha, once PV of tile i - 1 has completed
         auto rescale_o = [&](int i, float alpha) {
-            if (!wwait(bars.p_empty, (i - 1) & 1, 10)) return;
+            if (!wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) return;
             tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
@@ -781,38 +765,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_st();
         };
 
-        // the warp's 16 P values of tile i (fp16 pairs from the softmax) times each group's
-        // scales into tensor memory, once PV of tile i - 1 has completed, then P ready for the
-        // MMA: f16 (P s_g) for FP8 records, bf16 P for bf16 records (scale 1)
+        // the warp's 16 P values of tile i (fp16 pairs from the softmax) into P buffer i & 1, once
+        // PV of tile i - 2 (its last reader) has completed, then P ready for the MMA: f16 for FP8
+        // records (their values carry the scales), bf16 otherwise
         auto store_p = [&](int i, const uint32_t (&pk)[8]) {
-            if (i >= 1 && !wwait(bars.p_empty, (i - 1) & 1, 11)) return;
-            uint32_t pa[8], pb[8];
+            if (i >= 2 && !wwait(bars.pe(i & 1), ((i >> 1) & 1) ^ 1, 11)) return;
+            uint32_t pa[8];
             if (kFp8) {
-                const float2* sc = scales_of(i);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 q0 = sc[4 * k], q1 = sc[4 * k + 2];
-                    __half2 h2;
-                    *reinterpret_cast<uint32_t*>(&h2) = pk[k];
-                    const float2 pf = __half22float2(h2);
-                    pa[k] = pack_f16x2(pf.x * q0.x, pf.y * q1.x);
-                    pb[k] = pack_f16x2(pf.x * q0.y, pf.y * q1.y);
-                }
+                for (int k = 0; k < 8; ++k) pa[k] = pk[k];
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     __half2 h2;
                     *reinterpret_cast<uint32_t*>(&h2) = pk[k];
                     const float2 pf = __half22float2(h2);
-                    pa[k] = pb[k] = pack_bf16x2(pf.x, pf.y);
+                    pa[k] = pack_bf16x2(pf.x, pf.y);
                 }
             }
-            tmem_st8(tmem + lane_off + kTmemPa + 8 * ts, pa);
-            tmem_st8(tmem + lane_off + kTmemPb + 8 * ts, pb);
+            tmem_st8(tmem + lane_off + kTmemP + 32 * (i & 1) + 8 * ts, pa);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && !s_abort) mbar_arrive(bars.p_full);
+            if (lane == 0 && !s_abort) mbar_arrive(bars.pf(i & 1));
         };
 
         // O rows of this warp normalised by l (row sum) into the output or a partial slot
@@ -886,19 +861,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t mk0 = mk[0], mk1 = mk[1];
                 auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
                 uint4 raw[4], rraw = zero;
+                float sc[4];
                 if (ok) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) raw[k] = *reinterpret_cast<const uint4*>(lat + (at + 256 * k) * 16);
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = at + 256 * k;
+                        raw[k] = *reinterpret_cast<const uint4*>(lat + e * 16);
+                        // the scale of the piece's 128-dim group: this CTA's group (e & 15) >> 3
+                        sc[k] = reinterpret_cast<const float*>(sm + kOffScale + slot * kScaleBytes)
+                            [(e >> 4) * 4 + 2 * (int)r + ((e & 15) >> 3)];
+                    }
                     rraw = *reinterpret_cast<const uint4*>(rope + at * 16);
                 }
                 named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
                 if (ok) {
-                    // 64 rows x 16 chunks of 16 codes; piece at + 256 k is chunk ch of row `row`
+                    // 64 rows x 16 chunks of 16 codes; piece at + 256 k is chunk ch of row `row`,
+                    // written as f16(code * s_g)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int e = at + 256 * k, row = e >> 4, ch = e & 15;
                         uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                        if (valid(row)) e4m3x16_to_f16(raw[k], o);
+                        if (valid(row)) e4m3x16_scaled_f16(raw[k], sc[k], o);
                         // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte
                         // parts 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
                         uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
@@ -910,8 +893,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int row = at >> 2, c4 = at & 3;
                     if (!valid(row)) rraw = zero;
                     st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
-                    // scales of rows outside the request: zero (their P is zero); a visible row
-                    // whose group scale is above 255 (or not finite) would overflow f16(P s_g)
+                    // a visible row whose group scale is above 146 (or not finite) would overflow
+                    // f16(code * s_g)
                     if (at < kT) {
                         uint4* sc = reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + at * 16);
                         if (!valid(at)) {
@@ -1149,7 +1132,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lfull_remote = mapa(bars.l_full, peer);
             const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
-            constexpr float slack = kFp8 ? kLazySlackFp8 : kLazySlackBf16;
+            constexpr float slack = kLazySlack;
             const float p_max = exp2f(slack);
             float m_used = -INFINITY, l_part = 0.f;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
