@@ -127,12 +127,13 @@ int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_l
  *                when that is 0); 256-byte aligned; its contents are clobbered.
  * A page index outside [0, num_pages) met while reading records MLA_ERR_BOUNDS.
  * Arithmetic: scores and outputs accumulate in fp32 on the tensor cores.  bf16 records: bf16
- * operands, P rounded once to bf16.  FP8 records: each code times its 128-dim group's scale is
- * rounded once to f16 (relative error at most 2^-11), the latent query enters as f16, converted
- * once per request (exact for |q| in [2^-14, 65504); smaller magnitudes lose low bits), and P
- * is rounded once to f16.  Outside that range the FP8 path does not compute: a q_lat element of
- * magnitude 65520 or more, or a visible record with a group scale above 146 (absmax above
- * 65,408) or not finite, records MLA_ERR_RANGE (either would overflow f16). */
+ * operands, P rounded once to bf16.  FP8 records: the E4M3 codes enter as f16 (exact), and so
+ * does q_lat, converted once per request (exact for |q| in [2^-14, 65504); smaller magnitudes
+ * lose low bits).  Each 128-dim group's scale multiplies in fp32: on that group's partial score,
+ * and on P as f16(P * scale), which stays finite for group scales up to 255 (absmax up to
+ * 114,240) because the running max is kept within 2^8 of every P.  Outside those two ranges the
+ * FP8 path does not compute: a q_lat element of magnitude 65520 or more (it would overflow f16),
+ * or a visible record with a group scale above 255 (or not finite), records MLA_ERR_RANGE. */
 mla_status mla_decode(int32_t fmt, const void* pool, int64_t num_pages, const void* q_lat,
                       const void* q_rope, const int32_t* block_table, int32_t max_pages,
                       const int32_t* seq_lens, int32_t max_seq_len, const int32_t* topk_idx,

@@ -201,18 +201,6 @@ inline int clusters_for_tiles(long long w_max, int sms) {
     return c < 1 ? 1 : (int)c;
 }
 
-// 16 e4m3 codes times an fp32 scale to 16 f16 values (pairs, low half first): the product of the
-// exact code and the scale, rounded once to f16 (relative error at most 2^-11 in f16's normal range).
-__device__ __forceinline__ void e4m3x16_scaled_f16(const uint4 c, float s, uint32_t (&o)[8]) {
-    uint32_t h[8];
-    e4m3x16_to_f16(c, h);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
-        o[k] = pack_f16x2(f.x * s, f.y * s);
-    }
-}
-
 // One E4M3 code (the low byte of `code`) as a float, exactly.
 __device__ __forceinline__ float e4m3_to_float(uint32_t code) {
     uint32_t h;

@@ -71,15 +71,29 @@ constexpr int kThreads = 64 + kSoftmaxThreads + 32;
 constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps
 // the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
 // range of the exchange (bf16 records); 2^8 keeps P s_g within f16 range for s_g < 255 (FP8)
-constexpr float kLazySlack = 15.0f;
-constexpr float kMaxGroupScale = 146.0f;   // 448 * 146 = 65,408: every code * s_g is a finite f16
+// the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
+// range of the exchange (bf16 and shared K = V records); 2^8 keeps P s_g within f16 range for
+// s_g < 255 (FP8 mixed records)
+constexpr float kLazySlackBf16 = 15.0f;
+constexpr float kLazySlackFp8 = 8.0f;
+constexpr float kMaxGroupScale = 255.0f;   // 2^8 * 255 = 65280: P s_g stays a finite f16
 constexpr int kHalfLat = 256;          // latent dims per CTA
 constexpr int kHalfRope = 32;          // rope dims per CTA
 constexpr int kOwned = 64;             // heads whose softmax a CTA finishes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;         // O_r: columns [0, 256); group a [0, 128), group b [128, 256)
-constexpr uint32_t kTmemS = 256;       // two score accumulators [64 columns each]: tile i uses i & 1
-constexpr uint32_t kTmemP = 384;       // two P buffers [32 columns each: 64 16-bit values a lane]
+// Tensor memory.  bf16 and shared K = V records: two score accumulators of 64 columns (tile i uses
+// i & 1) and two P buffers of 32 columns (64 16-bit values a lane), so that QK of the next tiles
+// overlaps the softmax of this one.  FP8 mixed records keep the scores of their two 128-dim scale
+// groups and of the rope dims apart (each group's scale multiplies its partial score in fp32,
+// exactly), and P times each group's scale: one set of three accumulators and two P buffers.
+constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemP = 384;
+constexpr uint32_t kTmemSa = 256;
+constexpr uint32_t kTmemSb = 320;
+constexpr uint32_t kTmemSr = 384;
+constexpr uint32_t kTmemPa = 448;
+constexpr uint32_t kTmemPb = 480;
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 // shared-memory layout (bytes from a 1024-aligned base)
@@ -190,6 +204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr bool kV41 = kFmt == MLA_KV_V41_FP4;
     constexpr bool kShared = kV4 || kV41;     // K = V = the 512-dim entry; no separate rope
     constexpr bool kRaw = kFp8 || kShared;    // the producer warp stages raw record bytes
+    constexpr int kSB = kFp8 ? 1 : 2;         // score buffers (and P buffers)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -378,33 +393,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
             uint32_t polls = 0;
             while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
-                if (iq < n_local && iq <= ip + 2) {   // QK up to two tiles ahead of PV (two score buffers)
+                if (iq < n_local && iq <= ip + kSB) {   // QK up to kSB tiles ahead of PV (its score buffers)
                     const int s = iq % kNC;
-                    const int sb = iq & 1;
+                    const int sb = iq % kSB;
                     const bool ready = __shfl_sync(
                         0xffffffffu,
                         (!cq.first() || mbar_test(bars.q_ready, seg_q & 1)) &&
                             mbar_test(bars.cf(s), (iq / kNC) & 1) &&
-                            mbar_test(bars.se(sb), ((iq >> 1) & 1) ^ 1),
+                            mbar_test(bars.se(sb), ((iq / kSB) & 1) ^ 1),
                         0);
                     if (ready) {
                         tc_fence_after();
                         const uint32_t st_lo = ((sbase + kOffConv + s * kConvBytes) >> 4) & 0x3FFF;
                         if (elect_one()) {
+                            // FP8 records: one accumulator per scale group and one for the rope
+                            // dims; otherwise everything into score buffer sb
                             const uint32_t sacc = tmem + kTmemS + 64 * sb;
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
-                                    mma_bf16_ss(sacc, lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
+                                    mma_bf16_ss(kFp8 ? tmem + (k < 2 ? kTmemSa : kTmemSb) : sacc,
+                                                lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
                                                 lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qk, (k | kk) != 0 ? 1u : 0u);
+                                                id_qk, (kFp8 ? ((k & 1) | kk) : (k | kk)) != 0 ? 1u : 0u);
                             if (!kShared) {
 #pragma unroll
                                 for (int kk = 0; kk < 2; ++kk)
-                                    mma_bf16_ss(sacc, rope_hi | (qr_lo + kk * 2),
+                                    mma_bf16_ss(kFp8 ? tmem + kTmemSr : sacc, rope_hi | (qr_lo + kk * 2),
                                                 rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qr, 1u);
+                                                id_qr, (kFp8 && kk == 0) ? 0u : 1u);
                             }
                             mma_commit(bars.sf(sb));
                             if (cq.last()) mma_commit(bars.q_empty);
@@ -421,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool pv_ready = __shfl_sync(
                     0xffffffffu,
                     (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
-                        mbar_test(bars.pf(ip & 1), (ip >> 1) & 1),
+                        mbar_test(bars.pf(ip % kSB), (ip / kSB) & 1),
                     0);
                 if (!pv_ready) {
                     if (++polls > wait_limit) {
@@ -439,10 +457,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < kT / 16; ++kk) {
                             const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
-                            mma_bf16_ts(tmem + kTmemO + 128 * g, tmem + kTmemP + 32 * (ip & 1) + 8 * kk, vd,
-                                        id_pv, (!seg_first || kk > 0) ? 1u : 0u);
+                            mma_bf16_ts(tmem + kTmemO + 128 * g,
+                                        tmem + (kFp8 ? (g == 0 ? kTmemPa : kTmemPb) : kTmemP + 32 * (ip % kSB)) + 8 * kk,
+                                        vd, id_pv, (!seg_first || kk > 0) ? 1u : 0u);
                         }
-                    mma_commit(bars.pe(ip & 1));
+                    mma_commit(bars.pe(ip % kSB));
                     mma_commit(bars.ce(ip % kNC));
                     if (cp.last()) mma_commit(bars.o_full);
                 }
@@ -731,26 +750,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             return ok;
         };
 
-        // this CTA's partial scores of tile i for the warp's 16 positions (score buffer i & 1; the
-        // tile's mask, written with its slot, is read once the slot is complete)
+        // group scales of the warp's 16 positions of tile i (FP8 records): element 2 t is (s_a, s_b)
+        // of position 16 ts + t (each row holds the scales of all four groups)
+        auto scales_of = [&](int i) -> const float2* {
+            return reinterpret_cast<const float2*>(sm + kOffScale + (i % kNC) * kScaleBytes) + 32 * ts + (int)r;
+        };
+
+        // this CTA's partial scores of tile i for the warp's 16 positions: score buffer i % kSB, or
+        // for FP8 records s_a S_a + s_b S_b + S_rope (the tile's scales and mask, written with its
+        // slot, are read once the slot is complete)
         auto load_s = [&](int i, float (&v)[16]) -> bool {
             if (!wwait(bars.cf(i % kNC), (i / kNC) & 1, 18)) return false;
-            if (!wwait(bars.sf(i & 1), (i >> 1) & 1, 7)) return false;
+            if (!wwait(bars.sf(i % kSB), (i / kSB) & 1, 7)) return false;
             tc_fence_after();
-            uint32_t a[16];
-            tmem_ld16(tmem + lane_off + kTmemS + 64 * (i & 1) + kSlice * ts, a);
-            tmem_wait_ld();
+            if (kFp8) {
+                const float2* sc = scales_of(i);
+                uint32_t a[16], b[16];
+                tmem_ld16(tmem + lane_off + kTmemSa + kSlice * ts, a);
+                tmem_ld16(tmem + lane_off + kTmemSb + kSlice * ts, b);
+                tmem_wait_ld();
 #pragma unroll
-            for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(a[t]);
+                for (int t = 0; t < 16; ++t) {
+                    const float2 q = sc[2 * t];
+                    v[t] = fmaf(q.x, __uint_as_float(a[t]), q.y * __uint_as_float(b[t]));
+                }
+                uint32_t e[16];
+                tmem_ld16(tmem + lane_off + kTmemSr + kSlice * ts, e);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] += __uint_as_float(e[t]);
+            } else {
+                uint32_t a[16];
+                tmem_ld16(tmem + lane_off + kTmemS + 64 * (i % kSB) + kSlice * ts, a);
+                tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(a[t]);
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.se(i & 1));
+            if (lane == 0) mbar_arrive(bars.se(i % kSB));
             return true;
         };
 
         // O rows of this warp (its 64 columns) times alpha, once PV of tile i - 1 has completed
         auto rescale_o = [&](int i, float alpha) {
-            if (!wwait(bars.pe((i - 1) & 1), ((i - 1) >> 1) & 1, 10)) return;
+            if (!wwait(bars.pe((i - 1) % kSB), ((i - 1) / kSB) & 1, 10)) return;
             tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
@@ -765,16 +809,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_st();
         };
 
-        // the warp's 16 P values of tile i (fp16 pairs from the softmax) into P buffer i & 1, once
-        // PV of tile i - 2 (its last reader) has completed, then P ready for the MMA: f16 for FP8
-        // records (their values carry the scales), bf16 otherwise
+        // the warp's 16 P values of tile i (fp16 pairs from the softmax) into tensor memory, once
+        // PV of tile i - kSB (the last reader of that P buffer) has completed, then P ready for the
+        // MMA: f16 (P s_g) per scale group for FP8 records, bf16 P otherwise
         auto store_p = [&](int i, const uint32_t (&pk)[8]) {
-            if (i >= 2 && !wwait(bars.pe(i & 1), ((i >> 1) & 1) ^ 1, 11)) return;
-            uint32_t pa[8];
+            if (i >= kSB && !wwait(bars.pe(i % kSB), ((i / kSB) & 1) ^ 1, 11)) return;
             if (kFp8) {
+                uint32_t pa[8], pb[8];
+                const float2* sc = scales_of(i);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) pa[k] = pk[k];
+                for (int k = 0; k < 8; ++k) {
+                    const float2 q0 = sc[4 * k], q1 = sc[4 * k + 2];
+                    __half2 h2;
+                    *reinterpret_cast<uint32_t*>(&h2) = pk[k];
+                    const float2 pf = __half22float2(h2);
+                    pa[k] = pack_f16x2(pf.x * q0.x, pf.y * q1.x);
+                    pb[k] = pack_f16x2(pf.x * q0.y, pf.y * q1.y);
+                }
+                tmem_st8(tmem + lane_off + kTmemPa + 8 * ts, pa);
+                tmem_st8(tmem + lane_off + kTmemPb + 8 * ts, pb);
             } else {
+                uint32_t pa[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     __half2 h2;
@@ -782,12 +837,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const float2 pf = __half22float2(h2);
                     pa[k] = pack_bf16x2(pf.x, pf.y);
                 }
+                tmem_st8(tmem + lane_off + kTmemP + 32 * (i % kSB) + 8 * ts, pa);
             }
-            tmem_st8(tmem + lane_off + kTmemP + 32 * (i & 1) + 8 * ts, pa);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && !s_abort) mbar_arrive(bars.pf(i & 1));
+            if (lane == 0 && !s_abort) mbar_arrive(bars.pf(i % kSB));
         };
 
         // O rows of this warp normalised by l (row sum) into the output or a partial slot
@@ -861,27 +916,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t mk0 = mk[0], mk1 = mk[1];
                 auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
                 uint4 raw[4], rraw = zero;
-                float sc[4];
                 if (ok) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = at + 256 * k;
-                        raw[k] = *reinterpret_cast<const uint4*>(lat + e * 16);
-                        // the scale of the piece's 128-dim group: this CTA's group (e & 15) >> 3
-                        sc[k] = reinterpret_cast<const float*>(sm + kOffScale + slot * kScaleBytes)
-                            [(e >> 4) * 4 + 2 * (int)r + ((e & 15) >> 3)];
-                    }
+                    for (int k = 0; k < 4; ++k) raw[k] = *reinterpret_cast<const uint4*>(lat + (at + 256 * k) * 16);
                     rraw = *reinterpret_cast<const uint4*>(rope + at * 16);
                 }
                 named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
                 if (ok) {
-                    // 64 rows x 16 chunks of 16 codes; piece at + 256 k is chunk ch of row `row`,
-                    // written as f16(code * s_g)
+                    // 64 rows x 16 chunks of 16 codes; piece at + 256 k is chunk ch of row `row`
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int e = at + 256 * k, row = e >> 4, ch = e & 15;
                         uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                        if (valid(row)) e4m3x16_scaled_f16(raw[k], sc[k], o);
+                        if (valid(row)) e4m3x16_to_f16(raw[k], o);
                         // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte
                         // parts 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
                         uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
@@ -893,8 +940,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int row = at >> 2, c4 = at & 3;
                     if (!valid(row)) rraw = zero;
                     st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
-                    // a visible row whose group scale is above 146 (or not finite) would overflow
-                    // f16(code * s_g)
+                    // scales of rows outside the request: zero (their P is zero); a visible row
+                    // whose group scale is above 255 (or not finite) would overflow f16(P s_g)
                     if (at < kT) {
                         uint4* sc = reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + at * 16);
                         if (!valid(at)) {
@@ -1132,7 +1179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t lfull_remote = mapa(bars.l_full, peer);
             const bool lead = (ts == 0 && lg == 2 * (int)r && lane == 0);
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
-            constexpr float slack = kLazySlack;
+            constexpr float slack = kFp8 ? kLazySlackFp8 : kLazySlackBf16;
             const float p_max = exp2f(slack);
             float m_used = -INFINITY, l_part = 0.f;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {

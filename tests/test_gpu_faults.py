@@ -41,9 +41,9 @@ def _bf16(torch, x):
 
 def test_fp8_path_reports_values_outside_its_range():
     """The FP8 record path runs its latent products on f16 operands: a q_lat element that would
-    overflow f16, or a visible record whose group scale is above 146 (so that a code times the
-    scale could overflow f16), is reported as MLA_ERR_RANGE instead of giving silent inf/NaN.
-    Values at the edge of the range are accepted, and the next call after an error is correct."""
+    overflow f16, or a visible record whose group scale is above 255 (so that P times the scale
+    could overflow f16), is reported as MLA_ERR_RANGE instead of giving silent inf/NaN.  Values at
+    the edge of the range are accepted, and the next call after an error is correct."""
     import torch
     for topk in (None, 64):
         w = synth.make_workload("fp8_batch", B=2, seq_len=300) if topk is None else \
@@ -62,13 +62,12 @@ def test_fp8_path_reports_values_outside_its_range():
         assert mla.check_status() == 6                 # MLA_ERR_RANGE, then cleared
         assert mla.check_status() == 0
         dw.q_lat[1, 5, 17] = q0
-        # one visible record of request 0 with a large group-1 element: amax 65,280 gives the
-        # scale 145.71 (accepted: every code times it is a finite f16), amax 65,536 the scale
-        # 146.29 (refused)
+        # one visible record of request 0 with a large group-1 element: amax 114,176 gives the
+        # scale 254.86 (accepted), amax 114,688 the scale 256 (refused)
         t = 0 if topk is None else int(w.topk_idx[0, 0])
         c, r = dw.rows(0, t, t + 1)
         slot = dw.slots(0, t, t + 1)
-        for big, want in ((65280.0, 0), (65536.0, 6)):
+        for big, want in ((114176.0, 0), (114688.0, 6)):
             assert _bf16(torch, big) == big
             cb = c.clone()
             cb[0, 130] = big
