@@ -105,6 +105,18 @@ def test_running_max_growth(torch):
         _run_full_compare(torch, w, f"running-max growth fmt={fmt}")
 
 
+def test_running_max_growth_topk_rows(torch):
+    """The growth test of the dense paths, through top-k tiles of both formats: bf16 records use
+    the double-buffered score and P layout, FP8 records the per-group one."""
+    seq = [4096, 3000, 130, 8000, 65]
+    K = 1024
+    idx = np.stack([synth.sorted_distinct_sample(26, synth.STREAM_TOPK, b, n, min(K, n)).tolist() +
+                    [-1] * (K - min(K, n)) for b, n in enumerate(seq)]).astype(np.int32)
+    for fmt in (0, 1):
+        w = _custom(f"growth_topk{fmt}", fmt, seq, seed=26, scale=4.0, topk_idx=idx)
+        _run_full_compare(torch, w, f"running-max growth, top-k rows fmt={fmt}")
+
+
 def test_topk_sparse_with_padding(torch):
     seed = 24
     seq = [5000, 700, 4097]

@@ -123,3 +123,14 @@ def test_shared_append_codec_edges():
         got = pool.cpu().numpy()
         bad = np.nonzero(got != ref)[0]
         assert bad.size == 0, f"fmt {fmt}: first differing byte {bad[:4]} gpu {got[bad[:4]]} oracle {ref[bad[:4]]}"
+
+
+@pytest.mark.parametrize("fmt,tag", FORMATS)
+def test_shared_running_max_growth(fmt, tag):
+    """Scores spread wide (score scale 4 instead of 1/sqrt(512)): the running max grows by more
+    than the lazy-max slack on most tiles, so O rows are rescaled mid-segment on both CTAs of a
+    pair, with the double-buffered score and P layout, and long requests merge partials with very
+    different maxima (and the sink)."""
+    w = synth.make_shared_workload(f"growth_{tag}", fmt=fmt, seq_lens=[4096, 3000, 130, 8000, 65], seed=51 + fmt)
+    w.scale = 4.0
+    _run(w, f"growth {tag}")
