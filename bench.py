@@ -184,18 +184,33 @@ class ClockSampler:
 # Reference arm / CPU baseline: the fp64 oracle on the host cores
 # ----------------------------------------------------------------------------------------------
 
-def _oracle_requests(w, budget_s: float, nthreads: int):
+_POOLS = {}
+
+
+def _request_pool(w, b: int):
+    """Request b's rows in a one-request oracle pool (built once per run: drawing and encoding the
+    rows is set-up, not the oracle's decode)."""
     import oracle
     from mla_latent_kv_decode_gb300 import synth
+    key = (w.name, w.seed, b)
+    if key not in _POOLS:
+        n = int(w.seq_lens[b])
+        pool = oracle.new_pool(w.fmt, (n + 63) // 64)
+        c, r = synth.kv_rows(w.seed, b, 0, n)
+        oracle.cache_append(w.fmt, pool, c, r, np.arange(n, dtype=np.int32))
+        _POOLS[key] = pool
+    return _POOLS[key]
+
+
+def _oracle_requests(w, budget_s: float, nthreads: int):
+    import oracle
     ql, qr = w.queries()
     done, tokens, spent = 0, 0, 0.0
     b = 0
     while b < w.B and (spent < budget_s or done == 0):
         n = int(w.seq_lens[b])
         pages = (n + 63) // 64
-        pool = oracle.new_pool(w.fmt, pages)
-        c, r = synth.kv_rows(w.seed, b, 0, n)
-        oracle.cache_append(w.fmt, pool, c, r, np.arange(n, dtype=np.int32))
+        pool = _request_pool(w, b)
         bt = np.arange(pages, dtype=np.int32)[None]
         pairs = [(0, h) for h in range(w.H)]
         t0 = time.perf_counter()

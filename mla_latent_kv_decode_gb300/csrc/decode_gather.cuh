@@ -1225,8 +1225,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int t = 0; t < 16; t += 2) {
                         const bool live = m_used != -INFINITY;
-                        const float p0 = (live && ((vmask >> t) & 1)) ? ex2(x[t] - m_used) : 0.f;
-                        const float p1 = (live && ((vmask >> (t + 1)) & 1)) ? ex2(x[t + 1] - m_used) : 0.f;
+                        float p0 = (live && ((vmask >> t) & 1)) ? ex2(x[t] - m_used) : 0.f;
+                        float p1 = (live && ((vmask >> (t + 1)) & 1)) ? ex2(x[t + 1] - m_used) : 0.f;
+                        if (!kFp8) {
+                            // bf16 P: the row sum adds the values PV multiplies (each bf16 value,
+                            // at most 2^15, travels exactly as fp16), so the weights sum to one
+                            p0 = __bfloat162float(__float2bfloat16_rn(p0));
+                            p1 = __bfloat162float(__float2bfloat16_rn(p1));
+                        }
                         psum += p0 + p1;
                         const __half2 h2 = __floats2half2_rn(p0, p1);
                         pk[t / 2] = *reinterpret_cast<const uint32_t*>(&h2);
