@@ -1181,13 +1181,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t bar_vote = 1 + lg, bar_sync = 5 + lg;
             constexpr float slack = kFp8 ? kLazySlackFp8 : kLazySlackBf16;
             const float p_max = exp2f(slack);
-            float m_used = -INFINITY, l_part = 0.f;
+            // l_part sums the P values PV multiplies (it normalises O); lx_part the unrounded ones
+            // (it gives the log-sum-exp); they differ only for bf16 P
+            float m_used = -INFINITY, l_part = 0.f, lx_part = 0.f;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
                 const int xb = i & 1;
                 const bool first = cu.first();
                 if (first) {
                     m_used = -INFINITY;
                     l_part = 0.f;
+                    lx_part = 0.f;
                     cut_front = cu.t > 0;   // the request started before this cluster's range
                 }
                 float v[16];
@@ -1218,15 +1221,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // four slices raises m where it exceeds m by more than the slack, O is rescaled
                 // here and, through alpha sent with P, in the peer, and P is computed again.
                 float alpha = 1.0f;
-                float psum;
+                float psum, pxsum;
                 uint32_t pk[8];
                 auto exp_tile = [&]() {
                     psum = 0.f;
+                    pxsum = 0.f;
 #pragma unroll
                     for (int t = 0; t < 16; t += 2) {
                         const bool live = m_used != -INFINITY;
                         float p0 = (live && ((vmask >> t) & 1)) ? ex2(x[t] - m_used) : 0.f;
                         float p1 = (live && ((vmask >> (t + 1)) & 1)) ? ex2(x[t + 1] - m_used) : 0.f;
+                        pxsum += p0 + p1;
                         if (!kFp8) {
                             // bf16 P: the row sum adds the values PV multiplies (each bf16 value,
                             // at most 2^15, travels exactly as fp16), so the weights sum to one
@@ -1254,12 +1259,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         alpha = grow ? ex2(m_used - m_new) : 1.0f;
                         if (__any_sync(0xffffffffu, grow)) rescale_o(i, alpha);
                         l_part *= alpha;
+                        lx_part *= alpha;
                     }
                     m_used = m_new;
                     named_bar_sync(bar_sync, 128);   // red[] rows of this lane group are free again
                     exp_tile();
                 }
                 l_part += psum;
+                lx_part += pxsum;
                 // P of these heads (fp16, before the group scales) to the peer, once it has taken
                 // the previous one; both CTAs apply their group scales to these values
                 if (wwait(bars.pin_free, (i & 1) ^ 1, 15)) {
@@ -1279,14 +1286,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     named_bar_sync(bar_sync, 128);
                     const float l_row = (red[hh] + red[kOwned + hh]) + (red[2 * kOwned + hh] + red[3 * kOwned + hh]);
                     named_bar_sync(bar_sync, 128);
+                    float lx_row = l_row;
+                    if (!kFp8) {
+                        red[ts * kOwned + hh] = lx_part;
+                        named_bar_sync(bar_sync, 128);
+                        lx_row = (red[hh] + red[kOwned + hh]) + (red[2 * kOwned + hh] + red[3 * kOwned + hh]);
+                        named_bar_sync(bar_sync, 128);
+                    }
                     // shared K = V entries with a sink, request finished here: exp(z') joins the
                     // denominator, 2^(z' log2 e - m) in the units of l (the merge adds it otherwise)
                     float l_fin = l_row;
-                    float L = l_row > 0.f ? (m_used + log2f(l_row)) * 0.6931471805599453f : -INFINITY;
+                    float L = lx_row > 0.f ? (m_used + log2f(lx_row)) * 0.6931471805599453f : -INFINITY;
                     if (kShared && p.sink != nullptr && !partial) {
                         const float zl = __ldg(p.sink + h);
                         if (l_row > 0.f) {
-                            const float a = m_used + log2f(l_row), z2 = zl * 1.4426950408889634f;
+                            const float a = m_used + log2f(lx_row), z2 = zl * 1.4426950408889634f;
                             const float hi = fmaxf(a, z2), lo = fminf(a, z2);
                             L = (hi + log2f(1.0f + exp2f(lo - hi))) * 0.6931471805599453f;
                             l_fin = l_row + exp2f(z2 - m_used);   // inf when the sink dominates: O / inf = 0

@@ -125,12 +125,37 @@ def test_shared_append_codec_edges():
         assert bad.size == 0, f"fmt {fmt}: first differing byte {bad[:4]} gpu {got[bad[:4]]} oracle {ref[bad[:4]]}"
 
 
+def _growth_events(w, slack_nats=15 * np.log(2.0)):
+    """How often a head's running max (kept while every P stays within 2^15 of it, as the kernel
+    keeps it) has to grow, tile by tile of 64 entries, over the whole batch (from the oracle's
+    own entries and scores)."""
+    pool = _oracle_pool(w)
+    q = synth.bf16_bits_to_f32(w.queries()).astype(np.float64)
+    events = 0
+    for b in range(w.B):
+        n = int(w.seq_lens[b])
+        if n == 0:
+            continue
+        E = np.stack([oracle.shared_read(w.fmt, pool, int(s)) for s in w.slots(b, 0, n)])
+        sc = w.scale * (q[b] @ E.T)                       # [H, n]
+        m = sc[:, :64].max(axis=1)
+        for t0 in range(64, n, 64):
+            tm = sc[:, t0:t0 + 64].max(axis=1)
+            grow = tm > m + slack_nats
+            events += int(grow.sum())
+            m = np.where(grow, tm, m)
+    return events
+
+
 @pytest.mark.parametrize("fmt,tag", FORMATS)
 def test_shared_running_max_growth(fmt, tag):
-    """Scores spread wide (score scale 4 instead of 1/sqrt(512)): the running max grows by more
-    than the lazy-max slack on most tiles, so O rows are rescaled mid-segment on both CTAs of a
-    pair, with the double-buffered score and P layout, and long requests merge partials with very
-    different maxima (and the sink)."""
+    """Scores spread wide (score scale 1 instead of 1/sqrt(512), a score spread of about 23 nats):
+    heads' running maxima grow by more than the lazy-max slack hundreds of times, so O rows are
+    rescaled mid-segment on both CTAs of a pair, with the double-buffered score and P layout, and
+    long requests merge partials with very different maxima (and the sink).  (At scale 4 a few
+    entries hold nearly all the weight, and bf16 P, rounded to 2^-9, moves such an output by up to
+    2^-9 |E_1 - E_2|: beyond the 1e-2 bar for some rows; the MLA records' growth tests run there.)"""
     w = synth.make_shared_workload(f"growth_{tag}", fmt=fmt, seq_lens=[4096, 3000, 130, 8000, 65], seed=51 + fmt)
-    w.scale = 4.0
+    w.scale = 1.0
+    assert _growth_events(w) >= 200
     _run(w, f"growth {tag}")
