@@ -2,8 +2,8 @@
 // decode_gather.cuh -- the tensor-core decode kernel over rows it gathers itself (included by
 // decode_gather.cu and decode_shared.cu, which instantiate it for their record formats).
 //
-// Tensor-core absorbed MLA decode over rows the kernel gathers itself: the
-// FP8 mixed cache (dense) and the top-k sparse path (both cache formats).
+// Tensor-core absorbed MLA decode over rows the kernel gathers itself: the FP8 mixed cache
+// (pages and top-k rows), bf16 top-k rows, and the shared K = V entry formats.
 //
 // It computes what decode_tc.cu computes ("DeepSeek's KV Cache: From 3.9 MB to 890 B per Token",
 // Fig. 4 (1), Fig. 5 (2), Fig. 6 (2)) and shares its organisation: clusters of two CTAs that
@@ -15,13 +15,17 @@
 //   * a tile is 64 rows: the positions of one cache page (dense), or 64 consecutive entries of a
 //     request's top-k list (sparse: only listed positions enter the softmax, same page, Fig. 8
 //     and the DSA description on that page).  Rows outside the request (past its length, padding
-//     entries, entries >= N_b) are masked and read as zeros;
-//   * FP8 records: a producer warp copies each tile's raw bytes of this CTA's half into a
-//     conversion slot as soon as PV has released it (a page: three TMA boxes; top-k rows: 21
-//     16-byte cp.async pieces per row, one row per lane), with the row's four group scales and a
-//     64-bit mask of valid rows; the agent warps then convert the slot in place into the MMA
-//     operand layouts: latent [64 x 256] (128-byte swizzle), rope [64 x 32] (64-byte swizzle),
-//     zeros for rows outside the request;
+//     entries, entries >= N_b) are masked and their latent rows read as zeros;
+//   * raw record formats: a producer warp copies each tile's bytes of this CTA's half (a page:
+//     TMA boxes; top-k rows: 16-byte cp.async pieces, one row per lane) and each is converted
+//     into the MMA operand layouts, latent [64 x 256] (128-byte swizzle) and rope [64 x 32]
+//     (64-byte swizzle, straight from the copy).  Two ways, one per instantiation:
+//       - FP8 pages: the codes land in the conversion slot with the rope, the four group scales
+//         and a 64-bit mask of valid rows once PV has released the slot, and the agent warps
+//         convert them in place;
+//       - FP8 top-k rows and the shared K = V formats ("converter instantiations"): the codes of
+//         the next tile land in a staging buffer, and four converter warps write each piece
+//         converted into the slot once PV has released it (its rope and scales land there);
 //   * bf16 records (top-k only) are loaded by the agents from global memory straight into those
 //     layouts;
 //   * FP8 records (512 e4m3 codes, one fp32 scale per 128 dims, 64 bf16 rope dims; the 656-byte
@@ -33,22 +37,27 @@
 //     accumulator per group, and on P, O_g += (P s_g) V_g for the PV of group g, with P s_g
 //     rounded once to f16 (2^-11).  The running max is kept within 2^8 of every P here, so P s_g
 //     stays finite for group scales below 255 (absmax below 114,000).  BF16 records take scale 1
-//     and bf16 operands throughout.
+//     and bf16 operands throughout; shared K = V entries convert exactly to bf16 with their
+//     scales applied.
 //
 // Tensor memory (all 512 columns): O_r [0, 256), S_a [256, 320), S_b [320, 384),
-// S_rope [384, 448), P_a [448, 480), P_b [480, 512) (64 16-bit values per lane in 32 columns).
-// Shared memory: Q half (72 KB, TMA), three converted tiles (36 KB each), exchange buffers.
+// S_rope [384, 448), P_a [448, 480), P_b [480, 512) (64 16-bit values per lane in 32 columns);
+// other formats two score buffers and two P buffers in [256, 512).
+// Shared memory: Q half (72 KB, TMA), three conversion slots (36 KB each), the staging buffer
+// (16 KB; the second exchange buffer where nothing is staged), exchange buffers.
 //
-// Warp roles (608 threads): warp 0 Q loads (TMA) and the f16 conversion of Q; warp 1 MMA issuer
-// (+ TMEM owner); warps 2-17: thread = head = TMEM lane, four warps per 32-lane group, 16
-// positions of a tile each; the 8 warps on the owned heads' lanes run the softmax, the other 8
-// ("agents") forward partial scores, convert the tiles, place the peer's P and finish those O
-// rows; warp 18 loads the FP8 tiles.  Every wait is bounded: on expiry the kernel records
-// MLA_ERR_TIMEOUT, stops issuing, drains its MMAs, frees TMEM and returns.
+// Warp roles: warps 0-3: Q loads (TMA) and the f16 conversion of Q, the MMA issuer (+ TMEM owner),
+// the producer, and an idle warp; warps 4-19: thread = head = TMEM lane, four warps per 32-lane
+// group, 16 positions of a tile each; the 8 warps on the owned heads' lanes run the softmax, the
+// other 8 ("agents") forward partial scores, place the peer's P and finish those O rows (and
+// convert FP8 pages, or load bf16 rows); warps 20-23 (converter instantiations): the converters.
+// Every wait is bounded: on expiry the kernel records MLA_ERR_TIMEOUT, stops issuing, drains its
+// MMAs, frees TMEM and returns.
 //
-// The kernel is a template over (record format, tile kind), instantiated for FP8 pages, FP8 top-k
-// rows and bf16 top-k rows, so that each instantiation holds only its own paths (at 608 threads
-// a thread has 96 registers; the shared code spilled twice as much).
+// The kernel is a template over (record format, tile kind) so that each instantiation holds only
+// its own paths: at 640 threads a thread has 96 registers; converter instantiations launch 768
+// threads with 80 a thread and move registers from warps 0-3 and the converters to the owners and
+// agents (setmaxnreg).
 #include <cuda.h>
 #include <cstring>
 #include <cuda_fp16.h>
@@ -66,11 +75,32 @@ constexpr int kSegCost = 1;           // a segment start costs about one tile (s
 constexpr int kNC = 3;                 // converted tile slots
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
 constexpr int kSlice = kT / 4;         // positions per warp
-constexpr int kProducerWarp = 2 + kSoftmaxThreads / 32;   // warp 18: FP8 tile loads
-constexpr int kThreads = 64 + kSoftmaxThreads + 32;
-constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps
-// the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
-// range of the exchange (bf16 records); 2^8 keeps P s_g within f16 range for s_g < 255 (FP8)
+constexpr int kProducerWarp = 2;       // raw tile loads
+constexpr int kSoftWarp0 = 4;          // warps 4-19: owners and agents
+constexpr int kConvWarp0 = kSoftWarp0 + kSoftmaxThreads / 32;   // warps 20-23: conversion of raw tiles
+constexpr int kConvWarps = 4;
+constexpr uint32_t kBarAgents = 9;     // named barrier of the 8 agent warps (in-place conversion)
+// Instantiations whose raw tiles are converted by converter warps (FP8 top-k rows and the shared
+// K = V formats) rather than in place by the agents (FP8 pages; bf16 top-k rows are loaded by the
+// agents): they stage each tile's codes, and add four warps.
+constexpr bool gather_conv(int fmt, bool topk) { return fmt != MLA_KV_BF16 && (topk || fmt != MLA_KV_FP8_MIXED); }
+constexpr int gather_threads(int fmt, bool topk) {
+    return 32 * kSoftWarp0 + kSoftmaxThreads + (gather_conv(fmt, topk) ? 32 * kConvWarps : 0);
+}
+// Registers a thread (converter instantiations: 768 threads launch with 80 a thread; each warpgroup then
+// sets its own: kRegsW0 for warps 0-3, kRegsConv for the converters and kRegsSoftmax for each of
+// the four warpgroups of owners and agents, at most the launch's 6 x 80 per sub-partition lane;
+// all return to 80 before the common teardown).  A raise waits until other warpgroups have
+// released enough: the releases come first (warps 0-3 and the converters, at the start of their
+// roles) and the returns to 80 last.
+constexpr int kRegsLaunch = 80;
+constexpr int kRegsW0 = 64;
+constexpr int kRegsConv = 64;
+constexpr int kRegsSoftmax = 88;
+// every warp meets here after its warpgroup's first register change, so that no warpgroup takes
+// registers back (at its end) before the owners' and agents' raise has been granted
+constexpr uint32_t kBarRegs = 15;
+static_assert(kRegsW0 + kRegsConv + 4 * kRegsSoftmax <= 6 * kRegsLaunch, "register split above the launch's registers");
 // the running max is kept until a row max exceeds it by 2^slack: 2^15 keeps P within the fp16
 // range of the exchange (bf16 and shared K = V records); 2^8 keeps P s_g within f16 range for
 // s_g < 255 (FP8 mixed records)
@@ -108,18 +138,18 @@ constexpr int kOffQ = 0;
 constexpr int kOffQRope = kOffQ + 4 * kQLatChunk;      // 65536
 constexpr int kOffConv = kOffQRope + kQRopeBytes;      // 73728
 constexpr int kScaleBytes = kT * 16;                   // per slot: [64 rows][4 groups] fp32
-constexpr int kOffScale = kOffConv + kNC * kConvBytes; // 184320: [kNC][64 rows][4] fp32
-constexpr int kOffMask = kOffScale + kNC * kScaleBytes; // 187392: [kNC][2] uint32 valid rows
-constexpr int kOffX = kOffMask + 32;                   // 187424: 2 buffers [16][64][16 B]
-constexpr int kOffPIn = kOffX + 2 * kXBytes;           // 220192: [8][64][16 B] + alpha[64]
+constexpr int kStageBytes = kT * kHalfLat;             // converter instantiations: raw codes of the next
+                                                       // tile [64][256 B]; otherwise the second X buffer
+constexpr int kOffStage = kOffConv + kNC * kConvBytes; // 184320
+constexpr int kOffScale = kOffStage + kStageBytes;     // 200704: [kNC][64 rows][16 B]
+constexpr int kOffMask = kOffScale + kNC * kScaleBytes; // 203776: [kNC][2] uint32 valid rows + staging's [2]
+constexpr int kOffX = kOffMask + 32;                   // 203808: [16][64][16 B] (X buffer 0)
+constexpr int kOffPIn = kOffX + kXBytes;               // 220192: [8][64][16 B] + alpha[64]
 constexpr int kOffLIn = kOffPIn + kPInMsg;             // 228640: 2 x l[64] of the peer's heads
 constexpr int kOffBar = kOffLIn + 2 * kOwned * 4;      // 229152
-constexpr int kNumBars = 3 * kNC + 8 + 2 + 2 + 2 + 2 + 6;
+constexpr int kNumBars = 3 * kNC + 8 + 2 + 2 + 2 + 2 + 6 + 2;
 constexpr int kOffRed = (kOffBar + 8 * kNumBars + 15) & ~15;   // owned heads' exchange between slices [4][64]
 constexpr int kSmemBytes = kOffRed + 4 * kOwned * 4 + 1024;    // + alignment slack
-// raw FP8 bytes of one tile and CTA: codes [64][256] at the slot's start, rope [64][64 B] at its
-// rope region, scales [64][16 B]
-constexpr uint32_t kRawTileBytes = kT * (kHalfLat + 2 * kHalfRope + 16);   // 21504
 
 constexpr uint32_t kQBytes = 4 * kQLatChunk + kQRopeBytes;     // 73728 per CTA
 static_assert(kSmemBytes + 64 <= 232448, "shared memory above the 227 KB a CTA may use");
@@ -147,7 +177,8 @@ struct GatherParams {
 
 struct Bars {
     uint32_t c_full, c_empty;     // arrays of kNC
-    uint32_t r_full;              // array of kNC: raw FP8 bytes of a tile landed
+    uint32_t r_full;              // array of kNC: the slot's raw rope and scales landed
+    uint32_t stage_full, stage_empty;   // the staging buffer holds the next tile's raw codes / was read
     uint32_t s_full, s_empty, p_full, p_empty;   // arrays of 2 (score and P buffers)
     uint32_t x_full, x_free;      // arrays of 2
     uint32_t pin_full, pin_free;
@@ -170,6 +201,8 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
     b.c_full = a; a += 8 * kNC;
     b.c_empty = a; a += 8 * kNC;
     b.r_full = a; a += 8 * kNC;
+    b.stage_full = a; a += 8;
+    b.stage_empty = a; a += 8;
     b.s_full = a; a += 16;
     b.s_empty = a; a += 16;
     b.p_full = a; a += 16;
@@ -192,7 +225,7 @@ __device__ __forceinline__ Bars make_bars(uint32_t a) {
 // rows (dense bf16 pages take decode_tc_kernel), and pages and top-k rows of each shared K = V
 // entry format, so that each holds only its own paths.
 template <int kFmt, bool kTopk>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt, kTopk), 1)
     decode_gather_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                          const __grid_constant__ CUtensorMap tm_qrope,
                          const __grid_constant__ CUtensorMap tm_codes,    // pool fields as bytes
@@ -204,6 +237,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr bool kV41 = kFmt == MLA_KV_V41_FP4;
     constexpr bool kShared = kV4 || kV41;     // K = V = the 512-dim entry; no separate rope
     constexpr bool kRaw = kFp8 || kShared;    // the producer warp stages raw record bytes
+    constexpr bool kConv = gather_conv(kFmt, kTopk);   // converter warps (else in-place conversion)
+    constexpr int kNX = kConv ? 1 : 2;        // X buffers (the second one shares the staging buffer)
     constexpr int kSB = kFp8 ? 1 : 2;         // score buffers (and P buffers)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -237,12 +272,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (tid == 32) {
         for (int i = 0; i < kNC; ++i) {
-            mbar_init(bars.cf(i), 8);    // one arrive per agent warp once its rows are written
+            // one arrive per converter warp (raw formats) or agent warp (bf16) once its rows are written
+            mbar_init(bars.cf(i), kConv ? kConvWarps : 8);
             mbar_init(bars.ce(i), 1);
-            // dense FP8 tiles: the producer's one arrival with the TMA bytes; top-k FP8 tiles: one
-            // arrival per producer lane once its copies land, plus one after the mask is written
-            mbar_init(bars.rf(i), kTopk ? 33 : 1);
+            // pages: the producer's one arrival with the TMA bytes; top-k rows: one arrival per
+            // producer lane once its copies land
+            mbar_init(bars.rf(i), kTopk ? 32 : 1);
         }
+        // the staging buffer: as rf, plus (top-k) one arrival after the mask is written; emptied
+        // by one arrive per converter warp
+        mbar_init(bars.stage_full, kTopk ? 33 : 1);
+        mbar_init(bars.stage_empty, kConvWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.sf(i), 1);
             mbar_init(bars.se(i), kSoftmaxThreads / 32);   // one arrive per softmax warp
@@ -301,433 +341,595 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto pos_record = [&](const Cursor& cj, int pos) -> const uint8_t* { return record_at(pos, page_of(cj, pos)); };
     auto row_record = [&](const Cursor& cj, int row) -> const uint8_t* { return pos_record(cj, row_pos(cj, row)); };
 
-    if (n_local == 0 && warp >= 2) {
+    if (n_local == 0 && warp >= kSoftWarp0 && warp < kConvWarp0) {
         // an empty range: its partial slots must not contribute to any merge
-        const int h = tid - 64;
+        const int h = tid - 32 * kSoftWarp0;
         if (r == 0 && h < kHeads) {
             p.lse_part[(size_t)(2 * c) * kHeads + h] = -INFINITY;
             p.lse_part[(size_t)(2 * c + 1) * kHeads + h] = -INFINITY;
         }
     }
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ Q loads (TMA) + f16
-        // FP8 records: once a request's Q half has landed, the whole warp converts its latent
-        // part from bf16 to f16 in place (the swizzle permutes whole 16-byte chunks, so each
-        // chunk keeps its place), then releases it to the MMA issuer.
-        Cursor cu;
-        if (lane == 0 && n_local > 0) {
-            tma_prefetch_desc(&tm_qlat);
-            if (!kShared) tma_prefetch_desc(&tm_qrope);
+    if (warp < kSoftWarp0) {
+        // warps 0-3: Q loads, MMA issuer, raw tile loads (warp 3 idle)
+        if constexpr (kConv) {
+            reg_dealloc<kRegsW0>();
+            named_bar_sync(kBarRegs, gather_threads(kFmt, kTopk));
         }
-        cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-        int seg = 0;
-        for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-            if (!cu.first()) continue;
-            bool ok = !s_abort;
-            if (ok && seg > 0) ok = mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) fail(p.ctl, &s_abort, 1);
-                break;
+        if (warp == 0) {
+            // ------------------------------------------------------------------ Q loads (TMA) + f16
+            // FP8 records: once a request's Q half has landed, the whole warp converts its latent
+            // part from bf16 to f16 in place (the swizzle permutes whole 16-byte chunks, so each
+            // chunk keeps its place), then releases it to the MMA issuer.
+            Cursor cu;
+            if (lane == 0 && n_local > 0) {
+                tma_prefetch_desc(&tm_qlat);
+                if (!kShared) tma_prefetch_desc(&tm_qrope);
             }
-            if (lane == 0) {
-                const int qrow = cu.b * kHeads;
-                mbar_arrive_expect_tx(bars.q_full, kShared ? 4 * kQLatChunk : kQBytes);
-                for (int k = 0; k < 4; ++k)
-                    tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
-                                (int)r * kHalfLat + 64 * k, qrow);
-                if (!kShared) tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full, seg & 1, wait_limit));
-            if (!ok) {
-                if (lane == 0) fail(p.ctl, &s_abort, 19);
-                break;
-            }
-            if (kFp8) {
-                // an element that overflows f16 (|q| >= 65520) is outside this path's range
-                uint32_t inf = 0;
-#pragma unroll 8
-                for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
-                    uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
-                    const uint4 v = *q;
-                    const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                               bf16x2_to_f16x2(v.w));
-                    inf |= f16x2_inf_or_nan(f.x) | f16x2_inf_or_nan(f.y) | f16x2_inf_or_nan(f.z) |
-                           f16x2_inf_or_nan(f.w);
-                    *q = f;
-                }
-                fence_proxy_async_smem();
-                if (__any_sync(0xffffffffu, inf != 0) && lane == 0) record_error(p.ctl, MLA_ERR_RANGE, cu.b);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.q_ready);
-            ++seg;
-        }
-        // drain: the last Q load lands before this CTA may exit
-        if (lane == 0 && seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop so that its operands stay warp-uniform; one elected lane
-        // issues each MMA and commit.  QK of a tile: 8 MMAs per latent group into that group's
-        // accumulator (f16 operands for FP8 records), 2 rope MMAs (bf16); PV: per group, 4 MMAs
-        // of 128x128x16 with P times the group's scales from tensor memory.  One score set and
-        // one P set in tensor memory: QK of tile i + 1 follows the softmax's reads of tile i's
-        // scores, P of tile i + 1 follows PV of tile i.
-        if (n_local > 0) {
-            constexpr uint32_t id_qk = kFp8 ? idesc_f16(128, kT, 0, 0) : idesc_bf16(128, kT, 0, 0);
-            constexpr uint32_t id_qr = idesc_bf16(128, kT, 0, 0);
-            constexpr uint32_t id_pv = kFp8 ? idesc_f16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 1);
-            const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
-            const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
-            const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
-            const uint32_t lat_lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
-            const uint32_t rope_lo = (uint32_t)smem_desc(0, 16, 512, kSw64);
-            const uint32_t v_lo = (uint32_t)smem_desc(0, kKvLatChunk, 1024, kSw128);
-            const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
-            const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
-            Cursor cq, cp;
-            cq.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-            cp = cq;
-            int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
-            uint32_t polls = 0;
-            while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
-                if (iq < n_local && iq <= ip + kSB) {   // QK up to kSB tiles ahead of PV (its score buffers)
-                    const int s = iq % kNC;
-                    const int sb = iq % kSB;
-                    const bool ready = __shfl_sync(
-                        0xffffffffu,
-                        (!cq.first() || mbar_test(bars.q_ready, seg_q & 1)) &&
-                            mbar_test(bars.cf(s), (iq / kNC) & 1) &&
-                            mbar_test(bars.se(sb), ((iq / kSB) & 1) ^ 1),
-                        0);
-                    if (ready) {
-                        tc_fence_after();
-                        const uint32_t st_lo = ((sbase + kOffConv + s * kConvBytes) >> 4) & 0x3FFF;
-                        if (elect_one()) {
-                            // FP8 records: one accumulator per scale group and one for the rope
-                            // dims; otherwise everything into score buffer sb
-                            const uint32_t sacc = tmem + kTmemS + 64 * sb;
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    mma_bf16_ss(kFp8 ? tmem + (k < 2 ? kTmemSa : kTmemSb) : sacc,
-                                                lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
-                                                lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qk, (kFp8 ? ((k & 1) | kk) : (k | kk)) != 0 ? 1u : 0u);
-                            if (!kShared) {
-#pragma unroll
-                                for (int kk = 0; kk < 2; ++kk)
-                                    mma_bf16_ss(kFp8 ? tmem + kTmemSr : sacc, rope_hi | (qr_lo + kk * 2),
-                                                rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
-                                                id_qr, (kFp8 && kk == 0) ? 0u : 1u);
-                            }
-                            mma_commit(bars.sf(sb));
-                            if (cq.last()) mma_commit(bars.q_empty);
-                        }
-                        __syncwarp();
-                        if (cq.last()) ++seg_q;
-                        cq.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                        ++iq;
-                        polls = 0;
-                        continue;
-                    }
-                }
-                const bool seg_first = cp.first();
-                const bool pv_ready = __shfl_sync(
-                    0xffffffffu,
-                    (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
-                        mbar_test(bars.pf(ip % kSB), (ip / kSB) & 1),
-                    0);
-                if (!pv_ready) {
-                    if (++polls > wait_limit) {
-                        if (lane == 0) fail(p.ctl, &s_abort, 6);
-                        break;
-                    }
-                    continue;
-                }
-                polls = 0;
-                tc_fence_after();
-                const uint32_t v = ((sbase + kOffConv + (ip % kNC) * kConvBytes) >> 4) & 0x3FFF;
-                if (elect_one()) {
-#pragma unroll
-                    for (int g = 0; g < 2; ++g)
-#pragma unroll
-                        for (int kk = 0; kk < kT / 16; ++kk) {
-                            const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
-                            mma_bf16_ts(tmem + kTmemO + 128 * g,
-                                        tmem + (kFp8 ? (g == 0 ? kTmemPa : kTmemPb) : kTmemP + 32 * (ip % kSB)) + 8 * kk,
-                                        vd, id_pv, (!seg_first || kk > 0) ? 1u : 0u);
-                        }
-                    mma_commit(bars.pe(ip % kSB));
-                    mma_commit(bars.ce(ip % kNC));
-                    if (cp.last()) mma_commit(bars.o_full);
-                }
-                __syncwarp();
-                if (cp.last()) ++seg_p;
-                cp.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                ++ip;
-            }
-        }
-        __syncwarp();
-    } else if (warp == kProducerWarp) {
-        // ------------------------------------------------------------------ FP8 tile loads
-        // Tile j's raw bytes into conversion slot j % kNC once PV of tile j - kNC has released it,
-        // with the mask of valid rows (written before the arrival the agents wait on).  A dense
-        // tile is one page: three TMA boxes of its 64 rows (rows past the request's end are
-        // loaded and then zeroed by the agents).  A top-k tile: each lane copies its two rows with
-        // 16-byte cp.async (21 pieces per row: 16 of codes, the scales, 4 of rope) and arrives
-        // once they have landed.  Pages: the next tile's rows are looked up after a tile is
-        // issued, and the page kPfAhead tiles ahead is prefetched into L2.  Top-k rows: index
-        // loads, page loads and records run as a three-stage pipeline (see below), and each
-        // tile's rows are prefetched into L2 one tile ahead of their copies.
-        if (kRaw && n_local > 0) {
-            constexpr int kPfAhead = 3;
-            constexpr bool dense = !kTopk;
-            if (dense && lane == 0) {
-                tma_prefetch_desc(&tm_codes);
-                tma_prefetch_desc(&tm_krope);
-                tma_prefetch_desc(&tm_scl);
-            }
-            Cursor cj, cpf;   // the next tile to load, and (dense) the next tile to prefetch into L2
-            cj.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
-            cpf = cj;
-            int j_pf = 0;
-            // L2 prefetch of the rows of the records given (dense: lane 0 holds the page's row 0)
-            auto prefetch = [&](const uint8_t* f0, const uint8_t* f1) {
-                if (dense) {
-                    if (f0) {
-                        const int y = (int)((f0 - p.pool) / rec_bytes);   // slot of the page's row 0
-                        if (kFp8) {
-                            tma_prefetch_l2_2d(&tm_codes, kHalfLat * (int)r, y);
-                            tma_prefetch_l2_2d(&tm_krope, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
-                            tma_prefetch_l2_2d(&tm_scl, kFp8ScaleOff, y);
-                        } else if (kV4) {
-                            tma_prefetch_l2_3d(&tm_codes, kHalfLat * (int)r, 0, y / kPage);
-                            if (r == 1) tma_prefetch_l2_3d(&tm_krope, 0, 0, y / kPage);
-                            prefetch_l2(p.pool + (size_t)(y / kPage) * kV4PageBytes + kV4ScaleOff, kPage * 8);
-                        } else {
-                            tma_prefetch_l2_2d(&tm_codes, 128 * (int)r, y);
-                            tma_prefetch_l2_2d(&tm_scl, kV41ScaleOff + 16 * (int)r, y);
-                        }
-                    }
-                } else {
-                    // the lines of the row's codes half and of its scales and rope
-                    const uint8_t* pq[2] = {f0, f1};
-#pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        if (pq[q]) {
-                            if (kFp8) {
-                                prefetch_line_l2(pq[q] + kHalfLat * (int)r);
-                                prefetch_line_l2(pq[q] + kHalfLat * (int)r + 128);
-                                prefetch_line_l2(pq[q] + kFp8ScaleOff);
-                                prefetch_line_l2(pq[q] + kFp8RecordBytes - 16);
-                            } else if (kV4) {
-                                const size_t sl = (size_t)(pq[q] - p.pool) / kV4EntryBytes;
-                                const uint8_t* base = p.pool + (sl / kPage) * kV4PageBytes;
-                                const int row = (int)(sl % kPage);
-                                prefetch_l2(base + row * kENope + kHalfLat * (int)r, r == 0 ? 256 : 192);
-                                if (r == 1) prefetch_l2(base + kV4RopeOff + row * 128, 128);
-                                prefetch_line_l2(base + kV4ScaleOff + row * 8);
-                            } else {
-                                prefetch_l2(pq[q] + 128 * (int)r, 128);
-                                prefetch_line_l2(pq[q] + kV41ScaleOff + 16 * (int)r);
-                            }
-                        }
-                }
-            };
-            // Dense tiles: at the start of each iteration the page of tile j_pf (looked up by lane 0
-            // the iteration before) is prefetched and the page of the next tile to prefetch looked
-            // up; after a tile is issued, rows lane, lane + 32 of the next one are looked up.
-            const uint8_t* rec0 = nullptr;
-            const uint8_t* rec1 = nullptr;
-            const uint8_t* pf_page = nullptr;
-            auto prefetch_dense = [&]() {
-                prefetch(pf_page, nullptr);
-                pf_page = nullptr;
-                if (j_pf < n_local) {
-                    if (lane == 0) pf_page = row_record(cpf, 0);
-                    ++j_pf;
-                    cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-            };
-            // Top-k tiles: a three-stage pipeline in which every load is consumed one iteration
-            // after it is issued: index loads of tile j + 3, page loads of tile j + 2, records of
-            // tile j + 1 (whose rows are then prefetched into L2), run after tile j is issued.
-            Cursor cB = cj, cA = cj;   // the tiles of the page and index stages
-            int jB = 0, jA = 0;
-            int ia0 = -1, ia1 = -1;    // index stage results (raw list entries)
-            int pb0 = -1, pb1 = -1, gb0 = 0, gb1 = 0;   // page stage results: positions, pages
-            auto stage_a = [&]() {
-                ia0 = ia1 = -1;
-                if (jA < n_local) {
-                    const int e0 = cA.t * kT + lane, e1 = e0 + 32;
-                    const size_t base = (size_t)cA.b * p.topk;
-                    ia0 = e0 < p.topk ? __ldg(p.topk_idx + base + e0) : -1;
-                    ia1 = e1 < p.topk ? __ldg(p.topk_idx + base + e1) : -1;
-                }
-            };
-            auto stage_b = [&]() {   // consumes the index stage of the same tile, then advances it
-                pb0 = pb1 = -1;
-                if (jB < n_local) {
-                    pb0 = ia0 >= 0 && ia0 < cB.n ? ia0 : -1;
-                    pb1 = ia1 >= 0 && ia1 < cB.n ? ia1 : -1;
-                    gb0 = page_of(cB, pb0);
-                    gb1 = page_of(cB, pb1);
-                    ++jB;
-                    cB.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-                if (jA < n_local) {
-                    ++jA;
-                    cA.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
-                }
-                stage_a();
-            };
-            auto lookups_topk = [&](bool load_next) {   // records of the tile the page stage holds
-                rec0 = load_next ? record_at(pb0, gb0) : nullptr;
-                rec1 = load_next ? record_at(pb1, gb1) : nullptr;
-                prefetch(rec0, rec1);
-                stage_b();
-            };
-            if (dense) {
-                for (int k = 0; k < kPfAhead; ++k) prefetch_dense();
-                rec0 = row_record(cj, lane);
-                rec1 = row_record(cj, lane + 32);
-            } else {
-                stage_a();    // tile 0
-                stage_b();    // tile 0 pages, tile 1 indices
-                lookups_topk(true);
-            }
-            int issued = 0;
-            for (int j = 0; j < n_local; ++j) {
-                if (dense) prefetch_dense();
-                const int slot = j % kNC;
-                const uint32_t m0 = __ballot_sync(0xffffffffu, rec0 != nullptr);
-                const uint32_t m1 = __ballot_sync(0xffffffffu, rec1 != nullptr);
+            cu.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+            int seg = 0;
+            for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+                if (!cu.first()) continue;
                 bool ok = !s_abort;
-                if (ok && j >= kNC) ok = mbar_wait(bars.ce(slot), ((j / kNC) - 1) & 1, wait_limit);
+                if (ok && seg > 0) ok = mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
-                    if (lane == 0) fail(p.ctl, &s_abort, 20);
+                    if (lane == 0) fail(p.ctl, &s_abort, 1);
                     break;
                 }
-                const uint32_t dst = sbase + kOffConv + slot * kConvBytes;
-                const uint32_t dst_rope = dst + 4 * kKvLatChunk;
-                const uint32_t dst_scl = sbase + kOffScale + slot * kScaleBytes;
-                const uint32_t bar = bars.rf(slot);
                 if (lane == 0) {
-                    uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * slot;
-                    mk[0] = m0;
-                    mk[1] = m1;
-                    if (dense && (m0 & 1u)) {   // row 0 of a dense tile is visible unless its page is not
-                        const int y = (int)((rec0 - p.pool) / rec_bytes);
-                        if (kFp8) {
-                            mbar_arrive_expect_tx(bar, kRawTileBytes);
-                            tma_load_2d(dst, &tm_codes, bar, kHalfLat * (int)r, y);
-                            tma_load_2d(dst_rope, &tm_krope, bar, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
-                            tma_load_2d(dst_scl, &tm_scl, bar, kFp8ScaleOff, y);
-                        } else if (kV4) {
-                            // codes [64 x 256 B] of this half (CTA 1: dims 448.. read as zeros), CTA 1's
-                            // RoPE dims straight into their swizzled operand chunk, the page's scale bytes
-                            const int z = y / kPage;
-                            mbar_arrive_expect_tx(bar, kT * kHalfLat + (r == 1 ? kT * 128 : 0) + kT * 8);
-                            tma_load_3d(dst, &tm_codes, bar, kHalfLat * (int)r, 0, z);
-                            if (r == 1) tma_load_3d(dst + 3 * kKvLatChunk, &tm_krope, bar, 0, 0, z);
-                            bulk_load(dst_scl, p.pool + (size_t)z * kV4PageBytes + kV4ScaleOff, kT * 8, bar);
-                        } else {
-                            mbar_arrive_expect_tx(bar, kT * 128 + kT * 16);
-                            tma_load_2d(dst, &tm_codes, bar, 128 * (int)r, y);
-                            tma_load_2d(dst_scl, &tm_scl, bar, kV41ScaleOff + 16 * (int)r, y);
+                    const int qrow = cu.b * kHeads;
+                    mbar_arrive_expect_tx(bars.q_full, kShared ? 4 * kQLatChunk : kQBytes);
+                    for (int k = 0; k < 4; ++k)
+                        tma_load_2d(sbase + kOffQ + k * kQLatChunk, &tm_qlat, bars.q_full,
+                                    (int)r * kHalfLat + 64 * k, qrow);
+                    if (!kShared) tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full, seg & 1, wait_limit));
+                if (!ok) {
+                    if (lane == 0) fail(p.ctl, &s_abort, 19);
+                    break;
+                }
+                if (kFp8) {
+                    // an element that overflows f16 (|q| >= 65520) is outside this path's range
+                    uint32_t inf = 0;
+    #pragma unroll 8
+                    for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
+                        uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
+                        const uint4 v = *q;
+                        const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                                   bf16x2_to_f16x2(v.w));
+                        inf |= f16x2_inf_or_nan(f.x) | f16x2_inf_or_nan(f.y) | f16x2_inf_or_nan(f.z) |
+                               f16x2_inf_or_nan(f.w);
+                        *q = f;
+                    }
+                    fence_proxy_async_smem();
+                    if (__any_sync(0xffffffffu, inf != 0) && lane == 0) record_error(p.ctl, MLA_ERR_RANGE, cu.b);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.q_ready);
+                ++seg;
+            }
+            // drain: the last Q load lands before this CTA may exit
+            if (lane == 0 && seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
+            __syncwarp();
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------ MMA issuer
+            // The whole warp runs this loop so that its operands stay warp-uniform; one elected lane
+            // issues each MMA and commit.  QK of a tile: 8 MMAs per latent group into that group's
+            // accumulator (f16 operands for FP8 records), 2 rope MMAs (bf16); PV: per group, 4 MMAs
+            // of 128x128x16 with P times the group's scales from tensor memory.  One score set and
+            // one P set in tensor memory: QK of tile i + 1 follows the softmax's reads of tile i's
+            // scores, P of tile i + 1 follows PV of tile i.
+            if (n_local > 0) {
+                constexpr uint32_t id_qk = kFp8 ? idesc_f16(128, kT, 0, 0) : idesc_bf16(128, kT, 0, 0);
+                constexpr uint32_t id_qr = idesc_bf16(128, kT, 0, 0);
+                constexpr uint32_t id_pv = kFp8 ? idesc_f16(128, 128, 0, 1) : idesc_bf16(128, 128, 0, 1);
+                const uint64_t lat_hi = smem_desc(0, 16, 1024, kSw128) & 0xFFFFFFFF00000000ull;
+                const uint64_t rope_hi = smem_desc(0, 16, 512, kSw64) & 0xFFFFFFFF00000000ull;
+                const uint64_t v_hi = smem_desc(0, kKvLatChunk, 1024, kSw128) & 0xFFFFFFFF00000000ull;
+                const uint32_t lat_lo = (uint32_t)smem_desc(0, 16, 1024, kSw128);
+                const uint32_t rope_lo = (uint32_t)smem_desc(0, 16, 512, kSw64);
+                const uint32_t v_lo = (uint32_t)smem_desc(0, kKvLatChunk, 1024, kSw128);
+                const uint32_t ql_lo = lat_lo + (((sbase + kOffQ) >> 4) & 0x3FFF);
+                const uint32_t qr_lo = rope_lo + (((sbase + kOffQRope) >> 4) & 0x3FFF);
+                Cursor cq, cp;
+                cq.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+                cp = cq;
+                int iq = 0, ip = 0, seg_q = 0, seg_p = 0;
+                uint32_t polls = 0;
+                while (ip < n_local && !__any_sync(0xffffffffu, s_abort)) {
+                    if (iq < n_local && iq <= ip + kSB) {   // QK up to kSB tiles ahead of PV (its score buffers)
+                        const int s = iq % kNC;
+                        const int sb = iq % kSB;
+                        const bool ready = __shfl_sync(
+                            0xffffffffu,
+                            (!cq.first() || mbar_test(bars.q_ready, seg_q & 1)) &&
+                                mbar_test(bars.cf(s), (iq / kNC) & 1) &&
+                                mbar_test(bars.se(sb), ((iq / kSB) & 1) ^ 1),
+                            0);
+                        if (ready) {
+                            tc_fence_after();
+                            const uint32_t st_lo = ((sbase + kOffConv + s * kConvBytes) >> 4) & 0x3FFF;
+                            if (elect_one()) {
+                                // FP8 records: one accumulator per scale group and one for the rope
+                                // dims; otherwise everything into score buffer sb
+                                const uint32_t sacc = tmem + kTmemS + 64 * sb;
+    #pragma unroll
+                                for (int k = 0; k < 4; ++k)
+    #pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        mma_bf16_ss(kFp8 ? tmem + (k < 2 ? kTmemSa : kTmemSb) : sacc,
+                                                    lat_hi | (ql_lo + ((k * kQLatChunk + kk * 32) >> 4)),
+                                                    lat_hi | (st_lo + lat_lo + ((k * kKvLatChunk + kk * 32) >> 4)),
+                                                    id_qk, (kFp8 ? ((k & 1) | kk) : (k | kk)) != 0 ? 1u : 0u);
+                                if (!kShared) {
+    #pragma unroll
+                                    for (int kk = 0; kk < 2; ++kk)
+                                        mma_bf16_ss(kFp8 ? tmem + kTmemSr : sacc, rope_hi | (qr_lo + kk * 2),
+                                                    rope_hi | (st_lo + rope_lo + ((4 * kKvLatChunk + kk * 32) >> 4)),
+                                                    id_qr, (kFp8 && kk == 0) ? 0u : 1u);
+                                }
+                                mma_commit(bars.sf(sb));
+                                if (cq.last()) mma_commit(bars.q_empty);
+                            }
+                            __syncwarp();
+                            if (cq.last()) ++seg_q;
+                            cq.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                            ++iq;
+                            polls = 0;
+                            continue;
+                        }
+                    }
+                    const bool seg_first = cp.first();
+                    const bool pv_ready = __shfl_sync(
+                        0xffffffffu,
+                        (!seg_first || seg_p == 0 || mbar_test(bars.o_free, (seg_p - 1) & 1)) &&
+                            mbar_test(bars.pf(ip % kSB), (ip / kSB) & 1),
+                        0);
+                    if (!pv_ready) {
+                        if (++polls > wait_limit) {
+                            if (lane == 0) fail(p.ctl, &s_abort, 6);
+                            break;
+                        }
+                        continue;
+                    }
+                    polls = 0;
+                    tc_fence_after();
+                    const uint32_t v = ((sbase + kOffConv + (ip % kNC) * kConvBytes) >> 4) & 0x3FFF;
+                    if (elect_one()) {
+    #pragma unroll
+                        for (int g = 0; g < 2; ++g)
+    #pragma unroll
+                            for (int kk = 0; kk < kT / 16; ++kk) {
+                                const uint64_t vd = v_hi | (v + v_lo + ((2 * g * kKvLatChunk + kk * 16 * 128) >> 4));
+                                mma_bf16_ts(tmem + kTmemO + 128 * g,
+                                            tmem + (kFp8 ? (g == 0 ? kTmemPa : kTmemPb) : kTmemP + 32 * (ip % kSB)) + 8 * kk,
+                                            vd, id_pv, (!seg_first || kk > 0) ? 1u : 0u);
+                            }
+                        mma_commit(bars.pe(ip % kSB));
+                        mma_commit(bars.ce(ip % kNC));
+                        if (cp.last()) mma_commit(bars.o_full);
+                    }
+                    __syncwarp();
+                    if (cp.last()) ++seg_p;
+                    cp.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                    ++ip;
+                }
+            }
+            __syncwarp();
+        } else if (warp == kProducerWarp) {
+            // ------------------------------------------------------------------ FP8 tile loads
+            // Tile j's raw bytes into conversion slot j % kNC once PV of tile j - kNC has released it,
+            // with the mask of valid rows (written before the arrival the agents wait on).  A dense
+            // tile is one page: three TMA boxes of its 64 rows (rows past the request's end are
+            // loaded and then zeroed by the agents).  A top-k tile: each lane copies its two rows with
+            // 16-byte cp.async (21 pieces per row: 16 of codes, the scales, 4 of rope) and arrives
+            // once they have landed.  Pages: the next tile's rows are looked up after a tile is
+            // issued, and the page kPfAhead tiles ahead is prefetched into L2.  Top-k rows: index
+            // loads, page loads and records run as a three-stage pipeline (see below), and each
+            // tile's rows are prefetched into L2 one tile ahead of their copies.
+            if (kRaw && n_local > 0) {
+                constexpr int kPfAhead = 3;
+                constexpr bool dense = !kTopk;
+                if (dense && lane == 0) {
+                    tma_prefetch_desc(&tm_codes);
+                    tma_prefetch_desc(&tm_krope);
+                    tma_prefetch_desc(&tm_scl);
+                }
+                Cursor cj, cpf;   // the next tile to load, and (dense) the next tile to prefetch into L2
+                cj.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+                cpf = cj;
+                int j_pf = 0;
+                // L2 prefetch of the rows of the records given (dense: lane 0 holds the page's row 0)
+                auto prefetch = [&](const uint8_t* f0, const uint8_t* f1) {
+                    if (dense) {
+                        if (f0) {
+                            const int y = (int)((f0 - p.pool) / rec_bytes);   // slot of the page's row 0
+                            if (kFp8) {
+                                tma_prefetch_l2_2d(&tm_codes, kHalfLat * (int)r, y);
+                                tma_prefetch_l2_2d(&tm_krope, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
+                                tma_prefetch_l2_2d(&tm_scl, kFp8ScaleOff, y);
+                            } else if (kV4) {
+                                tma_prefetch_l2_3d(&tm_codes, kHalfLat * (int)r, 0, y / kPage);
+                                if (r == 1) tma_prefetch_l2_3d(&tm_krope, 0, 0, y / kPage);
+                                prefetch_l2(p.pool + (size_t)(y / kPage) * kV4PageBytes + kV4ScaleOff, kPage * 8);
+                            } else {
+                                tma_prefetch_l2_2d(&tm_codes, 128 * (int)r, y);
+                                tma_prefetch_l2_2d(&tm_scl, kV41ScaleOff + 16 * (int)r, y);
+                            }
                         }
                     } else {
-                        mbar_arrive(bar);
+                        // the lines of the row's codes half and of its scales and rope
+                        const uint8_t* pq[2] = {f0, f1};
+    #pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            if (pq[q]) {
+                                if (kFp8) {
+                                    prefetch_line_l2(pq[q] + kHalfLat * (int)r);
+                                    prefetch_line_l2(pq[q] + kHalfLat * (int)r + 128);
+                                    prefetch_line_l2(pq[q] + kFp8ScaleOff);
+                                    prefetch_line_l2(pq[q] + kFp8RecordBytes - 16);
+                                } else if (kV4) {
+                                    const size_t sl = (size_t)(pq[q] - p.pool) / kV4EntryBytes;
+                                    const uint8_t* base = p.pool + (sl / kPage) * kV4PageBytes;
+                                    const int row = (int)(sl % kPage);
+                                    prefetch_l2(base + row * kENope + kHalfLat * (int)r, r == 0 ? 256 : 192);
+                                    if (r == 1) prefetch_l2(base + kV4RopeOff + row * 128, 128);
+                                    prefetch_line_l2(base + kV4ScaleOff + row * 8);
+                                } else {
+                                    prefetch_l2(pq[q] + 128 * (int)r, 128);
+                                    prefetch_line_l2(pq[q] + kV41ScaleOff + 16 * (int)r);
+                                }
+                            }
                     }
+                };
+                // Dense tiles: at the start of each iteration the page of tile j_pf (looked up by lane 0
+                // the iteration before) is prefetched and the page of the next tile to prefetch looked
+                // up; after a tile is issued, rows lane, lane + 32 of the next one are looked up.
+                const uint8_t* rec0 = nullptr;
+                const uint8_t* rec1 = nullptr;
+                const uint8_t* pf_page = nullptr;
+                auto prefetch_dense = [&]() {
+                    prefetch(pf_page, nullptr);
+                    pf_page = nullptr;
+                    if (j_pf < n_local) {
+                        if (lane == 0) pf_page = row_record(cpf, 0);
+                        ++j_pf;
+                        cpf.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                    }
+                };
+                // Top-k tiles: a three-stage pipeline in which every load is consumed one iteration
+                // after it is issued: index loads of tile j + 3, page loads of tile j + 2, records of
+                // tile j + 1 (whose rows are then prefetched into L2), run after tile j is issued.
+                Cursor cB = cj, cA = cj;   // the tiles of the page and index stages
+                int jB = 0, jA = 0;
+                int ia0 = -1, ia1 = -1;    // index stage results (raw list entries)
+                int pb0 = -1, pb1 = -1, gb0 = 0, gb1 = 0;   // page stage results: positions, pages
+                auto stage_a = [&]() {
+                    ia0 = ia1 = -1;
+                    if (jA < n_local) {
+                        const int e0 = cA.t * kT + lane, e1 = e0 + 32;
+                        const size_t base = (size_t)cA.b * p.topk;
+                        ia0 = e0 < p.topk ? __ldg(p.topk_idx + base + e0) : -1;
+                        ia1 = e1 < p.topk ? __ldg(p.topk_idx + base + e1) : -1;
+                    }
+                };
+                auto stage_b = [&]() {   // consumes the index stage of the same tile, then advances it
+                    pb0 = pb1 = -1;
+                    if (jB < n_local) {
+                        pb0 = ia0 >= 0 && ia0 < cB.n ? ia0 : -1;
+                        pb1 = ia1 >= 0 && ia1 < cB.n ? ia1 : -1;
+                        gb0 = page_of(cB, pb0);
+                        gb1 = page_of(cB, pb1);
+                        ++jB;
+                        cB.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                    }
+                    if (jA < n_local) {
+                        ++jA;
+                        cA.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                    }
+                    stage_a();
+                };
+                auto lookups_topk = [&](bool load_next) {   // records of the tile the page stage holds
+                    rec0 = load_next ? record_at(pb0, gb0) : nullptr;
+                    rec1 = load_next ? record_at(pb1, gb1) : nullptr;
+                    prefetch(rec0, rec1);
+                    stage_b();
+                };
+                if (dense) {
+                    for (int k = 0; k < kPfAhead; ++k) prefetch_dense();
+                    rec0 = row_record(cj, lane);
+                    rec1 = row_record(cj, lane + 32);
+                } else {
+                    stage_a();    // tile 0
+                    stage_b();    // tile 0 pages, tile 1 indices
+                    lookups_topk(true);
                 }
-                if (!dense) {
-                    // each lane copies its row's 16-byte pieces starting at piece `lane`, so that
-                    // the 32 lanes of one copy instruction write different banks
-                    auto copy_row = [&](const uint8_t* rec, int row) {
+                int issued = 0, staged = 0;
+                const uint32_t stage = sbase + kOffStage;
+                constexpr int stage_row = kV41 ? 128 : kHalfLat;   // bytes of a row's codes in the staging buffer
+                for (int j = 0; j < n_local; ++j) {
+                    if (dense) prefetch_dense();
+                    const int slot = j % kNC;
+                    const uint32_t m0 = __ballot_sync(0xffffffffu, rec0 != nullptr);
+                    const uint32_t m1 = __ballot_sync(0xffffffffu, rec1 != nullptr);
+                    // (a) converter instantiations: tile j's codes into the staging buffer once the
+                    // converters have read tile j - 1's, with the mask of valid rows (written before the
+                    // arrival the converters wait on)
+                    bool ok = !s_abort;
+                    if (kConv && ok && j >= 1) ok = mbar_wait(bars.stage_empty, (j - 1) & 1, wait_limit);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) {
+                        if (lane == 0) fail(p.ctl, &s_abort, 20);
+                        break;
+                    }
+                    if (kConv && lane == 0) {
+                        uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * kNC;
+                        mk[0] = m0;
+                        mk[1] = m1;
+                        if (dense) {
+                            if (m0 & 1u) {   // row 0 of a dense tile is visible unless its page is not
+                                const int y = (int)((rec0 - p.pool) / rec_bytes);
+                                mbar_arrive_expect_tx(bars.stage_full, kT * stage_row);
+                                if (kFp8) tma_load_2d(stage, &tm_codes, bars.stage_full, kHalfLat * (int)r, y);
+                                // V4: codes [64 x 256 B] of this half (CTA 1: dims 448.. read as zeros)
+                                else if (kV4) tma_load_3d(stage, &tm_codes, bars.stage_full, kHalfLat * (int)r, 0, y / kPage);
+                                else tma_load_2d(stage, &tm_codes, bars.stage_full, 128 * (int)r, y);
+                            } else {
+                                mbar_arrive(bars.stage_full);
+                            }
+                        }
+                    }
+                    // top-k rows: each lane copies its rows' 16-byte pieces starting at piece `lane`, so
+                    // that the 32 lanes of one copy instruction write different banks
+                    auto copy_codes = [&](const uint8_t* rec, int row) {
                         if (!rec) return;
                         if (kFp8) {
                             const uint8_t* cs = rec + kHalfLat * (int)r;
-#pragma unroll
+    #pragma unroll
                             for (int k = 0; k < kHalfLat / 16; ++k) {
                                 const int q = (k + lane) & (kHalfLat / 16 - 1);
-                                cp_async16(dst + row * kHalfLat + 16 * q, cs + 16 * q);
-                            }
-                            cp_async16(dst_scl + row * 16, rec + kFp8ScaleOff);
-                            const uint8_t* rs = rec + kFp8RopeOff + 2 * kHalfRope * (int)r;
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const int q = (k + lane) & 3;
-                                cp_async16(dst_rope + row * 64 + 16 * q, rs + 16 * q);
+                                cp_async16(stage + row * kHalfLat + 16 * q, cs + 16 * q);
                             }
                         } else if (kV4) {
-                            // codes of this half (CTA 1: its 192) to the raw rows [64][256 B], CTA 1's
-                            // RoPE dims to their swizzled operand chunk, the 8 scale bytes to [64][8]
+                            // codes of this half (CTA 1: its 192; the rest of the row is never read)
                             const size_t sl = (size_t)(rec - p.pool) / kV4EntryBytes;
-                            const uint8_t* base = p.pool + (sl / kPage) * kV4PageBytes;
-                            const int prow = (int)(sl % kPage);
-                            const uint8_t* cs = base + prow * kENope + kHalfLat * (int)r;
+                            const uint8_t* cs = p.pool + (sl / kPage) * kV4PageBytes + (int)(sl % kPage) * kENope + kHalfLat * (int)r;
                             const int pieces = r == 0 ? 16 : 12;
-#pragma unroll
+    #pragma unroll
                             for (int k = 0; k < 16; ++k) {
                                 if (k >= pieces) break;
                                 const int q = (k + lane) % pieces;
-                                cp_async16(dst + row * kHalfLat + 16 * q, cs + 16 * q);
+                                cp_async16(stage + row * kHalfLat + 16 * q, cs + 16 * q);
                             }
-                            if (r == 1) {
-                                const uint8_t* rs = base + kV4RopeOff + prow * 128;
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) {
-                                    const int q = (k + lane) & 7;
-                                    cp_async16(dst + 3 * kKvLatChunk + row * 128 + ((q ^ (row & 7)) << 4), rs + 16 * q);
-                                }
-                            }
-                            cp_async8(dst_scl + row * 8, base + kV4ScaleOff + prow * 8);
                         } else {
                             const uint8_t* cs = rec + 128 * (int)r;
-#pragma unroll
+    #pragma unroll
                             for (int k = 0; k < 8; ++k) {
                                 const int q = (k + lane) & 7;
-                                cp_async16(dst + row * 128 + 16 * q, cs + 16 * q);
+                                cp_async16(stage + row * 128 + 16 * q, cs + 16 * q);
                             }
-                            cp_async16(dst_scl + row * 16, rec + kV41ScaleOff + 16 * (int)r);
                         }
                     };
-                    copy_row(rec0, lane);
-                    copy_row(rec1, lane + 32);
-                    cp_async_arrive_noinc(bar);
+                    if (kConv && !dense) {
+                        copy_codes(rec0, lane);
+                        copy_codes(rec1, lane + 32);
+                        cp_async_arrive_noinc(bars.stage_full);
+                        if (lane == 0) mbar_arrive(bars.stage_full);
+                    }
+                    if (kConv) ++staged;
+                    // (b) the tile's rope (FP8 mixed: straight into its 64-byte-swizzled operand; V4:
+                    // CTA 1's RoPE dims into operand chunk 3) and scales into slot j % kNC once PV of tile
+                    // j - kNC has released it; FP8 pages (converted in place) also take their codes there,
+                    // and the mask of valid rows
+                    if (ok && j >= kNC) ok = mbar_wait(bars.ce(slot), ((j / kNC) - 1) & 1, wait_limit);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) {
+                        if (lane == 0) fail(p.ctl, &s_abort, 21);
+                        break;
+                    }
+                    const uint32_t dst = sbase + kOffConv + slot * kConvBytes;
+                    const uint32_t dst_rope = dst + 4 * kKvLatChunk;
+                    const uint32_t dst_scl = sbase + kOffScale + slot * kScaleBytes;
+                    const uint32_t bar = bars.rf(slot);
+                    if (dense && lane == 0) {
+                        if (!kConv) {
+                            uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * slot;
+                            mk[0] = m0;
+                            mk[1] = m1;
+                        }
+                        if (m0 & 1u) {
+                            const int y = (int)((rec0 - p.pool) / rec_bytes);
+                            if (kFp8) {
+                                mbar_arrive_expect_tx(bar, kT * ((kConv ? 0 : kHalfLat) + 2 * kHalfRope + 16));
+                                if (!kConv) tma_load_2d(dst, &tm_codes, bar, kHalfLat * (int)r, y);
+                                tma_load_2d(dst_rope, &tm_krope, bar, kFp8RopeOff + 2 * kHalfRope * (int)r, y);
+                                tma_load_2d(dst_scl, &tm_scl, bar, kFp8ScaleOff, y);
+                            } else if (kV4) {
+                                const int z = y / kPage;
+                                mbar_arrive_expect_tx(bar, (r == 1 ? kT * 128 : 0) + kT * 8);
+                                if (r == 1) tma_load_3d(dst + 3 * kKvLatChunk, &tm_krope, bar, 0, 0, z);
+                                bulk_load(dst_scl, p.pool + (size_t)z * kV4PageBytes + kV4ScaleOff, kT * 8, bar);
+                            } else {
+                                mbar_arrive_expect_tx(bar, kT * 16);
+                                tma_load_2d(dst_scl, &tm_scl, bar, kV41ScaleOff + 16 * (int)r, y);
+                            }
+                        } else {
+                            mbar_arrive(bar);
+                        }
+                    }
+                    if (!dense) {
+                        auto copy_side = [&](const uint8_t* rec, int row) {
+                            if (!rec) return;
+                            if (kFp8) {
+                                cp_async16(dst_scl + row * 16, rec + kFp8ScaleOff);
+                                const uint8_t* rs = rec + kFp8RopeOff + 2 * kHalfRope * (int)r;
+    #pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const int q = (k + lane) & 3;
+                                    cp_async16(dst_rope + row * 64 + ((q ^ ((row >> 1) & 3)) << 4), rs + 16 * q);
+                                }
+                            } else if (kV4) {
+                                const size_t sl = (size_t)(rec - p.pool) / kV4EntryBytes;
+                                const uint8_t* base = p.pool + (sl / kPage) * kV4PageBytes;
+                                const int prow = (int)(sl % kPage);
+                                if (r == 1) {
+                                    const uint8_t* rs = base + kV4RopeOff + prow * 128;
+    #pragma unroll
+                                    for (int k = 0; k < 8; ++k) {
+                                        const int q = (k + lane) & 7;
+                                        cp_async16(dst + 3 * kKvLatChunk + row * 128 + ((q ^ (row & 7)) << 4), rs + 16 * q);
+                                    }
+                                }
+                                cp_async8(dst_scl + row * 8, base + kV4ScaleOff + prow * 8);
+                            } else {
+                                cp_async16(dst_scl + row * 16, rec + kV41ScaleOff + 16 * (int)r);
+                            }
+                        };
+                        copy_side(rec0, lane);
+                        copy_side(rec1, lane + 32);
+                        cp_async_arrive_noinc(bar);
+                    }
+                    __syncwarp();
+                    ++issued;
+                    cj.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                    if (dense) {
+                        rec0 = rec1 = nullptr;
+                        if (j + 1 < n_local) {
+                            rec0 = row_record(cj, lane);
+                            rec1 = row_record(cj, lane + 32);
+                        }
+                    } else {
+                        lookups_topk(j + 1 < n_local);
+                    }
                 }
-                __syncwarp();
-                ++issued;
-                cj.next(p.seq_lens, p.max_seq_len, p.B, p.topk);
+                // drain: the copies of the last tiles (one per slot, and the staging buffer's) land
+                // before this CTA may exit
                 if (dense) {
-                    rec0 = rec1 = nullptr;
-                    if (j + 1 < n_local) {
-                        rec0 = row_record(cj, lane);
-                        rec1 = row_record(cj, lane + 32);
+                    if (lane == 0) {
+                        for (int j = issued - 1; j >= 0 && j >= issued - kNC; --j)
+                            mbar_wait(bars.rf(j % kNC), (j / kNC) & 1, kDrainLimit);
+                        if (staged > 0) mbar_wait(bars.stage_full, (staged - 1) & 1, kDrainLimit);
                     }
                 } else {
-                    lookups_topk(j + 1 < n_local);
+                    cp_async_wait_all();
                 }
             }
-            // drain: the copies of the last tiles (one per slot) land before this CTA may exit
-            if (dense) {
-                if (lane == 0)
-                    for (int j = issued - 1; j >= 0 && j >= issued - kNC; --j)
-                        mbar_wait(bars.rf(j % kNC), (j / kNC) & 1, kDrainLimit);
-            } else {
-                cp_async_wait_all();
+            __syncwarp();
+        }
+        __syncwarp();
+        if constexpr (kConv) reg_alloc<kRegsLaunch>();
+    } else if (warp >= kConvWarp0) {
+        // ------------------------------------------------------------------ converters
+        // Tile j: once its codes have landed in the staging buffer, PV of tile j - kNC has freed
+        // slot j % kNC and the slot's rope and scales have landed, each 16-byte piece of codes is
+        // read and written converted into the MMA operand layout: latent chunks [64 rows x 64 dims]
+        // (128-byte swizzle), zeros for rows outside the request; the staging buffer is then
+        // released for tile j + 1.  FP8 mixed: E4M3 to f16 (exact); V4: E4M3 times 2^(UE8M0 - 127)
+        // to bf16 (exact), CTA 1's RoPE dims already in place (zeroed for rows outside); V4.1: E2M1
+        // times the E4M3 scale of its 16 dims to bf16 (exact).
+        if constexpr (kConv) {
+            reg_dealloc<kRegsConv>();
+            named_bar_sync(kBarRegs, gather_threads(kFmt, kTopk));
+        }
+        if (kConv && n_local > 0) {
+            const int ct = tid - kConvWarp0 * 32;   // 0 .. 127
+            Cursor cc;
+            cc.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
+            for (int j = 0; j < n_local; ++j, cc.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+                const int slot = j % kNC;
+                bool ok = !s_abort && mbar_wait(bars.stage_full, j & 1, wait_limit);
+                ok = ok && (j < kNC || mbar_wait(bars.ce(slot), ((j / kNC) - 1) & 1, wait_limit));
+                ok = ok && mbar_wait(bars.rf(slot), (j / kNC) & 1, wait_limit);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) fail(p.ctl, &s_abort, 22);
+                    break;
+                }
+                const uint32_t* smk = reinterpret_cast<const uint32_t*>(sm + kOffMask) + 2 * kNC;
+                const uint32_t mk0 = smk[0], mk1 = smk[1];
+                auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
+                uint8_t* lat = sm + kOffConv + slot * kConvBytes;
+                const uint8_t* scl = sm + kOffScale + slot * kScaleBytes;
+                const uint8_t* stg = sm + kOffStage;
+                // piece e = ct + 128 k: FP8 mixed and V4 [64 rows][16 x 16 B] (row e >> 4, dims 16 ch ..
+                // 16 ch + 15 of this half, ch = e & 15 = ct & 15); V4.1 [64 rows][8 x 16 B] (row e >> 3,
+                // dims 32 ch .. 32 ch + 31, ch = ct & 7)
+                if (!kV41) {
+                    const int ch = ct & 15;
+                    const bool rope_piece = kV4 && r == 1 && ch >= 12;   // V4, CTA 1: dims 448 .. 511
+                    const int s0 = 2 * (ch & 3);
+#pragma unroll 2
+                    for (int k = 0; k < 8; ++k) {
+                        const int row = (ct + 128 * k) >> 4;
+                        uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
+                        if (rope_piece && valid(row)) continue;
+                        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if (valid(row) && !rope_piece) {
+                            const uint4 raw = *reinterpret_cast<const uint4*>(stg + (ct + 128 * k) * 16);
+                            if (kFp8) {
+                                e4m3x16_to_f16(raw, o);
+                            } else {
+                                const uint32_t byte = scl[row * 8 + 4 * (int)r + (ch >> 2)];
+                                e4m3x16_scaled_bf16(raw, __uint_as_float(byte ? byte << 23 : 0x00400000u), o);   // 2^(byte - 127)
+                            }
+                        }
+                        st_shared_v4(dst + ((s0 ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        st_shared_v4(dst + (((s0 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
+                    }
+                } else {
+                    const int ch = ct & 7;
+#pragma unroll 1
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = (ct + 128 * k) >> 3;
+                        uint32_t o[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) o[t] = 0;
+                        if (valid(row))
+                            e2m1x32_scaled_bf16(*reinterpret_cast<const uint4*>(stg + (ct + 128 * k) * 16),
+                                                e4m3_to_float(scl[row * 16 + 2 * ch]),
+                                                e4m3_to_float(scl[row * 16 + 2 * ch + 1]), o);
+                        uint8_t* dst = lat + (ch >> 1) * kKvLatChunk + row * 128;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int part = 4 * (ch & 1) + q;
+                            st_shared_v4(dst + ((part ^ (row & 7)) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        }
+                    }
+                }
+                // every piece of the staging buffer read: it may take tile j + 1
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.stage_empty);
+                if (kFp8 && ct < kT) {
+                    // scales of rows outside the request: zero (their P is zero); a visible row whose
+                    // group scale is above 255 (or not finite) would overflow f16(P s_g)
+                    uint4* sc = reinterpret_cast<uint4*>(sm + kOffScale + slot * kScaleBytes + ct * 16);
+                    if (!valid(ct)) {
+                        *sc = make_uint4(0, 0, 0, 0);
+                    } else {
+                        const uint4 q = *sc;   // (a NaN fails every comparison)
+                        if (!(__uint_as_float(q.x) <= kMaxGroupScale) || !(__uint_as_float(q.y) <= kMaxGroupScale) ||
+                            !(__uint_as_float(q.z) <= kMaxGroupScale) || !(__uint_as_float(q.w) <= kMaxGroupScale))
+                            record_error(p.ctl, MLA_ERR_RANGE, cc.b);
+                    }
+                }
+                if (ct == 0) {
+                    uint32_t* mk = reinterpret_cast<uint32_t*>(sm + kOffMask) + 2 * slot;
+                    mk[0] = mk0;
+                    mk[1] = mk1;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.cf(slot));
             }
         }
         __syncwarp();
+        if constexpr (kConv) reg_alloc<kRegsLaunch>();
     } else {
         // ------------------------------------------------------------------ owners and agents
         // Lane group lg = warp % 4 (the TMEM lanes this warp may access: heads 32 lg .. 32 lg + 31,
-        // thread = head), slice ts = (warp - 2) / 4 (positions 16 ts .. 16 ts + 15 of a tile, and
+        // thread = head), slice ts = (warp - 4) / 4 (positions 16 ts .. 16 ts + 15 of a tile, and
         // O columns 64 ts .. 64 ts + 63 in corrections and epilogues).  Lane groups 2r, 2r + 1
         // hold the owned heads.
         //
@@ -735,8 +937,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // threads), which cannot time out, so these loops never leave early: after a failed
         // (bounded) wait they keep executing every barrier but skip the work, and waits return at
         // once.  Wait results are made warp-uniform before any warp-collective tcgen05 instruction.
+        if constexpr (kConv) {
+            reg_alloc<kRegsSoftmax>();
+            named_bar_sync(kBarRegs, gather_threads(kFmt, kTopk));
+        }
         const int lg = warp & 3;
-        const int ts = (warp - 2) >> 2;
+        const int ts = (warp - kSoftWarp0) >> 2;
         const int h = lg * 32 + lane;
         const bool owner = (lg >> 1) == (int)r;
         const int hh = h & (kOwned - 1);   // index among the owning CTA's heads
@@ -897,29 +1103,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int seg = 0;
         bool cut_front = false;
 
-        // Tile preparation (called by the agents): thread `at` of the 256 agent threads.
+        // Tile preparation by the agents (converter instantiations have their tiles prepared by the
+        // converter warps): thread `at` of the 256 agent threads puts tile j (cursor cj) into
+        // conversion slot j % kNC, this CTA's half of every row in the MMA layouts with zeros for
+        // rows outside the request: FP8 pages converted in place from the raw bytes the producer
+        // warp loaded there; bf16 top-k rows loaded from global memory once PV of tile j - kNC has
+        // freed the slot, with the mask of valid rows.
         const int at = ((lg & 1) * 4 + ts) * 32 + lane;
-        // Tile j (cursor cj) into conversion slot j % kNC: this CTA's half of every row in the
-        // MMA layouts, zeros for rows outside the request.  FP8 records: the producer warp has
-        // put the raw bytes into the slot (codes [64][256] at its start, rope [64][64 B] in its
-        // rope region, scales [64][16 B], the mask of valid rows); each agent thread reads its
-        // 16-byte pieces, all agents meet, and each writes its pieces converted.  bf16 records:
-        // the rows are loaded from global memory once PV of tile j - kNC has freed the slot.
         auto prepare = [&](int j, const Cursor& cj) {
             const int slot = j % kNC;
             uint8_t* lat = sm + kOffConv + slot * kConvBytes;
             uint8_t* rope = lat + 4 * kKvLatChunk;
             const uint4 zero = make_uint4(0, 0, 0, 0);
-            if (kFp8) {
+            if (kFp8 && !kConv) {
+                // FP8 pages: the producer warp has put the raw codes [64][256] at the slot's start
+                // (the rope dims, already in their operand layout, the scales and the mask of valid
+                // rows beside them); each agent thread reads its 16-byte pieces, all agents meet, and
+                // each writes its pieces converted (zeros for rows outside the request)
                 const bool ok = wwait(bars.rf(slot), (j / kNC) & 1, 17);
                 const uint32_t* mk = reinterpret_cast<const uint32_t*>(sm + kOffMask) + 2 * slot;
                 const uint32_t mk0 = mk[0], mk1 = mk[1];
                 auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
-                uint4 raw[4], rraw = zero;
+                uint4 raw[4];
                 if (ok) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) raw[k] = *reinterpret_cast<const uint4*>(lat + (at + 256 * k) * 16);
-                    rraw = *reinterpret_cast<const uint4*>(rope + at * 16);
                 }
                 named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
                 if (ok) {
@@ -929,17 +1137,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int e = at + 256 * k, row = e >> 4, ch = e & 15;
                         uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                         if (valid(row)) e4m3x16_to_f16(raw[k], o);
-                        // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte
-                        // parts 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
+                        // dims 16 ch .. 16 ch + 15 of this half: 64-dim chunk ch / 4, 16-byte parts
+                        // 2 (ch % 4) and 2 (ch % 4) + 1 of the row, 128-byte swizzle
                         uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
                         const int s0 = 2 * (ch & 3);
                         st_shared_v4(dst + ((s0 ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
                         st_shared_v4(dst + (((s0 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
                     }
-                    // rope: 64 rows x 4 chunks of 8 dims, 64-byte swizzle
-                    const int row = at >> 2, c4 = at & 3;
-                    if (!valid(row)) rraw = zero;
-                    st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
                     // scales of rows outside the request: zero (their P is zero); a visible row
                     // whose group scale is above 255 (or not finite) would overflow f16(P s_g)
                     if (at < kT) {
@@ -954,87 +1158,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-            } else if (kShared) {
-                // Shared K = V entries: the slot holds this CTA's raw codes (V4: [64][256 B], CTA 1's
-                // RoPE dims already in operand chunk 3; V4.1: [64][128 B]) and the rows' scale bytes
-                // (V4: [64][8], V4.1: [64][16]).  Every code converts exactly to bf16 as its value
-                // times its group's scale.  Each thread reads its raw pieces and scales, the eight
-                // agent warps meet, then each writes its pieces converted (zeros for rows outside the
-                // request).
-                const bool ok = wwait(bars.rf(slot), (j / kNC) & 1, 17);
-                const uint32_t* mk = reinterpret_cast<const uint32_t*>(sm + kOffMask) + 2 * slot;
-                const uint32_t mk0 = mk[0], mk1 = mk[1];
-                auto valid = [&](int row) -> bool { return ((row < 32 ? mk0 : mk1) >> (row & 31)) & 1u; };
-                const uint8_t* scl = sm + kOffScale + slot * kScaleBytes;
-                if (kV4) {
-                    // pieces e = at + 256 k of [64 rows][16 x 16 B]: row e >> 4, dims 16 ch .. 16 ch + 15
-                    // of this half with ch = at & 15 for every k; on CTA 1 ch >= 12 is RoPE (in place)
-                    const int ch = at & 15;
-                    const bool rope_piece = r == 1 && ch >= 12;
-                    uint4 raw[4];
-                    float sc[4];
-                    if (ok && !rope_piece) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int e = at + 256 * k, row = e >> 4;
-                            raw[k] = *reinterpret_cast<const uint4*>(lat + e * 16);
-                            const uint32_t byte = scl[row * 8 + 4 * (int)r + (ch >> 2)];
-                            sc[k] = __uint_as_float(byte ? byte << 23 : 0x00400000u);   // 2^(byte - 127)
-                        }
-                    }
-                    named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
-                    if (ok) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int e = at + 256 * k, row = e >> 4;
-                            uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
-                            const int s0 = 2 * (ch & 3);
-                            if (rope_piece && valid(row)) continue;
-                            uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                            if (!rope_piece && valid(row)) e4m3x16_scaled_bf16(raw[k], sc[k], o);
-                            st_shared_v4(dst + ((s0 ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
-                            st_shared_v4(dst + (((s0 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
-                        }
-                    }
-                } else {
-                    // pieces e = at + 256 k (k < 2) of [64 rows][8 x 16 B]: row e >> 3, dims 32 ch .. 32 ch
-                    // + 31 of this half with ch = at & 7, two scale groups of 16
-                    const int ch = at & 7;
-                    uint4 raw[2];
-                    float sc[2][2];
-                    if (ok) {
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int e = at + 256 * k, row = e >> 3;
-                            raw[k] = *reinterpret_cast<const uint4*>(lat + e * 16);
-                            sc[k][0] = e4m3_to_float(scl[row * 16 + 2 * ch]);
-                            sc[k][1] = e4m3_to_float(scl[row * 16 + 2 * ch + 1]);
-                        }
-                    }
-                    named_bar_sync(kBarAgents, kSoftmaxThreads / 2);   // every raw piece read
-                    if (ok) {
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int e = at + 256 * k, row = e >> 3;
-                            uint32_t o[16];
-#pragma unroll
-                            for (int t = 0; t < 16; ++t) o[t] = 0;
-                            if (valid(row)) e2m1x32_scaled_bf16(raw[k], sc[k][0], sc[k][1], o);
-                            uint8_t* dst = lat + (ch >> 1) * kKvLatChunk + row * 128;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int part = 4 * (ch & 1) + q;
-                                st_shared_v4(dst + ((part ^ (row & 7)) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2],
-                                             o[4 * q + 3]);
-                            }
-                        }
-                    }
-                }
-                // the rows' score and P scales: 1 (the conversion applied the entry's own), 0 outside
-                if (ok && at < kT)
-                    reinterpret_cast<float4*>(sm + kOffScale + slot * kScaleBytes)[at] =
-                        valid(at) ? make_float4(1.f, 1.f, 1.f, 1.f) : make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
+            } else if (!kRaw) {
                 // 64 rows x 32 chunks of 8 bf16 dims; this thread copies chunks at + 256 k
                 // (the first half loaded before the wait)
                 const int rope_off = 2 * kDc + 2 * kHalfRope * (int)r;
@@ -1072,8 +1196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     st_shared_v4(rope + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4), rraw.x, rraw.y, rraw.z, rraw.w);
                 }
                 if (at < kT) {
-                    // the row's group scales (1 for bf16 records) and the valid-row mask
-                    reinterpret_cast<float2*>(sm + kOffScale + slot * kScaleBytes)[2 * at + (int)r] = make_float2(1.f, 1.f);
+                    // the valid-row mask
                     const uint32_t m = __ballot_sync(0xffffffffu, srec != nullptr);
                     if (lane == 0) reinterpret_cast<uint32_t*>(sm + kOffMask)[2 * slot + (at >> 5)] = m;
                 }
@@ -1114,6 +1237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!owner) {
             // ------------------------------------------------------------ agents
             const uint32_t x_remote = mapa(sbase + kOffX, peer);
+            const uint32_t x1_remote = mapa(sbase + kOffStage, peer);
             const uint32_t xfull_remote = mapa(bars.x_full, peer);
             const uint32_t pinfree_remote = mapa(bars.pin_free, peer);
             const bool lead = (ts == 0 && lg == 2 * (int)peer && lane == 0);
@@ -1122,21 +1246,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             auto forward = [&](int i) {
                 float v[16];
                 if (!load_s(i, v)) return;
-                const int xb = i & 1;
-                if (!wwait(bars.xe(xb), ((i >> 1) & 1) ^ 1, 8)) return;
+                // buffer i % kNX (converter instantiations have one: the staging buffer takes the
+                // second) once the peer's owners have read the scores it held
+                const int xb = i % kNX;
+                if (!wwait(bars.xe(xb), ((i / kNX) & 1) ^ 1, 8)) return;
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                    st_async_v4(x_remote + xb * kXBytes + ((4 * ts + g) * kOwned + hh) * 16,
-                                xfull_remote + 8 * xb, __float_as_uint(v[4 * g]), __float_as_uint(v[4 * g + 1]),
+                    st_async_v4((xb == 0 ? x_remote : x1_remote) + ((4 * ts + g) * kOwned + hh) * 16, xfull_remote + 8 * xb, __float_as_uint(v[4 * g]), __float_as_uint(v[4 * g + 1]),
                                 __float_as_uint(v[4 * g + 2]), __float_as_uint(v[4 * g + 3]));
             };
 
-            for (int k = 0; k < 4; ++k) prefetch_step();   // tiles 2, 3, 4 prefetched, 5 addressed
-            prepare_until(2);
+            if (!kConv) {
+                for (int k = 0; k < 4; ++k) prefetch_step();   // tiles 2, 3, 4 prefetched, 5 addressed
+                prepare_until(2);
+            }
             if (n_local > 0) forward(0);
-            // Iteration i: the peer's P of tile i into tensor memory (PV of tile i can then go),
-            // then this CTA's scores of tile i + 1 to the peer and tile i + 2 converted.
+            // Iteration i: converter instantiations send this CTA's scores of tile i + 1 to the
+            // peer as soon as QK of tile i + 1 has completed (it does not wait for P of tile i),
+            // then place the peer's P of tile i in tensor memory (PV of tile i can then go).  The
+            // others place P of tile i first, then send the scores of tile i + 1, then prepare tile
+            // i + 2.
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
+                if (kConv && i + 1 < n_local) forward(i + 1);
                 const bool first = cu.first();
                 if (first) cut_front = cu.t > 0;
                 // the peer's P of its heads for tile i, and its rescale factors
@@ -1166,9 +1297,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     epilogue_rows(seg, cu, partial, l_row);
                     ++seg;
                 }
-                if (i + 1 < n_local) forward(i + 1);
-                prepare_until(i + 3);
-                prefetch_step();
+                if (!kConv) {
+                    if (i + 1 < n_local) forward(i + 1);
+                    prepare_until(i + 3);
+                    prefetch_step();
+                }
             }
         } else {
             // ------------------------------------------------------------ owners
@@ -1185,7 +1318,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // (it gives the log-sum-exp); they differ only for bf16 P
             float m_used = -INFINITY, l_part = 0.f, lx_part = 0.f;
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
-                const int xb = i & 1;
                 const bool first = cu.first();
                 if (first) {
                     m_used = -INFINITY;
@@ -1199,10 +1331,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t vmask =
                     (reinterpret_cast<const uint32_t*>(sm + kOffMask)[2 * (i % kNC) + (ts >> 1)] >> (16 * (ts & 1))) & 0xFFFFu;
                 // the peer's partial scores of these heads for tile i
+                const int xb = i % kNX;
                 if (lead && !s_abort) mbar_arrive_expect_tx(bars.xf(xb), kXBytes);
-                const bool xok = wwait(bars.xf(xb), (i >> 1) & 1, 9);
+                const bool xok = wwait(bars.xf(xb), (i / kNX) & 1, 9);
                 float x[16];
-                const uint8_t* xp = sm + kOffX + xb * kXBytes;
+                const uint8_t* xp = sm + (xb == 0 ? kOffX : kOffStage);
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const float4 q = *reinterpret_cast<const float4*>(xp + ((4 * ts + g) * kOwned + hh) * 16);
@@ -1322,6 +1455,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        __syncwarp();
+        if constexpr (kConv) reg_dealloc<kRegsLaunch>();
     }
 
     // ---------------------------------------------------------------------- teardown
@@ -1357,6 +1492,14 @@ cudaError_t launch_gather_instance(const DecodeArgs& a, const DecodePlan& plan, 
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
+        if (gather_conv(kFmt, kTopk)) {
+            // the warpgroups' register split adds up to 80 a thread at launch: a build that launches
+            // with fewer would leave a reg_alloc waiting forever, so it is refused here
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
+        }
         attr_set[dev] = true;
     }
     constexpr bool shared = kFmt == MLA_KV_V4_FP8 || kFmt == MLA_KV_V41_FP4;
@@ -1375,11 +1518,12 @@ cudaError_t launch_gather_instance(const DecodeArgs& a, const DecodePlan& plan, 
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const uint64_t rows = (uint64_t)a.num_pages * kPage;
     if (kFmt == MLA_KV_FP8_MIXED && !kTopk) {
-        // the pool as rows of 656 bytes; a box is 64 rows (one page) of a record's byte range
+        // the pool as rows of 656 bytes; a box is 64 rows (one page) of a record's byte range (the
+        // rope box lands in its operand layout, 64-byte swizzle)
         if (!encode_2d(&tm_codes, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, kHalfLat, kT,
                        CU_TENSOR_MAP_SWIZZLE_NONE, u8) ||
             !encode_2d(&tm_krope, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, 2 * kHalfRope, kT,
-                       CU_TENSOR_MAP_SWIZZLE_NONE, u8) ||
+                       CU_TENSOR_MAP_SWIZZLE_64B, u8) ||
             !encode_2d(&tm_scl, a.pool, kFp8RecordBytes, rows, kFp8RecordBytes, 16, kT,
                        CU_TENSOR_MAP_SWIZZLE_NONE, u8))
             return cudaErrorInvalidValue;
@@ -1427,7 +1571,7 @@ cudaError_t launch_gather_instance(const DecodeArgs& a, const DecodePlan& plan, 
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.sink = shared ? a.sink : nullptr;
     p.rope_cs = shared ? a.rope_cs : nullptr;
-    kernel<<<2 * C, kThreads, kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl, p);
+    kernel<<<2 * C, gather_threads(kFmt, kTopk), kSmemBytes, st>>>(tm_qlat, tm_qrope, tm_codes, tm_krope, tm_scl, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_merge_slots(o_part, lse_part, meta, a.out, a.lse, a.B, C, st, p.sink);
