@@ -71,6 +71,18 @@ namespace {
 using namespace ptx;
 using namespace dc;
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the same instruction):
+// reg_dealloc lowers this warpgroup's registers a thread to N, returning the rest to the CTA's
+// pool; reg_alloc raises them to N, waiting until the pool holds enough.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 constexpr int kSegCost = 1;           // a segment start costs about one tile (schedule units)
 constexpr int kNC = 3;                 // converted tile slots
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents

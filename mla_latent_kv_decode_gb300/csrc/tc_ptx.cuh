@@ -433,18 +433,6 @@ __device__ __forceinline__ void bulk_copy_s2c(uint32_t dst, uint32_t src, uint32
         : "memory");
 }
 
-// Per-warpgroup register budget (all four warps of a warpgroup execute the same instruction):
-// reg_dealloc lowers this warpgroup's registers a thread to N, returning the rest to the CTA's
-// pool; reg_alloc raises them to N, waiting until the pool holds enough.
-template <uint32_t N>
-__device__ __forceinline__ void reg_alloc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void reg_dealloc() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
