@@ -64,13 +64,13 @@ NCU_TRAFFIC = {
     ("a6a81cb6175a2d16", "tiny_dense"): 4_939_008,
     ("a6a81cb6175a2d16", "paged_batch"): 176_497_152,
     ("a6a81cb6175a2d16", "long_context"): 154_273_024,
-    ("7ec042eae824bb42", "fp8_batch"): 1_412_751_232,
-    ("7ec042eae824bb42", "topk_sparse"): 120_461_056,
-    ("7ec042eae824bb42", "v4_batch"): 1_259_511_552,
-    ("7ec042eae824bb42", "v41_batch"): 636_540_672,
+    ("5c8345d9e3722708", "fp8_batch"): 1_412_511_360,
+    ("5c8345d9e3722708", "topk_sparse"): 118_725_248,
+    ("5c8345d9e3722708", "v4_batch"): 1_263_935_232,
+    ("5c8345d9e3722708", "v41_batch"): 641_415_552,
     ("1a7398fbc27d89ce", "indexer_topk"): 1_142_927_360,
-    ("4257ceba335e021a", "value_project"): 197_980_416,
-    ("4257ceba335e021a", "value_project_merged"): 681_876_352,
+    ("46f7feafc1c08056", "value_project"): 224_005_632,
+    ("46f7feafc1c08056", "value_project_merged"): 682_509_184,
 }
 
 
