@@ -638,52 +638,33 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
 constexpr int kKWarps = kKThreads / 32;
 constexpr int kKU = 8;   // loads in flight per thread in the passes over the row
 
-// One warp: the bin of hist[0, nb) holding the krem-th largest key (a larger bin holds larger
-// keys) and how many keys of that bin are still to take (1 <= krem <= the histogram's total).
-__device__ __forceinline__ void select_digit(const uint32_t* hist, int nb, int krem, uint32_t* d_out,
-                                             int* krem_out) {
-    const int lane = threadIdx.x & 31;
-    const int per = nb / 32;   // bins per lane, lane 31 holding the largest
-    int sum = 0;
-    for (int i = 0; i < per; ++i) sum += (int)hist[lane * per + i];
-    int incl = sum;            // keys in this lane's bins and above
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-    }
-    const int above = incl - sum;
-    if (above < krem && krem <= incl) {   // exactly one lane
-        int rem = krem - above;
-        for (int i = per - 1; i >= 0; --i) {
-            const int c = (int)hist[lane * per + i];
-            if (c >= rem) {
-                *d_out = (uint32_t)(lane * per + i);
-                *krem_out = rem;
-                break;
-            }
-            rem -= c;
-        }
-    }
-}
-
 // One request per cluster of two CTAs; CTA q holds positions [q h, min(n, (q + 1) h)), h = the
 // row's first half rounded up.  The K-th largest key T is found one digit at a time (11, 11 and
 // 10 bits, most significant first) from the sum of the two CTAs' histograms of their halves
 // (the peer's read through distributed shared memory; two histogram buffers, so one cluster
-// barrier per digit suffices).  The histograms also give how many keys above T and equal to T the
-// first half holds, which places the second CTA's output.  Each warp of a CTA then owns a
+// barrier per digit suffices).  The first digit's keys crowd into few bins (their exponents), so
+// its histogram is counted in eight private copies (warp w into copy w % 8) that are then summed.
+// The digit is chosen by all threads at once: thread t holds bins [p t, p t + p) (p = bins / 1024)
+// of both halves' sum, one block-wide suffix sum gives each thread the keys in the bins above its
+// own, and the thread whose bins hold the krem-th largest key writes the digit.  The histograms
+// also give how many keys above T and equal to T the first half holds, which places the second
+// CTA's output.  Each warp of a CTA then owns a
 // contiguous range of its half: one pass counts the range's keys above and equal to T, and a
 // second writes its positions in order (the keys above T, and of the krem keys equal to T the
 // lowest positions).
+constexpr int kKPriv = 8;                                        // private copies of the first histogram
+constexpr int kKSmem = kKPriv * 2048 * (int)sizeof(uint32_t);    // dynamic shared memory: those copies
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
     topk_select_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ seq_lens, int K,
                        int32_t* __restrict__ idx) {
+    static_assert(kKWarps == 32, "the suffix sum over warps takes one warp");
+    extern __shared__ uint32_t priv[];   // [kKPriv][2048]
     __shared__ uint32_t hist[2][2048];
-    __shared__ uint32_t comb[2048];   // both halves' counts of the current digit
     __shared__ int wgt[kKWarps], weq[kKWarps];
-    __shared__ uint32_t s_prefix, s_mask, s_digit;
-    __shared__ int s_krem, s_krem_new, s_above0, s_eq0;
+    __shared__ uint32_t wsum[kKWarps], wsum0[kKWarps], wab[kKWarps], wab0[kKWarps];
+    __shared__ uint32_t s_prefix, s_mask;
+    __shared__ int s_krem, s_above0, s_eq0;
     const uint32_t q = cluster_rank();
     const int b = blockIdx.x >> 1, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t n64 = seq_lens[b];
@@ -710,10 +691,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
         const int shift = level == 0 ? 21 : (level == 1 ? 10 : 0);
         const int nb = level == 2 ? 1024 : 2048;
         const int hb = level & 1;
-        for (int j = tid; j < 2048; j += kKThreads) hist[hb][j] = 0;
+        if (level == 0) {
+            for (int j = tid; j < kKPriv * 2048; j += kKThreads) priv[j] = 0;
+        } else {
+            for (int j = tid; j < 2048; j += kKThreads) hist[hb][j] = 0;
+        }
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
         const int krem = s_krem;
+        uint32_t* hdst = level == 0 ? priv + (warp % kKPriv) * 2048 : hist[hb];
         for (int base = lo; base < hi; base += kKU * kKThreads) {
             uint32_t key[kKU];
 #pragma unroll
@@ -724,27 +710,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
 #pragma unroll
             for (int u = 0; u < kKU; ++u)
                 if (base + u * kKThreads + tid < hi && (key[u] & mask) == prefix)
-                    atomicAdd(&hist[hb][(key[u] >> shift) & (uint32_t)(nb - 1)], 1u);
+                    atomicAdd(&hdst[(key[u] >> shift) & (uint32_t)(nb - 1)], 1u);
+        }
+        if (level == 0) {
+            __syncthreads();
+            for (int j = tid; j < 2048; j += kKThreads) {
+                uint32_t sum = 0;
+#pragma unroll
+                for (int c = 0; c < kKPriv; ++c) sum += priv[c * 2048 + j];
+                hist[0][j] = sum;
+            }
         }
         cluster_sync();   // both halves' histograms of this digit are complete
-        for (int j = tid; j < nb; j += kKThreads)
-            comb[j] = hist[hb][j] + ld_cluster_u32(peer_hist + 4u * (uint32_t)(hb * 2048 + j));
-        __syncthreads();
-        if (warp == 0) select_digit(comb, nb, krem, &s_digit, &s_krem_new);
-        __syncthreads();
-        const uint32_t d = s_digit;
-        // the first half's keys in bins above d (all above T), and at the last digit in bin d
-        int a0 = 0;
-        for (int j = (int)d + 1 + tid; j < nb; j += kKThreads)
-            a0 += (int)(q == 0 ? hist[hb][j] : comb[j] - hist[hb][j]);
+        // this thread's bins: counts over both halves (c) and over the first half (f)
+        const int per = nb / kKThreads;   // 2 or 1
+        uint32_t c[2] = {0u, 0u}, f[2] = {0u, 0u};
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-        if (lane == 0 && a0) atomicAdd(&s_above0, a0);
-        if (tid == 0) {
-            if (level == 2) s_eq0 = (int)(q == 0 ? hist[hb][d] : comb[d] - hist[hb][d]);
-            s_krem = s_krem_new;
-            s_prefix = prefix | (d << shift);
-            s_mask = mask | ((uint32_t)(nb - 1) << shift);
+        for (int i = 0; i < 2; ++i) {
+            if (i < per) {
+                const int j = per * tid + i;
+                const uint32_t own = hist[hb][j];
+                const uint32_t oth = ld_cluster_u32(peer_hist + 4u * (uint32_t)(hb * 2048 + j));
+                c[i] = own + oth;
+                f[i] = q == 0 ? own : oth;
+            }
+        }
+        const uint32_t ct = c[0] + c[1], ft = f[0] + f[1];
+        // suffix sums: within the warp (a higher lane holds higher bins), then over the warps
+        uint32_t x = ct, x0 = ft;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, x, o), y0 = __shfl_down_sync(0xffffffffu, x0, o);
+            if (lane + o < 32) {
+                x += y;
+                x0 += y0;
+            }
+        }
+        if (lane == 0) {
+            wsum[warp] = x;
+            wsum0[warp] = x0;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t v = wsum[lane], v0 = wsum0[lane];
+            uint32_t sx = v, sx0 = v0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(0xffffffffu, sx, o), y0 = __shfl_down_sync(0xffffffffu, sx0, o);
+                if (lane + o < 32) {
+                    sx += y;
+                    sx0 += y0;
+                }
+            }
+            wab[lane] = sx - v;     // keys in the bins of the warps above
+            wab0[lane] = sx0 - v0;
+        }
+        __syncthreads();
+        const uint32_t above = wab[warp] + (x - ct);   // keys in every bin above this thread's
+        if (above < (uint32_t)krem && (uint32_t)krem <= above + ct) {   // exactly one thread
+            uint32_t rem = (uint32_t)krem - above;
+            uint32_t a0 = wab0[warp] + (x0 - ft);      // the first half's keys above
+#pragma unroll
+            for (int i = 1; i >= 0; --i) {
+                if (i >= per) continue;
+                if (rem <= c[i]) {
+                    const uint32_t d = (uint32_t)(per * tid + i);
+                    // the first half's keys in bins above d (all above T), and at the last digit in bin d
+                    s_above0 += (int)a0;
+                    if (level == 2) s_eq0 = (int)f[i];
+                    s_krem = (int)rem;
+                    s_prefix = prefix | (d << shift);
+                    s_mask = mask | ((uint32_t)(nb - 1) << shift);
+                    break;
+                }
+                rem -= c[i];
+                a0 += f[i];
+            }
         }
         __syncthreads();
     }
@@ -864,7 +905,17 @@ cudaError_t launch_indexer_score(const uint8_t* pool, int64_t num_pages, const _
 
 cudaError_t launch_topk_select(const float* scores, int64_t ld, const int32_t* seq_lens, int B, int K,
                                int32_t* idx, cudaStream_t st) {
-    topk_select_kernel<<<dim3(2u * (unsigned)B), kKThreads, 0, st>>>(scores, ld, seq_lens, K, idx);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    topk_select_kernel<<<dim3(2u * (unsigned)B), kKThreads, kKSmem, st>>>(scores, ld, seq_lens, K, idx);
     return cudaGetLastError();
 }
 
