@@ -648,12 +648,16 @@ constexpr int kKU = 8;   // loads in flight per thread in the passes over the ro
 // of both halves' sum, one block-wide suffix sum gives each thread the keys in the bins above its
 // own, and the thread whose bins hold the krem-th largest key writes the digit.  The histograms
 // also give how many keys above T and equal to T the first half holds, which places the second
-// CTA's output.  Each warp of a CTA then owns a
+// CTA's output.  After the first digit, one pass over the row keeps the keys of its bin (with their
+// positions) in shared memory and counts, per warp range, the keys above it; the later digits and
+// the counts of keys above and equal to T then come from those candidates alone.  If either CTA's
+// candidates do not fit, both take the later digits and the counts from the row.  Each warp of a CTA then owns a
 // contiguous range of its half: one pass counts the range's keys above and equal to T, and a
 // second writes its positions in order (the keys above T, and of the krem keys equal to T the
 // lowest positions).
 constexpr int kKPriv = 8;                                        // private copies of the first histogram
-constexpr int kKSmem = kKPriv * 2048 * (int)sizeof(uint32_t);    // dynamic shared memory: those copies
+constexpr int kKSmem = kKPriv * 2048 * (int)sizeof(uint32_t);    // dynamic shared memory: those copies,
+constexpr int kKCand = kKSmem / 8;                                // then up to 8,192 candidates (key, position)
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
     topk_select_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ seq_lens, int K,
@@ -664,7 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
     __shared__ int wgt[kKWarps], weq[kKWarps];
     __shared__ uint32_t wsum[kKWarps], wsum0[kKWarps], wab[kKWarps], wab0[kKWarps];
     __shared__ uint32_t s_prefix, s_mask;
-    __shared__ int s_krem, s_above0, s_eq0;
+    __shared__ int s_krem, s_above0, s_eq0, s_ncand;
     const uint32_t q = cluster_rank();
     const int b = blockIdx.x >> 1, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t n64 = seq_lens[b];
@@ -680,14 +684,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
     const int h = (n + 1) / 2;
     const int lo = (int)q * h, hi = q == 0 ? h : n;
     const uint32_t peer_hist = mapa(smem_u32(&hist[0][0]), q ^ 1u);
+    const uint32_t peer_ncand = mapa(smem_u32(&s_ncand), q ^ 1u);
     if (tid == 0) {
         s_prefix = 0;
         s_mask = 0;
         s_krem = K;
         s_above0 = 0;
         s_eq0 = 0;
+        s_ncand = 0;
     }
+    // each warp's contiguous range of this half (candidates, counts and the ordered write)
+    const unsigned lt = (1u << lane) - 1u;
+    const int L = (hi - lo + kKU * kKThreads - 1) / (kKU * kKThreads) * (kKU * 32);
+    const int r0 = lo + warp * L, r1 = min(hi, r0 + L);
+    uint2* cand = reinterpret_cast<uint2*>(priv);   // after the first digit: (key, position) of its bin
+    bool from_cand = false;                         // digits 2 and 3 over the candidates
+    int ncand = 0;
     for (int level = 0; level < 3; ++level) {
+        if (level == 1) {
+            // The keys of the first digit's bin d0 (the candidates) into shared memory in one pass
+            // over the row, and per warp range the keys above that bin (all above T).  If either
+            // CTA's candidates do not fit, both take digits 2 and 3 and the counts from the row.
+            const uint32_t d0 = s_prefix >> 21;
+            int g = 0;
+            for (int c0 = r0; c0 < r0 + L; c0 += 32 * kKU) {
+                uint32_t key[kKU];
+#pragma unroll
+                for (int u = 0; u < kKU; ++u) {
+                    const int t = c0 + 32 * u + lane;
+                    key[u] = t < r1 ? order_key(row[t]) : 0u;
+                }
+                // one shared-counter update per warp and chunk
+                unsigned cb[kKU];
+                int total = 0;
+#pragma unroll
+                for (int u = 0; u < kKU; ++u) {
+                    const bool in = c0 + 32 * u + lane < r1;
+                    g += (in && (key[u] >> 21) > d0) ? 1 : 0;
+                    cb[u] = __ballot_sync(0xffffffffu, in && (key[u] >> 21) == d0);
+                    total += __popc(cb[u]);
+                }
+                if (total > 0) {
+                    int base = 0;
+                    if (lane == 0) base = atomicAdd(&s_ncand, total);
+                    base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+                    for (int u = 0; u < kKU; ++u) {
+                        const int at = base + __popc(cb[u] & lt);
+                        if (((cb[u] >> lane) & 1u) && at < kKCand)
+                            cand[at] = make_uint2(key[u], (uint32_t)(c0 + 32 * u + lane));
+                        base += __popc(cb[u]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+            if (lane == 0) {
+                wgt[warp] = g;
+                weq[warp] = 0;
+            }
+            cluster_sync();   // both CTAs' candidate counts are final
+            ncand = s_ncand;
+            from_cand = ncand <= kKCand && (int)ld_cluster_u32(peer_ncand) <= kKCand;
+        }
         const int shift = level == 0 ? 21 : (level == 1 ? 10 : 0);
         const int nb = level == 2 ? 1024 : 2048;
         const int hb = level & 1;
@@ -700,7 +759,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
         const uint32_t prefix = s_prefix, mask = s_mask;
         const int krem = s_krem;
         uint32_t* hdst = level == 0 ? priv + (warp % kKPriv) * 2048 : hist[hb];
-        for (int base = lo; base < hi; base += kKU * kKThreads) {
+        if (from_cand) {
+            for (int i = tid; i < ncand; i += kKThreads) {
+                const uint32_t key = cand[i].x;
+                if ((key & mask) == prefix) atomicAdd(&hist[hb][(key >> shift) & (uint32_t)(nb - 1)], 1u);
+            }
+        }
+        for (int base = lo; base < (from_cand ? lo : hi); base += kKU * kKThreads) {
             uint32_t key[kKU];
 #pragma unroll
             for (int u = 0; u < kKU; ++u) {
@@ -793,33 +858,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
     const uint32_t T = s_prefix;
     const int krem = s_krem;   // keys equal to T to take, lowest positions first
 
-    // per warp range of this half: keys above T and equal to T
-    const unsigned lt = (1u << lane) - 1u;
-    const int L = (hi - lo + kKU * kKThreads - 1) / (kKU * kKThreads) * (kKU * 32);
-    const int r0 = lo + warp * L, r1 = min(hi, r0 + L);
-    int g = 0, e = 0;
-    for (int c0 = r0; c0 < r0 + L; c0 += 32 * kKU) {
-        uint32_t key[kKU];
+    // per warp range of this half: keys above T and equal to T (from the candidates: the range's
+    // keys above the first digit's bin, counted before, plus its candidates above / equal to T)
+    if (from_cand) {
+        for (int i = tid; i < ncand; i += kKThreads) {
+            const uint2 c = cand[i];
+            const int w = ((int)c.y - lo) / L;
+            if (c.x > T) atomicAdd(&wgt[w], 1);
+            else if (c.x == T) atomicAdd(&weq[w], 1);
+        }
+    } else {
+        int g = 0, e = 0;
+        for (int c0 = r0; c0 < r0 + L; c0 += 32 * kKU) {
+            uint32_t key[kKU];
 #pragma unroll
-        for (int u = 0; u < kKU; ++u) {
-            const int t = c0 + 32 * u + lane;
-            key[u] = t < r1 ? order_key(row[t]) : 0u;
+            for (int u = 0; u < kKU; ++u) {
+                const int t = c0 + 32 * u + lane;
+                key[u] = t < r1 ? order_key(row[t]) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kKU; ++u) {
+                const bool in = c0 + 32 * u + lane < r1;
+                g += (in && key[u] > T) ? 1 : 0;
+                e += (in && key[u] == T) ? 1 : 0;
+            }
         }
 #pragma unroll
-        for (int u = 0; u < kKU; ++u) {
-            const bool in = c0 + 32 * u + lane < r1;
-            g += (in && key[u] > T) ? 1 : 0;
-            e += (in && key[u] == T) ? 1 : 0;
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
         }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        g += __shfl_xor_sync(0xffffffffu, g, o);
-        e += __shfl_xor_sync(0xffffffffu, e, o);
-    }
-    if (lane == 0) {
-        wgt[warp] = g;
-        weq[warp] = e;
+        if (lane == 0) {
+            wgt[warp] = g;
+            weq[warp] = e;
+        }
     }
     __syncthreads();
     int above = q == 0 ? 0 : s_above0, eq_before = q == 0 ? 0 : s_eq0;

@@ -172,6 +172,27 @@ def test_topk_ties_and_edges(torch):
         assert np.array_equal(got, exp), K
 
 
+def test_topk_crowded_first_digit(torch):
+    """Keys crowding one bin of the first digit (one exponent and two mantissa bits) beyond the
+    8,192 candidates a CTA keeps in shared memory, in both halves or in the first only: both CTAs
+    of the pair then take the later digits from the row; a spread row keeps the candidate path."""
+    rng = np.random.default_rng(57)
+    B, ld = 4, 40000
+    s = np.empty((B, ld), np.float32)
+    s[0] = rng.uniform(1.0, 1.25, ld)                        # every key in one first-digit bin
+    s[1] = np.round(rng.uniform(1.0, 1.25, ld) * 64) / 64    # the same with heavy ties
+    s[2, :20000] = rng.uniform(1.0, 1.25, 20000)             # first half crowded, second spread
+    s[2, 20000:] = rng.standard_normal(20000)
+    s[3] = rng.standard_normal(ld)                           # candidates fit
+    seq = np.array([40000, 39999, 40000, 40000], np.int32)
+    sc = torch.from_numpy(s).cuda()
+    sl = torch.from_numpy(seq).cuda()
+    for K in (2048, 8000):
+        got = mla.topk_select(sc, sl, K).cpu().numpy()
+        exp = oracle.topk(s.astype(np.float64), seq, K)
+        assert np.array_equal(got, exp), K
+
+
 def test_indexer_selection_feeds_sparse_decode(torch):
     """Search keys -> scores -> top-k -> sparse FP8 decode of the picked positions, against the
     oracle decode of the same picks (the DSA path of "MLA that reads only the picked positions",
