@@ -636,6 +636,38 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
 }
 
 constexpr int kKWarps = kKThreads / 32;
+
+// f(key) for every order key of x[0, cnt), in no particular order, with 16-byte loads where x is
+// aligned (the unaligned head and the tail one value at a time).
+template <typename F>
+__device__ __forceinline__ void for_each_key(const float* __restrict__ x, int cnt, F f) {
+    const int tid = threadIdx.x;
+    int head = (int)(((16u - ((uint32_t)(uintptr_t)x & 15u)) & 15u) >> 2);
+    head = head < cnt ? head : cnt;
+    if (tid < head) f(order_key(x[tid]));
+    const float4* xv = reinterpret_cast<const float4*>(x + head);
+    const int nv = (cnt - head) >> 2;
+    constexpr int kV = 4;   // 16-byte loads in flight per thread
+    for (int base = 0; base < nv; base += kV * kKThreads) {
+        float4 v[kV];
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            const int i = base + u * kKThreads + tid;
+            v[u] = i < nv ? __ldg(xv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kV; ++u) {
+            if (base + u * kKThreads + tid < nv) {
+                f(order_key(v[u].x));
+                f(order_key(v[u].y));
+                f(order_key(v[u].z));
+                f(order_key(v[u].w));
+            }
+        }
+    }
+    const int t = head + 4 * nv + tid;
+    if (t < cnt) f(order_key(x[t]));
+}
 constexpr int kKU = 8;   // loads in flight per thread in the passes over the row
 
 // One request per cluster of two CTAs; CTA q holds positions [q h, min(n, (q + 1) h)), h = the
@@ -765,18 +797,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKThreads)
                 if ((key & mask) == prefix) atomicAdd(&hist[hb][(key >> shift) & (uint32_t)(nb - 1)], 1u);
             }
         }
-        for (int base = lo; base < (from_cand ? lo : hi); base += kKU * kKThreads) {
-            uint32_t key[kKU];
-#pragma unroll
-            for (int u = 0; u < kKU; ++u) {
-                const int t = base + u * kKThreads + tid;
-                key[u] = t < hi ? order_key(row[t]) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < kKU; ++u)
-                if (base + u * kKThreads + tid < hi && (key[u] & mask) == prefix)
-                    atomicAdd(&hdst[(key[u] >> shift) & (uint32_t)(nb - 1)], 1u);
-        }
+        if (!from_cand)
+            for_each_key(row + lo, hi - lo, [&](uint32_t key) {
+                if ((key & mask) == prefix) atomicAdd(&hdst[(key >> shift) & (uint32_t)(nb - 1)], 1u);
+            });
         if (level == 0) {
             __syncthreads();
             for (int j = tid; j < 2048; j += kKThreads) {
