@@ -68,7 +68,7 @@ NCU_TRAFFIC = {
     ("5c8345d9e3722708", "topk_sparse"): 118_725_248,
     ("5c8345d9e3722708", "v4_batch"): 1_263_935_232,
     ("5c8345d9e3722708", "v41_batch"): 641_415_552,
-    ("1a7398fbc27d89ce", "indexer_topk"): 1_142_927_360,
+    ("509e33095508b7b4", "indexer_topk"): 1_142_835_200,
     ("46f7feafc1c08056", "value_project"): 224_005_632,
     ("46f7feafc1c08056", "value_project_merged"): 682_509_184,
 }
