@@ -99,10 +99,10 @@ constexpr bool gather_conv(int fmt, bool topk) { return fmt != MLA_KV_BF16 && (t
 constexpr int gather_threads(int fmt, bool topk) {
     return 32 * kSoftWarp0 + kSoftmaxThreads + (gather_conv(fmt, topk) ? 32 * kConvWarps : 0);
 }
-// Registers a thread (converter instantiations: 768 threads launch with 80 a thread; each warpgroup then
-// sets its own: kRegsW0 for warps 0-3, kRegsConv for the converters and kRegsSoftmax for each of
-// the four warpgroups of owners and agents, at most the launch's 6 x 80 per sub-partition lane;
-// all return to 80 before the common teardown).  A raise waits until other warpgroups have
+// Registers a thread in converter instantiations: 768 threads launch with 80 a thread; each
+// warpgroup then sets its own, kRegsW0 for warps 0-3, kRegsConv for the converters and
+// kRegsSoftmax for each of the four warpgroups of owners and agents, at most the launch's 6 x 80
+// per sub-partition lane; all return to 80 before the common teardown.  A raise waits until other warpgroups have
 // released enough: the releases come first (warps 0-3 and the converters, at the start of their
 // roles) and the returns to 80 last.
 constexpr int kRegsLaunch = 80;
@@ -284,7 +284,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
 
     if (tid == 32) {
         for (int i = 0; i < kNC; ++i) {
-            // one arrive per converter warp (raw formats) or agent warp (bf16) once its rows are written
+            // one arrive per converter warp (converter instantiations) or agent warp (FP8 pages, bf16
+            // rows) once its rows are written
             mbar_init(bars.cf(i), kConv ? kConvWarps : 8);
             mbar_init(bars.ce(i), 1);
             // pages: the producer's one arrival with the TMA bytes; top-k rows: one arrival per
