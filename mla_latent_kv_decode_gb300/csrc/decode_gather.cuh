@@ -251,6 +251,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
     constexpr bool kRaw = kFp8 || kShared;    // the producer warp stages raw record bytes
     constexpr bool kConv = gather_conv(kFmt, kTopk);   // converter warps (else in-place conversion)
     constexpr int kNX = kConv ? 1 : 2;        // X buffers (the second one shares the staging buffer)
+    // converter warps that convert: FP8 top-k rows use only the two on the agents' sub-partitions,
+    // leaving the owners' to the softmax (measured faster there; the shared K = V formats, whose
+    // conversion is heavier, need all four)
+    constexpr int kConvActive = (kFp8 && kTopk) ? 2 : kConvWarps;
+    constexpr int kCT = 32 * kConvActive;     // converting threads
     constexpr int kSB = kFp8 ? 1 : 2;         // score buffers (and P buffers)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -286,7 +291,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
         for (int i = 0; i < kNC; ++i) {
             // one arrive per converter warp (converter instantiations) or agent warp (FP8 pages, bf16
             // rows) once its rows are written
-            mbar_init(bars.cf(i), kConv ? kConvWarps : 8);
+            mbar_init(bars.cf(i), kConv ? kConvActive : 8);
             mbar_init(bars.ce(i), 1);
             // pages: the producer's one arrival with the TMA bytes; top-k rows: one arrival per
             // producer lane once its copies land
@@ -295,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
         // the staging buffer: as rf, plus (top-k) one arrival after the mask is written; emptied
         // by one arrive per converter warp
         mbar_init(bars.stage_full, kTopk ? 33 : 1);
-        mbar_init(bars.stage_empty, kConvWarps);
+        mbar_init(bars.stage_empty, kConvActive);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.sf(i), 1);
             mbar_init(bars.se(i), kSoftmaxThreads / 32);   // one arrive per softmax warp
@@ -846,8 +851,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
             reg_dealloc<kRegsConv>();
             named_bar_sync(kBarRegs, gather_threads(kFmt, kTopk));
         }
-        if (kConv && n_local > 0) {
-            const int ct = tid - kConvWarp0 * 32;   // 0 .. 127
+        const int cw = warp - kConvWarp0;   // this converter's sub-partition
+        const bool converts = kConvActive == kConvWarps || (cw >> 1) == (int)(1u - r);
+        if (kConv && n_local > 0 && converts) {
+            const int ct = (kConvActive == kConvWarps ? cw : (cw & 1)) * 32 + lane;   // 0 .. kCT - 1
             Cursor cc;
             cc.init(p.seq_lens, p.max_seq_len, p.topk, start_b, start_t, n_local);
             for (int j = 0; j < n_local; ++j, cc.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
@@ -866,7 +873,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
                 uint8_t* lat = sm + kOffConv + slot * kConvBytes;
                 const uint8_t* scl = sm + kOffScale + slot * kScaleBytes;
                 const uint8_t* stg = sm + kOffStage;
-                // piece e = ct + 128 k: FP8 mixed and V4 [64 rows][16 x 16 B] (row e >> 4, dims 16 ch ..
+                // piece e = ct + kCT k: FP8 mixed and V4 [64 rows][16 x 16 B] (row e >> 4, dims 16 ch ..
                 // 16 ch + 15 of this half, ch = e & 15 = ct & 15); V4.1 [64 rows][8 x 16 B] (row e >> 3,
                 // dims 32 ch .. 32 ch + 31, ch = ct & 7)
                 if (!kV41) {
@@ -874,13 +881,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
                     const bool rope_piece = kV4 && r == 1 && ch >= 12;   // V4, CTA 1: dims 448 .. 511
                     const int s0 = 2 * (ch & 3);
 #pragma unroll 2
-                    for (int k = 0; k < 8; ++k) {
-                        const int row = (ct + 128 * k) >> 4;
+                    for (int k = 0; k < 1024 / kCT; ++k) {
+                        const int row = (ct + kCT * k) >> 4;
                         uint8_t* dst = lat + (ch >> 2) * kKvLatChunk + row * 128;
                         if (rope_piece && valid(row)) continue;
                         uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                         if (valid(row) && !rope_piece) {
-                            const uint4 raw = *reinterpret_cast<const uint4*>(stg + (ct + 128 * k) * 16);
+                            const uint4 raw = *reinterpret_cast<const uint4*>(stg + (ct + kCT * k) * 16);
                             if (kFp8) {
                                 e4m3x16_to_f16(raw, o);
                             } else {
@@ -894,13 +901,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
                 } else {
                     const int ch = ct & 7;
 #pragma unroll 1
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = (ct + 128 * k) >> 3;
+                    for (int k = 0; k < 512 / kCT; ++k) {
+                        const int row = (ct + kCT * k) >> 3;
                         uint32_t o[16];
 #pragma unroll
                         for (int t = 0; t < 16; ++t) o[t] = 0;
                         if (valid(row))
-                            e2m1x32_scaled_bf16(*reinterpret_cast<const uint4*>(stg + (ct + 128 * k) * 16),
+                            e2m1x32_scaled_bf16(*reinterpret_cast<const uint4*>(stg + (ct + kCT * k) * 16),
                                                 e4m3_to_float(scl[row * 16 + 2 * ch]),
                                                 e4m3_to_float(scl[row * 16 + 2 * ch + 1]), o);
                         uint8_t* dst = lat + (ch >> 1) * kKvLatChunk + row * 128;
