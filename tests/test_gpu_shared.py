@@ -97,6 +97,19 @@ def test_shared_topk_rows(fmt, tag):
     assert np.abs(ld.cpu().numpy() - lk.cpu().numpy()).max() <= 1e-3
 
 
+@pytest.mark.parametrize("fmt,tag", FORMATS)
+def test_shared_topk_all_padding_and_empty(fmt, tag):
+    """A list of padding only over a cached request, and a request with nothing cached: the sink
+    alone (zeros, lse = z'); a third request's list is ordinary."""
+    seed = 49 + fmt
+    seq = [700, 0, 300]
+    K = 128
+    idx = np.full((len(seq), K), -1, np.int32)
+    idx[2] = synth.sorted_distinct_sample(seed, synth.STREAM_TOPK, 2, seq[2], K)
+    w = synth.make_shared_workload(f"pad_{tag}", fmt=fmt, seq_lens=seq, seed=seed, topk_idx=idx)
+    _run(w, f"padding {tag}")
+
+
 def test_shared_append_codec_edges():
     """Groups at the edges of both codecs, bit-exact against the oracle's encoders: zero groups, a
     group whose amax is exactly 448 * 2^e, huge and tiny magnitudes, values on E2M1 midpoints."""
