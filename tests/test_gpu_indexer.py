@@ -172,6 +172,22 @@ def test_topk_ties_and_edges(torch):
         assert np.array_equal(got, exp), K
 
 
+def test_topk_unaligned_rows(torch):
+    """A row stride that is not a multiple of four scores, so that rows (and the second CTA's half)
+    start off a 16-byte boundary: the loads' unaligned heads and tails."""
+    rng = np.random.default_rng(59)
+    B, ld = 4, 9001
+    s = rng.standard_normal((B, ld)).astype(np.float32)
+    s[2] = np.round(s[2] * 8) / 8            # ties
+    seq = np.array([9001, 7777, 6003, 130], np.int32)
+    sc = torch.from_numpy(s).cuda()
+    sl = torch.from_numpy(seq).cuda()
+    for K in (1, 100, 2048):
+        got = mla.topk_select(sc, sl, K).cpu().numpy()
+        exp = oracle.topk(s.astype(np.float64), seq, K)
+        assert np.array_equal(got, exp), K
+
+
 def test_topk_crowded_first_digit(torch):
     """Keys crowding one bin of the first digit (one exponent and two mantissa bits) beyond the
     8,192 candidates a CTA keeps in shared memory, in both halves or in the first only: both CTAs
