@@ -654,6 +654,10 @@ def run_ours(args):
         configs["value_project"] = measure_value_project(args, torch, mla, harness, stream, barrier, peaks)
         configs["value_project_merged"] = measure_value_project(args, torch, mla, harness, stream, barrier, peaks,
                                                                 merged=True)
+        r = measure_indexer(args, torch, mla, stream, barrier, dist, world, peaks)
+        configs["indexer_topk"] = {"ms_per_step": round(r["ms"], 6), "steps": r["steps"], "value": r["value"],
+                                   "unit": r["unit"], "queries_per_s": r["queries_per_s"],
+                                   "roofline": r["roofline"], "e2e": r["e2e"], "config": r["config"]}
     if configs:
         line["configs"] = configs
     line["clocks"] = sampler.stop()
@@ -666,28 +670,12 @@ def run_ours(args):
     return 0
 
 
-def run_indexer(args):
+def measure_indexer(args, torch, mla, stream, barrier, dist, world, peaks, sampler=None):
     """The DSA lightning-indexer step (search-key scores of every cached position, then top-k per
-    query) on the indexer_topk workload: one graph of mla_indexer_score + mla_topk_select."""
-    import torch
-    import mla_latent_kv_decode_gb300 as mla
+    query) on the indexer_topk workload: one graph of mla_indexer_score + mla_topk_select.
+    Returns the workload, the step time and the line's figures; the device buffers are freed."""
     from mla_latent_kv_decode_gb300 import synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    mla.load()
     w = synth.make_index_workload(B=args.index_batch)
     pool = torch.zeros(mla.index_pool_bytes(w.num_pages), dtype=torch.uint8, device="cuda")
     chunk = 1 << 15
@@ -700,6 +688,7 @@ def run_indexer(args):
                                   (b * synth.KV_ROW_STRIDE + t0) * mla.INDEX_DIM, mla.INDEX_DIM, mla.INDEX_DIM)
             slot = torch.from_numpy(w.slots(b, t0, t1)).cuda()
             mla.index_append(pool, w.num_pages, kbuf[:t1 - t0], slot)
+    del kbuf
     q = torch.from_numpy(synth.index_queries(w.seed, w.B).view(np.int16)).cuda().view(torch.bfloat16)
     wt = torch.from_numpy(synth.index_weights(w.seed, w.B)).cuda()
     bt = torch.from_numpy(w.block_table).cuda()
@@ -707,7 +696,6 @@ def run_indexer(args):
     ld = w.max_seq_len
     scores = torch.empty((w.B, ld), dtype=torch.float32, device="cuda")
     idx = torch.empty((w.B, w.K), dtype=torch.int32, device="cuda")
-    stream = torch.cuda.Stream()
 
     def step():
         mla.indexer_score(pool, w.num_pages, q, wt, bt, sl, ld, scores=scores)
@@ -719,7 +707,7 @@ def run_indexer(args):
     stream.synchronize()
     rc = mla.check_status()
     if rc != 0:
-        raise mla.MlaError(rc, "warm-up")
+        raise mla.MlaError(rc, "indexer warm-up")
     graphs = {}
     for name, fn in (("step", step),
                      ("score", lambda: mla.indexer_score(pool, w.num_pages, q, wt, bt, sl, ld, scores=scores)),
@@ -728,8 +716,8 @@ def run_indexer(args):
         with torch.cuda.graph(g, stream=stream):
             fn()
         graphs[name] = g
-    sampler = ClockSampler(local)
-    sampler.start()
+    if sampler is not None:
+        sampler.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graphs["step"].replay()
@@ -751,10 +739,10 @@ def run_indexer(args):
     ms = max_over_ranks(ms, dist)
     score_ms = timed(graphs["score"], max(10, steps // 2))
     topk_ms = timed(graphs["topk"], max(10, steps // 2))
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler is not None else None
     rc = mla.check_status()
     if rc != 0:
-        raise mla.MlaError(rc, "timed region")
+        raise mla.MlaError(rc, "indexer timed region")
 
     # end to end: queries, weights, tables host -> device, the step, the picks device -> host
     host = {k: v.cpu().pin_memory() for k, v in (("q", q), ("w", wt), ("bt", bt), ("sl", sl))}
@@ -783,13 +771,14 @@ def run_indexer(args):
         e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e_steps
+    del graphs, pool, q, wt, bt, sl, scores, idx
+    torch.cuda.empty_cache()
 
     keys = int(w.seq_lens.astype(np.int64).sum())
     key_bytes = keys * 132
     alg_bytes = (key_bytes + w.B * 64 * 128 * 2 + w.B * 64 * 4 + w.B * w.K * 4 + w.block_table.size * 4
                  + w.B * 4)
     flops = 2 * 64 * 128 * keys
-    peaks = _peaks()
     s = ms / 1e3
     tensor_bound = flops / (peaks["bf16_tflops_sustained"] * 1e12) > alg_bytes / (peaks["hbm_gbs"] * 1e9)
     achieved = alg_bytes / s / 1e9
@@ -804,21 +793,55 @@ def run_indexer(args):
                      "bytes_per_launch": alg_bytes, "flops_per_launch": flops,
                      "score_ms": round(score_ms, 6), "topk_ms": round(topk_ms, 6),
                      "score_frac_of_hbm": round(key_bytes / (score_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)})
-    line = {
-        "metric": METRIC, "value": round(world * key_bytes / s / 1e9, 3), "unit": "search-key GB/s",
-        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    return {
+        "w": w, "steps": steps, "ms": ms, "clocks": clocks,
+        "value": round(world * key_bytes / s / 1e9, 3), "unit": "search-key GB/s",
         "config": {"workload": w.name, "B": w.B, "indexer_heads": 64, "indexer_dim": 128, "topk": w.K,
                    "description": w.description, "step": "mla_indexer_score + mla_topk_select",
                    "l2": f"inputs larger than L2: a {key_bytes / 2**30:.2f} GiB search-key pool",
                    "parallelism": f"replicas x{world}"},
         "queries_per_s": round(world * w.B / s, 1),
         "roofline": roofline,
-        "clocks": clocks,
         "e2e": {"value": round(world * key_bytes / (e2e_ms / 1e3) / 1e9, 3), "unit": "search-key GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": steps * 2,
+    }
+
+
+def run_indexer(args):
+    """The indexer_topk workload as its own JSON line (scores + top-k, with the oracle's CPU
+    baseline)."""
+    import torch
+    import mla_latent_kv_decode_gb300 as mla
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    mla.load()
+    r = measure_indexer(args, torch, mla, torch.cuda.Stream(), barrier, dist, world, _peaks(),
+                        sampler=ClockSampler(local))
+    w = r["w"]
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": r["unit"],
+        "n_gpus": world, "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(r["ms"], 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": r["config"],
+        "queries_per_s": r["queries_per_s"],
+        "roofline": r["roofline"],
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+        "gpu_launches": r["steps"] * 2,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = indexer_cpu_baseline(w, args.cpu_budget)
