@@ -11,7 +11,7 @@
 // Capacity drives the design.  O (128 x 512 fp32) fills all 512 columns of one SM's tensor memory
 // and Q (128 x 576 bf16, 144 KB) most of its shared memory, so the work runs on clusters of two
 // CTAs, r = 0, 1.  CTA r owns latent dims [256 r, 256 r + 256) and rope dims [32 r, 32 r + 32):
-//   * it streams only its 288 columns of every cached row (576 B per position) through a 4-page
+//   * it streams only its 288 columns of every cached row (576 B per position) through a 3-page
 //     TMA ring, and holds only its half of Q: the latent part in tensor memory (written by the
 //     softmax warps, which read it from global memory once per request), the rope part in shared
 //     memory;
@@ -92,7 +92,7 @@ constexpr int kPBytes = 128 * kT * 2;                  // P [128 heads x 64 pos]
 constexpr int kPMsgBytes = 2 * (32 * 128 + 32 * 4);    // the peer's P rows and rescale factors
 constexpr int kOffQRope = 0;
 constexpr int kOffKv = kOffQRope + kQRopeBytes;        // 8192
-constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 155648: 2 buffers [16][64][16 B]
+constexpr int kOffX = kOffKv + kNS * kStageBytes;      // 118784: 2 buffers [16][64][16 B]
 constexpr int kOffP = kOffX + kNX * kXBytes;           // kNP P buffers
 constexpr int kOffAlphaIn = kOffP + kNP * kPBytes;     // kNP x alpha[64] of the peer's heads
 constexpr int kOffAlphaOut = kOffAlphaIn + kNP * kOwned * 4;   // kNP x alpha[64], owned heads
