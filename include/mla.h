@@ -127,7 +127,10 @@ int32_t mla_decode_launches(int32_t fmt, int32_t B, int32_t H, int32_t max_seq_l
  *                when that is 0); 256-byte aligned; its contents are clobbered.
  * A page index outside [0, num_pages) met while reading records MLA_ERR_BOUNDS.
  * Arithmetic: scores and outputs accumulate in fp32 on the tensor cores.  bf16 records: bf16
- * operands, P rounded once to bf16.  FP8 records: the E4M3 codes enter as f16 (exact), and so
+ * operands, P rounded once to bf16 (2^-9 of each weight; O is divided by the sum of the rounded
+ * P, so the weights still sum to one).  Where the weight sits on two or three positions, that
+ * rounding moves an output element by up to about 2^-10 of the rows' difference, on top of the
+ * bf16 output's own rounding (up to 2^-9 of its magnitude).  FP8 records: the E4M3 codes enter as f16 (exact), and so
  * does q_lat, converted once per request (exact for |q| in [2^-14, 65504); smaller magnitudes
  * lose low bits).  Each 128-dim group's scale multiplies in fp32: on that group's partial score,
  * and on P as f16(P * scale), which stays finite for group scales up to 255 (absmax up to

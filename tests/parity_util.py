@@ -134,3 +134,73 @@ def twin_rows_at(w: synth.Workload, b: int, positions: np.ndarray):
         c[sel] = cc[positions[sel] - t0]
         r[sel] = rr[positions[sel] - t0]
     return c, r
+
+
+def custom_workload(name, fmt, seq_lens, seed, topk_idx=None, shuffle=True, appended=0, scale=None):
+    """An MLA workload (bf16 or FP8 mixed records) of the given request lengths over a shuffled
+    pool, optionally with top-k lists and a softmax scale of its own."""
+    seq = np.asarray(seq_lens, dtype=np.int32)
+    pages = int(((seq.astype(np.int64) + 63) // 64).sum())
+    perm = synth.permutation(seed, synth.STREAM_PERM, pages) if shuffle else None
+    bt, total = synth._block_table(seq, perm)
+    return synth.Workload(name, fmt, len(seq), 128, seed, seq, bt, total,
+                          topk_idx=None if topk_idx is None else np.asarray(topk_idx, np.int32),
+                          appended=appended, scale=synth.SCALE if scale is None else scale)
+
+
+def run_full_compare(w, what):
+    """Append every request's rows and decode the batch through the C ABI, then compare every
+    cache byte (bit-exact) and every output and log-sum-exp with the oracle."""
+    import mla_latent_kv_decode_gb300 as mla
+    from mla_latent_kv_decode_gb300 import harness
+    dw = harness.DeviceWorkload(w, gen="host")
+    dw.append()
+    out, lse = dw.decode()
+    assert mla.check_status() == 0
+    ref_pool = oracle_pool(w)
+    gpu_pool = dw.pools[0].cpu().numpy()
+    assert np.array_equal(gpu_pool, ref_pool), f"{what}: pool bytes differ"
+    ql, qr = w.queries()
+    ro, rl, _ = oracle.mla_decode(w.fmt, ref_pool, ql, qr, w.block_table, w.seq_lens, w.scale,
+                                  topk_idx=w.topk_idx)
+    go = out.float().cpu().numpy().reshape(-1, 512)
+    gl = lse.cpu().numpy().reshape(-1)
+    assert_decode_close(go, gl, ro, rl, what)
+    return dw
+
+
+def shared_oracle_pool(w, upto=None):
+    """Host pool of shared K = V entries (V4 or V4.1) holding every request's entries."""
+    pool = oracle.new_shared_pool(w.fmt, w.num_pages)
+    for b in range(w.B):
+        n = int(w.seq_lens[b] if upto is None else upto[b])
+        if n > 0:
+            assert oracle.shared_append(w.fmt, pool, synth.shared_entries(w.seed, b, 0, n), w.slots(b, 0, n)) == 0
+    return pool
+
+
+def run_shared_compare(w, what):
+    """The shared K = V path: entries appended and decoded through the C ABI, then every pool byte
+    (bit-exact), output and log-sum-exp compared with the oracle; a request with nothing visible
+    must give zeros and lse = z' (the sink)."""
+    import mla_latent_kv_decode_gb300 as mla
+    from mla_latent_kv_decode_gb300 import harness
+    dw = harness.SharedDeviceWorkload(w, gen="host")
+    dw.append()
+    out, lse = dw.decode()
+    assert mla.check_status() == 0
+    pool = shared_oracle_pool(w)
+    assert np.array_equal(dw.pools[0].cpu().numpy(), pool), f"{what}: pool bytes differ"
+    ro, rl = oracle.shared_kv_decode(w.fmt, pool, w.queries(), w.block_table, w.seq_lens, w.scale,
+                                     sink=w.sink(), rope_cs=w.rope_cs(), topk_idx=w.topk_idx)
+    go = out.float().cpu().numpy().reshape(-1, 512)
+    gl = lse.cpu().numpy().reshape(-1)
+    if w.use_sink:
+        sk = np.tile(w.sink(), w.B)
+        empty = np.isclose(rl, sk) & np.all(ro == 0, axis=1)
+        assert np.all(go[empty] == 0) and np.allclose(gl[empty], sk[empty])
+        keep = ~empty
+        assert_decode_close(go[keep], gl[keep], ro[keep], rl[keep], what)
+    else:
+        assert_decode_close(go, gl, ro, rl, what)
+    return dw

@@ -9,7 +9,8 @@ import pytest
 import oracle
 import mla_latent_kv_decode_gb300 as mla
 from mla_latent_kv_decode_gb300 import harness, synth
-from parity_util import (assert_decode_close, oracle_decode_pairs, oracle_pool, twin_rows,
+from parity_util import (assert_decode_close, custom_workload as _custom, oracle_decode_pairs,
+                         oracle_pool, run_full_compare, twin_rows,
                          twin_rows_at)
 
 pytestmark = pytest.mark.gpu
@@ -23,54 +24,26 @@ def torch():
     return t
 
 
-def _custom(name, fmt, seq_lens, seed, topk_idx=None, shuffle=True, appended=0, scale=None):
-    seq = np.asarray(seq_lens, dtype=np.int32)
-    pages = int(((seq.astype(np.int64) + 63) // 64).sum())
-    perm = synth.permutation(seed, synth.STREAM_PERM, pages) if shuffle else None
-    bt, total = synth._block_table(seq, perm)
-    return synth.Workload(name, fmt, len(seq), 128, seed, seq, bt, total,
-                          topk_idx=None if topk_idx is None else np.asarray(topk_idx, np.int32),
-                          appended=appended, scale=synth.SCALE if scale is None else scale)
-
-
-def _run_full_compare(torch, w, what, replicas=1):
-    dw = harness.DeviceWorkload(w, gen="host")
-    dw.append()
-    out, lse = dw.decode()
-    assert mla.check_status() == 0
-    # cache bytes: bit-exact against the oracle's encoder on the same rows
-    ref_pool = oracle_pool(w)
-    gpu_pool = dw.pools[0].cpu().numpy()
-    assert np.array_equal(gpu_pool, ref_pool), f"{what}: pool bytes differ"
-    ql, qr = w.queries()
-    ro, rl, _ = oracle.mla_decode(w.fmt, ref_pool, ql, qr, w.block_table, w.seq_lens, w.scale,
-                                  topk_idx=w.topk_idx)
-    go = out.float().cpu().numpy().reshape(-1, 512)
-    gl = lse.cpu().numpy().reshape(-1)
-    assert_decode_close(go, gl, ro, rl, what)
-    return dw
-
-
 def test_tiny_dense_full(torch):
     """B=1, 4,096 tokens, contiguous pages (the whole small workload, every output)."""
-    _run_full_compare(torch, synth.make_workload("tiny_dense"), "tiny_dense")
+    run_full_compare(synth.make_workload("tiny_dense"), "tiny_dense")
 
 
 def test_ragged_paged_batch_edges(torch):
     """Ragged lengths around the 64-token page and tile edges, shuffled pages, one empty request."""
     w = _custom("ragged", 0, [1, 63, 64, 65, 127, 0, 1000, 3000], seed=21)
-    _run_full_compare(torch, w, "ragged bf16")
+    run_full_compare(w, "ragged bf16")
 
 
 def test_split_kv_long_request(torch):
     """One long request split across many work units and merged (split-KV + LSE merge)."""
     w = _custom("long", 0, [20000], seed=22)
-    _run_full_compare(torch, w, "long bf16")
+    run_full_compare(w, "long bf16")
 
 
 def test_fp8_mixed_batch_with_append(torch):
     w = _custom("fp8", 1, [300, 64, 1, 777], seed=23, appended=64)
-    _run_full_compare(torch, w, "fp8 mixed")
+    run_full_compare(w, "fp8 mixed")
 
 
 def test_many_requests_mixed_lengths(torch):
@@ -84,7 +57,7 @@ def test_many_requests_mixed_lengths(torch):
     seq[5::13] = 64
     for fmt in (0, 1):
         w = _custom(f"many{fmt}", fmt, seq, seed=27)
-        _run_full_compare(torch, w, f"many requests fmt={fmt}")
+        run_full_compare(w, f"many requests fmt={fmt}")
 
 
 def test_few_long_requests_deep_merge(torch):
@@ -92,7 +65,7 @@ def test_few_long_requests_deep_merge(torch):
     block-per-head shape, with one empty request between them."""
     for fmt in (0, 1):
         w = _custom(f"few{fmt}", fmt, [17000, 0, 9000, 25001], seed=28)
-        _run_full_compare(torch, w, f"few long requests fmt={fmt}")
+        run_full_compare(w, f"few long requests fmt={fmt}")
 
 
 def test_running_max_growth(torch):
@@ -102,7 +75,7 @@ def test_running_max_growth(torch):
     pair, and requests split across clusters merge partials with very different maxima."""
     for fmt in (0, 1):
         w = _custom(f"growth{fmt}", fmt, [4096, 3000, 130, 8000, 65], seed=26, scale=4.0)
-        _run_full_compare(torch, w, f"running-max growth fmt={fmt}")
+        run_full_compare(w, f"running-max growth fmt={fmt}")
 
 
 def test_running_max_growth_topk_rows(torch):
@@ -114,7 +87,7 @@ def test_running_max_growth_topk_rows(torch):
                     [-1] * (K - min(K, n)) for b, n in enumerate(seq)]).astype(np.int32)
     for fmt in (0, 1):
         w = _custom(f"growth_topk{fmt}", fmt, seq, seed=26, scale=4.0, topk_idx=idx)
-        _run_full_compare(torch, w, f"running-max growth, top-k rows fmt={fmt}")
+        run_full_compare(w, f"running-max growth, top-k rows fmt={fmt}")
 
 
 def test_topk_sparse_with_padding(torch):
@@ -127,12 +100,12 @@ def test_topk_sparse_with_padding(torch):
     idx[2, -5:] = 4097 + np.arange(5)   # at/after seq_len: skipped
     for fmt in (0, 1):
         w = _custom(f"topk{fmt}", fmt, seq, seed=seed, topk_idx=idx)
-        _run_full_compare(torch, w, f"topk fmt={fmt}")
+        run_full_compare(w, f"topk fmt={fmt}")
 
 
 def test_topk_all_padding_and_empty(torch):
     w = _custom("topk_empty", 1, [100, 0], seed=25, topk_idx=np.full((2, 64), -1, np.int32))
-    _run_full_compare(torch, w, "topk all padding")
+    run_full_compare(w, "topk all padding")
 
 
 def test_combine_matches_oracle(torch):
@@ -304,8 +277,8 @@ def test_topk_listing_every_position_equals_dense(torch):
     for fmt in (0, 1):
         wd = _custom(f"dense{fmt}", fmt, seq, seed=30)
         wk = _custom(f"all{fmt}", fmt, seq, seed=30, topk_idx=idx)
-        dd = _run_full_compare(torch, wd, f"dense fmt={fmt}")
-        dk = _run_full_compare(torch, wk, f"top-k of every position fmt={fmt}")
+        dd = run_full_compare(wd, f"dense fmt={fmt}")
+        dk = run_full_compare(wk, f"top-k of every position fmt={fmt}")
         od, ld = dd.decode()
         ok, lk = dk.decode()
         assert np.abs(od.float().cpu().numpy() - ok.float().cpu().numpy()).max() <= 1e-2

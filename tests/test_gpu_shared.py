@@ -11,58 +11,26 @@ import pytest
 
 import oracle
 import mla_latent_kv_decode_gb300 as mla
-from mla_latent_kv_decode_gb300 import harness, synth
-from parity_util import assert_decode_close
+from mla_latent_kv_decode_gb300 import synth
+from parity_util import run_shared_compare, shared_oracle_pool
 
 pytestmark = pytest.mark.gpu
 
 FORMATS = [(2, "v4"), (3, "v41")]
 
 
-def _oracle_pool(w, upto=None):
-    pool = oracle.new_shared_pool(w.fmt, w.num_pages)
-    for b in range(w.B):
-        n = int(w.seq_lens[b] if upto is None else upto[b])
-        if n > 0:
-            assert oracle.shared_append(w.fmt, pool, synth.shared_entries(w.seed, b, 0, n), w.slots(b, 0, n)) == 0
-    return pool
-
-
-def _run(w, what):
-    dw = harness.SharedDeviceWorkload(w, gen="host")
-    dw.append()
-    out, lse = dw.decode()
-    assert mla.check_status() == 0
-    pool = _oracle_pool(w)
-    assert np.array_equal(dw.pools[0].cpu().numpy(), pool), f"{what}: pool bytes differ"
-    ro, rl = oracle.shared_kv_decode(w.fmt, pool, w.queries(), w.block_table, w.seq_lens, w.scale,
-                                     sink=w.sink(), rope_cs=w.rope_cs(), topk_idx=w.topk_idx)
-    go = out.float().cpu().numpy().reshape(-1, 512)
-    gl = lse.cpu().numpy().reshape(-1)
-    if w.use_sink:
-        # a request with nothing visible: zeros and lse = z'
-        sk = np.tile(w.sink(), w.B)
-        empty = np.isclose(rl, sk) & np.all(ro == 0, axis=1)
-        assert np.all(go[empty] == 0) and np.allclose(gl[empty], sk[empty])
-        keep = ~empty
-        assert_decode_close(go[keep], gl[keep], ro[keep], rl[keep], what)
-    else:
-        assert_decode_close(go, gl, ro, rl, what)
-    return dw
-
-
 @pytest.mark.parametrize("fmt,tag", FORMATS)
 def test_shared_ragged_batch(fmt, tag):
     """Ragged lengths around page edges, an empty request, shuffled pages; sinks and rotation."""
     w = synth.make_shared_workload(f"ragged_{tag}", fmt=fmt, seq_lens=[1, 63, 64, 65, 0, 700, 3000], seed=41 + fmt)
-    _run(w, f"ragged {tag}")
+    run_shared_compare(w, f"ragged {tag}")
 
 
 @pytest.mark.parametrize("fmt,tag", FORMATS)
 def test_shared_without_sink_or_rotation(fmt, tag):
     w = synth.make_shared_workload(f"plain_{tag}", fmt=fmt, seq_lens=[500, 129, 2000], seed=43 + fmt,
                                    use_sink=False, use_rope=False)
-    _run(w, f"plain {tag}")
+    run_shared_compare(w, f"plain {tag}")
 
 
 @pytest.mark.parametrize("fmt,tag", FORMATS)
@@ -70,7 +38,7 @@ def test_shared_long_requests_split_and_merged(fmt, tag):
     """Requests long enough to be cut across many clusters: partials are rotated back in place
     and the merge adds the sink once."""
     w = synth.make_shared_workload(f"long_{tag}", fmt=fmt, seq_lens=[20000, 9000, 0, 33], seed=45 + fmt)
-    _run(w, f"long {tag}")
+    run_shared_compare(w, f"long {tag}")
 
 
 @pytest.mark.parametrize("fmt,tag", FORMATS)
@@ -84,15 +52,15 @@ def test_shared_topk_rows(fmt, tag):
     idx[1, -20:] = -1
     idx[2, -5:] = 4097 + np.arange(5)
     w = synth.make_shared_workload(f"topk_{tag}", fmt=fmt, seq_lens=seq, seed=seed, topk_idx=idx)
-    _run(w, f"topk {tag}")
+    run_shared_compare(w, f"topk {tag}")
     seq = [130, 64]
     full = np.full((2, 192), -1, np.int32)
     for b, n in enumerate(seq):
         full[b, :n] = np.arange(n)
     wd = synth.make_shared_workload(f"dense_{tag}", fmt=fmt, seq_lens=seq, seed=seed + 1)
     wk = synth.make_shared_workload(f"all_{tag}", fmt=fmt, seq_lens=seq, seed=seed + 1, topk_idx=full)
-    od, ld = _run(wd, f"dense {tag}").decode()
-    ok, lk = _run(wk, f"all {tag}").decode()
+    od, ld = run_shared_compare(wd, f"dense {tag}").decode()
+    ok, lk = run_shared_compare(wk, f"all {tag}").decode()
     assert np.abs(od.float().cpu().numpy() - ok.float().cpu().numpy()).max() <= 1e-2
     assert np.abs(ld.cpu().numpy() - lk.cpu().numpy()).max() <= 1e-3
 
@@ -107,7 +75,7 @@ def test_shared_topk_all_padding_and_empty(fmt, tag):
     idx = np.full((len(seq), K), -1, np.int32)
     idx[2] = synth.sorted_distinct_sample(seed, synth.STREAM_TOPK, 2, seq[2], K)
     w = synth.make_shared_workload(f"pad_{tag}", fmt=fmt, seq_lens=seq, seed=seed, topk_idx=idx)
-    _run(w, f"padding {tag}")
+    run_shared_compare(w, f"padding {tag}")
 
 
 def test_shared_append_codec_edges():
@@ -142,7 +110,7 @@ def _growth_events(w, slack_nats=15 * np.log(2.0)):
     """How often a head's running max (kept while every P stays within 2^15 of it, as the kernel
     keeps it) has to grow, tile by tile of 64 entries, over the whole batch (from the oracle's
     own entries and scores)."""
-    pool = _oracle_pool(w)
+    pool = shared_oracle_pool(w)
     q = synth.bf16_bits_to_f32(w.queries()).astype(np.float64)
     events = 0
     for b in range(w.B):
@@ -171,4 +139,4 @@ def test_shared_running_max_growth(fmt, tag):
     w = synth.make_shared_workload(f"growth_{tag}", fmt=fmt, seq_lens=[4096, 3000, 130, 8000, 65], seed=51 + fmt)
     w.scale = 1.0
     assert _growth_events(w) >= 200
-    _run(w, f"growth {tag}")
+    run_shared_compare(w, f"growth {tag}")
