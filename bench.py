@@ -64,10 +64,10 @@ NCU_TRAFFIC = {
     ("a6a81cb6175a2d16", "tiny_dense"): 4_939_008,
     ("a6a81cb6175a2d16", "paged_batch"): 176_497_152,
     ("a6a81cb6175a2d16", "long_context"): 154_273_024,
-    ("ab784f167d639b61", "fp8_batch"): 1_412_305_152,
-    ("ab784f167d639b61", "topk_sparse"): 118_778_624,
-    ("ab784f167d639b61", "v4_batch"): 1_264_184_192,
-    ("ab784f167d639b61", "v41_batch"): 641_207_680,
+    ("5213971b4ddbd3b5", "fp8_batch"): 1_412_560_000,
+    ("5213971b4ddbd3b5", "topk_sparse"): 119_599_872,
+    ("5213971b4ddbd3b5", "v4_batch"): 1_264_051_456,
+    ("5213971b4ddbd3b5", "v41_batch"): 641_346_560,
     ("509e33095508b7b4", "indexer_topk"): 1_142_835_200,
     ("46f7feafc1c08056", "value_project"): 224_005_632,
     ("46f7feafc1c08056", "value_project_merged"): 682_509_184,

@@ -46,8 +46,8 @@
 // Shared memory: Q half (72 KB, TMA), three conversion slots (36 KB each), the staging buffer
 // (16 KB; the second exchange buffer where nothing is staged), exchange buffers.
 //
-// Warp roles: warps 0-3: Q loads (TMA) and the f16 conversion of Q, the MMA issuer (+ TMEM owner),
-// the producer, and an idle warp; warps 4-19: thread = head = TMEM lane, four warps per 32-lane
+// Warp roles: warps 0-3: Q loads (TMA) and the f16 conversion of Q (FP8 records: warps 0 and 3, a
+// half each), the MMA issuer (+ TMEM owner), the producer; warps 4-19: thread = head = TMEM lane, four warps per 32-lane
 // group, 16 positions of a tile each; the 8 warps on the owned heads' lanes run the softmax, the
 // other 8 ("agents") forward partial scores, place the peer's P and finish those O rows (and
 // convert FP8 pages, or load bf16 rows); warps 20-23 (converter instantiations): the converters.
@@ -250,6 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
     constexpr bool kShared = kV4 || kV41;     // K = V = the 512-dim entry; no separate rope
     constexpr bool kRaw = kFp8 || kShared;    // the producer warp stages raw record bytes
     constexpr bool kConv = gather_conv(kFmt, kTopk);   // converter warps (else in-place conversion)
+    constexpr bool kQSplit = kFp8;   // warps 0 and 3 share the f16 conversion of a request's Q half
     constexpr int kNX = kConv ? 1 : 2;        // X buffers (the second one shares the staging buffer)
     // converter warps that convert: FP8 top-k rows use only the two on the agents' sub-partitions,
     // leaving the owners' to the softmax (measured faster there; the shared K = V formats, whose
@@ -315,7 +316,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
         mbar_init(bars.pin_full, 1);
         mbar_init(bars.pin_free, 8);     // one remote arrive per peer agent warp
         mbar_init(bars.q_full, 1);
-        mbar_init(bars.q_ready, 1);
+        mbar_init(bars.q_ready, kQSplit ? 2 : 1);   // warps 0 and 3 convert a half each
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.o_full, 1);
         mbar_init(bars.o_free, kSoftmaxThreads / 32);
@@ -369,18 +370,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
     }
 
     if (warp < kSoftWarp0) {
-        // warps 0-3: Q loads, MMA issuer, raw tile loads (warp 3 idle)
+        // warps 0-3: Q loads, MMA issuer, raw tile loads, and (FP8 records) the Q conversion in warps 0 and 3
         if constexpr (kConv) {
             reg_dealloc<kRegsW0>();
             named_bar_sync(kBarRegs, gather_threads(kFmt, kTopk));
         }
-        if (warp == 0) {
+        if (warp == 0 || (kQSplit && warp == 3)) {
             // ------------------------------------------------------------------ Q loads (TMA) + f16
-            // FP8 records: once a request's Q half has landed, the whole warp converts its latent
-            // part from bf16 to f16 in place (the swizzle permutes whole 16-byte chunks, so each
-            // chunk keeps its place), then releases it to the MMA issuer.
+            // Warp 0 loads a request's Q half by TMA.  FP8 records: once it has landed, warps 0 and 3
+            // (two sub-partitions) convert its latent part from bf16 to f16 in place, half each (the
+            // swizzle permutes whole 16-byte chunks, so each chunk keeps its place), and release it to
+            // the MMA issuer.  Warp 0 then prefetches the next segment's Q half into L2.
+            const bool qlead = warp == 0;
             Cursor cu;
-            if (lane == 0 && n_local > 0) {
+            if (qlead && lane == 0 && n_local > 0) {
                 tma_prefetch_desc(&tm_qlat);
                 if (!kShared) tma_prefetch_desc(&tm_qrope);
             }
@@ -389,13 +392,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
             for (int i = 0; i < n_local; ++i, cu.next(p.seq_lens, p.max_seq_len, p.B, p.topk)) {
                 if (!cu.first()) continue;
                 bool ok = !s_abort;
-                if (ok && seg > 0) ok = mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit);
+                if (qlead && ok && seg > 0) ok = mbar_wait(bars.q_empty, (seg - 1) & 1, wait_limit);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
                     if (lane == 0) fail(p.ctl, &s_abort, 1);
                     break;
                 }
-                if (lane == 0) {
+                if (qlead && lane == 0) {
                     const int qrow = cu.b * kHeads;
                     mbar_arrive_expect_tx(bars.q_full, kShared ? 4 * kQLatChunk : kQBytes);
                     for (int k = 0; k < 4; ++k)
@@ -403,33 +406,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
                                     (int)r * kHalfLat + 64 * k, qrow);
                     if (!kShared) tma_load_2d(sbase + kOffQRope, &tm_qrope, bars.q_full, (int)r * kHalfRope, qrow);
                 }
-                ok = __all_sync(0xffffffffu, mbar_wait(bars.q_full, seg & 1, wait_limit));
+                // warp 3 waits for the whole segment: sleeping polls leave its sub-partition's issue
+                // slots to the softmax warps there
+                ok = __all_sync(0xffffffffu, qlead ? mbar_wait(bars.q_full, seg & 1, wait_limit)
+                                                   : mbar_wait_sleep(bars.q_full, seg & 1, wait_limit, 256));
                 if (!ok) {
                     if (lane == 0) fail(p.ctl, &s_abort, 19);
                     break;
                 }
                 if (kFp8) {
-                    // an element that overflows f16 (|q| >= 65520) is outside this path's range
-                    uint32_t inf = 0;
+                    // an element that overflows f16 (|q| >= 65520) is outside this path's range.  bf16
+                    // holds nothing in [65504, 65536), so that is a magnitude field of 0x4780 or more,
+                    // which (field + 0x3880) marks in bit 15 (two fields a word, no carry between
+                    // them; infinities and NaNs included)
+                    uint32_t big = 0;
     #pragma unroll 8
-                    for (int u = lane; u < 4 * kQLatChunk / 16; u += 32) {
+                    for (int u = lane + (qlead ? 0 : 32); u < 4 * kQLatChunk / 16; u += kQSplit ? 64 : 32) {
                         uint4* q = reinterpret_cast<uint4*>(sm + kOffQ) + u;
                         const uint4 v = *q;
-                        const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                                   bf16x2_to_f16x2(v.w));
-                        inf |= f16x2_inf_or_nan(f.x) | f16x2_inf_or_nan(f.y) | f16x2_inf_or_nan(f.z) |
-                               f16x2_inf_or_nan(f.w);
-                        *q = f;
+                        big |= ((v.x & 0x7FFF7FFFu) + 0x38803880u) | ((v.y & 0x7FFF7FFFu) + 0x38803880u) |
+                               ((v.z & 0x7FFF7FFFu) + 0x38803880u) | ((v.w & 0x7FFF7FFFu) + 0x38803880u);
+                        *q = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                        bf16x2_to_f16x2(v.w));
                     }
                     fence_proxy_async_smem();
-                    if (__any_sync(0xffffffffu, inf != 0) && lane == 0) record_error(p.ctl, MLA_ERR_RANGE, cu.b);
+                    if (__any_sync(0xffffffffu, (big & 0x80008000u) != 0) && lane == 0)
+                        record_error(p.ctl, MLA_ERR_RANGE, cu.b);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.q_ready);
+                if (qlead && lane == 0 && i + (cu.nt - cu.t) < n_local) {
+                    // the range goes on with the next request that has tiles: its Q half into L2
+                    int b = cu.b + 1;
+                    while (b + 1 < p.B && tiles_of(clamp_len(p.seq_lens[b], p.max_seq_len), p.topk) == 0) ++b;
+                    for (int k = 0; k < 4; ++k) tma_prefetch_l2_2d(&tm_qlat, (int)r * kHalfLat + 64 * k, b * kHeads);
+                    if (!kShared) tma_prefetch_l2_2d(&tm_qrope, (int)r * kHalfRope, b * kHeads);
+                }
                 ++seg;
             }
             // drain: the last Q load lands before this CTA may exit
-            if (lane == 0 && seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
+            if (qlead && lane == 0 && seg > 0) mbar_wait(bars.q_full, (seg - 1) & 1, kDrainLimit);
             __syncwarp();
         } else if (warp == 1) {
             // ------------------------------------------------------------------ MMA issuer
