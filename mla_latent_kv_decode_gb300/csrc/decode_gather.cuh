@@ -83,6 +83,15 @@ __device__ __forceinline__ void reg_dealloc() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Eight 32-bit words to global memory in one 256-bit store (the address 32-byte aligned).  A
+// thread's O row goes out this way in the epilogue: each store instruction touches a line per
+// thread, so halving the instructions of a row halves the lines an epilogue touches.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 constexpr int kSegCost = 1;           // a segment start costs about one tile (schedule units)
 constexpr int kNC = 3;                 // converted tile slots
 constexpr int kSoftmaxThreads = 512;   // 16 warps: 8 owners + 8 agents
@@ -1094,6 +1103,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
             tc_fence_after();
             const float inv = l_row > 0.f ? 1.0f / l_row : 0.0f;
             const size_t row = (size_t)cu.b * kHeads + h;
+            const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t o[32];
@@ -1113,20 +1123,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gather_threads(kFmt,
                     }
                 }
                 if (!partial) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDc + col);
+                    // 32 bf16 (64 bytes at a 64-byte offset in the row): 256-bit stores when the
+                    // output is 32-byte aligned (the interface promises 16)
+                    uint32_t w[16];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
+                    for (int k = 0; k < 16; ++k)
+                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + row * kDc + col);
+                    if (out32) {
+                        st_global_v8(dst, reinterpret_cast<const uint32_t(&)[8]>(w[0]));
+                        st_global_v8(dst + 8, reinterpret_cast<const uint32_t(&)[8]>(w[8]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            reinterpret_cast<uint4*>(dst)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    }
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
+                    // 32 fp32 (128 bytes at a 128-byte offset in a partial slot of the 256-byte
+                    // aligned workspace)
+                    uint32_t* dst = reinterpret_cast<uint32_t*>(p.o_part + ((size_t)slot * kHeads + h) * kDc + col);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(o[8 * k + e]) * inv);
+                        st_global_v8(dst + 8 * k, w);
+                    }
                 }
             }
             tc_fence_before();

@@ -283,3 +283,36 @@ def test_topk_listing_every_position_equals_dense(torch):
         ok, lk = dk.decode()
         assert np.abs(od.float().cpu().numpy() - ok.float().cpu().numpy()).max() <= 1e-2
         assert np.abs(ld.cpu().numpy() - lk.cpu().numpy()).max() <= 1e-3
+
+
+def _decode_into_offset_out(torch, dw):
+    """Decode again into an output 16 bytes past a 32-byte boundary (the interface asks only for
+    16-byte alignment); returns (out, lse)."""
+    shape, n = dw.out.shape, dw.out.numel()
+    buf = torch.empty(n + 32, dtype=torch.bfloat16, device="cuda")
+    off = ((16 - buf.data_ptr() % 32) % 32) // 2
+    dw.out = buf[off:off + n].view(shape)
+    assert dw.out.data_ptr() % 32 == 16
+    out, lse = dw.decode()
+    assert mla.check_status() == 0
+    return out, lse
+
+
+def test_output_aligned_to_16_bytes_only(torch):
+    """The epilogues store whole 32-byte pieces of a row when the output allows it and 16-byte
+    ones otherwise: the same bits either way, for every kernel that writes rows of out (bf16
+    pages, FP8 pages, FP8 and bf16 top-k rows, both shared K = V formats)."""
+    seq = [300, 64, 1, 777]
+    idx = np.stack([synth.sorted_distinct_sample(64, synth.STREAM_TOPK, b, n, 128) if n >= 128 else
+                    np.concatenate([np.arange(n), np.full(128 - n, -1)]) for b, n in enumerate(seq)]).astype(np.int32)
+    mla_cases = [_custom("al_bf16", 0, seq, seed=61), _custom("al_fp8", 1, seq, seed=62),
+                 _custom("al_fp8_topk", 1, seq, seed=63, topk_idx=idx), _custom("al_bf16_topk", 0, seq, seed=64, topk_idx=idx)]
+    shared_cases = [synth.make_shared_workload(f"al_shared{f}", fmt=f, seq_lens=seq, seed=65 + f) for f in (2, 3)]
+    for w, shared in [(w, False) for w in mla_cases] + [(w, True) for w in shared_cases]:
+        dw = (harness.SharedDeviceWorkload if shared else harness.DeviceWorkload)(w, gen="host")
+        dw.append()
+        ref_out, ref_lse = (t.clone() for t in dw.decode())
+        assert mla.check_status() == 0
+        assert dw.out.data_ptr() % 32 == 0
+        out, lse = _decode_into_offset_out(torch, dw)
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), w.name
