@@ -64,10 +64,10 @@ NCU_TRAFFIC = {
     ("a6a81cb6175a2d16", "tiny_dense"): 4_939_008,
     ("a6a81cb6175a2d16", "paged_batch"): 176_497_152,
     ("a6a81cb6175a2d16", "long_context"): 154_273_024,
-    ("5213971b4ddbd3b5", "fp8_batch"): 1_412_560_000,
-    ("5213971b4ddbd3b5", "topk_sparse"): 119_599_872,
-    ("5213971b4ddbd3b5", "v4_batch"): 1_264_051_456,
-    ("5213971b4ddbd3b5", "v41_batch"): 641_346_560,
+    ("4c1171a7fa215234", "fp8_batch"): 1_412_164_096,
+    ("4c1171a7fa215234", "topk_sparse"): 120_542_080,
+    ("4c1171a7fa215234", "v4_batch"): 1_263_980_032,
+    ("4c1171a7fa215234", "v41_batch"): 641_302_016,
     ("509e33095508b7b4", "indexer_topk"): 1_142_835_200,
     ("46f7feafc1c08056", "value_project"): 224_005_632,
     ("46f7feafc1c08056", "value_project_merged"): 682_509_184,
